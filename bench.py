@@ -1,0 +1,455 @@
+#!/usr/bin/env python3
+"""Benchmark: single-precision dense GEMM C = A @ B (row-major) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--algo auto|ffma|3xtf32]
+                    [--workload square_8192_normal] [--impl ours|reference]
+
+One step is one call of the library's public entry point (operand staging,
+the GEMM kernel and any split-K reduction, all on the GPU) on the 8192^3
+workload with N(0,1) inputs.  The inputs (2 x 256 MiB) are larger than the
+129 MB L2, so no flush is needed between steps; smaller workloads get an L2
+flush (a 512 MiB write) between timed steps, outside the timed pairs.
+
+Timing follows the lecture-12 benchmark helper and the cuda-gemm README's
+method: CUDA events per step on the launching stream after warm-up, device
+memory allocated once.  Printed as ONE JSON line by rank 0.
+
+--impl reference times the CPU oracle (the double-accumulation triple loop)
+on the host cores instead, each step a bounded sample of rows of the same
+workload.  Under torchrun (N > 1) every rank runs an independent replica
+(the operation has no data exchange), the time is the max over ranks and
+the value is the total work of all ranks over that time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP32 GEMM TFLOPS at M=N=K=8192 on 1 GB300 and % of FP32/tensor roofline"
+UNIT = "TFLOPS"
+L2_BYTES = 129 * 1000 * 1000
+# nominal dense tensor rates of the part (context for scaling a measured peak)
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_TF32_TFLOPS = 1100.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+FFMA_LANES_PER_SM = 128  # FP32 FMA units per SM (4 sub-partitions x 32)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (harness only: nothing of the GEMM is exchanged)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a scalar over all ranks (identity for a single process)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# peaks and clocks
+# ---------------------------------------------------------------------------
+def load_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock, power and throttle reasons in the background."""
+
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,nounits",
+                   "-lms", "100"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        with open(self.path) as f:
+            text = f.read()
+        os.unlink(self.path)
+        return self.summarise(text)
+
+    @staticmethod
+    def summarise(text: str) -> dict:
+        rows = [r for r in csv.reader(io.StringIO(text)) if r and not r[0].startswith("index")]
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                pw.append(float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": sorted(reasons), "samples": 0}
+        loaded = [s for s, p in zip(sm, pw) if p >= 0.5 * max(pw)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(pw)}
+
+
+def source_digest() -> str:
+    """Digest of the CUDA sources: ties stored ncu counters to the kernels they measured."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_fp32_gemm_row_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel: str, workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if still current."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            table = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = table.get(kernel, {}).get(workload)
+    if not e or e.get("source_digest") != source_digest():
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the baseline arm)
+# ---------------------------------------------------------------------------
+def oracle_rows_timing(A, B, seconds: float) -> dict:
+    """Time the oracle on the first R rows of C, R sized to take ~`seconds`."""
+    import oracle
+
+    M, K = A.shape
+    N = B.shape[1]
+    r0 = max(1, min(M, 2))
+    t0 = time.perf_counter()
+    oracle.ref_gemm_rows(A, B, 0, r0)
+    dt0 = max(time.perf_counter() - t0, 1e-6)
+    rows = int(max(1, min(M, r0 * seconds / dt0)))
+    t0 = time.perf_counter()
+    oracle.ref_gemm_rows(A, B, 0, rows)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * N * K
+    return {"rows": rows, "seconds": dt, "flops": flops, "tflops": flops / dt / 1e12,
+            "cores": oracle.max_threads()}
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the CPU oracle as it stands, bounded rows per step."""
+    import oracle
+    from seeded_inputs import workload_by_name, make_workload
+
+    if rank != 0:
+        return 0
+    w = workload_by_name(args.workload)
+    A, B = make_workload(w)
+    budget = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+    cal = oracle_rows_timing(A, B, budget)
+    rows = cal["rows"]
+    for _ in range(args.warmup):
+        oracle.ref_gemm_rows(A, B, 0, rows)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.ref_gemm_rows(A, B, 0, rows)
+        times.append(time.perf_counter() - t0)
+    flops = 2.0 * rows * w.N * w.K
+    total = sum(times)
+    value = flops * len(times) / total / 1e12
+    sample = (f"rows 0..{rows - 1} of the {w.M}x{w.N}x{w.K} product ({rows * w.N} of "
+              f"{w.M * w.N} outputs, full K) per step")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cal["cores"], "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import dense_fp32_gemm_row_gb300 as g
+    from seeded_inputs import make_workload, workload_by_name
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    g.load()
+
+    w = workload_by_name(args.workload)
+    algo = g.ALGOS[args.algo]
+    M, N, K = w.M, w.N, w.K
+    A_np, B_np = make_workload(w)
+    a = torch.from_numpy(A_np).to(dev)
+    b = torch.from_numpy(B_np).to(dev)
+    c = torch.empty((M, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    st, plan = g.gemm_f32_plan(M, N, K, algo, args.splits, a.data_ptr(), b.data_ptr(),
+                               c.data_ptr())
+    g.check(st, "plan")
+    input_bytes = 4 * (M * K + K * N)
+    flush = None
+    if input_bytes <= L2_BYTES * 2:
+        flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def step(ev_b=None, ev_e=None):
+        st = g.gemm_f32_algo_splitk_ev(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, algo,
+                                       args.splits, stream.cuda_stream,
+                                       ev_b.cuda_event if ev_b is not None else None,
+                                       ev_e.cuda_event if ev_e is not None else None)
+        g.check(st, "gemm_f32_algo_splitk_ev")
+
+    K_steps = args.steps
+    sb = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+    se = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+    ke = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps)]
+    for ev in sb + se + kb + ke:  # create the events so that their handles exist
+        ev.record(stream)
+    for _ in range(args.warmup):
+        step()
+        if flush is not None:
+            flush.zero_()
+    torch.cuda.synchronize(dev)
+    g.check(g.gemm_f32_device_status(1), "device status after warm-up")
+
+    gpu_uuid = None
+    try:
+        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(gpu_uuid)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(K_steps):
+        sb[i].record(stream)
+        step(kb[i], ke[i])
+        se[i].record(stream)
+        if flush is not None:
+            flush.zero_()
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    g.check(g.gemm_f32_device_status(1), "device status after timed steps")
+
+    step_ms = [sb[i].elapsed_time(se[i]) for i in range(K_steps)]
+    kern_ms = [kb[i].elapsed_time(ke[i]) for i in range(K_steps)]
+    if flush is None:
+        total_ms = sb[0].elapsed_time(se[-1])
+    else:
+        total_ms = sum(step_ms)
+    total_ms = reduce_max(total_ms, world, dev)
+    flops = 2.0 * M * N * K
+    value = flops * K_steps * world / (total_ms * 1e-3) / 1e12
+
+    # roofline of the dominant kernel (the GEMM kernel itself)
+    peaks, peak_src = load_peaks()
+    kern_mean_s = statistics.mean(kern_ms) * 1e-3
+    achieved = flops / kern_mean_s / 1e12
+    props = torch.cuda.get_device_properties(dev)
+    if plan["algo"] == g.ALGO_3XTF32:
+        bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        peak = bf16 * (NOMINAL_TF32_TFLOPS / NOMINAL_BF16_TFLOPS) / 3.0
+        bound, kname = "tensor", "sgemm_3xtf32"
+    else:
+        mhz = float(peaks.get("sm_max_mhz") or clocks.get("sm_max_mhz") or 2070.0)
+        peak = props.multi_processor_count * FFMA_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+        bound, kname = "alu", "sgemm_ffma"
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": stored_traffic(kname, w.name),
+                "kernel": kname, "peak_source": peak_src}
+
+    # end to end through the public entry point with pinned host buffers
+    e2e_steps = max(1, min(args.e2e_steps, K_steps))
+    hA = torch.from_numpy(A_np).pin_memory()
+    hB = torch.from_numpy(B_np).pin_memory()
+    hC = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    eb = torch.cuda.Event(enable_timing=True)
+    ee = torch.cuda.Event(enable_timing=True)
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    eb.record(stream)
+    for _ in range(e2e_steps):
+        a.copy_(hA, non_blocking=True)
+        b.copy_(hB, non_blocking=True)
+        g.check(g.gemm_f32_algo_splitk(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, algo,
+                                       args.splits, stream.cuda_stream), "e2e")
+        hC.copy_(c, non_blocking=True)
+    ee.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(eb.elapsed_time(ee), world, dev)
+    e2e_value = flops * e2e_steps * world / (e2e_ms * 1e-3) / 1e12
+    if not np.isfinite(hC[0, :8].numpy()).all():
+        raise SystemExit("non-finite output")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = oracle_rows_timing(A_np, B_np, args.cpu_seconds)
+        cpu = {"value": cb["tflops"], "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
+               "sample": (f"rows 0..{cb['rows'] - 1} of the {M}x{N}x{K} product "
+                          f"({cb['rows'] * N} outputs, full K, {cb['seconds']:.1f} s)")}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K_steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / K_steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "M": M, "N": N, "K": K, "dist": w.dist,
+                   "algo": {1: "ffma", 2: "3xtf32"}.get(plan["algo"], str(plan["algo"])),
+                   "splits": plan["splits"], "tile": [plan["tile_m"], plan["tile_n"],
+                                                      plan["tile_k"]],
+                   "stages": plan["stages"], "ctas": plan["ctas"],
+                   "l2": ("flush 512 MiB between steps" if flush is not None
+                          else "inputs larger than L2, no flush"),
+                   "parallelism": f"replicas{world}" if world > 1 else "single"},
+        "timing": {"step_ms_median": statistics.median(step_ms), "step_ms_mean":
+                   statistics.mean(step_ms), "step_ms_min": min(step_ms),
+                   "kernel_ms_mean": statistics.mean(kern_ms),
+                   "kernel_ms_median": statistics.median(kern_ms), "wall_s": wall},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": input_bytes,
+                "d2h_bytes_per_step": 4 * M * N, "steps": e2e_steps},
+        "gpu_launches": K_steps * plan["kernels"] + (0 if flush is None else 0),
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description="FP32 GEMM benchmark")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--algo", choices=["auto", "ffma", "3xtf32"], default="auto")
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--workload", default="square_8192_normal")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,96 @@
+// device_sync.cuh -- inline-PTX wrappers for sm_103a: mbarriers, tensor
+// memory access (TMA) tile loads, the global nanosecond timer, and the
+// bounded barrier wait every kernel of this library uses.
+//
+// Every wait on an mbarrier is bounded in time.  When the limit runs out the
+// waiting thread ORs a fault bit into the library's device fault word and the
+// kernel winds down instead of spinning forever; the host reads the word with
+// gemm_f32_device_status().
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+namespace gemm_f32_dev {
+
+// bits of the device fault word
+constexpr unsigned kFaultFullBarrier  = 1u << 0;  // consumer waited too long for a tile
+constexpr unsigned kFaultEmptyBarrier = 1u << 1;  // producer waited too long for a free slot
+constexpr unsigned kFaultDrain        = 1u << 2;  // in-flight copies did not land while winding down
+constexpr unsigned kFaultAccumBarrier = 1u << 3;  // epilogue / MMA accumulator handshake
+constexpr unsigned kFaultSelfTest     = 1u << 4;  // watchdog self-test barrier
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async proxy (TMA, tensor cores).
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait until the phase with the given parity has completed, for at most
+// timeout_ns nanoseconds.  Returns false (and sets `bit` in *fault) on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long timeout_ns,
+                                          unsigned* fault, unsigned bit) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > static_cast<uint64_t>(timeout_ns)) {
+            if (fault) atomicOr(fault, bit);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 2-D tiled TMA load of one box into shared memory; completion is signalled
+// as transaction bytes on the mbarrier.  c0 is the innermost coordinate.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+}  // namespace gemm_f32_dev

@@ -1,0 +1,141 @@
+// gemm_aux.cu -- the memory-bound helper kernels of the GEMM path:
+//
+//  * pad_copy:       copies a row-major operand into a buffer whose row
+//                    stride is a multiple of 16 bytes and whose base is
+//                    256-byte aligned, the form a TMA descriptor requires.
+//  * splitk_reduce:  C = sum of the split-K partial products, added in split
+//                    order 0, 1, ..., S-1 so that the result is deterministic.
+//  * fill_zero:      C = 0 for K == 0 (the empty sum of the lecture-12
+//                    golden reference).
+//  * watchdog:       a self-test that waits on a barrier nothing completes.
+//
+// All are grid-stride loops with coalesced accesses along rows; they are
+// bounded by HBM (or L2) bandwidth, never by arithmetic.
+#include <cstdint>
+
+#include "device_sync.cuh"
+#include "gemm_internal.h"
+
+namespace gemm_f32_impl {
+namespace {
+
+using namespace gemm_f32_dev;
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads)
+pad_copy_kernel(const float* __restrict__ src, long long lds, long long rows, long long cols,
+                float* __restrict__ dst, long long ldd) {
+    for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
+        const float* s = src + r * lds;
+        float* d = dst + r * ldd;
+        for (long long c = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; c < cols;
+             c += static_cast<long long>(gridDim.x) * kThreads)
+            d[c] = s[c];
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+splitk_reduce_kernel(const float* __restrict__ ws, long long split_stride, long long ldw,
+                     int splits, float* __restrict__ C, long long ldc, int M, int N) {
+    for (long long r = blockIdx.y; r < M; r += gridDim.y) {
+        const float* w = ws + r * ldw;
+        float* c = C + r * ldc;
+        for (long long j = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; j < N;
+             j += static_cast<long long>(gridDim.x) * kThreads) {
+            float sum = w[j];
+            for (int s = 1; s < splits; ++s) sum += w[s * split_stride + j];
+            c[j] = sum;
+        }
+    }
+}
+
+// Vector form: ldw, ldc, N multiples of 4 and both bases 16-byte aligned.
+__global__ void __launch_bounds__(kThreads)
+splitk_reduce4_kernel(const float4* __restrict__ ws, long long split_stride4, long long ldw4,
+                      int splits, float4* __restrict__ C, long long ldc4, int M, int N4) {
+    for (long long r = blockIdx.y; r < M; r += gridDim.y) {
+        const float4* w = ws + r * ldw4;
+        float4* c = C + r * ldc4;
+        for (long long j = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; j < N4;
+             j += static_cast<long long>(gridDim.x) * kThreads) {
+            float4 sum = w[j];
+            for (int s = 1; s < splits; ++s) {
+                const float4 v = w[s * split_stride4 + j];
+                sum.x += v.x;
+                sum.y += v.y;
+                sum.z += v.z;
+                sum.w += v.w;
+            }
+            c[j] = sum;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) fill_zero_kernel(float* __restrict__ C, long long n) {
+    for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * kThreads)
+        C[i] = 0.0f;
+}
+
+__global__ void watchdog_selftest_kernel(unsigned* fault, long long timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_addr(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // Nothing arrives on the barrier, so its first phase never completes and
+    // the bounded wait must give up after timeout_ns and flag the fault word.
+    mbar_wait(b, 0, timeout_ns, threadIdx.x == 0 ? fault : nullptr, kFaultSelfTest);
+}
+
+unsigned grid_1d(long long work, long long per_block, unsigned cap) {
+    long long g = (work + per_block - 1) / per_block;
+    if (g < 1) g = 1;
+    return static_cast<unsigned>(g < cap ? g : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_pad_copy(const float* src, long long lds, long long rows, long long cols,
+                            float* dst, long long ldd, cudaStream_t s) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    dim3 grid(grid_1d(cols, kThreads, 64), static_cast<unsigned>(rows < 65535 ? rows : 65535));
+    pad_copy_kernel<<<grid, kThreads, 0, s>>>(src, lds, rows, cols, dst, ldd);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_reduce(const float* ws, long long split_stride, long long ldw,
+                                 int splits, float* C, long long ldc, int M, int N,
+                                 cudaStream_t s) {
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    const unsigned gy = static_cast<unsigned>(M < 65535 ? M : 65535);
+    const bool vec = (N % 4 == 0) && (ldw % 4 == 0) && (ldc % 4 == 0) && (split_stride % 4 == 0) &&
+                     (reinterpret_cast<uintptr_t>(ws) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(C) % 16 == 0);
+    if (vec) {
+        dim3 grid(grid_1d(N / 4, kThreads, 64), gy);
+        splitk_reduce4_kernel<<<grid, kThreads, 0, s>>>(
+            reinterpret_cast<const float4*>(ws), split_stride / 4, ldw / 4, splits,
+            reinterpret_cast<float4*>(C), ldc / 4, M, N / 4);
+    } else {
+        dim3 grid(grid_1d(N, kThreads, 64), gy);
+        splitk_reduce_kernel<<<grid, kThreads, 0, s>>>(ws, split_stride, ldw, splits, C, ldc, M, N);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill_zero(float* C, long long count, cudaStream_t s) {
+    if (count <= 0) return cudaSuccess;
+    fill_zero_kernel<<<grid_1d(count, kThreads, 4096), kThreads, 0, s>>>(C, count);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_watchdog_selftest(unsigned* fault, long long timeout_ns, cudaStream_t s) {
+    watchdog_selftest_kernel<<<1, 32, 0, s>>>(fault, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace gemm_f32_impl

@@ -1,0 +1,49 @@
+// gemm_internal.h -- host-side interfaces between the C-ABI layer and the
+// kernel translation units of libgemmf32.so.  Not installed, not exported.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+namespace gemm_f32_impl {
+
+// Default wait limit for every bounded mbarrier wait in the library's kernels.
+constexpr long long kDefaultTimeoutNs = 2000000000LL;  // 2 s
+
+// ---- sgemm_ffma (CUDA-core FFMA kernel) -----------------------------------
+struct FfmaConfig {
+    int bm, bn, bk, stages, threads, ctas_per_sm;
+    int smem_bytes;  // dynamic shared memory per CTA
+};
+FfmaConfig ffma_config();
+
+struct FfmaArgs {
+    CUtensorMap tmA;  // A as {K, M}, box {bk, bm}, swizzled
+    CUtensorMap tmB;  // B as {N, K}, box {bn, bk}, unswizzled
+    float* out;             // C, or the split-K partial buffer
+    long long ldo;          // row stride of out (elements)
+    long long split_stride; // elements between consecutive split partials
+    int M, N, K;
+    int kb_per_split;       // K blocks (of bk) per split
+    int splits;
+    int vec_store;          // 1: ldo % 4 == 0 and out 16-byte aligned
+    unsigned* fault;
+    long long timeout_ns;
+};
+cudaError_t launch_sgemm_ffma(const FfmaArgs& a, cudaStream_t s);
+
+// ---- helper kernels (gemm_aux.cu) ------------------------------------------
+// dst[r*ldd + c] = src[r*lds + c] for r < rows, c < cols
+cudaError_t launch_pad_copy(const float* src, long long lds, long long rows, long long cols,
+                            float* dst, long long ldd, cudaStream_t s);
+// C[i*ldc + j] = sum_{s < splits} ws[s*split_stride + i*ldw + j], s ascending
+cudaError_t launch_splitk_reduce(const float* ws, long long split_stride, long long ldw,
+                                 int splits, float* C, long long ldc, int M, int N,
+                                 cudaStream_t s);
+// C[0 .. count) = 0
+cudaError_t launch_fill_zero(float* C, long long count, cudaStream_t s);
+// watchdog self-test: waits on a never-completed barrier for timeout_ns
+cudaError_t launch_watchdog_selftest(unsigned* fault, long long timeout_ns, cudaStream_t s);
+
+}  // namespace gemm_f32_impl

@@ -1,0 +1,171 @@
+/*
+ * gemm_f32.h -- C ABI of libgemmf32.so, single-precision dense matrix
+ * multiply C = A * B for one NVIDIA GB300 (sm_103a).
+ *
+ * Operation ("Lecture 12: final project", runguoli.com ECE408 notes l12,
+ * section 2, the general M/N/K kernel tiledMatMulKernel, and section 3, the
+ * CPU golden reference):
+ *
+ *     C[i][j] = sum_{k < K} A[i][k] * B[k][j]      0 <= i < M, 0 <= j < N
+ *
+ * Layout: A is M x K, B is K x N, C is M x N, all packed row-major
+ * (leading dimensions K, N and N elements).  There is no alpha, beta or
+ * transpose: C is overwritten.  All three are 4-byte floats in DEVICE memory
+ * of the current CUDA device; any alignment is accepted (4-byte aligned
+ * pointers that are not 16-byte aligned, and row strides that are not a
+ * multiple of 16 bytes, are served through an internal padded copy).
+ *
+ * Accuracy: every algorithm is checked against the double-accumulating CPU
+ * reference within |C - C_ref| <= 1e-3 + 1e-3 |C_ref| elementwise (the
+ * section 4 atol/rtol of the same page).  Results are run-to-run
+ * deterministic for a given (shape, algo, splits) on a given device.
+ *
+ * Edge semantics (same page, section 7, the early exits of main): a negative
+ * dimension is an error; M == 0 or N == 0 returns success and launches
+ * nothing; K == 0 writes C = 0.  Elements of memory outside C are never
+ * written (out-of-range rows and columns of a boundary tile are skipped, the
+ * lecture-5 coarsened kernel's predicated store).
+ *
+ * Ownership and ordering: the caller owns A, B and C; the library reads A
+ * and B, writes C and its own workspace, and keeps no reference to any of
+ * them after the call returns.  Every call is asynchronous on `stream`
+ * (enqueue and return; no implicit synchronisation).  The library owns a
+ * workspace per (device, stream), grown on demand: a call that must grow it
+ * synchronises that stream first.  gemm_f32_release() frees all of it.
+ * The entry points are thread-safe.
+ *
+ * Errors: 0 is success.  Negative values are library errors (GEMM_F32_ERR_*),
+ * positive values are the cudaError_t of the failing CUDA runtime call.  No
+ * entry point exits or aborts the process.  Nothing runs on the host CPU:
+ * there is no CPU fallback, and a device other than sm_103 is rejected.
+ */
+#ifndef GEMM_F32_H
+#define GEMM_F32_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define GEMM_F32_SUCCESS                 0
+/* negative dimension; NULL pointer with a nonzero extent; unknown algo;
+ * splits out of range; C overlapping A or B; a size product that overflows */
+#define GEMM_F32_ERR_INVALID_VALUE      (-1)
+/* no CUDA device, or the current device is not compute capability 10.3 */
+#define GEMM_F32_ERR_UNSUPPORTED_DEVICE (-2)
+/* the workspace could not be allocated */
+#define GEMM_F32_ERR_WORKSPACE          (-3)
+/* a kernel gave up waiting on one of its own pipeline barriers (watchdog) */
+#define GEMM_F32_ERR_DEVICE_TIMEOUT     (-4)
+/* the driver rejected a tensor-memory-access descriptor */
+#define GEMM_F32_ERR_DESCRIPTOR         (-5)
+
+/* ---- algorithms -------------------------------------------------------- */
+/* Choose by shape (currently the tensor-core kernel for all sizes). */
+#define GEMM_F32_ALGO_AUTO    0
+/* CUDA-core FFMA kernel: TMA-fed, swizzled shared-memory tiles, mbarrier
+ * pipeline, 8x8 register tile per thread. */
+#define GEMM_F32_ALGO_FFMA    1
+/* Tensor-core kernel: each operand split into a TF32 high part and a TF32
+ * low part, three tcgen05 products hi*hi + hi*lo + lo*hi accumulated in
+ * tensor memory in fp32. */
+#define GEMM_F32_ALGO_3XTF32  2
+
+/* Largest explicit split-K factor accepted by gemm_f32_algo_splitk. */
+#define GEMM_F32_MAX_SPLITS   256
+
+/*
+ * gemm_f32 -- C = A * B with the algorithm the library picks for the shape.
+ * Same as gemm_f32_algo(A, B, C, M, N, K, GEMM_F32_ALGO_AUTO, stream).
+ * A: M*K floats, B: K*N floats, C: M*N floats, device pointers, row-major.
+ */
+int gemm_f32(const float* A, const float* B, float* C, int M, int N, int K,
+             cudaStream_t stream);
+
+/*
+ * gemm_f32_algo -- as gemm_f32 with an explicit per-call algorithm
+ * (GEMM_F32_ALGO_*).  There is no global state: the choice applies to this
+ * call only.  The split-K factor is chosen by the library.
+ */
+int gemm_f32_algo(const float* A, const float* B, float* C, int M, int N, int K,
+                  int algo, cudaStream_t stream);
+
+/*
+ * gemm_f32_algo_splitk -- as gemm_f32_algo with an explicit split of the
+ * K dimension.  splits == 0 lets the library choose; 1 disables splitting;
+ * 2..GEMM_F32_MAX_SPLITS computes that many partial products over disjoint
+ * K ranges into the workspace and adds them in a fixed order (split 0 first)
+ * in a separate kernel, so the result is deterministic.  A split count
+ * larger than the number of K blocks is reduced to it.
+ */
+int gemm_f32_algo_splitk(const float* A, const float* B, float* C, int M, int N, int K,
+                         int algo, int splits, cudaStream_t stream);
+
+/*
+ * gemm_f32_algo_splitk_ev -- as gemm_f32_algo_splitk, and, for profiling,
+ * records `main_begin` on `stream` just before the main GEMM kernel is
+ * launched and `main_end` just after it (either may be NULL).  The events
+ * must belong to the current device.  Staging copies and the split-K
+ * reduction, when a call has them, fall outside the pair.
+ */
+int gemm_f32_algo_splitk_ev(const float* A, const float* B, float* C, int M, int N, int K,
+                            int algo, int splits, cudaStream_t stream,
+                            cudaEvent_t main_begin, cudaEvent_t main_end);
+
+/*
+ * gemm_f32_plan_info / gemm_f32_plan -- what a call with these arguments
+ * would launch, without launching anything.  Needs a device (it reads the
+ * SM count); returns a status code like the compute entry points.
+ */
+typedef struct gemm_f32_plan_info {
+    int algo;            /* resolved GEMM_F32_ALGO_FFMA or _3XTF32 (0 if no launch) */
+    int splits;          /* resolved split-K factor (1 = none) */
+    int tile_m;          /* output tile rows per CTA */
+    int tile_n;          /* output tile columns per CTA */
+    int tile_k;          /* K depth of one pipeline stage */
+    int stages;          /* pipeline stages in shared memory */
+    int ctas;            /* CTAs in the main kernel's grid */
+    int stage_a;         /* 1 if A goes through a staging copy */
+    int stage_b;         /* 1 if B goes through a staging copy */
+    int kernels;         /* kernel launches the call makes */
+    long long workspace_bytes; /* workspace the call needs */
+} gemm_f32_plan_info;
+
+int gemm_f32_plan(int M, int N, int K, int algo, int splits,
+                  const float* A, const float* B, const float* C,
+                  gemm_f32_plan_info* out);
+
+/*
+ * gemm_f32_device_status -- read (and with clear != 0, reset) the device
+ * fault word that kernels set when a bounded wait on one of their pipeline
+ * barriers runs out.  Synchronises the current device.  Returns 0, or
+ * GEMM_F32_ERR_DEVICE_TIMEOUT if a kernel reported a timeout since the last
+ * clear, or a positive cudaError_t.
+ */
+int gemm_f32_device_status(int clear);
+
+/*
+ * gemm_f32_selftest_watchdog -- launch on `stream` one kernel that waits on
+ * a shared-memory barrier that nothing ever completes, with a wait limit of
+ * timeout_ns nanoseconds (1e3 .. 1e10), then synchronise the stream and
+ * return gemm_f32_device_status(1).  A working watchdog returns
+ * GEMM_F32_ERR_DEVICE_TIMEOUT and leaves the context usable.
+ */
+int gemm_f32_selftest_watchdog(long long timeout_ns, cudaStream_t stream);
+
+/* Release every workspace (synchronises each device that has one). */
+int gemm_f32_release(void);
+
+/* Static text for a status code. */
+const char* gemm_f32_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int gemm_f32_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_F32_H */
