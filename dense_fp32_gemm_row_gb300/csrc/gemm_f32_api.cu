@@ -140,12 +140,13 @@ int workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
 
 struct Plan {
     int algo = 0;
+    int bn = 0;
     int splits = 1;
     int kb_per_split = 0;
     int stage_a = 0, stage_b = 0;
-    long long lda = 0, ldb = 0;   // row strides the kernel reads (elements)
+    long long lda = 0, ldb = 0;   // row strides of the operands the kernel reads (elements)
     long long ldw = 0;            // split-K partial row stride
-    size_t off_a = 0, off_b = 0, off_w = 0, ws_bytes = 0;
+    size_t off_a = 0, off_a2 = 0, off_b = 0, off_b2 = 0, off_w = 0, ws_bytes = 0;
     int tile_m = 0, tile_n = 0, tile_k = 0, stages = 0, ctas = 0, kernels = 0;
 };
 
@@ -169,23 +170,15 @@ int validate(const float* A, const float* B, const float* C, int M, int N, int K
     return GEMM_F32_SUCCESS;
 }
 
-void make_plan(const DeviceState& d, const float* A, const float* B, int M, int N, int K, int algo,
-               int splits, Plan* p) {
-    const FfmaConfig fc = ffma_config();
-    p->algo = (algo == GEMM_F32_ALGO_AUTO) ? GEMM_F32_ALGO_FFMA : algo;
-    p->tile_m = fc.bm;
-    p->tile_n = fc.bn;
-    p->tile_k = fc.bk;
-    p->stages = fc.stages;
-    const int tiles = ((M + fc.bm - 1) / fc.bm) * ((N + fc.bn - 1) / fc.bn);
-    const int kb_total = (K + fc.bk - 1) / fc.bk;
-    int s = splits;
+// Split-K factor: spread a grid that would fill less than half of the
+// concurrent CTA slots over disjoint K ranges, keeping >= 4 K blocks each.
+int choose_splits(int requested, int tiles, int kb_total, int slots) {
+    int s = requested;
     if (s == 0) {
-        const int slots = d.sm_count * fc.ctas_per_sm;
         s = 1;
         if (tiles * 2 <= slots) {
             s = slots / tiles;
-            const int max_by_depth = kb_total / 4;  // keep >= 4 K blocks per split
+            const int max_by_depth = kb_total / 4;
             if (s > max_by_depth) s = max_by_depth;
             if (s > GEMM_F32_MAX_SPLITS) s = GEMM_F32_MAX_SPLITS;
             if (s < 1) s = 1;
@@ -193,29 +186,73 @@ void make_plan(const DeviceState& d, const float* A, const float* B, int M, int 
     }
     if (s > kb_total) s = kb_total;
     if (s < 1) s = 1;
+    return s;
+}
+
+size_t carve(size_t* off, long long bytes) {
+    const size_t at = *off;
+    *off += static_cast<size_t>(round_up(bytes, 256));
+    return at;
+}
+
+void make_plan(const DeviceState& d, const float* A, const float* B, int M, int N, int K, int algo,
+               int splits, Plan* p) {
+    p->algo = (algo == GEMM_F32_ALGO_AUTO) ? GEMM_F32_ALGO_3XTF32 : algo;
+    int bm, bn, bk, slots;
+    if (p->algo == GEMM_F32_ALGO_3XTF32) {
+        // wide tiles unless they leave most SMs idle
+        const int tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
+        p->bn = (tiles256 >= d.sm_count || N <= 128) ? 256 : 128;
+        if (N <= 128) p->bn = 128;
+        const Tf32x3Config tc = tf32x3_config(p->bn);
+        bm = tc.bm;
+        bn = tc.bn;
+        bk = tc.bk;
+        p->stages = tc.stages;
+        slots = d.sm_count;
+    } else {
+        const FfmaConfig fc = ffma_config();
+        bm = fc.bm;
+        bn = fc.bn;
+        bk = fc.bk;
+        p->bn = bn;
+        p->stages = fc.stages;
+        slots = d.sm_count * fc.ctas_per_sm;
+    }
+    p->tile_m = bm;
+    p->tile_n = bn;
+    p->tile_k = bk;
+    const int tiles = ((M + bm - 1) / bm) * ((N + bn - 1) / bn);
+    const int kb_total = (K + bk - 1) / bk;
+    const int s = choose_splits(splits, tiles, kb_total, slots);
     p->kb_per_split = (kb_total + s - 1) / s;
     p->splits = (kb_total + p->kb_per_split - 1) / p->kb_per_split;
-    p->ctas = tiles * p->splits;
-
-    p->stage_a = (K % 4 != 0) || misaligned16(A);
-    p->stage_b = (N % 4 != 0) || misaligned16(B);
-    p->lda = p->stage_a ? round_up(K, 4) : K;
-    p->ldb = p->stage_b ? round_up(N, 4) : N;
+    const int units = tiles * p->splits;
     p->ldw = round_up(N, 4);
+
     size_t off = 0;
-    if (p->stage_a) {
-        p->off_a = off;
-        off += static_cast<size_t>(round_up(static_cast<long long>(M) * p->lda * 4, 256));
+    if (p->algo == GEMM_F32_ALGO_3XTF32) {
+        // A -> Ahi, Alo (M x K); B -> B^T hi, lo (N x K); rows padded to 16 bytes
+        p->stage_a = 1;
+        p->stage_b = 1;
+        p->lda = round_up(K, 4);
+        p->ldb = round_up(K, 4);
+        p->off_a = carve(&off, static_cast<long long>(M) * p->lda * 4);
+        p->off_a2 = carve(&off, static_cast<long long>(M) * p->lda * 4);
+        p->off_b = carve(&off, static_cast<long long>(N) * p->ldb * 4);
+        p->off_b2 = carve(&off, static_cast<long long>(N) * p->ldb * 4);
+        p->ctas = units < d.sm_count ? units : d.sm_count;
+    } else {
+        p->stage_a = (K % 4 != 0) || misaligned16(A);
+        p->stage_b = (N % 4 != 0) || misaligned16(B);
+        p->lda = p->stage_a ? round_up(K, 4) : K;
+        p->ldb = p->stage_b ? round_up(N, 4) : N;
+        if (p->stage_a) p->off_a = carve(&off, static_cast<long long>(M) * p->lda * 4);
+        if (p->stage_b) p->off_b = carve(&off, static_cast<long long>(K) * p->ldb * 4);
+        p->ctas = units;
     }
-    if (p->stage_b) {
-        p->off_b = off;
-        off += static_cast<size_t>(round_up(static_cast<long long>(K) * p->ldb * 4, 256));
-    }
-    if (p->splits > 1) {
-        p->off_w = off;
-        off += static_cast<size_t>(
-            round_up(static_cast<long long>(p->splits) * M * p->ldw * 4, 256));
-    }
+    if (p->splits > 1)
+        p->off_w = carve(&off, static_cast<long long>(p->splits) * M * p->ldw * 4);
     p->ws_bytes = off;
     p->kernels = 1 + p->stage_a + p->stage_b + (p->splits > 1 ? 1 : 0);
 }
@@ -224,7 +261,6 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int algo,
         cudaStream_t stream, cudaEvent_t ev_begin = nullptr, cudaEvent_t ev_end = nullptr) {
     int st = validate(A, B, C, M, N, K, algo, splits);
     if (st != GEMM_F32_SUCCESS) return st;
-    if (algo == GEMM_F32_ALGO_3XTF32) return GEMM_F32_ERR_INVALID_VALUE;  // not built yet
     if (M == 0 || N == 0) return GEMM_F32_SUCCESS;
 
     std::lock_guard<std::mutex> lock(g_mutex);
@@ -252,52 +288,95 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int algo,
         ws = static_cast<unsigned char*>(w);
     }
 
-    const float* a_src = A;
-    const float* b_src = B;
+    float* out = C;
+    long long ldo = N, split_stride = 0;
+    if (p.splits > 1) {
+        out = reinterpret_cast<float*>(ws + p.off_w);
+        ldo = p.ldw;
+        split_stride = static_cast<long long>(M) * p.ldw;
+    }
+    const int vec_store = (ldo % 4 == 0) && !misaligned16(out);
     cudaError_t e = cudaSuccess;
-    if (p.stage_a) {
-        float* dst = reinterpret_cast<float*>(ws + p.off_a);
-        e = launch_pad_copy(A, K, M, K, dst, p.lda, stream);
-        if (e != cudaSuccess) return static_cast<int>(e);
-        a_src = dst;
-    }
-    if (p.stage_b) {
-        float* dst = reinterpret_cast<float*>(ws + p.off_b);
-        e = launch_pad_copy(B, N, K, N, dst, p.ldb, stream);
-        if (e != cudaSuccess) return static_cast<int>(e);
-        b_src = dst;
-    }
 
-    const FfmaConfig fc = ffma_config();
-    FfmaArgs fa;
-    std::memset(&fa, 0, sizeof(fa));
-    st = encode_2d(&fa.tmA, a_src, K, M, p.lda, fc.bk, fc.bm, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st != GEMM_F32_SUCCESS) return st;
-    st = encode_2d(&fa.tmB, b_src, N, K, p.ldb, fc.bn, fc.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (st != GEMM_F32_SUCCESS) return st;
-    fa.M = M;
-    fa.N = N;
-    fa.K = K;
-    fa.kb_per_split = p.kb_per_split;
-    fa.splits = p.splits;
-    fa.fault = d->fault;
-    fa.timeout_ns = kDefaultTimeoutNs;
-    if (p.splits > 1) {
-        fa.out = reinterpret_cast<float*>(ws + p.off_w);
-        fa.ldo = p.ldw;
-        fa.split_stride = static_cast<long long>(M) * p.ldw;
+    if (p.algo == GEMM_F32_ALGO_3XTF32) {
+        float* a_hi = reinterpret_cast<float*>(ws + p.off_a);
+        float* a_lo = reinterpret_cast<float*>(ws + p.off_a2);
+        float* b_hi = reinterpret_cast<float*>(ws + p.off_b);
+        float* b_lo = reinterpret_cast<float*>(ws + p.off_b2);
+        if ((e = launch_split_rows(A, K, M, K, a_hi, a_lo, p.lda, stream)) != cudaSuccess)
+            return static_cast<int>(e);
+        if ((e = launch_split_transpose(B, N, K, N, b_hi, b_lo, p.ldb, stream)) != cudaSuccess)
+            return static_cast<int>(e);
+        Tf32x3Args ta;
+        std::memset(&ta, 0, sizeof(ta));
+        if ((st = encode_2d(&ta.tmAhi, a_hi, K, M, p.lda, p.tile_k, p.tile_m,
+                            CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
+            (st = encode_2d(&ta.tmAlo, a_lo, K, M, p.lda, p.tile_k, p.tile_m,
+                            CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
+            (st = encode_2d(&ta.tmBhi, b_hi, K, N, p.ldb, p.tile_k, p.tile_n,
+                            CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
+            (st = encode_2d(&ta.tmBlo, b_lo, K, N, p.ldb, p.tile_k, p.tile_n,
+                            CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS)
+            return st;
+        ta.out = out;
+        ta.ldo = ldo;
+        ta.split_stride = split_stride;
+        ta.M = M;
+        ta.N = N;
+        ta.K = K;
+        ta.bn = p.bn;
+        ta.kb_per_split = p.kb_per_split;
+        ta.splits = p.splits;
+        ta.vec_store = vec_store;
+        ta.fault = d->fault;
+        ta.timeout_ns = kDefaultTimeoutNs;
+        if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
+            return static_cast<int>(e);
+        if ((e = launch_sgemm_3xtf32(ta, stream, d->sm_count)) != cudaSuccess)
+            return static_cast<int>(e);
+        if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess)
+            return static_cast<int>(e);
     } else {
-        fa.out = C;
-        fa.ldo = N;
-        fa.split_stride = 0;
+        const float* a_src = A;
+        const float* b_src = B;
+        if (p.stage_a) {
+            float* dst = reinterpret_cast<float*>(ws + p.off_a);
+            if ((e = launch_pad_copy(A, K, M, K, dst, p.lda, stream)) != cudaSuccess)
+                return static_cast<int>(e);
+            a_src = dst;
+        }
+        if (p.stage_b) {
+            float* dst = reinterpret_cast<float*>(ws + p.off_b);
+            if ((e = launch_pad_copy(B, N, K, N, dst, p.ldb, stream)) != cudaSuccess)
+                return static_cast<int>(e);
+            b_src = dst;
+        }
+        FfmaArgs fa;
+        std::memset(&fa, 0, sizeof(fa));
+        if ((st = encode_2d(&fa.tmA, a_src, K, M, p.lda, p.tile_k, p.tile_m,
+                            CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
+            (st = encode_2d(&fa.tmB, b_src, N, K, p.ldb, p.tile_n, p.tile_k,
+                            CU_TENSOR_MAP_SWIZZLE_NONE)) != GEMM_F32_SUCCESS)
+            return st;
+        fa.out = out;
+        fa.ldo = ldo;
+        fa.split_stride = split_stride;
+        fa.M = M;
+        fa.N = N;
+        fa.K = K;
+        fa.kb_per_split = p.kb_per_split;
+        fa.splits = p.splits;
+        fa.vec_store = vec_store;
+        fa.fault = d->fault;
+        fa.timeout_ns = kDefaultTimeoutNs;
+        if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
+            return static_cast<int>(e);
+        if ((e = launch_sgemm_ffma(fa, stream)) != cudaSuccess) return static_cast<int>(e);
+        if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess)
+            return static_cast<int>(e);
     }
-    fa.vec_store = (fa.ldo % 4 == 0) && !misaligned16(fa.out);
-    if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess) return static_cast<int>(e);
-    e = launch_sgemm_ffma(fa, stream);
-    if (e != cudaSuccess) return static_cast<int>(e);
-    if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess) return static_cast<int>(e);
     if (p.splits > 1) {
-        e = launch_splitk_reduce(fa.out, fa.split_stride, p.ldw, p.splits, C, N, M, N, stream);
+        e = launch_splitk_reduce(out, split_stride, p.ldw, p.splits, C, N, M, N, stream);
         if (e != cudaSuccess) return static_cast<int>(e);
     }
     return GEMM_F32_SUCCESS;

@@ -33,6 +33,38 @@ struct FfmaArgs {
 };
 cudaError_t launch_sgemm_ffma(const FfmaArgs& a, cudaStream_t s);
 
+// ---- sgemm_3xtf32 (tcgen05 tensor-core kernel) -----------------------------
+struct Tf32x3Config {
+    int bm, bn, bk, stages, threads;
+    int smem_bytes;
+};
+Tf32x3Config tf32x3_config(int bn);  // bn = 128 or 256
+
+struct Tf32x3Args {
+    CUtensorMap tmAhi, tmAlo;  // A hi / lo as {K, M}, box {bk, bm}, 128-byte swizzle
+    CUtensorMap tmBhi, tmBlo;  // B^T hi / lo as {K, N}, box {bk, bn}, 128-byte swizzle
+    float* out;
+    long long ldo;
+    long long split_stride;
+    int M, N, K;
+    int bn;
+    int kb_per_split;
+    int splits;
+    int vec_store;
+    unsigned* fault;
+    long long timeout_ns;
+};
+// persistent grid of min(units, sm_count) CTAs
+cudaError_t launch_sgemm_3xtf32(const Tf32x3Args& a, cudaStream_t s, int sm_count);
+
+// ---- TF32 hi/lo staging (tf32_split.cu) --------------------------------------
+// hi/lo[r*ldd + c] from src[r*lds + c] (same orientation)
+cudaError_t launch_split_rows(const float* src, long long lds, long long rows, long long cols,
+                              float* hi, float* lo, long long ldd, cudaStream_t s);
+// hi/lo[n*ldt + k] from src[k*lds + n] (K x N -> N x K)
+cudaError_t launch_split_transpose(const float* src, long long lds, int K, int N, float* hi,
+                                   float* lo, long long ldt, cudaStream_t s);
+
 // ---- helper kernels (gemm_aux.cu) ------------------------------------------
 // dst[r*ldd + c] = src[r*lds + c] for r < rows, c < cols
 cudaError_t launch_pad_copy(const float* src, long long lds, long long rows, long long cols,

@@ -63,7 +63,7 @@ extern "C" {
 #define GEMM_F32_ERR_DESCRIPTOR         (-5)
 
 /* ---- algorithms -------------------------------------------------------- */
-/* Choose by shape (currently the tensor-core kernel for all sizes). */
+/* Choose by shape: currently the tensor-core 3xTF32 kernel for every shape. */
 #define GEMM_F32_ALGO_AUTO    0
 /* CUDA-core FFMA kernel: TMA-fed, swizzled shared-memory tiles, mbarrier
  * pipeline, 8x8 register tile per thread. */

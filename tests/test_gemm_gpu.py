@@ -142,10 +142,17 @@ def test_run_to_run_bitwise_determinism(algo):
 def test_plan_reports_split_k_and_staging():
     st, p = g.gemm_f32_plan(256, 256, 65536, g.ALGO_FFMA, 0)
     assert st == 0 and p["splits"] > 1 and p["workspace_bytes"] > 0
-    st, p = g.gemm_f32_plan(1025, 1023, 1000, g.ALGO_FFMA, 1, A=256, B=256, C=256)
+    fa, fb, fc = 1 << 32, 1 << 36, 1 << 40  # distinct 256-byte aligned addresses (never touched)
+    st, p = g.gemm_f32_plan(1025, 1023, 1000, g.ALGO_FFMA, 1, A=fa, B=fb, C=fc)
     assert st == 0 and p["stage_b"] == 1 and p["stage_a"] == 0 and p["splits"] == 1
-    st, p = g.gemm_f32_plan(8192, 8192, 8192, g.ALGO_AUTO, 0, A=256, B=256, C=256)
+    st, p = g.gemm_f32_plan(8192, 8192, 8192, g.ALGO_FFMA, 0, A=fa, B=fb, C=fc)
     assert st == 0 and p["splits"] == 1 and p["stage_a"] == 0 and p["stage_b"] == 0
+    assert p["kernels"] == 1
+    # the tensor-core path always stages the TF32 hi/lo split of both operands
+    st, p = g.gemm_f32_plan(8192, 8192, 8192, g.ALGO_AUTO, 0, A=fa, B=fb, C=fc)
+    assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["splits"] == 1
+    assert p["stage_a"] == 1 and p["stage_b"] == 1 and p["kernels"] == 3
+    assert p["ctas"] <= 160 and p["workspace_bytes"] >= 4 * 8192 * 8192 * 4
 
 
 def test_status_codes_on_device():
