@@ -179,14 +179,19 @@ class ClockSampler:
                 "power_w_max": max(pw)}
 
 
-def source_digest() -> str:
-    """Digest of the CUDA sources: ties stored ncu counters to the kernels they measured."""
+KERNEL_SOURCES = {
+    "sgemm_ffma": ["sgemm_ffma.cu", "device_sync.cuh"],
+    "sgemm_3xtf32": ["sgemm_3xtf32.cu", "device_sync.cuh", "tcgen05.cuh"],
+}
+
+
+def source_digest(kernel: str) -> str:
+    """Digest of a kernel's device sources: ties stored ncu counters to the code they measured."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_fp32_gemm_row_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -199,7 +204,7 @@ def stored_traffic(kernel: str, workload: str) -> float | None:
     except (OSError, ValueError):
         return None
     e = table.get(kernel, {}).get(workload)
-    if not e or e.get("source_digest") != source_digest():
+    if not e or e.get("source_digest") != source_digest(kernel):
         return None
     return float(e["dram_bytes_per_launch"])
 
