@@ -155,6 +155,34 @@ int gemm_f32_device_status(int clear);
  */
 int gemm_f32_selftest_watchdog(long long timeout_ns, cudaStream_t stream);
 
+/*
+ * gemm_f32_noalloc -- C = A * B on the CUDA-core FFMA kernel (with split-K
+ * when it helps) without allocating any memory.  The pages have no
+ * counterpart: this entry point exists for callers that cannot let a library
+ * allocate while they run -- programs that reserve their whole device memory
+ * budget up front and hand it out from their own pool, and latency-critical
+ * loops that cannot absorb the device-wide synchronisation of cudaFree.
+ * A, B, C, M, N, K and the result are exactly as for gemm_f32; `splits` is
+ * as for gemm_f32_algo_splitk (0 = choose, limited to what fits).
+ *
+ * Scratch (split-K partial sums, and padded copies of A or B when a row
+ * stride or base address is not 16-byte aligned) comes from one fixed
+ * device array of GEMM_F32_NOALLOC_SCRATCH_BYTES, compiled into the library
+ * and held by every GPU that loads it until the process exits.  A problem
+ * whose padded copies, or whose explicitly requested split partials
+ * (splits x M x roundup(N, 4) floats), do not fit returns
+ * GEMM_F32_ERR_INVALID_VALUE and launches nothing.  The first call on each
+ * device looks up the array's device address and clears its fault word (a
+ * kernel-side watchdog flag at the start of the array); make that first call
+ * before any stream capture begins.  Every call uses the same array, so
+ * calls whose work overlaps on the GPU (other streams, other host threads)
+ * race on it: serialise them.  No cudaMalloc, cudaFree or allocating
+ * library routine is called.
+ */
+#define GEMM_F32_NOALLOC_SCRATCH_BYTES (16u << 20)
+int gemm_f32_noalloc(const float* A, const float* B, float* C, int M, int N, int K,
+                     int splits, cudaStream_t stream);
+
 /* Release every workspace (synchronises each device that has one). */
 int gemm_f32_release(void);
 
