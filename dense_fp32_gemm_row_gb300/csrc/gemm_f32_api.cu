@@ -15,7 +15,7 @@
 #include <mutex>
 #include <utility>
 
-#include "../../include/gemm_f32.h"
+#include "gemm_f32.h"
 #include "gemm_internal.h"
 
 using namespace gemm_f32_impl;
@@ -140,6 +140,7 @@ int workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
 
 struct Plan {
     int algo = 0;
+    int variant = 0;  // FFMA tile variant
     int bn = 0;
     int splits = 1;
     int kb_per_split = 0;
@@ -211,7 +212,10 @@ void make_plan(const DeviceState& d, const float* A, const float* B, int M, int 
         p->stages = tc.stages;
         slots = d.sm_count;
     } else {
-        const FfmaConfig fc = ffma_config();
+        // wide tiles (8 x 16 per thread) once they fill every SM, else 128 x 128
+        const int tiles_wide = ((M + 127) / 128) * ((N + 255) / 256);
+        p->variant = tiles_wide >= d.sm_count ? 1 : 0;
+        const FfmaConfig fc = ffma_config(p->variant);
         bm = fc.bm;
         bn = fc.bn;
         bk = fc.bk;
@@ -369,6 +373,8 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int algo,
         fa.vec_store = vec_store;
         fa.fault = d->fault;
         fa.timeout_ns = kDefaultTimeoutNs;
+        fa.variant = p.variant;
+        fa.bn = p.tile_n;
         if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
             return static_cast<int>(e);
         if ((e = launch_sgemm_ffma(fa, stream)) != cudaSuccess) return static_cast<int>(e);

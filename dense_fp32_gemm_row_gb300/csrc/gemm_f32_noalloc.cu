@@ -30,7 +30,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/gemm_f32.h"
+#include "gemm_f32.h"
 #include "gemm_internal.h"
 
 using namespace gemm_f32_impl;
@@ -145,7 +145,7 @@ extern "C" int gemm_f32_noalloc(const float* A, const float* B, float* C, int M,
     }
 
     // scratch layout after the header: [padded A][padded B][split partials]
-    const FfmaConfig fc = ffma_config();
+    const FfmaConfig fc = ffma_config(0);
     const bool stage_a = (K % 4 != 0) || (reinterpret_cast<uintptr_t>(A) & 15u);
     const bool stage_b = (N % 4 != 0) || (reinterpret_cast<uintptr_t>(B) & 15u);
     const long long lda = stage_a ? up(K, 4) : K;
@@ -211,6 +211,8 @@ extern "C" int gemm_f32_noalloc(const float* A, const float* B, float* C, int M,
     fa.splits = s;
     fa.fault = fault;
     fa.timeout_ns = kDefaultTimeoutNs;
+    fa.variant = 0;
+    fa.bn = fc.bn;
     if (s > 1) {
         fa.out = parts;
         fa.ldo = ldw;

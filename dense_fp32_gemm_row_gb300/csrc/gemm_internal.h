@@ -15,8 +15,9 @@ constexpr long long kDefaultTimeoutNs = 2000000000LL;  // 2 s
 struct FfmaConfig {
     int bm, bn, bk, stages, threads, ctas_per_sm;
     int smem_bytes;  // dynamic shared memory per CTA
+    int variant;     // 0: 128 x 128 tiles, 8 x 8 per thread; 1: 128 x 256, 8 x 16
 };
-FfmaConfig ffma_config();
+FfmaConfig ffma_config(int variant);
 
 struct FfmaArgs {
     CUtensorMap tmA;  // A as {K, M}, box {bk, bm}, swizzled
@@ -30,6 +31,8 @@ struct FfmaArgs {
     int vec_store;          // 1: ldo % 4 == 0 and out 16-byte aligned
     unsigned* fault;
     long long timeout_ns;
+    int variant;            // ffma_config variant
+    int bn;                 // tile width the B descriptor's box was encoded with
 };
 cudaError_t launch_sgemm_ffma(const FfmaArgs& a, cudaStream_t s);
 

@@ -1,6 +1,6 @@
 // sgemm_ffma.cu -- the CUDA-core single-precision GEMM kernel for sm_103a.
 //
-// Computes one 128 x 128 tile of C = A * B (row-major, arbitrary M/N/K) per
+// Computes one 128 x BN tile of C = A * B (row-major, arbitrary M/N/K) per
 // CTA, or one split-K partial of it.  The general-M/N/K tiled kernel of
 // "Lecture 12: final project" (section 2, tiledMatMulKernel: zero-filled
 // out-of-range operand loads, guarded stores, C overwritten) and the
@@ -15,9 +15,9 @@
 //    inner loop carries no bounds checks.
 //  * A STAGES-deep ring of shared-memory stages, each with a "full"
 //    mbarrier (transaction-count completion of the TMA bytes) and an "empty"
-//    mbarrier (one arrival per consumer warp).  The refill of a stage is
-//    issued as soon as every warp has released it, STAGES-1 stages ahead of
-//    the consumer; no __syncthreads in the main loop.
+//    mbarrier (one arrival per consumer warp).  A stage released LAG
+//    iterations ago is refilled STAGES - LAG blocks ahead of the consumer; no
+//    __syncthreads in the main loop.
 //  * A (K-contiguous) lands 128-byte swizzled: row m's 16-byte chunk c sits at
 //    chunk c ^ (m & 7).  Each thread reads 4 consecutive k of one A row with a
 //    single 128-bit shared load; the four rows a warp touches at once have
@@ -25,8 +25,12 @@
 //    "+1 padding" (which TMA cannot produce).
 //  * B (N-contiguous) lands unswizzled; eight lanes read eight consecutive
 //    float4 of one k row, a conflict-free 128-byte wavefront.
-//  * 8 x 8 outputs per thread (rows tm + 4r, columns two float4 groups 32
-//    apart): per 4-deep k step a thread does 256 FFMA for 16 shared loads.
+//  * 8 x 4G outputs per thread (rows tm + 4r, columns G float4 groups 32
+//    apart).  A 128-bit shared load moves 4 floats to each of 32 threads in
+//    four 128-byte wavefronts, so a thread tile of TM x TN costs
+//    (TM + TN) / (TM TN) wavefronts per FFMA instruction: 0.25 for 8 x 8,
+//    which would need the whole 128-byte/clock shared-memory pipe at full
+//    FFMA rate, and 0.1875 for 8 x 16 (G = 4), which leaves a quarter of it.
 //  * Every accumulator sums its products in ascending k, so the result is
 //    run-to-run deterministic; split-K partials are summed in split order by
 //    a separate kernel.
@@ -43,38 +47,65 @@ namespace {
 
 using namespace gemm_f32_dev;
 
+// Packed two-lane fp32 FMA of sm_100-family GPUs: d.x = a.x b.x + d.x and
+// d.y = a.y b.y + d.y, each lane an IEEE fma like fmaf (same bits), one
+// instruction for two multiply-adds.
+__device__ __forceinline__ void ffma2(uint64_t& d, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ uint64_t pack2(float x, float y) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& x, float& y) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
+}
+__device__ __forceinline__ void lds_v2_b64(uint32_t addr, uint64_t& x, uint64_t& y) {
+    asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "r"(addr));
+}
+
 constexpr int BM = 128;
-constexpr int BN = 128;
 constexpr int BK = 32;       // 32 floats = one 128-byte swizzle row of A
-constexpr int STAGES = 3;
 constexpr int THREADS = 256;
 constexpr int WARPS = THREADS / 32;
-constexpr int CTAS_PER_SM = 2;
 constexpr int A_BYTES = BM * BK * 4;
-constexpr int B_BYTES = BK * BN * 4;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 2 * STAGES * 8 + 1024;  // + barriers + align slack
 constexpr int GROUP_M = 8;   // tile rows per raster group (L2 reuse of B panels)
 
-static_assert(BK == 32, "A-tile read addressing assumes the 128-byte swizzle of a 32-float row");
-static_assert(THREADS == 256 && BM == 128 && BN == 128, "warp layout is 4 x 2 warps of 32 x 64");
+// G: float4 column groups per thread (thread tile 8 x 4G, CTA tile 128 x 64G)
+template <int G, int STAGES, int LAG, int MIN_BLOCKS>
+struct FfmaVariant {
+    static constexpr int BN = 64 * G;
+    static constexpr int B_BYTES = BK * BN * 4;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 2 * STAGES * 8 + 1024;
+    static_assert(LAG >= 1 && LAG < STAGES, "refill lag");
+    static_assert(BN <= 256, "TMA box");
+};
 
-__global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
+// ORDER 0: for each A value, all 4G columns (the A register repeats in
+// consecutive FFMAs); ORDER 1: for each B value, all 8 rows (the B register
+// repeats); ORDER 2: as 0 with the accumulators held as column pairs and
+// updated by packed two-lane FMAs (the A value duplicated into both lanes).
+template <int G, int STAGES, int LAG, int MIN_BLOCKS, int ORDER>
+__global__ void __launch_bounds__(THREADS, MIN_BLOCKS)
 sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   float* __restrict__ out, long long ldo, long long split_stride, int M, int N,
                   int K, int kb_per_split, int vec_store, unsigned* fault, long long timeout_ns) {
+    using V = FfmaVariant<G, STAGES, LAG, MIN_BLOCKS>;
+    constexpr int BN = V::BN;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t smem_base = smem_addr(smem);
-    const uint32_t full0 = smem_base + STAGES * STAGE_BYTES;  // full[s]  at full0 + 8 s
-    const uint32_t empty0 = full0 + 8 * STAGES;               // empty[s] at empty0 + 8 s
+    const uint32_t full0 = smem_base + STAGES * V::STAGE_BYTES;  // full[s]  at full0 + 8 s
+    const uint32_t empty0 = full0 + 8 * STAGES;                  // empty[s] at empty0 + 8 s
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int wm = warp >> 1;  // 32-row slab of the tile
-    const int wn = warp & 1;   // 64-column slab of the tile
+    const int wn = warp & 1;   // (BN/2)-column slab of the tile
     const int tm = lane >> 3;  // 0..3
     const int tn = lane & 7;   // 0..7
 
@@ -109,41 +140,45 @@ sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         const int pre = min(STAGES, nkb);
         for (; issued < pre; ++issued) {
             const int s = issued % STAGES;
-            const uint32_t dst = smem_base + s * STAGE_BYTES;
+            const uint32_t dst = smem_base + s * V::STAGE_BYTES;
             const int k0 = (kb_begin + issued) * BK;
-            mbar_arrive_expect_tx(full0 + 8 * s, STAGE_BYTES);
+            mbar_arrive_expect_tx(full0 + 8 * s, V::STAGE_BYTES);
             tma_load_2d(dst, &tmA, full0 + 8 * s, k0, m0);
             tma_load_2d(dst + A_BYTES, &tmB, full0 + 8 * s, n0, k0);
         }
     }
 
-    float acc[8][8];
+    float acc[8][4 * G];
+    uint64_t acc2[8][2 * G];  // ORDER 2: column pairs (j, j+1)
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
+    for (int r = 0; r < 8; ++r) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[r][j] = 0.0f;
+        for (int j = 0; j < 4 * G; ++j) acc[r][j] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 2 * G; ++j) acc2[r][j] = 0ull;
+    }
 
     const float* smemf = reinterpret_cast<const float*>(smem);
-    const int a_off = (wm * 32 + tm) * BK;  // row wm*32+tm; row r of the thread is +4r
-    const int b_off = wn * 64 + tn * 4;     // first column group; second is +32
+    const int a_off = (wm * 32 + tm) * BK;      // row wm*32+tm; row r of the thread is +4r
+    const int b_off = wn * (BN / 2) + tn * 4;   // first column group; group g is +32 g
 
     bool ok = true;
     int kb = 0;
     for (; kb < nkb; ++kb) {
         const int s = kb % STAGES;
         bool prod_ok = true;
-        // refill the stage released in the previous iteration, STAGES-1 ahead
-        if (tid == 0 && kb >= 1) {
-            const int done = kb - 1;
+        // refill the stage released LAG iterations ago, STAGES - LAG blocks ahead
+        if (tid == 0 && kb >= LAG) {
+            const int done = kb - LAG;
             const int next = done + STAGES;
             if (next < nkb) {
                 const int sd = done % STAGES;
                 prod_ok = mbar_wait(empty0 + 8 * sd, (done / STAGES) & 1, timeout_ns, fault,
                                     kFaultEmptyBarrier);
                 if (prod_ok) {
-                    const uint32_t dst = smem_base + sd * STAGE_BYTES;
+                    const uint32_t dst = smem_base + sd * V::STAGE_BYTES;
                     const int k0 = (kb_begin + next) * BK;
-                    mbar_arrive_expect_tx(full0 + 8 * sd, STAGE_BYTES);
+                    mbar_arrive_expect_tx(full0 + 8 * sd, V::STAGE_BYTES);
                     tma_load_2d(dst, &tmA, full0 + 8 * sd, k0, m0);
                     tma_load_2d(dst + A_BYTES, &tmB, full0 + 8 * sd, n0, k0);
                     issued = next + 1;
@@ -157,34 +192,65 @@ sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             break;
         }
 
-        const float* As = smemf + s * (STAGE_BYTES / 4);
+        const float* As = smemf + s * (V::STAGE_BYTES / 4);
         const float* Bs = As + A_BYTES / 4;
 #pragma unroll
         for (int c = 0; c < BK / 4; ++c) {
-            float4 b0[4], b1[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                b0[q] = *reinterpret_cast<const float4*>(Bs + (c * 4 + q) * BN + b_off);
-                b1[q] = *reinterpret_cast<const float4*>(Bs + (c * 4 + q) * BN + b_off + 32);
-            }
             // rows with even r have (m & 7) == tm, odd r have tm + 4
             const int xe = (c ^ tm) << 2;
             const int xo = (c ^ (tm + 4)) << 2;
+            float4 a[8];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const float4 a = *reinterpret_cast<const float4*>(As + a_off + r * 4 * BK +
-                                                                  ((r & 1) ? xo : xe));
-                const float av[4] = {a.x, a.y, a.z, a.w};
+            for (int r = 0; r < 8; ++r)
+                a[r] = *reinterpret_cast<const float4*>(As + a_off + r * 4 * BK +
+                                                        ((r & 1) ? xo : xe));
+            if constexpr (ORDER == 2) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    acc[r][0] = fmaf(av[q], b0[q].x, acc[r][0]);
-                    acc[r][1] = fmaf(av[q], b0[q].y, acc[r][1]);
-                    acc[r][2] = fmaf(av[q], b0[q].z, acc[r][2]);
-                    acc[r][3] = fmaf(av[q], b0[q].w, acc[r][3]);
-                    acc[r][4] = fmaf(av[q], b1[q].x, acc[r][4]);
-                    acc[r][5] = fmaf(av[q], b1[q].y, acc[r][5]);
-                    acc[r][6] = fmaf(av[q], b1[q].z, acc[r][6]);
-                    acc[r][7] = fmaf(av[q], b1[q].w, acc[r][7]);
+                    uint64_t bp[2 * G];
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+                        lds_v2_b64(smem_addr(Bs + (c * 4 + q) * BN + b_off + 32 * g), bp[2 * g],
+                                   bp[2 * g + 1]);
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const float av = q == 0 ? a[r].x : q == 1 ? a[r].y : q == 2 ? a[r].z : a[r].w;
+                        const uint64_t ad = pack2(av, av);
+#pragma unroll
+                        for (int p = 0; p < 2 * G; ++p) ffma2(acc2[r][p], ad, bp[p]);
+                    }
+                }
+                continue;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float4 b[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    b[g] = *reinterpret_cast<const float4*>(Bs + (c * 4 + q) * BN + b_off + 32 * g);
+                if constexpr (ORDER == 0) {
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const float av = q == 0 ? a[r].x : q == 1 ? a[r].y : q == 2 ? a[r].z : a[r].w;
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            acc[r][4 * g + 0] = fmaf(av, b[g].x, acc[r][4 * g + 0]);
+                            acc[r][4 * g + 1] = fmaf(av, b[g].y, acc[r][4 * g + 1]);
+                            acc[r][4 * g + 2] = fmaf(av, b[g].z, acc[r][4 * g + 2]);
+                            acc[r][4 * g + 3] = fmaf(av, b[g].w, acc[r][4 * g + 3]);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4 * G; ++j) {
+                        const float4 bg = b[j >> 2];
+                        const float bv = (j & 3) == 0 ? bg.x : (j & 3) == 1 ? bg.y : (j & 3) == 2 ? bg.z : bg.w;
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) {
+                            const float av = q == 0 ? a[r].x : q == 1 ? a[r].y : q == 2 ? a[r].z : a[r].w;
+                            acc[r][j] = fmaf(av, bv, acc[r][j]);
+                        }
+                    }
                 }
             }
         }
@@ -202,6 +268,12 @@ sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         return;
     }
 
+    if constexpr (ORDER == 2) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int p = 0; p < 2 * G; ++p) unpack2(acc2[r][p], acc[r][2 * p], acc[r][2 * p + 1]);
+    }
     float* outp = out + static_cast<long long>(blockIdx.y) * split_stride;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
@@ -209,7 +281,7 @@ sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         if (m >= M) continue;
         float* row = outp + static_cast<long long>(m) * ldo;
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
+        for (int g = 0; g < G; ++g) {
             const int n = n0 + b_off + 32 * g;
             const float* v = &acc[r][4 * g];
             if (vec_store && n + 3 < N) {
@@ -223,27 +295,44 @@ sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
 }
 
-}  // namespace
+// the two variants the planner chooses between
+using Narrow = FfmaVariant<2, 3, 1, 2>;  // 128 x 128 tiles, 2 CTAs / SM
+using Wide = FfmaVariant<4, 4, 2, 1>;    // 128 x 256 tiles, 1 CTA / SM
 
-FfmaConfig ffma_config() { return {BM, BN, BK, STAGES, THREADS, CTAS_PER_SM, SMEM_BYTES}; }
-
-cudaError_t launch_sgemm_ffma(const FfmaArgs& a, cudaStream_t s) {
+template <int G, int STAGES, int LAG, int MIN_BLOCKS, int ORDER>
+cudaError_t launch_variant(const FfmaArgs& a, cudaStream_t s) {
+    using V = FfmaVariant<G, STAGES, LAG, MIN_BLOCKS>;
+    auto kern = sgemm_ffma_kernel<G, STAGES, LAG, MIN_BLOCKS, ORDER>;
+    // the kernel's stage layout and transaction count assume this box width
+    if (a.bn != V::BN) return cudaErrorInvalidValue;
     static thread_local int attr_done_dev = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (attr_done_dev != dev) {
-        e = cudaFuncSetAttribute(sgemm_ffma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, V::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_done_dev = dev;
     }
-    const int tiles = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
+    const int tiles = ((a.M + BM - 1) / BM) * ((a.N + V::BN - 1) / V::BN);
     dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(a.splits));
-    sgemm_ffma_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(a.tmA, a.tmB, a.out, a.ldo, a.split_stride,
-                                                         a.M, a.N, a.K, a.kb_per_split,
-                                                         a.vec_store, a.fault, a.timeout_ns);
+    kern<<<grid, THREADS, V::SMEM_BYTES, s>>>(a.tmA, a.tmB, a.out, a.ldo, a.split_stride, a.M, a.N,
+                                              a.K, a.kb_per_split, a.vec_store, a.fault,
+                                              a.timeout_ns);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+FfmaConfig ffma_config(int variant) {
+    if (variant == 1)
+        return {BM, Wide::BN, BK, 4, THREADS, 1, Wide::SMEM_BYTES, 1};
+    return {BM, Narrow::BN, BK, 3, THREADS, 2, Narrow::SMEM_BYTES, 0};
+}
+
+cudaError_t launch_sgemm_ffma(const FfmaArgs& a, cudaStream_t s) {
+    if (a.variant == 1) return launch_variant<4, 4, 2, 1, 2>(a, s);
+    return launch_variant<2, 3, 1, 2, 2>(a, s);
 }
 
 }  // namespace gemm_f32_impl

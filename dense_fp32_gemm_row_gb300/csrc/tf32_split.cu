@@ -44,6 +44,30 @@ split_rows_kernel(const float* __restrict__ src, long long lds, long long rows, 
     }
 }
 
+// Vector form: 4 consecutive elements per thread (cols, lds, ldd multiples of
+// 4 and both bases 16-byte aligned); one block covers 1024 columns of a row.
+__global__ void __launch_bounds__(kThreads)
+split_rows4_kernel(const float4* __restrict__ src, long long lds4, long long rows, long long cols4,
+                   float4* __restrict__ hi, float4* __restrict__ lo, long long ldd4) {
+    for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
+        for (long long c = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; c < cols4;
+             c += static_cast<long long>(gridDim.x) * kThreads) {
+            const float4 x = src[r * lds4 + c];
+            float4 h, l;
+            h.x = to_tf32(x.x);
+            h.y = to_tf32(x.y);
+            h.z = to_tf32(x.z);
+            h.w = to_tf32(x.w);
+            l.x = to_tf32(x.x - h.x);
+            l.y = to_tf32(x.y - h.y);
+            l.z = to_tf32(x.z - h.z);
+            l.w = to_tf32(x.w - h.w);
+            hi[r * ldd4 + c] = h;
+            lo[r * ldd4 + c] = l;
+        }
+    }
+}
+
 // 32 x 32 tiles through shared memory (row pitch 33 floats: the transposed
 // read of a column hits 32 different banks).  src is K x N with row stride
 // lds; hi/lo are N x K with row stride ldt.
@@ -84,10 +108,22 @@ split_transpose_kernel(const float* __restrict__ src, long long lds, int K, int 
 cudaError_t launch_split_rows(const float* src, long long lds, long long rows, long long cols,
                               float* hi, float* lo, long long ldd, cudaStream_t s) {
     if (rows <= 0 || cols <= 0) return cudaSuccess;
-    long long gx = (cols + kThreads - 1) / kThreads;
-    if (gx > 64) gx = 64;
-    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(rows < 65535 ? rows : 65535));
-    split_rows_kernel<<<grid, kThreads, 0, s>>>(src, lds, rows, cols, hi, lo, ldd);
+    const unsigned gy = static_cast<unsigned>(rows < 65535 ? rows : 65535);
+    const bool vec = (cols % 4 == 0) && (lds % 4 == 0) && (ldd % 4 == 0) &&
+                     ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(hi) |
+                       reinterpret_cast<uintptr_t>(lo)) % 16 == 0);
+    if (vec) {
+        long long gx = (cols / 4 + kThreads - 1) / kThreads;
+        if (gx > 64) gx = 64;
+        split_rows4_kernel<<<dim3(static_cast<unsigned>(gx), gy), kThreads, 0, s>>>(
+            reinterpret_cast<const float4*>(src), lds / 4, rows, cols / 4,
+            reinterpret_cast<float4*>(hi), reinterpret_cast<float4*>(lo), ldd / 4);
+    } else {
+        long long gx = (cols + kThreads - 1) / kThreads;
+        if (gx > 64) gx = 64;
+        split_rows_kernel<<<dim3(static_cast<unsigned>(gx), gy), kThreads, 0, s>>>(
+            src, lds, rows, cols, hi, lo, ldd);
+    }
     return cudaGetLastError();
 }
 
