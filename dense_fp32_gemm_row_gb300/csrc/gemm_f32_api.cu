@@ -142,6 +142,8 @@ struct Plan {
     int algo = 0;
     int variant = 0;  // FFMA tile variant
     int bn = 0;
+    int pair = 0;     // 3xTF32: two-CTA kernel
+    int box_n = 0;    // 3xTF32: B^T rows per TMA box
     int splits = 1;
     int kb_per_split = 0;
     int stage_a = 0, stage_b = 0;
@@ -201,16 +203,20 @@ void make_plan(const DeviceState& d, const float* A, const float* B, int M, int 
     p->algo = (algo == GEMM_F32_ALGO_AUTO) ? GEMM_F32_ALGO_3XTF32 : algo;
     int bm, bn, bk, slots;
     if (p->algo == GEMM_F32_ALGO_3XTF32) {
-        // wide tiles unless they leave most SMs idle
+        // the two-CTA 256 x 256 kernel when its tiles fill every SM pair;
+        // otherwise one CTA per 128 x 256 tile, or 128 x 128 for narrow or
+        // small outputs
+        const int units_pair = ((M + 255) / 256) * ((N + 255) / 256);
         const int tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
-        p->bn = (tiles256 >= d.sm_count || N <= 128) ? 256 : 128;
-        if (N <= 128) p->bn = 128;
-        const Tf32x3Config tc = tf32x3_config(p->bn);
+        p->pair = units_pair >= d.sm_count / 2 ? 1 : 0;
+        p->bn = (p->pair || (tiles256 >= d.sm_count && N > 128)) ? 256 : 128;
+        const Tf32x3Config tc = tf32x3_config(p->bn, p->pair != 0);
         bm = tc.bm;
         bn = tc.bn;
         bk = tc.bk;
         p->stages = tc.stages;
-        slots = d.sm_count;
+        p->box_n = tc.box_n;
+        slots = p->pair ? d.sm_count / 2 : d.sm_count;
     } else {
         // wide tiles (8 x 16 per thread) once they fill every SM, else 128 x 128
         const int tiles_wide = ((M + 127) / 128) * ((N + 255) / 256);
@@ -245,7 +251,8 @@ void make_plan(const DeviceState& d, const float* A, const float* B, int M, int 
         p->off_a2 = carve(&off, static_cast<long long>(M) * p->lda * 4);
         p->off_b = carve(&off, static_cast<long long>(N) * p->ldb * 4);
         p->off_b2 = carve(&off, static_cast<long long>(N) * p->ldb * 4);
-        p->ctas = units < d.sm_count ? units : d.sm_count;
+        p->ctas = units < slots ? units : slots;
+        if (p->pair) p->ctas *= 2;
     } else {
         p->stage_a = (K % 4 != 0) || misaligned16(A);
         p->stage_b = (N % 4 != 0) || misaligned16(B);
@@ -313,13 +320,14 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int algo,
             return static_cast<int>(e);
         Tf32x3Args ta;
         std::memset(&ta, 0, sizeof(ta));
-        if ((st = encode_2d(&ta.tmAhi, a_hi, K, M, p.lda, p.tile_k, p.tile_m,
+        // one CTA loads 128 rows of A and box_n rows of B^T per stage
+        if ((st = encode_2d(&ta.tmAhi, a_hi, K, M, p.lda, p.tile_k, 128,
                             CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
-            (st = encode_2d(&ta.tmAlo, a_lo, K, M, p.lda, p.tile_k, p.tile_m,
+            (st = encode_2d(&ta.tmAlo, a_lo, K, M, p.lda, p.tile_k, 128,
                             CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
-            (st = encode_2d(&ta.tmBhi, b_hi, K, N, p.ldb, p.tile_k, p.tile_n,
+            (st = encode_2d(&ta.tmBhi, b_hi, K, N, p.ldb, p.tile_k, p.box_n,
                             CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
-            (st = encode_2d(&ta.tmBlo, b_lo, K, N, p.ldb, p.tile_k, p.tile_n,
+            (st = encode_2d(&ta.tmBlo, b_lo, K, N, p.ldb, p.tile_k, p.box_n,
                             CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS)
             return st;
         ta.out = out;
@@ -329,6 +337,7 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int algo,
         ta.N = N;
         ta.K = K;
         ta.bn = p.bn;
+        ta.pair = p.pair;
         ta.kb_per_split = p.kb_per_split;
         ta.splits = p.splits;
         ta.vec_store = vec_store;

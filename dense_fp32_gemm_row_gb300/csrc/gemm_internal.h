@@ -38,10 +38,13 @@ cudaError_t launch_sgemm_ffma(const FfmaArgs& a, cudaStream_t s);
 
 // ---- sgemm_3xtf32 (tcgen05 tensor-core kernel) -----------------------------
 struct Tf32x3Config {
-    int bm, bn, bk, stages, threads;
+    int bm, bn, bk, stages, threads;  // bm x bn: output tile of one work unit
     int smem_bytes;
+    int pair;    // 1: a two-CTA cluster shares each MMA (M = 256)
+    int box_n;   // rows of B^T one CTA loads per stage (TMA box height)
 };
-Tf32x3Config tf32x3_config(int bn);  // bn = 128 or 256
+// bn = 128 or 256 for one CTA per tile; pair = the 256 x 256 two-CTA kernel
+Tf32x3Config tf32x3_config(int bn, bool pair);
 
 struct Tf32x3Args {
     CUtensorMap tmAhi, tmAlo;  // A hi / lo as {K, M}, box {bk, bm}, 128-byte swizzle
@@ -51,13 +54,15 @@ struct Tf32x3Args {
     long long split_stride;
     int M, N, K;
     int bn;
+    int pair;
     int kb_per_split;
     int splits;
     int vec_store;
     unsigned* fault;
     long long timeout_ns;
 };
-// persistent grid of min(units, sm_count) CTAs
+// persistent grid: min(units, sm_count) CTAs, or for the pair kernel
+// 2 x min(units, co-resident clusters)
 cudaError_t launch_sgemm_3xtf32(const Tf32x3Args& a, cudaStream_t s, int sm_count);
 
 // ---- TF32 hi/lo staging (tf32_split.cu) --------------------------------------

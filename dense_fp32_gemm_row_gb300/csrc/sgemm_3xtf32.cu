@@ -75,7 +75,7 @@ struct Unit {
 };
 
 __device__ __forceinline__ Unit decode(int u, int tiles_m, int tiles_n, int kb_per_split,
-                                       int kb_total, int bn) {
+                                       int kb_total, int bn, int bm = BM) {
     const int tiles = tiles_m * tiles_n;
     Unit w;
     w.split = u / tiles;
@@ -85,7 +85,7 @@ __device__ __forceinline__ Unit decode(int u, int tiles_m, int tiles_n, int kb_p
     const int first_m = group * GROUP_M;
     const int rows_in_group = min(tiles_m - first_m, GROUP_M);
     const int within = t - group * per_group;
-    w.m0 = (first_m + within % rows_in_group) * BM;
+    w.m0 = (first_m + within % rows_in_group) * bm;
     w.n0 = (within / rows_in_group) * bn;
     w.kb_begin = w.split * kb_per_split;
     w.nkb = max(0, min(kb_total, w.kb_begin + kb_per_split) - w.kb_begin);
@@ -355,14 +355,300 @@ cudaError_t launch_impl(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
     return cudaGetLastError();
 }
 
+
+// ============================================================================
+// CTA-pair variant: a cluster of two CTAs on two SMs computes a 256 x 256
+// tile with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 8).  CTA rank r
+// loads rows m0 + 128 r of Ahi/Alo and rows n0 + 128 r of B^T hi/lo into its
+// own shared memory, so every SM reads 8 KB of operands per MMA instead of
+// the 12 KB of the single-CTA 128 x 256 MMA; that is what lets the tensor
+// pipe outrun shared-memory bandwidth.  Each CTA's tensor memory holds its
+// 128 rows x 256 columns; its epilogue warps promote and store them.
+//   * both producers arrive (with their own transaction bytes) on the
+//     leader's full barrier and point their TMA completions at it;
+//   * the leader's MMA lane issues the pair MMAs and multicasts each commit
+//     to the same barrier offset in both CTAs (stage free / chunk ready);
+//   * both epilogues release a chunk buffer by arriving on the leader's
+//     acc_empty barrier.
+// ============================================================================
+template <int STAGES>
+struct PairCfg {
+    static constexpr int BN = 256;       // MMA N, shared by the pair
+    static constexpr int HALF_N = 128;   // B^T rows held by each CTA
+    static constexpr int A_BYTES = BM * BK * 4;
+    static constexpr int B_BYTES = HALF_N * BK * 4;
+    static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int EPI_WARPS = BN / EPI_COLS * 4;
+    static constexpr int THREADS = 128 + 32 * EPI_WARPS;
+    static constexpr int NBARS = 2 * STAGES + 5;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NBARS * 8 + 16 + 1024;
+    static constexpr uint32_t IDESC = idesc_tf32_f32(2 * BM, BN);
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
+
+template <int STAGES>
+__global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
+sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
+                         const __grid_constant__ CUtensorMap tmAlo,
+                         const __grid_constant__ CUtensorMap tmBhi,
+                         const __grid_constant__ CUtensorMap tmBlo, float* __restrict__ out,
+                         long long ldo, long long split_stride, int M, int N, int K,
+                         int kb_per_split, int splits, int vec_store, unsigned* fault,
+                         long long timeout_ns) {
+    using C = PairCfg<STAGES>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t bar0 = sbase + STAGES * C::STAGE_BYTES;
+    const uint32_t full0 = bar0;                  // full[s]: used in the leader, count 2
+    const uint32_t empty0 = bar0 + 8 * STAGES;    // empty[s]: both CTAs, one multicast commit
+    const uint32_t accf0 = bar0 + 16 * STAGES;    // acc_full[b]: both CTAs, one multicast commit
+    const uint32_t acce0 = accf0 + 16;            // acc_empty[b]: leader, both epilogues
+    const uint32_t drain = acce0 + 16;
+    uint32_t* tmem_slot =
+        reinterpret_cast<uint32_t*>(smem + STAGES * C::STAGE_BYTES + C::NBARS * 8);
+    const uint32_t abort_flag = smem_addr(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int cluster = blockIdx.x >> 1;
+    const int nclusters = gridDim.x >> 1;
+    const int tiles_m = (M + 2 * BM - 1) / (2 * BM);
+    const int tiles_n = (N + C::BN - 1) / C::BN;
+    const int units = tiles_m * tiles_n * splits;
+    const int kb_total = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmAhi);
+        prefetch_tmap(&tmAlo);
+        prefetch_tmap(&tmBhi);
+        prefetch_tmap(&tmBlo);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 2);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf0 + 8 * b, 1);
+            mbar_init(acce0 + 8 * b, 2 * C::EPI_WARPS);
+        }
+        mbar_init(drain, 1);
+        st_shared_volatile(abort_flag, 0u);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_addr(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------ TMA producer (both CTAs) ------------------
+            int it = 0;
+            bool ok = true;
+            for (int u = cluster; u < units && ok; u += nclusters) {
+                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, 2 * BM);
+                const int ma = w.m0 + static_cast<int>(rank) * BM;
+                const int nb = w.n0 + static_cast<int>(rank) * C::HALF_N;
+                for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    if (it >= STAGES &&
+                        !role_wait(empty0 + 8 * s, ((it / STAGES) & 1) ^ 1, timeout_ns, fault,
+                                   kFaultEmptyBarrier, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = sbase + s * C::STAGE_BYTES;
+                    const uint32_t fb = map_to_cta(full0 + 8 * s, 0);
+                    const int k0 = (w.kb_begin + kb) * BK;
+                    mbar_arrive_expect_tx_cluster(fb, C::STAGE_BYTES);
+                    tma_load_2d_pair(st, &tmAhi, fb, k0, ma);
+                    tma_load_2d_pair(st + C::A_BYTES, &tmAlo, fb, k0, ma);
+                    tma_load_2d_pair(st + 2 * C::A_BYTES, &tmBhi, fb, k0, nb);
+                    tma_load_2d_pair(st + 2 * C::A_BYTES + C::B_BYTES, &tmBlo, fb, k0, nb);
+                }
+            }
+            // wind down: every stage this CTA filled has been consumed and released
+            const long long tail = ok ? timeout_ns : timeout_ns / 8 + 1000;
+            for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+                mbar_wait(empty0 + 8 * (j % STAGES), (j / STAGES) & 1, tail, fault, kFaultDrain);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // ------------------------------ MMA issuer (leader CTA) ------------------
+            int it = 0;
+            int g = 0;
+            bool ok = true;
+            for (int u = cluster; u < units && ok; u += nclusters) {
+                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, 2 * BM);
+                for (int c0 = 0; c0 < w.nkb && ok; c0 += CH, ++g) {
+                    const int buf = g & 1;
+                    if (g >= 2 && !role_wait(acce0 + 8 * buf, ((g >> 1) & 1) ^ 1, timeout_ns, fault,
+                                             kFaultAccumBarrier, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(buf * C::BN);
+                    const int c1 = min(w.nkb, c0 + CH);
+                    for (int kb = c0; kb < c1; ++kb, ++it) {
+                        const int s = it % STAGES;
+                        if (!role_wait(full0 + 8 * s, (it / STAGES) & 1, timeout_ns, fault,
+                                       kFaultFullBarrier, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t st = sbase + s * C::STAGE_BYTES;
+                        const uint64_t a_hi = smem_desc_sw128_kmajor(st);
+                        const uint64_t a_lo = smem_desc_sw128_kmajor(st + C::A_BYTES);
+                        const uint64_t b_hi = smem_desc_sw128_kmajor(st + 2 * C::A_BYTES);
+                        const uint64_t b_lo =
+                            smem_desc_sw128_kmajor(st + 2 * C::A_BYTES + C::B_BYTES);
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k) {
+                            const uint64_t off = static_cast<uint64_t>(k * UMMA_K * 4) >> 4;
+                            const uint32_t acc = (kb > c0 || k > 0) ? 1u : 0u;
+                            mma_tf32_pair(d, a_lo + off, b_hi + off, C::IDESC, acc);
+                            mma_tf32_pair(d, a_hi + off, b_lo + off, C::IDESC, 1u);
+                            mma_tf32_pair(d, a_hi + off, b_hi + off, C::IDESC, 1u);
+                        }
+                        mma_commit_pair_multicast(empty0 + 8 * s, 0x3);
+                    }
+                    if (!ok) break;
+                    mma_commit_pair_multicast(accf0 + 8 * buf, 0x3);
+                }
+            }
+            mma_commit_pair(drain);
+            mbar_wait(drain, 0, ok ? timeout_ns : timeout_ns / 8 + 1000, fault, kFaultDrain);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------ epilogue (both CTAs) ----------------------
+        const int e = warp - 4;
+        const int q = warp & 3;
+        const int col0 = (e >> 2) * EPI_COLS;
+        const int row = 32 * q + lane;
+        float acc[EPI_COLS];
+        int g = 0;
+        bool ok = true;
+        for (int u = cluster; u < units && ok; u += nclusters) {
+            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, 2 * BM);
+            for (int c0 = 0; c0 < w.nkb; c0 += CH, ++g) {
+                const int buf = g & 1;
+                const bool got = role_wait(accf0 + 8 * buf, (g >> 1) & 1, timeout_ns, fault,
+                                           kFaultAccumBarrier, abort_flag);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                                       static_cast<uint32_t>(buf * C::BN + col0);
+#pragma unroll
+                for (int j = 0; j < EPI_COLS / 16; ++j) {
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(tbase + 16 * j, r);
+                    tmem_ld_wait(r);
+                    if (c0 == 0) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[16 * j + i] = __uint_as_float(r[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[16 * j + i] += __uint_as_float(r[i]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(map_to_cta(acce0 + 8 * buf, 0));
+            }
+            if (!ok) break;
+            const int m = w.m0 + static_cast<int>(rank) * BM + row;
+            if (m < M) {
+                float* orow = out + static_cast<long long>(w.split) * split_stride +
+                              static_cast<long long>(m) * ldo;
+                const int nb = w.n0 + col0;
+                if (vec_store && nb + EPI_COLS <= N) {
+#pragma unroll
+                    for (int j = 0; j < EPI_COLS; j += 4)
+                        *reinterpret_cast<float4*>(orow + nb + j) =
+                            make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < EPI_COLS; ++j)
+                        if (nb + j < N) orow[nb + j] = acc[j];
+                }
+            }
+        }
+    }
+
+    // neither CTA may leave while its partner can still reach its shared memory
+    tc_fence_before();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    }
+}
+
+template <int STAGES>
+cudaError_t launch_pair(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
+    using C = PairCfg<STAGES>;
+    auto kern = sgemm_3xtf32_pair_kernel<STAGES>;
+    static thread_local int attr_done_dev = -1;
+    static thread_local int max_clusters = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (attr_done_dev != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        cfg.gridDim = dim3(2 * (sm_count / 2));
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        max_clusters = n;
+        attr_done_dev = dev;
+    }
+    const int units = ((a.M + 2 * BM - 1) / (2 * BM)) * ((a.N + C::BN - 1) / C::BN) * a.splits;
+    const int clusters = units < max_clusters ? units : max_clusters;
+    cfg.gridDim = dim3(2 * clusters);
+    e = cudaLaunchKernelEx(&cfg, kern, a.tmAhi, a.tmAlo, a.tmBhi, a.tmBlo, a.out, a.ldo,
+                           a.split_stride, a.M, a.N, a.K, a.kb_per_split, a.splits, a.vec_store,
+                           a.fault, a.timeout_ns);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 }  // namespace
 
-Tf32x3Config tf32x3_config(int bn) {
-    if (bn == 128) return {BM, 128, BK, 3, Cfg<128, 3>::THREADS, Cfg<128, 3>::SMEM_BYTES};
-    return {BM, 256, BK, 2, Cfg<256, 2>::THREADS, Cfg<256, 2>::SMEM_BYTES};
+Tf32x3Config tf32x3_config(int bn, bool pair) {
+    if (pair) return {2 * BM, 256, BK, 3, PairCfg<3>::THREADS, PairCfg<3>::SMEM_BYTES, 1, 128};
+    if (bn == 128) return {BM, 128, BK, 3, Cfg<128, 3>::THREADS, Cfg<128, 3>::SMEM_BYTES, 0, 128};
+    return {BM, 256, BK, 2, Cfg<256, 2>::THREADS, Cfg<256, 2>::SMEM_BYTES, 0, 256};
 }
 
 cudaError_t launch_sgemm_3xtf32(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
+    if (a.pair) return launch_pair<3>(a, s, sm_count);
     if (a.bn == 128) return launch_impl<128, 3>(a, s, sm_count);
     return launch_impl<256, 2>(a, s, sm_count);
 }

@@ -91,6 +91,35 @@ def test_edge_shapes(shape, algo):
     _check(_gpu.run(A, B, algo), oracle.ref_gemm(A, B), label=f"{shape}/{algo}")
 
 
+# shapes whose 256 x 256 tiles fill every SM pair: these run the two-CTA
+# tensor-core kernel (ragged in M, N and K, and one with split-K)
+PAIR_SHAPES = [(2304, 2304, 512), (2305, 2049, 1000), (2560, 2330, 77), (4096, 2048, 3000)]
+
+
+@pytest.mark.parametrize("shape", PAIR_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_pair_kernel_shapes(shape):
+    M, N, K = shape
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_3XTF32, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["tile_m"] == 256 and p["tile_n"] == 256, p
+    A, B = make_workload(2, M=M, N=N, K=K)
+    C = _gpu.run(A, B, g.ALGO_3XTF32)
+    rng = np.random.default_rng(M + N + K)
+    rows = np.concatenate([np.arange(M), rng.integers(0, M, 3000), np.full(N, M - 1)])
+    cols = np.concatenate([rng.integers(0, N, M), rng.integers(0, N, 3000), np.arange(N)])
+    _check(C[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols), label=f"pair {shape}")
+
+
+def test_pair_kernel_split_k_deterministic():
+    M, N, K = 2304, 2304, 4096
+    A, B = make_workload(4, M=M, N=N, K=K)
+    C1 = _gpu.run(A, B, g.ALGO_3XTF32, 3)
+    C2 = _gpu.run(A, B, g.ALGO_3XTF32, 3)
+    assert np.array_equal(C1.view(np.uint32), C2.view(np.uint32))
+    rng = np.random.default_rng(7)
+    rows, cols = rng.integers(0, M, 4000), rng.integers(0, N, 4000)
+    _check(C1[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols), label="pair split 3")
+
+
 @pytest.mark.parametrize("algo", [g.ALGO_FFMA, g.ALGO_3XTF32], ids=["ffma", "3xtf32"])
 @pytest.mark.parametrize("offsets", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (3, 2, 1)])
 def test_misaligned_pointers(offsets, algo):
