@@ -213,22 +213,56 @@ def stored_traffic(kernel: str, workload: str) -> float | None:
 # CPU oracle timing (the baseline arm)
 # ---------------------------------------------------------------------------
 def oracle_rows_timing(A, B, seconds: float) -> dict:
-    """Time the oracle on the first R rows of C, R sized to take ~`seconds`."""
+    """Time the oracle on the first R rows of C, R sized to take ~`seconds`.
+
+    A warm-up pass on a few rows (page-in, thread start) is followed by a
+    calibration pass; R is a multiple of the oracle's thread count so that
+    every thread gets the same number of rows.
+    """
     import oracle
 
     M, K = A.shape
     N = B.shape[1]
-    r0 = max(1, min(M, 2))
+    threads = max(1, oracle.max_threads())
+    oracle.ref_gemm_rows(A, B, 0, min(M, threads))  # warm-up
+    cal = min(M, 2 * threads)
     t0 = time.perf_counter()
-    oracle.ref_gemm_rows(A, B, 0, r0)
-    dt0 = max(time.perf_counter() - t0, 1e-6)
-    rows = int(max(1, min(M, r0 * seconds / dt0)))
+    oracle.ref_gemm_rows(A, B, 0, cal)
+    per_row = max(time.perf_counter() - t0, 1e-6) / cal
+    rows = int(seconds / per_row) // threads * threads
+    rows = int(max(threads, min(M, rows)))
+    rows = min(rows, M)
     t0 = time.perf_counter()
     oracle.ref_gemm_rows(A, B, 0, rows)
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * N * K
     return {"rows": rows, "seconds": dt, "flops": flops, "tflops": flops / dt / 1e12,
-            "cores": oracle.max_threads()}
+            "cores": threads}
+
+
+def cublas_context(a, b, steps: int = 10) -> float | None:
+    """cuBLAS SGEMM (torch.matmul, TF32 off) on the same device tensors: context only."""
+    import torch
+
+    prev = torch.backends.cuda.matmul.allow_tf32
+    try:
+        torch.backends.cuda.matmul.allow_tf32 = False
+        for _ in range(3):
+            c = a @ b
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            c = a @ b
+        e1.record()
+        torch.cuda.synchronize()
+        del c
+        ms = e0.elapsed_time(e1) / steps
+        return 2.0 * a.shape[0] * a.shape[1] * b.shape[1] / (ms * 1e-3) / 1e12
+    except Exception:
+        return None
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
 
 
 def run_reference(args, world, rank):
@@ -396,6 +430,11 @@ def run_ours(args, world, rank, local):
     if not np.isfinite(hC[0, :8].numpy()).all():
         raise SystemExit("non-finite output")
 
+    context = None
+    if not args.no_context:
+        context = {"cublas_sgemm_tflops": cublas_context(a, b),
+                   "note": "torch.matmul fp32 with TF32 disabled, same inputs, not linked"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = oracle_rows_timing(A_np, B_np, args.cpu_seconds)
@@ -423,8 +462,9 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": input_bytes,
                 "d2h_bytes_per_step": 4 * M * N, "steps": e2e_steps},
-        "gpu_launches": K_steps * plan["kernels"] + (0 if flush is None else 0),
+        "gpu_launches": K_steps * plan["kernels"],
         "clocks": clocks,
+        "context": context,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -447,6 +487,7 @@ def main(argv=None) -> int:
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-context", action="store_true", help="skip the cuBLAS context timing")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
