@@ -407,22 +407,26 @@ def run_ours(args, world, rank, local):
                 "frac": achieved / peak, "traffic": stored_traffic(kname, w.name),
                 "kernel": kname, "peak_source": peak_src}
 
-    # end to end through the public entry point with pinned host buffers
+    # end to end through the public host-buffer entry point (pinned host
+    # memory): every step copies A and B in and C out inside the call
     e2e_steps = max(1, min(args.e2e_steps, K_steps))
     hA = torch.from_numpy(A_np).pin_memory()
     hB = torch.from_numpy(B_np).pin_memory()
     hC = torch.empty((M, N), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        g.check(g.gemm_f32_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), M, N, K, algo,
+                                stream.cuda_stream), "gemm_f32_host")
+
+    for _ in range(2):
+        e2e_step()
     eb = torch.cuda.Event(enable_timing=True)
     ee = torch.cuda.Event(enable_timing=True)
     barrier(world, dev)
     torch.cuda.synchronize(dev)
     eb.record(stream)
     for _ in range(e2e_steps):
-        a.copy_(hA, non_blocking=True)
-        b.copy_(hB, non_blocking=True)
-        g.check(g.gemm_f32_algo_splitk(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, algo,
-                                       args.splits, stream.cuda_stream), "e2e")
-        hC.copy_(c, non_blocking=True)
+        e2e_step()
     ee.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = reduce_max(eb.elapsed_time(ee), world, dev)
@@ -461,7 +465,7 @@ def run_ours(args, world, rank, local):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": input_bytes,
-                "d2h_bytes_per_step": 4 * M * N, "steps": e2e_steps},
+                "d2h_bytes_per_step": 4 * M * N, "steps": e2e_steps, "entry": "gemm_f32_host"},
         "gpu_launches": K_steps * plan["kernels"],
         "clocks": clocks,
         "context": context,

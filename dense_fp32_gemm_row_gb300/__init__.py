@@ -28,7 +28,7 @@ __all__ = [
     "SUCCESS", "ERR_INVALID_VALUE", "ERR_UNSUPPORTED_DEVICE", "ERR_WORKSPACE",
     "ERR_DEVICE_TIMEOUT", "ERR_DESCRIPTOR", "GemmError",
     "library_path", "load", "gemm_f32", "gemm_f32_algo", "gemm_f32_algo_splitk",
-    "gemm_f32_algo_splitk_ev", "gemm_f32_noalloc",
+    "gemm_f32_algo_splitk_ev", "gemm_f32_noalloc", "gemm_f32_host",
     "gemm_f32_plan", "gemm_f32_device_status", "gemm_f32_selftest_watchdog",
     "gemm_f32_release", "gemm_f32_status_string", "gemm_f32_version", "matmul", "check",
 ]
@@ -94,6 +94,7 @@ def load():
         lib.gemm_f32_algo_splitk_ev.argtypes = [vp, vp, vp, i, i, i, i, i, vp, vp, vp]
         lib.gemm_f32_plan.argtypes = [i, i, i, i, i, vp, vp, vp, ctypes.POINTER(PlanInfo)]
         lib.gemm_f32_noalloc.argtypes = [vp, vp, vp, i, i, i, i, vp]
+        lib.gemm_f32_host.argtypes = [vp, vp, vp, i, i, i, i, vp]
         lib.gemm_f32_device_status.argtypes = [i]
         lib.gemm_f32_selftest_watchdog.argtypes = [ll, vp]
         lib.gemm_f32_release.argtypes = []
@@ -101,7 +102,7 @@ def load():
         lib.gemm_f32_status_string.restype = ctypes.c_char_p
         lib.gemm_f32_version.argtypes = []
         for name in ("gemm_f32", "gemm_f32_algo", "gemm_f32_algo_splitk",
-                     "gemm_f32_algo_splitk_ev", "gemm_f32_noalloc", "gemm_f32_plan", "gemm_f32_noalloc",
+                     "gemm_f32_algo_splitk_ev", "gemm_f32_noalloc", "gemm_f32_host", "gemm_f32_plan", "gemm_f32_noalloc",
                      "gemm_f32_device_status", "gemm_f32_selftest_watchdog", "gemm_f32_release",
                      "gemm_f32_version"):
             getattr(lib, name).restype = ctypes.c_int
@@ -130,6 +131,11 @@ def gemm_f32_algo_splitk_ev(A, B, C, M, N, K, algo, splits, stream=0, main_begin
     """``main_begin``/``main_end``: raw cudaEvent_t handles (e.g. ``torch.cuda.Event().cuda_event``)."""
     return load().gemm_f32_algo_splitk_ev(_p(A), _p(B), _p(C), M, N, K, algo, splits, _p(stream),
                                           _p(main_begin), _p(main_end))
+
+
+def gemm_f32_host(A, B, C, M, N, K, algo=ALGO_AUTO, stream=0) -> int:
+    """C = A @ B with HOST pointers; copies overlap the GEMM by row panels (asynchronous)."""
+    return load().gemm_f32_host(_p(A), _p(B), _p(C), M, N, K, algo, _p(stream))
 
 
 def gemm_f32_noalloc(A, B, C, M, N, K, splits=0, stream=0) -> int:

@@ -268,6 +268,140 @@ void make_plan(const DeviceState& d, const float* A, const float* B, int M, int 
     p->kernels = 1 + p->stage_a + p->stage_b + (p->splits > 1 ? 1 : 0);
 }
 
+// Device operands the GEMM kernel reads, after staging.
+struct Operands {
+    const float* a = nullptr;  // FFMA: A (padded copy when its layout needs one)
+    const float* b = nullptr;  // FFMA: B (padded copy when its layout needs one)
+    const float* a_hi = nullptr;
+    const float* a_lo = nullptr;  // 3xTF32: split A, rows padded to lda
+    const float* b_hi = nullptr;
+    const float* b_lo = nullptr;  // 3xTF32: split B^T (N x K), rows padded to ldb
+};
+
+// Stage B once per call: split + transpose (3xTF32) or pad (FFMA, if needed).
+int stage_b(const Plan& p, const float* B, int K, int N, unsigned char* ws, Operands* o,
+            cudaStream_t stream) {
+    cudaError_t e = cudaSuccess;
+    if (p.algo == GEMM_F32_ALGO_3XTF32) {
+        float* hi = reinterpret_cast<float*>(ws + p.off_b);
+        float* lo = reinterpret_cast<float*>(ws + p.off_b2);
+        if ((e = launch_split_transpose(B, N, K, N, hi, lo, p.ldb, stream)) != cudaSuccess)
+            return static_cast<int>(e);
+        o->b_hi = hi;
+        o->b_lo = lo;
+    } else if (p.stage_b) {
+        float* dst = reinterpret_cast<float*>(ws + p.off_b);
+        if ((e = launch_pad_copy(B, N, K, N, dst, p.ldb, stream)) != cudaSuccess)
+            return static_cast<int>(e);
+        o->b = dst;
+    } else {
+        o->b = B;
+    }
+    return GEMM_F32_SUCCESS;
+}
+
+// Stage M rows of A: split (3xTF32) or pad (FFMA, if needed).
+int stage_a(const Plan& p, const float* A, int M, int K, unsigned char* ws, Operands* o,
+            cudaStream_t stream) {
+    cudaError_t e = cudaSuccess;
+    if (p.algo == GEMM_F32_ALGO_3XTF32) {
+        float* hi = reinterpret_cast<float*>(ws + p.off_a);
+        float* lo = reinterpret_cast<float*>(ws + p.off_a2);
+        if ((e = launch_split_rows(A, K, M, K, hi, lo, p.lda, stream)) != cudaSuccess)
+            return static_cast<int>(e);
+        o->a_hi = hi;
+        o->a_lo = lo;
+    } else if (p.stage_a) {
+        float* dst = reinterpret_cast<float*>(ws + p.off_a);
+        if ((e = launch_pad_copy(A, K, M, K, dst, p.lda, stream)) != cudaSuccess)
+            return static_cast<int>(e);
+        o->a = dst;
+    } else {
+        o->a = A;
+    }
+    return GEMM_F32_SUCCESS;
+}
+
+// The GEMM kernel on staged operands (M rows), then the split-K reduction.
+int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C, int M, int N,
+                int K, unsigned char* ws, cudaStream_t stream, cudaEvent_t ev_begin,
+                cudaEvent_t ev_end) {
+    float* out = C;
+    long long ldo = N, split_stride = 0;
+    if (p.splits > 1) {
+        out = reinterpret_cast<float*>(ws + p.off_w);
+        ldo = p.ldw;
+        split_stride = static_cast<long long>(M) * p.ldw;
+    }
+    const int vec_store = (ldo % 4 == 0) && !misaligned16(out);
+    cudaError_t e = cudaSuccess;
+    int st = GEMM_F32_SUCCESS;
+    if (p.algo == GEMM_F32_ALGO_3XTF32) {
+        Tf32x3Args ta;
+        std::memset(&ta, 0, sizeof(ta));
+        // one CTA loads 128 rows of A and box_n rows of B^T per stage
+        if ((st = encode_2d(&ta.tmAhi, o.a_hi, K, M, p.lda, p.tile_k, 128,
+                            CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
+            (st = encode_2d(&ta.tmAlo, o.a_lo, K, M, p.lda, p.tile_k, 128,
+                            CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
+            (st = encode_2d(&ta.tmBhi, o.b_hi, K, N, p.ldb, p.tile_k, p.box_n,
+                            CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
+            (st = encode_2d(&ta.tmBlo, o.b_lo, K, N, p.ldb, p.tile_k, p.box_n,
+                            CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS)
+            return st;
+        ta.out = out;
+        ta.ldo = ldo;
+        ta.split_stride = split_stride;
+        ta.M = M;
+        ta.N = N;
+        ta.K = K;
+        ta.bn = p.bn;
+        ta.pair = p.pair;
+        ta.kb_per_split = p.kb_per_split;
+        ta.splits = p.splits;
+        ta.vec_store = vec_store;
+        ta.fault = d.fault;
+        ta.timeout_ns = kDefaultTimeoutNs;
+        if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
+            return static_cast<int>(e);
+        if ((e = launch_sgemm_3xtf32(ta, stream, d.sm_count)) != cudaSuccess)
+            return static_cast<int>(e);
+        if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess)
+            return static_cast<int>(e);
+    } else {
+        FfmaArgs fa;
+        std::memset(&fa, 0, sizeof(fa));
+        if ((st = encode_2d(&fa.tmA, o.a, K, M, p.lda, p.tile_k, p.tile_m,
+                            CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
+            (st = encode_2d(&fa.tmB, o.b, N, K, p.ldb, p.tile_n, p.tile_k,
+                            CU_TENSOR_MAP_SWIZZLE_NONE)) != GEMM_F32_SUCCESS)
+            return st;
+        fa.out = out;
+        fa.ldo = ldo;
+        fa.split_stride = split_stride;
+        fa.M = M;
+        fa.N = N;
+        fa.K = K;
+        fa.kb_per_split = p.kb_per_split;
+        fa.splits = p.splits;
+        fa.vec_store = vec_store;
+        fa.fault = d.fault;
+        fa.timeout_ns = kDefaultTimeoutNs;
+        fa.variant = p.variant;
+        fa.bn = p.tile_n;
+        if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
+            return static_cast<int>(e);
+        if ((e = launch_sgemm_ffma(fa, stream)) != cudaSuccess) return static_cast<int>(e);
+        if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess)
+            return static_cast<int>(e);
+    }
+    if (p.splits > 1) {
+        e = launch_splitk_reduce(out, split_stride, p.ldw, p.splits, C, N, M, N, stream);
+        if (e != cudaSuccess) return static_cast<int>(e);
+    }
+    return GEMM_F32_SUCCESS;
+}
+
 int run(const float* A, const float* B, float* C, int M, int N, int K, int algo, int splits,
         cudaStream_t stream, cudaEvent_t ev_begin = nullptr, cudaEvent_t ev_end = nullptr) {
     int st = validate(A, B, C, M, N, K, algo, splits);
@@ -298,102 +432,145 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int algo,
         if (st != GEMM_F32_SUCCESS) return st;
         ws = static_cast<unsigned char*>(w);
     }
+    Operands o;
+    if ((st = stage_a(p, A, M, K, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
+    if ((st = stage_b(p, B, K, N, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
+    return launch_gemm(p, *d, o, C, M, N, K, ws, stream, ev_begin, ev_end);
+}
 
-    float* out = C;
-    long long ldo = N, split_stride = 0;
-    if (p.splits > 1) {
-        out = reinterpret_cast<float*>(ws + p.off_w);
-        ldo = p.ldw;
-        split_stride = static_cast<long long>(M) * p.ldw;
-    }
-    const int vec_store = (ldo % 4 == 0) && !misaligned16(out);
+// ---- host-buffer entry: copies overlapped with the GEMM, by row panels ----
+constexpr int kMaxPanels = 16;
+
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev_start = nullptr, ev_b = nullptr, ev_done = nullptr;
+    cudaEvent_t ev_a[kMaxPanels] = {}, ev_c[kMaxPanels] = {};
+    void* dev_buf = nullptr;  // device copies of A, B and C
+    size_t dev_bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, HostPipe> g_pipes;
+
+// Side streams, events and the device copies for (dev, stream); g_mutex held.
+int host_pipe(int dev, cudaStream_t stream, size_t bytes, HostPipe** out) {
+    HostPipe& hp = g_pipes[std::make_pair(dev, stream)];
     cudaError_t e = cudaSuccess;
+    if (!hp.ready) {
+        const unsigned fl = cudaEventDisableTiming;
+        if ((e = cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&hp.ev_start, fl)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&hp.ev_b, fl)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&hp.ev_done, fl)) != cudaSuccess)
+            return static_cast<int>(e);
+        for (int i = 0; i < kMaxPanels; ++i)
+            if ((e = cudaEventCreateWithFlags(&hp.ev_a[i], fl)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&hp.ev_c[i], fl)) != cudaSuccess)
+                return static_cast<int>(e);
+        hp.ready = true;
+    }
+    if (hp.dev_bytes < bytes) {
+        if (hp.dev_buf) {
+            if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return static_cast<int>(e);
+            cudaFree(hp.dev_buf);
+            hp.dev_buf = nullptr;
+            hp.dev_bytes = 0;
+        }
+        if (cudaMalloc(&hp.dev_buf, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_F32_ERR_WORKSPACE;
+        }
+        hp.dev_bytes = bytes;
+    }
+    *out = &hp;
+    return GEMM_F32_SUCCESS;
+}
 
-    if (p.algo == GEMM_F32_ALGO_3XTF32) {
-        float* a_hi = reinterpret_cast<float*>(ws + p.off_a);
-        float* a_lo = reinterpret_cast<float*>(ws + p.off_a2);
-        float* b_hi = reinterpret_cast<float*>(ws + p.off_b);
-        float* b_lo = reinterpret_cast<float*>(ws + p.off_b2);
-        if ((e = launch_split_rows(A, K, M, K, a_hi, a_lo, p.lda, stream)) != cudaSuccess)
-            return static_cast<int>(e);
-        if ((e = launch_split_transpose(B, N, K, N, b_hi, b_lo, p.ldb, stream)) != cudaSuccess)
-            return static_cast<int>(e);
-        Tf32x3Args ta;
-        std::memset(&ta, 0, sizeof(ta));
-        // one CTA loads 128 rows of A and box_n rows of B^T per stage
-        if ((st = encode_2d(&ta.tmAhi, a_hi, K, M, p.lda, p.tile_k, 128,
-                            CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
-            (st = encode_2d(&ta.tmAlo, a_lo, K, M, p.lda, p.tile_k, 128,
-                            CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
-            (st = encode_2d(&ta.tmBhi, b_hi, K, N, p.ldb, p.tile_k, p.box_n,
-                            CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
-            (st = encode_2d(&ta.tmBlo, b_lo, K, N, p.ldb, p.tile_k, p.box_n,
-                            CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS)
-            return st;
-        ta.out = out;
-        ta.ldo = ldo;
-        ta.split_stride = split_stride;
-        ta.M = M;
-        ta.N = N;
-        ta.K = K;
-        ta.bn = p.bn;
-        ta.pair = p.pair;
-        ta.kb_per_split = p.kb_per_split;
-        ta.splits = p.splits;
-        ta.vec_store = vec_store;
-        ta.fault = d->fault;
-        ta.timeout_ns = kDefaultTimeoutNs;
-        if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
-            return static_cast<int>(e);
-        if ((e = launch_sgemm_3xtf32(ta, stream, d->sm_count)) != cudaSuccess)
-            return static_cast<int>(e);
-        if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess)
-            return static_cast<int>(e);
-    } else {
-        const float* a_src = A;
-        const float* b_src = B;
-        if (p.stage_a) {
-            float* dst = reinterpret_cast<float*>(ws + p.off_a);
-            if ((e = launch_pad_copy(A, K, M, K, dst, p.lda, stream)) != cudaSuccess)
-                return static_cast<int>(e);
-            a_src = dst;
-        }
-        if (p.stage_b) {
-            float* dst = reinterpret_cast<float*>(ws + p.off_b);
-            if ((e = launch_pad_copy(B, N, K, N, dst, p.ldb, stream)) != cudaSuccess)
-                return static_cast<int>(e);
-            b_src = dst;
-        }
-        FfmaArgs fa;
-        std::memset(&fa, 0, sizeof(fa));
-        if ((st = encode_2d(&fa.tmA, a_src, K, M, p.lda, p.tile_k, p.tile_m,
-                            CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
-            (st = encode_2d(&fa.tmB, b_src, N, K, p.ldb, p.tile_n, p.tile_k,
-                            CU_TENSOR_MAP_SWIZZLE_NONE)) != GEMM_F32_SUCCESS)
-            return st;
-        fa.out = out;
-        fa.ldo = ldo;
-        fa.split_stride = split_stride;
-        fa.M = M;
-        fa.N = N;
-        fa.K = K;
-        fa.kb_per_split = p.kb_per_split;
-        fa.splits = p.splits;
-        fa.vec_store = vec_store;
-        fa.fault = d->fault;
-        fa.timeout_ns = kDefaultTimeoutNs;
-        fa.variant = p.variant;
-        fa.bn = p.tile_n;
-        if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
-            return static_cast<int>(e);
-        if ((e = launch_sgemm_ffma(fa, stream)) != cudaSuccess) return static_cast<int>(e);
-        if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess)
-            return static_cast<int>(e);
+int run_host(const float* A, const float* B, float* C, int M, int N, int K, int algo,
+             cudaStream_t stream) {
+    int st = validate(A, B, C, M, N, K, algo, 0);
+    if (st != GEMM_F32_SUCCESS) return st;
+    if (M == 0 || N == 0) return GEMM_F32_SUCCESS;
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* d = nullptr;
+    int dev = 0;
+    if ((st = device_state(&d, &dev)) != GEMM_F32_SUCCESS) return st;
+    if ((st = get_encoder()) != GEMM_F32_SUCCESS) return st;
+
+    // device copies: A (M x K), B (K x N), C (M x N), each 256-byte aligned
+    const size_t bytes_a = static_cast<size_t>(round_up(static_cast<long long>(M) * K * 4, 256));
+    const size_t bytes_b = static_cast<size_t>(round_up(static_cast<long long>(K) * N * 4, 256));
+    const size_t bytes_c = static_cast<size_t>(round_up(static_cast<long long>(M) * N * 4, 256));
+    HostPipe* hp = nullptr;
+    if ((st = host_pipe(dev, stream, bytes_a + bytes_b + bytes_c, &hp)) != GEMM_F32_SUCCESS)
+        return st;
+    float* dA = static_cast<float*>(hp->dev_buf);
+    float* dB = reinterpret_cast<float*>(static_cast<unsigned char*>(hp->dev_buf) + bytes_a);
+    float* dC = reinterpret_cast<float*>(static_cast<unsigned char*>(hp->dev_buf) + bytes_a +
+                                         bytes_b);
+
+    // row panels: at least 512 rows, at most kMaxPanels of them
+    long long rows = (M + 7) / 8;
+    rows = round_up(rows < 512 ? 512 : rows, 128);
+    if ((M + rows - 1) / rows > kMaxPanels) rows = round_up((M + kMaxPanels - 1) / kMaxPanels, 128);
+    const int P = static_cast<int>(rows < M ? rows : M);
+    const int panels = (M + P - 1) / P;
+
+    cudaError_t e = cudaSuccess;
+#define GEMM_F32_TRY(x)                                      \
+    do {                                                     \
+        if ((e = (x)) != cudaSuccess) return static_cast<int>(e); \
+    } while (0)
+    // the side streams start after everything already queued on `stream`
+    GEMM_F32_TRY(cudaEventRecord(hp->ev_start, stream));
+    GEMM_F32_TRY(cudaStreamWaitEvent(hp->s_in, hp->ev_start, 0));
+    GEMM_F32_TRY(cudaStreamWaitEvent(hp->s_out, hp->ev_start, 0));
+
+    if (K == 0) {
+        GEMM_F32_TRY(launch_fill_zero(dC, static_cast<long long>(M) * N, stream));
+        GEMM_F32_TRY(cudaMemcpyAsync(C, dC, static_cast<size_t>(M) * N * 4,
+                                     cudaMemcpyDeviceToHost, stream));
+        return GEMM_F32_SUCCESS;
     }
-    if (p.splits > 1) {
-        e = launch_splitk_reduce(out, split_stride, p.ldw, p.splits, C, N, M, N, stream);
-        if (e != cudaSuccess) return static_cast<int>(e);
+
+    Plan p;
+    make_plan(*d, dA, dB, P, N, K, algo, 0, &p);
+    unsigned char* ws = nullptr;
+    if (p.ws_bytes) {
+        void* w = nullptr;
+        if ((st = workspace(dev, stream, p.ws_bytes, &w)) != GEMM_F32_SUCCESS) return st;
+        ws = static_cast<unsigned char*>(w);
     }
+
+    GEMM_F32_TRY(cudaMemcpyAsync(dB, B, static_cast<size_t>(K) * N * 4, cudaMemcpyHostToDevice,
+                                 hp->s_in));
+    GEMM_F32_TRY(cudaEventRecord(hp->ev_b, hp->s_in));
+    GEMM_F32_TRY(cudaStreamWaitEvent(stream, hp->ev_b, 0));
+    Operands o;
+    if ((st = stage_b(p, dB, K, N, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
+
+    for (int i = 0; i < panels; ++i) {
+        const int r0 = i * P;
+        const int mp = (M - r0) < P ? (M - r0) : P;
+        const size_t off_a = static_cast<size_t>(r0) * K, off_c = static_cast<size_t>(r0) * N;
+        GEMM_F32_TRY(cudaMemcpyAsync(dA + off_a, A + off_a, static_cast<size_t>(mp) * K * 4,
+                                     cudaMemcpyHostToDevice, hp->s_in));
+        GEMM_F32_TRY(cudaEventRecord(hp->ev_a[i], hp->s_in));
+        GEMM_F32_TRY(cudaStreamWaitEvent(stream, hp->ev_a[i], 0));
+        if ((st = stage_a(p, dA + off_a, mp, K, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
+        if ((st = launch_gemm(p, *d, o, dC + off_c, mp, N, K, ws, stream, nullptr, nullptr)) !=
+            GEMM_F32_SUCCESS)
+            return st;
+        GEMM_F32_TRY(cudaEventRecord(hp->ev_c[i], stream));
+        GEMM_F32_TRY(cudaStreamWaitEvent(hp->s_out, hp->ev_c[i], 0));
+        GEMM_F32_TRY(cudaMemcpyAsync(C + off_c, dC + off_c, static_cast<size_t>(mp) * N * 4,
+                                     cudaMemcpyDeviceToHost, hp->s_out));
+    }
+    // the call is complete on `stream` once the last panel of C is on the host
+    GEMM_F32_TRY(cudaEventRecord(hp->ev_done, hp->s_out));
+    GEMM_F32_TRY(cudaStreamWaitEvent(stream, hp->ev_done, 0));
+#undef GEMM_F32_TRY
     return GEMM_F32_SUCCESS;
 }
 
@@ -419,6 +596,11 @@ int gemm_f32_algo_splitk_ev(const float* A, const float* B, float* C, int M, int
                             int algo, int splits, cudaStream_t stream, cudaEvent_t main_begin,
                             cudaEvent_t main_end) {
     return run(A, B, C, M, N, K, algo, splits, stream, main_begin, main_end);
+}
+
+int gemm_f32_host(const float* A, const float* B, float* C, int M, int N, int K, int algo,
+                  cudaStream_t stream) {
+    return run_host(A, B, C, M, N, K, algo, stream);
 }
 
 int gemm_f32_plan(int M, int N, int K, int algo, int splits, const float* A, const float* B,
@@ -502,6 +684,25 @@ int gemm_f32_release(void) {
         cudaFree(kv.second.ptr);
     }
     g_ws.clear();
+    for (auto& kv : g_pipes) {
+        HostPipe& hp = kv.second;
+        cudaSetDevice(kv.first.first);
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess && status == GEMM_F32_SUCCESS) status = static_cast<int>(e);
+        if (hp.dev_buf) cudaFree(hp.dev_buf);
+        if (hp.ready) {
+            cudaStreamDestroy(hp.s_in);
+            cudaStreamDestroy(hp.s_out);
+            cudaEventDestroy(hp.ev_start);
+            cudaEventDestroy(hp.ev_b);
+            cudaEventDestroy(hp.ev_done);
+            for (int i = 0; i < kMaxPanels; ++i) {
+                cudaEventDestroy(hp.ev_a[i]);
+                cudaEventDestroy(hp.ev_c[i]);
+            }
+        }
+    }
+    g_pipes.clear();
     cudaSetDevice(prev);
     return status;
 }

@@ -115,6 +115,21 @@ int gemm_f32_algo_splitk_ev(const float* A, const float* B, float* C, int M, int
                             cudaEvent_t main_begin, cudaEvent_t main_end);
 
 /*
+ * gemm_f32_host -- C = A * B where A, B and C are HOST pointers (row-major,
+ * same shapes as gemm_f32).  The library copies B to the device, then walks
+ * row panels of A and C: the copy of panel i+1 of A, the GEMM of panel i
+ * and the copy back of panel i-1 of C run at the same time on the call's
+ * stream and two internal streams.  Page-locked host memory is needed for
+ * that overlap (pageable memory works, serialised).  Asynchronous on
+ * `stream`: the host buffers must stay valid, and C is complete, only when
+ * `stream` has reached the end of the call.  Device copies of A, B and C
+ * are kept in a library buffer per (device, stream), grown on demand like
+ * the workspace; gemm_f32_release() frees them.  Same status codes.
+ */
+int gemm_f32_host(const float* A, const float* B, float* C, int M, int N, int K, int algo,
+                  cudaStream_t stream);
+
+/*
  * gemm_f32_plan_info / gemm_f32_plan -- what a call with these arguments
  * would launch, without launching anything.  Needs a device (it reads the
  * SM count); returns a status code like the compute entry points.

@@ -206,3 +206,28 @@ def test_watchdog_times_out_and_context_survives():
     assert g.gemm_f32_device_status(1) == g.SUCCESS
     A, B = make_workload(1, M=65, N=66, K=67)
     _check(_gpu.run(A, B, g.ALGO_FFMA), oracle.ref_gemm(A, B), label="after watchdog")
+
+
+@pytest.mark.parametrize("shape", [(1025, 1023, 1000), (8192, 512, 256), (4100, 2304, 96),
+                                   (3, 5, 7), (64, 48, 0)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_host_buffer_entry(shape, pinned):
+    t = _gpu.torch()
+    M, N, K = shape
+    A, B = make_workload(1, M=M, N=N, K=K)
+    hA, hB = t.from_numpy(A), t.from_numpy(B)
+    hC = t.full((M + 2, N), float("nan"))  # one guard row after C
+    if pinned:
+        hA, hB, hC = hA.pin_memory(), hB.pin_memory(), hC.pin_memory()
+    s = t.cuda.current_stream()
+    for algo in (g.ALGO_3XTF32, g.ALGO_FFMA):
+        hC.fill_(float("nan"))
+        st = g.gemm_f32_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), M, N, K, algo,
+                             s.cuda_stream)
+        g.check(st, "gemm_f32_host")
+        s.synchronize()
+        g.check(g.gemm_f32_device_status(1), "device status")
+        out = hC.numpy()
+        assert np.isnan(out[M:]).all(), "write past C"
+        _check(out[:M].copy(), oracle.ref_gemm(A, B), label=f"host {shape} {algo}")
