@@ -60,6 +60,9 @@ def _bind(path: str):
     lib.ref_gemm_entries.restype = None
     lib.ref_gemm_rows.argtypes = [f32p, f32p, i64, i64, i64, i64, i64, f32p, ctypes.c_int]
     lib.ref_gemm_rows.restype = None
+    lib.ref_gemm_ex.argtypes = [ctypes.c_int, ctypes.c_int, i64, i64, i64, ctypes.c_double, f32p,
+                                i64, f32p, i64, ctypes.c_double, f32p, i64, ctypes.c_int]
+    lib.ref_gemm_ex.restype = None
     lib.ref_max_threads.argtypes = []
     lib.ref_max_threads.restype = ctypes.c_int
     return lib
@@ -128,6 +131,29 @@ def ref_gemm_rows(A: np.ndarray, B: np.ndarray, row0: int, nrows: int,
     if nrows and N:
         _load().ref_gemm_rows(_ptr(A), _ptr(B), M, N, K, int(row0), int(nrows), _ptr(out),
                               int(nthreads))
+    return out
+
+
+def ref_gemm_ex(transa: int, transb: int, M: int, N: int, K: int, alpha: float,
+                A: np.ndarray, lda: int, B: np.ndarray, ldb: int, beta: float,
+                C: np.ndarray, ldc: int, nthreads: int = 0) -> np.ndarray:
+    """General form C = alpha op(A) op(B) + beta C on flat row-major buffers.
+
+    ``A``, ``B`` and ``C`` are flat float32 arrays holding the matrices with
+    the given leading dimensions; returns a new flat copy of ``C`` with the
+    M x N block updated (elements outside it are left as they were).
+    """
+    A = _f32(np.ravel(A))
+    B = _f32(np.ravel(B))
+    out = _f32(np.ravel(C)).copy()
+    need_a = ((K - 1) * lda + M if transa else (M - 1) * lda + K) if M and K else 0
+    need_b = ((N - 1) * ldb + K if transb else (K - 1) * ldb + N) if K and N else 0
+    need_c = (M - 1) * ldc + N if M and N else 0
+    if A.size < need_a or B.size < need_b or out.size < need_c:
+        raise ValueError("buffer smaller than its leading dimension implies")
+    if M and N:
+        _load().ref_gemm_ex(int(transa), int(transb), M, N, K, float(alpha), _ptr(A), lda,
+                            _ptr(B), ldb, float(beta), _ptr(out), ldc, int(nthreads))
     return out
 
 

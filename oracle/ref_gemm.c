@@ -82,6 +82,42 @@ void ref_gemm_rows(const float* A, const float* B, int64_t M, int64_t N, int64_t
     (void)nthreads;
 }
 
+/*
+ * General form, row-major with leading dimensions and transposes:
+ *
+ *     C[i][j] = (float)( alpha * S + beta * (double)C[i][j] )     (beta != 0)
+ *     C[i][j] = (float)( alpha * S )                              (beta == 0)
+ *     S       = sum_{k ascending} (double)opA(i, k) * (double)opB(k, j)
+ *
+ * opA(i, k) = A[i*lda + k] (transa == 0) or A[k*lda + i] (transa == 1);
+ * opB(k, j) = B[k*ldb + j] (transb == 0) or B[j*ldb + k] (transb == 1);
+ * C[i][j] lives at C[i*ldc + j].  With beta == 0 the old C is never read, so
+ * a NaN there cannot leak into the result (the usual BLAS convention).
+ * alpha * S and beta * C are formed and added in double; one final rounding.
+ */
+void ref_gemm_ex(int transa, int transb, int64_t M, int64_t N, int64_t K, double alpha,
+                 const float* A, int64_t lda, const float* B, int64_t ldb, double beta,
+                 float* C, int64_t ldc, int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double sum = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double a = transa ? (double)A[k * lda + i] : (double)A[i * lda + k];
+                const double b = transb ? (double)B[j * ldb + k] : (double)B[k * ldb + j];
+                sum += a * b;
+            }
+            double r = alpha * sum;
+            if (beta != 0.0) r += beta * (double)C[i * ldc + j];
+            C[i * ldc + j] = (float)r;
+        }
+    (void)nthreads;
+}
+
 /* Threads the OpenMP runtime would use (1 without OpenMP). */
 int ref_max_threads(void)
 {

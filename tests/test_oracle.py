@@ -224,3 +224,62 @@ def test_comparator_tolerance_edges_and_nan():
         g = ref.copy()
         g[2] = poison
         assert not oracle.compare(g, ref)["pass"]
+
+
+# ---------------------------------------------------------------------------
+# general form: transposes, leading dimensions, alpha and beta
+# ---------------------------------------------------------------------------
+def test_general_form_reduces_to_plain_product():
+    A, B = make_workload(1, M=37, N=29, K=41)
+    C = oracle.ref_gemm(A, B)
+    got = oracle.ref_gemm_ex(0, 0, 37, 29, 41, 1.0, A, 41, B, 29, 0.0,
+                             np.full(37 * 29, np.nan, np.float32), 29)
+    assert np.array_equal(got.reshape(37, 29), C)
+
+
+def test_transposed_storage_gives_same_bits():
+    A, B = make_workload(2, M=23, N=19, K=31)
+    C = oracle.ref_gemm(A, B)
+    At = np.ascontiguousarray(A.T)  # K x M storage
+    Bt = np.ascontiguousarray(B.T)  # N x K storage
+    for ta, tb, a, lda, b, ldb in ((1, 0, At, 23, B, 19), (0, 1, A, 31, Bt, 31),
+                                   (1, 1, At, 23, Bt, 31)):
+        got = oracle.ref_gemm_ex(ta, tb, 23, 19, 31, 1.0, a, lda, b, ldb, 0.0,
+                                 np.zeros(23 * 19, np.float32), 19)
+        assert np.array_equal(got.reshape(23, 19), C), (ta, tb)
+
+
+def test_leading_dimensions_pick_the_right_submatrix():
+    # embed A (5 x 7) in a 5 x 11 buffer and C (5 x 3) in a 5 x 8 buffer
+    A = quantised_fill(5 * 7, 3).reshape(5, 7)
+    B = quantised_fill(7 * 3, 4).reshape(7, 3)
+    Abuf = np.full((5, 11), 1e30, np.float32)
+    Abuf[:, :7] = A
+    Cbuf = np.full((5, 8), 7.0, np.float32)
+    got = oracle.ref_gemm_ex(0, 0, 5, 3, 7, 1.0, Abuf, 11, B, 3, 0.0, Cbuf, 8).reshape(5, 8)
+    Ai = np.rint(A * 4).astype(np.int64)
+    Bi = np.rint(B * 4).astype(np.int64)
+    assert np.array_equal(got[:, :3], ((Ai @ Bi) / 16.0).astype(np.float32))
+    assert np.all(got[:, 3:] == 7.0)
+
+
+def test_alpha_beta_exact_on_dyadic_values():
+    # quantised inputs, alpha and beta powers of two, C old on a 1/16 grid:
+    # every step is exact, so the result is alpha S + beta C exactly
+    A = quantised_fill(9 * 13, 5).reshape(9, 13)
+    B = quantised_fill(13 * 6, 6).reshape(13, 6)
+    Cold = (quantised_fill(9 * 6, 7) / 4).astype(np.float32).reshape(9, 6)
+    S = (np.rint(A * 4).astype(np.int64) @ np.rint(B * 4).astype(np.int64)) / 16.0
+    got = oracle.ref_gemm_ex(0, 0, 9, 6, 13, 0.5, A, 13, B, 6, -2.0, Cold, 6).reshape(9, 6)
+    assert np.array_equal(got, (0.5 * S - 2.0 * Cold).astype(np.float32))
+
+
+def test_beta_zero_never_reads_c():
+    A, B = make_workload(1, M=4, N=5, K=6)
+    got = oracle.ref_gemm_ex(0, 0, 4, 5, 6, 1.0, A, 6, B, 5, 0.0,
+                             np.full(20, np.nan, np.float32), 5)
+    assert np.isfinite(got).all()
+    # beta != 0 with a NaN in C propagates it
+    got = oracle.ref_gemm_ex(0, 0, 4, 5, 6, 1.0, A, 6, B, 5, 1.0,
+                             np.full(20, np.nan, np.float32), 5)
+    assert np.isnan(got).all()
