@@ -479,6 +479,84 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+def run_curve(args) -> int:
+    """--curve: square sizes 128 .. 8192 for both kernels and cuBLAS context, as CSV.
+
+    The scaling report of "Lecture 12: final project" (its roofline report
+    program) on this library: per size and kernel the median call time over
+    `--steps` calls (L2 flushed between calls below 256 MiB of inputs),
+    TFLOP/s, compulsory bytes 4(MK + KN + MN), arithmetic intensity, the
+    bandwidth those bytes imply, the fraction of the kernel's roofline, and a
+    check of 512 sampled outputs against the CPU oracle.
+    """
+    import numpy as np
+    import torch
+
+    import dense_fp32_gemm_row_gb300 as g
+    import oracle
+    from seeded_inputs import make_workload
+
+    g.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    peaks, _ = load_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    mhz = float(peaks.get("sm_max_mhz") or 2070.0)
+    peak_ffma = props.multi_processor_count * FFMA_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+    peak_3x = float(peaks.get("bf16_tflops", 1900.0)) * NOMINAL_TF32_TFLOPS / NOMINAL_BF16_TFLOPS / 3
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    print("kernel,size,ms,tflops,bytes_gb,ai,bw_gbs,pct_roofline,check", flush=True)
+    sizes = [int(x) for x in args.curve_sizes.split(",")]
+    for n in sizes:
+        A_np, B_np = make_workload(2, M=n, N=n, K=n)
+        a = torch.from_numpy(A_np).to(dev)
+        b = torch.from_numpy(B_np).to(dev)
+        c = torch.empty((n, n), dtype=torch.float32, device=dev)
+        big = 8 * n * n >= 256 * 1024 * 1024
+        rng = np.random.default_rng(n)
+        rows, cols = rng.integers(0, n, 512), rng.integers(0, n, 512)
+        want = oracle.ref_gemm_entries(A_np, B_np, rows, cols)
+        flops = 2.0 * n ** 3
+        bytes_ = 4.0 * 3 * n * n
+        for name in ("ffma", "3xtf32", "cublas"):
+            if name == "cublas":
+                prev = torch.backends.cuda.matmul.allow_tf32
+                torch.backends.cuda.matmul.allow_tf32 = False
+
+                def call():
+                    torch.matmul(a, b, out=c)
+            else:
+                algo = g.ALGOS[name]
+
+                def call():
+                    g.check(g.gemm_f32_algo(a.data_ptr(), b.data_ptr(), c.data_ptr(), n, n, n,
+                                            algo, stream.cuda_stream), name)
+            for _ in range(3):
+                call()
+            times = []
+            for _ in range(args.steps):
+                if not big:
+                    flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
+            if name == "cublas":
+                torch.backends.cuda.matmul.allow_tf32 = prev
+            ms = statistics.median(times)
+            tf = flops / (ms * 1e-3) / 1e12
+            got = c.cpu().numpy()[rows, cols]
+            ok = oracle.compare(got, want)["pass"]
+            peak = {"ffma": peak_ffma, "3xtf32": peak_3x, "cublas": peak_ffma}[name]
+            print(f"{name},{n},{ms:.4f},{tf:.2f},{bytes_ / 1e9:.4f},{flops / bytes_:.1f},"
+                  f"{bytes_ / (ms * 1e-3) / 1e9:.1f},{100 * tf / peak:.1f},"
+                  f"{'pass' if ok else 'FAIL'}", flush=True)
+    return 0
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description="FP32 GEMM benchmark")
     ap.add_argument("--gpus", type=int, default=1)
@@ -492,10 +570,15 @@ def main(argv=None) -> int:
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true", help="skip the cuBLAS context timing")
+    ap.add_argument("--curve", action="store_true",
+                    help="print the size-scaling CSV (128 .. 8192) instead of the JSON line")
+    ap.add_argument("--curve-sizes", default="128,256,512,1024,2048,4096,8192")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_env()
+    if args.curve:
+        return run_curve(args)
     if args.impl == "reference":
         return run_reference(args, world, rank)
     return run_ours(args, world, rank, local)

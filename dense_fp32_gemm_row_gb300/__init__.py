@@ -28,7 +28,7 @@ __all__ = [
     "SUCCESS", "ERR_INVALID_VALUE", "ERR_UNSUPPORTED_DEVICE", "ERR_WORKSPACE",
     "ERR_DEVICE_TIMEOUT", "ERR_DESCRIPTOR", "GemmError",
     "library_path", "load", "gemm_f32", "gemm_f32_algo", "gemm_f32_algo_splitk",
-    "gemm_f32_algo_splitk_ev", "gemm_f32_noalloc", "gemm_f32_host",
+    "gemm_f32_algo_splitk_ev", "gemm_f32_noalloc", "gemm_f32_host", "gemm_f32_ex",
     "gemm_f32_plan", "gemm_f32_device_status", "gemm_f32_selftest_watchdog",
     "gemm_f32_release", "gemm_f32_status_string", "gemm_f32_version", "matmul", "check",
 ]
@@ -95,6 +95,8 @@ def load():
         lib.gemm_f32_plan.argtypes = [i, i, i, i, i, vp, vp, vp, ctypes.POINTER(PlanInfo)]
         lib.gemm_f32_noalloc.argtypes = [vp, vp, vp, i, i, i, i, vp]
         lib.gemm_f32_host.argtypes = [vp, vp, vp, i, i, i, i, vp]
+        f = ctypes.c_float
+        lib.gemm_f32_ex.argtypes = [i, i, i, i, i, f, vp, ll, vp, ll, f, vp, ll, i, i, vp]
         lib.gemm_f32_device_status.argtypes = [i]
         lib.gemm_f32_selftest_watchdog.argtypes = [ll, vp]
         lib.gemm_f32_release.argtypes = []
@@ -102,7 +104,7 @@ def load():
         lib.gemm_f32_status_string.restype = ctypes.c_char_p
         lib.gemm_f32_version.argtypes = []
         for name in ("gemm_f32", "gemm_f32_algo", "gemm_f32_algo_splitk",
-                     "gemm_f32_algo_splitk_ev", "gemm_f32_noalloc", "gemm_f32_host", "gemm_f32_plan", "gemm_f32_noalloc",
+                     "gemm_f32_algo_splitk_ev", "gemm_f32_noalloc", "gemm_f32_host", "gemm_f32_ex", "gemm_f32_plan", "gemm_f32_noalloc",
                      "gemm_f32_device_status", "gemm_f32_selftest_watchdog", "gemm_f32_release",
                      "gemm_f32_version"):
             getattr(lib, name).restype = ctypes.c_int
@@ -131,6 +133,14 @@ def gemm_f32_algo_splitk_ev(A, B, C, M, N, K, algo, splits, stream=0, main_begin
     """``main_begin``/``main_end``: raw cudaEvent_t handles (e.g. ``torch.cuda.Event().cuda_event``)."""
     return load().gemm_f32_algo_splitk_ev(_p(A), _p(B), _p(C), M, N, K, algo, splits, _p(stream),
                                           _p(main_begin), _p(main_end))
+
+
+def gemm_f32_ex(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, algo=ALGO_AUTO,
+                splits=0, stream=0) -> int:
+    """C = alpha op(A) op(B) + beta C, row-major with leading dimensions (see gemm_f32.h)."""
+    return load().gemm_f32_ex(int(transa), int(transb), M, N, K, float(alpha), _p(A), int(lda),
+                              _p(B), int(ldb), float(beta), _p(C), int(ldc), int(algo),
+                              int(splits), _p(stream))
 
 
 def gemm_f32_host(A, B, C, M, N, K, algo=ALGO_AUTO, stream=0) -> int:

@@ -6,7 +6,9 @@
 //  * splitk_reduce:  C = sum of the split-K partial products, added in split
 //                    order 0, 1, ..., S-1 so that the result is deterministic.
 //  * fill_zero:      C = 0 for K == 0 (the empty sum of the lecture-12
-//                    golden reference).
+//                    golden reference); scale_c: C = beta C for K == 0.
+//  * transpose_pad:  a transposed copy, for operands stored the other way
+//                    round from what a kernel reads.
 //  * watchdog:       a self-test that waits on a barrier nothing completes.
 //
 // All are grid-stride loops with coalesced accesses along rows; they are
@@ -14,6 +16,7 @@
 #include <cstdint>
 
 #include "device_sync.cuh"
+#include "epilogue.cuh"
 #include "gemm_internal.h"
 
 namespace gemm_f32_impl {
@@ -37,7 +40,8 @@ pad_copy_kernel(const float* __restrict__ src, long long lds, long long rows, lo
 
 __global__ void __launch_bounds__(kThreads)
 splitk_reduce_kernel(const float* __restrict__ ws, long long split_stride, long long ldw,
-                     int splits, float* __restrict__ C, long long ldc, int M, int N) {
+                     int splits, float* __restrict__ C, long long ldc, int M, int N, float alpha,
+                     float beta, int mode) {
     for (long long r = blockIdx.y; r < M; r += gridDim.y) {
         const float* w = ws + r * ldw;
         float* c = C + r * ldc;
@@ -45,7 +49,7 @@ splitk_reduce_kernel(const float* __restrict__ ws, long long split_stride, long 
              j += static_cast<long long>(gridDim.x) * kThreads) {
             float sum = w[j];
             for (int s = 1; s < splits; ++s) sum += w[s * split_stride + j];
-            c[j] = sum;
+            c[j] = scale1(sum, c + j, alpha, beta, mode);
         }
     }
 }
@@ -53,10 +57,11 @@ splitk_reduce_kernel(const float* __restrict__ ws, long long split_stride, long 
 // Vector form: ldw, ldc, N multiples of 4 and both bases 16-byte aligned.
 __global__ void __launch_bounds__(kThreads)
 splitk_reduce4_kernel(const float4* __restrict__ ws, long long split_stride4, long long ldw4,
-                      int splits, float4* __restrict__ C, long long ldc4, int M, int N4) {
+                      int splits, float* __restrict__ C, long long ldc, int M, int N4, float alpha,
+                      float beta, int mode) {
     for (long long r = blockIdx.y; r < M; r += gridDim.y) {
         const float4* w = ws + r * ldw4;
-        float4* c = C + r * ldc4;
+        float* c = C + r * ldc;
         for (long long j = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; j < N4;
              j += static_cast<long long>(gridDim.x) * kThreads) {
             float4 sum = w[j];
@@ -67,9 +72,43 @@ splitk_reduce4_kernel(const float4* __restrict__ ws, long long split_stride4, lo
                 sum.z += v.z;
                 sum.w += v.w;
             }
-            c[j] = sum;
+            store4(c, static_cast<int>(4 * j), 4 * N4, sum, true, alpha, beta, mode);
         }
     }
+}
+
+// 32 x 32 tiles through shared memory, row pitch 33 (conflict-free columns).
+__global__ void __launch_bounds__(256)
+transpose_pad_kernel(const float* __restrict__ src, long long lds, long long rows, long long cols,
+                     float* __restrict__ dst, long long ldd) {
+    __shared__ float tile[32][33];
+    const int tx = threadIdx.x;
+    const int ty = threadIdx.y;
+    const long long c0 = static_cast<long long>(blockIdx.x) * 32;
+    const long long rblocks = (rows + 31) / 32;
+    for (long long rb = blockIdx.y; rb < rblocks; rb += gridDim.y) {
+        const long long r0 = rb * 32;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const long long r = r0 + ty + 8 * i, c = c0 + tx;
+            tile[ty + 8 * i][tx] = (r < rows && c < cols) ? src[r * lds + c] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const long long c = c0 + ty + 8 * i, r = r0 + tx;
+            if (c < cols && r < rows) dst[c * ldd + r] = tile[tx][ty + 8 * i];
+        }
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+scale_c_kernel(float* __restrict__ C, long long ldc, int M, int N, float beta) {
+    for (long long r = blockIdx.y; r < M; r += gridDim.y)
+        for (long long j = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; j < N;
+             j += static_cast<long long>(gridDim.x) * kThreads)
+            C[r * ldc + j] = beta == 0.0f ? 0.0f : beta * C[r * ldc + j];
 }
 
 __global__ void __launch_bounds__(kThreads) fill_zero_kernel(float* __restrict__ C, long long n) {
@@ -108,8 +147,8 @@ cudaError_t launch_pad_copy(const float* src, long long lds, long long rows, lon
 }
 
 cudaError_t launch_splitk_reduce(const float* ws, long long split_stride, long long ldw,
-                                 int splits, float* C, long long ldc, int M, int N,
-                                 cudaStream_t s) {
+                                 int splits, float* C, long long ldc, int M, int N, float alpha,
+                                 float beta, int scale_mode, cudaStream_t s) {
     if (M <= 0 || N <= 0) return cudaSuccess;
     const unsigned gy = static_cast<unsigned>(M < 65535 ? M : 65535);
     const bool vec = (N % 4 == 0) && (ldw % 4 == 0) && (ldc % 4 == 0) && (split_stride % 4 == 0) &&
@@ -118,12 +157,30 @@ cudaError_t launch_splitk_reduce(const float* ws, long long split_stride, long l
     if (vec) {
         dim3 grid(grid_1d(N / 4, kThreads, 64), gy);
         splitk_reduce4_kernel<<<grid, kThreads, 0, s>>>(
-            reinterpret_cast<const float4*>(ws), split_stride / 4, ldw / 4, splits,
-            reinterpret_cast<float4*>(C), ldc / 4, M, N / 4);
+            reinterpret_cast<const float4*>(ws), split_stride / 4, ldw / 4, splits, C, ldc, M,
+            N / 4, alpha, beta, scale_mode);
     } else {
         dim3 grid(grid_1d(N, kThreads, 64), gy);
-        splitk_reduce_kernel<<<grid, kThreads, 0, s>>>(ws, split_stride, ldw, splits, C, ldc, M, N);
+        splitk_reduce_kernel<<<grid, kThreads, 0, s>>>(ws, split_stride, ldw, splits, C, ldc, M, N,
+                                                       alpha, beta, scale_mode);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_pad(const float* src, long long lds, long long rows, long long cols,
+                                 float* dst, long long ldd, cudaStream_t s) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    const long long rblocks = (rows + 31) / 32;
+    dim3 grid(static_cast<unsigned>((cols + 31) / 32),
+              static_cast<unsigned>(rblocks < 65535 ? rblocks : 65535));
+    transpose_pad_kernel<<<grid, dim3(32, 8), 0, s>>>(src, lds, rows, cols, dst, ldd);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scale_c(float* C, long long ldc, int M, int N, float beta, cudaStream_t s) {
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    dim3 grid(grid_1d(N, kThreads, 64), static_cast<unsigned>(M < 65535 ? M : 65535));
+    scale_c_kernel<<<grid, kThreads, 0, s>>>(C, ldc, M, N, beta);
     return cudaGetLastError();
 }
 

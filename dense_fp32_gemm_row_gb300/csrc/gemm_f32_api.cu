@@ -153,21 +153,67 @@ struct Plan {
     int tile_m = 0, tile_n = 0, tile_k = 0, stages = 0, ctas = 0, kernels = 0;
 };
 
-int validate(const float* A, const float* B, const float* C, int M, int N, int K, int algo,
-             int splits, bool need_ptrs = true) {
+// One call's operands in the general row-major form C = alpha op(A) op(B) +
+// beta C.  op(A) is M x K: A[i*lda + k], or A[k*lda + i] when ta; op(B) is
+// K x N: B[k*ldb + j], or B[j*ldb + k] when tb; C[i*ldc + j].
+struct Problem {
+    int M = 0, N = 0, K = 0;
+    const float* A = nullptr;
+    long long lda = 0;
+    int ta = 0;
+    const float* B = nullptr;
+    long long ldb = 0;
+    int tb = 0;
+    float* C = nullptr;
+    long long ldc = 0;
+    float alpha = 1.0f, beta = 0.0f;
+};
+
+Problem packed(const float* A, const float* B, float* C, int M, int N, int K) {
+    Problem q;
+    q.M = M;
+    q.N = N;
+    q.K = K;
+    // packed strides; an empty dimension still has a stride of at least 1
+    q.A = A;
+    q.lda = K > 1 ? K : 1;
+    q.B = B;
+    q.ldb = N > 1 ? N : 1;
+    q.C = C;
+    q.ldc = N > 1 ? N : 1;
+    return q;
+}
+
+// epilogue mode: plain store, alpha scale, or alpha and beta (reads C)
+int scale_mode(const Problem& q) {
+    if (q.beta != 0.0f) return 2;
+    return q.alpha == 1.0f ? 0 : 1;
+}
+
+int validate(const Problem& q, int algo, int splits, bool need_ptrs = true) {
+    const int M = q.M, N = q.N, K = q.K;
     if (M < 0 || N < 0 || K < 0) return GEMM_F32_ERR_INVALID_VALUE;
     if (algo < GEMM_F32_ALGO_AUTO || algo > GEMM_F32_ALGO_3XTF32) return GEMM_F32_ERR_INVALID_VALUE;
     if (splits < 0 || splits > GEMM_F32_MAX_SPLITS) return GEMM_F32_ERR_INVALID_VALUE;
-    const size_t a_bytes = static_cast<size_t>(M) * static_cast<size_t>(K) * 4u;
-    const size_t b_bytes = static_cast<size_t>(K) * static_cast<size_t>(N) * 4u;
-    const size_t c_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * 4u;
+    if ((q.ta != 0 && q.ta != 1) || (q.tb != 0 && q.tb != 1)) return GEMM_F32_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return GEMM_F32_SUCCESS;  // empty output: nothing is looked at
+    // stored shapes: A is (ta ? K x M : M x K), B is (tb ? N x K : K x N)
+    const long long a_rows = q.ta ? K : M, a_cols = q.ta ? M : K;
+    const long long b_rows = q.tb ? N : K, b_cols = q.tb ? K : N;
+    if (q.lda < (a_cols > 1 ? a_cols : 1) || q.ldb < (b_cols > 1 ? b_cols : 1) ||
+        q.ldc < (N > 1 ? N : 1))
+        return GEMM_F32_ERR_INVALID_VALUE;
+    const size_t a_bytes = (a_rows && a_cols) ? static_cast<size_t>((a_rows - 1) * q.lda + a_cols) * 4u : 0;
+    const size_t b_bytes = (b_rows && b_cols) ? static_cast<size_t>((b_rows - 1) * q.ldb + b_cols) * 4u : 0;
+    const size_t c_bytes = (M && N) ? static_cast<size_t>((static_cast<long long>(M) - 1) * q.ldc + N) * 4u : 0;
     if (M > 0 && N > 0) {
-        if (need_ptrs && !C) return GEMM_F32_ERR_INVALID_VALUE;
-        if (need_ptrs && K > 0 && (!A || !B)) return GEMM_F32_ERR_INVALID_VALUE;
-        if (overlaps(C, c_bytes, A, a_bytes) || overlaps(C, c_bytes, B, b_bytes))
+        if (need_ptrs && !q.C) return GEMM_F32_ERR_INVALID_VALUE;
+        if (need_ptrs && K > 0 && (!q.A || !q.B)) return GEMM_F32_ERR_INVALID_VALUE;
+        if (overlaps(q.C, c_bytes, q.A, a_bytes) || overlaps(q.C, c_bytes, q.B, b_bytes))
             return GEMM_F32_ERR_INVALID_VALUE;
-        if ((reinterpret_cast<uintptr_t>(C) & 3u) || (A && (reinterpret_cast<uintptr_t>(A) & 3u)) ||
-            (B && (reinterpret_cast<uintptr_t>(B) & 3u)))
+        if ((reinterpret_cast<uintptr_t>(q.C) & 3u) ||
+            (q.A && (reinterpret_cast<uintptr_t>(q.A) & 3u)) ||
+            (q.B && (reinterpret_cast<uintptr_t>(q.B) & 3u)))
             return GEMM_F32_ERR_INVALID_VALUE;
     }
     return GEMM_F32_SUCCESS;
@@ -198,8 +244,8 @@ size_t carve(size_t* off, long long bytes) {
     return at;
 }
 
-void make_plan(const DeviceState& d, const float* A, const float* B, int M, int N, int K, int algo,
-               int splits, Plan* p) {
+void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Plan* p) {
+    const int M = q.M, N = q.N, K = q.K;
     p->algo = (algo == GEMM_F32_ALGO_AUTO) ? GEMM_F32_ALGO_3XTF32 : algo;
     int bm, bn, bk, slots;
     if (p->algo == GEMM_F32_ALGO_3XTF32) {
@@ -254,10 +300,12 @@ void make_plan(const DeviceState& d, const float* A, const float* B, int M, int 
         p->ctas = units < slots ? units : slots;
         if (p->pair) p->ctas *= 2;
     } else {
-        p->stage_a = (K % 4 != 0) || misaligned16(A);
-        p->stage_b = (N % 4 != 0) || misaligned16(B);
-        p->lda = p->stage_a ? round_up(K, 4) : K;
-        p->ldb = p->stage_b ? round_up(N, 4) : N;
+        // read in place when TMA can describe the operand as stored: K- (A)
+        // or N-contiguous (B) rows, 16-byte row stride and base
+        p->stage_a = q.ta || (q.lda % 4 != 0) || misaligned16(q.A);
+        p->stage_b = q.tb || (q.ldb % 4 != 0) || misaligned16(q.B);
+        p->lda = p->stage_a ? round_up(K, 4) : q.lda;
+        p->ldb = p->stage_b ? round_up(N, 4) : q.ldb;
         if (p->stage_a) p->off_a = carve(&off, static_cast<long long>(M) * p->lda * 4);
         if (p->stage_b) p->off_b = carve(&off, static_cast<long long>(K) * p->ldb * 4);
         p->ctas = units;
@@ -278,60 +326,71 @@ struct Operands {
     const float* b_lo = nullptr;  // 3xTF32: split B^T (N x K), rows padded to ldb
 };
 
-// Stage B once per call: split + transpose (3xTF32) or pad (FFMA, if needed).
-int stage_b(const Plan& p, const float* B, int K, int N, unsigned char* ws, Operands* o,
-            cudaStream_t stream) {
+// Stage B once per call: K-major TF32 hi/lo (3xTF32), or an N-contiguous
+// padded copy (FFMA) when B cannot be read in place.
+int stage_b(const Plan& p, const Problem& q, unsigned char* ws, Operands* o, cudaStream_t stream) {
     cudaError_t e = cudaSuccess;
+    const int K = q.K, N = q.N;
     if (p.algo == GEMM_F32_ALGO_3XTF32) {
         float* hi = reinterpret_cast<float*>(ws + p.off_b);
         float* lo = reinterpret_cast<float*>(ws + p.off_b2);
-        if ((e = launch_split_transpose(B, N, K, N, hi, lo, p.ldb, stream)) != cudaSuccess)
-            return static_cast<int>(e);
+        e = q.tb ? launch_split_rows(q.B, q.ldb, N, K, hi, lo, p.ldb, stream)        // N x K already
+                 : launch_split_transpose(q.B, q.ldb, K, N, hi, lo, p.ldb, stream);  // K x N -> N x K
+        if (e != cudaSuccess) return static_cast<int>(e);
         o->b_hi = hi;
         o->b_lo = lo;
     } else if (p.stage_b) {
         float* dst = reinterpret_cast<float*>(ws + p.off_b);
-        if ((e = launch_pad_copy(B, N, K, N, dst, p.ldb, stream)) != cudaSuccess)
-            return static_cast<int>(e);
+        e = q.tb ? launch_transpose_pad(q.B, q.ldb, N, K, dst, p.ldb, stream)
+                 : launch_pad_copy(q.B, q.ldb, K, N, dst, p.ldb, stream);
+        if (e != cudaSuccess) return static_cast<int>(e);
         o->b = dst;
     } else {
-        o->b = B;
+        o->b = q.B;
     }
     return GEMM_F32_SUCCESS;
 }
 
-// Stage M rows of A: split (3xTF32) or pad (FFMA, if needed).
-int stage_a(const Plan& p, const float* A, int M, int K, unsigned char* ws, Operands* o,
+// Stage op(A) rows [r0, r0 + M) (r0 > 0 only for untransposed A): TF32 hi/lo
+// (3xTF32), or a K-contiguous padded copy (FFMA) when A cannot be read in place.
+int stage_a(const Plan& p, const Problem& q, long long r0, int M, unsigned char* ws, Operands* o,
             cudaStream_t stream) {
     cudaError_t e = cudaSuccess;
+    const int K = q.K;
+    const float* a = q.ta ? q.A + r0 : q.A + r0 * q.lda;
     if (p.algo == GEMM_F32_ALGO_3XTF32) {
         float* hi = reinterpret_cast<float*>(ws + p.off_a);
         float* lo = reinterpret_cast<float*>(ws + p.off_a2);
-        if ((e = launch_split_rows(A, K, M, K, hi, lo, p.lda, stream)) != cudaSuccess)
-            return static_cast<int>(e);
+        e = q.ta ? launch_split_transpose(a, q.lda, K, M, hi, lo, p.lda, stream)  // K x M -> M x K
+                 : launch_split_rows(a, q.lda, M, K, hi, lo, p.lda, stream);
+        if (e != cudaSuccess) return static_cast<int>(e);
         o->a_hi = hi;
         o->a_lo = lo;
     } else if (p.stage_a) {
         float* dst = reinterpret_cast<float*>(ws + p.off_a);
-        if ((e = launch_pad_copy(A, K, M, K, dst, p.lda, stream)) != cudaSuccess)
-            return static_cast<int>(e);
+        e = q.ta ? launch_transpose_pad(a, q.lda, K, M, dst, p.lda, stream)
+                 : launch_pad_copy(a, q.lda, M, K, dst, p.lda, stream);
+        if (e != cudaSuccess) return static_cast<int>(e);
         o->a = dst;
     } else {
-        o->a = A;
+        o->a = a;
     }
     return GEMM_F32_SUCCESS;
 }
 
-// The GEMM kernel on staged operands (M rows), then the split-K reduction.
-int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C, int M, int N,
-                int K, unsigned char* ws, cudaStream_t stream, cudaEvent_t ev_begin,
-                cudaEvent_t ev_end) {
+// The GEMM kernel on staged operands: M rows of C starting at C (row stride
+// ldc), then the split-K reduction.  alpha/beta are applied where C is written.
+int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C, long long ldc,
+                int M, int N, int K, float alpha, float beta, int mode, unsigned char* ws,
+                cudaStream_t stream, cudaEvent_t ev_begin, cudaEvent_t ev_end) {
     float* out = C;
-    long long ldo = N, split_stride = 0;
+    long long ldo = ldc, split_stride = 0;
+    int kmode = mode;
     if (p.splits > 1) {
         out = reinterpret_cast<float*>(ws + p.off_w);
         ldo = p.ldw;
         split_stride = static_cast<long long>(M) * p.ldw;
+        kmode = 0;  // partials are raw sums; the reduction scales
     }
     const int vec_store = (ldo % 4 == 0) && !misaligned16(out);
     cudaError_t e = cudaSuccess;
@@ -362,6 +421,9 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
         ta.vec_store = vec_store;
         ta.fault = d.fault;
         ta.timeout_ns = kDefaultTimeoutNs;
+        ta.alpha = alpha;
+        ta.beta = beta;
+        ta.scale_mode = kmode;
         if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
             return static_cast<int>(e);
         if ((e = launch_sgemm_3xtf32(ta, stream, d.sm_count)) != cudaSuccess)
@@ -389,6 +451,9 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
         fa.timeout_ns = kDefaultTimeoutNs;
         fa.variant = p.variant;
         fa.bn = p.tile_n;
+        fa.alpha = alpha;
+        fa.beta = beta;
+        fa.scale_mode = kmode;
         if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
             return static_cast<int>(e);
         if ((e = launch_sgemm_ffma(fa, stream)) != cudaSuccess) return static_cast<int>(e);
@@ -396,17 +461,18 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
             return static_cast<int>(e);
     }
     if (p.splits > 1) {
-        e = launch_splitk_reduce(out, split_stride, p.ldw, p.splits, C, N, M, N, stream);
+        e = launch_splitk_reduce(out, split_stride, p.ldw, p.splits, C, ldc, M, N, alpha, beta,
+                                 mode, stream);
         if (e != cudaSuccess) return static_cast<int>(e);
     }
     return GEMM_F32_SUCCESS;
 }
 
-int run(const float* A, const float* B, float* C, int M, int N, int K, int algo, int splits,
-        cudaStream_t stream, cudaEvent_t ev_begin = nullptr, cudaEvent_t ev_end = nullptr) {
-    int st = validate(A, B, C, M, N, K, algo, splits);
+int run(const Problem& q, int algo, int splits, cudaStream_t stream,
+        cudaEvent_t ev_begin = nullptr, cudaEvent_t ev_end = nullptr) {
+    int st = validate(q, algo, splits);
     if (st != GEMM_F32_SUCCESS) return st;
-    if (M == 0 || N == 0) return GEMM_F32_SUCCESS;
+    if (q.M == 0 || q.N == 0) return GEMM_F32_SUCCESS;
 
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState* d = nullptr;
@@ -414,8 +480,9 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int algo,
     st = device_state(&d, &dev);
     if (st != GEMM_F32_SUCCESS) return st;
 
-    if (K == 0) {
-        cudaError_t e = launch_fill_zero(C, static_cast<long long>(M) * N, stream);
+    if (q.K == 0 || q.alpha == 0.0f) {
+        // empty sum (or a zero multiplier): C = beta C, A and B not read
+        cudaError_t e = launch_scale_c(q.C, q.ldc, q.M, q.N, q.beta, stream);
         return e == cudaSuccess ? GEMM_F32_SUCCESS : static_cast<int>(e);
     }
 
@@ -423,7 +490,7 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int algo,
     if (st != GEMM_F32_SUCCESS) return st;
 
     Plan p;
-    make_plan(*d, A, B, M, N, K, algo, splits, &p);
+    make_plan(*d, q, algo, splits, &p);
 
     unsigned char* ws = nullptr;
     if (p.ws_bytes) {
@@ -433,9 +500,10 @@ int run(const float* A, const float* B, float* C, int M, int N, int K, int algo,
         ws = static_cast<unsigned char*>(w);
     }
     Operands o;
-    if ((st = stage_a(p, A, M, K, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
-    if ((st = stage_b(p, B, K, N, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
-    return launch_gemm(p, *d, o, C, M, N, K, ws, stream, ev_begin, ev_end);
+    if ((st = stage_a(p, q, 0, q.M, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
+    if ((st = stage_b(p, q, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
+    return launch_gemm(p, *d, o, q.C, q.ldc, q.M, q.N, q.K, q.alpha, q.beta, scale_mode(q), ws,
+                       stream, ev_begin, ev_end);
 }
 
 // ---- host-buffer entry: copies overlapped with the GEMM, by row panels ----
@@ -488,7 +556,7 @@ int host_pipe(int dev, cudaStream_t stream, size_t bytes, HostPipe** out) {
 
 int run_host(const float* A, const float* B, float* C, int M, int N, int K, int algo,
              cudaStream_t stream) {
-    int st = validate(A, B, C, M, N, K, algo, 0);
+    int st = validate(packed(A, B, C, M, N, K), algo, 0);
     if (st != GEMM_F32_SUCCESS) return st;
     if (M == 0 || N == 0) return GEMM_F32_SUCCESS;
 
@@ -534,8 +602,12 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
         return GEMM_F32_SUCCESS;
     }
 
+    // device-side problem: the device copies, one panel of P rows at a time
+    Problem q = packed(dA, dB, dC, M, N, K);
+    Problem qp = q;
+    qp.M = P;
     Plan p;
-    make_plan(*d, dA, dB, P, N, K, algo, 0, &p);
+    make_plan(*d, qp, algo, 0, &p);
     unsigned char* ws = nullptr;
     if (p.ws_bytes) {
         void* w = nullptr;
@@ -548,7 +620,7 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
     GEMM_F32_TRY(cudaEventRecord(hp->ev_b, hp->s_in));
     GEMM_F32_TRY(cudaStreamWaitEvent(stream, hp->ev_b, 0));
     Operands o;
-    if ((st = stage_b(p, dB, K, N, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
+    if ((st = stage_b(p, q, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
 
     for (int i = 0; i < panels; ++i) {
         const int r0 = i * P;
@@ -558,9 +630,9 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
                                      cudaMemcpyHostToDevice, hp->s_in));
         GEMM_F32_TRY(cudaEventRecord(hp->ev_a[i], hp->s_in));
         GEMM_F32_TRY(cudaStreamWaitEvent(stream, hp->ev_a[i], 0));
-        if ((st = stage_a(p, dA + off_a, mp, K, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
-        if ((st = launch_gemm(p, *d, o, dC + off_c, mp, N, K, ws, stream, nullptr, nullptr)) !=
-            GEMM_F32_SUCCESS)
+        if ((st = stage_a(p, q, r0, mp, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
+        if ((st = launch_gemm(p, *d, o, dC + off_c, N, mp, N, K, 1.0f, 0.0f, 0, ws, stream,
+                              nullptr, nullptr)) != GEMM_F32_SUCCESS)
             return st;
         GEMM_F32_TRY(cudaEventRecord(hp->ev_c[i], stream));
         GEMM_F32_TRY(cudaStreamWaitEvent(hp->s_out, hp->ev_c[i], 0));
@@ -579,23 +651,43 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
 extern "C" {
 
 int gemm_f32(const float* A, const float* B, float* C, int M, int N, int K, cudaStream_t stream) {
-    return run(A, B, C, M, N, K, GEMM_F32_ALGO_AUTO, 0, stream);
+    return run(packed(A, B, C, M, N, K), GEMM_F32_ALGO_AUTO, 0, stream);
 }
 
 int gemm_f32_algo(const float* A, const float* B, float* C, int M, int N, int K, int algo,
                   cudaStream_t stream) {
-    return run(A, B, C, M, N, K, algo, 0, stream);
+    return run(packed(A, B, C, M, N, K), algo, 0, stream);
 }
 
 int gemm_f32_algo_splitk(const float* A, const float* B, float* C, int M, int N, int K, int algo,
                          int splits, cudaStream_t stream) {
-    return run(A, B, C, M, N, K, algo, splits, stream);
+    return run(packed(A, B, C, M, N, K), algo, splits, stream);
+}
+
+int gemm_f32_ex(int transa, int transb, int M, int N, int K, float alpha, const float* A,
+                long long lda, const float* B, long long ldb, float beta, float* C, long long ldc,
+                int algo, int splits, cudaStream_t stream) {
+    Problem q;
+    q.M = M;
+    q.N = N;
+    q.K = K;
+    q.A = A;
+    q.lda = lda;
+    q.ta = transa;
+    q.B = B;
+    q.ldb = ldb;
+    q.tb = transb;
+    q.C = C;
+    q.ldc = ldc;
+    q.alpha = alpha;
+    q.beta = beta;
+    return run(q, algo, splits, stream);
 }
 
 int gemm_f32_algo_splitk_ev(const float* A, const float* B, float* C, int M, int N, int K,
                             int algo, int splits, cudaStream_t stream, cudaEvent_t main_begin,
                             cudaEvent_t main_end) {
-    return run(A, B, C, M, N, K, algo, splits, stream, main_begin, main_end);
+    return run(packed(A, B, C, M, N, K), algo, splits, stream, main_begin, main_end);
 }
 
 int gemm_f32_host(const float* A, const float* B, float* C, int M, int N, int K, int algo,
@@ -608,7 +700,8 @@ int gemm_f32_plan(int M, int N, int K, int algo, int splits, const float* A, con
     if (!out) return GEMM_F32_ERR_INVALID_VALUE;
     std::memset(out, 0, sizeof(*out));
     // pointers are optional here: they only decide the alignment staging
-    int st = validate(A, B, C, M, N, K, algo, splits, false);
+    const Problem q = packed(A, B, const_cast<float*>(C), M, N, K);
+    int st = validate(q, algo, splits, false);
     if (st != GEMM_F32_SUCCESS) return st;
     out->splits = 1;
     if (M == 0 || N == 0) return GEMM_F32_SUCCESS;
@@ -622,7 +715,7 @@ int gemm_f32_plan(int M, int N, int K, int algo, int splits, const float* A, con
         return GEMM_F32_SUCCESS;
     }
     Plan p;
-    make_plan(*d, A, B, M, N, K, algo, splits, &p);
+    make_plan(*d, q, algo, splits, &p);
     out->algo = p.algo;
     out->splits = p.splits;
     out->tile_m = p.tile_m;

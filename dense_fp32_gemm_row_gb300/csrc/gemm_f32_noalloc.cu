@@ -225,7 +225,8 @@ extern "C" int gemm_f32_noalloc(const float* A, const float* B, float* C, int M,
     fa.vec_store = (fa.ldo % 4 == 0) && !(reinterpret_cast<uintptr_t>(fa.out) & 15u);
     if ((e = launch_sgemm_ffma(fa, stream)) != cudaSuccess) return static_cast<int>(e);
     if (s > 1 &&
-        (e = launch_splitk_reduce(parts, fa.split_stride, ldw, s, C, N, M, N, stream)) != cudaSuccess)
+        (e = launch_splitk_reduce(parts, fa.split_stride, ldw, s, C, N, M, N, 1.0f, 0.0f, 0,
+                                  stream)) != cudaSuccess)
         return static_cast<int>(e);
     return GEMM_F32_SUCCESS;
 }

@@ -33,6 +33,8 @@ struct FfmaArgs {
     long long timeout_ns;
     int variant;            // ffma_config variant
     int bn;                 // tile width the B descriptor's box was encoded with
+    float alpha, beta;      // output scaling (epilogue.cuh modes)
+    int scale_mode;         // 0 plain, 1 alpha, 2 alpha and beta (reads C)
 };
 cudaError_t launch_sgemm_ffma(const FfmaArgs& a, cudaStream_t s);
 
@@ -60,6 +62,8 @@ struct Tf32x3Args {
     int vec_store;
     unsigned* fault;
     long long timeout_ns;
+    float alpha, beta;      // output scaling (epilogue.cuh modes)
+    int scale_mode;
 };
 // persistent grid: min(units, sm_count) CTAs, or for the pair kernel
 // 2 x min(units, co-resident clusters)
@@ -77,10 +81,16 @@ cudaError_t launch_split_transpose(const float* src, long long lds, int K, int N
 // dst[r*ldd + c] = src[r*lds + c] for r < rows, c < cols
 cudaError_t launch_pad_copy(const float* src, long long lds, long long rows, long long cols,
                             float* dst, long long ldd, cudaStream_t s);
-// C[i*ldc + j] = sum_{s < splits} ws[s*split_stride + i*ldw + j], s ascending
+// v = sum_{s < splits} ws[s*split_stride + i*ldw + j], s ascending; then
+// C[i*ldc + j] = v, alpha v or alpha v + beta C (scale_mode 0, 1, 2)
 cudaError_t launch_splitk_reduce(const float* ws, long long split_stride, long long ldw,
                                  int splits, float* C, long long ldc, int M, int N,
-                                 cudaStream_t s);
+                                 float alpha, float beta, int scale_mode, cudaStream_t s);
+// dst[c*ldd + r] = src[r*lds + c] for r < rows, c < cols (a transposed copy)
+cudaError_t launch_transpose_pad(const float* src, long long lds, long long rows, long long cols,
+                                 float* dst, long long ldd, cudaStream_t s);
+// C[i*ldc + j] = beta C (or 0 when beta == 0) for i < M, j < N: the K = 0 case
+cudaError_t launch_scale_c(float* C, long long ldc, int M, int N, float beta, cudaStream_t s);
 // C[0 .. count) = 0
 cudaError_t launch_fill_zero(float* C, long long count, cudaStream_t s);
 // watchdog self-test: waits on a never-completed barrier for timeout_ns

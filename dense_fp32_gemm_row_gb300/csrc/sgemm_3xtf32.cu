@@ -38,6 +38,7 @@
 #include <cstdint>
 
 #include "device_sync.cuh"
+#include "epilogue.cuh"
 #include "gemm_internal.h"
 #include "tcgen05.cuh"
 
@@ -131,7 +132,8 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
                     const __grid_constant__ CUtensorMap tmBhi,
                     const __grid_constant__ CUtensorMap tmBlo, float* __restrict__ out,
                     long long ldo, long long split_stride, int M, int N, int K, int kb_per_split,
-                    int splits, int vec_store, unsigned* fault, long long timeout_ns) {
+                    int splits, int vec_store, unsigned* fault, long long timeout_ns,
+                    float alpha, float beta, int scale_mode) {
     using C = Cfg<BN, STAGES>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -312,16 +314,10 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
                 float* orow = out + static_cast<long long>(w.split) * split_stride +
                               static_cast<long long>(m) * ldo;
                 const int nb = w.n0 + col0;
-                if (vec_store && nb + EPI_COLS <= N) {
 #pragma unroll
-                    for (int j = 0; j < EPI_COLS; j += 4)
-                        *reinterpret_cast<float4*>(orow + nb + j) =
-                            make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < EPI_COLS; ++j)
-                        if (nb + j < N) orow[nb + j] = acc[j];
-                }
+                for (int j = 0; j < EPI_COLS; j += 4)
+                    store4(orow, nb + j, N, make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]),
+                           vec_store != 0, alpha, beta, scale_mode);
             }
         }
     }
@@ -351,7 +347,8 @@ cudaError_t launch_impl(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
     const int grid = units < sm_count ? units : sm_count;
     sgemm_3xtf32_kernel<BN, STAGES><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(
         a.tmAhi, a.tmAlo, a.tmBhi, a.tmBlo, a.out, a.ldo, a.split_stride, a.M, a.N, a.K,
-        a.kb_per_split, a.splits, a.vec_store, a.fault, a.timeout_ns);
+        a.kb_per_split, a.splits, a.vec_store, a.fault, a.timeout_ns, a.alpha, a.beta,
+        a.scale_mode);
     return cudaGetLastError();
 }
 
@@ -395,7 +392,7 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                          const __grid_constant__ CUtensorMap tmBlo, float* __restrict__ out,
                          long long ldo, long long split_stride, int M, int N, int K,
                          int kb_per_split, int splits, int vec_store, unsigned* fault,
-                         long long timeout_ns) {
+                         long long timeout_ns, float alpha, float beta, int scale_mode) {
     using C = PairCfg<STAGES>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -575,16 +572,10 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                 float* orow = out + static_cast<long long>(w.split) * split_stride +
                               static_cast<long long>(m) * ldo;
                 const int nb = w.n0 + col0;
-                if (vec_store && nb + EPI_COLS <= N) {
 #pragma unroll
-                    for (int j = 0; j < EPI_COLS; j += 4)
-                        *reinterpret_cast<float4*>(orow + nb + j) =
-                            make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < EPI_COLS; ++j)
-                        if (nb + j < N) orow[nb + j] = acc[j];
-                }
+                for (int j = 0; j < EPI_COLS; j += 4)
+                    store4(orow, nb + j, N, make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]),
+                           vec_store != 0, alpha, beta, scale_mode);
             }
         }
     }
@@ -634,7 +625,7 @@ cudaError_t launch_pair(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
     cfg.gridDim = dim3(2 * clusters);
     e = cudaLaunchKernelEx(&cfg, kern, a.tmAhi, a.tmAlo, a.tmBhi, a.tmBlo, a.out, a.ldo,
                            a.split_stride, a.M, a.N, a.K, a.kb_per_split, a.splits, a.vec_store,
-                           a.fault, a.timeout_ns);
+                           a.fault, a.timeout_ns, a.alpha, a.beta, a.scale_mode);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -40,6 +40,7 @@
 #include <cstdint>
 
 #include "device_sync.cuh"
+#include "epilogue.cuh"
 #include "gemm_internal.h"
 
 namespace gemm_f32_impl {
@@ -91,7 +92,8 @@ template <int G, int STAGES, int LAG, int MIN_BLOCKS, int ORDER>
 __global__ void __launch_bounds__(THREADS, MIN_BLOCKS)
 sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   float* __restrict__ out, long long ldo, long long split_stride, int M, int N,
-                  int K, int kb_per_split, int vec_store, unsigned* fault, long long timeout_ns) {
+                  int K, int kb_per_split, int vec_store, unsigned* fault, long long timeout_ns,
+                  float alpha, float beta, int scale_mode) {
     using V = FfmaVariant<G, STAGES, LAG, MIN_BLOCKS>;
     constexpr int BN = V::BN;
     extern __shared__ unsigned char smem_raw[];
@@ -282,15 +284,9 @@ sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         float* row = outp + static_cast<long long>(m) * ldo;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            const int n = n0 + b_off + 32 * g;
             const float* v = &acc[r][4 * g];
-            if (vec_store && n + 3 < N) {
-                *reinterpret_cast<float4*>(row + n) = make_float4(v[0], v[1], v[2], v[3]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (n + e < N) row[n + e] = v[e];
-            }
+            store4(row, n0 + b_off + 32 * g, N, make_float4(v[0], v[1], v[2], v[3]),
+                   vec_store != 0, alpha, beta, scale_mode);
         }
     }
 }
@@ -318,7 +314,7 @@ cudaError_t launch_variant(const FfmaArgs& a, cudaStream_t s) {
     dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(a.splits));
     kern<<<grid, THREADS, V::SMEM_BYTES, s>>>(a.tmA, a.tmB, a.out, a.ldo, a.split_stride, a.M, a.N,
                                               a.K, a.kb_per_split, a.vec_store, a.fault,
-                                              a.timeout_ns);
+                                              a.timeout_ns, a.alpha, a.beta, a.scale_mode);
     return cudaGetLastError();
 }
 

@@ -104,6 +104,29 @@ int gemm_f32_algo_splitk(const float* A, const float* B, float* C, int M, int N,
                          int algo, int splits, cudaStream_t stream);
 
 /*
+ * gemm_f32_ex -- the general row-major form
+ *
+ *     C = alpha * op(A) * op(B) + beta * C
+ *
+ * op(A) is M x K: element (i, k) is A[i*lda + k] (transa == 0, A stored
+ * M x K, lda >= K) or A[k*lda + i] (transa == 1, A stored K x M, lda >= M).
+ * op(B) is K x N: element (k, j) is B[k*ldb + j] (transb == 0, ldb >= N) or
+ * B[j*ldb + k] (transb == 1, B stored N x K, ldb >= K).  C[i][j] is
+ * C[i*ldc + j], ldc >= N.  Leading dimensions are in elements.  With
+ * beta == 0 the old C is not read (NaN or garbage there is harmless); with
+ * alpha == 0 or K == 0 A and B are not read and C = beta * C.  algo and
+ * splits as for gemm_f32_algo_splitk.  Operands that TMA cannot read in
+ * place (transposed for the CUDA-core kernel, or a row stride / base not
+ * 16-byte aligned) are first copied into the workspace.  The pages have only
+ * the packed alpha = 1, beta = 0 form; this is the same product with the
+ * interface a BLAS-style caller expects.  transa or transb other than 0 or
+ * 1, or a leading dimension below its minimum, is GEMM_F32_ERR_INVALID_VALUE.
+ */
+int gemm_f32_ex(int transa, int transb, int M, int N, int K, float alpha, const float* A,
+                long long lda, const float* B, long long ldb, float beta, float* C,
+                long long ldc, int algo, int splits, cudaStream_t stream);
+
+/*
  * gemm_f32_algo_splitk_ev -- as gemm_f32_algo_splitk, and, for profiling,
  * records `main_begin` on `stream` just before the main GEMM kernel is
  * launched and `main_end` just after it (either may be NULL).  The events

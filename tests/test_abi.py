@@ -110,3 +110,20 @@ def test_matmul_rejects_cpu_tensors(lib):
     torch = pytest.importorskip("torch")
     with pytest.raises(ValueError):
         g.matmul(torch.zeros(2, 3), torch.zeros(3, 4))
+
+
+def test_general_entry_validates_layout(lib):
+    A, B, C = FAKE_A, FAKE_B, FAKE_C
+    ex = g.gemm_f32_ex
+    # transpose flags must be 0 or 1
+    assert ex(2, 0, 4, 4, 4, 1.0, A, 4, B, 4, 0.0, C, 4) == g.ERR_INVALID_VALUE
+    # leading dimensions below their minimum
+    assert ex(0, 0, 4, 5, 6, 1.0, A, 5, B, 5, 0.0, C, 5) == g.ERR_INVALID_VALUE   # lda < K
+    assert ex(1, 0, 4, 5, 6, 1.0, A, 3, B, 5, 0.0, C, 5) == g.ERR_INVALID_VALUE   # lda < M
+    assert ex(0, 0, 4, 5, 6, 1.0, A, 6, B, 4, 0.0, C, 5) == g.ERR_INVALID_VALUE   # ldb < N
+    assert ex(0, 1, 4, 5, 6, 1.0, A, 6, B, 5, 0.0, C, 5) == g.ERR_INVALID_VALUE   # ldb < K
+    assert ex(0, 0, 4, 5, 6, 1.0, A, 6, B, 5, 0.0, C, 4) == g.ERR_INVALID_VALUE   # ldc < N
+    # C overlapping A through A's leading dimension
+    assert ex(0, 0, 4, 4, 4, 1.0, A, 1000, B, 4, 0.0, A + 4 * 2000, 4) == g.ERR_INVALID_VALUE
+    # empty output: success without a device
+    assert ex(0, 0, 0, 5, 6, 1.0, 0, 6, 0, 5, 0.0, 0, 5) == g.SUCCESS

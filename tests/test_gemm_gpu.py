@@ -231,3 +231,53 @@ def test_host_buffer_entry(shape, pinned):
         out = hC.numpy()
         assert np.isnan(out[M:]).all(), "write past C"
         _check(out[:M].copy(), oracle.ref_gemm(A, B), label=f"host {shape} {algo}")
+
+
+def _ex_case(M, N, K, ta, tb, pad, alpha, beta, algo, splits=0, c_nan=False):
+    t = _gpu.torch()
+    rng = np.random.default_rng(M * 7 + N * 5 + K * 3 + ta * 2 + tb)
+    lda = (M if ta else K) + pad
+    ldb = (K if tb else N) + pad
+    ldc = N + pad
+    a_rows = K if ta else M
+    b_rows = N if tb else K
+    A = rng.uniform(-1, 1, (a_rows, lda)).astype(np.float32)
+    B = rng.uniform(-1, 1, (b_rows, ldb)).astype(np.float32)
+    C0 = rng.uniform(-1, 1, (M, ldc)).astype(np.float32)
+    if c_nan:
+        C0[:, :N] = np.nan
+    want = oracle.ref_gemm_ex(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc).reshape(M, ldc)
+    a = t.from_numpy(A).cuda()
+    b = t.from_numpy(B).cuda()
+    c = t.from_numpy(C0).cuda()
+    s = t.cuda.current_stream()
+    st = g.gemm_f32_ex(ta, tb, M, N, K, alpha, a.data_ptr(), lda, b.data_ptr(), ldb, beta,
+                       c.data_ptr(), ldc, algo, splits, s.cuda_stream)
+    g.check(st, "gemm_f32_ex")
+    s.synchronize()
+    g.check(g.gemm_f32_device_status(1), "device status")
+    got = c.cpu().numpy()
+    assert np.array_equal(got[:, N:].view(np.uint32), C0[:, N:].view(np.uint32)), "write past N"
+    _check(got[:, :N].copy(), want[:, :N].copy(),
+           label=f"ex {M}x{N}x{K} ta{ta} tb{tb} pad{pad} a{alpha} b{beta} algo{algo} s{splits}")
+
+
+@pytest.mark.parametrize("algo", [g.ALGO_FFMA, g.ALGO_3XTF32], ids=["ffma", "3xtf32"])
+@pytest.mark.parametrize("ta,tb", [(0, 0), (1, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("pad", [0, 3, 8])
+def test_general_form_layouts(algo, ta, tb, pad):
+    _ex_case(300, 203, 150, ta, tb, pad, 1.0, 0.0, algo)
+    _ex_case(129, 257, 1000, ta, tb, pad, -1.25, 0.75, algo)
+
+
+@pytest.mark.parametrize("algo", [g.ALGO_FFMA, g.ALGO_3XTF32], ids=["ffma", "3xtf32"])
+def test_general_form_alpha_beta_rules(algo):
+    _ex_case(200, 160, 96, 0, 0, 4, 0.5, -2.0, algo)
+    _ex_case(200, 160, 96, 0, 0, 4, 2.0, 0.0, algo, c_nan=True)    # beta 0: C never read
+    _ex_case(200, 160, 96, 1, 1, 0, 0.0, 0.5, algo)                # alpha 0: C = beta C
+    _ex_case(200, 160, 0, 0, 0, 4, 1.0, 3.0, algo)                 # K 0: C = beta C
+    _ex_case(160, 200, 8209, 0, 1, 1, 0.25, 1.0, algo, splits=3)   # split-K applies alpha, beta
+
+
+def test_general_form_on_the_pair_kernel():
+    _ex_case(2304, 2304, 512, 1, 0, 4, -0.5, 1.5, g.ALGO_3XTF32)
