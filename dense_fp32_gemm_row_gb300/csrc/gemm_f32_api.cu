@@ -144,6 +144,8 @@ struct Plan {
     int bn = 0;
     int pair = 0;     // 3xTF32: two-CTA kernel
     int box_n = 0;    // 3xTF32: B^T rows per TMA box
+    int tail_tiles = 0, tail_splits = 0;  // pair kernel: K-split last partial round
+    size_t off_t = 0;
     int splits = 1;
     int kb_per_split = 0;
     int stage_a = 0, stage_b = 0;
@@ -312,8 +314,26 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     }
     if (p->splits > 1)
         p->off_w = carve(&off, static_cast<long long>(p->splits) * M * p->ldw * 4);
+    // The pair kernel's last round of tiles is usually only partly full
+    // (e.g. 1024 tiles over 76 clusters leave 36 for the 14th round).  Cut
+    // those tiles into T K shares (T * tail <= clusters) so that the last
+    // round takes 1/T of the time; a fix-up kernel adds the shares.
+    int clusters = 0;
+    if (p->pair && p->splits == 1 && splits == 0 &&
+        tf32x3_pair_clusters(d.sm_count, &clusters) == cudaSuccess && tiles > clusters) {
+        const int r = tiles % clusters;
+        int t = r ? clusters / r : 0;
+        if (t > 4) t = 4;
+        if (r && t >= 2 && kb_total >= 2 * t) {
+            p->tail_tiles = r;
+            p->tail_splits = t;
+            p->off_t = carve(&off, static_cast<long long>(r) * t * 256 * 256 * 4);
+            p->ctas = 2 * clusters;
+        }
+    }
+    cudaGetLastError();
     p->ws_bytes = off;
-    p->kernels = 1 + p->stage_a + p->stage_b + (p->splits > 1 ? 1 : 0);
+    p->kernels = 1 + p->stage_a + p->stage_b + (p->splits > 1 ? 1 : 0) + (p->tail_tiles ? 1 : 0);
 }
 
 // Device operands the GEMM kernel reads, after staging.
@@ -424,6 +444,9 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
         ta.alpha = alpha;
         ta.beta = beta;
         ta.scale_mode = kmode;
+        ta.tail_tiles = p.tail_tiles;
+        ta.tail_splits = p.tail_splits;
+        ta.tail_ws = p.tail_tiles ? reinterpret_cast<float*>(ws + p.off_t) : nullptr;
         if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
             return static_cast<int>(e);
         if ((e = launch_sgemm_3xtf32(ta, stream, d.sm_count)) != cudaSuccess)

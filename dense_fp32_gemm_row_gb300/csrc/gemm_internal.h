@@ -64,7 +64,14 @@ struct Tf32x3Args {
     long long timeout_ns;
     float alpha, beta;      // output scaling (epilogue.cuh modes)
     int scale_mode;
+    // pair kernel, splits == 1: the last tail_tiles tiles are cut into
+    // tail_splits K shares written to tail_ws (tail_tiles x tail_splits x
+    // 256 x 256 floats) and summed into C by a fix-up kernel
+    int tail_tiles, tail_splits;
+    float* tail_ws;
 };
+// co-resident two-CTA clusters of the pair kernel on the current device
+cudaError_t tf32x3_pair_clusters(int sm_count, int* clusters);
 // persistent grid: min(units, sm_count) CTAs, or for the pair kernel
 // 2 x min(units, co-resident clusters)
 cudaError_t launch_sgemm_3xtf32(const Tf32x3Args& a, cudaStream_t s, int sm_count);

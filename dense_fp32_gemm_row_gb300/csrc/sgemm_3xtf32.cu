@@ -50,7 +50,7 @@ using namespace gemm_f32_dev;
 constexpr int BM = 128;
 constexpr int BK = 32;      // one 128-byte swizzle row of tf32
 constexpr int UMMA_K = 8;   // K of one kind::tf32 MMA
-constexpr int CH = 2;       // K blocks per tensor-core chunk (64-deep K)
+constexpr int CH = 4;       // K blocks per tensor-core chunk (128-deep K)
 constexpr int EPI_COLS = 128;  // accumulator columns per epilogue thread
 constexpr int GROUP_M = 8;
 
@@ -73,6 +73,7 @@ struct Cfg {
 
 struct Unit {
     int m0, n0, split, kb_begin, nkb;
+    int slot;  // >= 0: a K share of a tail tile, written raw to the tail workspace
 };
 
 __device__ __forceinline__ Unit decode(int u, int tiles_m, int tiles_n, int kb_per_split,
@@ -90,6 +91,27 @@ __device__ __forceinline__ Unit decode(int u, int tiles_m, int tiles_n, int kb_p
     w.n0 = (within / rows_in_group) * bn;
     w.kb_begin = w.split * kb_per_split;
     w.nkb = max(0, min(kb_total, w.kb_begin + kb_per_split) - w.kb_begin);
+    w.slot = -1;
+    return w;
+}
+
+// Work units of the pair kernel.  Without a tail (tail_tiles == 0) they are
+// (tile, split) pairs as above.  With one, the last tail_tiles tiles of the
+// raster (what would otherwise be a partly idle last round of the persistent
+// grid) are each cut into tail_splits K ranges: unit full + t is share
+// t % tail_splits of tile full + t / tail_splits, and its raw sum goes to
+// slot t of the tail workspace, to be added up by the fix-up kernel.
+__device__ __forceinline__ Unit decode_pair(int u, int tiles_m, int tiles_n, int kb_per_split,
+                                            int kb_total, int bn, int tail_tiles,
+                                            int tail_splits) {
+    const int full = tiles_m * tiles_n - tail_tiles;
+    if (tail_tiles == 0 || u < full) return decode(u, tiles_m, tiles_n, kb_per_split, kb_total, bn, 2 * BM);
+    const int t = u - full;
+    Unit w = decode(full + t / tail_splits, tiles_m, tiles_n, kb_total, kb_total, bn, 2 * BM);
+    const int per = (kb_total + tail_splits - 1) / tail_splits;
+    w.kb_begin = (t % tail_splits) * per;
+    w.nkb = max(0, min(kb_total, w.kb_begin + per) - w.kb_begin);
+    w.slot = t;
     return w;
 }
 
@@ -392,7 +414,8 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                          const __grid_constant__ CUtensorMap tmBlo, float* __restrict__ out,
                          long long ldo, long long split_stride, int M, int N, int K,
                          int kb_per_split, int splits, int vec_store, unsigned* fault,
-                         long long timeout_ns, float alpha, float beta, int scale_mode) {
+                         long long timeout_ns, float alpha, float beta, int scale_mode,
+                         int tail_tiles, int tail_splits, float* __restrict__ tail_ws) {
     using C = PairCfg<STAGES>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -415,7 +438,8 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
     const int nclusters = gridDim.x >> 1;
     const int tiles_m = (M + 2 * BM - 1) / (2 * BM);
     const int tiles_n = (N + C::BN - 1) / C::BN;
-    const int units = tiles_m * tiles_n * splits;
+    const int units = tail_tiles ? tiles_m * tiles_n - tail_tiles + tail_tiles * tail_splits
+                                 : tiles_m * tiles_n * splits;
     const int kb_total = (K + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
@@ -450,7 +474,7 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
             int it = 0;
             bool ok = true;
             for (int u = cluster; u < units && ok; u += nclusters) {
-                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, 2 * BM);
+                const Unit w = decode_pair(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, tail_tiles, tail_splits);
                 const int ma = w.m0 + static_cast<int>(rank) * BM;
                 const int nb = w.n0 + static_cast<int>(rank) * C::HALF_N;
                 for (int kb = 0; kb < w.nkb; ++kb, ++it) {
@@ -484,7 +508,7 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
             int g = 0;
             bool ok = true;
             for (int u = cluster; u < units && ok; u += nclusters) {
-                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, 2 * BM);
+                const Unit w = decode_pair(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, tail_tiles, tail_splits);
                 for (int c0 = 0; c0 < w.nkb && ok; c0 += CH, ++g) {
                     const int buf = g & 1;
                     if (g >= 2 && !role_wait(acce0 + 8 * buf, ((g >> 1) & 1) ^ 1, timeout_ns, fault,
@@ -537,7 +561,7 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
         int g = 0;
         bool ok = true;
         for (int u = cluster; u < units && ok; u += nclusters) {
-            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, 2 * BM);
+            const Unit w = decode_pair(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, tail_tiles, tail_splits);
             for (int c0 = 0; c0 < w.nkb; c0 += CH, ++g) {
                 const int buf = g & 1;
                 const bool got = role_wait(accf0 + 8 * buf, (g >> 1) & 1, timeout_ns, fault,
@@ -567,6 +591,17 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                 if (lane == 0) mbar_arrive_cluster(map_to_cta(acce0 + 8 * buf, 0));
             }
             if (!ok) break;
+            if (w.slot >= 0) {
+                // a K share of a tail tile: the raw 256 x 256 sum, tile-local rows
+                float* trow = tail_ws + static_cast<long long>(w.slot) * (2 * BM * C::BN) +
+                              static_cast<long long>(static_cast<int>(rank) * BM + row) * C::BN;
+#pragma unroll
+                for (int j = 0; j < EPI_COLS; j += 4)
+                    store4(trow, col0 + j, C::BN,
+                           make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]), true, 1.0f,
+                           0.0f, kStorePlain);
+                continue;
+            }
             const int m = w.m0 + static_cast<int>(rank) * BM + row;
             if (m < M) {
                 float* orow = out + static_cast<long long>(w.split) * split_stride +
@@ -589,14 +624,68 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
     }
 }
 
+// Tail fix-up: C = sum of the tail_splits K shares of each tail tile, added
+// in share order (deterministic), then scaled like any other output.
+// One block per (tile, row), one thread per column.
+__global__ void __launch_bounds__(256)
+pair_tail_fixup_kernel(const float* __restrict__ tail_ws, int tiles_m, int tiles_n,
+                       int tail_tiles, int tail_splits, float* __restrict__ C, long long ldc, int M,
+                       int N, float alpha, float beta, int mode) {
+    constexpr int TM = 2 * BM, TN = PairCfg<3>::BN;
+    const int t = blockIdx.x;
+    const int i = blockIdx.y;
+    const int j = threadIdx.x;
+    const Unit w = decode(tiles_m * tiles_n - tail_tiles + t, tiles_m, tiles_n, 1, 1, TN, TM);
+    const int m = w.m0 + i, n = w.n0 + j;
+    if (m >= M || n >= N) return;
+    const float* src = tail_ws + static_cast<long long>(t) * tail_splits * TM * TN +
+                       static_cast<long long>(i) * TN + j;
+    float sum = src[0];
+    for (int p = 1; p < tail_splits; ++p) sum += src[static_cast<long long>(p) * TM * TN];
+    float* dst = C + static_cast<long long>(m) * ldc + n;
+    *dst = scale1(sum, dst, alpha, beta, mode);
+}
+
+// Co-resident clusters of the pair kernel on this device (cached per device).
+cudaError_t pair_clusters(int sm_count, int* out) {
+    using C = PairCfg<3>;
+    static thread_local int done_dev = -1;
+    static thread_local int clusters = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (done_dev != dev) {
+        auto kern = sgemm_3xtf32_pair_kernel<3>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * (sm_count / 2));
+        cfg.blockDim = dim3(C::THREADS);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        clusters = n;
+        done_dev = dev;
+    }
+    *out = clusters;
+    return cudaSuccess;
+}
+
 template <int STAGES>
 cudaError_t launch_pair(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
     using C = PairCfg<STAGES>;
     auto kern = sgemm_3xtf32_pair_kernel<STAGES>;
-    static thread_local int attr_done_dev = -1;
-    static thread_local int max_clusters = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    int max_clusters = 0;
+    cudaError_t e = pair_clusters(sm_count, &max_clusters);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -609,28 +698,33 @@ cudaError_t launch_pair(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (attr_done_dev != dev) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        cfg.gridDim = dim3(2 * (sm_count / 2));
-        int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        if (n < 1) return cudaErrorInvalidConfiguration;
-        max_clusters = n;
-        attr_done_dev = dev;
-    }
-    const int units = ((a.M + 2 * BM - 1) / (2 * BM)) * ((a.N + C::BN - 1) / C::BN) * a.splits;
+    const int tiles_m = (a.M + 2 * BM - 1) / (2 * BM);
+    const int tiles_n = (a.N + C::BN - 1) / C::BN;
+    const int units = a.tail_tiles
+                          ? tiles_m * tiles_n - a.tail_tiles + a.tail_tiles * a.tail_splits
+                          : tiles_m * tiles_n * a.splits;
     const int clusters = units < max_clusters ? units : max_clusters;
     cfg.gridDim = dim3(2 * clusters);
     e = cudaLaunchKernelEx(&cfg, kern, a.tmAhi, a.tmAlo, a.tmBhi, a.tmBlo, a.out, a.ldo,
                            a.split_stride, a.M, a.N, a.K, a.kb_per_split, a.splits, a.vec_store,
-                           a.fault, a.timeout_ns, a.alpha, a.beta, a.scale_mode);
+                           a.fault, a.timeout_ns, a.alpha, a.beta, a.scale_mode, a.tail_tiles,
+                           a.tail_splits, a.tail_ws);
     if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (a.tail_tiles) {
+        pair_tail_fixup_kernel<<<dim3(a.tail_tiles, 2 * BM), C::BN, 0, s>>>(
+            a.tail_ws, tiles_m, tiles_n, a.tail_tiles, a.tail_splits, a.out, a.ldo, a.M, a.N,
+            a.alpha, a.beta, a.scale_mode);
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 }  // namespace
+
+cudaError_t tf32x3_pair_clusters(int sm_count, int* clusters) {
+    return pair_clusters(sm_count, clusters);
+}
 
 Tf32x3Config tf32x3_config(int bn, bool pair) {
     if (pair) return {2 * BM, 256, BK, 3, PairCfg<3>::THREADS, PairCfg<3>::SMEM_BYTES, 1, 128};
