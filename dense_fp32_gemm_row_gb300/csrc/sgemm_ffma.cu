@@ -84,11 +84,9 @@ struct FfmaVariant {
     static_assert(BN <= 256, "TMA box");
 };
 
-// ORDER 0: for each A value, all 4G columns (the A register repeats in
-// consecutive FFMAs); ORDER 1: for each B value, all 8 rows (the B register
-// repeats); ORDER 2: as 0 with the accumulators held as column pairs and
-// updated by packed two-lane FMAs (the A value duplicated into both lanes).
-template <int G, int STAGES, int LAG, int MIN_BLOCKS, int ORDER>
+// Accumulators are held as column pairs and updated by packed two-lane FMAs,
+// the A value duplicated into both lanes.
+template <int G, int STAGES, int LAG, int MIN_BLOCKS>
 __global__ void __launch_bounds__(THREADS, MIN_BLOCKS)
 sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   float* __restrict__ out, long long ldo, long long split_stride, int M, int N,
@@ -150,15 +148,11 @@ sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
     }
 
-    float acc[8][4 * G];
-    uint64_t acc2[8][2 * G];  // ORDER 2: column pairs (j, j+1)
+    uint64_t acc2[8][2 * G];  // column pairs (2p, 2p+1) of each of the 8 rows
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-#pragma unroll
-        for (int j = 0; j < 4 * G; ++j) acc[r][j] = 0.0f;
+    for (int r = 0; r < 8; ++r)
 #pragma unroll
         for (int j = 0; j < 2 * G; ++j) acc2[r][j] = 0ull;
-    }
 
     const float* smemf = reinterpret_cast<const float*>(smem);
     const int a_off = (wm * 32 + tm) * BK;      // row wm*32+tm; row r of the thread is +4r
@@ -206,53 +200,19 @@ sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             for (int r = 0; r < 8; ++r)
                 a[r] = *reinterpret_cast<const float4*>(As + a_off + r * 4 * BK +
                                                         ((r & 1) ? xo : xe));
-            if constexpr (ORDER == 2) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint64_t bp[2 * G];
-#pragma unroll
-                    for (int g = 0; g < G; ++g)
-                        lds_v2_b64(smem_addr(Bs + (c * 4 + q) * BN + b_off + 32 * g), bp[2 * g],
-                                   bp[2 * g + 1]);
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        const float av = q == 0 ? a[r].x : q == 1 ? a[r].y : q == 2 ? a[r].z : a[r].w;
-                        const uint64_t ad = pack2(av, av);
-#pragma unroll
-                        for (int p = 0; p < 2 * G; ++p) ffma2(acc2[r][p], ad, bp[p]);
-                    }
-                }
-                continue;
-            }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                float4 b[G];
+                uint64_t bp[2 * G];
 #pragma unroll
                 for (int g = 0; g < G; ++g)
-                    b[g] = *reinterpret_cast<const float4*>(Bs + (c * 4 + q) * BN + b_off + 32 * g);
-                if constexpr (ORDER == 0) {
+                    lds_v2_b64(smem_addr(Bs + (c * 4 + q) * BN + b_off + 32 * g), bp[2 * g],
+                               bp[2 * g + 1]);
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        const float av = q == 0 ? a[r].x : q == 1 ? a[r].y : q == 2 ? a[r].z : a[r].w;
+                for (int r = 0; r < 8; ++r) {
+                    const float av = q == 0 ? a[r].x : q == 1 ? a[r].y : q == 2 ? a[r].z : a[r].w;
+                    const uint64_t ad = pack2(av, av);
 #pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            acc[r][4 * g + 0] = fmaf(av, b[g].x, acc[r][4 * g + 0]);
-                            acc[r][4 * g + 1] = fmaf(av, b[g].y, acc[r][4 * g + 1]);
-                            acc[r][4 * g + 2] = fmaf(av, b[g].z, acc[r][4 * g + 2]);
-                            acc[r][4 * g + 3] = fmaf(av, b[g].w, acc[r][4 * g + 3]);
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 4 * G; ++j) {
-                        const float4 bg = b[j >> 2];
-                        const float bv = (j & 3) == 0 ? bg.x : (j & 3) == 1 ? bg.y : (j & 3) == 2 ? bg.z : bg.w;
-#pragma unroll
-                        for (int r = 0; r < 8; ++r) {
-                            const float av = q == 0 ? a[r].x : q == 1 ? a[r].y : q == 2 ? a[r].z : a[r].w;
-                            acc[r][j] = fmaf(av, bv, acc[r][j]);
-                        }
-                    }
+                    for (int p = 0; p < 2 * G; ++p) ffma2(acc2[r][p], ad, bp[p]);
                 }
             }
         }
@@ -270,12 +230,11 @@ sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         return;
     }
 
-    if constexpr (ORDER == 2) {
+    float acc[8][4 * G];
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
+    for (int r = 0; r < 8; ++r)
 #pragma unroll
-            for (int p = 0; p < 2 * G; ++p) unpack2(acc2[r][p], acc[r][2 * p], acc[r][2 * p + 1]);
-    }
+        for (int p = 0; p < 2 * G; ++p) unpack2(acc2[r][p], acc[r][2 * p], acc[r][2 * p + 1]);
     float* outp = out + static_cast<long long>(blockIdx.y) * split_stride;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
@@ -295,10 +254,10 @@ sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 using Narrow = FfmaVariant<2, 3, 1, 2>;  // 128 x 128 tiles, 2 CTAs / SM
 using Wide = FfmaVariant<4, 4, 2, 1>;    // 128 x 256 tiles, 1 CTA / SM
 
-template <int G, int STAGES, int LAG, int MIN_BLOCKS, int ORDER>
+template <int G, int STAGES, int LAG, int MIN_BLOCKS>
 cudaError_t launch_variant(const FfmaArgs& a, cudaStream_t s) {
     using V = FfmaVariant<G, STAGES, LAG, MIN_BLOCKS>;
-    auto kern = sgemm_ffma_kernel<G, STAGES, LAG, MIN_BLOCKS, ORDER>;
+    auto kern = sgemm_ffma_kernel<G, STAGES, LAG, MIN_BLOCKS>;
     // the kernel's stage layout and transaction count assume this box width
     if (a.bn != V::BN) return cudaErrorInvalidValue;
     static thread_local int attr_done_dev = -1;
@@ -327,8 +286,8 @@ FfmaConfig ffma_config(int variant) {
 }
 
 cudaError_t launch_sgemm_ffma(const FfmaArgs& a, cudaStream_t s) {
-    if (a.variant == 1) return launch_variant<4, 4, 2, 1, 2>(a, s);
-    return launch_variant<2, 3, 1, 2, 2>(a, s);
+    if (a.variant == 1) return launch_variant<4, 4, 2, 1>(a, s);
+    return launch_variant<2, 3, 1, 2>(a, s);
 }
 
 }  // namespace gemm_f32_impl
