@@ -487,13 +487,14 @@ def run_curve(args) -> int:
     `--steps` calls (L2 flushed between calls below 256 MiB of inputs),
     TFLOP/s, compulsory bytes 4(MK + KN + MN), arithmetic intensity, the
     bandwidth those bytes imply, the fraction of the kernel's roofline, and a
-    check of 512 sampled outputs against the CPU oracle.
+    cross-check of every output against cuBLAS SGEMM within 1e-3 + 1e-3 |ref|
+    (the report program's GPU-against-GPU check; parity against the CPU
+    oracle is the test suite's job).
     """
     import numpy as np
     import torch
 
     import dense_fp32_gemm_row_gb300 as g
-    import oracle
     from seeded_inputs import make_workload
 
     g.load()
@@ -505,7 +506,7 @@ def run_curve(args) -> int:
     peak_ffma = props.multi_processor_count * FFMA_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
     peak_3x = float(peaks.get("bf16_tflops", 1900.0)) * NOMINAL_TF32_TFLOPS / NOMINAL_BF16_TFLOPS / 3
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    print("kernel,size,ms,tflops,bytes_gb,ai,bw_gbs,pct_roofline,check", flush=True)
+    print("kernel,size,ms,tflops,bytes_gb,ai,bw_gbs,pct_roofline,xcheck_cublas", flush=True)
     sizes = [int(x) for x in args.curve_sizes.split(",")]
     for n in sizes:
         A_np, B_np = make_workload(2, M=n, N=n, K=n)
@@ -513,9 +514,10 @@ def run_curve(args) -> int:
         b = torch.from_numpy(B_np).to(dev)
         c = torch.empty((n, n), dtype=torch.float32, device=dev)
         big = 8 * n * n >= 256 * 1024 * 1024
-        rng = np.random.default_rng(n)
-        rows, cols = rng.integers(0, n, 512), rng.integers(0, n, 512)
-        want = oracle.ref_gemm_entries(A_np, B_np, rows, cols)
+        prev = torch.backends.cuda.matmul.allow_tf32
+        torch.backends.cuda.matmul.allow_tf32 = False
+        ref = torch.matmul(a, b)
+        torch.backends.cuda.matmul.allow_tf32 = prev
         flops = 2.0 * n ** 3
         bytes_ = 4.0 * 3 * n * n
         for name in ("ffma", "3xtf32", "cublas"):
@@ -548,8 +550,7 @@ def run_curve(args) -> int:
                 torch.backends.cuda.matmul.allow_tf32 = prev
             ms = statistics.median(times)
             tf = flops / (ms * 1e-3) / 1e12
-            got = c.cpu().numpy()[rows, cols]
-            ok = oracle.compare(got, want)["pass"]
+            ok = bool(((c - ref).abs() <= 1e-3 + 1e-3 * ref.abs()).all().item())
             peak = {"ffma": peak_ffma, "3xtf32": peak_3x, "cublas": peak_ffma}[name]
             print(f"{name},{n},{ms:.4f},{tf:.2f},{bytes_ / 1e9:.4f},{flops / bytes_:.1f},"
                   f"{bytes_ / (ms * 1e-3) / 1e9:.1f},{100 * tf / peak:.1f},"

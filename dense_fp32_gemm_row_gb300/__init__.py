@@ -29,6 +29,8 @@ __all__ = [
     "ERR_DEVICE_TIMEOUT", "ERR_DESCRIPTOR", "GemmError",
     "library_path", "load", "gemm_f32", "gemm_f32_algo", "gemm_f32_algo_splitk",
     "gemm_f32_algo_splitk_ev", "gemm_f32_noalloc", "gemm_f32_host", "gemm_f32_ex",
+    "gemm_f32_configured", "gemm_f32_plan_config", "Config", "TILE_AUTO", "TILE_128x128",
+    "TILE_128x256", "TILE_256x256_PAIR",
     "gemm_f32_plan", "gemm_f32_device_status", "gemm_f32_selftest_watchdog",
     "gemm_f32_release", "gemm_f32_status_string", "gemm_f32_version", "matmul", "check",
 ]
@@ -58,6 +60,16 @@ class GemmError(RuntimeError):
     def __init__(self, status: int, where: str = ""):
         self.status = status
         super().__init__(f"{where}: status {status} ({gemm_f32_status_string(status)})")
+
+
+TILE_AUTO = 0
+TILE_128x128 = 1
+TILE_128x256 = 2
+TILE_256x256_PAIR = 3
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("algo", ctypes.c_int), ("tile", ctypes.c_int), ("splits", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -95,6 +107,9 @@ def load():
         lib.gemm_f32_plan.argtypes = [i, i, i, i, i, vp, vp, vp, ctypes.POINTER(PlanInfo)]
         lib.gemm_f32_noalloc.argtypes = [vp, vp, vp, i, i, i, i, vp]
         lib.gemm_f32_host.argtypes = [vp, vp, vp, i, i, i, i, vp]
+        lib.gemm_f32_configured.argtypes = [vp, vp, vp, i, i, i, ctypes.POINTER(Config), vp]
+        lib.gemm_f32_plan_config.argtypes = [i, i, i, ctypes.POINTER(Config), vp, vp, vp,
+                                             ctypes.POINTER(PlanInfo)]
         f = ctypes.c_float
         lib.gemm_f32_ex.argtypes = [i, i, i, i, i, f, vp, ll, vp, ll, f, vp, ll, i, i, vp]
         lib.gemm_f32_device_status.argtypes = [i]
@@ -104,7 +119,8 @@ def load():
         lib.gemm_f32_status_string.restype = ctypes.c_char_p
         lib.gemm_f32_version.argtypes = []
         for name in ("gemm_f32", "gemm_f32_algo", "gemm_f32_algo_splitk",
-                     "gemm_f32_algo_splitk_ev", "gemm_f32_noalloc", "gemm_f32_host", "gemm_f32_ex", "gemm_f32_plan", "gemm_f32_noalloc",
+                     "gemm_f32_algo_splitk_ev", "gemm_f32_plan", "gemm_f32_noalloc",
+                     "gemm_f32_host", "gemm_f32_ex", "gemm_f32_configured", "gemm_f32_plan_config",
                      "gemm_f32_device_status", "gemm_f32_selftest_watchdog", "gemm_f32_release",
                      "gemm_f32_version"):
             getattr(lib, name).restype = ctypes.c_int
@@ -141,6 +157,20 @@ def gemm_f32_ex(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, al
     return load().gemm_f32_ex(int(transa), int(transb), M, N, K, float(alpha), _p(A), int(lda),
                               _p(B), int(ldb), float(beta), _p(C), int(ldc), int(algo),
                               int(splits), _p(stream))
+
+
+def gemm_f32_configured(A, B, C, M, N, K, algo, tile=TILE_AUTO, splits=0, stream=0) -> int:
+    """C = A @ B with a forced kernel configuration (algorithm, tile, split-K)."""
+    cfg = Config(int(algo), int(tile), int(splits))
+    return load().gemm_f32_configured(_p(A), _p(B), _p(C), M, N, K, ctypes.byref(cfg), _p(stream))
+
+
+def gemm_f32_plan_config(M, N, K, algo, tile=TILE_AUTO, splits=0, A=0, B=0, C=0):
+    cfg = Config(int(algo), int(tile), int(splits))
+    info = PlanInfo()
+    st = load().gemm_f32_plan_config(M, N, K, ctypes.byref(cfg), _p(A), _p(B), _p(C),
+                                     ctypes.byref(info))
+    return st, info.as_dict()
 
 
 def gemm_f32_host(A, B, C, M, N, K, algo=ALGO_AUTO, stream=0) -> int:

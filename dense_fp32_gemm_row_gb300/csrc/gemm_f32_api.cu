@@ -223,13 +223,13 @@ int validate(const Problem& q, int algo, int splits, bool need_ptrs = true) {
 
 // Split-K factor: spread a grid that would fill less than half of the
 // concurrent CTA slots over disjoint K ranges, keeping >= 4 K blocks each.
-int choose_splits(int requested, int tiles, int kb_total, int slots) {
+int choose_splits(int requested, int tiles, int kb_total, int slots, int min_kb = 4) {
     int s = requested;
     if (s == 0) {
         s = 1;
         if (tiles * 2 <= slots) {
             s = slots / tiles;
-            const int max_by_depth = kb_total / 4;
+            const int max_by_depth = kb_total / min_kb;
             if (s > max_by_depth) s = max_by_depth;
             if (s > GEMM_F32_MAX_SPLITS) s = GEMM_F32_MAX_SPLITS;
             if (s < 1) s = 1;
@@ -246,18 +246,31 @@ size_t carve(size_t* off, long long bytes) {
     return at;
 }
 
-void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Plan* p) {
+void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Plan* p,
+               int tile = GEMM_F32_TILE_AUTO) {
     const int M = q.M, N = q.N, K = q.K;
-    p->algo = (algo == GEMM_F32_ALGO_AUTO) ? GEMM_F32_ALGO_3XTF32 : algo;
+    // AUTO: the tensor-core kernel, except for tiny problems (under about
+    // 2.7e8 multiply-adds, e.g. 512^3), where the CUDA-core kernel's single
+    // launch beats the three of the tensor-core path (design-space sweep:
+    // 19.1 vs 26.2 us at 512^3)
+    const double macs = static_cast<double>(M) * N * K;
+    p->algo = algo != GEMM_F32_ALGO_AUTO ? algo
+              : macs < 2.7e8             ? GEMM_F32_ALGO_FFMA
+                                         : GEMM_F32_ALGO_3XTF32;
     int bm, bn, bk, slots;
     if (p->algo == GEMM_F32_ALGO_3XTF32) {
         // the two-CTA 256 x 256 kernel when its tiles fill every SM pair;
-        // otherwise one CTA per 128 x 256 tile, or 128 x 128 for narrow or
-        // small outputs
+        // otherwise one CTA per 128 x 256 tile when those fill at least three
+        // quarters of the SMs (2048^3: 100 vs 105 us for 128 x 128), else
+        // 128 x 128 tiles with split-K
         const int units_pair = ((M + 255) / 256) * ((N + 255) / 256);
         const int tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
         p->pair = units_pair >= d.sm_count / 2 ? 1 : 0;
-        p->bn = (p->pair || (tiles256 >= d.sm_count && N > 128)) ? 256 : 128;
+        p->bn = (p->pair || (4 * tiles256 >= 3 * d.sm_count && N > 128)) ? 256 : 128;
+        if (tile != GEMM_F32_TILE_AUTO) {
+            p->pair = tile == GEMM_F32_TILE_256x256_PAIR;
+            p->bn = tile == GEMM_F32_TILE_128x128 ? 128 : 256;
+        }
         const Tf32x3Config tc = tf32x3_config(p->bn, p->pair != 0);
         bm = tc.bm;
         bn = tc.bn;
@@ -269,6 +282,7 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         // wide tiles (8 x 16 per thread) once they fill every SM, else 128 x 128
         const int tiles_wide = ((M + 127) / 128) * ((N + 255) / 256);
         p->variant = tiles_wide >= d.sm_count ? 1 : 0;
+        if (tile != GEMM_F32_TILE_AUTO) p->variant = tile == GEMM_F32_TILE_128x256 ? 1 : 0;
         const FfmaConfig fc = ffma_config(p->variant);
         bm = fc.bm;
         bn = fc.bn;
@@ -282,7 +296,10 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     p->tile_k = bk;
     const int tiles = ((M + bm - 1) / bm) * ((N + bn - 1) / bn);
     const int kb_total = (K + bk - 1) / bk;
-    const int s = choose_splits(splits, tiles, kb_total, slots);
+    // the CUDA-core kernel keeps >= 2 K blocks a split (512^3: 8 splits,
+    // 19.1 us, against 25.2 us with 4); the tensor-core kernels >= 4
+    const int s = choose_splits(splits, tiles, kb_total, slots,
+                                p->algo == GEMM_F32_ALGO_FFMA ? 2 : 4);
     p->kb_per_split = (kb_total + s - 1) / s;
     p->splits = (kb_total + p->kb_per_split - 1) / p->kb_per_split;
     const int units = tiles * p->splits;
@@ -492,7 +509,8 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
 }
 
 int run(const Problem& q, int algo, int splits, cudaStream_t stream,
-        cudaEvent_t ev_begin = nullptr, cudaEvent_t ev_end = nullptr) {
+        cudaEvent_t ev_begin = nullptr, cudaEvent_t ev_end = nullptr,
+        int tile = GEMM_F32_TILE_AUTO) {
     int st = validate(q, algo, splits);
     if (st != GEMM_F32_SUCCESS) return st;
     if (q.M == 0 || q.N == 0) return GEMM_F32_SUCCESS;
@@ -513,7 +531,7 @@ int run(const Problem& q, int algo, int splits, cudaStream_t stream,
     if (st != GEMM_F32_SUCCESS) return st;
 
     Plan p;
-    make_plan(*d, q, algo, splits, &p);
+    make_plan(*d, q, algo, splits, &p, tile);
 
     unsigned char* ws = nullptr;
     if (p.ws_bytes) {
@@ -669,6 +687,18 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
     return GEMM_F32_SUCCESS;
 }
 
+// A forced configuration: tile id within range and valid for the algorithm.
+int check_config(const gemm_f32_config* cfg) {
+    if (!cfg) return GEMM_F32_ERR_INVALID_VALUE;
+    if (cfg->tile < GEMM_F32_TILE_AUTO || cfg->tile > GEMM_F32_TILE_256x256_PAIR)
+        return GEMM_F32_ERR_INVALID_VALUE;
+    if (cfg->tile == GEMM_F32_TILE_256x256_PAIR && cfg->algo == GEMM_F32_ALGO_FFMA)
+        return GEMM_F32_ERR_INVALID_VALUE;
+    if (cfg->tile != GEMM_F32_TILE_AUTO && cfg->algo == GEMM_F32_ALGO_AUTO)
+        return GEMM_F32_ERR_INVALID_VALUE;  // a tile names one algorithm's kernels
+    return GEMM_F32_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -713,18 +743,28 @@ int gemm_f32_algo_splitk_ev(const float* A, const float* B, float* C, int M, int
     return run(packed(A, B, C, M, N, K), algo, splits, stream, main_begin, main_end);
 }
 
+int gemm_f32_configured(const float* A, const float* B, float* C, int M, int N, int K,
+                        const gemm_f32_config* cfg, cudaStream_t stream) {
+    const int st = check_config(cfg);
+    if (st != GEMM_F32_SUCCESS) return st;
+    return run(packed(A, B, C, M, N, K), cfg->algo, cfg->splits, stream, nullptr, nullptr,
+               cfg->tile);
+}
+
 int gemm_f32_host(const float* A, const float* B, float* C, int M, int N, int K, int algo,
                   cudaStream_t stream) {
     return run_host(A, B, C, M, N, K, algo, stream);
 }
 
-int gemm_f32_plan(int M, int N, int K, int algo, int splits, const float* A, const float* B,
-                  const float* C, gemm_f32_plan_info* out) {
+int gemm_f32_plan_config(int M, int N, int K, const gemm_f32_config* cfg, const float* A,
+                         const float* B, const float* C, gemm_f32_plan_info* out) {
     if (!out) return GEMM_F32_ERR_INVALID_VALUE;
     std::memset(out, 0, sizeof(*out));
+    int st = check_config(cfg);
+    if (st != GEMM_F32_SUCCESS) return st;
     // pointers are optional here: they only decide the alignment staging
     const Problem q = packed(A, B, const_cast<float*>(C), M, N, K);
-    int st = validate(q, algo, splits, false);
+    st = validate(q, cfg->algo, cfg->splits, false);
     if (st != GEMM_F32_SUCCESS) return st;
     out->splits = 1;
     if (M == 0 || N == 0) return GEMM_F32_SUCCESS;
@@ -738,7 +778,7 @@ int gemm_f32_plan(int M, int N, int K, int algo, int splits, const float* A, con
         return GEMM_F32_SUCCESS;
     }
     Plan p;
-    make_plan(*d, q, algo, splits, &p);
+    make_plan(*d, q, cfg->algo, cfg->splits, &p, cfg->tile);
     out->algo = p.algo;
     out->splits = p.splits;
     out->tile_m = p.tile_m;
@@ -751,6 +791,15 @@ int gemm_f32_plan(int M, int N, int K, int algo, int splits, const float* A, con
     out->kernels = p.kernels;
     out->workspace_bytes = static_cast<long long>(p.ws_bytes);
     return GEMM_F32_SUCCESS;
+}
+
+int gemm_f32_plan(int M, int N, int K, int algo, int splits, const float* A, const float* B,
+                  const float* C, gemm_f32_plan_info* out) {
+    gemm_f32_config cfg;
+    cfg.algo = algo;
+    cfg.tile = GEMM_F32_TILE_AUTO;
+    cfg.splits = splits;
+    return gemm_f32_plan_config(M, N, K, &cfg, A, B, C, out);
 }
 
 int gemm_f32_device_status(int clear) {

@@ -63,7 +63,8 @@ extern "C" {
 #define GEMM_F32_ERR_DESCRIPTOR         (-5)
 
 /* ---- algorithms -------------------------------------------------------- */
-/* Choose by shape: currently the tensor-core 3xTF32 kernel for every shape. */
+/* Choose by shape: the tensor-core 3xTF32 kernels, except the CUDA-core
+ * kernel for tiny problems (under about 2.7e8 multiply-adds). */
 #define GEMM_F32_ALGO_AUTO    0
 /* CUDA-core FFMA kernel: TMA-fed, swizzled shared-memory tiles, mbarrier
  * pipeline, 8x8 register tile per thread. */
@@ -174,6 +175,33 @@ typedef struct gemm_f32_plan_info {
 int gemm_f32_plan(int M, int N, int K, int algo, int splits,
                   const float* A, const float* B, const float* C,
                   gemm_f32_plan_info* out);
+
+/*
+ * gemm_f32_config / gemm_f32_configured / gemm_f32_plan_config -- run (or
+ * plan) C = A * B with a forced kernel configuration instead of the
+ * library's choice: the tool behind design-space sweeps ("Lecture 12: final
+ * project", the sweep program: try every configuration, check it, time it,
+ * rank it).  Arguments as for gemm_f32; the config fields:
+ *   algo    GEMM_F32_ALGO_FFMA or _3XTF32 (AUTO only with tile = AUTO)
+ *   tile    GEMM_F32_TILE_* below; 0 lets the library choose
+ *   splits  as for gemm_f32_algo_splitk (0 = choose)
+ * The 256 x 256 CTA-pair tile exists for 3XTF32 only.  Invalid combinations
+ * return GEMM_F32_ERR_INVALID_VALUE.
+ */
+#define GEMM_F32_TILE_AUTO          0
+#define GEMM_F32_TILE_128x128       1
+#define GEMM_F32_TILE_128x256       2
+#define GEMM_F32_TILE_256x256_PAIR  3
+typedef struct gemm_f32_config {
+    int algo;
+    int tile;
+    int splits;
+} gemm_f32_config;
+
+int gemm_f32_configured(const float* A, const float* B, float* C, int M, int N, int K,
+                        const gemm_f32_config* cfg, cudaStream_t stream);
+int gemm_f32_plan_config(int M, int N, int K, const gemm_f32_config* cfg, const float* A,
+                         const float* B, const float* C, gemm_f32_plan_info* out);
 
 /*
  * gemm_f32_device_status -- read (and with clear != 0, reset) the device

@@ -282,3 +282,38 @@ def test_general_form_alpha_beta_rules(algo):
 
 def test_general_form_on_the_pair_kernel():
     _ex_case(2304, 2304, 512, 1, 0, 4, -0.5, 1.5, g.ALGO_3XTF32)
+
+
+@pytest.mark.parametrize("algo,tile", [(g.ALGO_FFMA, g.TILE_128x128), (g.ALGO_FFMA, g.TILE_128x256),
+                                       (g.ALGO_3XTF32, g.TILE_128x128),
+                                       (g.ALGO_3XTF32, g.TILE_128x256),
+                                       (g.ALGO_3XTF32, g.TILE_256x256_PAIR)],
+                         ids=["ffma-128", "ffma-256", "3x-128", "3x-256", "3x-pair"])
+@pytest.mark.parametrize("splits", [1, 5])
+def test_forced_configurations(algo, tile, splits):
+    t = _gpu.torch()
+    M, N, K = 333, 517, 1100
+    A, B = make_workload(1, M=M, N=N, K=K)
+    st, p = g.gemm_f32_plan_config(M, N, K, algo, tile, splits, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["algo"] == algo and p["splits"] == splits
+    want_tile = {g.TILE_128x128: (128, 128), g.TILE_128x256: (128, 256),
+                 g.TILE_256x256_PAIR: (256, 256)}[tile]
+    assert (p["tile_m"], p["tile_n"]) == want_tile
+    a = t.from_numpy(A).cuda()
+    b = t.from_numpy(B).cuda()
+    c = t.full((M, N), float("nan"), device="cuda")
+    s = t.cuda.current_stream()
+    g.check(g.gemm_f32_configured(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, algo, tile,
+                                  splits, s.cuda_stream), "configured")
+    s.synchronize()
+    g.check(g.gemm_f32_device_status(1), "device status")
+    _check(c.cpu().numpy(), oracle.ref_gemm(A, B), label=f"config {algo}/{tile}/{splits}")
+
+
+def test_invalid_configurations_are_refused():
+    fa, fb, fc = 1 << 32, 1 << 36, 1 << 40
+    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_FFMA, g.TILE_256x256_PAIR, 0) == \
+        g.ERR_INVALID_VALUE
+    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_AUTO, g.TILE_128x128, 0) == \
+        g.ERR_INVALID_VALUE
+    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_3XTF32, 7, 0) == g.ERR_INVALID_VALUE
