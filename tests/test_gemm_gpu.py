@@ -317,3 +317,36 @@ def test_invalid_configurations_are_refused():
     assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_AUTO, g.TILE_128x128, 0) == \
         g.ERR_INVALID_VALUE
     assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_3XTF32, 7, 0) == g.ERR_INVALID_VALUE
+
+
+@pytest.mark.parametrize("algo", [g.ALGO_FFMA, g.ALGO_3XTF32], ids=["ffma", "3xtf32"])
+def test_output_beyond_2_31_elements(algo):
+    # C has 65600 x 33000 = 2.16e9 elements (8.7 GB): row offsets overflow
+    # 32 bits, so every store path must index in 64 bits
+    t = _gpu.torch()
+    M, N, K = 65600, 33000, 36
+    A, B = make_workload(1, M=M, N=N, K=K)
+    a = t.from_numpy(A).cuda()
+    b = t.from_numpy(B).cuda()
+    c = t.empty((M, N), device="cuda")
+    s = t.cuda.current_stream()
+    g.check(g.gemm_f32_algo(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, algo,
+                            s.cuda_stream), "big output")
+    s.synchronize()
+    g.check(g.gemm_f32_device_status(1), "device status")
+    rng = np.random.default_rng(11)
+    rows = np.concatenate([rng.integers(0, M, 3000), [M - 1, M - 1, 0, 65536]])
+    cols = np.concatenate([rng.integers(0, N, 3000), [N - 1, 0, N - 1, 32767]])
+    got = c[t.from_numpy(rows).cuda(), t.from_numpy(cols).cuda()].cpu().numpy()
+    _check(got, oracle.ref_gemm_entries(A, B, rows, cols), label=f"big output {algo}")
+    del c
+
+
+@pytest.mark.parametrize("algo", [g.ALGO_FFMA, g.ALGO_3XTF32], ids=["ffma", "3xtf32"])
+def test_million_deep_k(algo):
+    M, N, K = 130, 70, 1 << 20
+    A, B = make_workload(4, M=M, N=N, K=K)
+    C = _gpu.run(A, B, algo)
+    rng = np.random.default_rng(12)
+    rows, cols = rng.integers(0, M, 600), rng.integers(0, N, 600)
+    _check(C[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols), label=f"K=2^20 {algo}")
