@@ -508,26 +508,16 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
     return GEMM_F32_SUCCESS;
 }
 
-int run(const Problem& q, int algo, int splits, cudaStream_t stream,
-        cudaEvent_t ev_begin = nullptr, cudaEvent_t ev_end = nullptr,
-        int tile = GEMM_F32_TILE_AUTO) {
-    int st = validate(q, algo, splits);
-    if (st != GEMM_F32_SUCCESS) return st;
+// Enqueue one GEMM on `stream` (validated problem, g_mutex held, device known).
+int enqueue(const Problem& q, int algo, int splits, DeviceState* d, int dev, cudaStream_t stream,
+            cudaEvent_t ev_begin, cudaEvent_t ev_end, int tile) {
     if (q.M == 0 || q.N == 0) return GEMM_F32_SUCCESS;
-
-    std::lock_guard<std::mutex> lock(g_mutex);
-    DeviceState* d = nullptr;
-    int dev = 0;
-    st = device_state(&d, &dev);
-    if (st != GEMM_F32_SUCCESS) return st;
-
     if (q.K == 0 || q.alpha == 0.0f) {
         // empty sum (or a zero multiplier): C = beta C, A and B not read
         cudaError_t e = launch_scale_c(q.C, q.ldc, q.M, q.N, q.beta, stream);
         return e == cudaSuccess ? GEMM_F32_SUCCESS : static_cast<int>(e);
     }
-
-    st = get_encoder();
+    int st = get_encoder();
     if (st != GEMM_F32_SUCCESS) return st;
 
     Plan p;
@@ -545,6 +535,21 @@ int run(const Problem& q, int algo, int splits, cudaStream_t stream,
     if ((st = stage_b(p, q, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
     return launch_gemm(p, *d, o, q.C, q.ldc, q.M, q.N, q.K, q.alpha, q.beta, scale_mode(q), ws,
                        stream, ev_begin, ev_end);
+}
+
+int run(const Problem& q, int algo, int splits, cudaStream_t stream,
+        cudaEvent_t ev_begin = nullptr, cudaEvent_t ev_end = nullptr,
+        int tile = GEMM_F32_TILE_AUTO) {
+    int st = validate(q, algo, splits);
+    if (st != GEMM_F32_SUCCESS) return st;
+    if (q.M == 0 || q.N == 0) return GEMM_F32_SUCCESS;
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* d = nullptr;
+    int dev = 0;
+    st = device_state(&d, &dev);
+    if (st != GEMM_F32_SUCCESS) return st;
+    return enqueue(q, algo, splits, d, dev, stream, ev_begin, ev_end, tile);
 }
 
 // ---- host-buffer entry: copies overlapped with the GEMM, by row panels ----
@@ -595,6 +600,68 @@ int host_pipe(int dev, cudaStream_t stream, size_t bytes, HostPipe** out) {
     return GEMM_F32_SUCCESS;
 }
 
+// Deep K: K panels.  Panel k of A (M x Kp, a strided 2-D copy from the host)
+// and of B (Kp x N rows) arrive on the copy-in stream while the GEMM of panel
+// k-1 runs; panel k accumulates into C (beta = 1 after the first).  The last
+// panel's GEMM is cut into row blocks so that finished rows of C go back to
+// the host on the copy-out stream while the rest is still computing.  Only
+// the first panel's copy and the last row block's copy are not overlapped.
+int run_host_kpanels(const float* A, const float* B, float* C, int M, int N, int K, int algo,
+                     DeviceState* d, int dev, HostPipe* hp, float* dA, float* dB, float* dC,
+                     int kp, cudaStream_t stream) {
+    cudaError_t e = cudaSuccess;
+    int st = GEMM_F32_SUCCESS;
+    const int panels = (K + kp - 1) / kp;
+    for (int i = 0; i < panels; ++i) {
+        const int k0 = i * kp;
+        const int kw = (K - k0) < kp ? (K - k0) : kp;
+        float* a_i = dA + static_cast<size_t>(i) * M * kp;  // panel i, row stride kp
+        float* b_i = dB + static_cast<size_t>(k0) * N;      // rows k0 .. k0+kw of B
+        if ((e = cudaMemcpy2DAsync(a_i, static_cast<size_t>(kp) * 4, A + k0,
+                                   static_cast<size_t>(K) * 4, static_cast<size_t>(kw) * 4, M,
+                                   cudaMemcpyHostToDevice, hp->s_in)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(b_i, B + static_cast<size_t>(k0) * N,
+                                 static_cast<size_t>(kw) * N * 4, cudaMemcpyHostToDevice,
+                                 hp->s_in)) != cudaSuccess ||
+            (e = cudaEventRecord(hp->ev_a[i], hp->s_in)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(stream, hp->ev_a[i], 0)) != cudaSuccess)
+            return static_cast<int>(e);
+        Problem q = packed(a_i, b_i, dC, M, N, kw);
+        q.lda = kp;
+        q.beta = i ? 1.0f : 0.0f;
+        if (i + 1 < panels) {
+            if ((st = enqueue(q, algo, 0, d, dev, stream, nullptr, nullptr, GEMM_F32_TILE_AUTO)) !=
+                GEMM_F32_SUCCESS)
+                return st;
+            continue;
+        }
+        // last panel: row blocks, each copied back as soon as it is final
+        const int blocks = M >= 4096 ? 8 : (M >= 1024 ? 4 : 1);
+        const int rows = ((M + blocks - 1) / blocks + 255) / 256 * 256;
+        for (int r0 = 0, j = 0; r0 < M; r0 += rows, ++j) {
+            const int mr = (M - r0) < rows ? (M - r0) : rows;
+            Problem qr = q;
+            qr.M = mr;
+            qr.A = a_i + static_cast<size_t>(r0) * kp;
+            qr.C = dC + static_cast<size_t>(r0) * N;
+            if ((st = enqueue(qr, algo, 0, d, dev, stream, nullptr, nullptr, GEMM_F32_TILE_AUTO)) !=
+                GEMM_F32_SUCCESS)
+                return st;
+            if ((e = cudaEventRecord(hp->ev_c[j], stream)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(hp->s_out, hp->ev_c[j], 0)) != cudaSuccess ||
+                (e = cudaMemcpyAsync(C + static_cast<size_t>(r0) * N,
+                                     dC + static_cast<size_t>(r0) * N,
+                                     static_cast<size_t>(mr) * N * 4, cudaMemcpyDeviceToHost,
+                                     hp->s_out)) != cudaSuccess)
+                return static_cast<int>(e);
+        }
+    }
+    if ((e = cudaEventRecord(hp->ev_done, hp->s_out)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(stream, hp->ev_done, 0)) != cudaSuccess)
+        return static_cast<int>(e);
+    return GEMM_F32_SUCCESS;
+}
+
 int run_host(const float* A, const float* B, float* C, int M, int N, int K, int algo,
              cudaStream_t stream) {
     int st = validate(packed(A, B, C, M, N, K), algo, 0);
@@ -607,8 +674,21 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
     if ((st = device_state(&d, &dev)) != GEMM_F32_SUCCESS) return st;
     if ((st = get_encoder()) != GEMM_F32_SUCCESS) return st;
 
-    // device copies: A (M x K), B (K x N), C (M x N), each 256-byte aligned
-    const size_t bytes_a = static_cast<size_t>(round_up(static_cast<long long>(M) * K * 4, 256));
+    // Row panels need all of B before the first GEMM: with B arriving at
+    // ~210 GB/s and the GEMM at ~300 TFLOP/s that wait is about 2900/M of the
+    // compute time.  For M <= 4096 with deep K the K-panel schedule (panels of
+    // >= 1024, first GEMM after one panel) wins; at 8192^3 row panels were
+    // measured faster (185.6 vs 174.3 TFLOPS end to end: K panels re-read C).
+    const bool kpanels =
+        K >= 2048 && M <= 4096 && static_cast<long long>(M) * N >= (1LL << 22);
+    const int kp = !kpanels ? K
+                   : (K + kMaxPanels - 1) / kMaxPanels > 1024
+                       ? static_cast<int>(round_up((K + kMaxPanels - 1) / kMaxPanels, 32))
+                       : 1024;
+    const long long a_cols = kpanels ? static_cast<long long>((K + kp - 1) / kp) * kp : K;
+    // device copies: A (M x K, or its K panels), B (K x N), C (M x N), 256-byte aligned
+    const size_t bytes_a =
+        static_cast<size_t>(round_up(static_cast<long long>(M) * a_cols * 4, 256));
     const size_t bytes_b = static_cast<size_t>(round_up(static_cast<long long>(K) * N * 4, 256));
     const size_t bytes_c = static_cast<size_t>(round_up(static_cast<long long>(M) * N * 4, 256));
     HostPipe* hp = nullptr;
@@ -618,6 +698,14 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
     float* dB = reinterpret_cast<float*>(static_cast<unsigned char*>(hp->dev_buf) + bytes_a);
     float* dC = reinterpret_cast<float*>(static_cast<unsigned char*>(hp->dev_buf) + bytes_a +
                                          bytes_b);
+
+    if (kpanels) {
+        cudaError_t e0 = cudaEventRecord(hp->ev_start, stream);
+        if (e0 == cudaSuccess) e0 = cudaStreamWaitEvent(hp->s_in, hp->ev_start, 0);
+        if (e0 == cudaSuccess) e0 = cudaStreamWaitEvent(hp->s_out, hp->ev_start, 0);
+        if (e0 != cudaSuccess) return static_cast<int>(e0);
+        return run_host_kpanels(A, B, C, M, N, K, algo, d, dev, hp, dA, dB, dC, kp, stream);
+    }
 
     // row panels: at least 512 rows, at most kMaxPanels of them
     long long rows = (M + 7) / 8;

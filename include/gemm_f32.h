@@ -143,7 +143,9 @@ int gemm_f32_algo_splitk_ev(const float* A, const float* B, float* C, int M, int
  * same shapes as gemm_f32).  The library copies B to the device, then walks
  * row panels of A and C: the copy of panel i+1 of A, the GEMM of panel i
  * and the copy back of panel i-1 of C run at the same time on the call's
- * stream and two internal streams.  Page-locked host memory is needed for
+ * stream and two internal streams.  For deep K with M <= 4096 it walks K
+ * panels instead (each accumulates into C, the first GEMM starts after one
+ * panel of A and B has arrived, the last panel returns C by row blocks).  Page-locked host memory is needed for
  * that overlap (pageable memory works, serialised).  Asynchronous on
  * `stream`: the host buffers must stay valid, and C is complete, only when
  * `stream` has reached the end of the call.  Device copies of A, B and C

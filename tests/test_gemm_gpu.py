@@ -350,3 +350,31 @@ def test_million_deep_k(algo):
     rng = np.random.default_rng(12)
     rows, cols = rng.integers(0, M, 600), rng.integers(0, N, 600)
     _check(C[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols), label=f"K=2^20 {algo}")
+
+
+@pytest.mark.parametrize("shape", [(2100, 2050, 3000), (4096, 1100, 8200)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("algo", [g.ALGO_3XTF32, g.ALGO_FFMA], ids=["3xtf32", "ffma"])
+def test_host_buffer_entry_k_panels(shape, algo):
+    # deep K and a large output: the host entry streams K panels of A and B
+    # and returns the last panel's rows block by block
+    t = _gpu.torch()
+    M, N, K = shape
+    A, B = make_workload(2, M=M, N=N, K=K)
+    hA = t.from_numpy(A).pin_memory()
+    hB = t.from_numpy(B).pin_memory()
+    hC = t.full((M + 1, N), float("nan")).pin_memory()
+    s = t.cuda.current_stream()
+    for _ in range(2):  # twice: the second call reuses every buffer and event
+        hC.fill_(float("nan"))
+        g.check(g.gemm_f32_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), M, N, K, algo,
+                                s.cuda_stream), "gemm_f32_host")
+        s.synchronize()
+        g.check(g.gemm_f32_device_status(1), "device status")
+        out = hC.numpy()
+        assert np.isnan(out[M]).all(), "write past C"
+        rng = np.random.default_rng(M + K)
+        rows = np.concatenate([rng.integers(0, M, 4000), np.arange(0, M, 97)])
+        cols = np.concatenate([rng.integers(0, N, 4000), np.arange(0, M, 97) % N])
+        _check(out[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols),
+               label=f"host k-panels {shape} {algo}")
