@@ -707,9 +707,11 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
         return run_host_kpanels(A, B, C, M, N, K, algo, d, dev, hp, dA, dB, dC, kp, stream);
     }
 
-    // row panels: at least 512 rows, at most kMaxPanels of them
-    long long rows = (M + 7) / 8;
-    rows = round_up(rows < 512 ? 512 : rows, 128);
+    // row panels: a quarter of M (at least 512 rows, at most kMaxPanels of
+    // them); big enough for a panel's tiles to fill several rounds of the
+    // persistent grid
+    long long rows = (M + 3) / 4;
+    rows = round_up(rows < 512 ? 512 : rows, 256);
     if ((M + rows - 1) / rows > kMaxPanels) rows = round_up((M + kMaxPanels - 1) / kMaxPanels, 128);
     const int P = static_cast<int>(rows < M ? rows : M);
     const int panels = (M + P - 1) / P;
