@@ -30,7 +30,7 @@ __all__ = [
     "library_path", "load", "gemm_f32", "gemm_f32_algo", "gemm_f32_algo_splitk",
     "gemm_f32_algo_splitk_ev", "gemm_f32_noalloc", "gemm_f32_host", "gemm_f32_ex",
     "gemm_f32_configured", "gemm_f32_plan_config", "Config", "TILE_AUTO", "TILE_128x128",
-    "TILE_128x256", "TILE_256x256_PAIR",
+    "TILE_128x256", "TILE_256x256_PAIR", "TILE_256x256_PAIR_SPLIT",
     "gemm_f32_plan", "gemm_f32_device_status", "gemm_f32_selftest_watchdog",
     "gemm_f32_release", "gemm_f32_status_string", "gemm_f32_version", "matmul", "check",
 ]
@@ -66,6 +66,7 @@ TILE_AUTO = 0
 TILE_128x128 = 1
 TILE_128x256 = 2
 TILE_256x256_PAIR = 3
+TILE_256x256_PAIR_SPLIT = 4
 
 
 class Config(ctypes.Structure):
@@ -78,6 +79,7 @@ class PlanInfo(ctypes.Structure):
         ("tile_n", ctypes.c_int), ("tile_k", ctypes.c_int), ("stages", ctypes.c_int),
         ("ctas", ctypes.c_int), ("stage_a", ctypes.c_int), ("stage_b", ctypes.c_int),
         ("kernels", ctypes.c_int), ("workspace_bytes", ctypes.c_longlong),
+        ("split_in_kernel", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:

@@ -143,6 +143,7 @@ struct Plan {
     int variant = 0;  // FFMA tile variant
     int bn = 0;
     int pair = 0;     // 3xTF32: two-CTA kernel
+    int split_in_kernel = 0;  // 3xTF32 pair kernel: TF32 split done in shared memory
     int box_n = 0;    // 3xTF32: B^T rows per TMA box
     int tail_tiles = 0, tail_splits = 0;  // pair kernel: K-split last partial round
     size_t off_t = 0;
@@ -267,8 +268,22 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         const int tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
         p->pair = units_pair >= d.sm_count / 2 ? 1 : 0;
         p->bn = (p->pair || (4 * tiles256 >= 3 * d.sm_count && N > 128)) ? 256 : 128;
+        // Few flops per operand element (2 M N / (M + N) below ~700, e.g.
+        // 256 x 256 x 65536): the staging pass over A and B (12 bytes per
+        // element) costs more than the tensor work, so the pair kernel that
+        // splits A and B in shared memory, at about 55 % of the staged
+        // kernel's rate but reading each operand once as stored, is faster
+        // (256 x 256 x 65536: 0.097 against 0.143 ms; 2048^3: 0.139
+        // against 0.099 ms the other way round).
+        const double per_element = 2.0 * M * N / (static_cast<double>(M) + N);
+        if (per_element < 700.0) {
+            p->pair = 1;
+            p->split_in_kernel = 1;
+            p->bn = 256;
+        }
         if (tile != GEMM_F32_TILE_AUTO) {
-            p->pair = tile == GEMM_F32_TILE_256x256_PAIR;
+            p->pair = tile == GEMM_F32_TILE_256x256_PAIR || tile == GEMM_F32_TILE_256x256_PAIR_SPLIT;
+            p->split_in_kernel = tile == GEMM_F32_TILE_256x256_PAIR_SPLIT;
             p->bn = tile == GEMM_F32_TILE_128x128 ? 128 : 256;
         }
         const Tf32x3Config tc = tf32x3_config(p->bn, p->pair != 0);
@@ -306,7 +321,7 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     p->ldw = round_up(N, 4);
 
     size_t off = 0;
-    if (p->algo == GEMM_F32_ALGO_3XTF32) {
+    if (p->algo == GEMM_F32_ALGO_3XTF32 && !p->split_in_kernel) {
         // A -> Ahi, Alo (M x K); B -> B^T hi, lo (N x K); rows padded to 16 bytes
         p->stage_a = 1;
         p->stage_b = 1;
@@ -319,8 +334,9 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         p->ctas = units < slots ? units : slots;
         if (p->pair) p->ctas *= 2;
     } else {
-        // read in place when TMA can describe the operand as stored: K- (A)
-        // or N-contiguous (B) rows, 16-byte row stride and base
+        // FFMA, and 3xTF32 splitting in the kernel: read in place when TMA
+        // can describe the operand as stored: K- (A) or N-contiguous (B)
+        // rows, 16-byte row stride and base
         p->stage_a = q.ta || (q.lda % 4 != 0) || misaligned16(q.A);
         p->stage_b = q.tb || (q.ldb % 4 != 0) || misaligned16(q.B);
         p->lda = p->stage_a ? round_up(K, 4) : q.lda;
@@ -328,6 +344,7 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         if (p->stage_a) p->off_a = carve(&off, static_cast<long long>(M) * p->lda * 4);
         if (p->stage_b) p->off_b = carve(&off, static_cast<long long>(K) * p->ldb * 4);
         p->ctas = units;
+        if (p->pair) p->ctas = 2 * (units < slots ? units : slots);
     }
     if (p->splits > 1)
         p->off_w = carve(&off, static_cast<long long>(p->splits) * M * p->ldw * 4);
@@ -368,7 +385,7 @@ struct Operands {
 int stage_b(const Plan& p, const Problem& q, unsigned char* ws, Operands* o, cudaStream_t stream) {
     cudaError_t e = cudaSuccess;
     const int K = q.K, N = q.N;
-    if (p.algo == GEMM_F32_ALGO_3XTF32) {
+    if (p.algo == GEMM_F32_ALGO_3XTF32 && !p.split_in_kernel) {
         float* hi = reinterpret_cast<float*>(ws + p.off_b);
         float* lo = reinterpret_cast<float*>(ws + p.off_b2);
         e = q.tb ? launch_split_rows(q.B, q.ldb, N, K, hi, lo, p.ldb, stream)        // N x K already
@@ -395,7 +412,7 @@ int stage_a(const Plan& p, const Problem& q, long long r0, int M, unsigned char*
     cudaError_t e = cudaSuccess;
     const int K = q.K;
     const float* a = q.ta ? q.A + r0 : q.A + r0 * q.lda;
-    if (p.algo == GEMM_F32_ALGO_3XTF32) {
+    if (p.algo == GEMM_F32_ALGO_3XTF32 && !p.split_in_kernel) {
         float* hi = reinterpret_cast<float*>(ws + p.off_a);
         float* lo = reinterpret_cast<float*>(ws + p.off_a2);
         e = q.ta ? launch_split_transpose(a, q.lda, K, M, hi, lo, p.lda, stream)  // K x M -> M x K
@@ -435,8 +452,18 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
     if (p.algo == GEMM_F32_ALGO_3XTF32) {
         Tf32x3Args ta;
         std::memset(&ta, 0, sizeof(ta));
-        // one CTA loads 128 rows of A and box_n rows of B^T per stage
-        if ((st = encode_2d(&ta.tmAhi, o.a_hi, K, M, p.lda, p.tile_k, 128,
+        if (p.split_in_kernel) {
+            // the operands as stored: A {K, M} in 128 x 32 boxes, B {N, K}
+            // in 32 x 32 boxes (one 128-byte swizzle row wide)
+            if ((st = encode_2d(&ta.tmAhi, o.a, K, M, p.lda, p.tile_k, 128,
+                                CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
+                (st = encode_2d(&ta.tmBhi, o.b, N, K, p.ldb, 32, p.tile_k,
+                                CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS)
+                return st;
+            ta.tmAlo = ta.tmAhi;
+            ta.tmBlo = ta.tmBhi;
+            ta.split_in_kernel = 1;
+        } else if ((st = encode_2d(&ta.tmAhi, o.a_hi, K, M, p.lda, p.tile_k, 128,
                             CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
             (st = encode_2d(&ta.tmAlo, o.a_lo, K, M, p.lda, p.tile_k, 128,
                             CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
@@ -780,9 +807,10 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
 // A forced configuration: tile id within range and valid for the algorithm.
 int check_config(const gemm_f32_config* cfg) {
     if (!cfg) return GEMM_F32_ERR_INVALID_VALUE;
-    if (cfg->tile < GEMM_F32_TILE_AUTO || cfg->tile > GEMM_F32_TILE_256x256_PAIR)
+    if (cfg->tile < GEMM_F32_TILE_AUTO || cfg->tile > GEMM_F32_TILE_256x256_PAIR_SPLIT)
         return GEMM_F32_ERR_INVALID_VALUE;
-    if (cfg->tile == GEMM_F32_TILE_256x256_PAIR && cfg->algo == GEMM_F32_ALGO_FFMA)
+    if ((cfg->tile == GEMM_F32_TILE_256x256_PAIR || cfg->tile == GEMM_F32_TILE_256x256_PAIR_SPLIT) &&
+        cfg->algo == GEMM_F32_ALGO_FFMA)
         return GEMM_F32_ERR_INVALID_VALUE;
     if (cfg->tile != GEMM_F32_TILE_AUTO && cfg->algo == GEMM_F32_ALGO_AUTO)
         return GEMM_F32_ERR_INVALID_VALUE;  // a tile names one algorithm's kernels
@@ -880,6 +908,7 @@ int gemm_f32_plan_config(int M, int N, int K, const gemm_f32_config* cfg, const 
     out->stage_b = p.stage_b;
     out->kernels = p.kernels;
     out->workspace_bytes = static_cast<long long>(p.ws_bytes);
+    out->split_in_kernel = p.split_in_kernel;
     return GEMM_F32_SUCCESS;
 }
 

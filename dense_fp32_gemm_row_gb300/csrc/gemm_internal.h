@@ -49,8 +49,13 @@ struct Tf32x3Config {
 Tf32x3Config tf32x3_config(int bn, bool pair);
 
 struct Tf32x3Args {
-    CUtensorMap tmAhi, tmAlo;  // A hi / lo as {K, M}, box {bk, bm}, 128-byte swizzle
-    CUtensorMap tmBhi, tmBlo;  // B^T hi / lo as {K, N}, box {bk, bn}, 128-byte swizzle
+    // pre-split operands: A hi / lo as {K, M}, box {bk, bm}, and B^T hi / lo
+    // as {K, N}, box {bk, box_n}, all with 128-byte swizzle.  split_in_kernel
+    // (pair kernel only): tmAhi is A as stored, {K, M}, box {bk, 128}, and
+    // tmBhi is B as stored, {N, K}, box {32, bk}; tmAlo and tmBlo are unused.
+    CUtensorMap tmAhi, tmAlo;
+    CUtensorMap tmBhi, tmBlo;
+    int split_in_kernel;
     float* out;
     long long ldo;
     long long split_stride;

@@ -126,13 +126,20 @@ __device__ __forceinline__ void st_shared_volatile(uint32_t addr, uint32_t v) {
 
 // Bounded wait that also gives up when another role has aborted (the abort
 // word is a shared-memory flag any role sets when one of its waits times out).
+// CLUSTER: acquire at cluster scope (the other CTA of the pair arrives after
+// writing shared memory that this CTA's MMAs read).
+template <bool CLUSTER>
+__device__ __forceinline__ bool try_wait_scoped(uint32_t bar, uint32_t parity) {
+    return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+}
+template <bool CLUSTER>
 __device__ __forceinline__ bool role_wait_slow(uint32_t bar, uint32_t parity, long long timeout_ns,
                                             unsigned* fault, unsigned bit, uint32_t abort_flag) {
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (try_wait_scoped<CLUSTER>(bar, parity)) return true;
         if (ld_shared_volatile(abort_flag)) return false;
         if (globaltimer_ns() - t0 > static_cast<uint64_t>(timeout_ns)) {
             if (fault) atomicOr(fault, bit);
@@ -141,10 +148,18 @@ __device__ __forceinline__ bool role_wait_slow(uint32_t bar, uint32_t parity, lo
         }
     }
 }
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, long long timeout_ns,
                                           unsigned* fault, unsigned bit, uint32_t abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    return role_wait_slow(bar, parity, timeout_ns, fault, bit, abort_flag);
+    if (try_wait_scoped<CLUSTER>(bar, parity)) return true;
+    return role_wait_slow<CLUSTER>(bar, parity, timeout_ns, fault, bit, abort_flag);
+}
+
+// Round to TF32 (nearest, ties away from zero): the split of tf32_split.cu.
+__device__ __forceinline__ float to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
 }
 
 template <int BN, int STAGES>
@@ -378,36 +393,144 @@ cudaError_t launch_impl(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
 // ============================================================================
 // CTA-pair variant: a cluster of two CTAs on two SMs computes a 256 x 256
 // tile with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 8).  CTA rank r
-// loads rows m0 + 128 r of Ahi/Alo and rows n0 + 128 r of B^T hi/lo into its
-// own shared memory, so every SM reads 8 KB of operands per MMA instead of
-// the 12 KB of the single-CTA 128 x 256 MMA; that is what lets the tensor
-// pipe outrun shared-memory bandwidth.  Each CTA's tensor memory holds its
-// 128 rows x 256 columns; its epilogue warps promote and store them.
-//   * both producers arrive (with their own transaction bytes) on the
-//     leader's full barrier and point their TMA completions at it;
-//   * the leader's MMA lane issues the pair MMAs and multicasts each commit
-//     to the same barrier offset in both CTAs (stage free / chunk ready);
-//   * both epilogues release a chunk buffer by arriving on the leader's
-//     acc_empty barrier.
+// holds rows m0 + 128 r of A and columns n0 + 128 r of B in its own shared
+// memory, so every SM reads 8 KB of operands per MMA instead of the 12 KB of
+// the single-CTA 128 x 256 MMA; that is what lets the tensor pipe outrun
+// shared-memory bandwidth.  Each CTA's tensor memory holds its 128 rows x 256
+// columns; its epilogue warps promote and store them.
+//
+// Two ways to feed it, chosen by SPLIT_IN_KERNEL:
+//   false  the operands arrive pre-split (Ahi, Alo and the transposed Bhi,
+//          Blo planes of tf32_split.cu), all K-major.  Both producers arrive
+//          (with their own transaction bytes) on the leader's full barrier
+//          and point their TMA completions at it.
+//   true   each CTA's producer loads the operands as stored into the hi
+//          slots, signalling its own full barrier: a 128 x 32 box of A
+//          (K-major already) and four 32 x 32 boxes of B (N-contiguous).
+//          Warps 2-3 of each CTA then split the stage in shared memory:
+//          A elementwise in place (hi = tf32(x) where x was, lo = tf32(x -
+//          hi) in the lo slot); B by 4 x 4 blocks read into registers,
+//          transposed and written back K-major as hi and lo.  These are the
+//          values and the layout the staging kernels would have produced,
+//          so the MMAs are the same.  The splitters fence their writes for
+//          the tensor core and arrive on the leader's converted barrier.
+//          (The tensor core is not given B N-major: with the B-major bit of
+//          the instruction descriptor set, kind::tf32 MMAs of this kernel
+//          wrote zeros on this part.)
+// In both, the leader's MMA lane multicasts each commit to the same barrier
+// offset in both CTAs (stage free / chunk ready), and both epilogues release
+// a chunk buffer by arriving on the leader's acc_empty barrier.
 // ============================================================================
-template <int STAGES>
+template <int STAGES, bool SPLIT_IN_KERNEL = false>
 struct PairCfg {
     static constexpr int BN = 256;       // MMA N, shared by the pair
-    static constexpr int HALF_N = 128;   // B^T rows held by each CTA
+    static constexpr int HALF_N = 128;   // columns of B held by each CTA
     static constexpr int A_BYTES = BM * BK * 4;
     static constexpr int B_BYTES = HALF_N * BK * 4;
+    static constexpr int B_BOX_N = 32;   // N-contiguous B box width: one 128-byte swizzle row
+    static constexpr int B_BOX_BYTES = B_BOX_N * BK * 4;
     static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int EPI_WARPS = BN / EPI_COLS * 4;
     static constexpr int THREADS = 128 + 32 * EPI_WARPS;
-    static constexpr int NBARS = 2 * STAGES + 5;
+    static constexpr int CONV_THREADS = 64;  // warps 2-3
+    // full, empty, converted (per stage), acc_full x2, acc_empty x2, drain
+    static constexpr int NBARS = 3 * STAGES + 5;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NBARS * 8 + 16 + 1024;
     static constexpr uint32_t IDESC = idesc_tf32_f32(2 * BM, BN);
+    static_assert(A_BYTES == B_BYTES && B_BYTES == 16384 && CONV_THREADS == 64,
+                  "the splitter's thread-to-element maps below");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
-template <int STAGES>
-__global__ void __launch_bounds__(PairCfg<STAGES>::THREADS, 1)
+__device__ __forceinline__ float4 tf32x4(float4 x) {
+    return make_float4(to_tf32(x.x), to_tf32(x.y), to_tf32(x.z), to_tf32(x.w));
+}
+
+__device__ __forceinline__ float4 sub4(float4 a, float4 b) {
+    return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w);
+}
+
+__device__ __forceinline__ float lane_of(float4 v, int e) {
+    return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+
+// Rotate the four lanes of v left by r (0..3): result.x = v[r], .y = v[r + 1], ...
+__device__ __forceinline__ float4 rotate4(float4 v, int r) {
+    const float4 a = (r & 1) ? make_float4(v.y, v.z, v.w, v.x) : v;
+    return (r & 2) ? make_float4(a.z, a.w, a.x, a.y) : a;
+}
+
+// A slot (16 KB at sa, K-major, 128-byte swizzled as the TMA wrote it): each
+// value x becomes hi = tf32(x) where it is and lo = tf32(x - hi) 16 KB
+// further on.  The map is elementwise, so the layout carries over.  Thread t
+// of the 64 takes 16-byte words t, t + 64, ... (conflict-free).
+__device__ __forceinline__ void split_a_stage(uint32_t sa, int t) {
+#pragma unroll 1
+    for (int i0 = 0; i0 < 16; i0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = lds128(sa + 16 * t + 1024 * (i0 + j));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 h = tf32x4(v[j]);
+            const uint32_t a = sa + 16 * t + 1024 * (i0 + j);
+            sts128(a, h);
+            sts128(a + 16384, tf32x4(sub4(v[j], h)));
+        }
+    }
+}
+
+// B slot (16 KB at sb): on entry four TMA boxes of 32 k-rows x 32 columns
+// (128-byte rows, box j holding columns 32 j .. 32 j + 31; 16-byte chunk c
+// of row k sits at chunk c ^ (k & 7)).  On exit the K-major hi plane in its
+// place (row n = 128 bytes of k = 0..31, chunk q at q ^ (n & 7): the layout
+// TMA gives a box of the transposed copy) and the lo plane 16 KB further on.
+// Splitter warp w owns boxes 2w and 2w + 1, i.e. bytes [8192 w, 8192 w +
+// 8192) of both layouts, so the in-place transpose needs no other warp.
+// Lane l takes the 4 x 4 blocks (n = 32 j + 4 c .. + 3, k = 4 kq .. + 3)
+// with c = l % 8, kq = l / 8 and l / 8 + 4, j = 2w, 2w + 1: it loads all of
+// them (eight lanes read one 128-byte row: conflict-free), the warp syncs,
+// then it stores each n's four k values as one 16-byte word.  The store
+// order over a block's four n is rotated by c / 2 so that the eight lanes
+// of a quarter-warp write eight different n % 8, i.e. eight different
+// 16-byte bank groups.
+__device__ __forceinline__ void split_b_stage(uint32_t sb, int w, int lane) {
+    const int c = lane & 7;
+    const int rot = (c >> 1) & 3;
+    float4 v[2][2][4];  // [box j - 2w][kq half][k - 4 kq], lanes over n - 32 j - 4 c
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const int k = 4 * ((lane >> 3) + 4 * h) + kk;
+                v[jj][h][kk] = rotate4(
+                    lds128(sb + (2 * w + jj) * 4096 + k * 128 + ((c ^ (k & 7)) << 4)), rot);
+            }
+    __syncwarp();  // every raw word of this warp's half is in registers
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int kq = (lane >> 3) + 4 * h;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int n = 32 * (2 * w + jj) + 4 * c + ((e + rot) & 3);
+                // lane e of the rotated words is column n; k = 4 kq + 0..3
+                const float4 x = make_float4(lane_of(v[jj][h][0], e), lane_of(v[jj][h][1], e),
+                                             lane_of(v[jj][h][2], e), lane_of(v[jj][h][3], e));
+                const float4 hi = tf32x4(x);
+                const uint32_t a = sb + n * 128 + ((kq ^ (n & 7)) << 4);
+                sts128(a, hi);
+                sts128(a + 16384, tf32x4(sub4(x, hi)));
+            }
+        }
+}
+
+template <int STAGES, bool SPLIT_IN_KERNEL>
+__global__ void __launch_bounds__(PairCfg<STAGES, SPLIT_IN_KERNEL>::THREADS, 1)
 sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                          const __grid_constant__ CUtensorMap tmAlo,
                          const __grid_constant__ CUtensorMap tmBhi,
@@ -416,15 +539,18 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                          int kb_per_split, int splits, int vec_store, unsigned* fault,
                          long long timeout_ns, float alpha, float beta, int scale_mode,
                          int tail_tiles, int tail_splits, float* __restrict__ tail_ws) {
-    using C = PairCfg<STAGES>;
+    using C = PairCfg<STAGES, SPLIT_IN_KERNEL>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_addr(smem);
     const uint32_t bar0 = sbase + STAGES * C::STAGE_BYTES;
-    const uint32_t full0 = bar0;                  // full[s]: used in the leader, count 2
+    // full[s]: pre-split operands: the leader's, count 2 (both producers);
+    //          split in kernel: each CTA's own, count 1
+    const uint32_t full0 = bar0;
     const uint32_t empty0 = bar0 + 8 * STAGES;    // empty[s]: both CTAs, one multicast commit
-    const uint32_t accf0 = bar0 + 16 * STAGES;    // acc_full[b]: both CTAs, one multicast commit
+    const uint32_t conv0 = bar0 + 16 * STAGES;    // converted[s]: leader, 2 warps x 2 CTAs
+    const uint32_t accf0 = bar0 + 24 * STAGES;    // acc_full[b]: both CTAs, one multicast commit
     const uint32_t acce0 = accf0 + 16;            // acc_empty[b]: leader, both epilogues
     const uint32_t drain = acce0 + 16;
     uint32_t* tmem_slot =
@@ -444,12 +570,15 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
 
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmAhi);
-        prefetch_tmap(&tmAlo);
         prefetch_tmap(&tmBhi);
-        prefetch_tmap(&tmBlo);
+        if (!SPLIT_IN_KERNEL) {
+            prefetch_tmap(&tmAlo);
+            prefetch_tmap(&tmBlo);
+        }
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, 2);
+            mbar_init(full0 + 8 * s, SPLIT_IN_KERNEL ? 1 : 2);
             mbar_init(empty0 + 8 * s, 1);
+            mbar_init(conv0 + 8 * s, 2 * (C::CONV_THREADS / 32));
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf0 + 8 * b, 1);
@@ -486,19 +615,33 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                         break;
                     }
                     const uint32_t st = sbase + s * C::STAGE_BYTES;
-                    const uint32_t fb = map_to_cta(full0 + 8 * s, 0);
                     const int k0 = (w.kb_begin + kb) * BK;
-                    mbar_arrive_expect_tx_cluster(fb, C::STAGE_BYTES);
-                    tma_load_2d_pair(st, &tmAhi, fb, k0, ma);
-                    tma_load_2d_pair(st + C::A_BYTES, &tmAlo, fb, k0, ma);
-                    tma_load_2d_pair(st + 2 * C::A_BYTES, &tmBhi, fb, k0, nb);
-                    tma_load_2d_pair(st + 2 * C::A_BYTES + C::B_BYTES, &tmBlo, fb, k0, nb);
+                    if (SPLIT_IN_KERNEL) {
+                        const uint32_t fb = full0 + 8 * s;
+                        mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES);
+                        tma_load_2d(st, &tmAhi, fb, k0, ma);
+#pragma unroll
+                        for (int j = 0; j < C::HALF_N / C::B_BOX_N; ++j)
+                            tma_load_2d(st + 2 * C::A_BYTES + j * C::B_BOX_BYTES, &tmBhi, fb,
+                                        nb + j * C::B_BOX_N, k0);
+                    } else {
+                        const uint32_t fb = map_to_cta(full0 + 8 * s, 0);
+                        mbar_arrive_expect_tx_cluster(fb, C::STAGE_BYTES);
+                        tma_load_2d_pair(st, &tmAhi, fb, k0, ma);
+                        tma_load_2d_pair(st + C::A_BYTES, &tmAlo, fb, k0, ma);
+                        tma_load_2d_pair(st + 2 * C::A_BYTES, &tmBhi, fb, k0, nb);
+                        tma_load_2d_pair(st + 2 * C::A_BYTES + C::B_BYTES, &tmBlo, fb, k0, nb);
+                    }
                 }
             }
-            // wind down: every stage this CTA filled has been consumed and released
+            // wind down: every stage this CTA filled has landed (own full
+            // barrier, split in kernel) and been consumed and released
             const long long tail = ok ? timeout_ns : timeout_ns / 8 + 1000;
-            for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+            for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j) {
+                if (SPLIT_IN_KERNEL)
+                    mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1, tail, fault, kFaultDrain);
                 mbar_wait(empty0 + 8 * (j % STAGES), (j / STAGES) & 1, tail, fault, kFaultDrain);
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -521,8 +664,13 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                     const int c1 = min(w.nkb, c0 + CH);
                     for (int kb = c0; kb < c1; ++kb, ++it) {
                         const int s = it % STAGES;
-                        if (!role_wait(full0 + 8 * s, (it / STAGES) & 1, timeout_ns, fault,
-                                       kFaultFullBarrier, abort_flag)) {
+                        const bool got =
+                            SPLIT_IN_KERNEL
+                                ? role_wait<true>(conv0 + 8 * s, (it / STAGES) & 1, timeout_ns,
+                                                  fault, kFaultFullBarrier, abort_flag)
+                                : role_wait(full0 + 8 * s, (it / STAGES) & 1, timeout_ns, fault,
+                                            kFaultFullBarrier, abort_flag);
+                        if (!got) {
                             ok = false;
                             break;
                         }
@@ -551,7 +699,35 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
             mbar_wait(drain, 0, ok ? timeout_ns : timeout_ns / 8 + 1000, fault, kFaultDrain);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp < 4) {
+        if (SPLIT_IN_KERNEL) {
+            // ------------------------------ splitter (warps 2-3, both CTAs) -----------
+            const int t = threadIdx.x - 64;
+            const uint32_t conv_leader = map_to_cta(conv0, 0);
+            int it = 0;
+            bool ok = true;
+            for (int u = cluster; u < units && ok; u += nclusters) {
+                const Unit w = decode_pair(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN,
+                                           tail_tiles, tail_splits);
+                for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const bool got = role_wait(full0 + 8 * s, (it / STAGES) & 1, timeout_ns, fault,
+                                               kFaultFullBarrier, abort_flag);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = sbase + s * C::STAGE_BYTES;
+                    split_a_stage(st, t);
+                    split_b_stage(st + 2 * C::A_BYTES, warp - 2, lane);
+                    // the tensor core reads these words through the async proxy
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(conv_leader + 8 * s);
+                }
+            }
+        }
+    } else {
         // ------------------------------ epilogue (both CTAs) ----------------------
         const int e = warp - 4;
         const int q = warp & 3;
@@ -655,7 +831,7 @@ cudaError_t pair_clusters(int sm_count, int* out) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (done_dev != dev) {
-        auto kern = sgemm_3xtf32_pair_kernel<3>;
+        auto kern = sgemm_3xtf32_pair_kernel<3, false>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
@@ -680,13 +856,23 @@ cudaError_t pair_clusters(int sm_count, int* out) {
     return cudaSuccess;
 }
 
-template <int STAGES>
+template <int STAGES, bool SPLIT_IN_KERNEL>
 cudaError_t launch_pair(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
-    using C = PairCfg<STAGES>;
-    auto kern = sgemm_3xtf32_pair_kernel<STAGES>;
+    using C = PairCfg<STAGES, SPLIT_IN_KERNEL>;
+    static_assert(C::SMEM_BYTES == PairCfg<3>::SMEM_BYTES && C::THREADS == PairCfg<3>::THREADS,
+                  "both pair kernels have the occupancy pair_clusters measures");
+    auto kern = sgemm_3xtf32_pair_kernel<STAGES, SPLIT_IN_KERNEL>;
     int max_clusters = 0;
     cudaError_t e = pair_clusters(sm_count, &max_clusters);
     if (e != cudaSuccess) return e;
+    static thread_local int attr_done_dev = -1;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (attr_done_dev != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done_dev = dev;
+    }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -733,7 +919,9 @@ Tf32x3Config tf32x3_config(int bn, bool pair) {
 }
 
 cudaError_t launch_sgemm_3xtf32(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
-    if (a.pair) return launch_pair<3>(a, s, sm_count);
+    if (a.pair)
+        return a.split_in_kernel ? launch_pair<3, true>(a, s, sm_count)
+                                 : launch_pair<3, false>(a, s, sm_count);
     if (a.bn == 128) return launch_impl<128, 3>(a, s, sm_count);
     return launch_impl<256, 2>(a, s, sm_count);
 }

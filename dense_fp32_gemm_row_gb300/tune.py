@@ -7,7 +7,8 @@ The library-side counterpart of the sweep program of "Lecture 12: final
 project" (block size x tile depth x coarsening, each combination checked for
 correctness before it is timed, then ranked).  Here the configuration space
 is the library's own: algorithm (CUDA-core FFMA or 3xTF32 tensor cores) x
-tile (128x128, 128x256, and for 3xTF32 the 256x256 two-CTA tile) x split-K
+tile (128x128, 128x256, and for 3xTF32 the 256x256 two-CTA tile, fed by
+staging kernels or splitting its operands in shared memory) x split-K
 factor.  Every configuration runs once through ``gemm_f32_configured`` and
 must match cuBLAS SGEMM (TF32 off) within 1e-3 + 1e-3 |ref| on every output
 before it is timed (median of ``--repeats`` calls, CUDA events, L2 flushed
@@ -32,7 +33,8 @@ SPLITS = (1, 2, 4, 8, 16, 32, 64)
 
 def _configs(g):
     for algo, tiles in ((g.ALGO_FFMA, (g.TILE_128x128, g.TILE_128x256)),
-                        (g.ALGO_3XTF32, (g.TILE_128x128, g.TILE_128x256, g.TILE_256x256_PAIR))):
+                        (g.ALGO_3XTF32, (g.TILE_128x128, g.TILE_128x256, g.TILE_256x256_PAIR,
+                                         g.TILE_256x256_PAIR_SPLIT))):
         for tile in tiles:
             for splits in SPLITS:
                 yield algo, tile, splits
@@ -48,7 +50,7 @@ def sweep(shapes, repeats: int, out=sys.stdout) -> list[dict]:
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     names = {g.ALGO_FFMA: "ffma", g.ALGO_3XTF32: "3xtf32", g.ALGO_AUTO: "auto"}
-    tiles = {0: "auto", 1: "128x128", 2: "128x256", 3: "256x256pair"}
+    tiles = {0: "auto", 1: "128x128", 2: "128x256", 3: "256x256pair", 4: "256x256pair-split"}
     writer = csv.writer(out)
     writer.writerow(["shape", "algo", "tile", "splits", "ctas", "kernels", "ms", "tflops",
                      "check", "rank"])
@@ -108,7 +110,8 @@ def sweep(shapes, repeats: int, out=sys.stdout) -> list[dict]:
             ms = timed(call) if ok else float("nan")
             results.append({"shape": f"{M}x{N}x{K}", "algo": names[algo],
                             "tile": tiles[tile] if algo != g.ALGO_AUTO else
-                            f"{plan['tile_m']}x{plan['tile_n']}",
+                            f"{plan['tile_m']}x{plan['tile_n']}"
+                            + ("-split" if plan.get("split_in_kernel") else ""),
                             "splits": plan["splits"], "ctas": plan["ctas"],
                             "kernels": plan["kernels"], "ms": ms,
                             "tflops": flops / (ms * 1e-3) / 1e12 if ok else 0.0,

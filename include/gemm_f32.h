@@ -172,6 +172,7 @@ typedef struct gemm_f32_plan_info {
     int stage_b;         /* 1 if B goes through a staging copy */
     int kernels;         /* kernel launches the call makes */
     long long workspace_bytes; /* workspace the call needs */
+    int split_in_kernel; /* 1 if the 3XTF32 TF32 split happens inside the GEMM kernel */
 } gemm_f32_plan_info;
 
 int gemm_f32_plan(int M, int N, int K, int algo, int splits,
@@ -187,13 +188,16 @@ int gemm_f32_plan(int M, int N, int K, int algo, int splits,
  *   algo    GEMM_F32_ALGO_FFMA or _3XTF32 (AUTO only with tile = AUTO)
  *   tile    GEMM_F32_TILE_* below; 0 lets the library choose
  *   splits  as for gemm_f32_algo_splitk (0 = choose)
- * The 256 x 256 CTA-pair tile exists for 3XTF32 only.  Invalid combinations
- * return GEMM_F32_ERR_INVALID_VALUE.
+ * The 256 x 256 CTA-pair tiles exist for 3XTF32 only: _PAIR reads TF32
+ * hi/lo copies of A and B written by staging kernels, _PAIR_SPLIT reads A
+ * and B as stored and splits each tile in shared memory (same products, no
+ * staging pass).  Invalid combinations return GEMM_F32_ERR_INVALID_VALUE.
  */
 #define GEMM_F32_TILE_AUTO          0
 #define GEMM_F32_TILE_128x128       1
 #define GEMM_F32_TILE_128x256       2
 #define GEMM_F32_TILE_256x256_PAIR  3
+#define GEMM_F32_TILE_256x256_PAIR_SPLIT 4
 typedef struct gemm_f32_config {
     int algo;
     int tile;

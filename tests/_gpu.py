@@ -52,3 +52,27 @@ def run(A: np.ndarray, B: np.ndarray, algo: int = g.ALGO_AUTO, splits: int = 0,
         assert np.all(lo == SENTINEL_BITS), "write before C"
         assert np.all(hi == SENTINEL_BITS), "write after C"
     return host[GUARD + offsets[2]:GUARD + offsets[2] + M * N].reshape(M, N).copy()
+
+
+def run_configured(A: np.ndarray, B: np.ndarray, algo: int, tile: int, splits: int = 0,
+                   offsets=(0, 0, 0)) -> np.ndarray:
+    """C = A @ B through gemm_f32_configured (forced kernel configuration),
+    with the same guard bands as ``run``."""
+    t = torch()
+    M, K = A.shape
+    N = B.shape[1]
+    _, a = upload(A, offsets[0])
+    _, b = upload(B, offsets[1])
+    cbuf = t.empty(M * N + 2 * GUARD + offsets[2], dtype=t.float32, device="cuda")
+    cbuf.view(t.int32).fill_(int(SENTINEL_BITS.view(np.int32)))
+    c = cbuf[GUARD + offsets[2]:GUARD + offsets[2] + M * N]
+    s = t.cuda.current_stream()
+    g.check(g.gemm_f32_configured(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, algo, tile,
+                                  splits, s.cuda_stream), "gemm_f32_configured")
+    s.synchronize()
+    g.check(g.gemm_f32_device_status(1), "device status")
+    host = cbuf.cpu().numpy()
+    assert np.all(host[:GUARD + offsets[2]].view(np.uint32) == SENTINEL_BITS), "write before C"
+    assert np.all(host[GUARD + offsets[2] + M * N:].view(np.uint32) == SENTINEL_BITS), \
+        "write after C"
+    return host[GUARD + offsets[2]:GUARD + offsets[2] + M * N].reshape(M, N).copy()

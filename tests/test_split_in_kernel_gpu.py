@@ -1,0 +1,123 @@
+"""GPU parity of the CTA-pair 3xTF32 kernel that splits A and B into TF32
+hi/lo parts in shared memory (GEMM_F32_TILE_256x256_PAIR_SPLIT) instead of
+reading copies written by staging kernels.
+
+Against the oracle, elementwise within 1e-3 + 1e-3 |C_ref| (NaN guard bands
+around C); against the pre-split pair kernel, bit for bit: both form the same
+hi = tf32(x), lo = tf32(x - hi) values and issue the same MMAs in the same
+order, the B operand only being read through a different shared-memory
+layout.
+"""
+
+import numpy as np
+import pytest
+
+import dense_fp32_gemm_row_gb300 as g
+import oracle
+from seeded_inputs import make_workload
+
+from . import _gpu
+from .test_gemm_gpu import _check
+
+pytestmark = pytest.mark.gpu
+
+SPLIT = g.TILE_256x256_PAIR_SPLIT
+PRESPLIT = g.TILE_256x256_PAIR
+
+# ragged in M, N (not a multiple of the 32-column B boxes) and K; several
+# rounds of the persistent grid with a K-split tail (2304^2: 81 tiles)
+SHAPES = [(256, 256, 32), (300, 200, 40), (2304, 2304, 512), (2305, 2049, 1000),
+          (2560, 2330, 77), (1025, 1023, 1000), (513, 4100, 333)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    torch = pytest.importorskip("torch")
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    g.load()
+    yield
+    g.gemm_f32_release()
+
+
+def _sample(M, N, seed, n=3000):
+    rng = np.random.default_rng(seed)
+    rows = np.concatenate([np.arange(M), rng.integers(0, M, n), np.full(N, M - 1)])
+    cols = np.concatenate([rng.integers(0, N, M), rng.integers(0, N, n), np.arange(N)])
+    return rows, cols
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_parity_and_equal_to_presplit(shape):
+    M, N, K = shape
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, SPLIT, 0, A=1 << 32, B=1 << 36,
+                                   C=1 << 40)
+    assert st == 0 and p["split_in_kernel"] == 1 and (p["tile_m"], p["tile_n"]) == (256, 256)
+    # read in place unless a row stride is not a multiple of 16 bytes
+    assert p["stage_a"] == (K % 4 != 0) and p["stage_b"] == (N % 4 != 0), p
+    A, B = make_workload(2, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, SPLIT)
+    rows, cols = _sample(M, N, M * 7 + N + K)
+    _check(C[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols), label=f"split {shape}")
+    C0 = _gpu.run_configured(A, B, g.ALGO_3XTF32, PRESPLIT)
+    assert np.array_equal(C.view(np.uint32), C0.view(np.uint32)), \
+        f"differs from the pre-split kernel at {np.argwhere(C.view(np.uint32) != C0.view(np.uint32))[:5]}"
+
+
+@pytest.mark.parametrize("splits", [2, 7])
+def test_split_k(splits):
+    M, N, K = 600, 700, 5000
+    A, B = make_workload(4, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, SPLIT, splits)
+    _check(C, oracle.ref_gemm(A, B), label=f"split-in-kernel, {splits} K splits")
+    C2 = _gpu.run_configured(A, B, g.ALGO_3XTF32, SPLIT, splits)
+    assert np.array_equal(C.view(np.uint32), C2.view(np.uint32)), "not run-to-run deterministic"
+
+
+def test_deep_k_one_tile():
+    # one output tile, K spread over many clusters (split-K with workspace)
+    M, N, K = 256, 256, 65536
+    A, B = make_workload(4, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, SPLIT, 0)
+    _check(C, oracle.ref_gemm(A, B), label="256x256x65536 split in kernel")
+
+
+@pytest.mark.parametrize("offsets", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (3, 2, 1)])
+def test_misaligned_operands_are_staged(offsets):
+    M, N, K = 700, 900, 300   # row strides of A and B are multiples of 16 bytes
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, SPLIT, 0,
+                                   A=(1 << 32) + 4 * offsets[0], B=(1 << 36) + 4 * offsets[1],
+                                   C=(1 << 40) + 4 * offsets[2])
+    assert st == 0 and p["stage_a"] == (offsets[0] % 4 != 0) and \
+        p["stage_b"] == (offsets[1] % 4 != 0), p
+    A, B = make_workload(1, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, SPLIT, 0, offsets=offsets)
+    _check(C, oracle.ref_gemm(A, B), label=f"split in kernel, offsets {offsets}")
+
+
+def test_quantised_exact():
+    A, B = make_workload(0)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, SPLIT, 0)
+    _check(C, oracle.ref_gemm(A, B), exact=True, label="quantised 512^3, split in kernel")
+
+
+@pytest.mark.parametrize("shape,want", [((256, 256, 65536), 1), ((65536, 256, 1024), 1),
+                                        ((2048, 2048, 2048), 0), ((8192, 8192, 8192), 0),
+                                        ((1025, 1023, 1000), 0)],
+                         ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
+def test_auto_splits_in_kernel_when_staging_dominates(shape, want):
+    # AUTO takes the in-kernel split when 2 M N / (M + N) < 700 flops per
+    # operand element (the staging pass would cost more than the MMAs)
+    M, N, K = shape
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["split_in_kernel"] == want, p
+    if want:
+        assert (p["tile_m"], p["tile_n"]) == (256, 256) and p["stage_a"] == 0 and p["stage_b"] == 0
+
+
+def test_auto_skinny_parity():
+    # the in-kernel split chosen by AUTO on a tall, narrow product (ragged N)
+    M, N, K = 9000, 200, 3000
+    A, B = make_workload(1, M=M, N=N, K=K)
+    C = _gpu.run(A, B, g.ALGO_AUTO)
+    rows, cols = _sample(M, N, 5)
+    _check(C[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols), label="auto skinny")
