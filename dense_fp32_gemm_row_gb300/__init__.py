@@ -79,7 +79,7 @@ class PlanInfo(ctypes.Structure):
         ("tile_n", ctypes.c_int), ("tile_k", ctypes.c_int), ("stages", ctypes.c_int),
         ("ctas", ctypes.c_int), ("stage_a", ctypes.c_int), ("stage_b", ctypes.c_int),
         ("kernels", ctypes.c_int), ("workspace_bytes", ctypes.c_longlong),
-        ("split_in_kernel", ctypes.c_int),
+        ("split_in_kernel", ctypes.c_int), ("cluster_reduce", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:

@@ -144,6 +144,7 @@ struct Plan {
     int bn = 0;
     int pair = 0;     // 3xTF32: two-CTA kernel
     int split_in_kernel = 0;  // 3xTF32 pair kernel: TF32 split done in shared memory
+    int cluster_splits = 0;   // FFMA: split-K partials added inside a cluster (2..8)
     int box_n = 0;    // 3xTF32: B^T rows per TMA box
     int tail_tiles = 0, tail_splits = 0;  // pair kernel: K-split last partial round
     size_t off_t = 0;
@@ -346,7 +347,13 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         p->ctas = units;
         if (p->pair) p->ctas = 2 * (units < slots ? units : slots);
     }
-    if (p->splits > 1)
+    // FFMA with 2..4 splits: each tile's splits run as one thread-block
+    // cluster and add their partials through distributed shared memory (no
+    // workspace, no reduction kernel); more splits use the workspace, which
+    // measured faster from 8 splits on (512^3: 19.1 against 23.2 us)
+    if (p->algo == GEMM_F32_ALGO_FFMA && p->splits >= 2 && p->splits <= 4)
+        p->cluster_splits = p->splits;
+    if (p->splits > 1 && !p->cluster_splits)
         p->off_w = carve(&off, static_cast<long long>(p->splits) * M * p->ldw * 4);
     // The pair kernel's last round of tiles is usually only partly full
     // (e.g. 1024 tiles over 76 clusters leave 36 for the 14th round).  Cut
@@ -367,7 +374,8 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     }
     cudaGetLastError();
     p->ws_bytes = off;
-    p->kernels = 1 + p->stage_a + p->stage_b + (p->splits > 1 ? 1 : 0) + (p->tail_tiles ? 1 : 0);
+    p->kernels = 1 + p->stage_a + p->stage_b + (p->splits > 1 && !p->cluster_splits ? 1 : 0) +
+                 (p->tail_tiles ? 1 : 0);
 }
 
 // Device operands the GEMM kernel reads, after staging.
@@ -440,7 +448,7 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
     float* out = C;
     long long ldo = ldc, split_stride = 0;
     int kmode = mode;
-    if (p.splits > 1) {
+    if (p.splits > 1 && !p.cluster_splits) {
         out = reinterpret_cast<float*>(ws + p.off_w);
         ldo = p.ldw;
         split_stride = static_cast<long long>(M) * p.ldw;
@@ -521,13 +529,14 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
         fa.alpha = alpha;
         fa.beta = beta;
         fa.scale_mode = kmode;
+        fa.cluster_splits = p.cluster_splits;
         if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
             return static_cast<int>(e);
         if ((e = launch_sgemm_ffma(fa, stream)) != cudaSuccess) return static_cast<int>(e);
         if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess)
             return static_cast<int>(e);
     }
-    if (p.splits > 1) {
+    if (p.splits > 1 && !p.cluster_splits) {
         e = launch_splitk_reduce(out, split_stride, p.ldw, p.splits, C, ldc, M, N, alpha, beta,
                                  mode, stream);
         if (e != cudaSuccess) return static_cast<int>(e);
@@ -909,6 +918,7 @@ int gemm_f32_plan_config(int M, int N, int K, const gemm_f32_config* cfg, const 
     out->kernels = p.kernels;
     out->workspace_bytes = static_cast<long long>(p.ws_bytes);
     out->split_in_kernel = p.split_in_kernel;
+    out->cluster_reduce = p.cluster_splits ? 1 : 0;
     return GEMM_F32_SUCCESS;
 }
 

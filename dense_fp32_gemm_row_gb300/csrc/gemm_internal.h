@@ -35,6 +35,10 @@ struct FfmaArgs {
     int bn;                 // tile width the B descriptor's box was encoded with
     float alpha, beta;      // output scaling (epilogue.cuh modes)
     int scale_mode;         // 0 plain, 1 alpha, 2 alpha and beta (reads C)
+    // 0: split s writes its partial to out + s * split_stride.  2..4 (equal
+    // to splits): each tile's splits run as one cluster and add their
+    // partials in split order through distributed shared memory; out is C.
+    int cluster_splits;
 };
 cudaError_t launch_sgemm_ffma(const FfmaArgs& a, cudaStream_t s);
 

@@ -32,8 +32,13 @@
 //    which would need the whole 128-byte/clock shared-memory pipe at full
 //    FFMA rate, and 0.1875 for 8 x 16 (G = 4), which leaves a quarter of it.
 //  * Every accumulator sums its products in ascending k, so the result is
-//    run-to-run deterministic; split-K partials are summed in split order by
-//    a separate kernel.
+//    run-to-run deterministic.  Split-K partials are summed in split order,
+//    either by a separate kernel over a workspace or, for 2..4 splits, inside
+//    a thread-block cluster: the S CTAs computing one tile's K splits form a
+//    cluster, each parks its partial tile in its own shared memory, and after
+//    a cluster barrier CTA r adds up rows r/S .. (r+1)/S of the tile over
+//    distributed shared memory, split 0 first (the workspace kernel's order,
+//    so both give the same bits), and writes them to C.
 //  * The epilogue stores float4 when the row stride allows it and falls back
 //    to predicated scalar stores on ragged edges; nothing outside C is
 //    written.
@@ -66,8 +71,21 @@ __device__ __forceinline__ void lds_v2_b64(uint32_t addr, uint64_t& x, uint64_t&
     asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "r"(addr));
 }
 
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t cluster_addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
 constexpr int BM = 128;
 constexpr int BK = 32;       // 32 floats = one 128-byte swizzle row of A
+// splits added inside a cluster: at 512^3 (a latency-bound call) 2 and 4
+// splits ran faster in a cluster than through the workspace (33.5 / 23.2
+// against 35.5 / 24.6 us) but 8 ran slower (23.2 against 19.1 us)
+constexpr int MAX_CLUSTER_SPLITS = 4;
 constexpr int THREADS = 256;
 constexpr int WARPS = THREADS / 32;
 constexpr int A_BYTES = BM * BK * 4;
@@ -82,6 +100,7 @@ struct FfmaVariant {
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 2 * STAGES * 8 + 1024;
     static_assert(LAG >= 1 && LAG < STAGES, "refill lag");
     static_assert(BN <= 256, "TMA box");
+    static_assert(BM * BN * 4 <= STAGES * STAGE_BYTES, "a partial tile fits in the stages");
 };
 
 // Accumulators are held as column pairs and updated by packed two-lane FMAs,
@@ -91,7 +110,7 @@ __global__ void __launch_bounds__(THREADS, MIN_BLOCKS)
 sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   float* __restrict__ out, long long ldo, long long split_stride, int M, int N,
                   int K, int kb_per_split, int vec_store, unsigned* fault, long long timeout_ns,
-                  float alpha, float beta, int scale_mode) {
+                  float alpha, float beta, int scale_mode, int cluster_splits) {
     using V = FfmaVariant<G, STAGES, LAG, MIN_BLOCKS>;
     constexpr int BN = V::BN;
     extern __shared__ unsigned char smem_raw[];
@@ -227,7 +246,10 @@ sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1, timeout_ns / 4 + 1000, fault,
                           kFaultDrain);
         }
-        return;
+        // a cluster member still takes both cluster barriers below, so that
+        // its partners are not left waiting (the result is void: the fault
+        // word reports the timeout)
+        if (cluster_splits < 2) return;
     }
 
     float acc[8][4 * G];
@@ -235,6 +257,58 @@ sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     for (int r = 0; r < 8; ++r)
 #pragma unroll
         for (int p = 0; p < 2 * G; ++p) unpack2(acc2[r][p], acc[r][2 * p], acc[r][2 * p + 1]);
+
+    if (cluster_splits >= 2) {
+        // ---- split-K reduction inside the cluster (blockIdx.y = split = rank) ----
+        __syncthreads();  // every warp is done with the stages
+        // this CTA's partial tile, BM x BN row-major, over the first stages
+        if (ok) {
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    sts128(smem_base + 4u * static_cast<uint32_t>((wm * 32 + tm + 4 * r) * BN +
+                                                                  b_off + 32 * g),
+                           make_float4(acc[r][4 * g], acc[r][4 * g + 1], acc[r][4 * g + 2],
+                                       acc[r][4 * g + 3]));
+        }
+        cluster_sync();  // all partials written and visible across the cluster
+        const int S = cluster_splits;
+        const int rank = blockIdx.y;
+        const int rows = (BM + S - 1) / S;
+        const int r0 = rank * rows;
+        const int r1 = min(BM, r0 + rows);
+        constexpr int Q = BN / 4;  // float4 per tile row
+        uint32_t peer[MAX_CLUSTER_SPLITS];
+#pragma unroll
+        for (int q = 0; q < MAX_CLUSTER_SPLITS; ++q)
+            peer[q] = q < S ? map_to_cta(smem_base, static_cast<uint32_t>(q)) : 0u;
+        if (ok) {
+            for (int idx = tid; idx < (r1 - r0) * Q; idx += THREADS) {
+                const int i = r0 + idx / Q;
+                const int j4 = idx - (idx / Q) * Q;
+                const int m = m0 + i;
+                if (m >= M) continue;
+                const uint32_t off = 4u * static_cast<uint32_t>(i * BN + 4 * j4);
+                float4 sum = ld_dsmem_v4(peer[0] + off);
+#pragma unroll
+                for (int q = 1; q < MAX_CLUSTER_SPLITS; ++q) {
+                    if (q < S) {
+                        const float4 v = ld_dsmem_v4(peer[q] + off);
+                        sum.x += v.x;
+                        sum.y += v.y;
+                        sum.z += v.z;
+                        sum.w += v.w;
+                    }
+                }
+                store4(out + static_cast<long long>(m) * ldo, n0 + 4 * j4, N, sum, vec_store != 0,
+                       alpha, beta, scale_mode);
+            }
+        }
+        cluster_sync();  // no CTA leaves while a partner may still read its partial
+        return;
+    }
+
     float* outp = out + static_cast<long long>(blockIdx.y) * split_stride;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
@@ -271,9 +345,31 @@ cudaError_t launch_variant(const FfmaArgs& a, cudaStream_t s) {
     }
     const int tiles = ((a.M + BM - 1) / BM) * ((a.N + V::BN - 1) / V::BN);
     dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(a.splits));
+    if (a.cluster_splits) {
+        // the splits of one tile form a cluster along y
+        if (a.cluster_splits != a.splits || a.splits < 2 || a.splits > MAX_CLUSTER_SPLITS)
+            return cudaErrorInvalidValue;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = static_cast<unsigned>(a.splits);
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = V::SMEM_BYTES;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.out, a.ldo, a.split_stride, a.M, a.N,
+                               a.K, a.kb_per_split, a.vec_store, a.fault, a.timeout_ns, a.alpha,
+                               a.beta, a.scale_mode, a.cluster_splits);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     kern<<<grid, THREADS, V::SMEM_BYTES, s>>>(a.tmA, a.tmB, a.out, a.ldo, a.split_stride, a.M, a.N,
                                               a.K, a.kb_per_split, a.vec_store, a.fault,
-                                              a.timeout_ns, a.alpha, a.beta, a.scale_mode);
+                                              a.timeout_ns, a.alpha, a.beta, a.scale_mode, 0);
     return cudaGetLastError();
 }
 

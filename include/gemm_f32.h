@@ -173,6 +173,8 @@ typedef struct gemm_f32_plan_info {
     int kernels;         /* kernel launches the call makes */
     long long workspace_bytes; /* workspace the call needs */
     int split_in_kernel; /* 1 if the 3XTF32 TF32 split happens inside the GEMM kernel */
+    int cluster_reduce;  /* 1 if split-K partials are added inside thread-block clusters
+                            (no workspace, no reduction kernel) */
 } gemm_f32_plan_info;
 
 int gemm_f32_plan(int M, int N, int K, int algo, int splits,

@@ -1,0 +1,97 @@
+"""GPU parity of the CUDA-core kernel's in-cluster split-K reduction: for
+2..4 K splits the splits of one output tile run as a thread-block cluster
+and add their partial tiles through distributed shared memory, split 0
+first, with no workspace and no reduction kernel.
+
+Against the oracle within 1e-3 + 1e-3 |C_ref| (NaN guard bands around C);
+against the workspace reduction (gemm_f32_noalloc: same kernel, partials in
+a scratch array, summed by the reduction kernel in the same split order),
+bit for bit.
+"""
+
+import numpy as np
+import pytest
+
+import dense_fp32_gemm_row_gb300 as g
+import oracle
+from seeded_inputs import make_workload
+
+from . import _gpu
+from .test_gemm_gpu import _check, _ex_case
+
+pytestmark = pytest.mark.gpu
+
+NOALLOC_SCRATCH_BYTES = 16 << 20  # GEMM_F32_NOALLOC_SCRATCH_BYTES in gemm_f32.h
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    torch = pytest.importorskip("torch")
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    g.load()
+    yield
+    g.gemm_f32_release()
+
+
+@pytest.mark.parametrize("splits,want", [(2, 1), (3, 1), (4, 1), (5, 0), (8, 0), (1, 0)])
+def test_plan(splits, want):
+    M, N, K = 300, 260, 4000
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_FFMA, splits, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["splits"] == splits and p["cluster_reduce"] == want, p
+    if want:
+        assert p["workspace_bytes"] == 0 and p["kernels"] == 1, p
+
+
+def test_auto_reduces_in_cluster():
+    # AUTO's CUDA-core plan for 1000 x 1000 x 250 (64 tiles): 4 splits, in a cluster
+    M, N, K = 1000, 1000, 250
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["algo"] == g.ALGO_FFMA and p["splits"] == 4 and p["cluster_reduce"] == 1
+    A, B = make_workload(2, M=M, N=N, K=K)
+    _check(_gpu.run(A, B, g.ALGO_AUTO), oracle.ref_gemm(A, B), label="auto 1000x1000x250")
+
+
+@pytest.mark.parametrize("splits", [2, 3, 4, 8])
+@pytest.mark.parametrize("shape", [(300, 260, 4000), (129, 1000, 2049), (1025, 1023, 1000)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_parity_and_equal_to_workspace_reduction(shape, splits):
+    M, N, K = shape
+    A, B = make_workload(1, M=M, N=N, K=K)
+    C = _gpu.run(A, B, g.ALGO_FFMA, splits)
+    _check(C, oracle.ref_gemm(A, B), label=f"cluster reduce {shape} s{splits}")
+    # the workspace path of the same kernel (narrow tiles at these sizes),
+    # where its partials and padded copies fit the no-allocation scratch
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_FFMA, splits, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert p["tile_n"] == 128
+    ld4 = lambda x: (x + 3) // 4 * 4
+    need = 4 * (splits * M * ld4(N) + (M * ld4(K) if K % 4 else 0) + (K * ld4(N) if N % 4 else 0))
+    if need > NOALLOC_SCRATCH_BYTES:
+        return
+    t = _gpu.torch()
+    a = t.from_numpy(A).cuda()
+    b = t.from_numpy(B).cuda()
+    c = t.empty((M, N), device="cuda")
+    s = t.cuda.current_stream()
+    g.check(g.gemm_f32_noalloc(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, splits,
+                               s.cuda_stream), "noalloc")
+    s.synchronize()
+    W = c.cpu().numpy()
+    assert np.array_equal(C.view(np.uint32), W.view(np.uint32)), "differs from the workspace sum"
+
+
+def test_wide_tiles_in_cluster():
+    M, N, K = 384, 700, 3000
+    A, B = make_workload(2, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_FFMA, g.TILE_128x256, 3)
+    _check(C, oracle.ref_gemm(A, B), label="wide tiles, 3 splits in a cluster")
+
+
+def test_alpha_beta_applied_by_the_cluster_reduction():
+    _ex_case(200, 300, 5000, 0, 0, 3, -0.75, 1.5, g.ALGO_FFMA, splits=4)
+    _ex_case(200, 300, 5000, 1, 1, 0, 2.0, 0.0, g.ALGO_FFMA, splits=3, c_nan=True)
+
+
+def test_quantised_exact_in_cluster():
+    A, B = make_workload(0)
+    C = _gpu.run(A, B, g.ALGO_FFMA, 4)
+    _check(C, oracle.ref_gemm(A, B), exact=True, label="quantised 512^3, 4 splits in a cluster")
