@@ -451,6 +451,12 @@ __device__ __forceinline__ float4 sub4(float4 a, float4 b) {
     return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w);
 }
 
+// The TF32 split of four values: hi = tf32(x), lo = tf32(x - hi).
+__device__ __forceinline__ void split4(float4 x, float4& hi, float4& lo) {
+    hi = tf32x4(x);
+    lo = tf32x4(sub4(x, hi));
+}
+
 __device__ __forceinline__ float lane_of(float4 v, int e) {
     return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
 }
@@ -473,10 +479,11 @@ __device__ __forceinline__ void split_a_stage(uint32_t sa, int t) {
         for (int j = 0; j < 8; ++j) v[j] = lds128(sa + 16 * t + 1024 * (i0 + j));
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const float4 h = tf32x4(v[j]);
+            float4 h, l;
+            split4(v[j], h, l);
             const uint32_t a = sa + 16 * t + 1024 * (i0 + j);
             sts128(a, h);
-            sts128(a + 16384, tf32x4(sub4(v[j], h)));
+            sts128(a + 16384, l);
         }
     }
 }
@@ -521,10 +528,11 @@ __device__ __forceinline__ void split_b_stage(uint32_t sb, int w, int lane) {
                 // lane e of the rotated words is column n; k = 4 kq + 0..3
                 const float4 x = make_float4(lane_of(v[jj][h][0], e), lane_of(v[jj][h][1], e),
                                              lane_of(v[jj][h][2], e), lane_of(v[jj][h][3], e));
-                const float4 hi = tf32x4(x);
+                float4 hi, lo;
+                split4(x, hi, lo);
                 const uint32_t a = sb + n * 128 + ((kq ^ (n & 7)) << 4);
                 sts128(a, hi);
-                sts128(a + 16384, tf32x4(sub4(x, hi)));
+                sts128(a + 16384, lo);
             }
         }
 }
