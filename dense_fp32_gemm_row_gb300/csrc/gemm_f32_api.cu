@@ -144,7 +144,8 @@ struct Plan {
     int bn = 0;
     int pair = 0;     // 3xTF32: two-CTA kernel
     int split_in_kernel = 0;  // 3xTF32 pair kernel: TF32 split done in shared memory
-    int cluster_splits = 0;   // FFMA: split-K partials added inside a cluster (2..8)
+    int cluster_splits = 0;   // FFMA: split-K partials added inside a cluster (2..4)
+    int fused_staging = 0;    // 3xTF32 staged: A and B split by one launch
     int box_n = 0;    // 3xTF32: B^T rows per TMA box
     int tail_tiles = 0, tail_splits = 0;  // pair kernel: K-split last partial round
     size_t off_t = 0;
@@ -251,13 +252,14 @@ size_t carve(size_t* off, long long bytes) {
 void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Plan* p,
                int tile = GEMM_F32_TILE_AUTO) {
     const int M = q.M, N = q.N, K = q.K;
-    // AUTO: the tensor-core kernel, except for tiny problems (under about
-    // 2.7e8 multiply-adds, e.g. 512^3), where the CUDA-core kernel's single
-    // launch beats the three of the tensor-core path (design-space sweep:
-    // 19.1 vs 26.2 us at 512^3)
+    // AUTO: the tensor-core kernel, except for tiny problems (under 5e7
+    // multiply-adds, e.g. 256^3: 17.1 against 25.2 us), where the CUDA-core
+    // kernel's single launch beats the staging launch plus GEMM of the
+    // tensor-core path.  From 512^3 on the tensor-core path is ahead (512^3:
+    // 18.0 us with 4 splits added in a cluster, against 19.1 us)
     const double macs = static_cast<double>(M) * N * K;
     p->algo = algo != GEMM_F32_ALGO_AUTO ? algo
-              : macs < 2.7e8             ? GEMM_F32_ALGO_FFMA
+              : macs < 5e7               ? GEMM_F32_ALGO_FFMA
                                          : GEMM_F32_ALGO_3XTF32;
     int bm, bn, bk, slots;
     if (p->algo == GEMM_F32_ALGO_3XTF32) {
@@ -276,8 +278,13 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         // kernel's rate but reading each operand once as stored, is faster
         // (256 x 256 x 65536: 0.097 against 0.143 ms; 2048^3: 0.139
         // against 0.099 ms the other way round).
+        // Only when the operands are big enough for the staging pass to
+        // matter (at least 16M elements: 192 MB of staging traffic); small
+        // ones are faster staged, with their split-K added in a cluster
+        // (512^3: 19.1 against 28.3 us)
         const double per_element = 2.0 * M * N / (static_cast<double>(M) + N);
-        if (per_element < 700.0) {
+        const double operand_elements = (static_cast<double>(M) + N) * K;
+        if (per_element < 700.0 && operand_elements >= 16e6) {
             p->pair = 1;
             p->split_in_kernel = 1;
             p->bn = 256;
@@ -313,9 +320,16 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     const int tiles = ((M + bm - 1) / bm) * ((N + bn - 1) / bn);
     const int kb_total = (K + bk - 1) / bk;
     // the CUDA-core kernel keeps >= 2 K blocks a split (512^3: 8 splits,
-    // 19.1 us, against 25.2 us with 4); the tensor-core kernels >= 4
-    const int s = choose_splits(splits, tiles, kb_total, slots,
-                                p->algo == GEMM_F32_ALGO_FFMA ? 2 : 4);
+    // 19.1 us, against 25.2 us with 4) unless K is at most 4 blocks (128^3:
+    // 4 splits of one block, 13.0 us, against 17.1 us with 2); the
+    // tensor-core kernels >= 4
+    int s = choose_splits(splits, tiles, kb_total, slots,
+                          p->algo == GEMM_F32_ALGO_FFMA ? (kb_total <= 4 ? 1 : 2) : 4);
+    // The single-CTA tensor-core kernel adds up to 8 splits inside a cluster
+    // (no reduction launch, ~6 us saved); for K <= 4096 that beats the extra
+    // splits' shorter main loops (300 x 260 x 3000: 8 splits in a cluster
+    // 25.8 us, 16 through the workspace 28.3 us)
+    if (splits == 0 && p->algo == GEMM_F32_ALGO_3XTF32 && !p->pair && s > 8 && K <= 4096) s = 8;
     p->kb_per_split = (kb_total + s - 1) / s;
     p->splits = (kb_total + p->kb_per_split - 1) / p->kb_per_split;
     const int units = tiles * p->splits;
@@ -353,6 +367,11 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     // measured faster from 8 splits on (512^3: 19.1 against 23.2 us)
     if (p->algo == GEMM_F32_ALGO_FFMA && p->splits >= 2 && p->splits <= 4)
         p->cluster_splits = p->splits;
+    // The single-CTA tensor-core kernel likewise, when every CTA gets exactly
+    // one unit (its stage memory then holds the partial after the main loop)
+    if (p->algo == GEMM_F32_ALGO_3XTF32 && !p->pair && p->splits >= 2 && p->splits <= 8 &&
+        units <= d.sm_count)
+        p->cluster_splits = p->splits;
     if (p->splits > 1 && !p->cluster_splits)
         p->off_w = carve(&off, static_cast<long long>(p->splits) * M * p->ldw * 4);
     // The pair kernel's last round of tiles is usually only partly full
@@ -374,8 +393,11 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     }
     cudaGetLastError();
     p->ws_bytes = off;
-    p->kernels = 1 + p->stage_a + p->stage_b + (p->splits > 1 && !p->cluster_splits ? 1 : 0) +
-                 (p->tail_tiles ? 1 : 0);
+    // pre-split operands as stored (A row-major, B not transposed): one
+    // staging launch for both
+    p->fused_staging = p->algo == GEMM_F32_ALGO_3XTF32 && !p->split_in_kernel && !q.ta && !q.tb;
+    p->kernels = 1 + p->stage_a + p->stage_b - p->fused_staging +
+                 (p->splits > 1 && !p->cluster_splits ? 1 : 0) + (p->tail_tiles ? 1 : 0);
 }
 
 // Device operands the GEMM kernel reads, after staging.
@@ -499,6 +521,7 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
         ta.tail_tiles = p.tail_tiles;
         ta.tail_splits = p.tail_splits;
         ta.tail_ws = p.tail_tiles ? reinterpret_cast<float*>(ws + p.off_t) : nullptr;
+        ta.cluster_splits = p.cluster_splits;
         if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
             return static_cast<int>(e);
         if ((e = launch_sgemm_3xtf32(ta, stream, d.sm_count)) != cudaSuccess)
@@ -567,8 +590,22 @@ int enqueue(const Problem& q, int algo, int splits, DeviceState* d, int dev, cud
         ws = static_cast<unsigned char*>(w);
     }
     Operands o;
-    if ((st = stage_a(p, q, 0, q.M, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
-    if ((st = stage_b(p, q, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
+    if (p.fused_staging) {
+        float* a_hi = reinterpret_cast<float*>(ws + p.off_a);
+        float* a_lo = reinterpret_cast<float*>(ws + p.off_a2);
+        float* b_hi = reinterpret_cast<float*>(ws + p.off_b);
+        float* b_lo = reinterpret_cast<float*>(ws + p.off_b2);
+        const cudaError_t e = launch_split_operands(q.A, q.lda, q.M, q.K, a_hi, a_lo, p.lda, q.B,
+                                                    q.ldb, q.N, b_hi, b_lo, p.ldb, stream);
+        if (e != cudaSuccess) return static_cast<int>(e);
+        o.a_hi = a_hi;
+        o.a_lo = a_lo;
+        o.b_hi = b_hi;
+        o.b_lo = b_lo;
+    } else {
+        if ((st = stage_a(p, q, 0, q.M, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
+        if ((st = stage_b(p, q, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
+    }
     return launch_gemm(p, *d, o, q.C, q.ldc, q.M, q.N, q.K, q.alpha, q.beta, scale_mode(q), ws,
                        stream, ev_begin, ev_end);
 }

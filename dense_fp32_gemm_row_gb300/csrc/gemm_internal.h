@@ -78,6 +78,10 @@ struct Tf32x3Args {
     // 256 x 256 floats) and summed into C by a fix-up kernel
     int tail_tiles, tail_splits;
     float* tail_ws;
+    // single-CTA kernels, 0 or 2..8 (equal to splits, one unit per CTA): each
+    // tile's splits run as one cluster and add their partials in split order
+    // through distributed shared memory; out is C
+    int cluster_splits;
 };
 // co-resident two-CTA clusters of the pair kernel on the current device
 cudaError_t tf32x3_pair_clusters(int sm_count, int* clusters);
@@ -92,6 +96,11 @@ cudaError_t launch_split_rows(const float* src, long long lds, long long rows, l
 // hi/lo[n*ldt + k] from src[k*lds + n] (K x N -> N x K)
 cudaError_t launch_split_transpose(const float* src, long long lds, int K, int N, float* hi,
                                    float* lo, long long ldt, cudaStream_t s);
+// both of the above in one launch: A (M x K, row stride lda) -> a_hi/a_lo
+// (row stride ldd) and B (K x N, row stride ldb) -> b_hi/b_lo (N x K, ldt)
+cudaError_t launch_split_operands(const float* a, long long lda, int M, int K, float* a_hi,
+                                  float* a_lo, long long ldd, const float* b, long long ldb, int N,
+                                  float* b_hi, float* b_lo, long long ldt, cudaStream_t s);
 
 // ---- helper kernels (gemm_aux.cu) ------------------------------------------
 // dst[r*ldd + c] = src[r*lds + c] for r < rows, c < cols

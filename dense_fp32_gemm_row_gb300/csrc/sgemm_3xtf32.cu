@@ -53,6 +53,16 @@ constexpr int UMMA_K = 8;   // K of one kind::tf32 MMA
 constexpr int CH = 4;       // K blocks per tensor-core chunk (128-deep K)
 constexpr int EPI_COLS = 128;  // accumulator columns per epilogue thread
 constexpr int GROUP_M = 8;
+constexpr int kMaxClusterSplits = 8;  // split-K partials added inside a (portable) cluster
+
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t cluster_addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
 
 template <int BN, int STAGES>
 struct Cfg {
@@ -76,12 +86,15 @@ struct Unit {
     int slot;  // >= 0: a K share of a tail tile, written raw to the tail workspace
 };
 
+// Work unit u: split u / tiles of tile u % tiles (split-major), or, when the
+// splits of a tile form one cluster (cluster_splits = S > 0), split u % S of
+// tile u / S (tile-major, so that a cluster's CTAs share a tile).
 __device__ __forceinline__ Unit decode(int u, int tiles_m, int tiles_n, int kb_per_split,
-                                       int kb_total, int bn, int bm = BM) {
+                                       int kb_total, int bn, int bm = BM, int cluster_splits = 0) {
     const int tiles = tiles_m * tiles_n;
     Unit w;
-    w.split = u / tiles;
-    const int t = u - w.split * tiles;
+    w.split = cluster_splits ? u % cluster_splits : u / tiles;
+    const int t = cluster_splits ? u / cluster_splits : u - w.split * tiles;
     const int per_group = GROUP_M * tiles_n;
     const int group = t / per_group;
     const int first_m = group * GROUP_M;
@@ -170,7 +183,7 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
                     const __grid_constant__ CUtensorMap tmBlo, float* __restrict__ out,
                     long long ldo, long long split_stride, int M, int N, int K, int kb_per_split,
                     int splits, int vec_store, unsigned* fault, long long timeout_ns,
-                    float alpha, float beta, int scale_mode) {
+                    float alpha, float beta, int scale_mode, int cluster_splits) {
     using C = Cfg<BN, STAGES>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -224,7 +237,8 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
             int it = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, BN);
+                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, BN, BM,
+                                      cluster_splits);
                 for (int kb = 0; kb < w.nkb; ++kb, ++it) {
                     const int s = it % STAGES;
                     if (it >= STAGES &&
@@ -259,7 +273,8 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
             int g = 0;   // chunks issued (tensor-memory buffer g & 1)
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, BN);
+                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, BN, BM,
+                                      cluster_splits);
                 for (int c0 = 0; c0 < w.nkb && ok; c0 += CH, ++g) {
                     const int buf = g & 1;
                     if (g >= 2 && !role_wait(acce0 + 8 * buf, ((g >> 1) & 1) ^ 1, timeout_ns, fault,
@@ -314,7 +329,8 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
         int g = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, BN);
+            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, BN, BM,
+                                  cluster_splits);
             for (int c0 = 0; c0 < w.nkb; c0 += CH, ++g) {
                 const int buf = g & 1;
                 const bool got = role_wait(accf0 + 8 * buf, (g >> 1) & 1, timeout_ns, fault,
@@ -346,6 +362,18 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
                 if (lane == 0) mbar_arrive(acce0 + 8 * buf);
             }
             if (!ok) break;
+            if (cluster_splits) {
+                // this CTA's only unit: its partial tile goes into the stage
+                // memory (every MMA, and so every operand read, has completed),
+                // row-major 128 x BN with 16-byte word c of row r at c ^ (r & 7)
+#pragma unroll
+                for (int j = 0; j < EPI_COLS; j += 4) {
+                    const int c4 = (col0 + j) >> 2;
+                    sts128(sbase + 16u * static_cast<uint32_t>(row * (BN / 4) + (c4 ^ (row & 7))),
+                           make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]));
+                }
+                continue;
+            }
             const int m = w.m0 + row;
             if (m < M) {
                 float* orow = out + static_cast<long long>(w.split) * split_stride +
@@ -357,6 +385,48 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
                            vec_store != 0, alpha, beta, scale_mode);
             }
         }
+    }
+
+    if (cluster_splits) {
+        // ---- split-K reduction inside the cluster: the S CTAs of the cluster
+        // hold the S K splits of one tile (each its only unit).  Every thread
+        // of every CTA takes both barriers, whatever its role did. ----
+        cluster_sync();  // all partials parked and visible across the cluster
+        const int S = cluster_splits;
+        const uint32_t rank = cluster_ctarank();
+        const Unit w = decode(static_cast<int>(blockIdx.x), tiles_m, tiles_n, kb_per_split,
+                              kb_total, BN, BM, S);
+        const int rows = (BM + S - 1) / S;
+        const int r0 = static_cast<int>(rank) * rows;
+        const int r1 = min(BM, r0 + rows);
+        constexpr int Q = BN / 4;  // 16-byte words per tile row
+        uint32_t peer[kMaxClusterSplits];
+#pragma unroll
+        for (int q = 0; q < kMaxClusterSplits; ++q)
+            peer[q] = q < S ? map_to_cta(sbase, static_cast<uint32_t>(q)) : 0u;
+        if (ld_shared_volatile(abort_flag) == 0u) {
+            for (int idx = threadIdx.x; idx < (r1 - r0) * Q; idx += C::THREADS) {
+                const int i = r0 + idx / Q;
+                const int c4 = idx - (idx / Q) * Q;
+                const int m = w.m0 + i;
+                if (m >= M) continue;
+                const uint32_t off = 16u * static_cast<uint32_t>(i * Q + (c4 ^ (i & 7)));
+                float4 sum = ld_dsmem_v4(peer[0] + off);
+#pragma unroll
+                for (int q = 1; q < kMaxClusterSplits; ++q) {
+                    if (q < S) {
+                        const float4 v = ld_dsmem_v4(peer[q] + off);
+                        sum.x += v.x;
+                        sum.y += v.y;
+                        sum.z += v.z;
+                        sum.w += v.w;
+                    }
+                }
+                store4(out + static_cast<long long>(m) * ldo, w.n0 + 4 * c4, N, sum,
+                       vec_store != 0, alpha, beta, scale_mode);
+            }
+        }
+        cluster_sync();  // no CTA leaves while a partner may still read its partial
     }
 
     tc_fence_before();
@@ -381,11 +451,34 @@ cudaError_t launch_impl(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
         attr_done_dev = dev;
     }
     const int units = ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN) * a.splits;
+    if (a.cluster_splits) {
+        // one unit per CTA, the splits of a tile as one cluster
+        if (a.cluster_splits != a.splits || a.splits < 2 || a.splits > kMaxClusterSplits)
+            return cudaErrorInvalidValue;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(a.splits);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(units));
+        cfg.blockDim = dim3(C::THREADS);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel<BN, STAGES>, a.tmAhi, a.tmAlo, a.tmBhi,
+                               a.tmBlo, a.out, a.ldo, a.split_stride, a.M, a.N, a.K,
+                               a.kb_per_split, a.splits, a.vec_store, a.fault, a.timeout_ns,
+                               a.alpha, a.beta, a.scale_mode, a.cluster_splits);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     const int grid = units < sm_count ? units : sm_count;
     sgemm_3xtf32_kernel<BN, STAGES><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(
         a.tmAhi, a.tmAlo, a.tmBhi, a.tmBlo, a.out, a.ldo, a.split_stride, a.M, a.N, a.K,
         a.kb_per_split, a.splits, a.vec_store, a.fault, a.timeout_ns, a.alpha, a.beta,
-        a.scale_mode);
+        a.scale_mode, 0);
     return cudaGetLastError();
 }
 

@@ -43,11 +43,15 @@ def test_plan(splits, want):
 
 
 def test_auto_reduces_in_cluster():
-    # AUTO's CUDA-core plan for 1000 x 1000 x 250 (64 tiles): 4 splits, in a cluster
+    # the CUDA-core plan for 1000 x 1000 x 250 (64 tiles): 4 splits, in a cluster
     M, N, K = 1000, 1000, 250
-    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
-    assert st == 0 and p["algo"] == g.ALGO_FFMA and p["splits"] == 4 and p["cluster_reduce"] == 1
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_FFMA, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["splits"] == 4 and p["cluster_reduce"] == 1
     A, B = make_workload(2, M=M, N=N, K=K)
+    _check(_gpu.run(A, B, g.ALGO_FFMA), oracle.ref_gemm(A, B), label="ffma 1000x1000x250")
+    # AUTO's choice there: the tensor-core kernel, 2 splits, in a cluster
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["splits"] == 2 and p["cluster_reduce"] == 1
     _check(_gpu.run(A, B, g.ALGO_AUTO), oracle.ref_gemm(A, B), label="auto 1000x1000x250")
 
 
@@ -95,3 +99,53 @@ def test_quantised_exact_in_cluster():
     A, B = make_workload(0)
     C = _gpu.run(A, B, g.ALGO_FFMA, 4)
     _check(C, oracle.ref_gemm(A, B), exact=True, label="quantised 512^3, 4 splits in a cluster")
+
+
+# ---- the single-CTA tensor-core (3xTF32) kernel: 2..8 splits, one unit per CTA ----
+
+def _configured(A, B, tile, splits):
+    return _gpu.run_configured(A, B, g.ALGO_3XTF32, tile, splits)
+
+
+@pytest.mark.parametrize("tile,splits", [(g.TILE_128x128, 2), (g.TILE_128x128, 3),
+                                         (g.TILE_128x128, 5), (g.TILE_128x128, 8),
+                                         (g.TILE_128x256, 3)])
+def test_3xtf32_cluster_equals_split_order_sum_of_partials(tile, splits):
+    # Each split's partial is the same kernel run alone on that K range (same
+    # tile, same MMAs, same promotion chunks), so the cluster's result must be
+    # those partials added in split order, bit for bit.
+    M, N, K = 300, 260, 3000
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, tile, splits, A=1 << 32, B=1 << 36,
+                                   C=1 << 40)
+    assert st == 0 and p["splits"] == splits and p["cluster_reduce"] == 1, p
+    assert p["workspace_bytes"] > 0 and p["kernels"] == 2, p  # staging + GEMM, no reduction
+    A, B = make_workload(2, M=M, N=N, K=K)
+    C = _configured(A, B, tile, splits)
+    _check(C, oracle.ref_gemm(A, B), label=f"3xtf32 cluster {tile}/{splits}")
+    kb = (K + 31) // 32
+    per = (kb + splits - 1) // splits
+    total = None
+    for s in range(splits):
+        k0, k1 = s * per * 32, min(K, (s + 1) * per * 32)
+        part = _configured(np.ascontiguousarray(A[:, k0:k1]), np.ascontiguousarray(B[k0:k1]),
+                           tile, 1)
+        total = part if total is None else (total + part).astype(np.float32)
+    assert np.array_equal(C.view(np.uint32), total.view(np.uint32)), \
+        "cluster sum differs from the split-order sum of the partials"
+
+
+def test_3xtf32_auto_ragged_plan_reduces_in_cluster():
+    st, p = g.gemm_f32_plan(1025, 1023, 1000, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["splits"] == 2 and p["cluster_reduce"] == 1
+
+
+def test_3xtf32_more_units_than_sms_uses_the_workspace():
+    # 40 x 40 tiles x 2 splits = 3200 units: persistent CTAs take several
+    # units each, so the partials go through the workspace
+    st, p = g.gemm_f32_plan_config(5120, 5120, 4096, g.ALGO_3XTF32, g.TILE_128x128, 2,
+                                   A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["cluster_reduce"] == 0, p
+
+
+def test_3xtf32_cluster_alpha_beta():
+    _ex_case(300, 260, 3000, 0, 0, 5, 0.5, -1.25, g.ALGO_3XTF32, splits=4)
