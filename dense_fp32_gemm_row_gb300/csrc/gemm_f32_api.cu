@@ -320,16 +320,20 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     const int tiles = ((M + bm - 1) / bm) * ((N + bn - 1) / bn);
     const int kb_total = (K + bk - 1) / bk;
     // the CUDA-core kernel keeps >= 2 K blocks a split (512^3: 8 splits,
-    // 19.1 us, against 25.2 us with 4) unless K is at most 4 blocks (128^3:
-    // 4 splits of one block, 13.0 us, against 17.1 us with 2); the
-    // tensor-core kernels >= 4
+    // 19.1 us, against 25.2 us with 4) unless K is at most 8 blocks (128^3:
+    // 4 splits of one block, 13.0 us, against 17.1 us with 2; 256^3: 8
+    // splits, 15.0 us, against 17.0 us with 4); the tensor-core kernels >= 4
     int s = choose_splits(splits, tiles, kb_total, slots,
-                          p->algo == GEMM_F32_ALGO_FFMA ? (kb_total <= 4 ? 1 : 2) : 4);
+                          p->algo == GEMM_F32_ALGO_FFMA ? (kb_total <= 8 ? 1 : 2) : 4);
     // The single-CTA tensor-core kernel adds up to 8 splits inside a cluster
     // (no reduction launch, ~6 us saved); for K <= 4096 that beats the extra
     // splits' shorter main loops (300 x 260 x 3000: 8 splits in a cluster
-    // 25.8 us, 16 through the workspace 28.3 us)
-    if (splits == 0 && p->algo == GEMM_F32_ALGO_3XTF32 && !p->pair && s > 8 && K <= 4096) s = 8;
+    // 25.8 us, 16 through the workspace 28.3 us), and for K <= 1024 four
+    // splits beat eight (400 x 400 x 1024: 21.1 against 25.2 us)
+    if (splits == 0 && p->algo == GEMM_F32_ALGO_3XTF32 && !p->pair && K <= 4096) {
+        const int cap = K <= 1024 ? 4 : 8;
+        if (s > cap) s = cap;
+    }
     p->kb_per_split = (kb_total + s - 1) / s;
     p->splits = (kb_total + p->kb_per_split - 1) / p->kb_per_split;
     const int units = tiles * p->splits;

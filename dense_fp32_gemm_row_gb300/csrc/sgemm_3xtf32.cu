@@ -53,6 +53,12 @@ constexpr int UMMA_K = 8;   // K of one kind::tf32 MMA
 constexpr int CH = 4;       // K blocks per tensor-core chunk (128-deep K)
 constexpr int EPI_COLS = 128;  // accumulator columns per epilogue thread
 constexpr int GROUP_M = 8;
+// K blocks between an L2 prefetch and the load of the same boxes, in the
+// pair kernel that splits in shared memory: its stages wait on DRAM (it reads
+// each operand once), and prefetching two blocks ahead took 256 x 256 x 65536
+// from 88.7 to 84.5 us.  The kernels on pre-split operands run slower with
+// prefetching (8192^3: 3.85 against 4.42 ms), so they do not prefetch.
+constexpr int kPrefetchAhead = 2;
 constexpr int kMaxClusterSplits = 8;  // split-K partials added inside a (portable) cluster
 
 __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t cluster_addr) {
@@ -255,6 +261,7 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
                     tma_load_2d(st + C::A_BYTES, &tmAlo, fb, k0, w.m0);
                     tma_load_2d(st + 2 * C::A_BYTES, &tmBhi, fb, k0, w.n0);
                     tma_load_2d(st + 2 * C::A_BYTES + C::B_BYTES, &tmBlo, fb, k0, w.n0);
+
                 }
             }
             // wind down: every issued copy has landed and every stage has been
@@ -725,6 +732,13 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                         for (int j = 0; j < C::HALF_N / C::B_BOX_N; ++j)
                             tma_load_2d(st + 2 * C::A_BYTES + j * C::B_BOX_BYTES, &tmBhi, fb,
                                         nb + j * C::B_BOX_N, k0);
+                        if (kb + kPrefetchAhead < w.nkb) {
+                            const int kp = k0 + kPrefetchAhead * BK;
+                            tma_prefetch_2d(&tmAhi, kp, ma);
+#pragma unroll
+                            for (int j = 0; j < C::HALF_N / C::B_BOX_N; ++j)
+                                tma_prefetch_2d(&tmBhi, nb + j * C::B_BOX_N, kp);
+                        }
                     } else {
                         const uint32_t fb = map_to_cta(full0 + 8 * s, 0);
                         mbar_arrive_expect_tx_cluster(fb, C::STAGE_BYTES);

@@ -3,10 +3,9 @@ hi/lo parts in shared memory (GEMM_F32_TILE_256x256_PAIR_SPLIT) instead of
 reading copies written by staging kernels.
 
 Against the oracle, elementwise within 1e-3 + 1e-3 |C_ref| (NaN guard bands
-around C); against the pre-split pair kernel, bit for bit: both form the same
-hi = tf32(x), lo = tf32(x - hi) values and issue the same MMAs in the same
-order, the B operand only being read through a different shared-memory
-layout.
+around C); against the pre-split pair kernel, bit for bit when neither splits
+K: both form the same hi = tf32(x), lo = tf32(x - hi) values and issue the
+same MMAs in the same order, promoted in the same 128-deep chunks.
 """
 
 import numpy as np
@@ -58,9 +57,13 @@ def test_parity_and_equal_to_presplit(shape):
     C = _gpu.run_configured(A, B, g.ALGO_3XTF32, SPLIT)
     rows, cols = _sample(M, N, M * 7 + N + K)
     _check(C[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols), label=f"split {shape}")
-    C0 = _gpu.run_configured(A, B, g.ALGO_3XTF32, PRESPLIT)
-    assert np.array_equal(C.view(np.uint32), C0.view(np.uint32)), \
-        f"differs from the pre-split kernel at {np.argwhere(C.view(np.uint32) != C0.view(np.uint32))[:5]}"
+    # bit for bit against the staged pair kernel, both without split-K (the
+    # two kernels' stages are 32 and 16 deep, so their split-K boundaries
+    # differ; their 128-deep promotion chunks coincide)
+    C1 = _gpu.run_configured(A, B, g.ALGO_3XTF32, SPLIT, 1)
+    C0 = _gpu.run_configured(A, B, g.ALGO_3XTF32, PRESPLIT, 1)
+    assert np.array_equal(C1.view(np.uint32), C0.view(np.uint32)), \
+        f"differs from the pre-split kernel at {np.argwhere(C1.view(np.uint32) != C0.view(np.uint32))[:5]}"
 
 
 @pytest.mark.parametrize("splits", [2, 7])
