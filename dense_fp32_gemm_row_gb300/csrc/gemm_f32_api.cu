@@ -148,6 +148,7 @@ struct Plan {
     int fused_staging = 0;    // 3xTF32 staged: A and B split by one launch
     int box_n = 0;    // 3xTF32: B^T rows per TMA box
     int tail_tiles = 0, tail_splits = 0;  // pair kernel: K-split last partial round
+    int tail_m = 0, tail_n = 0;           // the output extent the tail split was planned for
     size_t off_t = 0;
     int splits = 1;
     int kb_per_split = 0;
@@ -391,6 +392,8 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         if (r && t >= 2 && kb_total >= 2 * t) {
             p->tail_tiles = r;
             p->tail_splits = t;
+            p->tail_m = M;
+            p->tail_n = N;
             p->off_t = carve(&off, static_cast<long long>(r) * t * 256 * 256 * 4);
             p->ctas = 2 * clusters;
         }
@@ -522,9 +525,13 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
         ta.alpha = alpha;
         ta.beta = beta;
         ta.scale_mode = kmode;
-        ta.tail_tiles = p.tail_tiles;
-        ta.tail_splits = p.tail_splits;
-        ta.tail_ws = p.tail_tiles ? reinterpret_cast<float*>(ws + p.off_t) : nullptr;
+        // the tail split names tiles of the extent it was planned for; a
+        // launch on another extent (a shorter last row panel, a column
+        // block) runs without it
+        const bool tail = p.tail_tiles && M == p.tail_m && N == p.tail_n;
+        ta.tail_tiles = tail ? p.tail_tiles : 0;
+        ta.tail_splits = tail ? p.tail_splits : 0;
+        ta.tail_ws = tail ? reinterpret_cast<float*>(ws + p.off_t) : nullptr;
         ta.cluster_splits = p.cluster_splits;
         if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
             return static_cast<int>(e);
@@ -631,12 +638,14 @@ int run(const Problem& q, int algo, int splits, cudaStream_t stream,
 
 // ---- host-buffer entry: copies overlapped with the GEMM, by row panels ----
 constexpr int kMaxPanels = 16;
+constexpr int kMaxColBlocks = 4;  // column blocks of the first and last row panel
 
 struct HostPipe {
     bool ready = false;
     cudaStream_t s_in = nullptr, s_out = nullptr;
     cudaEvent_t ev_start = nullptr, ev_b = nullptr, ev_done = nullptr;
     cudaEvent_t ev_a[kMaxPanels] = {}, ev_c[kMaxPanels] = {};
+    cudaEvent_t ev_bblk[kMaxColBlocks] = {}, ev_cblk[kMaxColBlocks] = {};
     void* dev_buf = nullptr;  // device copies of A, B and C
     size_t dev_bytes = 0;
 };
@@ -657,6 +666,10 @@ int host_pipe(int dev, cudaStream_t stream, size_t bytes, HostPipe** out) {
         for (int i = 0; i < kMaxPanels; ++i)
             if ((e = cudaEventCreateWithFlags(&hp.ev_a[i], fl)) != cudaSuccess ||
                 (e = cudaEventCreateWithFlags(&hp.ev_c[i], fl)) != cudaSuccess)
+                return static_cast<int>(e);
+        for (int i = 0; i < kMaxColBlocks; ++i)
+            if ((e = cudaEventCreateWithFlags(&hp.ev_bblk[i], fl)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&hp.ev_cblk[i], fl)) != cudaSuccess)
                 return static_cast<int>(e);
         hp.ready = true;
     }
@@ -816,36 +829,132 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
     qp.M = P;
     Plan p;
     make_plan(*d, qp, algo, 0, &p);
+
+    // Column blocks.  With row panels alone the first GEMM waits for all of
+    // B (8192^3: 1.25 ms of copying).  On staged tensor-core operands the
+    // first and the last row panel are instead computed by column blocks of
+    // B: the first block's GEMM starts once panel 0 of A and that block of B
+    // are on the device (B's blocks are staged into the full B^T planes, so
+    // the middle panels reuse them), and the last panel's blocks go back to
+    // the host one by one, so only the last block's copy is not overlapped.
+    const int nc = static_cast<int>(round_up((N + 3) / 4, 256));
+    const int nblk = (N + nc - 1) / nc;
+    Plan pc;
+    bool col_blocks = p.algo == GEMM_F32_ALGO_3XTF32 && !p.split_in_kernel && p.splits == 1 &&
+                      panels >= 2 && N >= 1024 && nblk >= 2 && nblk <= kMaxColBlocks;
+    if (col_blocks) {
+        Problem qc = qp;
+        qc.N = nc;
+        make_plan(*d, qc, algo, 0, &pc);
+        // the block GEMMs read the panel plan's staged operands; only their
+        // split-K partials or tail shares need space, after the panel plan's
+        col_blocks = pc.algo == GEMM_F32_ALGO_3XTF32 && !pc.split_in_kernel &&
+                     pc.lda == p.lda && pc.ldb == p.ldb && pc.tile_k == p.tile_k;
+        pc.off_w += p.ws_bytes;
+        pc.off_t += p.ws_bytes;
+    }
+    const size_t ws_total = p.ws_bytes + (col_blocks ? pc.ws_bytes : 0);
     unsigned char* ws = nullptr;
-    if (p.ws_bytes) {
+    if (ws_total) {
         void* w = nullptr;
-        if ((st = workspace(dev, stream, p.ws_bytes, &w)) != GEMM_F32_SUCCESS) return st;
+        if ((st = workspace(dev, stream, ws_total, &w)) != GEMM_F32_SUCCESS) return st;
         ws = static_cast<unsigned char*>(w);
     }
 
-    GEMM_F32_TRY(cudaMemcpyAsync(dB, B, static_cast<size_t>(K) * N * 4, cudaMemcpyHostToDevice,
-                                 hp->s_in));
-    GEMM_F32_TRY(cudaEventRecord(hp->ev_b, hp->s_in));
-    GEMM_F32_TRY(cudaStreamWaitEvent(stream, hp->ev_b, 0));
-    Operands o;
-    if ((st = stage_b(p, q, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
-
-    for (int i = 0; i < panels; ++i) {
-        const int r0 = i * P;
-        const int mp = (M - r0) < P ? (M - r0) : P;
-        const size_t off_a = static_cast<size_t>(r0) * K, off_c = static_cast<size_t>(r0) * N;
-        GEMM_F32_TRY(cudaMemcpyAsync(dA + off_a, A + off_a, static_cast<size_t>(mp) * K * 4,
+    if (!col_blocks) {
+        GEMM_F32_TRY(cudaMemcpyAsync(dB, B, static_cast<size_t>(K) * N * 4,
                                      cudaMemcpyHostToDevice, hp->s_in));
-        GEMM_F32_TRY(cudaEventRecord(hp->ev_a[i], hp->s_in));
-        GEMM_F32_TRY(cudaStreamWaitEvent(stream, hp->ev_a[i], 0));
-        if ((st = stage_a(p, q, r0, mp, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
-        if ((st = launch_gemm(p, *d, o, dC + off_c, N, mp, N, K, 1.0f, 0.0f, 0, ws, stream,
-                              nullptr, nullptr)) != GEMM_F32_SUCCESS)
-            return st;
-        GEMM_F32_TRY(cudaEventRecord(hp->ev_c[i], stream));
-        GEMM_F32_TRY(cudaStreamWaitEvent(hp->s_out, hp->ev_c[i], 0));
-        GEMM_F32_TRY(cudaMemcpyAsync(C + off_c, dC + off_c, static_cast<size_t>(mp) * N * 4,
-                                     cudaMemcpyDeviceToHost, hp->s_out));
+        GEMM_F32_TRY(cudaEventRecord(hp->ev_b, hp->s_in));
+        GEMM_F32_TRY(cudaStreamWaitEvent(stream, hp->ev_b, 0));
+        Operands o;
+        if ((st = stage_b(p, q, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
+
+        for (int i = 0; i < panels; ++i) {
+            const int r0 = i * P;
+            const int mp = (M - r0) < P ? (M - r0) : P;
+            const size_t off_a = static_cast<size_t>(r0) * K, off_c = static_cast<size_t>(r0) * N;
+            GEMM_F32_TRY(cudaMemcpyAsync(dA + off_a, A + off_a, static_cast<size_t>(mp) * K * 4,
+                                         cudaMemcpyHostToDevice, hp->s_in));
+            GEMM_F32_TRY(cudaEventRecord(hp->ev_a[i], hp->s_in));
+            GEMM_F32_TRY(cudaStreamWaitEvent(stream, hp->ev_a[i], 0));
+            if ((st = stage_a(p, q, r0, mp, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
+            if ((st = launch_gemm(p, *d, o, dC + off_c, N, mp, N, K, 1.0f, 0.0f, 0, ws, stream,
+                                  nullptr, nullptr)) != GEMM_F32_SUCCESS)
+                return st;
+            GEMM_F32_TRY(cudaEventRecord(hp->ev_c[i], stream));
+            GEMM_F32_TRY(cudaStreamWaitEvent(hp->s_out, hp->ev_c[i], 0));
+            GEMM_F32_TRY(cudaMemcpyAsync(C + off_c, dC + off_c, static_cast<size_t>(mp) * N * 4,
+                                         cudaMemcpyDeviceToHost, hp->s_out));
+        }
+    } else {
+        // copies in: A panel 0, the column blocks of B, then the other A panels
+        GEMM_F32_TRY(cudaMemcpyAsync(dA, A, static_cast<size_t>(P) * K * 4, cudaMemcpyHostToDevice,
+                                     hp->s_in));
+        GEMM_F32_TRY(cudaEventRecord(hp->ev_a[0], hp->s_in));
+        for (int c = 0; c < nblk; ++c) {
+            const int c0 = c * nc, w = (N - c0) < nc ? (N - c0) : nc;
+            GEMM_F32_TRY(cudaMemcpy2DAsync(dB + c0, static_cast<size_t>(N) * 4, B + c0,
+                                           static_cast<size_t>(N) * 4, static_cast<size_t>(w) * 4,
+                                           K, cudaMemcpyHostToDevice, hp->s_in));
+            GEMM_F32_TRY(cudaEventRecord(hp->ev_bblk[c], hp->s_in));
+        }
+        for (int i = 1; i < panels; ++i) {
+            const int r0 = i * P;
+            const int mp = (M - r0) < P ? (M - r0) : P;
+            const size_t off_a = static_cast<size_t>(r0) * K;
+            GEMM_F32_TRY(cudaMemcpyAsync(dA + off_a, A + off_a, static_cast<size_t>(mp) * K * 4,
+                                         cudaMemcpyHostToDevice, hp->s_in));
+            GEMM_F32_TRY(cudaEventRecord(hp->ev_a[i], hp->s_in));
+        }
+        Operands o;
+        float* bt_hi = reinterpret_cast<float*>(ws + p.off_b);
+        float* bt_lo = reinterpret_cast<float*>(ws + p.off_b2);
+        o.b_hi = bt_hi;
+        o.b_lo = bt_lo;
+        for (int i = 0; i < panels; ++i) {
+            const int r0 = i * P;
+            const int mp = (M - r0) < P ? (M - r0) : P;
+            const size_t off_c = static_cast<size_t>(r0) * N;
+            GEMM_F32_TRY(cudaStreamWaitEvent(stream, hp->ev_a[i], 0));
+            if ((st = stage_a(p, q, r0, mp, ws, &o, stream)) != GEMM_F32_SUCCESS) return st;
+            if (i == 0 || i == panels - 1) {
+                for (int c = 0; c < nblk; ++c) {
+                    const int c0 = c * nc, w = (N - c0) < nc ? (N - c0) : nc;
+                    if (i == 0) {
+                        // stage this block of B into rows c0.. of the B^T planes
+                        GEMM_F32_TRY(cudaStreamWaitEvent(stream, hp->ev_bblk[c], 0));
+                        GEMM_F32_TRY(launch_split_transpose(dB + c0, N, K, w,
+                                                            bt_hi + static_cast<size_t>(c0) * p.ldb,
+                                                            bt_lo + static_cast<size_t>(c0) * p.ldb,
+                                                            p.ldb, stream));
+                    }
+                    Operands ob = o;
+                    ob.b_hi = bt_hi + static_cast<size_t>(c0) * p.ldb;
+                    ob.b_lo = bt_lo + static_cast<size_t>(c0) * p.ldb;
+                    if ((st = launch_gemm(pc, *d, ob, dC + off_c + c0, N, mp, w, K, 1.0f, 0.0f, 0,
+                                          ws, stream, nullptr, nullptr)) != GEMM_F32_SUCCESS)
+                        return st;
+                    if (i == panels - 1) {
+                        // this block of the last panel is final: back to the host
+                        GEMM_F32_TRY(cudaEventRecord(hp->ev_cblk[c], stream));
+                        GEMM_F32_TRY(cudaStreamWaitEvent(hp->s_out, hp->ev_cblk[c], 0));
+                        GEMM_F32_TRY(cudaMemcpy2DAsync(
+                            C + off_c + c0, static_cast<size_t>(N) * 4, dC + off_c + c0,
+                            static_cast<size_t>(N) * 4, static_cast<size_t>(w) * 4, mp,
+                            cudaMemcpyDeviceToHost, hp->s_out));
+                    }
+                }
+                if (i == panels - 1) continue;
+            } else {
+                if ((st = launch_gemm(p, *d, o, dC + off_c, N, mp, N, K, 1.0f, 0.0f, 0, ws, stream,
+                                      nullptr, nullptr)) != GEMM_F32_SUCCESS)
+                    return st;
+            }
+            GEMM_F32_TRY(cudaEventRecord(hp->ev_c[i], stream));
+            GEMM_F32_TRY(cudaStreamWaitEvent(hp->s_out, hp->ev_c[i], 0));
+            GEMM_F32_TRY(cudaMemcpyAsync(C + off_c, dC + off_c, static_cast<size_t>(mp) * N * 4,
+                                         cudaMemcpyDeviceToHost, hp->s_out));
+        }
     }
     // the call is complete on `stream` once the last panel of C is on the host
     GEMM_F32_TRY(cudaEventRecord(hp->ev_done, hp->s_out));

@@ -382,3 +382,31 @@ def test_host_buffer_entry_k_panels(shape, algo):
         cols = np.concatenate([rng.integers(0, N, 4000), np.arange(0, M, 97) % N])
         _check(out[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols),
                label=f"host k-panels {shape} {algo}")
+
+
+@pytest.mark.parametrize("shape", [(4096, 4096, 1024), (8192, 2048, 1536), (5000, 3001, 700)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_host_buffer_entry_column_blocks(shape):
+    # row panels whose first and last panel run by column blocks of B (the
+    # first GEMM starts after one block of B; the last panel returns block by
+    # block), ragged last panel and ragged N included
+    t = _gpu.torch()
+    M, N, K = shape
+    A, B = make_workload(2, M=M, N=N, K=K)
+    hA = t.from_numpy(A).pin_memory()
+    hB = t.from_numpy(B).pin_memory()
+    hC = t.full((M + 1, N), float("nan")).pin_memory()
+    s = t.cuda.current_stream()
+    for _ in range(2):  # the second call reuses the buffers and events
+        hC.fill_(float("nan"))
+        g.check(g.gemm_f32_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), M, N, K,
+                                g.ALGO_AUTO, s.cuda_stream), "gemm_f32_host")
+        s.synchronize()
+        g.check(g.gemm_f32_device_status(1), "device status")
+        out = hC.numpy()
+        assert np.isnan(out[M:]).all(), "write past C"
+        rng = np.random.default_rng(M + N)
+        rows = np.concatenate([np.arange(M), rng.integers(0, M, 4000), np.full(N, M - 1)])
+        cols = np.concatenate([rng.integers(0, N, M), rng.integers(0, N, 4000), np.arange(N)])
+        _check(out[rows, cols].copy(), oracle.ref_gemm_entries(A, B, rows, cols),
+               label=f"host column blocks {shape}")
