@@ -137,6 +137,19 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, 
                  : "memory");
 }
 
+// ---- programmatic dependent launch ----------------------------------------
+// A kernel launched with the programmatic-stream-serialization attribute may
+// start while the kernel before it in the stream is still running (once all
+// of that kernel's blocks have started and triggered).  pdl_wait() returns
+// when that predecessor has completed and its memory writes are visible; it
+// returns at once for a kernel launched without the attribute.  Nothing the
+// predecessor writes may be read, and nothing it reads may be written, before
+// it.  pdl_trigger() lets this grid's successor launch early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- thread-block clusters ------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

@@ -29,6 +29,7 @@ constexpr int kThreads = 256;
 __global__ void __launch_bounds__(kThreads)
 pad_copy_kernel(const float* __restrict__ src, long long lds, long long rows, long long cols,
                 float* __restrict__ dst, long long ldd) {
+    pdl_trigger();
     for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
         const float* s = src + r * lds;
         float* d = dst + r * ldd;
@@ -42,6 +43,7 @@ __global__ void __launch_bounds__(kThreads)
 splitk_reduce_kernel(const float* __restrict__ ws, long long split_stride, long long ldw,
                      int splits, float* __restrict__ C, long long ldc, int M, int N, float alpha,
                      float beta, int mode) {
+    pdl_wait();  // the partials of the GEMM kernel before it
     for (long long r = blockIdx.y; r < M; r += gridDim.y) {
         const float* w = ws + r * ldw;
         float* c = C + r * ldc;
@@ -59,6 +61,7 @@ __global__ void __launch_bounds__(kThreads)
 splitk_reduce4_kernel(const float4* __restrict__ ws, long long split_stride4, long long ldw4,
                       int splits, float* __restrict__ C, long long ldc, int M, int N4, float alpha,
                       float beta, int mode) {
+    pdl_wait();  // the partials of the GEMM kernel before it
     for (long long r = blockIdx.y; r < M; r += gridDim.y) {
         const float4* w = ws + r * ldw4;
         float* c = C + r * ldc;
@@ -81,6 +84,7 @@ splitk_reduce4_kernel(const float4* __restrict__ ws, long long split_stride4, lo
 __global__ void __launch_bounds__(256)
 transpose_pad_kernel(const float* __restrict__ src, long long lds, long long rows, long long cols,
                      float* __restrict__ dst, long long ldd) {
+    pdl_trigger();
     __shared__ float tile[32][33];
     const int tx = threadIdx.x;
     const int ty = threadIdx.y;
@@ -154,16 +158,25 @@ cudaError_t launch_splitk_reduce(const float* ws, long long split_stride, long l
     const bool vec = (N % 4 == 0) && (ldw % 4 == 0) && (ldc % 4 == 0) && (split_stride % 4 == 0) &&
                      (reinterpret_cast<uintptr_t>(ws) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(C) % 16 == 0);
+    // launched programmatically after the GEMM kernel (pdl_wait in the kernel)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
     if (vec) {
-        dim3 grid(grid_1d(N / 4, kThreads, 64), gy);
-        splitk_reduce4_kernel<<<grid, kThreads, 0, s>>>(
-            reinterpret_cast<const float4*>(ws), split_stride / 4, ldw / 4, splits, C, ldc, M,
-            N / 4, alpha, beta, scale_mode);
+        cfg.gridDim = dim3(grid_1d(N / 4, kThreads, 64), gy);
+        e = cudaLaunchKernelEx(&cfg, splitk_reduce4_kernel, reinterpret_cast<const float4*>(ws),
+                               split_stride / 4, ldw / 4, splits, C, ldc, M, N / 4, alpha, beta,
+                               scale_mode);
     } else {
-        dim3 grid(grid_1d(N, kThreads, 64), gy);
-        splitk_reduce_kernel<<<grid, kThreads, 0, s>>>(ws, split_stride, ldw, splits, C, ldc, M, N,
-                                                       alpha, beta, scale_mode);
+        cfg.gridDim = dim3(grid_1d(N, kThreads, 64), gy);
+        e = cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, ws, split_stride, ldw, splits, C, ldc,
+                               M, N, alpha, beta, scale_mode);
     }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -280,12 +280,14 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         // (256 x 256 x 65536: 0.097 against 0.143 ms; 2048^3: 0.139
         // against 0.099 ms the other way round).
         // Only when the operands are big enough for the staging pass to
-        // matter (at least 16M elements: 192 MB of staging traffic); small
+        // matter (at least 20M elements: 240 MB of staging traffic); smaller
         // ones are faster staged, with their split-K added in a cluster
-        // (512^3: 19.1 against 28.3 us)
+        // (512^3: 19.1 against 28.3 us; 300 x 260 x 30000, 16.8M elements:
+        // 96 against 117 us; 1024 x 256 x 16384, 21M: 83 against 91 us the
+        // other way round)
         const double per_element = 2.0 * M * N / (static_cast<double>(M) + N);
         const double operand_elements = (static_cast<double>(M) + N) * K;
-        if (per_element < 700.0 && operand_elements >= 16e6) {
+        if (per_element < 700.0 && operand_elements >= 20e6) {
             p->pair = 1;
             p->split_in_kernel = 1;
             p->bn = 256;

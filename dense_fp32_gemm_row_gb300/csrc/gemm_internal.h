@@ -11,6 +11,16 @@ namespace gemm_f32_impl {
 // Default wait limit for every bounded mbarrier wait in the library's kernels.
 constexpr long long kDefaultTimeoutNs = 2000000000LL;  // 2 s
 
+// Launch attribute of a kernel that may start before its predecessor in the
+// stream ends (programmatic dependent launch); the kernel calls pdl_wait()
+// before it touches memory the predecessor writes or reads.
+inline cudaLaunchAttribute pdl_attribute() {
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    return a;
+}
+
 // ---- sgemm_ffma (CUDA-core FFMA kernel) -----------------------------------
 struct FfmaConfig {
     int bm, bn, bk, stages, threads, ctas_per_sm;

@@ -236,6 +236,10 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // launched programmatically: the set-up above overlapped the staging
+    // kernel; its operands are read only after this
+    pdl_wait();
+    pdl_trigger();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -463,17 +467,18 @@ cudaError_t launch_impl(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
         if (a.cluster_splits != a.splits || a.splits < 2 || a.splits > kMaxClusterSplits)
             return cudaErrorInvalidValue;
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = static_cast<unsigned>(a.splits);
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1] = pdl_attribute();
         cfg.gridDim = dim3(static_cast<unsigned>(units));
         cfg.blockDim = dim3(C::THREADS);
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = s;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
         e = cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel<BN, STAGES>, a.tmAhi, a.tmAlo, a.tmBhi,
                                a.tmBlo, a.out, a.ldo, a.split_stride, a.M, a.N, a.K,
                                a.kb_per_split, a.splits, a.vec_store, a.fault, a.timeout_ns,
@@ -482,10 +487,19 @@ cudaError_t launch_impl(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
         return cudaGetLastError();
     }
     const int grid = units < sm_count ? units : sm_count;
-    sgemm_3xtf32_kernel<BN, STAGES><<<grid, C::THREADS, C::SMEM_BYTES, s>>>(
-        a.tmAhi, a.tmAlo, a.tmBhi, a.tmBlo, a.out, a.ldo, a.split_stride, a.M, a.N, a.K,
-        a.kb_per_split, a.splits, a.vec_store, a.fault, a.timeout_ns, a.alpha, a.beta,
-        a.scale_mode, 0);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel<BN, STAGES>, a.tmAhi, a.tmAlo, a.tmBhi,
+                           a.tmBlo, a.out, a.ldo, a.split_stride, a.M, a.N, a.K, a.kb_per_split,
+                           a.splits, a.vec_store, a.fault, a.timeout_ns, a.alpha, a.beta,
+                           a.scale_mode, 0);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -704,6 +718,8 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
     cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();  // as in the single-CTA kernel
+    pdl_trigger();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -922,6 +938,7 @@ __global__ void __launch_bounds__(256)
 pair_tail_fixup_kernel(const float* __restrict__ tail_ws, int tiles_m, int tiles_n,
                        int tail_tiles, int tail_splits, float* __restrict__ C, long long ldc, int M,
                        int N, float alpha, float beta, int mode) {
+    pdl_wait();  // the shares written by the GEMM kernel before it
     constexpr int TM = 2 * BM, TN = PairCfg<3>::BN;
     const int t = blockIdx.x;
     const int i = blockIdx.y;
@@ -989,16 +1006,17 @@ cudaError_t launch_pair(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
         attr_done_dev = dev;
     }
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     const int tiles_m = (a.M + 2 * BM - 1) / (2 * BM);
     const int tiles_n = (a.N + C::BN - 1) / C::BN;
     const int units = a.tail_tiles
@@ -1013,9 +1031,17 @@ cudaError_t launch_pair(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
     if (e != cudaSuccess) return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (a.tail_tiles) {
-        pair_tail_fixup_kernel<<<dim3(a.tail_tiles, 2 * BM), C::BN, 0, s>>>(
-            a.tail_ws, tiles_m, tiles_n, a.tail_tiles, a.tail_splits, a.out, a.ldo, a.M, a.N,
-            a.alpha, a.beta, a.scale_mode);
+        cudaLaunchConfig_t fc = {};
+        cudaLaunchAttribute fattr[1] = {pdl_attribute()};
+        fc.gridDim = dim3(static_cast<unsigned>(a.tail_tiles), 2 * BM);
+        fc.blockDim = dim3(C::BN);
+        fc.stream = s;
+        fc.attrs = fattr;
+        fc.numAttrs = 1;
+        e = cudaLaunchKernelEx(&fc, pair_tail_fixup_kernel, static_cast<const float*>(a.tail_ws),
+                               tiles_m, tiles_n, a.tail_tiles, a.tail_splits, a.out, a.ldo, a.M,
+                               a.N, a.alpha, a.beta, a.scale_mode);
+        if (e != cudaSuccess) return e;
         e = cudaGetLastError();
     }
     return e;

@@ -153,6 +153,10 @@ sgemm_ffma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         fence_barrier_init();
     }
     __syncthreads();
+    // launched programmatically: operands (possibly padded by the kernel
+    // before) are read only after this
+    pdl_wait();
+    pdl_trigger();
 
     int issued = 0;  // k blocks whose loads thread 0 has issued
     if (tid == 0) {
@@ -350,26 +354,36 @@ cudaError_t launch_variant(const FfmaArgs& a, cudaStream_t s) {
         if (a.cluster_splits != a.splits || a.splits < 2 || a.splits > MAX_CLUSTER_SPLITS)
             return cudaErrorInvalidValue;
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 1;
         attr[0].val.clusterDim.y = static_cast<unsigned>(a.splits);
         attr[0].val.clusterDim.z = 1;
+        attr[1] = pdl_attribute();
         cfg.gridDim = grid;
         cfg.blockDim = dim3(THREADS);
         cfg.dynamicSmemBytes = V::SMEM_BYTES;
         cfg.stream = s;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
         e = cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.out, a.ldo, a.split_stride, a.M, a.N,
                                a.K, a.kb_per_split, a.vec_store, a.fault, a.timeout_ns, a.alpha,
                                a.beta, a.scale_mode, a.cluster_splits);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
-    kern<<<grid, THREADS, V::SMEM_BYTES, s>>>(a.tmA, a.tmB, a.out, a.ldo, a.split_stride, a.M, a.N,
-                                              a.K, a.kb_per_split, a.vec_store, a.fault,
-                                              a.timeout_ns, a.alpha, a.beta, a.scale_mode, 0);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = V::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.out, a.ldo, a.split_stride, a.M, a.N, a.K,
+                           a.kb_per_split, a.vec_store, a.fault, a.timeout_ns, a.alpha, a.beta,
+                           a.scale_mode, 0);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -16,10 +16,13 @@
 // the TMA descriptors.  Both kernels are memory-bound copies.
 #include <cstdint>
 
+#include "device_sync.cuh"
 #include "gemm_internal.h"
 
 namespace gemm_f32_impl {
 namespace {
+
+using gemm_f32_dev::pdl_trigger;
 
 __device__ __forceinline__ float to_tf32(float x) {
     uint32_t r;
@@ -115,6 +118,7 @@ __device__ __forceinline__ void split_transpose_body(const float* __restrict__ s
 __global__ void __launch_bounds__(kThreads)
 split_rows_kernel(const float* __restrict__ src, long long lds, long long rows, long long cols,
                   float* __restrict__ hi, float* __restrict__ lo, long long ldd) {
+    pdl_trigger();  // the GEMM may launch; it waits for this grid to finish
     split_rows_body(src, lds, rows, cols, hi, lo, ldd, blockIdx.x, blockIdx.y, gridDim.x,
                     gridDim.y);
 }
@@ -122,6 +126,7 @@ split_rows_kernel(const float* __restrict__ src, long long lds, long long rows, 
 __global__ void __launch_bounds__(kThreads)
 split_rows4_kernel(const float4* __restrict__ src, long long lds4, long long rows, long long cols4,
                    float4* __restrict__ hi, float4* __restrict__ lo, long long ldd4) {
+    pdl_trigger();  // the GEMM may launch; it waits for this grid to finish
     split_rows4_body(src, lds4, rows, cols4, hi, lo, ldd4, blockIdx.x, blockIdx.y, gridDim.x,
                      gridDim.y);
 }
@@ -129,6 +134,7 @@ split_rows4_kernel(const float4* __restrict__ src, long long lds4, long long row
 __global__ void __launch_bounds__(kThreads)
 split_transpose_kernel(const float* __restrict__ src, long long lds, int K, int N,
                        float* __restrict__ hi, float* __restrict__ lo, long long ldt) {
+    pdl_trigger();  // the GEMM may launch; it waits for this grid to finish
     __shared__ float tile[32][33];
     split_transpose_body(src, lds, K, N, hi, lo, ldt, blockIdx.x, blockIdx.y, gridDim.y, tile);
 }
@@ -142,6 +148,7 @@ split_operands_kernel(const float* __restrict__ a, long long lda, long long a_ro
                       const float* __restrict__ b, long long ldb, int K, int N,
                       float* __restrict__ b_hi, float* __restrict__ b_lo, long long ldt,
                       unsigned gb_x, unsigned gb_y) {
+    pdl_trigger();  // the GEMM may launch; it waits for this grid to finish
     __shared__ float tile[32][33];
     const unsigned na = ga_x * ga_y;
     if (blockIdx.x < na) {

@@ -106,11 +106,12 @@ def test_quantised_exact():
 @pytest.mark.parametrize("shape,want", [((256, 256, 65536), 1), ((65536, 256, 1024), 1),
                                         ((2048, 2048, 2048), 0), ((8192, 8192, 8192), 0),
                                         ((1025, 1023, 1000), 0), ((512, 512, 512), 0),
-                                        ((384, 384, 20000), 0)],
+                                        ((384, 384, 20000), 0), ((300, 260, 30000), 0),
+                                        ((1024, 256, 16384), 1)],
                          ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
 def test_auto_splits_in_kernel_when_staging_dominates(shape, want):
     # AUTO takes the in-kernel split when 2 M N / (M + N) < 700 flops per
-    # operand element and the operands hold at least 16M elements (the
+    # operand element and the operands hold at least 20M elements (the
     # staging pass would cost more than the MMAs)
     M, N, K = shape
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
