@@ -127,3 +127,14 @@ def test_auto_skinny_parity():
     C = _gpu.run(A, B, g.ALGO_AUTO)
     rows, cols = _sample(M, N, 5)
     _check(C[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols), label="auto skinny")
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 0), (1, 1)])
+def test_general_form_through_the_in_kernel_split(ta, tb):
+    # alpha/beta, leading dimensions and (staged) transposes on a shape AUTO
+    # sends to the pair kernel that splits in shared memory
+    from .test_gemm_gpu import _ex_case
+    M, N, K = 1024, 256, 16384
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["split_in_kernel"] == 1, p
+    _ex_case(M, N, K, ta, tb, 4, -0.75, 1.25, g.ALGO_AUTO)
