@@ -847,7 +847,10 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
     if (col_blocks) {
         Problem qc = qp;
         qc.N = nc;
-        make_plan(*d, qc, algo, 0, &pc);
+        // the two-CTA kernel for a block (2048 x 2048: 64 pair tiles in one
+        // round), faster there than the single-CTA 128 x 256 kernel AUTO picks
+        make_plan(*d, qc, GEMM_F32_ALGO_3XTF32, 0, &pc,
+                  nc >= 1024 ? GEMM_F32_TILE_256x256_PAIR : GEMM_F32_TILE_AUTO);
         // the block GEMMs read the panel plan's staged operands; only their
         // split-K partials or tail shares need space, after the panel plan's
         col_blocks = pc.algo == GEMM_F32_ALGO_3XTF32 && !pc.split_in_kernel &&
