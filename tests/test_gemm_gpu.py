@@ -34,11 +34,20 @@ def _device():
 def _check(got, want, exact=False, label=""):
     if exact:
         assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), f"{label}: not bit-exact"
-        return
+        return None
     res = oracle.compare(got, want)
     print(f"{label}: max_abs={res['max_abs']:.3e} max_rel={res['max_rel']:.3e} "
           f"worst err/tol={res['worst_ratio']:.3f}")
     assert res["pass"], f"{label}: first bad index {res['first_bad']} ({res})"
+    return res
+
+
+# Headroom on the named workloads: the worst |err| / (1e-3 + 1e-3 |ref|) seen
+# is 0.27 (CUDA-core kernel at 8192^3), 0.12 (tensor cores at 8192^3), 0.10
+# (256 x 256 x 65536); twice the worst still passes, so a regression of the
+# arithmetic (a lost promotion chunk, a dropped correction term) shows here
+# before it fails the tolerance.
+HEADROOM = 0.5
 
 
 _REF_CACHE = {}
@@ -56,8 +65,9 @@ def _workload_with_ref(index):
 def test_workload_full_parity(index, algo):
     A, B, C_ref = _workload_with_ref(index)
     C = _gpu.run(A, B, algo)
-    _check(C, C_ref, exact=(WORKLOADS[index].dist == "quantised"),
-           label=f"{WORKLOADS[index].name}/{algo}")
+    res = _check(C, C_ref, exact=(WORKLOADS[index].dist == "quantised"),
+                 label=f"{WORKLOADS[index].name}/{algo}")
+    assert res is None or res["worst_ratio"] < HEADROOM, res
 
 
 @pytest.mark.parametrize("algo", ALGOS, ids=ALGO_IDS)
@@ -73,7 +83,8 @@ def test_square_8192_normal_sampled_parity(algo):
     cols = np.concatenate([np.arange(N), np.arange(N), np.full(M, 0), np.full(M, 4321),
                            [0, N - 1, 0, N - 1], rng.integers(0, N, 4096)])
     want = oracle.ref_gemm_entries(A, B, rows, cols)
-    _check(C[rows, cols], want, label=f"square_8192_normal/{algo}")
+    res = _check(C[rows, cols], want, label=f"square_8192_normal/{algo}")
+    assert res["worst_ratio"] < HEADROOM, res
 
 
 EDGE_SHAPES = [
