@@ -272,22 +272,23 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         const int tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
         p->pair = units_pair >= d.sm_count / 2 ? 1 : 0;
         p->bn = (p->pair || (4 * tiles256 >= 3 * d.sm_count && N > 128)) ? 256 : 128;
-        // Few flops per operand element (2 M N / (M + N) below ~700, e.g.
-        // 256 x 256 x 65536): the staging pass over A and B (12 bytes per
-        // element) costs more than the tensor work, so the pair kernel that
-        // splits A and B in shared memory, at about 55 % of the staged
-        // kernel's rate but reading each operand once as stored, is faster
-        // (256 x 256 x 65536: 0.097 against 0.143 ms; 2048^3: 0.139
-        // against 0.099 ms the other way round).
-        // Only when the operands are big enough for the staging pass to
-        // matter (at least 20M elements: 240 MB of staging traffic); smaller
-        // ones are faster staged, with their split-K added in a cluster
-        // (512^3: 19.1 against 28.3 us; 300 x 260 x 30000, 16.8M elements:
-        // 96 against 117 us; 1024 x 256 x 16384, 21M: 83 against 91 us the
-        // other way round)
+        // Few flops per operand element: the staging pass over A and B (12
+        // bytes per element) then costs more than the tensor work saved by
+        // the staged kernel, so the pair kernel that splits A and B in shared
+        // memory (about 120-145 TFLOP/s, reading each operand once as
+        // stored) is faster.  The rule, fitted to measurements: 2 M N / (M +
+        // N) below 900, the 256 x 256 pair tiles wasting at most 15 % of
+        // their work on padding, and at least 4M operand elements.  In:
+        // 256 x 256 x 65536 (0.072 against 0.143 ms staged), 512 x 512 x 8192
+        // (45.7 against 49.8 us), 2048 x 512 x 8192 (117 against 128 us).
+        // Out: 1024^2 x 4096 (66 against 70 us), 700^2 x 4096 (padding 20 %),
+        // 384^2 x 20000 (78 %), 512^3 (small: 19 against 28 us).
         const double per_element = 2.0 * M * N / (static_cast<double>(M) + N);
+        const double padded =
+            static_cast<double>(round_up(M, 256)) * static_cast<double>(round_up(N, 256));
+        const double waste = padded / (static_cast<double>(M) * N);
         const double operand_elements = (static_cast<double>(M) + N) * K;
-        if (per_element < 700.0 && operand_elements >= 20e6) {
+        if (per_element < 900.0 && waste <= 1.15 && operand_elements >= 4e6) {
             p->pair = 1;
             p->split_in_kernel = 1;
             p->bn = 256;

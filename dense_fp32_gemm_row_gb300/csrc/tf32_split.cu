@@ -2,7 +2,7 @@
 //
 // Each fp32 value x is written as two TF32 numbers (fp32 bit patterns whose
 // low 13 mantissa bits are zero):
-//     hi = tf32(x)          round to nearest, ties away from zero
+//     hi = tf32(x)          round to nearest, ties to even
 //     lo = tf32(x - hi)     x - hi is exact in fp32
 // so that x = hi + lo up to the rounding of lo (relative 2^-22 of x).  The
 // product A*B is then taken as Ahi*Bhi + Ahi*Blo + Alo*Bhi, dropping the
@@ -26,7 +26,7 @@ using gemm_f32_dev::pdl_trigger;
 
 __device__ __forceinline__ float to_tf32(float x) {
     uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    asm("cvt.rn.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
     return __uint_as_float(r);
 }
 

@@ -107,12 +107,14 @@ def test_quantised_exact():
                                         ((2048, 2048, 2048), 0), ((8192, 8192, 8192), 0),
                                         ((1025, 1023, 1000), 0), ((512, 512, 512), 0),
                                         ((384, 384, 20000), 0), ((300, 260, 30000), 0),
-                                        ((1024, 256, 16384), 1)],
+                                        ((1024, 256, 16384), 1), ((512, 512, 8192), 1),
+                                        ((2048, 512, 8192), 1), ((700, 700, 4096), 0),
+                                        ((1024, 1024, 4096), 0)],
                          ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
 def test_auto_splits_in_kernel_when_staging_dominates(shape, want):
-    # AUTO takes the in-kernel split when 2 M N / (M + N) < 700 flops per
-    # operand element and the operands hold at least 20M elements (the
-    # staging pass would cost more than the MMAs)
+    # AUTO takes the in-kernel split when 2 M N / (M + N) < 900, the pair
+    # tiles waste at most 15 % on padding and the operands hold at least 4M
+    # elements (the staging pass would cost more than the MMAs)
     M, N, K = shape
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["split_in_kernel"] == want, p
