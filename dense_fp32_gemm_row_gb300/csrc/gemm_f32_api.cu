@@ -154,6 +154,10 @@ struct Plan {
     int kb_per_split = 0;
     int stage_a = 0, stage_b = 0;
     long long lda = 0, ldb = 0;   // row strides of the operands the kernel reads (elements)
+    // 3xTF32 staged: A is its own high part (read in place, row stride
+    // lda_hi); only its low plane is written
+    int a_in_place = 0;
+    long long lda_hi = 0;
     long long ldw = 0;            // split-K partial row stride
     size_t off_a = 0, off_a2 = 0, off_b = 0, off_b2 = 0, off_w = 0, ws_bytes = 0;
     int tile_m = 0, tile_n = 0, tile_k = 0, stages = 0, ctas = 0, kernels = 0;
@@ -345,12 +349,15 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
 
     size_t off = 0;
     if (p->algo == GEMM_F32_ALGO_3XTF32 && !p->split_in_kernel) {
-        // A -> Ahi, Alo (M x K); B -> B^T hi, lo (N x K); rows padded to 16 bytes
+        // A -> Alo (M x K), and Ahi unless TMA can read A in place as its own
+        // high part; B -> B^T hi, lo (N x K); rows padded to 16 bytes
         p->stage_a = 1;
         p->stage_b = 1;
         p->lda = round_up(K, 4);
         p->ldb = round_up(K, 4);
-        p->off_a = carve(&off, static_cast<long long>(M) * p->lda * 4);
+        p->a_in_place = !q.ta && q.lda % 4 == 0 && !misaligned16(q.A);
+        p->lda_hi = p->a_in_place ? q.lda : p->lda;
+        if (!p->a_in_place) p->off_a = carve(&off, static_cast<long long>(M) * p->lda * 4);
         p->off_a2 = carve(&off, static_cast<long long>(M) * p->lda * 4);
         p->off_b = carve(&off, static_cast<long long>(N) * p->ldb * 4);
         p->off_b2 = carve(&off, static_cast<long long>(N) * p->ldb * 4);
@@ -453,12 +460,12 @@ int stage_a(const Plan& p, const Problem& q, long long r0, int M, unsigned char*
     const int K = q.K;
     const float* a = q.ta ? q.A + r0 : q.A + r0 * q.lda;
     if (p.algo == GEMM_F32_ALGO_3XTF32 && !p.split_in_kernel) {
-        float* hi = reinterpret_cast<float*>(ws + p.off_a);
+        float* hi = p.a_in_place ? nullptr : reinterpret_cast<float*>(ws + p.off_a);
         float* lo = reinterpret_cast<float*>(ws + p.off_a2);
         e = q.ta ? launch_split_transpose(a, q.lda, K, M, hi, lo, p.lda, stream)  // K x M -> M x K
                  : launch_split_rows(a, q.lda, M, K, hi, lo, p.lda, stream);
         if (e != cudaSuccess) return static_cast<int>(e);
-        o->a_hi = hi;
+        o->a_hi = p.a_in_place ? a : hi;
         o->a_lo = lo;
     } else if (p.stage_a) {
         float* dst = reinterpret_cast<float*>(ws + p.off_a);
@@ -503,7 +510,7 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
             ta.tmAlo = ta.tmAhi;
             ta.tmBlo = ta.tmBhi;
             ta.split_in_kernel = 1;
-        } else if ((st = encode_2d(&ta.tmAhi, o.a_hi, K, M, p.lda, p.tile_k, 128,
+        } else if ((st = encode_2d(&ta.tmAhi, o.a_hi, K, M, p.lda_hi, p.tile_k, 128,
                             CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
             (st = encode_2d(&ta.tmAlo, o.a_lo, K, M, p.lda, p.tile_k, 128,
                             CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
@@ -605,14 +612,14 @@ int enqueue(const Problem& q, int algo, int splits, DeviceState* d, int dev, cud
     }
     Operands o;
     if (p.fused_staging) {
-        float* a_hi = reinterpret_cast<float*>(ws + p.off_a);
+        float* a_hi = p.a_in_place ? nullptr : reinterpret_cast<float*>(ws + p.off_a);
         float* a_lo = reinterpret_cast<float*>(ws + p.off_a2);
         float* b_hi = reinterpret_cast<float*>(ws + p.off_b);
         float* b_lo = reinterpret_cast<float*>(ws + p.off_b2);
         const cudaError_t e = launch_split_operands(q.A, q.lda, q.M, q.K, a_hi, a_lo, p.lda, q.B,
                                                     q.ldb, q.N, b_hi, b_lo, p.ldb, stream);
         if (e != cudaSuccess) return static_cast<int>(e);
-        o.a_hi = a_hi;
+        o.a_hi = p.a_in_place ? q.A : a_hi;
         o.a_lo = a_lo;
         o.b_hi = b_hi;
         o.b_lo = b_lo;
@@ -855,7 +862,8 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
         // the block GEMMs read the panel plan's staged operands; only their
         // split-K partials or tail shares need space, after the panel plan's
         col_blocks = pc.algo == GEMM_F32_ALGO_3XTF32 && !pc.split_in_kernel &&
-                     pc.lda == p.lda && pc.ldb == p.ldb && pc.tile_k == p.tile_k;
+                     pc.lda == p.lda && pc.lda_hi == p.lda_hi && pc.ldb == p.ldb &&
+                     pc.tile_k == p.tile_k;
         pc.off_w += p.ws_bytes;
         pc.off_t += p.ws_bytes;
     }

@@ -64,7 +64,9 @@ Tf32x3Config tf32x3_config(int bn, bool pair);
 
 struct Tf32x3Args {
     // pre-split operands: A hi / lo as {K, M}, box {bk, bm}, and B^T hi / lo
-    // as {K, N}, box {bk, box_n}, all with 128-byte swizzle.  split_in_kernel
+    // as {K, N}, box {bk, box_n}, all with 128-byte swizzle (A hi may be A
+    // itself, with its own row stride: the high part is the fp32 word, which
+    // the tensor core truncates to TF32).  split_in_kernel
     // (pair kernel only): tmAhi is A as stored, {K, M}, box {bk, 128}, and
     // tmBhi is B as stored, {N, K}, box {32, bk}; tmAlo and tmBlo are unused.
     CUtensorMap tmAhi, tmAlo;
@@ -100,14 +102,17 @@ cudaError_t tf32x3_pair_clusters(int sm_count, int* clusters);
 cudaError_t launch_sgemm_3xtf32(const Tf32x3Args& a, cudaStream_t s, int sm_count);
 
 // ---- TF32 hi/lo staging (tf32_split.cu) --------------------------------------
-// hi/lo[r*ldd + c] from src[r*lds + c] (same orientation)
+// hi = x as stored (read by the tensor core as trunc(x)), lo = tf32(x - trunc(x)).
+// hi/lo[r*ldd + c] from src[r*lds + c] (same orientation); hi may be null
+// (lo only)
 cudaError_t launch_split_rows(const float* src, long long lds, long long rows, long long cols,
                               float* hi, float* lo, long long ldd, cudaStream_t s);
 // hi/lo[n*ldt + k] from src[k*lds + n] (K x N -> N x K)
 cudaError_t launch_split_transpose(const float* src, long long lds, int K, int N, float* hi,
                                    float* lo, long long ldt, cudaStream_t s);
 // both of the above in one launch: A (M x K, row stride lda) -> a_hi/a_lo
-// (row stride ldd) and B (K x N, row stride ldb) -> b_hi/b_lo (N x K, ldt)
+// (row stride ldd; a_hi may be null) and B (K x N, row stride ldb) ->
+// b_hi/b_lo (N x K, ldt)
 cudaError_t launch_split_operands(const float* a, long long lda, int M, int K, float* a_hi,
                                   float* a_lo, long long ldd, const float* b, long long ldb, int N,
                                   float* b_hi, float* b_lo, long long ldt, cudaStream_t s);

@@ -1,7 +1,8 @@
 // sgemm_3xtf32.cu -- single-precision GEMM on the sm_103a tensor cores.
 //
 // C = A * B with FP32-level accuracy from TF32 tensor-core products: the
-// operands arrive pre-split into TF32 high and low parts (tf32_split.cu), and
+// operands arrive pre-split into high and low parts (tf32_split.cu; the high
+// part is the fp32 word itself, which the tensor core reads truncated), and
 // every K step issues three tcgen05.mma kind::tf32 products into one fp32
 // accumulator in tensor memory:  Alo*Bhi + Ahi*Blo + Ahi*Bhi  (small terms
 // first, Alo*Blo dropped).  See "Lecture 12: final project" (section 2,
@@ -35,6 +36,21 @@
 // the grid size.  Every mbarrier wait is bounded; a timeout sets the device
 // fault word and a shared abort flag, and the CTA winds down (waits, bounded,
 // for its in-flight copies and MMAs, then frees its tensor memory).
+//
+// Split K without a workspace (cluster_splits = S, 2..8): the grid is one
+// unit per CTA and the S K splits of a tile are the S CTAs of one cluster.
+// Each parks its partial tile in its own (drained) stage memory; after a
+// cluster barrier every CTA sums a 1/S band of rows over the S partials
+// through distributed shared memory, in split order, and stores it.
+//
+// Both kernels of this file are launched as programmatic dependents: their
+// set-up (barriers, tensor memory, descriptor prefetch) overlaps the tail of
+// the kernel before them on the stream, and they wait for it (griddepcontrol)
+// before the first operand load.
+//
+// The CTA-pair kernel further down (cta_group::2, 256 x 256 tiles) shares the
+// chunked promotion, the bounded waits and the tail handling; its header
+// describes its roles and its in-shared-memory split of raw operands.
 #include <cstdint>
 
 #include "device_sync.cuh"
@@ -174,7 +190,7 @@ __device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, long lo
     return role_wait_slow<CLUSTER>(bar, parity, timeout_ns, fault, bit, abort_flag);
 }
 
-// Round to TF32 (nearest, ties to even): the split of tf32_split.cu.  The
+// Round to TF32 (nearest, ties to even), for the low part of the split.  The
 // ties-to-even form is a single native conversion; the ties-away form
 // (cvt.rna) made the in-kernel split a fifth slower (4096^3: 0.996 against
 // 0.799 ms) and gives no better split.
@@ -525,9 +541,10 @@ cudaError_t launch_impl(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
 //          slots, signalling its own full barrier: a 128 x 32 box of A
 //          (K-major already) and four 32 x 32 boxes of B (N-contiguous).
 //          Warps 2-3 of each CTA then split the stage in shared memory:
-//          A elementwise in place (hi = tf32(x) where x was, lo = tf32(x -
-//          hi) in the lo slot); B by 4 x 4 blocks read into registers,
-//          transposed and written back K-major as hi and lo.  These are the
+//          A elementwise (x stays in the hi slot as its own high part, lo =
+//          tf32(x - trunc(x)) goes to the lo slot); B by 4 x 4 blocks read
+//          into registers, transposed and written back K-major as hi (the
+//          words themselves) and lo.  These are the
 //          values and the layout the staging kernels would have produced,
 //          so the MMAs are the same.  The splitters fence their writes for
 //          the tensor core and arrive on the leader's converted barrier.
@@ -568,11 +585,19 @@ __device__ __forceinline__ float4 sub4(float4 a, float4 b) {
     return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w);
 }
 
-// The TF32 split of four values: hi = tf32(x), lo = tf32(x - hi).
-__device__ __forceinline__ void split4(float4 x, float4& hi, float4& lo) {
-    hi = tf32x4(x);
-    lo = tf32x4(sub4(x, hi));
+// x with the low 13 mantissa bits of each lane cleared: the TF32 value the
+// tensor core reads from the fp32 word x (it truncates; measured on this
+// part for ties and near-ties of both parities and signs).
+__device__ __forceinline__ float4 trunc4(float4 x) {
+    return make_float4(__uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u),
+                       __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u),
+                       __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u),
+                       __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u));
 }
+
+// The low part of the TF32 split of four values, lo = tf32(x - trunc(x));
+// the high part is the word x itself (the split of tf32_split.cu).
+__device__ __forceinline__ float4 lo4(float4 x) { return tf32x4(sub4(x, trunc4(x))); }
 
 __device__ __forceinline__ float lane_of(float4 v, int e) {
     return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
@@ -585,9 +610,10 @@ __device__ __forceinline__ float4 rotate4(float4 v, int r) {
 }
 
 // A slot (16 KB at sa, K-major, 128-byte swizzled as the TMA wrote it): each
-// value x becomes hi = tf32(x) where it is and lo = tf32(x - hi) 16 KB
-// further on.  The map is elementwise, so the layout carries over.  Thread t
-// of the 64 takes 16-byte words t, t + 64, ... (conflict-free).
+// value x stays where it is as its own high part, and lo = tf32(x -
+// trunc(x)) goes 16 KB further on.  The map is elementwise, so the layout
+// carries over.  Thread t of the 64 takes 16-byte words t, t + 64, ...
+// (conflict-free).
 __device__ __forceinline__ void split_a_stage(uint32_t sa, int t) {
 #pragma unroll 1
     for (int i0 = 0; i0 < 16; i0 += 8) {
@@ -595,13 +621,8 @@ __device__ __forceinline__ void split_a_stage(uint32_t sa, int t) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[j] = lds128(sa + 16 * t + 1024 * (i0 + j));
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float4 h, l;
-            split4(v[j], h, l);
-            const uint32_t a = sa + 16 * t + 1024 * (i0 + j);
-            sts128(a, h);
-            sts128(a + 16384, l);
-        }
+        for (int j = 0; j < 8; ++j)
+            sts128(sa + 16 * t + 1024 * (i0 + j) + 16384, lo4(v[j]));
     }
 }
 
@@ -645,11 +666,9 @@ __device__ __forceinline__ void split_b_stage(uint32_t sb, int w, int lane) {
                 // lane e of the rotated words is column n; k = 4 kq + 0..3
                 const float4 x = make_float4(lane_of(v[jj][h][0], e), lane_of(v[jj][h][1], e),
                                              lane_of(v[jj][h][2], e), lane_of(v[jj][h][3], e));
-                float4 hi, lo;
-                split4(x, hi, lo);
                 const uint32_t a = sb + n * 128 + ((kq ^ (n & 7)) << 4);
-                sts128(a, hi);
-                sts128(a + 16384, lo);
+                sts128(a, x);
+                sts128(a + 16384, lo4(x));
             }
         }
 }

@@ -64,14 +64,16 @@ extern "C" {
 
 /* ---- algorithms -------------------------------------------------------- */
 /* Choose by shape: the tensor-core 3xTF32 kernels, except the CUDA-core
- * kernel for tiny problems (under about 2.7e8 multiply-adds). */
+ * kernel for tiny problems (under 5e7 multiply-adds). */
 #define GEMM_F32_ALGO_AUTO    0
 /* CUDA-core FFMA kernel: TMA-fed, swizzled shared-memory tiles, mbarrier
- * pipeline, 8x8 register tile per thread. */
+ * pipeline, 8x8 or 8x16 register tile per thread. */
 #define GEMM_F32_ALGO_FFMA    1
-/* Tensor-core kernel: each operand split into a TF32 high part and a TF32
- * low part, three tcgen05 products hi*hi + hi*lo + lo*hi accumulated in
- * tensor memory in fp32. */
+/* Tensor-core kernel: each operand x split into a TF32 high part trunc(x)
+ * (the fp32 word itself, which the tensor core reads truncated) and a TF32
+ * low part tf32(x - trunc(x)); three tcgen05 products hi*hi + hi*lo + lo*hi
+ * accumulated in tensor memory in fp32, promoted every 128 K into fp32
+ * registers. */
 #define GEMM_F32_ALGO_3XTF32  2
 
 /* Largest explicit split-K factor accepted by gemm_f32_algo_splitk. */

@@ -4,7 +4,8 @@ reading copies written by staging kernels.
 
 Against the oracle, elementwise within 1e-3 + 1e-3 |C_ref| (NaN guard bands
 around C); against the pre-split pair kernel, bit for bit when neither splits
-K: both form the same hi = tf32(x), lo = tf32(x - hi) values and issue the
+K: both give the tensor core the same high parts (the fp32 words, which it
+reads truncated to TF32) and low parts lo = tf32(x - trunc(x)), and issue the
 same MMAs in the same order, promoted in the same 128-deep chunks.
 """
 
