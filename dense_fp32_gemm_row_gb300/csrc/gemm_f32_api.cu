@@ -268,31 +268,34 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
                                          : GEMM_F32_ALGO_3XTF32;
     int bm, bn, bk, slots;
     if (p->algo == GEMM_F32_ALGO_3XTF32) {
-        // the two-CTA 256 x 256 kernel when its tiles fill every SM pair;
-        // otherwise one CTA per 128 x 256 tile when those fill at least three
-        // quarters of the SMs (2048^3: 100 vs 105 us for 128 x 128), else
+        // the two-CTA 256 x 256 kernel when its tiles fill at least four
+        // fifths of the SM pairs (it keeps the tensor pipe busier than one
+        // CTA per tile: 2048^2 x 8192, 64 pair tiles on 76 pairs, 309 against
+        // 330 us for 128 x 256; 2048^3 even); otherwise one CTA per 128 x 256
+        // tile when those fill at least three quarters of the SMs, else
         // 128 x 128 tiles with split-K
         const int units_pair = ((M + 255) / 256) * ((N + 255) / 256);
         const int tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
-        p->pair = units_pair >= d.sm_count / 2 ? 1 : 0;
+        p->pair = 5 * units_pair >= 4 * (d.sm_count / 2) ? 1 : 0;
         p->bn = (p->pair || (4 * tiles256 >= 3 * d.sm_count && N > 128)) ? 256 : 128;
-        // Few flops per operand element: the staging pass over A and B (12
+        // Few flops per operand element: the staging pass over A and B (8-12
         // bytes per element) then costs more than the tensor work saved by
         // the staged kernel, so the pair kernel that splits A and B in shared
-        // memory (about 120-145 TFLOP/s, reading each operand once as
+        // memory (about 120-150 TFLOP/s, reading each operand once as
         // stored) is faster.  The rule, fitted to measurements: 2 M N / (M +
-        // N) below 900, the 256 x 256 pair tiles wasting at most 15 % of
+        // N) below 700, the 256 x 256 pair tiles wasting at most 15 % of
         // their work on padding, and at least 4M operand elements.  In:
-        // 256 x 256 x 65536 (0.072 against 0.143 ms staged), 512 x 512 x 8192
-        // (45.7 against 49.8 us), 2048 x 512 x 8192 (117 against 128 us).
-        // Out: 1024^2 x 4096 (66 against 70 us), 700^2 x 4096 (padding 20 %),
-        // 384^2 x 20000 (78 %), 512^3 (small: 19 against 28 us).
+        // 256 x 256 x 65536 (71 against 116 us staged), 512^2 x 4096 (33.4
+        // against 36.5 us), 8192 x 256 x 8192 (208 against 238 us).  Out:
+        // 768^2 x 4096 (128 x 128 tiles staged 39.6 against 49.2 us),
+        // 1024^2 x 4096 (60 against 69 us), 700^2 x 4096 (padding 20 %),
+        // 384^2 x 32768 (78 %), 512^3 (small).
         const double per_element = 2.0 * M * N / (static_cast<double>(M) + N);
         const double padded =
             static_cast<double>(round_up(M, 256)) * static_cast<double>(round_up(N, 256));
         const double waste = padded / (static_cast<double>(M) * N);
         const double operand_elements = (static_cast<double>(M) + N) * K;
-        if (per_element < 900.0 && waste <= 1.15 && operand_elements >= 4e6) {
+        if (per_element < 700.0 && waste <= 1.15 && operand_elements >= 4e6) {
             p->pair = 1;
             p->split_in_kernel = 1;
             p->bn = 256;

@@ -2,6 +2,7 @@
 
     python -m dense_fp32_gemm_row_gb300.tune [--shapes 2048x2048x2048,...]
                                              [--repeats 10] [--csv out.csv]
+                                             [--quick]
 
 The library-side counterpart of the sweep program of "Lecture 12: final
 project" (block size x tile depth x coarsening, each combination checked for
@@ -17,6 +18,8 @@ between calls when the inputs fit in it).  The library's own choice
 from the best configuration per shape.
 
 Prints one CSV row per configuration and a summary line per shape.
+``--quick`` narrows the space to the tensor-core tiles with the library's
+own split-K choice (splits = 0), the check of AUTO's tile rules.
 """
 
 from __future__ import annotations
@@ -31,7 +34,12 @@ DEFAULT_SHAPES = ("512x512x512,1025x1023x1000,2048x2048x2048,4096x4096x4096,"
 SPLITS = (1, 2, 4, 8, 16, 32, 64)
 
 
-def _configs(g):
+def _configs(g, quick: bool = False):
+    if quick:
+        for tile in (g.TILE_128x128, g.TILE_128x256, g.TILE_256x256_PAIR,
+                     g.TILE_256x256_PAIR_SPLIT):
+            yield g.ALGO_3XTF32, tile, 0
+        return
     for algo, tiles in ((g.ALGO_FFMA, (g.TILE_128x128, g.TILE_128x256)),
                         (g.ALGO_3XTF32, (g.TILE_128x128, g.TILE_128x256, g.TILE_256x256_PAIR,
                                          g.TILE_256x256_PAIR_SPLIT))):
@@ -40,7 +48,7 @@ def _configs(g):
                 yield algo, tile, splits
 
 
-def sweep(shapes, repeats: int, out=sys.stdout) -> list[dict]:
+def sweep(shapes, repeats: int, out=sys.stdout, quick: bool = False) -> list[dict]:
     import torch
 
     import dense_fp32_gemm_row_gb300 as g
@@ -85,7 +93,7 @@ def sweep(shapes, repeats: int, out=sys.stdout) -> list[dict]:
             return statistics.median(ts)
 
         results = []
-        candidates = [(g.ALGO_AUTO, 0, 0)] + list(_configs(g))
+        candidates = [(g.ALGO_AUTO, 0, 0)] + list(_configs(g, quick))
         for algo, tile, splits in candidates:
             st, plan = (g.gemm_f32_plan(M, N, K, algo, splits, a.data_ptr(), b.data_ptr(),
                                         c.data_ptr()) if algo == g.ALGO_AUTO else
@@ -140,15 +148,17 @@ def main(argv=None) -> int:
     ap.add_argument("--shapes", default=DEFAULT_SHAPES)
     ap.add_argument("--repeats", type=int, default=10)
     ap.add_argument("--csv", default=None, help="also write the table to this file")
+    ap.add_argument("--quick", action="store_true",
+                    help="3xTF32 tiles with the library's split-K choice only")
     args = ap.parse_args(argv)
     shapes = [tuple(int(v) for v in s.split("x")) for s in args.shapes.split(",") if s]
     if args.csv:
         with open(args.csv, "w") as f:
-            sweep(shapes, args.repeats, out=f)
+            sweep(shapes, args.repeats, out=f, quick=args.quick)
         with open(args.csv) as f:
             sys.stdout.write(f.read())
     else:
-        sweep(shapes, args.repeats)
+        sweep(shapes, args.repeats, quick=args.quick)
     return 0
 
 

@@ -127,3 +127,16 @@ def test_general_entry_validates_layout(lib):
     assert ex(0, 0, 4, 4, 4, 1.0, A, 1000, B, 4, 0.0, A + 4 * 2000, 4) == g.ERR_INVALID_VALUE
     # empty output: success without a device
     assert ex(0, 0, 0, 5, 6, 1.0, 0, 6, 0, 5, 0.0, 0, 5) == g.SUCCESS
+
+
+def test_tune_configuration_space():
+    # the sweep tool's grid: every (algo, tile, splits) once; --quick keeps
+    # the tensor-core tiles with the library's own split choice
+    from dense_fp32_gemm_row_gb300 import tune
+    full = list(tune._configs(g))
+    assert len(full) == len(set(full)) == (2 + 4) * len(tune.SPLITS)
+    assert {a for a, _, _ in full} == {g.ALGO_FFMA, g.ALGO_3XTF32}
+    quick = list(tune._configs(g, quick=True))
+    assert quick == [(g.ALGO_3XTF32, t, 0) for t in (g.TILE_128x128, g.TILE_128x256,
+                                                       g.TILE_256x256_PAIR,
+                                                       g.TILE_256x256_PAIR_SPLIT)]

@@ -102,9 +102,23 @@ def test_edge_shapes(shape, algo):
     _check(_gpu.run(A, B, algo), oracle.ref_gemm(A, B), label=f"{shape}/{algo}")
 
 
-# shapes whose 256 x 256 tiles fill every SM pair: these run the two-CTA
-# tensor-core kernel (ragged in M, N and K, and one with split-K)
+# shapes whose 256 x 256 tiles fill at least four fifths of the SM pairs:
+# these run the two-CTA tensor-core kernel (ragged in M, N and K, and one with
+# split-K)
 PAIR_SHAPES = [(2304, 2304, 512), (2305, 2049, 1000), (2560, 2330, 77), (4096, 2048, 3000)]
+
+
+@pytest.mark.parametrize("shape", [(2048, 2048, 2048), (2048, 2048, 8192), (1792, 1792, 4096),
+                                   (1536, 1536, 4096), (2304, 2304, 512)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_pair_kernel_rule(shape):
+    # the staged tensor-core path takes the two-CTA kernel once its 256 x 256
+    # tiles fill at least four fifths of the SM pairs
+    M, N, K = shape
+    pairs = _gpu.torch().cuda.get_device_properties(0).multi_processor_count // 2
+    units = ((M + 255) // 256) * ((N + 255) // 256)
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_3XTF32, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and (p["tile_m"] == 256) == (5 * units >= 4 * pairs), (units, pairs, p)
 
 
 @pytest.mark.parametrize("shape", PAIR_SHAPES, ids=lambda s: "x".join(map(str, s)))

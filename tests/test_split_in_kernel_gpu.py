@@ -109,11 +109,12 @@ def test_quantised_exact():
                                         ((1025, 1023, 1000), 0), ((512, 512, 512), 0),
                                         ((384, 384, 20000), 0), ((300, 260, 30000), 0),
                                         ((1024, 256, 16384), 1), ((512, 512, 8192), 1),
-                                        ((2048, 512, 8192), 1), ((700, 700, 4096), 0),
+                                        ((2048, 512, 8192), 0), ((700, 700, 4096), 0),
+                                        ((768, 768, 4096), 0), ((512, 512, 4096), 1),
                                         ((1024, 1024, 4096), 0)],
                          ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
 def test_auto_splits_in_kernel_when_staging_dominates(shape, want):
-    # AUTO takes the in-kernel split when 2 M N / (M + N) < 900, the pair
+    # AUTO takes the in-kernel split when 2 M N / (M + N) < 700, the pair
     # tiles waste at most 15 % on padding and the operands hold at least 4M
     # elements (the staging pass would cost more than the MMAs)
     M, N, K = shape
