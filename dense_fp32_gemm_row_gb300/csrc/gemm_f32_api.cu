@@ -281,21 +281,29 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         // Few flops per operand element: the staging pass over A and B (8-12
         // bytes per element) then costs more than the tensor work saved by
         // the staged kernel, so the pair kernel that splits A and B in shared
-        // memory (about 120-150 TFLOP/s, reading each operand once as
-        // stored) is faster.  The rule, fitted to measurements: 2 M N / (M +
-        // N) below 700, the 256 x 256 pair tiles wasting at most 15 % of
-        // their work on padding, and at least 4M operand elements.  In:
-        // 256 x 256 x 65536 (71 against 116 us staged), 512^2 x 4096 (33.4
-        // against 36.5 us), 8192 x 256 x 8192 (208 against 238 us).  Out:
-        // 768^2 x 4096 (128 x 128 tiles staged 39.6 against 49.2 us),
-        // 1024^2 x 4096 (60 against 69 us), 700^2 x 4096 (padding 20 %),
-        // 384^2 x 32768 (78 %), 512^3 (small).
+        // memory (about 130-210 TFLOP/s, reading each operand once as
+        // stored) is faster.  The rule, fitted to measurements (at least 4M
+        // operand elements in both cases):
+        //  * 2 M N / (M + N) below 700 with the 256 x 256 pair tiles wasting
+        //    at most 15 % on padding: 256 x 256 x 65536 (65 against 116 us
+        //    staged), 512^2 x 4096 (32.8 against 35.5 us); 768^2 x 4096
+        //    stays staged (39.6 against 45.7 us: the pair kernel's split-K
+        //    goes through a workspace, the staged 128 x 128 tiles' through a
+        //    cluster);
+        //  * K >= 8192 (the split kernel's reduction is then a small part of
+        //    the call) with 2 M N / (M + N) below 1800 and at most 50 %
+        //    padding: 1024^2 x 8192 (101 against 109 us), 1280^2 x 8192 (132
+        //    against 145), 1536^2 x 8192 (182 against 191), 640^2 x 8192
+        //    (62 against 64, 44 % padding); 2048^2 x 8192 stays staged (309
+        //    against 326 us), as do 8192^3, 700^2 x 4096 and 512^3.
         const double per_element = 2.0 * M * N / (static_cast<double>(M) + N);
         const double padded =
             static_cast<double>(round_up(M, 256)) * static_cast<double>(round_up(N, 256));
         const double waste = padded / (static_cast<double>(M) * N);
         const double operand_elements = (static_cast<double>(M) + N) * K;
-        if (per_element < 700.0 && waste <= 1.15 && operand_elements >= 4e6) {
+        const bool few_flops = per_element < 700.0 && waste <= 1.15;
+        const bool deep_k = K >= 8192 && per_element < 1800.0 && waste <= 1.5;
+        if (operand_elements >= 4e6 && (few_flops || deep_k)) {
             p->pair = 1;
             p->split_in_kernel = 1;
             p->bn = 256;

@@ -540,7 +540,8 @@ cudaError_t launch_impl(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
 //   true   each CTA's producer loads the operands as stored into the hi
 //          slots, signalling its own full barrier: a 128 x 32 box of A
 //          (K-major already) and four 32 x 32 boxes of B (N-contiguous).
-//          Warps 2-3 of each CTA then split the stage in shared memory:
+//          Warp 2 or 3 of each CTA (taking turns by stage fill) then
+//          splits the stage in shared memory:
 //          A elementwise (x stays in the hi slot as its own high part, lo =
 //          tf32(x - trunc(x)) goes to the lo slot); B by 4 x 4 blocks read
 //          into registers, transposed and written back K-major as hi (the
@@ -567,7 +568,8 @@ struct PairCfg {
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int EPI_WARPS = BN / EPI_COLS * 4;
     static constexpr int THREADS = 128 + 32 * EPI_WARPS;
-    static constexpr int CONV_THREADS = 64;  // warps 2-3
+    // splitter warps 2-3: each splits whole stages, the two taking turns
+    static constexpr int CONV_THREADS = 64;
     // full, empty, converted (per stage), acc_full x2, acc_empty x2, drain
     static constexpr int NBARS = 3 * STAGES + 5;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NBARS * 8 + 16 + 1024;
@@ -612,8 +614,8 @@ __device__ __forceinline__ float4 rotate4(float4 v, int r) {
 // A slot (16 KB at sa, K-major, 128-byte swizzled as the TMA wrote it): each
 // value x stays where it is as its own high part, and lo = tf32(x -
 // trunc(x)) goes 16 KB further on.  The map is elementwise, so the layout
-// carries over.  Thread t of the 64 takes 16-byte words t, t + 64, ...
-// (conflict-free).
+// carries over.  Call t takes 16-byte words t, t + 64, ... (t = 0..63: two
+// calls by the 32 lanes of one warp, t = lane and lane + 32; conflict-free).
 __device__ __forceinline__ void split_a_stage(uint32_t sa, int t) {
 #pragma unroll 1
     for (int i0 = 0; i0 < 16; i0 += 8) {
@@ -631,8 +633,9 @@ __device__ __forceinline__ void split_a_stage(uint32_t sa, int t) {
 // of row k sits at chunk c ^ (k & 7)).  On exit the K-major hi plane in its
 // place (row n = 128 bytes of k = 0..31, chunk q at q ^ (n & 7): the layout
 // TMA gives a box of the transposed copy) and the lo plane 16 KB further on.
-// Splitter warp w owns boxes 2w and 2w + 1, i.e. bytes [8192 w, 8192 w +
-// 8192) of both layouts, so the in-place transpose needs no other warp.
+// Call w (0, 1) does boxes 2w and 2w + 1, i.e. bytes [8192 w, 8192 w +
+// 8192) of both layouts, so the in-place transpose of one call needs only
+// its own warp; one warp makes both calls for a stage.
 // Lane l takes the 4 x 4 blocks (n = 32 j + 4 c .. + 3, k = 4 kq .. + 3)
 // with c = l % 8, kq = l / 8 and l / 8 + 4, j = 2w, 2w + 1: it loads all of
 // them (eight lanes read one 128-byte row: conflict-free), the warp syncs,
@@ -693,7 +696,7 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
     //          split in kernel: each CTA's own, count 1
     const uint32_t full0 = bar0;
     const uint32_t empty0 = bar0 + 8 * STAGES;    // empty[s]: both CTAs, one multicast commit
-    const uint32_t conv0 = bar0 + 16 * STAGES;    // converted[s]: leader, 2 warps x 2 CTAs
+    const uint32_t conv0 = bar0 + 16 * STAGES;    // converted[s]: leader, 1 warp x 2 CTAs
     const uint32_t accf0 = bar0 + 24 * STAGES;    // acc_full[b]: both CTAs, one multicast commit
     const uint32_t acce0 = accf0 + 16;            // acc_empty[b]: leader, both epilogues
     const uint32_t drain = acce0 + 16;
@@ -722,7 +725,7 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8 * s, SPLIT_IN_KERNEL ? 1 : 2);
             mbar_init(empty0 + 8 * s, 1);
-            mbar_init(conv0 + 8 * s, 2 * (C::CONV_THREADS / 32));
+            mbar_init(conv0 + 8 * s, 2);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf0 + 8 * b, 1);
@@ -855,7 +858,12 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
     } else if (warp < 4) {
         if (SPLIT_IN_KERNEL) {
             // ------------------------------ splitter (warps 2-3, both CTAs) -----------
-            const int t = threadIdx.x - 64;
+            // Warp 2 splits the even-numbered stage fills, warp 3 the odd
+            // ones, each a whole stage: one warp's wait for its stores to
+            // drain (the fence before the arrive) overlaps the other's
+            // conversions.  Splitting every stage by both warps, half each,
+            // was slower by 7-13 % (8192^3 on this kernel: 4.94 against 4.28
+            // ms; 256 x 256 x 65536: 71.3 against 66.2 us).
             const uint32_t conv_leader = map_to_cta(conv0, 0);
             int it = 0;
             bool ok = true;
@@ -863,6 +871,7 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                 const Unit w = decode_pair(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN,
                                            tail_tiles, tail_splits);
                 for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+                    if ((it & 1) != warp - 2) continue;  // the other splitter's turn
                     const int s = it % STAGES;
                     const bool got = role_wait(full0 + 8 * s, (it / STAGES) & 1, timeout_ns, fault,
                                                kFaultFullBarrier, abort_flag);
@@ -871,8 +880,10 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                         break;
                     }
                     const uint32_t st = sbase + s * C::STAGE_BYTES;
-                    split_a_stage(st, t);
-                    split_b_stage(st + 2 * C::A_BYTES, warp - 2, lane);
+                    split_a_stage(st, lane);
+                    split_a_stage(st, lane + 32);
+                    split_b_stage(st + 2 * C::A_BYTES, 0, lane);
+                    split_b_stage(st + 2 * C::A_BYTES, 1, lane);
                     // the tensor core reads these words through the async proxy
                     fence_proxy_async_smem();
                     __syncwarp();

@@ -109,14 +109,18 @@ def test_quantised_exact():
                                         ((1025, 1023, 1000), 0), ((512, 512, 512), 0),
                                         ((384, 384, 20000), 0), ((300, 260, 30000), 0),
                                         ((1024, 256, 16384), 1), ((512, 512, 8192), 1),
-                                        ((2048, 512, 8192), 0), ((700, 700, 4096), 0),
+                                        ((2048, 512, 8192), 1), ((700, 700, 4096), 0),
                                         ((768, 768, 4096), 0), ((512, 512, 4096), 1),
+                                        ((1024, 1024, 8192), 1), ((640, 640, 8192), 1),
+                                        ((1536, 1536, 8192), 1), ((2048, 2048, 8192), 0),
+                                        ((1536, 1536, 4096), 0), ((384, 384, 32768), 0),
                                         ((1024, 1024, 4096), 0)],
                          ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
 def test_auto_splits_in_kernel_when_staging_dominates(shape, want):
-    # AUTO takes the in-kernel split when 2 M N / (M + N) < 700, the pair
-    # tiles waste at most 15 % on padding and the operands hold at least 4M
-    # elements (the staging pass would cost more than the MMAs)
+    # AUTO takes the in-kernel split when the operands hold at least 4M
+    # elements and either 2 M N / (M + N) < 700 with the pair tiles wasting
+    # at most 15 % on padding, or K >= 8192 with 2 M N / (M + N) < 1800 and
+    # at most 50 % padding (the staging pass would cost more than it saves)
     M, N, K = shape
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["split_in_kernel"] == want, p
@@ -125,8 +129,11 @@ def test_auto_splits_in_kernel_when_staging_dominates(shape, want):
 
 
 def test_auto_skinny_parity():
-    # the in-kernel split chosen by AUTO on a tall, narrow product (ragged N)
-    M, N, K = 9000, 200, 3000
+    # the in-kernel split chosen by AUTO on a tall, narrow, deep product
+    # (ragged M and N: 31 % of the pair tiles' area is padding)
+    M, N, K = 9000, 200, 8192
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["split_in_kernel"] == 1, p
     A, B = make_workload(1, M=M, N=N, K=K)
     C = _gpu.run(A, B, g.ALGO_AUTO)
     rows, cols = _sample(M, N, 5)
