@@ -569,12 +569,21 @@ struct PairCfg {
     static constexpr int EPI_WARPS = BN / EPI_COLS * 4;
     static constexpr int THREADS = 128 + 32 * EPI_WARPS;
     // splitter warps 2-3: each splits whole stages, the two taking turns
-    static constexpr int CONV_THREADS = 64;
-    // full, empty, converted (per stage), acc_full x2, acc_empty x2, drain
-    static constexpr int NBARS = 3 * STAGES + 5;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NBARS * 8 + 16 + 1024;
+    static constexpr int NSPLIT = 2;
+    // Full barriers.  Pre-split operands: one per stage.  Split in kernel:
+    // one per (stage fill mod STAGES * NSPLIT), so that every full barrier
+    // is waited on by one splitter warp, phase after phase.  (With one
+    // barrier per stage, a warp that takes every other fill of a stage would
+    // skip a phase, and a parity wait cannot tell phase k from phase k + 2.)
+    static constexpr int NFULL = SPLIT_IN_KERNEL ? STAGES * NSPLIT : STAGES;
+    // full (NFULL), empty, converted (per stage), acc_full x2, acc_empty x2, drain
+    static constexpr int NBARS = NFULL + 2 * STAGES + 5;
+    // both variants reserve room for the split variant's barriers, so that
+    // they have the same shared-memory size (and occupancy)
+    static constexpr int SMEM_BYTES =
+        STAGES * STAGE_BYTES + (STAGES * NSPLIT + 2 * STAGES + 5) * 8 + 16 + 1024;
     static constexpr uint32_t IDESC = idesc_tf32_f32(2 * BM, BN);
-    static_assert(A_BYTES == B_BYTES && B_BYTES == 16384 && CONV_THREADS == 64,
+    static_assert(A_BYTES == B_BYTES && B_BYTES == 16384,
                   "the splitter's thread-to-element maps below");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
@@ -692,12 +701,13 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_addr(smem);
     const uint32_t bar0 = sbase + STAGES * C::STAGE_BYTES;
-    // full[s]: pre-split operands: the leader's, count 2 (both producers);
-    //          split in kernel: each CTA's own, count 1
+    // full[f]: pre-split operands: f = stage, the leader's, count 2 (both
+    //          producers); split in kernel: f = fill mod NFULL, each CTA's
+    //          own, count 1
     const uint32_t full0 = bar0;
-    const uint32_t empty0 = bar0 + 8 * STAGES;    // empty[s]: both CTAs, one multicast commit
-    const uint32_t conv0 = bar0 + 16 * STAGES;    // converted[s]: leader, 1 warp x 2 CTAs
-    const uint32_t accf0 = bar0 + 24 * STAGES;    // acc_full[b]: both CTAs, one multicast commit
+    const uint32_t empty0 = full0 + 8 * C::NFULL;  // empty[s]: both CTAs, one multicast commit
+    const uint32_t conv0 = empty0 + 8 * STAGES;    // converted[s]: leader, 1 warp x 2 CTAs
+    const uint32_t accf0 = conv0 + 8 * STAGES;     // acc_full[b]: both CTAs, one multicast commit
     const uint32_t acce0 = accf0 + 16;            // acc_empty[b]: leader, both epilogues
     const uint32_t drain = acce0 + 16;
     uint32_t* tmem_slot =
@@ -722,8 +732,8 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
             prefetch_tmap(&tmAlo);
             prefetch_tmap(&tmBlo);
         }
+        for (int f = 0; f < C::NFULL; ++f) mbar_init(full0 + 8 * f, SPLIT_IN_KERNEL ? 1 : 2);
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, SPLIT_IN_KERNEL ? 1 : 2);
             mbar_init(empty0 + 8 * s, 1);
             mbar_init(conv0 + 8 * s, 2);
         }
@@ -766,7 +776,7 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                     const uint32_t st = sbase + s * C::STAGE_BYTES;
                     const int k0 = (w.kb_begin + kb) * BK;
                     if (SPLIT_IN_KERNEL) {
-                        const uint32_t fb = full0 + 8 * s;
+                        const uint32_t fb = full0 + 8 * (it % C::NFULL);
                         mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES);
                         tma_load_2d(st, &tmAhi, fb, k0, ma);
 #pragma unroll
@@ -795,7 +805,8 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
             const long long tail = ok ? timeout_ns : timeout_ns / 8 + 1000;
             for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j) {
                 if (SPLIT_IN_KERNEL)
-                    mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1, tail, fault, kFaultDrain);
+                    mbar_wait(full0 + 8 * (j % C::NFULL), (j / C::NFULL) & 1, tail, fault,
+                              kFaultDrain);
                 mbar_wait(empty0 + 8 * (j % STAGES), (j / STAGES) & 1, tail, fault, kFaultDrain);
             }
         }
@@ -871,10 +882,10 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                 const Unit w = decode_pair(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN,
                                            tail_tiles, tail_splits);
                 for (int kb = 0; kb < w.nkb; ++kb, ++it) {
-                    if ((it & 1) != warp - 2) continue;  // the other splitter's turn
+                    if (it % C::NSPLIT != warp - 2) continue;  // the other splitter's turn
                     const int s = it % STAGES;
-                    const bool got = role_wait(full0 + 8 * s, (it / STAGES) & 1, timeout_ns, fault,
-                                               kFaultFullBarrier, abort_flag);
+                    const bool got = role_wait(full0 + 8 * (it % C::NFULL), (it / C::NFULL) & 1,
+                                               timeout_ns, fault, kFaultFullBarrier, abort_flag);
                     if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
                         break;
