@@ -311,6 +311,18 @@ def test_general_form_alpha_beta_rules(algo):
     _ex_case(160, 200, 8209, 0, 1, 1, 0.25, 1.0, algo, splits=3)   # split-K applies alpha, beta
 
 
+@pytest.mark.parametrize("M,N,K,pad", [(130, 1022, 65, 2), (257, 1020, 130, 0), (64, 65, 63, 3),
+                                       (300, 4, 200, 0), (96, 130, 1, 2), (200, 66, 4097, 2)],
+                         ids=lambda v: str(v))
+def test_staging_edges(M, N, K, pad):
+    # the 3xTF32 staging kernels at their edges: B rows whose stride allows
+    # 16-byte loads but whose last 4-column group is ragged (N % 4 != 0 with
+    # N + pad a multiple of 4), 64 x 64 transpose tiles ragged in K and N,
+    # K = 1, and A read in place or copied (lda = K + pad)
+    _ex_case(M, N, K, 0, 0, pad, 1.0, 0.0, g.ALGO_3XTF32)
+    _ex_case(M, N, K, 1, 1, pad, 1.0, 0.0, g.ALGO_3XTF32)
+
+
 def test_general_form_on_the_pair_kernel():
     _ex_case(2304, 2304, 512, 1, 0, 4, -0.5, 1.5, g.ALGO_3XTF32)
 
