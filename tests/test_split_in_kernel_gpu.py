@@ -149,3 +149,51 @@ def test_general_form_through_the_in_kernel_split(ta, tb):
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and p["split_in_kernel"] == 1, p
     _ex_case(M, N, K, ta, tb, 4, -0.75, 1.25, g.ALGO_AUTO)
+
+
+def _full_mantissa_values(n, rng):
+    """fp32 values with all 23 mantissa bits in play: random words over
+    exponents 2^-20 .. 2^20 of both signs, plus words whose low 13 bits sit at
+    and around the TF32 rounding tie (0x0fff, 0x1000, 0x1001) for even and odd
+    TF32 mantissas."""
+    special = []
+    for m in (0, 1, 2, 3, 1022, 1023):
+        for low in (0x0001, 0x0fff, 0x1000, 0x1001, 0x1fff):
+            for e in (0, 5, -7):
+                for sign in (0, 1):
+                    special.append((sign << 31) | ((127 + e) << 23) | (m << 13) | low)
+    words = (rng.integers(0, 2, n, dtype=np.uint32) << 31) | \
+            (rng.integers(107, 148, n, dtype=np.uint32) << 23) | \
+            rng.integers(0, 1 << 23, n, dtype=np.uint32)
+    words[:len(special)] = np.array(special, dtype=np.uint32)
+    return words.view(np.float32)
+
+
+@pytest.mark.parametrize("tile", [g.TILE_128x128, PRESPLIT, SPLIT],
+                         ids=["single-cta-staged", "pair-staged", "pair-split"])
+def test_split_reconstructs_each_operand(tile):
+    # With a 0/1 selection matrix as the other operand, C reproduces one
+    # operand's elements through the TF32 split: hi (the fp32 word itself,
+    # read by the tensor core as trunc(x)) plus lo = tf32(x - trunc(x)).
+    # That sum is within 2^-22 |x| of x, and the tensor core's two-term
+    # accumulation adds at most one fp32 ulp, so |C - x| <= 2^-20 |x| holds.
+    # A tensor core that rounded the word instead of truncating it would be
+    # off by up to 2^-11 |x|: the bound pins the reading the split relies on.
+    rng = np.random.default_rng(11)
+    M = N = 256
+    K = 64
+    X = _full_mantissa_values(M * K, rng).reshape(M, K)
+    S = np.zeros((K, N), dtype=np.float32)
+    S[np.arange(N) % K, np.arange(N)] = 1.0          # column n selects k = n % K
+    want_a = X[:, np.arange(N) % K].astype(np.float64)
+    got_a = _gpu.run_configured(X, S, g.ALGO_3XTF32, tile, 1).astype(np.float64)
+    assert np.all(np.abs(got_a - want_a) <= 2.0 ** -20 * np.abs(want_a)), \
+        float(np.max(np.abs(got_a - want_a) / np.abs(want_a)))
+    # the other side: B split (and, staged, transposed) the same way
+    Y = _full_mantissa_values(K * N, rng).reshape(K, N)
+    T = np.zeros((M, K), dtype=np.float32)
+    T[np.arange(M), np.arange(M) % K] = 1.0          # row m selects k = m % K
+    want_b = Y[np.arange(M) % K, :].astype(np.float64)
+    got_b = _gpu.run_configured(T, Y, g.ALGO_3XTF32, tile, 1).astype(np.float64)
+    assert np.all(np.abs(got_b - want_b) <= 2.0 ** -20 * np.abs(want_b)), \
+        float(np.max(np.abs(got_b - want_b) / np.abs(want_b)))
