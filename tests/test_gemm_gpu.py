@@ -452,3 +452,30 @@ def test_host_buffer_entry_column_blocks(shape):
         cols = np.concatenate([rng.integers(0, N, M), rng.integers(0, N, 4000), np.arange(N)])
         _check(out[rows, cols].copy(), oracle.ref_gemm_entries(A, B, rows, cols),
                label=f"host column blocks {shape}")
+
+
+def test_host_buffer_entry_split_panels():
+    # row panels whose GEMMs split A and B in shared memory (each 1280 x 1024
+    # x 8192 panel has few flops per operand element and deep K), ragged last
+    # panel; the panel plan is checked so the case keeps covering that path
+    t = _gpu.torch()
+    M, N, K = 5000, 1024, 8192
+    st, p = g.gemm_f32_plan(1280, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["split_in_kernel"] == 1, p
+    A, B = make_workload(1, M=M, N=N, K=K)
+    hA = t.from_numpy(A).pin_memory()
+    hB = t.from_numpy(B).pin_memory()
+    hC = t.full((M + 1, N), float("nan")).pin_memory()
+    s = t.cuda.current_stream()
+    g.check(g.gemm_f32_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), M, N, K, g.ALGO_AUTO,
+                            s.cuda_stream), "gemm_f32_host")
+    s.synchronize()
+    g.check(g.gemm_f32_device_status(1), "device status")
+    out = hC.numpy()
+    assert np.isnan(out[M:]).all(), "write past C"
+    rng = np.random.default_rng(5)
+    rows = np.concatenate([np.arange(M), rng.integers(0, M, 3000)])
+    cols = np.concatenate([rng.integers(0, N, M), rng.integers(0, N, 3000)])
+    _check(out[rows, cols].copy(), oracle.ref_gemm_entries(A, B, rows, cols),
+           label="host split panels")
+
