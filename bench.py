@@ -212,28 +212,30 @@ def stored_traffic(kernel: str, workload: str) -> float | None:
 # ---------------------------------------------------------------------------
 # CPU oracle timing (the baseline arm)
 # ---------------------------------------------------------------------------
-def oracle_rows_timing(A, B, seconds: float) -> dict:
+def oracle_rows_timing(A, B, seconds: float, single_thread: bool = False) -> dict:
     """Time the oracle on the first R rows of C, R sized to take ~`seconds`.
 
     A warm-up pass on a few rows (page-in, thread start) is followed by a
     calibration pass; R is a multiple of the oracle's thread count so that
-    every thread gets the same number of rows.
+    every thread gets the same number of rows.  single_thread: the oracle on
+    one host thread.
     """
     import oracle
 
     M, K = A.shape
     N = B.shape[1]
-    threads = max(1, oracle.max_threads())
-    oracle.ref_gemm_rows(A, B, 0, min(M, threads))  # warm-up
+    nt = 1 if single_thread else 0  # 0: all of the oracle's threads
+    threads = 1 if single_thread else max(1, oracle.max_threads())
+    oracle.ref_gemm_rows(A, B, 0, min(M, threads), nthreads=nt)  # warm-up
     cal = min(M, 2 * threads)
     t0 = time.perf_counter()
-    oracle.ref_gemm_rows(A, B, 0, cal)
+    oracle.ref_gemm_rows(A, B, 0, cal, nthreads=nt)
     per_row = max(time.perf_counter() - t0, 1e-6) / cal
     rows = int(seconds / per_row) // threads * threads
     rows = int(max(threads, min(M, rows)))
     rows = min(rows, M)
     t0 = time.perf_counter()
-    oracle.ref_gemm_rows(A, B, 0, rows)
+    oracle.ref_gemm_rows(A, B, 0, rows, nthreads=nt)
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * N * K
     return {"rows": rows, "seconds": dt, "flops": flops, "tflops": flops / dt / 1e12,
@@ -460,6 +462,13 @@ def run_ours(args, world, rank, local):
         cpu = {"value": cb["tflops"], "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
                "sample": (f"rows 0..{cb['rows'] - 1} of the {M}x{N}x{K} product "
                           f"({cb['rows'] * N} outputs, full K, {cb['seconds']:.1f} s)")}
+        if 2.0 * M * N * K <= 2.0 * 2048 ** 3:
+            # the small workloads also on one host thread
+            c1 = oracle_rows_timing(A_np, B_np, min(args.cpu_seconds, 10.0), single_thread=True)
+            cpu["single_thread"] = {
+                "value": c1["tflops"], "unit": UNIT, "cores": 1,
+                "sample": (f"rows 0..{c1['rows'] - 1} of the product "
+                           f"({c1['rows'] * N} outputs, full K, {c1['seconds']:.1f} s)")}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K_steps,
