@@ -248,6 +248,30 @@ int choose_splits(int requested, int tiles, int kb_total, int slots, int min_kb 
     return s;
 }
 
+// The split-K factor the single-CTA tensor-core kernel gets for tiles of
+// 128 x bn (see make_plan): choose_splits, capped at 4 (K <= 1024) or 8
+// (K <= 4096) splits when the library chooses.
+int single_cta_splits(int sm_count, int tiles, int K, int splits) {
+    const int kb_total = (K + 31) / 32;
+    int s = choose_splits(splits, tiles, kb_total, sm_count, 4);
+    if (splits == 0 && K <= 4096) {
+        const int cap = K <= 1024 ? 4 : 8;
+        if (s > cap) s = cap;
+    }
+    return s;
+}
+
+// The fraction of the SMs' round capacity that 128 x bn tiles with their
+// split-K factor keep busy, divided by the padding of N to whole tiles.
+double single_cta_fill(int sm_count, int M, int N, int K, int bn, int splits) {
+    const int tiles_n = (N + bn - 1) / bn;
+    const int tiles = ((M + 127) / 128) * tiles_n;
+    const long long units = static_cast<long long>(tiles) * single_cta_splits(sm_count, tiles, K, splits);
+    const long long rounds = (units + sm_count - 1) / sm_count;
+    const double busy = static_cast<double>(units) / (static_cast<double>(rounds) * sm_count);
+    return busy * N / (static_cast<double>(tiles_n) * bn);
+}
+
 size_t carve(size_t* off, long long bytes) {
     const size_t at = *off;
     *off += static_cast<size_t>(round_up(bytes, 256));
@@ -271,13 +295,26 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         // the two-CTA 256 x 256 kernel when its tiles fill at least four
         // fifths of the SM pairs (it keeps the tensor pipe busier than one
         // CTA per tile: 2048^2 x 8192, 64 pair tiles on 76 pairs, 309 against
-        // 330 us for 128 x 256; 2048^3 even); otherwise one CTA per 128 x 256
-        // tile when those fill at least three quarters of the SMs, else
-        // 128 x 128 tiles with split-K
+        // 330 us for 128 x 256; 2048^3 even) and K is at least 1024 (with a
+        // few K blocks per tile the fill and the 256 x 256 epilogue of each
+        // tile dominate: 2378 x 4792 x 286, 74 against 49 us for 128 x 128);
+        // otherwise one CTA per 128 x 256 tile when those fill at least three
+        // quarters of the SMs, else 128 x 128 tiles with split-K
         const int units_pair = ((M + 255) / 256) * ((N + 255) / 256);
         const int tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
-        p->pair = 5 * units_pair >= 4 * (d.sm_count / 2) ? 1 : 0;
+        p->pair = (5 * units_pair >= 4 * (d.sm_count / 2) && K >= 1024) ? 1 : 0;
         p->bn = (p->pair || (4 * tiles256 >= 3 * d.sm_count && N > 128)) ? 256 : 128;
+        if (!p->pair) {
+            // ... unless the other single-CTA width keeps clearly more of the
+            // SMs busy (its tiles x K splits per round, net of padding in N):
+            // 5170 x 151 x 5906, 82 tiles of 128 x 128 leave 46 % of the SMs
+            // idle where 41 of 128 x 256 in 3 in-cluster splits fill 81 %
+            // (162 against 214 us)
+            const double u128 = single_cta_fill(d.sm_count, M, N, K, 128, splits);
+            const double u256 = single_cta_fill(d.sm_count, M, N, K, 256, splits);
+            if (u256 > 1.1 * u128) p->bn = 256;
+            else if (u128 > 1.1 * u256) p->bn = 128;
+        }
         // Few flops per operand element: the staging pass over A and B (8-12
         // bytes per element) then costs more than the tensor work saved by
         // the staged kernel, so the pair kernel that splits A and B in shared

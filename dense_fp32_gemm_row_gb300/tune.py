@@ -13,7 +13,8 @@ staging kernels or splitting its operands in shared memory) x split-K
 factor.  Every configuration runs once through ``gemm_f32_configured`` and
 must match cuBLAS SGEMM (TF32 off) within 1e-3 + 1e-3 |ref| on every output
 before it is timed (median of ``--repeats`` calls, CUDA events, L2 flushed
-between calls when the inputs fit in it).  The library's own choice
+between calls when the inputs fit in it; the configurations of a shape are
+timed round-robin, one call each per round).  The library's own choice
 (``gemm_f32``, AUTO) is timed alongside so the table shows how far AUTO is
 from the best configuration per shape.
 
@@ -76,23 +77,22 @@ def sweep(shapes, repeats: int, out=sys.stdout, quick: bool = False) -> list[dic
         fits_l2 = 4 * (M * K + K * N) < 256 * 1024 * 1024
         flops = 2.0 * M * N * K
 
-        def timed(call):
-            for _ in range(2):
-                call()
-            ts = []
-            for _ in range(repeats):
-                if fits_l2:
-                    flush.zero_()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                call()
-                e1.record(stream)
-                e1.synchronize()
-                ts.append(e0.elapsed_time(e1))
-            return statistics.median(ts)
+        def timed_once(call):
+            if fits_l2:
+                flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            e1.synchronize()
+            return e0.elapsed_time(e1)
 
-        results = []
+        # every configuration is checked first, then all passing ones are
+        # timed round-robin (one call each per round), so that none is
+        # favoured or penalised by its place in the order (clock and cache
+        # state drift over a shape's run)
+        results, calls = [], []
         candidates = [(g.ALGO_AUTO, 0, 0)] + list(_configs(g, quick))
         for algo, tile, splits in candidates:
             st, plan = (g.gemm_f32_plan(M, N, K, algo, splits, a.data_ptr(), b.data_ptr(),
@@ -115,15 +115,26 @@ def sweep(shapes, repeats: int, out=sys.stdout, quick: bool = False) -> list[dic
             call()
             stream.synchronize()
             ok = bool(((c - ref).abs() <= 1e-3 + 1e-3 * ref.abs()).all().item())
-            ms = timed(call) if ok else float("nan")
             results.append({"shape": f"{M}x{N}x{K}", "algo": names[algo],
                             "tile": tiles[tile] if algo != g.ALGO_AUTO else
                             f"{plan['tile_m']}x{plan['tile_n']}"
                             + ("-split" if plan.get("split_in_kernel") else ""),
                             "splits": plan["splits"], "ctas": plan["ctas"],
-                            "kernels": plan["kernels"], "ms": ms,
-                            "tflops": flops / (ms * 1e-3) / 1e12 if ok else 0.0,
+                            "kernels": plan["kernels"], "ms": float("nan"), "tflops": 0.0,
                             "check": "pass" if ok else "FAIL", "auto": algo == g.ALGO_AUTO})
+            calls.append(call if ok else None)
+        live = [i for i, cl in enumerate(calls) if cl is not None]
+        for i in live:
+            for _ in range(2):
+                calls[i]()
+        times = {i: [] for i in live}
+        for _ in range(repeats):
+            for i in live:
+                times[i].append(timed_once(calls[i]))
+        for i in live:
+            ms = statistics.median(times[i])
+            results[i]["ms"] = ms
+            results[i]["tflops"] = flops / (ms * 1e-3) / 1e12
         ranked = sorted((r for r in results if r["check"] == "pass" and not r["auto"]),
                         key=lambda r: r["ms"])
         for i, r in enumerate(ranked):

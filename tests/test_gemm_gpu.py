@@ -113,21 +113,37 @@ PAIR_SHAPES = [(2304, 2304, 512), (2305, 2049, 1000), (2560, 2330, 77), (4096, 2
                          ids=lambda s: "x".join(map(str, s)))
 def test_pair_kernel_rule(shape):
     # the staged tensor-core path takes the two-CTA kernel once its 256 x 256
-    # tiles fill at least four fifths of the SM pairs
+    # tiles fill at least four fifths of the SM pairs and K is at least 1024
     M, N, K = shape
     pairs = _gpu.torch().cuda.get_device_properties(0).multi_processor_count // 2
     units = ((M + 255) // 256) * ((N + 255) // 256)
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_3XTF32, 0, A=1 << 32, B=1 << 36, C=1 << 40)
-    assert st == 0 and (p["tile_m"] == 256) == (5 * units >= 4 * pairs), (units, pairs, p)
+    want = 5 * units >= 4 * pairs and K >= 1024
+    assert st == 0 and (p["tile_m"] == 256) == want, (units, pairs, p)
+
+
+@pytest.mark.parametrize("shape,bn", [((5170, 151, 5906), 256), ((2378, 4792, 286), 128),
+                                      ((1025, 1023, 1000), 128), ((5514, 160, 43878), 256)],
+                         ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
+def test_single_cta_width_rule(shape, bn):
+    # the single-CTA width: 128 x 256 when its tiles fill three quarters of
+    # the SMs, or when with their split-K factor they keep clearly (10 %) more
+    # of the SMs busy, net of padding, than 128 x 128 tiles (and vice versa)
+    M, N, K = shape
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_3XTF32, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["tile_m"] == 128 and p["tile_n"] == bn, p
 
 
 @pytest.mark.parametrize("shape", PAIR_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_pair_kernel_shapes(shape):
+    # the two-CTA kernel on staged operands, forced (AUTO takes it only from
+    # K = 1024 on), over ragged M, N and K down to K = 77
     M, N, K = shape
-    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_3XTF32, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, g.TILE_256x256_PAIR, 0,
+                                   A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and p["tile_m"] == 256 and p["tile_n"] == 256, p
     A, B = make_workload(2, M=M, N=N, K=K)
-    C = _gpu.run(A, B, g.ALGO_3XTF32)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, g.TILE_256x256_PAIR)
     rng = np.random.default_rng(M + N + K)
     rows = np.concatenate([np.arange(M), rng.integers(0, M, 3000), np.full(N, M - 1)])
     cols = np.concatenate([rng.integers(0, N, M), rng.integers(0, N, 3000), np.arange(N)])
