@@ -250,13 +250,28 @@ int choose_splits(int requested, int tiles, int kb_total, int slots, int min_kb 
 
 // The split-K factor the single-CTA tensor-core kernel gets for tiles of
 // 128 x bn (see make_plan): choose_splits, capped at 4 (K <= 1024) or 8
-// (K <= 4096) splits when the library chooses.
-int single_cta_splits(int sm_count, int tiles, int K, int splits) {
+// (K <= 4096) splits when the library chooses.  A factor of 2..8 with one
+// unit per CTA adds its partials inside clusters, all of which must be
+// co-resident: a library-chosen factor is lowered until the tiles' clusters
+// fit on the device at once (101 x 5159 x 61036: 21 tiles of 128 x 256 in
+// clusters of 7 ran in two waves, only 15 such clusters fitting).
+int single_cta_splits(int sm_count, int tiles, int K, int splits, int bn) {
     const int kb_total = (K + 31) / 32;
     int s = choose_splits(splits, tiles, kb_total, sm_count, 4);
     if (splits == 0 && K <= 4096) {
         const int cap = K <= 1024 ? 4 : 8;
         if (s > cap) s = cap;
+    }
+    if (splits == 0) {
+        while (s >= 2 && s <= 8 && static_cast<long long>(tiles) * s <= sm_count) {
+            int fit = 0;
+            if (tf32x3_single_cluster_capacity(bn, s, &fit) != cudaSuccess) {
+                cudaGetLastError();
+                break;
+            }
+            if (tiles <= fit) break;
+            --s;
+        }
     }
     return s;
 }
@@ -266,7 +281,8 @@ int single_cta_splits(int sm_count, int tiles, int K, int splits) {
 double single_cta_fill(int sm_count, int M, int N, int K, int bn, int splits) {
     const int tiles_n = (N + bn - 1) / bn;
     const int tiles = ((M + 127) / 128) * tiles_n;
-    const long long units = static_cast<long long>(tiles) * single_cta_splits(sm_count, tiles, K, splits);
+    const long long units =
+        static_cast<long long>(tiles) * single_cta_splits(sm_count, tiles, K, splits, bn);
     const long long rounds = (units + sm_count - 1) / sm_count;
     const double busy = static_cast<double>(units) / (static_cast<double>(rounds) * sm_count);
     return busy * N / (static_cast<double>(tiles_n) * bn);
@@ -309,9 +325,12 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
             // SMs busy (its tiles x K splits per round, net of padding in N):
             // 5170 x 151 x 5906, 82 tiles of 128 x 128 leave 46 % of the SMs
             // idle where 41 of 128 x 256 in 3 in-cluster splits fill 81 %
-            // (162 against 214 us)
+            // (162 against 214 us).  The 128 x 256 kernel's 2-stage ring runs
+            // a unit of given work ~15 % slower than the 3-stage 128 x 128
+            // one, so its fill counts 0.85 (896^2 x 4096: 5 splits of 128 x
+            // 256, 87 us, against 3 of 128 x 128, 75 us)
             const double u128 = single_cta_fill(d.sm_count, M, N, K, 128, splits);
-            const double u256 = single_cta_fill(d.sm_count, M, N, K, 256, splits);
+            const double u256 = 0.85 * single_cta_fill(d.sm_count, M, N, K, 256, splits);
             if (u256 > 1.1 * u128) p->bn = 256;
             else if (u128 > 1.1 * u256) p->bn = 128;
         }
@@ -385,11 +404,10 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     // (no reduction launch, ~6 us saved); for K <= 4096 that beats the extra
     // splits' shorter main loops (300 x 260 x 3000: 8 splits in a cluster
     // 25.8 us, 16 through the workspace 28.3 us), and for K <= 1024 four
-    // splits beat eight (400 x 400 x 1024: 21.1 against 25.2 us)
-    if (splits == 0 && p->algo == GEMM_F32_ALGO_3XTF32 && !p->pair && K <= 4096) {
-        const int cap = K <= 1024 ? 4 : 8;
-        if (s > cap) s = cap;
-    }
+    // splits beat eight (400 x 400 x 1024: 21.1 against 25.2 us); its
+    // clusters must all fit on the device at once (single_cta_splits)
+    if (p->algo == GEMM_F32_ALGO_3XTF32 && !p->pair)
+        s = single_cta_splits(d.sm_count, tiles, K, splits, p->bn);
     p->kb_per_split = (kb_total + s - 1) / s;
     p->splits = (kb_total + p->kb_per_split - 1) / p->kb_per_split;
     const int units = tiles * p->splits;
@@ -433,8 +451,15 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     // The single-CTA tensor-core kernel likewise, when every CTA gets exactly
     // one unit (its stage memory then holds the partial after the main loop)
     if (p->algo == GEMM_F32_ALGO_3XTF32 && !p->pair && p->splits >= 2 && p->splits <= 8 &&
-        units <= d.sm_count)
-        p->cluster_splits = p->splits;
+        units <= d.sm_count) {
+        // ... whose clusters all fit on the device at once (else, with a
+        // caller's split factor, the workspace reduction)
+        int fit = 0;
+        if (tf32x3_single_cluster_capacity(p->bn, p->splits, &fit) == cudaSuccess &&
+            tiles <= fit)
+            p->cluster_splits = p->splits;
+        cudaGetLastError();
+    }
     if (p->splits > 1 && !p->cluster_splits)
         p->off_w = carve(&off, static_cast<long long>(p->splits) * M * p->ldw * 4);
     // The pair kernel's last round of tiles is usually only partly full

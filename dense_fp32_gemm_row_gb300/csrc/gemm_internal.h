@@ -97,6 +97,11 @@ struct Tf32x3Args {
 };
 // co-resident two-CTA clusters of the pair kernel on the current device
 cudaError_t tf32x3_pair_clusters(int sm_count, int* clusters);
+// co-resident clusters of `splits` (1..8) CTAs of the single-CTA kernel with
+// 128 x bn tiles on the current device: the SMs do not divide into every
+// cluster size (GB300, one CTA per SM: 76 of 2, 46 of 3, 36 of 4, 28 of 5,
+// 23 of 6, 15 of 7 or 8)
+cudaError_t tf32x3_single_cluster_capacity(int bn, int splits, int* clusters);
 // persistent grid: min(units, sm_count) CTAs, or for the pair kernel
 // 2 x min(units, co-resident clusters)
 cudaError_t launch_sgemm_3xtf32(const Tf32x3Args& a, cudaStream_t s, int sm_count);

@@ -1103,6 +1103,51 @@ Tf32x3Config tf32x3_config(int bn, bool pair) {
     return {BM, 256, BK, 2, Cfg<256, 2>::THREADS, Cfg<256, 2>::SMEM_BYTES, 0, 256};
 }
 
+namespace {
+// Co-resident clusters of `splits` CTAs of the single-CTA kernel (one CTA per
+// SM by its shared memory), from the occupancy calculator, cached per device.
+template <int BN, int STAGES>
+cudaError_t single_cluster_capacity(int splits, int* clusters) {
+    using C = Cfg<BN, STAGES>;
+    static thread_local int cached_dev = -1;
+    static thread_local int cap[kMaxClusterSplits + 1] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (cached_dev != dev) {
+        auto kern = sgemm_3xtf32_kernel<BN, STAGES>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        for (int sz = 1; sz <= kMaxClusterSplits; ++sz) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = static_cast<unsigned>(sz);
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(static_cast<unsigned>(sz));
+            cfg.blockDim = dim3(C::THREADS);
+            cfg.dynamicSmemBytes = C::SMEM_BYTES;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+            if (e != cudaSuccess) return e;
+            cap[sz] = n;
+        }
+        cached_dev = dev;
+    }
+    *clusters = cap[splits];
+    return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t tf32x3_single_cluster_capacity(int bn, int splits, int* clusters) {
+    if (splits < 1 || splits > kMaxClusterSplits) return cudaErrorInvalidValue;
+    return bn == 128 ? single_cluster_capacity<128, 3>(splits, clusters)
+                     : single_cluster_capacity<256, 2>(splits, clusters);
+}
+
 cudaError_t launch_sgemm_3xtf32(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
     if (a.pair)
         return a.split_in_kernel ? launch_pair<3, true>(a, s, sm_count)

@@ -149,3 +149,19 @@ def test_3xtf32_more_units_than_sms_uses_the_workspace():
 
 def test_3xtf32_cluster_alpha_beta():
     _ex_case(300, 260, 3000, 0, 0, 5, 0.5, -1.25, g.ALGO_3XTF32, splits=4)
+
+
+def test_3xtf32_clusters_that_do_not_all_fit_use_the_workspace():
+    # 21 tiles of 128 x 256 in clusters of 7: fewer such clusters fit on the
+    # device at once (15 on a 152-SM GB300), so a caller's 7-way split goes
+    # through the workspace instead of running the clusters in two waves,
+    # and AUTO picks a plan whose clusters do fit (128 x 128, 3 splits)
+    if _gpu.torch().cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("cluster capacities measured on a 152-SM part")
+    M, N, K = 101, 5159, 61036
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, g.TILE_128x256, 7,
+                                   A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["splits"] == 7 and p["cluster_reduce"] == 0, p
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and (p["tile_m"], p["tile_n"]) == (128, 128) and p["splits"] == 3, p
+    assert p["cluster_reduce"] == 1, p

@@ -128,7 +128,8 @@ def test_pair_kernel_rule(shape):
 def test_single_cta_width_rule(shape, bn):
     # the single-CTA width: 128 x 256 when its tiles fill three quarters of
     # the SMs, or when with their split-K factor they keep clearly (10 %) more
-    # of the SMs busy, net of padding, than 128 x 128 tiles (and vice versa)
+    # of the SMs busy, net of padding and of the 2-stage kernel's lower rate
+    # (x 0.85), than 128 x 128 tiles (and vice versa)
     M, N, K = shape
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_3XTF32, 0, A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and p["tile_m"] == 128 and p["tile_n"] == bn, p
