@@ -45,6 +45,7 @@ L2_BYTES = 129 * 1000 * 1000
 # nominal dense tensor rates of the part (context for scaling a measured peak)
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_TF32_TFLOPS = 1100.0
+SUSTAINED_S = 2.0  # timed regions longer than this are scored against the sustained peak
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "sm_max_mhz": 2070.0}
 FFMA_LANES_PER_SM = 128  # FP32 FMA units per SM (4 sub-partitions x 32)
@@ -412,8 +413,14 @@ def run_ours(args, world, rank, local):
     kern_mean_s = statistics.mean(kern_ms) * 1e-3
     achieved = flops / kern_mean_s / 1e12
     props = torch.cuda.get_device_properties(dev)
+    # a timed region of more than SUSTAINED_S seconds runs under the power
+    # cap (measured: 1.37 kW, SM clock 1.86 GHz over 7.6 s of 8192^3 calls),
+    # so its tensor peak is the sustained bf16 figure, else the burst one
+    sustained = total_ms * 1e-3 > SUSTAINED_S
+    peak_kind = "sustained" if sustained else "burst"
     if plan["algo"] == g.ALGO_3XTF32:
-        bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+        bf16 = float(peaks.get(key, FALLBACK_PEAKS[key]))
         peak = bf16 * (NOMINAL_TF32_TFLOPS / NOMINAL_BF16_TFLOPS) / 3.0
         bound, kname = "tensor", "sgemm_3xtf32"
     else:
@@ -422,7 +429,7 @@ def run_ours(args, world, rank, local):
         bound, kname = "alu", "sgemm_ffma"
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": stored_traffic(kname, w.name),
-                "kernel": kname, "peak_source": peak_src}
+                "kernel": kname, "peak_source": peak_src, "peak_kind": peak_kind}
 
     # end to end through the public host-buffer entry point (pinned host
     # memory): every step copies A and B in and C out inside the call
