@@ -73,7 +73,10 @@ extern "C" {
  * (the fp32 word itself, which the tensor core reads truncated) and a TF32
  * low part tf32(x - trunc(x)); three tcgen05 products hi*hi + hi*lo + lo*hi
  * accumulated in tensor memory in fp32, promoted every 128 K into fp32
- * registers. */
+ * registers.  Non-finite operands: an Inf's low part is Inf - Inf = NaN, so
+ * an output that is +-Inf in exact arithmetic may come back NaN; NaN inputs
+ * still give NaN, and outputs whose row of op(A) and column of op(B) are
+ * finite are unaffected.  The FFMA kernel follows IEEE fp32 there. */
 #define GEMM_F32_ALGO_3XTF32  2
 
 /* Largest explicit split-K factor accepted by gemm_f32_algo_splitk. */

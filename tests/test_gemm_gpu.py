@@ -496,3 +496,34 @@ def test_host_buffer_entry_split_panels():
     _check(out[rows, cols].copy(), oracle.ref_gemm_entries(A, B, rows, cols),
            label="host split panels")
 
+
+
+@pytest.mark.parametrize("algo", [g.ALGO_FFMA, g.ALGO_3XTF32], ids=["ffma", "3xtf32"])
+def test_non_finite_inputs(algo):
+    # NaN and +-Inf in A and B.  FFMA follows IEEE fp32 exactly: an output is
+    # NaN, +Inf or -Inf exactly where the oracle's is.  3xTF32 splits each
+    # value into hi + lo, and an Inf's low part (Inf - Inf) and the cross
+    # products Inf * (a zero low part) are NaN, so where the oracle gives
+    # +-Inf it gives +-Inf or NaN; NaN stays NaN.  Outputs whose row of A and
+    # column of B are finite are checked against the oracle as usual.
+    M, N, K = 96, 80, 64
+    A, B = make_workload(1, M=M, N=N, K=K)
+    A[3, 5] = np.inf
+    A[10, 7] = -np.inf
+    A[20, 9] = np.nan
+    B[11, 30] = np.inf
+    B[12, 31] = np.nan
+    B[5, 40] = 0.0          # Inf * 0 in the exact sum: NaN at C[3, 40]
+    want = oracle.ref_gemm(A, B)
+    got = _gpu.run(A, B, algo)
+    assert np.array_equal(np.isnan(got) & np.isnan(want), np.isnan(want)), "NaN lost"
+    inf_w = np.isinf(want)
+    if algo == g.ALGO_FFMA:
+        assert np.array_equal(np.isnan(got), np.isnan(want))
+        assert np.array_equal(got[inf_w], want[inf_w])
+    else:
+        assert np.all(np.isnan(got[inf_w]) | (got[inf_w] == want[inf_w]))
+    finite_rows = np.isfinite(A).all(axis=1)
+    finite_cols = np.isfinite(B).all(axis=0)
+    sel = np.ix_(finite_rows, finite_cols)
+    _check(got[sel].copy(), want[sel].copy(), label=f"finite part/{algo}")
