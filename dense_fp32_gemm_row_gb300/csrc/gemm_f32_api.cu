@@ -616,6 +616,12 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
         ta.tail_splits = tail ? p.tail_splits : 0;
         ta.tail_ws = tail ? reinterpret_cast<float*>(ws + p.off_t) : nullptr;
         ta.cluster_splits = p.cluster_splits;
+        if (p.pair && vec_store && p.splits == 1 && kmode != 2) {  // no beta term
+            if ((st = encode_2d(&ta.tmC, out, N, M, ldo, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B)) !=
+                GEMM_F32_SUCCESS)
+                return st;
+            ta.tma_store = 1;
+        }
         if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
             return static_cast<int>(e);
         if ((e = launch_sgemm_3xtf32(ta, stream, d.sm_count)) != cudaSuccess)

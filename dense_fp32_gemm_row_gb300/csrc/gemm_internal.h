@@ -90,6 +90,12 @@ struct Tf32x3Args {
     // 256 x 256 floats) and summed into C by a fix-up kernel
     int tail_tiles, tail_splits;
     float* tail_ws;
+    // pair kernel: tma_store = 1 writes C through shared memory with TMA
+    // stores, tmC being C as {N, M}, box {16, 32}, 64-byte swizzle (splits
+    // == 1, C 16-byte aligned with a row stride that is a multiple of 4, and
+    // no beta term)
+    CUtensorMap tmC;
+    int tma_store;
     // single-CTA kernels, 0 or 2..8 (equal to splits, one unit per CTA): each
     // tile's splits run as one cluster and add their partials in split order
     // through distributed shared memory; out is C

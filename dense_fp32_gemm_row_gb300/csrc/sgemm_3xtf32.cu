@@ -578,10 +578,15 @@ struct PairCfg {
     static constexpr int NFULL = SPLIT_IN_KERNEL ? STAGES * NSPLIT : STAGES;
     // full (NFULL), empty, converted (per stage), acc_full x2, acc_empty x2, drain
     static constexpr int NBARS = NFULL + 2 * STAGES + 5;
+    // output slabs of the TMA-store epilogue: two per epilogue warp, each 32
+    // rows x 16 columns (64-byte swizzle), after the stages
+    static constexpr int EPI_SLAB_COLS = 16;
+    static constexpr int EPI_SLAB_BYTES = 32 * EPI_SLAB_COLS * 4;
+    static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_SLAB_BYTES;
     // both variants reserve room for the split variant's barriers, so that
     // they have the same shared-memory size (and occupancy)
-    static constexpr int SMEM_BYTES =
-        STAGES * STAGE_BYTES + (STAGES * NSPLIT + 2 * STAGES + 5) * 8 + 16 + 1024;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES +
+                                      (STAGES * NSPLIT + 2 * STAGES + 5) * 8 + 16 + 1024;
     static constexpr uint32_t IDESC = idesc_tf32_f32(2 * BM, BN);
     static_assert(A_BYTES == B_BYTES && B_BYTES == 16384,
                   "the splitter's thread-to-element maps below");
@@ -694,13 +699,15 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                          long long ldo, long long split_stride, int M, int N, int K,
                          int kb_per_split, int splits, int vec_store, unsigned* fault,
                          long long timeout_ns, float alpha, float beta, int scale_mode,
-                         int tail_tiles, int tail_splits, float* __restrict__ tail_ws) {
+                         int tail_tiles, int tail_splits, float* __restrict__ tail_ws,
+                         const __grid_constant__ CUtensorMap tmC, int tma_store) {
     using C = PairCfg<STAGES, SPLIT_IN_KERNEL>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t bar0 = sbase + STAGES * C::STAGE_BYTES;
+    const uint32_t epi0 = sbase + STAGES * C::STAGE_BYTES;  // output slabs
+    const uint32_t bar0 = epi0 + C::EPI_BYTES;
     // full[f]: pre-split operands: f = stage, the leader's, count 2 (both
     //          producers); split in kernel: f = fill mod NFULL, each CTA's
     //          own, count 1
@@ -710,8 +717,8 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
     const uint32_t accf0 = conv0 + 8 * STAGES;     // acc_full[b]: both CTAs, one multicast commit
     const uint32_t acce0 = accf0 + 16;            // acc_empty[b]: leader, both epilogues
     const uint32_t drain = acce0 + 16;
-    uint32_t* tmem_slot =
-        reinterpret_cast<uint32_t*>(smem + STAGES * C::STAGE_BYTES + C::NBARS * 8);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + STAGES * C::STAGE_BYTES +
+                                                      C::EPI_BYTES + C::NBARS * 8);
     const uint32_t abort_flag = smem_addr(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -732,6 +739,7 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
             prefetch_tmap(&tmAlo);
             prefetch_tmap(&tmBlo);
         }
+        if (tma_store) prefetch_tmap(&tmC);
         for (int f = 0; f < C::NFULL; ++f) mbar_init(full0 + 8 * f, SPLIT_IN_KERNEL ? 1 : 2);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(empty0 + 8 * s, 1);
@@ -910,6 +918,7 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
         const int row = 32 * q + lane;
         float acc[EPI_COLS];
         int g = 0;
+        int stores = 0;  // TMA stores this warp has issued
         bool ok = true;
         for (int u = cluster; u < units && ok; u += nclusters) {
             const Unit w = decode_pair(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, tail_tiles, tail_splits);
@@ -953,6 +962,48 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                            0.0f, kStorePlain);
                 continue;
             }
+            if (tma_store) {
+                // Through shared memory: 16-column pieces of the warp's 32
+                // rows go to one of its two slabs (64-byte swizzle: the 16-byte
+                // chunk c of row r sits at chunk c ^ ((r >> 1) & 3), so the
+                // lanes' float4 writes hit distinct banks) and out with one
+                // TMA store each, whole lines, while the next tile's MMAs
+                // run.  Ragged edges are clipped by the tensor map's extent.
+                // Pieces wholly outside C are skipped, and the slabs alternate
+                // by stores issued (not by piece), so that the store that last
+                // read a slab is always the one before the latest.
+                const uint32_t slabs = epi0 + static_cast<uint32_t>(e) * 2 * C::EPI_SLAB_BYTES;
+                const int y = w.m0 + static_cast<int>(rank) * BM + 32 * q;
+#pragma unroll
+                for (int pc = 0; pc < EPI_COLS / C::EPI_SLAB_COLS; ++pc) {
+                    const int x = w.n0 + col0 + pc * C::EPI_SLAB_COLS;
+                    if (y >= M || x >= N) continue;  // the same for the whole warp
+                    const uint32_t slab = slabs + (stores & 1) * C::EPI_SLAB_BYTES;
+                    ++stores;
+                    // the store issued from this slab two stores ago has read it
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < C::EPI_SLAB_COLS / 4; ++c) {
+                        const int j = pc * C::EPI_SLAB_COLS + 4 * c;
+                        float4 v = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                        if (scale_mode == kStoreAlpha) {
+                            v.x *= alpha;
+                            v.y *= alpha;
+                            v.z *= alpha;
+                            v.w *= alpha;
+                        }
+                        sts128(slab + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), v);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, slab, x, y);
+                        bulk_commit();
+                    }
+                }
+                continue;
+            }
             const int m = w.m0 + static_cast<int>(rank) * BM + row;
             if (m < M) {
                 float* orow = out + static_cast<long long>(w.split) * split_stride +
@@ -964,6 +1015,9 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                            vec_store != 0, alpha, beta, scale_mode);
             }
         }
+        // the output stores have completed (and no longer read the slabs)
+        if (tma_store && lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     // neither CTA may leave while its partner can still reach its shared memory
@@ -1071,7 +1125,7 @@ cudaError_t launch_pair(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
     e = cudaLaunchKernelEx(&cfg, kern, a.tmAhi, a.tmAlo, a.tmBhi, a.tmBlo, a.out, a.ldo,
                            a.split_stride, a.M, a.N, a.K, a.kb_per_split, a.splits, a.vec_store,
                            a.fault, a.timeout_ns, a.alpha, a.beta, a.scale_mode, a.tail_tiles,
-                           a.tail_splits, a.tail_ws);
+                           a.tail_splits, a.tail_ws, a.tmC, a.tma_store);
     if (e != cudaSuccess) return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (a.tail_tiles) {

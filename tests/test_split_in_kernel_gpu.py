@@ -197,3 +197,32 @@ def test_split_reconstructs_each_operand(tile):
     got_b = _gpu.run_configured(T, Y, g.ALGO_3XTF32, tile, 1).astype(np.float64)
     assert np.all(np.abs(got_b - want_b) <= 2.0 ** -20 * np.abs(want_b)), \
         float(np.max(np.abs(got_b - want_b) / np.abs(want_b)))
+
+
+@pytest.mark.parametrize("tile", [PRESPLIT, SPLIT], ids=["pair-staged", "pair-split"])
+@pytest.mark.parametrize("shape", [(256, 200, 64), (300, 200, 1000), (520, 100, 96),
+                                   (257, 1028, 64), (700, 452, 300)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_pair_output_boxes(tile, shape):
+    # Both pair kernels write C through shared memory with TMA stores of 32-row
+    # x 16-column boxes.  A ragged N leaves one box partly inside C followed by
+    # boxes wholly outside it (not issued); a ragged M leaves warps whose rows
+    # are all outside.  Every element is compared, and a second run must give
+    # the same bits (a slab reused before its store had read it would not).
+    M, N, K = shape
+    A, B = make_workload(3, M=M, N=N, K=K)
+    want = oracle.ref_gemm(A, B)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, tile, 1)
+    _check(C, want, label=f"pair output boxes {shape}")
+    C2 = _gpu.run_configured(A, B, g.ALGO_3XTF32, tile, 1)
+    assert np.array_equal(C.view(np.uint32), C2.view(np.uint32)), "not run-to-run identical"
+
+
+def test_pair_output_boxes_alpha():
+    # alpha without beta: the pair kernel scales the values it stages for the
+    # TMA stores; ragged N (2100 = 8 * 256 + 52) and a padded row stride
+    from .test_gemm_gpu import _ex_case
+    M, N, K = 2100, 2100, 1024
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and (p["tile_m"], p["tile_n"]) == (256, 256), p
+    _ex_case(M, N, K, 0, 0, 4, 0.5, 0.0, g.ALGO_AUTO)
