@@ -90,10 +90,11 @@ struct Tf32x3Args {
     // 256 x 256 floats) and summed into C by a fix-up kernel
     int tail_tiles, tail_splits;
     float* tail_ws;
-    // pair kernel: tma_store = 1 writes C through shared memory with TMA
+    // tma_store = 1: the GEMM kernel writes C through shared memory with TMA
     // stores, tmC being C as {N, M}, box {16, 32}, 64-byte swizzle (splits
-    // == 1, C 16-byte aligned with a row stride that is a multiple of 4, and
-    // no beta term)
+    // == 1 without a cluster split, C 16-byte aligned with N and the row
+    // stride multiples of 4, no beta term, and not the pair kernel that
+    // splits in shared memory)
     CUtensorMap tmC;
     int tma_store;
     // single-CTA kernels, 0 or 2..8 (equal to splits, one unit per CTA): each

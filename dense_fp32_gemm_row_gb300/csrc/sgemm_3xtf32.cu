@@ -29,9 +29,14 @@
 //               +31 (rows) and 128 of the BN columns; per chunk it reads them
 //               with tcgen05.ld, hands the chunk buffer back at once, and adds
 //               the values into its 128 register accumulators; at the end of
-//               a tile it stores them to C (float4 where the row stride
-//               allows, predicated on ragged edges) while the MMAs of the next
-//               tile already run.
+//               a tile it writes them to C while the MMAs of the next tile
+//               already run: through two 2 KB shared-memory slabs and TMA
+//               stores of 32 x 16 boxes (one K split, no beta term, C rows a
+//               whole number of 16-byte units), else with its own stores
+//               (float4 where the row stride allows, predicated on ragged
+//               edges).  One thread storing a whole row puts 32 rows in each
+//               warp store; on 8192 x 8192 x 1024 that left the tensor pipe
+//               waiting ~7 us per tile, which the TMA stores remove.
 // Work units are (tile, split) pairs in a grouped raster order, strided by
 // the grid size.  Every mbarrier wait is bounded; a timeout sets the device
 // fault word and a shared abort flag, and the CTA winds down (waits, bounded,
@@ -86,6 +91,55 @@ __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t cluster_addr) {
     return v;
 }
 
+// Output slabs of the TMA-store epilogue: two per epilogue warp, each 32 rows
+// x 16 columns of C with 64-byte swizzle, after the pipeline stages.
+constexpr int EPI_SLAB_COLS = 16;
+constexpr int EPI_SLAB_BYTES = 32 * EPI_SLAB_COLS * 4;
+
+// One warp's 32 rows x EPI_COLS columns of C (lane = row y + lane, columns x0
+// ..) through its two shared-memory slabs and TMA stores.  A 16-column piece
+// goes to a slab (the 16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3),
+// the 64-byte swizzle, so the lanes' float4 writes hit distinct banks) and out
+// with one TMA store: whole lines, and the warp moves on while the store
+// drains.  Ragged edges are clipped by the tensor map's extent; pieces wholly
+// outside C are skipped, and the slabs alternate by stores issued (`stores`,
+// the warp's running count), so that the store that last read a slab is
+// always the one before the latest.
+__device__ __forceinline__ void store_rows_tma(const float (&acc)[EPI_COLS], uint32_t slabs,
+                                               int& stores, int lane, const CUtensorMap* tmC,
+                                               int x0, int y, int M, int N, float alpha,
+                                               int scale_mode) {
+    if (y >= M) return;  // the same for the whole warp
+#pragma unroll
+    for (int pc = 0; pc < EPI_COLS / EPI_SLAB_COLS; ++pc) {
+        const int x = x0 + pc * EPI_SLAB_COLS;
+        if (x >= N) continue;
+        const uint32_t slab = slabs + (stores & 1) * EPI_SLAB_BYTES;
+        ++stores;
+        // the store issued from this slab two stores ago has read it
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < EPI_SLAB_COLS / 4; ++c) {
+            const int j = pc * EPI_SLAB_COLS + 4 * c;
+            float4 v = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+            if (scale_mode == kStoreAlpha) {
+                v.x *= alpha;
+                v.y *= alpha;
+                v.z *= alpha;
+                v.w *= alpha;
+            }
+            sts128(slab + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), v);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmC, slab, x, y);
+            bulk_commit();
+        }
+    }
+}
+
 template <int BN, int STAGES>
 struct Cfg {
     static constexpr int EPI_WARPS = 4 * (BN / EPI_COLS);
@@ -96,7 +150,8 @@ struct Cfg {
     static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int NBARS = 2 * STAGES + 5;  // full, empty, acc_full x2, acc_empty x2, drain
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NBARS * 8 + 16 + 1024;
+    static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_SLAB_BYTES;  // output slabs
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + NBARS * 8 + 16 + 1024;
     static constexpr uint32_t IDESC = idesc_tf32_f32(BM, BN);
     static_assert(BN % EPI_COLS == 0 && BN <= 256, "MMA N for M = 128, whole epilogue blocks");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512 || TMEM_COLS == 128, "power-of-two TMEM");
@@ -208,19 +263,22 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
                     const __grid_constant__ CUtensorMap tmBlo, float* __restrict__ out,
                     long long ldo, long long split_stride, int M, int N, int K, int kb_per_split,
                     int splits, int vec_store, unsigned* fault, long long timeout_ns,
-                    float alpha, float beta, int scale_mode, int cluster_splits) {
+                    float alpha, float beta, int scale_mode, int cluster_splits,
+                    const __grid_constant__ CUtensorMap tmC, int tma_store) {
     using C = Cfg<BN, STAGES>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t bar0 = sbase + STAGES * C::STAGE_BYTES;
+    const uint32_t epi0 = sbase + STAGES * C::STAGE_BYTES;  // output slabs
+    const uint32_t bar0 = epi0 + C::EPI_BYTES;
     const uint32_t full0 = bar0;                      // full[s]      = full0 + 8 s
     const uint32_t empty0 = bar0 + 8 * STAGES;        // empty[s]     = empty0 + 8 s
     const uint32_t accf0 = bar0 + 16 * STAGES;        // acc_full[b]  = accf0 + 8 b
     const uint32_t acce0 = accf0 + 16;                // acc_empty[b] = acce0 + 8 b
     const uint32_t drain = acce0 + 16;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + STAGES * C::STAGE_BYTES + C::NBARS * 8);
+    uint32_t* tmem_slot =
+        reinterpret_cast<uint32_t*>(smem + STAGES * C::STAGE_BYTES + C::EPI_BYTES + C::NBARS * 8);
     const uint32_t abort_flag = smem_addr(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -235,6 +293,7 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
         prefetch_tmap(&tmAlo);
         prefetch_tmap(&tmBhi);
         prefetch_tmap(&tmBlo);
+        if (tma_store) prefetch_tmap(&tmC);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
@@ -357,6 +416,7 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
         const int row = 32 * q + lane;
         float acc[EPI_COLS];
         int g = 0;
+        int stores = 0;  // TMA stores this warp has issued
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
             const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, BN, BM,
@@ -404,6 +464,11 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
                 }
                 continue;
             }
+            if (tma_store) {
+                store_rows_tma(acc, epi0 + static_cast<uint32_t>(e) * 2 * EPI_SLAB_BYTES, stores,
+                               lane, &tmC, w.n0 + col0, w.m0 + 32 * q, M, N, alpha, scale_mode);
+                continue;
+            }
             const int m = w.m0 + row;
             if (m < M) {
                 float* orow = out + static_cast<long long>(w.split) * split_stride +
@@ -415,6 +480,9 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
                            vec_store != 0, alpha, beta, scale_mode);
             }
         }
+        // the output stores have completed (and no longer read the slabs)
+        if (tma_store && lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     if (cluster_splits) {
@@ -501,7 +569,7 @@ cudaError_t launch_impl(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
         e = cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel<BN, STAGES>, a.tmAhi, a.tmAlo, a.tmBhi,
                                a.tmBlo, a.out, a.ldo, a.split_stride, a.M, a.N, a.K,
                                a.kb_per_split, a.splits, a.vec_store, a.fault, a.timeout_ns,
-                               a.alpha, a.beta, a.scale_mode, a.cluster_splits);
+                               a.alpha, a.beta, a.scale_mode, a.cluster_splits, a.tmC, 0);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
@@ -517,7 +585,7 @@ cudaError_t launch_impl(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
     e = cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel<BN, STAGES>, a.tmAhi, a.tmAlo, a.tmBhi,
                            a.tmBlo, a.out, a.ldo, a.split_stride, a.M, a.N, a.K, a.kb_per_split,
                            a.splits, a.vec_store, a.fault, a.timeout_ns, a.alpha, a.beta,
-                           a.scale_mode, 0);
+                           a.scale_mode, 0, a.tmC, a.tma_store);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -578,11 +646,7 @@ struct PairCfg {
     static constexpr int NFULL = SPLIT_IN_KERNEL ? STAGES * NSPLIT : STAGES;
     // full (NFULL), empty, converted (per stage), acc_full x2, acc_empty x2, drain
     static constexpr int NBARS = NFULL + 2 * STAGES + 5;
-    // output slabs of the TMA-store epilogue: two per epilogue warp, each 32
-    // rows x 16 columns (64-byte swizzle), after the stages
-    static constexpr int EPI_SLAB_COLS = 16;
-    static constexpr int EPI_SLAB_BYTES = 32 * EPI_SLAB_COLS * 4;
-    static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_SLAB_BYTES;
+    static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_SLAB_BYTES;  // output slabs
     // both variants reserve room for the split variant's barriers, so that
     // they have the same shared-memory size (and occupancy)
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES +
@@ -739,7 +803,7 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
             prefetch_tmap(&tmAlo);
             prefetch_tmap(&tmBlo);
         }
-        if (tma_store) prefetch_tmap(&tmC);
+        if (!SPLIT_IN_KERNEL && tma_store) prefetch_tmap(&tmC);
         for (int f = 0; f < C::NFULL; ++f) mbar_init(full0 + 8 * f, SPLIT_IN_KERNEL ? 1 : 2);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(empty0 + 8 * s, 1);
@@ -962,46 +1026,15 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
                            0.0f, kStorePlain);
                 continue;
             }
-            if (tma_store) {
-                // Through shared memory: 16-column pieces of the warp's 32
-                // rows go to one of its two slabs (64-byte swizzle: the 16-byte
-                // chunk c of row r sits at chunk c ^ ((r >> 1) & 3), so the
-                // lanes' float4 writes hit distinct banks) and out with one
-                // TMA store each, whole lines, while the next tile's MMAs
-                // run.  Ragged edges are clipped by the tensor map's extent.
-                // Pieces wholly outside C are skipped, and the slabs alternate
-                // by stores issued (not by piece), so that the store that last
-                // read a slab is always the one before the latest.
-                const uint32_t slabs = epi0 + static_cast<uint32_t>(e) * 2 * C::EPI_SLAB_BYTES;
-                const int y = w.m0 + static_cast<int>(rank) * BM + 32 * q;
-#pragma unroll
-                for (int pc = 0; pc < EPI_COLS / C::EPI_SLAB_COLS; ++pc) {
-                    const int x = w.n0 + col0 + pc * C::EPI_SLAB_COLS;
-                    if (y >= M || x >= N) continue;  // the same for the whole warp
-                    const uint32_t slab = slabs + (stores & 1) * C::EPI_SLAB_BYTES;
-                    ++stores;
-                    // the store issued from this slab two stores ago has read it
-                    if (lane == 0) bulk_wait_read<1>();
-                    __syncwarp();
-#pragma unroll
-                    for (int c = 0; c < C::EPI_SLAB_COLS / 4; ++c) {
-                        const int j = pc * C::EPI_SLAB_COLS + 4 * c;
-                        float4 v = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-                        if (scale_mode == kStoreAlpha) {
-                            v.x *= alpha;
-                            v.y *= alpha;
-                            v.z *= alpha;
-                            v.w *= alpha;
-                        }
-                        sts128(slab + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), v);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tmC, slab, x, y);
-                        bulk_commit();
-                    }
-                }
+            // The variant that splits in shared memory keeps the per-thread
+            // stores: its splitter warps are short of registers, and with the
+            // TMA path compiled in it ran 5-10 % slower on deep K (2048 x
+            // 512 x 8192: 0.111 against 0.101 ms) though few of its tiles
+            // reach the epilogue.
+            if (!SPLIT_IN_KERNEL && tma_store) {
+                store_rows_tma(acc, epi0 + static_cast<uint32_t>(e) * 2 * EPI_SLAB_BYTES, stores,
+                               lane, &tmC, w.n0 + col0, w.m0 + static_cast<int>(rank) * BM + 32 * q,
+                               M, N, alpha, scale_mode);
                 continue;
             }
             const int m = w.m0 + static_cast<int>(rank) * BM + row;
@@ -1016,7 +1049,7 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
             }
         }
         // the output stores have completed (and no longer read the slabs)
-        if (tma_store && lane == 0) bulk_wait_all();
+        if (!SPLIT_IN_KERNEL && tma_store && lane == 0) bulk_wait_all();
         __syncwarp();
     }
 

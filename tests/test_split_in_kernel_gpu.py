@@ -226,3 +226,14 @@ def test_pair_output_boxes_alpha():
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and (p["tile_m"], p["tile_n"]) == (256, 256), p
     _ex_case(M, N, K, 0, 0, 4, 0.5, 0.0, g.ALGO_AUTO)
+
+
+def test_pair_output_ragged_row_in_padded_stride():
+    # N % 4 != 0 with a row stride that is a multiple of 4 (ldc = N + 2): the
+    # columns past N (the padding) must come back untouched, so the kernel may
+    # not store the last row piece as a whole 16-byte unit
+    from .test_gemm_gpu import _ex_case
+    M, N, K = 2100, 2102, 1024
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and (p["tile_m"], p["tile_n"]) == (256, 256), p
+    _ex_case(M, N, K, 0, 0, 2, 1.0, 0.0, g.ALGO_AUTO)
