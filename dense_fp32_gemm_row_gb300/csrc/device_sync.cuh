@@ -19,6 +19,7 @@ constexpr unsigned kFaultEmptyBarrier = 1u << 1;  // producer waited too long fo
 constexpr unsigned kFaultDrain        = 1u << 2;  // in-flight copies did not land while winding down
 constexpr unsigned kFaultAccumBarrier = 1u << 3;  // epilogue / MMA accumulator handshake
 constexpr unsigned kFaultSelfTest     = 1u << 4;  // watchdog self-test barrier
+constexpr unsigned kFaultOutputLoad   = 1u << 5;  // epilogue waited too long for a box of the old C
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

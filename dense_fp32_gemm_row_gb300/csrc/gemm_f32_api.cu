@@ -616,12 +616,12 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
         ta.tail_splits = tail ? p.tail_splits : 0;
         ta.tail_ws = tail ? reinterpret_cast<float*>(ws + p.off_t) : nullptr;
         ta.cluster_splits = p.cluster_splits;
-        // C through TMA stores: one K split, no beta term (mode 2 reads C),
-        // and not the kernel that splits in shared memory.  TMA stores clip
-        // a box at C's extent in 16-byte pieces: the row length must be a
-        // whole number of them, or a ragged last piece would be written in
-        // full, past column N.
-        if (vec_store && N % 4 == 0 && p.splits == 1 && kmode != 2 && !p.split_in_kernel) {
+        // C through TMA stores (and, with a beta term, TMA loads of the old
+        // C): one K split, and not the kernel that splits in shared memory.
+        // TMA stores clip a box at C's extent in 16-byte pieces: the row
+        // length must be a whole number of them, or a ragged last piece
+        // would be written in full, past column N.
+        if (vec_store && N % 4 == 0 && p.splits == 1 && !p.split_in_kernel) {
             if ((st = encode_2d(&ta.tmC, out, N, M, ldo, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B)) !=
                 GEMM_F32_SUCCESS)
                 return st;

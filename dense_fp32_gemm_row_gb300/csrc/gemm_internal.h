@@ -91,10 +91,10 @@ struct Tf32x3Args {
     int tail_tiles, tail_splits;
     float* tail_ws;
     // tma_store = 1: the GEMM kernel writes C through shared memory with TMA
-    // stores, tmC being C as {N, M}, box {16, 32}, 64-byte swizzle (splits
-    // == 1 without a cluster split, C 16-byte aligned with N and the row
-    // stride multiples of 4, no beta term, and not the pair kernel that
-    // splits in shared memory)
+    // stores (reading the old C with TMA loads for a beta term), tmC being C
+    // as {N, M}, box {16, 32}, 64-byte swizzle (splits == 1 without a
+    // cluster split, C 16-byte aligned with N and the row stride multiples
+    // of 4, and not the pair kernel that splits in shared memory)
     CUtensorMap tmC;
     int tma_store;
     // single-CTA kernels, 0 or 2..8 (equal to splits, one unit per CTA): each

@@ -31,8 +31,9 @@
 //               the values into its 128 register accumulators; at the end of
 //               a tile it writes them to C while the MMAs of the next tile
 //               already run: through two 2 KB shared-memory slabs and TMA
-//               stores of 32 x 16 boxes (one K split, no beta term, C rows a
-//               whole number of 16-byte units), else with its own stores
+//               stores of 32 x 16 boxes, a beta term reading the old box
+//               with a TMA load (one K split, C rows a whole number of
+//               16-byte units), else with its own loads and stores
 //               (float4 where the row stride allows, predicated on ragged
 //               edges).  One thread storing a whole row puts 32 rows in each
 //               warp store; on 8192 x 8192 x 1024 that left the tensor pipe
@@ -96,50 +97,6 @@ __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t cluster_addr) {
 constexpr int EPI_SLAB_COLS = 16;
 constexpr int EPI_SLAB_BYTES = 32 * EPI_SLAB_COLS * 4;
 
-// One warp's 32 rows x EPI_COLS columns of C (lane = row y + lane, columns x0
-// ..) through its two shared-memory slabs and TMA stores.  A 16-column piece
-// goes to a slab (the 16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3),
-// the 64-byte swizzle, so the lanes' float4 writes hit distinct banks) and out
-// with one TMA store: whole lines, and the warp moves on while the store
-// drains.  Ragged edges are clipped by the tensor map's extent; pieces wholly
-// outside C are skipped, and the slabs alternate by stores issued (`stores`,
-// the warp's running count), so that the store that last read a slab is
-// always the one before the latest.
-__device__ __forceinline__ void store_rows_tma(const float (&acc)[EPI_COLS], uint32_t slabs,
-                                               int& stores, int lane, const CUtensorMap* tmC,
-                                               int x0, int y, int M, int N, float alpha,
-                                               int scale_mode) {
-    if (y >= M) return;  // the same for the whole warp
-#pragma unroll
-    for (int pc = 0; pc < EPI_COLS / EPI_SLAB_COLS; ++pc) {
-        const int x = x0 + pc * EPI_SLAB_COLS;
-        if (x >= N) continue;
-        const uint32_t slab = slabs + (stores & 1) * EPI_SLAB_BYTES;
-        ++stores;
-        // the store issued from this slab two stores ago has read it
-        if (lane == 0) bulk_wait_read<1>();
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < EPI_SLAB_COLS / 4; ++c) {
-            const int j = pc * EPI_SLAB_COLS + 4 * c;
-            float4 v = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-            if (scale_mode == kStoreAlpha) {
-                v.x *= alpha;
-                v.y *= alpha;
-                v.z *= alpha;
-                v.w *= alpha;
-            }
-            sts128(slab + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), v);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            tma_store_2d(tmC, slab, x, y);
-            bulk_commit();
-        }
-    }
-}
-
 template <int BN, int STAGES>
 struct Cfg {
     static constexpr int EPI_WARPS = 4 * (BN / EPI_COLS);
@@ -149,7 +106,8 @@ struct Cfg {
     static constexpr int B_BYTES = BN * BK * 4;
     static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int NBARS = 2 * STAGES + 5;  // full, empty, acc_full x2, acc_empty x2, drain
+    // full, empty, acc_full x2, acc_empty x2, drain, old-C load per epilogue warp
+    static constexpr int NBARS = 2 * STAGES + 5 + EPI_WARPS;
     static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_SLAB_BYTES;  // output slabs
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + NBARS * 8 + 16 + 1024;
     static constexpr uint32_t IDESC = idesc_tf32_f32(BM, BN);
@@ -255,6 +213,87 @@ __device__ __forceinline__ float to_tf32(float x) {
     return __uint_as_float(r);
 }
 
+// One warp's 32 rows x EPI_COLS columns of C (lane = row y + lane, columns x0
+// ..) through its two shared-memory slabs and TMA stores.  A 16-column piece
+// goes to a slab (the 16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3),
+// the 64-byte swizzle, so the lanes' float4 writes hit distinct banks) and out
+// with one TMA store: whole lines, and the warp moves on while the store
+// drains.  Ragged edges are clipped by the tensor map's extent; pieces wholly
+// outside C are skipped, and the slabs alternate by stores issued (`stores`,
+// the warp's running count), so that the store that last read a slab is
+// always the one before the latest.  With a beta term the old box of C is
+// first loaded into the slab (TMA, completion on the warp's barrier `cbar`,
+// `loads` counting its phases; a bounded wait) and each lane replaces its row
+// of it by alpha v + beta C.  Returns false if that wait gave up.
+__device__ __forceinline__ bool store_rows_tma(const float (&acc)[EPI_COLS], uint32_t slabs,
+                                               int& stores, int& loads, uint32_t cbar, int lane,
+                                               const CUtensorMap* tmC, int x0, int y, int M,
+                                               int N, float alpha, float beta, int scale_mode,
+                                               long long timeout_ns, unsigned* fault,
+                                               uint32_t abort_flag) {
+    if (y >= M) return true;  // the same for the whole warp
+    const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
+#pragma unroll
+    for (int pc = 0; pc < EPI_COLS / EPI_SLAB_COLS; ++pc) {
+        const int x = x0 + pc * EPI_SLAB_COLS;
+        if (x >= N) continue;
+        const uint32_t slab = slabs + (stores & 1) * EPI_SLAB_BYTES;
+        ++stores;
+        // the store issued from this slab two stores ago has read it
+        if (lane == 0) {
+            bulk_wait_read<1>();
+            if (scale_mode == kStoreAlphaBeta) {
+                mbar_arrive_expect_tx(cbar, EPI_SLAB_BYTES);
+                tma_load_2d(slab, tmC, cbar, x, y);
+            }
+        }
+        __syncwarp();
+        if (scale_mode == kStoreAlphaBeta) {
+            const bool got = role_wait(cbar, static_cast<uint32_t>(loads & 1), timeout_ns, fault,
+                                       kFaultOutputLoad, abort_flag);
+            ++loads;
+            if (!__all_sync(0xffffffffu, got)) return false;
+        }
+#pragma unroll
+        for (int c = 0; c < EPI_SLAB_COLS / 4; ++c) {
+            const int j = pc * EPI_SLAB_COLS + 4 * c;
+            const uint32_t a = slab + lane * 64 + ((static_cast<uint32_t>(c) ^ sw) << 4);
+            float4 v = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+            if (scale_mode != kStorePlain) {
+                v.x *= alpha;
+                v.y *= alpha;
+                v.z *= alpha;
+                v.w *= alpha;
+            }
+            if (scale_mode == kStoreAlphaBeta) {
+                const float4 o = lds128(a);
+                v.x = fmaf(beta, o.x, v.x);
+                v.y = fmaf(beta, o.y, v.y);
+                v.z = fmaf(beta, o.z, v.z);
+                v.w = fmaf(beta, o.w, v.w);
+            }
+            sts128(a, v);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmC, slab, x, y);
+            bulk_commit();
+        }
+    }
+    return true;
+}
+
+// With a beta term: bring the warp's boxes of the old C into L2 when its tile
+// starts, so that the loads of store_rows_tma find them there (lane 0).
+__device__ __forceinline__ void prefetch_rows_tma(const CUtensorMap* tmC, int x0, int y, int M,
+                                                  int N) {
+    if (y >= M) return;
+#pragma unroll
+    for (int pc = 0; pc < EPI_COLS / EPI_SLAB_COLS; ++pc)
+        if (x0 + pc * EPI_SLAB_COLS < N) tma_prefetch_2d(tmC, x0 + pc * EPI_SLAB_COLS, y);
+}
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(Cfg<BN, STAGES>::THREADS, 1)
 sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
@@ -277,6 +316,7 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
     const uint32_t accf0 = bar0 + 16 * STAGES;        // acc_full[b]  = accf0 + 8 b
     const uint32_t acce0 = accf0 + 16;                // acc_empty[b] = acce0 + 8 b
     const uint32_t drain = acce0 + 16;
+    const uint32_t cload0 = drain + 8;                // old-C load of epilogue warp e: + 8 e
     uint32_t* tmem_slot =
         reinterpret_cast<uint32_t*>(smem + STAGES * C::STAGE_BYTES + C::EPI_BYTES + C::NBARS * 8);
     const uint32_t abort_flag = smem_addr(tmem_slot + 1);
@@ -303,6 +343,7 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
             mbar_init(acce0 + 8 * b, C::EPI_WARPS);
         }
         mbar_init(drain, 1);
+        for (int w = 0; w < C::EPI_WARPS; ++w) mbar_init(cload0 + 8 * w, 1);
         st_shared_volatile(abort_flag, 0u);
         fence_barrier_init();
     }
@@ -417,10 +458,13 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
         float acc[EPI_COLS];
         int g = 0;
         int stores = 0;  // TMA stores this warp has issued
+        int loads = 0;   // old-C boxes this warp has loaded
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
             const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, BN, BM,
                                   cluster_splits);
+            if (tma_store && scale_mode == kStoreAlphaBeta && lane == 0)
+                prefetch_rows_tma(&tmC, w.n0 + col0, w.m0 + 32 * q, M, N);
             for (int c0 = 0; c0 < w.nkb; c0 += CH, ++g) {
                 const int buf = g & 1;
                 const bool got = role_wait(accf0 + 8 * buf, (g >> 1) & 1, timeout_ns, fault,
@@ -465,8 +509,10 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
                 continue;
             }
             if (tma_store) {
-                store_rows_tma(acc, epi0 + static_cast<uint32_t>(e) * 2 * EPI_SLAB_BYTES, stores,
-                               lane, &tmC, w.n0 + col0, w.m0 + 32 * q, M, N, alpha, scale_mode);
+                ok = store_rows_tma(acc, epi0 + static_cast<uint32_t>(e) * 2 * EPI_SLAB_BYTES,
+                                    stores, loads, cload0 + 8 * e, lane, &tmC, w.n0 + col0,
+                                    w.m0 + 32 * q, M, N, alpha, beta, scale_mode, timeout_ns,
+                                    fault, abort_flag);
                 continue;
             }
             const int m = w.m0 + row;
@@ -645,12 +691,14 @@ struct PairCfg {
     // skip a phase, and a parity wait cannot tell phase k from phase k + 2.)
     static constexpr int NFULL = SPLIT_IN_KERNEL ? STAGES * NSPLIT : STAGES;
     // full (NFULL), empty, converted (per stage), acc_full x2, acc_empty x2, drain
-    static constexpr int NBARS = NFULL + 2 * STAGES + 5;
+    // ... and an old-C load barrier per epilogue warp
+    static constexpr int NBARS = NFULL + 2 * STAGES + 5 + EPI_WARPS;
     static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_SLAB_BYTES;  // output slabs
     // both variants reserve room for the split variant's barriers, so that
     // they have the same shared-memory size (and occupancy)
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES +
-                                      (STAGES * NSPLIT + 2 * STAGES + 5) * 8 + 16 + 1024;
+                                      (STAGES * NSPLIT + 2 * STAGES + 5 + EPI_WARPS) * 8 + 16 +
+                                      1024;
     static constexpr uint32_t IDESC = idesc_tf32_f32(2 * BM, BN);
     static_assert(A_BYTES == B_BYTES && B_BYTES == 16384,
                   "the splitter's thread-to-element maps below");
@@ -781,6 +829,7 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
     const uint32_t accf0 = conv0 + 8 * STAGES;     // acc_full[b]: both CTAs, one multicast commit
     const uint32_t acce0 = accf0 + 16;            // acc_empty[b]: leader, both epilogues
     const uint32_t drain = acce0 + 16;
+    const uint32_t cload0 = drain + 8;             // old-C load of epilogue warp e: + 8 e
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + STAGES * C::STAGE_BYTES +
                                                       C::EPI_BYTES + C::NBARS * 8);
     const uint32_t abort_flag = smem_addr(tmem_slot + 1);
@@ -814,6 +863,7 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
             mbar_init(acce0 + 8 * b, 2 * C::EPI_WARPS);
         }
         mbar_init(drain, 1);
+        for (int w = 0; w < C::EPI_WARPS; ++w) mbar_init(cload0 + 8 * w, 1);
         st_shared_volatile(abort_flag, 0u);
         fence_barrier_init();
     }
@@ -983,9 +1033,14 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
         float acc[EPI_COLS];
         int g = 0;
         int stores = 0;  // TMA stores this warp has issued
+        int loads = 0;   // old-C boxes this warp has loaded
         bool ok = true;
         for (int u = cluster; u < units && ok; u += nclusters) {
             const Unit w = decode_pair(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, tail_tiles, tail_splits);
+            if (!SPLIT_IN_KERNEL && tma_store && scale_mode == kStoreAlphaBeta && w.slot < 0 &&
+                lane == 0)
+                prefetch_rows_tma(&tmC, w.n0 + col0, w.m0 + static_cast<int>(rank) * BM + 32 * q, M,
+                                  N);
             for (int c0 = 0; c0 < w.nkb; c0 += CH, ++g) {
                 const int buf = g & 1;
                 const bool got = role_wait(accf0 + 8 * buf, (g >> 1) & 1, timeout_ns, fault,
@@ -1032,9 +1087,10 @@ sgemm_3xtf32_pair_kernel(const __grid_constant__ CUtensorMap tmAhi,
             // 512 x 8192: 0.111 against 0.101 ms) though few of its tiles
             // reach the epilogue.
             if (!SPLIT_IN_KERNEL && tma_store) {
-                store_rows_tma(acc, epi0 + static_cast<uint32_t>(e) * 2 * EPI_SLAB_BYTES, stores,
-                               lane, &tmC, w.n0 + col0, w.m0 + static_cast<int>(rank) * BM + 32 * q,
-                               M, N, alpha, scale_mode);
+                ok = store_rows_tma(acc, epi0 + static_cast<uint32_t>(e) * 2 * EPI_SLAB_BYTES,
+                                    stores, loads, cload0 + 8 * e, lane, &tmC, w.n0 + col0,
+                                    w.m0 + static_cast<int>(rank) * BM + 32 * q, M, N, alpha,
+                                    beta, scale_mode, timeout_ns, fault, abort_flag);
                 continue;
             }
             const int m = w.m0 + static_cast<int>(rank) * BM + row;

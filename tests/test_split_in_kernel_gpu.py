@@ -228,6 +228,20 @@ def test_pair_output_boxes_alpha():
     _ex_case(M, N, K, 0, 0, 4, 0.5, 0.0, g.ALGO_AUTO)
 
 
+@pytest.mark.parametrize("shape,algo", [((2100, 2100, 1024), g.ALGO_AUTO),
+                                        ((300, 200, 40), g.ALGO_3XTF32),
+                                        ((520, 100, 2000), g.ALGO_3XTF32)],
+                         ids=["pair", "single-128", "single-ragged-m"])
+def test_output_boxes_with_beta(shape, algo):
+    # alpha and beta: the kernels load each 32 x 16 box of the old C into
+    # their shared-memory slab (TMA, clipped boxes zero-filled outside C),
+    # replace it by alpha v + beta C and store it back
+    from .test_gemm_gpu import _ex_case
+    M, N, K = shape
+    _ex_case(M, N, K, 0, 0, 4, 0.5, -0.75, algo)
+    _ex_case(M, N, K, 0, 0, 0, 1.0, 1.0, algo)
+
+
 def test_pair_output_ragged_row_in_padded_stride():
     # N % 4 != 0 with a row stride that is a multiple of 4 (ldc = N + 2): the
     # columns past N (the padding) must come back untouched, so the kernel may
