@@ -26,7 +26,7 @@ import threading
 __all__ = [
     "ALGO_AUTO", "ALGO_FFMA", "ALGO_3XTF32", "ALGOS", "MAX_SPLITS",
     "SUCCESS", "ERR_INVALID_VALUE", "ERR_UNSUPPORTED_DEVICE", "ERR_WORKSPACE",
-    "ERR_DEVICE_TIMEOUT", "ERR_DESCRIPTOR", "GemmError",
+    "ERR_DEVICE_TIMEOUT", "ERR_DESCRIPTOR", "ERR_CAPTURE", "GemmError",
     "library_path", "load", "gemm_f32", "gemm_f32_algo", "gemm_f32_algo_splitk",
     "gemm_f32_algo_splitk_ev", "gemm_f32_noalloc", "gemm_f32_host", "gemm_f32_ex",
     "gemm_f32_configured", "gemm_f32_plan_config", "Config", "TILE_AUTO", "TILE_128x128",
@@ -47,6 +47,7 @@ ERR_UNSUPPORTED_DEVICE = -2
 ERR_WORKSPACE = -3
 ERR_DEVICE_TIMEOUT = -4
 ERR_DESCRIPTOR = -5
+ERR_CAPTURE = -6
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libgemmf32.so")

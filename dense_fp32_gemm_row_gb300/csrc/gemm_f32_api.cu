@@ -57,7 +57,20 @@ bool overlaps(const void* a, size_t abytes, const void* b, size_t bbytes) {
 }
 
 // Device lookup; g_mutex must be held.
-int device_state(DeviceState** out, int* dev_out) {
+// True if `stream` is being captured into a CUDA graph (or cannot be asked).
+bool stream_capturing(cudaStream_t stream) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return true;
+    }
+    return cs != cudaStreamCaptureStatusNone;
+}
+
+// The device's state, set up on first use.  `capture_stream`: the stream of
+// the call, which must not be capturing a graph while the set-up (allocation
+// and zeroing of the fault word) runs.
+int device_state(DeviceState** out, int* dev_out, const cudaStream_t* capture_stream = nullptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
@@ -66,6 +79,7 @@ int device_state(DeviceState** out, int* dev_out) {
     if (dev < 0 || dev >= kMaxDevices) return GEMM_F32_ERR_UNSUPPORTED_DEVICE;
     DeviceState& d = g_dev[dev];
     if (!d.ready) {
+        if (capture_stream && stream_capturing(*capture_stream)) return GEMM_F32_ERR_CAPTURE;
         if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) !=
                 cudaSuccess ||
             cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) !=
@@ -118,6 +132,8 @@ int encode_2d(CUtensorMap* map, const float* base, long long dim0, long long dim
 int workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
     Workspace& w = g_ws[std::make_pair(dev, stream)];
     if (w.bytes < bytes) {
+        // growing synchronises the stream and allocates: not while capturing
+        if (stream_capturing(stream)) return GEMM_F32_ERR_CAPTURE;
         if (w.ptr) {
             // earlier calls on this stream may still read the old buffer
             cudaError_t e = cudaStreamSynchronize(stream);
@@ -725,7 +741,7 @@ int run(const Problem& q, int algo, int splits, cudaStream_t stream,
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState* d = nullptr;
     int dev = 0;
-    st = device_state(&d, &dev);
+    st = device_state(&d, &dev, &stream);
     if (st != GEMM_F32_SUCCESS) return st;
     return enqueue(q, algo, splits, d, dev, stream, ev_begin, ev_end, tile);
 }
@@ -749,6 +765,8 @@ std::map<std::pair<int, cudaStream_t>, HostPipe> g_pipes;
 int host_pipe(int dev, cudaStream_t stream, size_t bytes, HostPipe** out) {
     HostPipe& hp = g_pipes[std::make_pair(dev, stream)];
     cudaError_t e = cudaSuccess;
+    if ((!hp.ready || hp.dev_bytes < bytes) && stream_capturing(stream))
+        return GEMM_F32_ERR_CAPTURE;
     if (!hp.ready) {
         const unsigned fl = cudaEventDisableTiming;
         if ((e = cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking)) != cudaSuccess ||
@@ -855,7 +873,7 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState* d = nullptr;
     int dev = 0;
-    if ((st = device_state(&d, &dev)) != GEMM_F32_SUCCESS) return st;
+    if ((st = device_state(&d, &dev, &stream)) != GEMM_F32_SUCCESS) return st;
     if ((st = get_encoder()) != GEMM_F32_SUCCESS) return st;
 
     // Row panels need all of B before the first GEMM: with B arriving at
@@ -1257,6 +1275,8 @@ const char* gemm_f32_status_string(int status) {
         case GEMM_F32_ERR_WORKSPACE: return "workspace allocation failed";
         case GEMM_F32_ERR_DEVICE_TIMEOUT: return "device barrier wait timed out";
         case GEMM_F32_ERR_DESCRIPTOR: return "tensor map encoding failed";
+        case GEMM_F32_ERR_CAPTURE:
+            return "set-up or allocation needed while the stream is captured (call once before capturing)";
         default: break;
     }
     if (status > 0) return cudaGetErrorString(static_cast<cudaError_t>(status));

@@ -34,6 +34,15 @@
  * synchronises that stream first.  gemm_f32_release() frees all of it.
  * The entry points are thread-safe.
  *
+ * CUDA graphs: the calls that take a stream can be captured from it
+ * (cudaStreamBeginCapture) and replayed; the graph keeps the pointers,
+ * shapes and plan of the capture and reads what the buffers hold at replay.
+ * The first call on a device sets it up, and a call may have to grow the
+ * stream's workspace (or the host entry's device copies); neither is allowed
+ * during a capture, so such a call returns GEMM_F32_ERR_CAPTURE without
+ * enqueuing anything.  Issue each captured call once on the same stream
+ * before capturing it.
+ *
  * Errors: 0 is success.  Negative values are library errors (GEMM_F32_ERR_*),
  * positive values are the cudaError_t of the failing CUDA runtime call.  No
  * entry point exits or aborts the process.  Nothing runs on the host CPU:
@@ -61,6 +70,11 @@ extern "C" {
 #define GEMM_F32_ERR_DEVICE_TIMEOUT     (-4)
 /* the driver rejected a tensor-memory-access descriptor */
 #define GEMM_F32_ERR_DESCRIPTOR         (-5)
+/* the stream is being captured into a CUDA graph and the call would first
+ * have to set up this device or allocate device memory (a larger workspace,
+ * the host entry's device copies), which capture does not allow: issue the
+ * same call once on the stream before capturing it.  Nothing was enqueued. */
+#define GEMM_F32_ERR_CAPTURE            (-6)
 
 /* ---- algorithms -------------------------------------------------------- */
 /* Choose by shape: the tensor-core 3xTF32 kernels, except the CUDA-core

@@ -54,6 +54,7 @@ def test_status_strings_and_version(lib):
     assert g.gemm_f32_status_string(0) == "success"
     assert "invalid" in g.gemm_f32_status_string(g.ERR_INVALID_VALUE)
     assert "timed out" in g.gemm_f32_status_string(g.ERR_DEVICE_TIMEOUT)
+    assert "captured" in g.gemm_f32_status_string(g.ERR_CAPTURE)
     assert g.gemm_f32_status_string(-99) == "unknown status"
     assert g.gemm_f32_version() >= 100
 
