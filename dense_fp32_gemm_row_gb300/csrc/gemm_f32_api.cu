@@ -1260,6 +1260,10 @@ int gemm_f32_release(void) {
                 cudaEventDestroy(hp.ev_a[i]);
                 cudaEventDestroy(hp.ev_c[i]);
             }
+            for (int i = 0; i < kMaxColBlocks; ++i) {
+                cudaEventDestroy(hp.ev_bblk[i]);
+                cudaEventDestroy(hp.ev_cblk[i]);
+            }
         }
     }
     g_pipes.clear();
