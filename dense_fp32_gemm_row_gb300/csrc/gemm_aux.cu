@@ -4,7 +4,10 @@
 //                    stride is a multiple of 16 bytes and whose base is
 //                    256-byte aligned, the form a TMA descriptor requires.
 //  * splitk_reduce:  C = sum of the split-K partial products, added in split
-//                    order 0, 1, ..., S-1 so that the result is deterministic.
+//                    order 0, 1, ..., S-1 so that the result is deterministic;
+//                    the partials are loaded several at a time (independent
+//                    loads in flight), and few outputs with many partials
+//                    get one thread per output over a flat grid.
 //  * fill_zero:      C = 0 for K == 0 (the empty sum of the lecture-12
 //                    golden reference); scale_c: C = beta C for K == 0.
 //  * transpose_pad:  a transposed copy, for operands stored the other way
@@ -12,7 +15,8 @@
 //  * watchdog:       a self-test that waits on a barrier nothing completes.
 //
 // All are grid-stride loops with coalesced accesses along rows; they are
-// bounded by HBM (or L2) bandwidth, never by arithmetic.
+// bounded by HBM (or L2) bandwidth or, for a reduction of few outputs, by the
+// latency of each thread's loads, never by arithmetic.
 #include <cstdint>
 
 #include "device_sync.cuh"
@@ -57,6 +61,9 @@ splitk_reduce_kernel(const float* __restrict__ ws, long long split_stride, long 
 }
 
 // Vector form: ldw, ldc, N multiples of 4 and both bases 16-byte aligned.
+// The partials are loaded kVecBatch at a time (independent loads in flight)
+// and added in split order, as above.
+constexpr int kVecBatch = 4;
 __global__ void __launch_bounds__(kThreads)
 splitk_reduce4_kernel(const float4* __restrict__ ws, long long split_stride4, long long ldw4,
                       int splits, float* __restrict__ C, long long ldc, int M, int N4, float alpha,
@@ -68,15 +75,54 @@ splitk_reduce4_kernel(const float4* __restrict__ ws, long long split_stride4, lo
         for (long long j = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; j < N4;
              j += static_cast<long long>(gridDim.x) * kThreads) {
             float4 sum = w[j];
-            for (int s = 1; s < splits; ++s) {
-                const float4 v = w[s * split_stride4 + j];
-                sum.x += v.x;
-                sum.y += v.y;
-                sum.z += v.z;
-                sum.w += v.w;
+            for (int s0 = 1; s0 < splits; s0 += kVecBatch) {
+                float4 v[kVecBatch];
+#pragma unroll
+                for (int b = 0; b < kVecBatch; ++b)
+                    if (s0 + b < splits) v[b] = w[(s0 + b) * split_stride4 + j];
+#pragma unroll
+                for (int b = 0; b < kVecBatch; ++b) {
+                    if (s0 + b < splits) {
+                        sum.x += v[b].x;
+                        sum.y += v[b].y;
+                        sum.z += v[b].z;
+                        sum.w += v[b].w;
+                    }
+                }
             }
             store4(c, static_cast<int>(4 * j), 4 * N4, sum, true, alpha, beta, mode);
         }
+    }
+}
+
+// Few outputs, many partials (256 x 256 x 65536: 65536 outputs, 76 partials
+// each): one output per thread over a flat index, so that every SM takes
+// part, with kDeepBatch partials loaded at once; each thread's chain of
+// round trips to L2 is what bounds the kernel.  Same split order.
+constexpr int kDeepBatch = 40;
+__global__ void __launch_bounds__(kThreads)
+splitk_reduce_deep_kernel(const float* __restrict__ ws, long long split_stride, long long ldw,
+                          int splits, float* __restrict__ C, long long ldc, int M, int N,
+                          float alpha, float beta, int mode) {
+    pdl_wait();  // the partials of the GEMM kernel before it
+    const long long total = static_cast<long long>(M) * N;
+    for (long long idx = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * kThreads) {
+        const long long r = idx / N;
+        const long long j = idx - r * N;
+        const float* w = ws + r * ldw + j;
+        float sum = w[0];
+        for (int s0 = 1; s0 < splits; s0 += kDeepBatch) {
+            float v[kDeepBatch];
+#pragma unroll
+            for (int b = 0; b < kDeepBatch; ++b)
+                if (s0 + b < splits) v[b] = w[static_cast<long long>(s0 + b) * split_stride];
+#pragma unroll
+            for (int b = 0; b < kDeepBatch; ++b)
+                if (s0 + b < splits) sum += v[b];
+        }
+        float* c = C + r * ldc + j;
+        *c = scale1(sum, c, alpha, beta, mode);
     }
 }
 
@@ -166,7 +212,14 @@ cudaError_t launch_splitk_reduce(const float* ws, long long split_stride, long l
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e;
-    if (vec) {
+    if (splits >= 8 && static_cast<long long>(M) * N <= (1LL << 20)) {
+        // latency-bound: a flat grid of one output per thread
+        const long long total = static_cast<long long>(M) * N;
+        const long long blocks = (total + kThreads - 1) / kThreads;
+        cfg.gridDim = dim3(static_cast<unsigned>(blocks < 65535 ? blocks : 65535));
+        e = cudaLaunchKernelEx(&cfg, splitk_reduce_deep_kernel, ws, split_stride, ldw, splits, C,
+                               ldc, M, N, alpha, beta, scale_mode);
+    } else if (vec) {
         cfg.gridDim = dim3(grid_1d(N / 4, kThreads, 64), gy);
         e = cudaLaunchKernelEx(&cfg, splitk_reduce4_kernel, reinterpret_cast<const float4*>(ws),
                                split_stride / 4, ldw / 4, splits, C, ldc, M, N / 4, alpha, beta,
