@@ -326,6 +326,9 @@ def test_general_form_alpha_beta_rules(algo):
     _ex_case(200, 160, 96, 1, 1, 0, 0.0, 0.5, algo)                # alpha 0: C = beta C
     _ex_case(200, 160, 0, 0, 0, 4, 1.0, 3.0, algo)                 # K 0: C = beta C
     _ex_case(160, 200, 8209, 0, 1, 1, 0.25, 1.0, algo, splits=3)   # split-K applies alpha, beta
+    # 12 partials of few outputs: the flat one-output-per-thread reduction,
+    # on a row stride of N + 3 (no vector stores) with alpha and beta
+    _ex_case(150, 130, 12000, 0, 0, 3, 0.5, -0.75, algo, splits=12)
 
 
 @pytest.mark.parametrize("M,N,K,pad", [(130, 1022, 65, 2), (257, 1020, 130, 0), (64, 65, 63, 3),
