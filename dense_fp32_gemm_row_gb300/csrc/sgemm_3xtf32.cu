@@ -249,10 +249,17 @@ __device__ __forceinline__ bool store_rows_tma(const float (&acc)[EPI_COLS], uin
         }
         __syncwarp();
         if (scale_mode == kStoreAlphaBeta) {
-            const bool got = role_wait(cbar, static_cast<uint32_t>(loads & 1), timeout_ns, fault,
-                                       kFaultOutputLoad, abort_flag);
+            const uint32_t parity = static_cast<uint32_t>(loads & 1);
+            const bool got =
+                role_wait(cbar, parity, timeout_ns, fault, kFaultOutputLoad, abort_flag);
             ++loads;
-            if (!__all_sync(0xffffffffu, got)) return false;
+            if (!__all_sync(0xffffffffu, got)) {
+                // giving up (another role aborted, or this wait timed out):
+                // the load may still be landing in the slab, so wait for it,
+                // bounded, before the CTA can leave
+                mbar_wait(cbar, parity, timeout_ns / 8 + 1000, fault, kFaultDrain);
+                return false;
+            }
         }
 #pragma unroll
         for (int c = 0; c < EPI_SLAB_COLS / 4; ++c) {
