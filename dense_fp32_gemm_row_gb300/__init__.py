@@ -30,7 +30,7 @@ __all__ = [
     "library_path", "load", "gemm_f32", "gemm_f32_algo", "gemm_f32_algo_splitk",
     "gemm_f32_algo_splitk_ev", "gemm_f32_noalloc", "gemm_f32_host", "gemm_f32_ex",
     "gemm_f32_configured", "gemm_f32_plan_config", "Config", "TILE_AUTO", "TILE_128x128",
-    "TILE_128x256", "TILE_256x256_PAIR", "TILE_256x256_PAIR_SPLIT",
+    "TILE_128x256", "TILE_256x256_PAIR", "TILE_256x256_PAIR_SPLIT", "TILE_128x128_SPLIT",
     "gemm_f32_plan", "gemm_f32_device_status", "gemm_f32_selftest_watchdog",
     "gemm_f32_release", "gemm_f32_status_string", "gemm_f32_version", "matmul", "check",
 ]
@@ -68,6 +68,7 @@ TILE_128x128 = 1
 TILE_128x256 = 2
 TILE_256x256_PAIR = 3
 TILE_256x256_PAIR_SPLIT = 4
+TILE_128x128_SPLIT = 5
 
 
 class Config(ctypes.Structure):

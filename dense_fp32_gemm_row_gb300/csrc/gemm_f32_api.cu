@@ -380,10 +380,33 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
             p->split_in_kernel = 1;
             p->bn = 256;
         }
+        // The single-CTA 128 x 128 kernel that splits in shared memory: its
+        // main loop is bound by the splitter warps (a 128 x 128 tile has half
+        // the pair tile's tensor work per stage split), so it only wins where
+        // the staging pass is large beside the GEMM and A and B can be read
+        // as stored: more than 75 MB of staging traffic (8 bytes per element
+        // of A, 12 per element of B) and fewer than 400 flops per operand
+        // element.  Against the staged 128 x 128 kernel: 89 x 1216 x 24336
+        // 74 against 120 us, 128 x 2048 x 32768 136 against 242, 384^2 x
+        // 32768 89 against 105, 160 x 640 x 24000 76 against 91, 384^2 x
+        // 20000 62 against 71, 200^2 x 20000 43.7 against 45.7; 300 x 296 x
+        // 12000 (71 MB) 47.7 against 44.7 stays staged, as do 512^3 (19.1
+        // against 18.1 us), 1025 x 1023 x 1000 (35.5 against 27.3 us) and
+        // 386 x 358 x 15342 (124 against 71 us), whose row strides need
+        // padded copies anyway.
+        const double staging_bytes = 8.0 * M * K + 12.0 * static_cast<double>(K) * N;
+        const bool in_place = !q.ta && !q.tb && q.lda % 4 == 0 && q.ldb % 4 == 0 &&
+                              !misaligned16(q.A) && !misaligned16(q.B);
+        if (!p->pair && in_place && staging_bytes > 75e6 && per_element < 400.0) {
+            p->split_in_kernel = 1;
+            p->bn = 128;
+        }
         if (tile != GEMM_F32_TILE_AUTO) {
             p->pair = tile == GEMM_F32_TILE_256x256_PAIR || tile == GEMM_F32_TILE_256x256_PAIR_SPLIT;
-            p->split_in_kernel = tile == GEMM_F32_TILE_256x256_PAIR_SPLIT;
-            p->bn = tile == GEMM_F32_TILE_128x128 ? 128 : 256;
+            p->split_in_kernel =
+                tile == GEMM_F32_TILE_256x256_PAIR_SPLIT || tile == GEMM_F32_TILE_128x128_SPLIT;
+            p->bn = (tile == GEMM_F32_TILE_128x128 || tile == GEMM_F32_TILE_128x128_SPLIT) ? 128
+                                                                                          : 256;
         }
         const Tf32x3Config tc = tf32x3_config(p->bn, p->pair != 0);
         bm = tc.bm;
@@ -633,11 +656,12 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
         ta.tail_ws = tail ? reinterpret_cast<float*>(ws + p.off_t) : nullptr;
         ta.cluster_splits = p.cluster_splits;
         // C through TMA stores (and, with a beta term, TMA loads of the old
-        // C): one K split, and not the kernel that splits in shared memory.
+        // C): one K split, and not the pair kernel that splits in shared
+        // memory.
         // TMA stores clip a box at C's extent in 16-byte pieces: the row
         // length must be a whole number of them, or a ragged last piece
         // would be written in full, past column N.
-        if (vec_store && N % 4 == 0 && p.splits == 1 && !p.split_in_kernel) {
+        if (vec_store && N % 4 == 0 && p.splits == 1 && !(p.split_in_kernel && p.pair)) {
             if ((st = encode_2d(&ta.tmC, out, N, M, ldo, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B)) !=
                 GEMM_F32_SUCCESS)
                 return st;
@@ -1082,9 +1106,10 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
 // A forced configuration: tile id within range and valid for the algorithm.
 int check_config(const gemm_f32_config* cfg) {
     if (!cfg) return GEMM_F32_ERR_INVALID_VALUE;
-    if (cfg->tile < GEMM_F32_TILE_AUTO || cfg->tile > GEMM_F32_TILE_256x256_PAIR_SPLIT)
+    if (cfg->tile < GEMM_F32_TILE_AUTO || cfg->tile > GEMM_F32_TILE_128x128_SPLIT)
         return GEMM_F32_ERR_INVALID_VALUE;
-    if ((cfg->tile == GEMM_F32_TILE_256x256_PAIR || cfg->tile == GEMM_F32_TILE_256x256_PAIR_SPLIT) &&
+    if ((cfg->tile == GEMM_F32_TILE_256x256_PAIR || cfg->tile == GEMM_F32_TILE_256x256_PAIR_SPLIT ||
+         cfg->tile == GEMM_F32_TILE_128x128_SPLIT) &&
         cfg->algo == GEMM_F32_ALGO_FFMA)
         return GEMM_F32_ERR_INVALID_VALUE;
     if (cfg->tile != GEMM_F32_TILE_AUTO && cfg->algo == GEMM_F32_ALGO_AUTO)

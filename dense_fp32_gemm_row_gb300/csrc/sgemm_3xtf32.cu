@@ -23,8 +23,9 @@
 //   warp 1      allocates 2*BN tensor-memory columns (two chunk accumulators),
 //               and one lane issues the MMAs (128 x BN x 8 each) and the
 //               commits that release a stage / publish a chunk;
-//   warps 2-3   idle (the epilogue starts on a warpgroup boundary, as the
-//               tensor-memory lane quarters follow the warp index modulo 4);
+//   warps 2-3   idle, or the splitters below (the epilogue starts on a
+//               warpgroup boundary, as the tensor-memory lane quarters
+//               follow the warp index modulo 4);
 //   warps 4..   the epilogue: warp e owns tensor-memory lanes 32*(e % 4) ..
 //               +31 (rows) and 128 of the BN columns; per chunk it reads them
 //               with tcgen05.ld, hands the chunk buffer back at once, and adds
@@ -42,6 +43,12 @@
 // the grid size.  Every mbarrier wait is bounded; a timeout sets the device
 // fault word and a shared abort flag, and the CTA winds down (waits, bounded,
 // for its in-flight copies and MMAs, then frees its tensor memory).
+//
+// SPLIT_IN_KERNEL (128 x 128 tiles only): A and B arrive as stored, a 128 x
+// 32 box of A and four 32 x 32 boxes of B per stage, and warps 2-3 split
+// them in shared memory exactly as in the pair kernel further down (whose
+// header describes the split); the MMA lane then waits on the stage's
+// converted barrier instead of its full barrier.
 //
 // Split K without a workspace (cluster_splits = S, 2..8): the grid is one
 // unit per CTA and the S K splits of a tile are the S CTAs of one cluster.
@@ -106,8 +113,13 @@ struct Cfg {
     static constexpr int B_BYTES = BN * BK * 4;
     static constexpr int STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
-    // full, empty, acc_full x2, acc_empty x2, drain, old-C load per epilogue warp
-    static constexpr int NBARS = 2 * STAGES + 5 + EPI_WARPS;
+    // Barriers: full (one per stage; in the variant that splits A and B in
+    // shared memory one per stage fill mod 2 STAGES, each waited on by one
+    // of the two splitter warps), empty, converted (that variant), acc_full
+    // x2, acc_empty x2, drain, old-C load per epilogue warp.  Both variants
+    // reserve the larger set: one shared-memory size, one occupancy.
+    static constexpr int NSPLIT = 2;
+    static constexpr int NBARS = STAGES * NSPLIT + 2 * STAGES + 5 + EPI_WARPS;
     static constexpr int EPI_BYTES = EPI_WARPS * 2 * EPI_SLAB_BYTES;  // output slabs
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + NBARS * 8 + 16 + 1024;
     static constexpr uint32_t IDESC = idesc_tf32_f32(BM, BN);
@@ -301,7 +313,104 @@ __device__ __forceinline__ void prefetch_rows_tma(const CUtensorMap* tmC, int x0
         if (x0 + pc * EPI_SLAB_COLS < N) tma_prefetch_2d(tmC, x0 + pc * EPI_SLAB_COLS, y);
 }
 
-template <int BN, int STAGES>
+__device__ __forceinline__ float4 tf32x4(float4 x) {
+    return make_float4(to_tf32(x.x), to_tf32(x.y), to_tf32(x.z), to_tf32(x.w));
+}
+
+__device__ __forceinline__ float4 sub4(float4 a, float4 b) {
+    return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w);
+}
+
+// x with the low 13 mantissa bits of each lane cleared: the TF32 value the
+// tensor core reads from the fp32 word x (it truncates; measured on this
+// part for ties and near-ties of both parities and signs).
+__device__ __forceinline__ float4 trunc4(float4 x) {
+    return make_float4(__uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u),
+                       __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u),
+                       __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u),
+                       __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u));
+}
+
+// The low part of the TF32 split of four values, lo = tf32(x - trunc(x));
+// the high part is the word x itself (the split of tf32_split.cu).
+__device__ __forceinline__ float4 lo4(float4 x) { return tf32x4(sub4(x, trunc4(x))); }
+
+__device__ __forceinline__ float lane_of(float4 v, int e) {
+    return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+
+// Rotate the four lanes of v left by r (0..3): result.x = v[r], .y = v[r + 1], ...
+__device__ __forceinline__ float4 rotate4(float4 v, int r) {
+    const float4 a = (r & 1) ? make_float4(v.y, v.z, v.w, v.x) : v;
+    return (r & 2) ? make_float4(a.z, a.w, a.x, a.y) : a;
+}
+
+// A slot (16 KB at sa, K-major, 128-byte swizzled as the TMA wrote it): each
+// value x stays where it is as its own high part, and lo = tf32(x -
+// trunc(x)) goes 16 KB further on.  The map is elementwise, so the layout
+// carries over.  Call t takes 16-byte words t, t + 64, ... (t = 0..63: two
+// calls by the 32 lanes of one warp, t = lane and lane + 32; conflict-free).
+__device__ __forceinline__ void split_a_stage(uint32_t sa, int t) {
+#pragma unroll 1
+    for (int i0 = 0; i0 < 16; i0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = lds128(sa + 16 * t + 1024 * (i0 + j));
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            sts128(sa + 16 * t + 1024 * (i0 + j) + 16384, lo4(v[j]));
+    }
+}
+
+// B slot (16 KB at sb): on entry four TMA boxes of 32 k-rows x 32 columns
+// (128-byte rows, box j holding columns 32 j .. 32 j + 31; 16-byte chunk c
+// of row k sits at chunk c ^ (k & 7)).  On exit the K-major hi plane in its
+// place (row n = 128 bytes of k = 0..31, chunk q at q ^ (n & 7): the layout
+// TMA gives a box of the transposed copy) and the lo plane 16 KB further on.
+// Call w (0, 1) does boxes 2w and 2w + 1, i.e. bytes [8192 w, 8192 w +
+// 8192) of both layouts, so the in-place transpose of one call needs only
+// its own warp; one warp makes both calls for a stage.
+// Lane l takes the 4 x 4 blocks (n = 32 j + 4 c .. + 3, k = 4 kq .. + 3)
+// with c = l % 8, kq = l / 8 and l / 8 + 4, j = 2w, 2w + 1: it loads all of
+// them (eight lanes read one 128-byte row: conflict-free), the warp syncs,
+// then it stores each n's four k values as one 16-byte word.  The store
+// order over a block's four n is rotated by c / 2 so that the eight lanes
+// of a quarter-warp write eight different n % 8, i.e. eight different
+// 16-byte bank groups.
+__device__ __forceinline__ void split_b_stage(uint32_t sb, int w, int lane) {
+    const int c = lane & 7;
+    const int rot = (c >> 1) & 3;
+    float4 v[2][2][4];  // [box j - 2w][kq half][k - 4 kq], lanes over n - 32 j - 4 c
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const int k = 4 * ((lane >> 3) + 4 * h) + kk;
+                v[jj][h][kk] = rotate4(
+                    lds128(sb + (2 * w + jj) * 4096 + k * 128 + ((c ^ (k & 7)) << 4)), rot);
+            }
+    __syncwarp();  // every raw word of this warp's half is in registers
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int kq = (lane >> 3) + 4 * h;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int n = 32 * (2 * w + jj) + 4 * c + ((e + rot) & 3);
+                // lane e of the rotated words is column n; k = 4 kq + 0..3
+                const float4 x = make_float4(lane_of(v[jj][h][0], e), lane_of(v[jj][h][1], e),
+                                             lane_of(v[jj][h][2], e), lane_of(v[jj][h][3], e));
+                const uint32_t a = sb + n * 128 + ((kq ^ (n & 7)) << 4);
+                sts128(a, x);
+                sts128(a + 16384, lo4(x));
+            }
+        }
+}
+
+template <int BN, int STAGES, bool SPLIT_IN_KERNEL = false>
 __global__ void __launch_bounds__(Cfg<BN, STAGES>::THREADS, 1)
 sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
                     const __grid_constant__ CUtensorMap tmAlo,
@@ -312,16 +421,20 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
                     float alpha, float beta, int scale_mode, int cluster_splits,
                     const __grid_constant__ CUtensorMap tmC, int tma_store) {
     using C = Cfg<BN, STAGES>;
+    static_assert(!SPLIT_IN_KERNEL || BN == 128, "the splitter's maps: 128 x 32 A and B slots");
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_addr(smem);
     const uint32_t epi0 = sbase + STAGES * C::STAGE_BYTES;  // output slabs
     const uint32_t bar0 = epi0 + C::EPI_BYTES;
-    const uint32_t full0 = bar0;                      // full[s]      = full0 + 8 s
-    const uint32_t empty0 = bar0 + 8 * STAGES;        // empty[s]     = empty0 + 8 s
-    const uint32_t accf0 = bar0 + 16 * STAGES;        // acc_full[b]  = accf0 + 8 b
-    const uint32_t acce0 = accf0 + 16;                // acc_empty[b] = acce0 + 8 b
+    // full[f]: f = stage, or (split in kernel) f = stage fill mod NFULL
+    constexpr int NFULL = SPLIT_IN_KERNEL ? STAGES * C::NSPLIT : STAGES;
+    const uint32_t full0 = bar0;
+    const uint32_t empty0 = full0 + 8 * STAGES * C::NSPLIT;  // empty[s]     = empty0 + 8 s
+    const uint32_t conv0 = empty0 + 8 * STAGES;              // converted[s] = conv0 + 8 s
+    const uint32_t accf0 = conv0 + 8 * STAGES;               // acc_full[b]  = accf0 + 8 b
+    const uint32_t acce0 = accf0 + 16;                       // acc_empty[b] = acce0 + 8 b
     const uint32_t drain = acce0 + 16;
     const uint32_t cload0 = drain + 8;                // old-C load of epilogue warp e: + 8 e
     uint32_t* tmem_slot =
@@ -337,13 +450,16 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
 
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmAhi);
-        prefetch_tmap(&tmAlo);
         prefetch_tmap(&tmBhi);
-        prefetch_tmap(&tmBlo);
+        if (!SPLIT_IN_KERNEL) {
+            prefetch_tmap(&tmAlo);
+            prefetch_tmap(&tmBlo);
+        }
         if (tma_store) prefetch_tmap(&tmC);
+        for (int f = 0; f < NFULL; ++f) mbar_init(full0 + 8 * f, 1);
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
+            mbar_init(conv0 + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf0 + 8 * b, 1);
@@ -384,13 +500,33 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
                         break;
                     }
                     const uint32_t st = sbase + s * C::STAGE_BYTES;
-                    const uint32_t fb = full0 + 8 * s;
                     const int k0 = (w.kb_begin + kb) * BK;
-                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-                    tma_load_2d(st, &tmAhi, fb, k0, w.m0);
-                    tma_load_2d(st + C::A_BYTES, &tmAlo, fb, k0, w.m0);
-                    tma_load_2d(st + 2 * C::A_BYTES, &tmBhi, fb, k0, w.n0);
-                    tma_load_2d(st + 2 * C::A_BYTES + C::B_BYTES, &tmBlo, fb, k0, w.n0);
+                    if (SPLIT_IN_KERNEL) {
+                        // A and B as stored, into the hi slots: a 128 x 32
+                        // box of A (K-major already) and four 32 x 32 boxes
+                        // of B (N-contiguous), for a splitter warp to split
+                        const uint32_t fb = full0 + 8 * (it % NFULL);
+                        mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES);
+                        tma_load_2d(st, &tmAhi, fb, k0, w.m0);
+#pragma unroll
+                        for (int j = 0; j < BN / 32; ++j)
+                            tma_load_2d(st + 2 * C::A_BYTES + j * 4096, &tmBhi, fb, w.n0 + 32 * j,
+                                        k0);
+                        if (kb + kPrefetchAhead < w.nkb) {
+                            const int kp = k0 + kPrefetchAhead * BK;
+                            tma_prefetch_2d(&tmAhi, kp, w.m0);
+#pragma unroll
+                            for (int j = 0; j < BN / 32; ++j)
+                                tma_prefetch_2d(&tmBhi, w.n0 + 32 * j, kp);
+                        }
+                    } else {
+                        const uint32_t fb = full0 + 8 * s;
+                        mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                        tma_load_2d(st, &tmAhi, fb, k0, w.m0);
+                        tma_load_2d(st + C::A_BYTES, &tmAlo, fb, k0, w.m0);
+                        tma_load_2d(st + 2 * C::A_BYTES, &tmBhi, fb, k0, w.n0);
+                        tma_load_2d(st + 2 * C::A_BYTES + C::B_BYTES, &tmBlo, fb, k0, w.n0);
+                    }
 
                 }
             }
@@ -398,7 +534,7 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
             // released by the MMA commits before the CTA may exit
             const long long tail = ok ? timeout_ns : timeout_ns / 8 + 1000;
             for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j) {
-                mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1, tail, fault, kFaultDrain);
+                mbar_wait(full0 + 8 * (j % NFULL), (j / NFULL) & 1, tail, fault, kFaultDrain);
                 mbar_wait(empty0 + 8 * (j % STAGES), (j / STAGES) & 1, tail, fault, kFaultDrain);
             }
         }
@@ -424,8 +560,10 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
                     const int c1 = min(w.nkb, c0 + CH);
                     for (int kb = c0; kb < c1; ++kb, ++it) {
                         const int s = it % STAGES;
-                        if (!role_wait(full0 + 8 * s, (it / STAGES) & 1, timeout_ns, fault,
-                                       kFaultFullBarrier, abort_flag)) {
+                        // split in kernel: the stage's converted barrier
+                        if (!role_wait((SPLIT_IN_KERNEL ? conv0 : full0) + 8 * s,
+                                       (it / STAGES) & 1, timeout_ns, fault, kFaultFullBarrier,
+                                       abort_flag)) {
                             ok = false;
                             break;
                         }
@@ -456,7 +594,40 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
             mbar_wait(drain, 0, ok ? timeout_ns : timeout_ns / 8 + 1000, fault, kFaultDrain);
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp < 4) {
+        if (SPLIT_IN_KERNEL) {
+            // ------------------------------ splitter (warps 2-3) ----------------------
+            // as in the pair kernel: warp 2 splits the even-numbered stage
+            // fills, warp 3 the odd ones, each a whole stage, so that one
+            // warp's store drain overlaps the other's conversions
+            int it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, BN, BM,
+                                      cluster_splits);
+                for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+                    if (it % C::NSPLIT != warp - 2) continue;  // the other splitter's turn
+                    const int s = it % STAGES;
+                    const bool got = role_wait(full0 + 8 * (it % NFULL), (it / NFULL) & 1,
+                                               timeout_ns, fault, kFaultFullBarrier, abort_flag);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = sbase + s * C::STAGE_BYTES;
+                    split_a_stage(st, lane);
+                    split_a_stage(st, lane + 32);
+                    split_b_stage(st + 2 * C::A_BYTES, 0, lane);
+                    split_b_stage(st + 2 * C::A_BYTES, 1, lane);
+                    // the tensor core reads these words through the async proxy
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(conv0 + 8 * s);
+                }
+            }
+        }
+        __syncwarp();
+    } else {
         // ------------------------------ epilogue ----------------------------------
         const int e = warp - 4;
         const int q = warp & 3;             // tensor-memory lanes 32q .. 32q+31
@@ -588,15 +759,16 @@ sgemm_3xtf32_kernel(const __grid_constant__ CUtensorMap tmAhi,
     }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool SPLIT_IN_KERNEL = false>
 cudaError_t launch_impl(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
     using C = Cfg<BN, STAGES>;
+    constexpr auto kern = sgemm_3xtf32_kernel<BN, STAGES, SPLIT_IN_KERNEL>;
     static thread_local int attr_done_dev = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (attr_done_dev != dev) {
-        e = cudaFuncSetAttribute(sgemm_3xtf32_kernel<BN, STAGES>,
+        e = cudaFuncSetAttribute(kern,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_done_dev = dev;
@@ -619,7 +791,7 @@ cudaError_t launch_impl(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
         cfg.stream = s;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        e = cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel<BN, STAGES>, a.tmAhi, a.tmAlo, a.tmBhi,
+        e = cudaLaunchKernelEx(&cfg, kern, a.tmAhi, a.tmAlo, a.tmBhi,
                                a.tmBlo, a.out, a.ldo, a.split_stride, a.M, a.N, a.K,
                                a.kb_per_split, a.splits, a.vec_store, a.fault, a.timeout_ns,
                                a.alpha, a.beta, a.scale_mode, a.cluster_splits, a.tmC, 0);
@@ -635,7 +807,7 @@ cudaError_t launch_impl(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, sgemm_3xtf32_kernel<BN, STAGES>, a.tmAhi, a.tmAlo, a.tmBhi,
+    e = cudaLaunchKernelEx(&cfg, kern, a.tmAhi, a.tmAlo, a.tmBhi,
                            a.tmBlo, a.out, a.ldo, a.split_stride, a.M, a.N, a.K, a.kb_per_split,
                            a.splits, a.vec_store, a.fault, a.timeout_ns, a.alpha, a.beta,
                            a.scale_mode, 0, a.tmC, a.tma_store);
@@ -711,103 +883,6 @@ struct PairCfg {
                   "the splitter's thread-to-element maps below");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
-
-__device__ __forceinline__ float4 tf32x4(float4 x) {
-    return make_float4(to_tf32(x.x), to_tf32(x.y), to_tf32(x.z), to_tf32(x.w));
-}
-
-__device__ __forceinline__ float4 sub4(float4 a, float4 b) {
-    return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w);
-}
-
-// x with the low 13 mantissa bits of each lane cleared: the TF32 value the
-// tensor core reads from the fp32 word x (it truncates; measured on this
-// part for ties and near-ties of both parities and signs).
-__device__ __forceinline__ float4 trunc4(float4 x) {
-    return make_float4(__uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u),
-                       __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u),
-                       __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u),
-                       __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u));
-}
-
-// The low part of the TF32 split of four values, lo = tf32(x - trunc(x));
-// the high part is the word x itself (the split of tf32_split.cu).
-__device__ __forceinline__ float4 lo4(float4 x) { return tf32x4(sub4(x, trunc4(x))); }
-
-__device__ __forceinline__ float lane_of(float4 v, int e) {
-    return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
-}
-
-// Rotate the four lanes of v left by r (0..3): result.x = v[r], .y = v[r + 1], ...
-__device__ __forceinline__ float4 rotate4(float4 v, int r) {
-    const float4 a = (r & 1) ? make_float4(v.y, v.z, v.w, v.x) : v;
-    return (r & 2) ? make_float4(a.z, a.w, a.x, a.y) : a;
-}
-
-// A slot (16 KB at sa, K-major, 128-byte swizzled as the TMA wrote it): each
-// value x stays where it is as its own high part, and lo = tf32(x -
-// trunc(x)) goes 16 KB further on.  The map is elementwise, so the layout
-// carries over.  Call t takes 16-byte words t, t + 64, ... (t = 0..63: two
-// calls by the 32 lanes of one warp, t = lane and lane + 32; conflict-free).
-__device__ __forceinline__ void split_a_stage(uint32_t sa, int t) {
-#pragma unroll 1
-    for (int i0 = 0; i0 < 16; i0 += 8) {
-        float4 v[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = lds128(sa + 16 * t + 1024 * (i0 + j));
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            sts128(sa + 16 * t + 1024 * (i0 + j) + 16384, lo4(v[j]));
-    }
-}
-
-// B slot (16 KB at sb): on entry four TMA boxes of 32 k-rows x 32 columns
-// (128-byte rows, box j holding columns 32 j .. 32 j + 31; 16-byte chunk c
-// of row k sits at chunk c ^ (k & 7)).  On exit the K-major hi plane in its
-// place (row n = 128 bytes of k = 0..31, chunk q at q ^ (n & 7): the layout
-// TMA gives a box of the transposed copy) and the lo plane 16 KB further on.
-// Call w (0, 1) does boxes 2w and 2w + 1, i.e. bytes [8192 w, 8192 w +
-// 8192) of both layouts, so the in-place transpose of one call needs only
-// its own warp; one warp makes both calls for a stage.
-// Lane l takes the 4 x 4 blocks (n = 32 j + 4 c .. + 3, k = 4 kq .. + 3)
-// with c = l % 8, kq = l / 8 and l / 8 + 4, j = 2w, 2w + 1: it loads all of
-// them (eight lanes read one 128-byte row: conflict-free), the warp syncs,
-// then it stores each n's four k values as one 16-byte word.  The store
-// order over a block's four n is rotated by c / 2 so that the eight lanes
-// of a quarter-warp write eight different n % 8, i.e. eight different
-// 16-byte bank groups.
-__device__ __forceinline__ void split_b_stage(uint32_t sb, int w, int lane) {
-    const int c = lane & 7;
-    const int rot = (c >> 1) & 3;
-    float4 v[2][2][4];  // [box j - 2w][kq half][k - 4 kq], lanes over n - 32 j - 4 c
-#pragma unroll
-    for (int jj = 0; jj < 2; ++jj)
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const int k = 4 * ((lane >> 3) + 4 * h) + kk;
-                v[jj][h][kk] = rotate4(
-                    lds128(sb + (2 * w + jj) * 4096 + k * 128 + ((c ^ (k & 7)) << 4)), rot);
-            }
-    __syncwarp();  // every raw word of this warp's half is in registers
-#pragma unroll
-    for (int jj = 0; jj < 2; ++jj)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int kq = (lane >> 3) + 4 * h;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int n = 32 * (2 * w + jj) + 4 * c + ((e + rot) & 3);
-                // lane e of the rotated words is column n; k = 4 kq + 0..3
-                const float4 x = make_float4(lane_of(v[jj][h][0], e), lane_of(v[jj][h][1], e),
-                                             lane_of(v[jj][h][2], e), lane_of(v[jj][h][3], e));
-                const uint32_t a = sb + n * 128 + ((kq ^ (n & 7)) << 4);
-                sts128(a, x);
-                sts128(a + 16384, lo4(x));
-            }
-        }
-}
 
 template <int STAGES, bool SPLIT_IN_KERNEL>
 __global__ void __launch_bounds__(PairCfg<STAGES, SPLIT_IN_KERNEL>::THREADS, 1)
@@ -1302,7 +1377,9 @@ cudaError_t launch_sgemm_3xtf32(const Tf32x3Args& a, cudaStream_t s, int sm_coun
     if (a.pair)
         return a.split_in_kernel ? launch_pair<3, true>(a, s, sm_count)
                                  : launch_pair<3, false>(a, s, sm_count);
-    if (a.bn == 128) return launch_impl<128, 3>(a, s, sm_count);
+    if (a.bn == 128)
+        return a.split_in_kernel ? launch_impl<128, 3, true>(a, s, sm_count)
+                                 : launch_impl<128, 3>(a, s, sm_count);
     return launch_impl<256, 2>(a, s, sm_count);
 }
 

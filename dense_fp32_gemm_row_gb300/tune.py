@@ -9,8 +9,8 @@ project" (block size x tile depth x coarsening, each combination checked for
 correctness before it is timed, then ranked).  Here the configuration space
 is the library's own: algorithm (CUDA-core FFMA or 3xTF32 tensor cores) x
 tile (128x128, 128x256, and for 3xTF32 the 256x256 two-CTA tile, fed by
-staging kernels or splitting its operands in shared memory) x split-K
-factor.  Every configuration runs once through ``gemm_f32_configured`` and
+staging kernels or splitting its operands in shared memory, and a 128x128
+tile that splits in shared memory too) x split-K factor.  Every configuration runs once through ``gemm_f32_configured`` and
 must match cuBLAS SGEMM (TF32 off) within 1e-3 + 1e-3 |ref| on every output
 before it is timed (median of ``--repeats`` calls, CUDA events, L2 flushed
 between calls when the inputs fit in it; the configurations of a shape are
@@ -38,12 +38,12 @@ SPLITS = (1, 2, 4, 8, 16, 32, 64)
 def _configs(g, quick: bool = False):
     if quick:
         for tile in (g.TILE_128x128, g.TILE_128x256, g.TILE_256x256_PAIR,
-                     g.TILE_256x256_PAIR_SPLIT):
+                     g.TILE_256x256_PAIR_SPLIT, g.TILE_128x128_SPLIT):
             yield g.ALGO_3XTF32, tile, 0
         return
     for algo, tiles in ((g.ALGO_FFMA, (g.TILE_128x128, g.TILE_128x256)),
                         (g.ALGO_3XTF32, (g.TILE_128x128, g.TILE_128x256, g.TILE_256x256_PAIR,
-                                         g.TILE_256x256_PAIR_SPLIT))):
+                                         g.TILE_256x256_PAIR_SPLIT, g.TILE_128x128_SPLIT))):
         for tile in tiles:
             for splits in SPLITS:
                 yield algo, tile, splits
@@ -59,7 +59,8 @@ def sweep(shapes, repeats: int, out=sys.stdout, quick: bool = False) -> list[dic
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     names = {g.ALGO_FFMA: "ffma", g.ALGO_3XTF32: "3xtf32", g.ALGO_AUTO: "auto"}
-    tiles = {0: "auto", 1: "128x128", 2: "128x256", 3: "256x256pair", 4: "256x256pair-split"}
+    tiles = {0: "auto", 1: "128x128", 2: "128x256", 3: "256x256pair", 4: "256x256pair-split",
+             5: "128x128-split"}
     writer = csv.writer(out)
     writer.writerow(["shape", "algo", "tile", "splits", "ctas", "kernels", "ms", "tflops",
                      "check", "rank"])

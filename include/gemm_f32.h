@@ -78,7 +78,9 @@ extern "C" {
 
 /* ---- algorithms -------------------------------------------------------- */
 /* Choose by shape: the tensor-core 3xTF32 kernels, except the CUDA-core
- * kernel for tiny problems (under 5e7 multiply-adds). */
+ * kernel for tiny problems (under 5e7 multiply-adds); among the tensor-core
+ * kernels, those that split A and B in shared memory when staging them
+ * would cost more than it saves (few flops per operand element). */
 #define GEMM_F32_ALGO_AUTO    0
 /* CUDA-core FFMA kernel: TMA-fed, swizzled shared-memory tiles, mbarrier
  * pipeline, 8x8 or 8x16 register tile per thread. */
@@ -212,13 +214,17 @@ int gemm_f32_plan(int M, int N, int K, int algo, int splits,
  * The 256 x 256 CTA-pair tiles exist for 3XTF32 only: _PAIR reads TF32
  * hi/lo copies of A and B written by staging kernels, _PAIR_SPLIT reads A
  * and B as stored and splits each tile in shared memory (same products, no
- * staging pass).  Invalid combinations return GEMM_F32_ERR_INVALID_VALUE.
+ * staging pass).  _128x128_SPLIT is the single-CTA 128 x 128 tile that
+ * likewise reads A and B as stored and splits them in shared memory (no
+ * staging launch: for small calls, where that launch is a large part of
+ * the call).  Invalid combinations return GEMM_F32_ERR_INVALID_VALUE.
  */
 #define GEMM_F32_TILE_AUTO          0
 #define GEMM_F32_TILE_128x128       1
 #define GEMM_F32_TILE_128x256       2
 #define GEMM_F32_TILE_256x256_PAIR  3
 #define GEMM_F32_TILE_256x256_PAIR_SPLIT 4
+#define GEMM_F32_TILE_128x128_SPLIT 5
 typedef struct gemm_f32_config {
     int algo;
     int tile;

@@ -351,8 +351,10 @@ def test_general_form_on_the_pair_kernel():
                                        (g.ALGO_3XTF32, g.TILE_128x128),
                                        (g.ALGO_3XTF32, g.TILE_128x256),
                                        (g.ALGO_3XTF32, g.TILE_256x256_PAIR),
-                                       (g.ALGO_3XTF32, g.TILE_256x256_PAIR_SPLIT)],
-                         ids=["ffma-128", "ffma-256", "3x-128", "3x-256", "3x-pair", "3x-pair-split"])
+                                       (g.ALGO_3XTF32, g.TILE_256x256_PAIR_SPLIT),
+                                       (g.ALGO_3XTF32, g.TILE_128x128_SPLIT)],
+                         ids=["ffma-128", "ffma-256", "3x-128", "3x-256", "3x-pair", "3x-pair-split",
+                              "3x-128-split"])
 @pytest.mark.parametrize("splits", [1, 5])
 def test_forced_configurations(algo, tile, splits):
     t = _gpu.torch()
@@ -361,7 +363,8 @@ def test_forced_configurations(algo, tile, splits):
     st, p = g.gemm_f32_plan_config(M, N, K, algo, tile, splits, A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and p["algo"] == algo and p["splits"] == splits
     want_tile = {g.TILE_128x128: (128, 128), g.TILE_128x256: (128, 256),
-                 g.TILE_256x256_PAIR: (256, 256), g.TILE_256x256_PAIR_SPLIT: (256, 256)}[tile]
+                 g.TILE_256x256_PAIR: (256, 256), g.TILE_256x256_PAIR_SPLIT: (256, 256),
+                 g.TILE_128x128_SPLIT: (128, 128)}[tile]
     assert (p["tile_m"], p["tile_n"]) == want_tile
     a = t.from_numpy(A).cuda()
     b = t.from_numpy(B).cuda()
@@ -382,6 +385,9 @@ def test_invalid_configurations_are_refused():
         g.ERR_INVALID_VALUE
     assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_FFMA, g.TILE_256x256_PAIR_SPLIT,
                                  0) == g.ERR_INVALID_VALUE
+    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_FFMA, g.TILE_128x128_SPLIT,
+                                 0) == g.ERR_INVALID_VALUE
+    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_3XTF32, 6, 0) == g.ERR_INVALID_VALUE
     assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_3XTF32, 7, 0) == g.ERR_INVALID_VALUE
 
 

@@ -1,6 +1,7 @@
-"""GPU parity of the CTA-pair 3xTF32 kernel that splits A and B into TF32
-hi/lo parts in shared memory (GEMM_F32_TILE_256x256_PAIR_SPLIT) instead of
-reading copies written by staging kernels.
+"""GPU parity of the 3xTF32 kernels that split A and B into TF32 hi/lo parts
+in shared memory (the CTA pair, GEMM_F32_TILE_256x256_PAIR_SPLIT, and the
+single-CTA 128 x 128 tile, GEMM_F32_TILE_128x128_SPLIT) instead of reading
+copies written by staging kernels.
 
 Against the oracle, elementwise within 1e-3 + 1e-3 |C_ref| (NaN guard bands
 around C); against the pre-split pair kernel, bit for bit when neither splits
@@ -117,15 +118,16 @@ def test_quantised_exact():
                                         ((1024, 1024, 4096), 0)],
                          ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
 def test_auto_splits_in_kernel_when_staging_dominates(shape, want):
-    # AUTO takes the in-kernel split when the operands hold at least 4M
+    # AUTO takes the pair kernel's in-kernel split when the operands hold at least 4M
     # elements and either 2 M N / (M + N) < 700 with the pair tiles wasting
     # at most 15 % on padding, or K >= 8192 with 2 M N / (M + N) < 1800 and
     # at most 50 % padding (the staging pass would cost more than it saves)
     M, N, K = shape
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
-    assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["split_in_kernel"] == want, p
+    pair_split = p["split_in_kernel"] == 1 and (p["tile_m"], p["tile_n"]) == (256, 256)
+    assert st == 0 and p["algo"] == g.ALGO_3XTF32 and pair_split == bool(want), p
     if want:
-        assert (p["tile_m"], p["tile_n"]) == (256, 256) and p["stage_a"] == 0 and p["stage_b"] == 0
+        assert p["stage_a"] == 0 and p["stage_b"] == 0
 
 
 def test_auto_skinny_parity():
@@ -169,8 +171,8 @@ def _full_mantissa_values(n, rng):
     return words.view(np.float32)
 
 
-@pytest.mark.parametrize("tile", [g.TILE_128x128, PRESPLIT, SPLIT],
-                         ids=["single-cta-staged", "pair-staged", "pair-split"])
+@pytest.mark.parametrize("tile", [g.TILE_128x128, PRESPLIT, SPLIT, g.TILE_128x128_SPLIT],
+                         ids=["single-cta-staged", "pair-staged", "pair-split", "single-cta-split"])
 def test_split_reconstructs_each_operand(tile):
     # With a 0/1 selection matrix as the other operand, C reproduces one
     # operand's elements through the TF32 split: hi (the fp32 word itself,
@@ -251,3 +253,87 @@ def test_pair_output_ragged_row_in_padded_stride():
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and (p["tile_m"], p["tile_n"]) == (256, 256), p
     _ex_case(M, N, K, 0, 0, 2, 1.0, 0.0, g.ALGO_AUTO)
+
+
+SINGLE_SPLIT = g.TILE_128x128_SPLIT
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_single_cta_split_parity_and_equal_to_staged(shape):
+    # the single-CTA 128 x 128 kernel splitting in shared memory: against the
+    # oracle, and bit for bit against the staged 128 x 128 kernel without
+    # split-K (the same high and low parts, the same MMAs in the same order,
+    # the same 128-deep promotion chunks)
+    M, N, K = shape
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, SINGLE_SPLIT, 1, A=1 << 32,
+                                   B=1 << 36, C=1 << 40)
+    assert st == 0 and p["split_in_kernel"] == 1 and (p["tile_m"], p["tile_n"]) == (128, 128)
+    assert p["stage_a"] == (K % 4 != 0) and p["stage_b"] == (N % 4 != 0), p
+    A, B = make_workload(2, M=M, N=N, K=K)
+    C1 = _gpu.run_configured(A, B, g.ALGO_3XTF32, SINGLE_SPLIT, 1)
+    rows, cols = _sample(M, N, M * 5 + N + K)
+    _check(C1[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols),
+           label=f"single-CTA split {shape}")
+    C0 = _gpu.run_configured(A, B, g.ALGO_3XTF32, g.TILE_128x128, 1)
+    assert np.array_equal(C1.view(np.uint32), C0.view(np.uint32)), \
+        f"differs from the staged kernel at {np.argwhere(C1.view(np.uint32) != C0.view(np.uint32))[:5]}"
+
+
+@pytest.mark.parametrize("splits", [2, 4, 8, 12])
+def test_single_cta_split_with_split_k(splits):
+    # 2..8: the K splits of a tile added inside a cluster; 12: through the
+    # workspace and the reduction kernel
+    M, N, K = 300, 260, 3000
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, SINGLE_SPLIT, splits, A=1 << 32,
+                                   B=1 << 36, C=1 << 40)
+    assert st == 0 and p["splits"] == splits and p["split_in_kernel"] == 1, p
+    assert p["cluster_reduce"] == (1 if splits <= 8 else 0), p
+    A, B = make_workload(4, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, SINGLE_SPLIT, splits)
+    _check(C, oracle.ref_gemm(A, B), label=f"single-CTA split, {splits} K splits")
+    C2 = _gpu.run_configured(A, B, g.ALGO_3XTF32, SINGLE_SPLIT, splits)
+    assert np.array_equal(C.view(np.uint32), C2.view(np.uint32)), "not run-to-run deterministic"
+
+
+@pytest.mark.parametrize("offsets", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (3, 2, 1)])
+def test_single_cta_split_misaligned_operands(offsets):
+    M, N, K = 700, 900, 300
+    A, B = make_workload(1, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, SINGLE_SPLIT, 0, offsets=offsets)
+    _check(C, oracle.ref_gemm(A, B), label=f"single-CTA split, offsets {offsets}")
+
+
+def test_single_cta_split_quantised_exact():
+    A, B = make_workload(0)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, SINGLE_SPLIT, 0)
+    _check(C, oracle.ref_gemm(A, B), exact=True, label="quantised 512^3, single-CTA split")
+
+
+@pytest.mark.parametrize("shape,want", [((89, 1216, 24336), 1), ((200, 200, 20000), 1),
+                                        ((128, 2048, 32768), 1), ((386, 360, 15344), 1),
+                                        ((386, 358, 15342), 0), ((640, 384, 16384), 0),
+                                        ((512, 512, 512), 0), ((1025, 1023, 1000), 0),
+                                        ((128, 4096, 1024), 0), ((256, 256, 65536), 0),
+                                        ((300, 296, 12000), 0), ((384, 384, 20000), 1)],
+                         ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
+def test_auto_single_cta_split_rule(shape, want):
+    # AUTO takes the single-CTA kernel that splits in shared memory when the
+    # pair kernel is not chosen, A and B can be read as stored, staging would
+    # move more than 75 MB and there are under 400 flops per operand element
+    # (386 x 358 x 15342: strides not a multiple of 16 bytes; 640 x 384 x
+    # 16384: 480 flops per element; 128 x 4096 x 1024: 51 MB and 300 x 296 x
+    # 12000: 71 MB of staging; 256 x 256 x 65536: the pair kernel that
+    # splits in shared memory)
+    M, N, K = shape
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0, st
+    single_split = p["split_in_kernel"] == 1 and (p["tile_m"], p["tile_n"]) == (128, 128)
+    assert single_split == bool(want), p
+
+
+def test_auto_single_cta_split_parity():
+    M, N, K = 89, 1216, 24336
+    A, B = make_workload(1, M=M, N=N, K=K)
+    C = _gpu.run(A, B, g.ALGO_AUTO)
+    rows, cols = _sample(M, N, 9)
+    _check(C[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols), label="auto single-CTA split")
