@@ -14,6 +14,7 @@
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "gemm_f32.h"
 #include "gemm_internal.h"
@@ -39,6 +40,11 @@ struct DeviceState {
 struct Workspace {
     void* ptr = nullptr;
     size_t bytes = 0;
+    // a call captured into a CUDA graph used ptr: the graph keeps the
+    // pointer, so a grown workspace retires the old buffer (freed by
+    // gemm_f32_release) instead of freeing it
+    bool captured = false;
+    std::vector<void*> retired;
 };
 
 std::mutex g_mutex;
@@ -131,16 +137,21 @@ int encode_2d(CUtensorMap* map, const float* base, long long dim0, long long dim
 // Workspace of at least `bytes` for (dev, stream); g_mutex must be held.
 int workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
     Workspace& w = g_ws[std::make_pair(dev, stream)];
+    const bool capturing = stream_capturing(stream);
     if (w.bytes < bytes) {
         // growing synchronises the stream and allocates: not while capturing
-        if (stream_capturing(stream)) return GEMM_F32_ERR_CAPTURE;
+        if (capturing) return GEMM_F32_ERR_CAPTURE;
         if (w.ptr) {
             // earlier calls on this stream may still read the old buffer
             cudaError_t e = cudaStreamSynchronize(stream);
             if (e != cudaSuccess) return static_cast<int>(e);
-            cudaFree(w.ptr);
+            if (w.captured)
+                w.retired.push_back(w.ptr);
+            else
+                cudaFree(w.ptr);
             w.ptr = nullptr;
             w.bytes = 0;
+            w.captured = false;
         }
         const size_t grow = static_cast<size_t>(round_up(static_cast<long long>(bytes), 1 << 20));
         if (cudaMalloc(&w.ptr, grow) != cudaSuccess) {
@@ -150,6 +161,7 @@ int workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
         }
         w.bytes = grow;
     }
+    if (capturing) w.captured = true;
     *out = w.ptr;
     return GEMM_F32_SUCCESS;
 }
@@ -782,6 +794,8 @@ struct HostPipe {
     cudaEvent_t ev_bblk[kMaxColBlocks] = {}, ev_cblk[kMaxColBlocks] = {};
     void* dev_buf = nullptr;  // device copies of A, B and C
     size_t dev_bytes = 0;
+    bool captured = false;          // as for Workspace
+    std::vector<void*> retired;
 };
 std::map<std::pair<int, cudaStream_t>, HostPipe> g_pipes;
 
@@ -789,8 +803,9 @@ std::map<std::pair<int, cudaStream_t>, HostPipe> g_pipes;
 int host_pipe(int dev, cudaStream_t stream, size_t bytes, HostPipe** out) {
     HostPipe& hp = g_pipes[std::make_pair(dev, stream)];
     cudaError_t e = cudaSuccess;
-    if ((!hp.ready || hp.dev_bytes < bytes) && stream_capturing(stream))
-        return GEMM_F32_ERR_CAPTURE;
+    const bool capturing = stream_capturing(stream);
+    if ((!hp.ready || hp.dev_bytes < bytes) && capturing) return GEMM_F32_ERR_CAPTURE;
+    if (capturing) hp.captured = true;
     if (!hp.ready) {
         const unsigned fl = cudaEventDisableTiming;
         if ((e = cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking)) != cudaSuccess ||
@@ -812,9 +827,13 @@ int host_pipe(int dev, cudaStream_t stream, size_t bytes, HostPipe** out) {
     if (hp.dev_bytes < bytes) {
         if (hp.dev_buf) {
             if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return static_cast<int>(e);
-            cudaFree(hp.dev_buf);
+            if (hp.captured)
+                hp.retired.push_back(hp.dev_buf);
+            else
+                cudaFree(hp.dev_buf);
             hp.dev_buf = nullptr;
             hp.dev_bytes = 0;
+            hp.captured = false;
         }
         if (cudaMalloc(&hp.dev_buf, bytes) != cudaSuccess) {
             cudaGetLastError();
@@ -1268,6 +1287,10 @@ int gemm_f32_release(void) {
         if (e != cudaSuccess && status == GEMM_F32_SUCCESS) status = static_cast<int>(e);
         cudaFree(kv.second.ptr);
     }
+    for (auto& kv : g_ws) {
+        cudaSetDevice(kv.first.first);
+        for (void* p : kv.second.retired) cudaFree(p);
+    }
     g_ws.clear();
     for (auto& kv : g_pipes) {
         HostPipe& hp = kv.second;
@@ -1275,6 +1298,7 @@ int gemm_f32_release(void) {
         cudaError_t e = cudaDeviceSynchronize();
         if (e != cudaSuccess && status == GEMM_F32_SUCCESS) status = static_cast<int>(e);
         if (hp.dev_buf) cudaFree(hp.dev_buf);
+        for (void* p : hp.retired) cudaFree(p);
         if (hp.ready) {
             cudaStreamDestroy(hp.s_in);
             cudaStreamDestroy(hp.s_out);

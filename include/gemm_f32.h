@@ -41,7 +41,10 @@
  * stream's workspace (or the host entry's device copies); neither is allowed
  * during a capture, so such a call returns GEMM_F32_ERR_CAPTURE without
  * enqueuing anything.  Issue each captured call once on the same stream
- * before capturing it.
+ * before capturing it.  Device memory a captured call uses (the stream's
+ * workspace, the host entry's device copies) stays allocated while later
+ * calls grow those buffers, until gemm_f32_release(): do not release while
+ * a graph that holds such a call may still be replayed.
  *
  * Errors: 0 is success.  Negative values are library errors (GEMM_F32_ERR_*),
  * positive values are the cudaError_t of the failing CUDA runtime call.  No

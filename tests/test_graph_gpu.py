@@ -119,6 +119,43 @@ def test_capture_refuses_to_grow_the_workspace():
     _check(c.cpu().numpy()[rows, cols], want, label="replay after the refusal")
 
 
+def test_replay_after_the_workspace_grew():
+    # a later, larger call on the same stream grows its workspace; the buffer
+    # the captured graph holds must stay allocated (retired, not freed)
+    t = _gpu.torch()
+    s = t.cuda.Stream()
+    M, N, K = 300, 260, 512
+    a = t.rand((M, K), device="cuda") - 0.5
+    b = t.rand((K, N), device="cuda") - 0.5
+    c = t.zeros((M, N), device="cuda")
+
+    def call():
+        return g.gemm_f32_algo(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K,
+                               g.ALGO_3XTF32, s.cuda_stream)
+
+    g.check(call(), "warm-up")
+    s.synchronize()
+    graph = t.cuda.CUDAGraph()
+    with t.cuda.graph(graph, stream=s):
+        g.check(call(), "captured call")
+    # a much larger call on the same stream: its workspace grows past the old one
+    big = 4096
+    x = t.rand((big, big), device="cuda")
+    y = t.empty((big, big), device="cuda")
+    g.check(g.gemm_f32_algo(x.data_ptr(), x.data_ptr(), y.data_ptr(), big, big, big,
+                            g.ALGO_3XTF32, s.cuda_stream), "large call")
+    s.synchronize()
+    a.copy_(t.rand((M, K), device="cuda") - 0.5)
+    c.zero_()
+    t.cuda.synchronize()
+    graph.replay()
+    t.cuda.synchronize()
+    g.check(g.gemm_f32_device_status(1), "device status")
+    A = a.cpu().numpy()
+    B = b.cpu().numpy()
+    _check(c.cpu().numpy(), oracle.ref_gemm(A, B), label="replay after the workspace grew")
+
+
 @pytest.mark.parametrize("shape", [(2304, 2304, 1024), (1024, 1024, 4096)],
                          ids=["row-panels", "k-panels"])
 def test_host_entry_captured(shape):
