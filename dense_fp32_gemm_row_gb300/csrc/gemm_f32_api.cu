@@ -387,7 +387,14 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         const double operand_elements = (static_cast<double>(M) + N) * K;
         const bool few_flops = per_element < 700.0 && waste <= 1.15;
         const bool deep_k = K >= 8192 && per_element < 1800.0 && waste <= 1.5;
-        if (operand_elements >= 4e6 && (few_flops || deep_k)) {
+        // Both kernels that split in shared memory pay off only when they
+        // read A and B as stored: operands whose row stride or base is not a
+        // multiple of 16 bytes need padded copies for TMA anyway (177 x 4459
+        // x 16098: 502 us splitting in the pair kernel, 359 us staged on 128 x
+        // 256 tiles; 1500 x 2079 x 21955: 1202 against 1079 us)
+        const bool in_place = !q.ta && !q.tb && q.lda % 4 == 0 && q.ldb % 4 == 0 &&
+                              !misaligned16(q.A) && !misaligned16(q.B);
+        if (operand_elements >= 4e6 && (few_flops || deep_k) && in_place) {
             p->pair = 1;
             p->split_in_kernel = 1;
             p->bn = 256;
@@ -407,8 +414,6 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         // 386 x 358 x 15342 (124 against 71 us), whose row strides need
         // padded copies anyway.
         const double staging_bytes = 8.0 * M * K + 12.0 * static_cast<double>(K) * N;
-        const bool in_place = !q.ta && !q.tb && q.lda % 4 == 0 && q.ldb % 4 == 0 &&
-                              !misaligned16(q.A) && !misaligned16(q.B);
         if (!p->pair && in_place && staging_bytes > 75e6 && per_element < 400.0) {
             p->split_in_kernel = 1;
             p->bn = 128;

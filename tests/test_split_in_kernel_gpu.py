@@ -109,6 +109,8 @@ def test_quantised_exact():
                                         ((2048, 2048, 2048), 0), ((8192, 8192, 8192), 0),
                                         ((1025, 1023, 1000), 0), ((512, 512, 512), 0),
                                         ((384, 384, 20000), 0), ((300, 260, 30000), 0),
+                                        ((177, 4459, 16098), 0), ((9000, 200, 8190), 0),
+                                        ((9000, 200, 8192), 1),
                                         ((1024, 256, 16384), 1), ((512, 512, 8192), 1),
                                         ((2048, 512, 8192), 1), ((700, 700, 4096), 0),
                                         ((768, 768, 4096), 0), ((512, 512, 4096), 1),
@@ -121,7 +123,9 @@ def test_auto_splits_in_kernel_when_staging_dominates(shape, want):
     # AUTO takes the pair kernel's in-kernel split when the operands hold at least 4M
     # elements and either 2 M N / (M + N) < 700 with the pair tiles wasting
     # at most 15 % on padding, or K >= 8192 with 2 M N / (M + N) < 1800 and
-    # at most 50 % padding (the staging pass would cost more than it saves)
+    # at most 50 % padding (the staging pass would cost more than it saves),
+    # and A and B can be read as stored (177 x 4459 x 16098 and 9000 x 200 x
+    # 8190 have row strides that are not multiples of 16 bytes)
     M, N, K = shape
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
     pair_split = p["split_in_kernel"] == 1 and (p["tile_m"], p["tile_n"]) == (256, 256)
