@@ -359,7 +359,13 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
             // 256, 87 us, against 3 of 128 x 128, 75 us)
             const double u128 = single_cta_fill(d.sm_count, M, N, K, 128, splits);
             const double u256 = 0.85 * single_cta_fill(d.sm_count, M, N, K, 256, splits);
-            if (u256 > 1.1 * u128) p->bn = 256;
+            // With deep K (>= 8192) the 128 x 256 kernel, whose tiles read
+            // less shared memory per flop, unless 128 x 128 tiles keep 3 %
+            // more of the SMs busy (unweighted fills): 177 x 4459 x 16098 361
+            // against 397 us, 1500 x 2079 x 21955 1087 against 1272 us, 272 x
+            // 6979 x 37601 2139 against 2396 us
+            if (K >= 8192) p->bn = (u128 > 1.03 * (u256 / 0.85)) ? 128 : 256;
+            else if (u256 > 1.1 * u128) p->bn = 256;
             else if (u128 > 1.1 * u256) p->bn = 128;
         }
         // Few flops per operand element: the staging pass over A and B (8-12
