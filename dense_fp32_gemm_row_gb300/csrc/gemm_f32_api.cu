@@ -359,12 +359,18 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
             // 256, 87 us, against 3 of 128 x 128, 75 us)
             const double u128 = single_cta_fill(d.sm_count, M, N, K, 128, splits);
             const double u256 = 0.85 * single_cta_fill(d.sm_count, M, N, K, 256, splits);
-            // With deep K (>= 8192) the 128 x 256 kernel, whose tiles read
-            // less shared memory per flop, unless 128 x 128 tiles keep 3 %
-            // more of the SMs busy (unweighted fills): 177 x 4459 x 16098 361
-            // against 397 us, 1500 x 2079 x 21955 1087 against 1272 us, 272 x
-            // 6979 x 37601 2139 against 2396 us
-            if (K >= 8192) p->bn = (u128 > 1.03 * (u256 / 0.85)) ? 128 : 256;
+            // With deep K (>= 8192, and each 128 x 256 unit at least 2048 of
+            // it) the 128 x 256 kernel, whose tiles read less shared memory
+            // per flop, unless 128 x 128 tiles keep 3 % more of the SMs busy
+            // (unweighted fills): 177 x 4459 x 16098 361 against 397 us,
+            // 1500 x 2079 x 21955 1087 against 1272 us, 272 x 6979 x 37601
+            // 2139 against 2396 us.  Shorter units pay the 2-stage ring's
+            // fill too often: 640^2 x 8192, 10 splits of 819, 73 against 61
+            // us for 128 x 128 tiles.
+            const int tiles_256 = ((M + 127) / 128) * ((N + 255) / 256);
+            const int s256 = single_cta_splits(d.sm_count, tiles_256, K, splits, 256);
+            if (K >= 8192 && K / s256 >= 2048)
+                p->bn = (u128 > 1.03 * (u256 / 0.85)) ? 128 : 256;
             else if (u256 > 1.1 * u128) p->bn = 256;
             else if (u128 > 1.1 * u256) p->bn = 128;
         }
@@ -381,18 +387,19 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         //    goes through a workspace, the staged 128 x 128 tiles' through a
         //    cluster);
         //  * K >= 8192 (the split kernel's reduction is then a small part of
-        //    the call) with 2 M N / (M + N) below 1800 and at most 50 %
+        //    the call) with 2 M N / (M + N) below 1800 and at most 40 %
         //    padding: 1024^2 x 8192 (101 against 109 us), 1280^2 x 8192 (132
-        //    against 145), 1536^2 x 8192 (182 against 191), 640^2 x 8192
-        //    (62 against 64, 44 % padding); 2048^2 x 8192 stays staged (309
-        //    against 326 us), as do 8192^3, 700^2 x 4096 and 512^3.
+        //    against 145), 1536^2 x 8192 (182 against 191); 640^2 x 8192
+        //    (44 % padding) stays staged since the staged kernels write C
+        //    with TMA stores (60 against 62-68 us), as do 2048^2 x 8192 (309
+        //    against 326 us), 8192^3, 700^2 x 4096 and 512^3.
         const double per_element = 2.0 * M * N / (static_cast<double>(M) + N);
         const double padded =
             static_cast<double>(round_up(M, 256)) * static_cast<double>(round_up(N, 256));
         const double waste = padded / (static_cast<double>(M) * N);
         const double operand_elements = (static_cast<double>(M) + N) * K;
         const bool few_flops = per_element < 700.0 && waste <= 1.15;
-        const bool deep_k = K >= 8192 && per_element < 1800.0 && waste <= 1.5;
+        const bool deep_k = K >= 8192 && per_element < 1800.0 && waste <= 1.4;
         // Both kernels that split in shared memory pay off only when they
         // read A and B as stored: operands whose row stride or base is not a
         // multiple of 16 bytes need padded copies for TMA anyway (177 x 4459

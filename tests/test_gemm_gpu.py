@@ -126,14 +126,15 @@ def test_pair_kernel_rule(shape):
                                       ((1025, 1023, 1000), 128), ((5514, 160, 43878), 256),
                                       ((177, 4459, 16098), 256), ((1500, 2079, 21955), 256),
                                       ((272, 6979, 37601), 256), ((985, 523, 32870), 128),
-                                      ((896, 896, 4096), 128)],
+                                      ((896, 896, 4096), 128), ((640, 640, 8192), 128)],
                          ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
 def test_single_cta_width_rule(shape, bn):
     # the single-CTA width: 128 x 256 when its tiles fill three quarters of
     # the SMs, or when with their split-K factor they keep clearly (10 %) more
     # of the SMs busy, net of padding and of the 2-stage kernel's lower rate
-    # (x 0.85), than 128 x 128 tiles (and vice versa); with K >= 8192,
-    # 128 x 256 unless 128 x 128 tiles keep 3 % more of the SMs busy
+    # (x 0.85), than 128 x 128 tiles (and vice versa); with K >= 8192 and
+    # at least 2048 of it per 128 x 256 unit, 128 x 256 unless 128 x 128
+    # tiles keep 3 % more of the SMs busy (640^2 x 8192: 10 splits of 819)
     M, N, K = shape
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_3XTF32, 0, A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and p["tile_m"] == 128 and p["tile_n"] == bn, p
