@@ -347,6 +347,18 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         const int units_pair = ((M + 255) / 256) * ((N + 255) / 256);
         const int tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
         p->pair = (5 * units_pair >= 4 * (d.sm_count / 2) && K >= 1024) ? 1 : 0;
+        if (!p->pair && K >= 1024) {
+            // ... or when its tiles, net of padding, keep at least as much of
+            // the machine busy as 128 x 128 tiles with their split-K factor
+            // (1792^2 x 4096: 49 pair tiles and 196 single tiles both fill 64
+            // %; 162.5 against 172.7 us)
+            const int pairs = d.sm_count / 2;
+            const int rounds = (units_pair + pairs - 1) / pairs;
+            const double pad = static_cast<double>(M) * N /
+                               (static_cast<double>(round_up(M, 256)) * round_up(N, 256));
+            const double pair_fill = static_cast<double>(units_pair) / (rounds * pairs) * pad;
+            if (pair_fill >= single_cta_fill(d.sm_count, M, N, K, 128, splits)) p->pair = 1;
+        }
         p->bn = (p->pair || (4 * tiles256 >= 3 * d.sm_count && N > 128)) ? 256 : 128;
         if (!p->pair) {
             // ... unless the other single-CTA width keeps clearly more of the
