@@ -274,6 +274,100 @@ def test_alpha_beta_exact_on_dyadic_values():
     assert np.array_equal(got, (0.5 * S - 2.0 * Cold).astype(np.float32))
 
 
+def _round_f32(x: Fraction) -> np.float32:
+    """The float32 nearest an exact rational, ties to even (normal range).
+
+    Works on the rational itself, so no intermediate double rounding can hide
+    a second rounding in the oracle.
+    """
+    if x == 0:
+        return np.float32(0.0)
+    sign = -1 if x < 0 else 1
+    a = abs(x)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    assert -126 <= e <= 127, "chosen inputs stay in float32's normal range"
+    scaled = a / Fraction(2) ** (e - 23)          # in [2^23, 2^24)
+    m = scaled.numerator // scaled.denominator
+    rem = scaled - m
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and m % 2 == 1):
+        m += 1
+    return np.float32(sign * m * 2.0 ** (e - 23))  # m * 2^(e-23) is exact in double
+
+
+def test_round_f32_helper_against_numpy_on_doubles():
+    # on values that are doubles, numpy's double -> float32 cast is correctly
+    # rounded, so the helper must agree with it everywhere, ties included
+    rng = _rng(17)
+    vals = list(rng.standard_normal(2000) * 2.0 ** rng.integers(-40, 40, 2000))
+    vals += [1.0 + 2.0 ** -24, 1.0 + 3 * 2.0 ** -24, -(1.0 + 2.0 ** -24), 1.0 - 2.0 ** -25]
+    for v in vals:
+        assert _round_f32(Fraction(float(v))) == np.float32(v), v
+
+
+def test_alpha_beta_rounded_once_near_cancellation():
+    # alpha = fl32(1/3), beta = -alpha and an old C one part in 2^9 to 2^14
+    # away from S: alpha*S + beta*C nearly cancels, so rounding alpha*S to
+    # float32 before the add (a double rounding) changes the result by far
+    # more than an ulp of it.  Every double step the general form takes is
+    # exact here (S has <= 23 significant bits, alpha*S <= 47, beta*C <= 48,
+    # and the two products lie within a factor of two of each other), so the
+    # expected value is the exact rational result rounded once.
+    M, N, K = 6, 5, 7
+    rng = _rng(23)
+    Ai = rng.integers(-1024, 1025, size=(M, K))
+    Bi = rng.integers(-1024, 1025, size=(K, N))
+    A = (Ai / 256.0).astype(np.float32)
+    B = (Bi / 256.0).astype(np.float32)
+    S = [[sum(Fraction(int(Ai[i, k]) * int(Bi[k, j]), 65536) for k in range(K))
+          for j in range(N)] for i in range(M)]
+    alpha = np.float32(1.0 / 3.0)
+    beta = -alpha
+    Cold = np.empty((M, N), np.float32)
+    for i in range(M):
+        for j in range(N):
+            s = S[i][j] if S[i][j] != 0 else Fraction(1)
+            delta = Fraction(int(rng.integers(1, 32)), 2 ** int(rng.integers(9, 15)))
+            Cold[i, j] = np.float32(float(s * (1 + delta)))
+    want = np.empty((M, N), np.float32)
+    twice = np.empty((M, N), np.float32)
+    for i in range(M):
+        for j in range(N):
+            exact = Fraction(float(alpha)) * S[i][j] + Fraction(float(beta)) * Fraction(float(Cold[i, j]))
+            want[i, j] = _round_f32(exact)
+            rounded_first = Fraction(float(_round_f32(Fraction(float(alpha)) * S[i][j])))
+            twice[i, j] = _round_f32(rounded_first + Fraction(float(beta)) * Fraction(float(Cold[i, j])))
+    # the case has teeth: a double rounding differs on most entries
+    assert np.mean(want != twice) > 0.5
+    got = oracle.ref_gemm_ex(0, 0, M, N, K, float(alpha), A, K, B, N, float(beta), Cold, N)
+    assert np.array_equal(got.reshape(M, N), want)
+
+
+def test_alpha_beta_general_values_within_one_ulp_of_exact():
+    # general alpha, beta, operands and old C: the exact rational alpha*S +
+    # beta*C rounded once, against which the oracle's double arithmetic may
+    # differ by at most one float32 ulp, and rarely
+    M, N, K = 9, 8, 23
+    rng = _rng(29)
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    B = rng.standard_normal((K, N)).astype(np.float32)
+    Cold = rng.standard_normal((M, N)).astype(np.float32)
+    alpha, beta = np.float32(0.7071), np.float32(-1.3)
+    want = np.empty((M, N), np.float32)
+    for i in range(M):
+        for j in range(N):
+            s = sum(Fraction(float(A[i, k])) * Fraction(float(B[k, j])) for k in range(K))
+            want[i, j] = _round_f32(Fraction(float(alpha)) * s
+                                    + Fraction(float(beta)) * Fraction(float(Cold[i, j])))
+    got = oracle.ref_gemm_ex(0, 0, M, N, K, float(alpha), A, K, B, N, float(beta), Cold, N)
+    dist = _ulp_distance(got.reshape(M, N), want)
+    assert dist.max() <= 1
+    assert np.mean(dist == 0) >= 0.95
+
+
 def test_beta_zero_never_reads_c():
     A, B = make_workload(1, M=4, N=5, K=6)
     got = oracle.ref_gemm_ex(0, 0, 4, 5, 6, 1.0, A, 6, B, 5, 0.0,

@@ -27,6 +27,20 @@ MUTANTS = {
                               "float f = (float)sum; if ((double)f > sum && sum > 0) "
                               "f = __builtin_nextafterf(f, 0.0f); return f;"),
     "absolute_value_result": ("return (float)sum;", "return (float)(sum < 0 ? -sum : sum);"),
+    # the general form's own loop and its alpha/beta step
+    "ex_alpha_product_rounded_to_float": ("double r = alpha * sum;",
+                                          "double r = (double)(float)(alpha * sum);"),
+    "ex_beta_product_in_float": ("r += beta * (double)C[i * ldc + j];",
+                                 "r += (double)((float)beta * C[i * ldc + j]);"),
+    "ex_beta_applied_when_zero": ("if (beta != 0.0) r += beta", "r += beta"),
+    "ex_float_accumulator": ("            double sum = 0.0;\n            for (int64_t k = 0; k < K; ++k) {",
+                             "            float sum = 0.0f;\n            for (int64_t k = 0; k < K; ++k) {"),
+    "ex_transa_indices_swapped": ("transa ? (double)A[k * lda + i] : (double)A[i * lda + k]",
+                                  "transa ? (double)A[i * lda + k] : (double)A[k * lda + i]"),
+    "ex_transb_indices_swapped": ("transb ? (double)B[j * ldb + k] : (double)B[k * ldb + j]",
+                                  "transb ? (double)B[k * ldb + j] : (double)B[j * ldb + k]"),
+    "ex_leading_dimension_ignored": ("(double)A[i * lda + k]", "(double)A[i * K + k]"),
+    "ex_alpha_dropped": ("double r = alpha * sum;", "double r = sum;"),
 }
 
 PINS = [
@@ -39,6 +53,13 @@ PINS = [
     pins.test_double_accumulation_survives_cancellation,
     lambda: pins.test_final_conversion_rounds_to_nearest_even([1.0, 2.0 ** -24, 2.0 ** -40]),
     pins.test_transpose_invariant_bitwise,
+    pins.test_general_form_reduces_to_plain_product,
+    pins.test_transposed_storage_gives_same_bits,
+    pins.test_leading_dimensions_pick_the_right_submatrix,
+    pins.test_alpha_beta_exact_on_dyadic_values,
+    pins.test_alpha_beta_rounded_once_near_cancellation,
+    pins.test_alpha_beta_general_values_within_one_ulp_of_exact,
+    pins.test_beta_zero_never_reads_c,
 ]
 
 
