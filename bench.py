@@ -515,18 +515,23 @@ def run_curve(args) -> int:
     """--curve: square sizes 128 .. 8192 for both kernels and cuBLAS context, as CSV.
 
     The scaling report of "Lecture 12: final project" (its roofline report
-    program) on this library: per size and kernel the median call time over
-    `--steps` calls (L2 flushed between calls below 256 MiB of inputs),
+    program, CSV columns kernel, size, ms, gflops, bytes_gb, ai, bw_gbs,
+    occup, check) on this library: per size and kernel the median call time
+    over `--steps` calls (L2 flushed between calls below 256 MiB of inputs),
     TFLOP/s, compulsory bytes 4(MK + KN + MN), arithmetic intensity, the
-    bandwidth those bytes imply, the fraction of the kernel's roofline, and a
-    cross-check of every output against cuBLAS SGEMM within 1e-3 + 1e-3 |ref|
-    (the report program's GPU-against-GPU check; parity against the CPU
-    oracle is the test suite's job).
+    bandwidth those bytes imply, the fraction of the kernel's roofline, the
+    occupancy of the main kernel (resident threads per SM over the SM's
+    maximum, from the occupancy calculator through the library's plan; empty
+    for cuBLAS), and the check of the output against the CPU oracle within
+    1e-3 + 1e-3 |ref| after the timing: every output up to 2048, beyond that
+    the first and last rows and columns plus 4096 random entries (the oracle
+    evaluates those one by one).  `checked` is the number of outputs compared.
     """
     import numpy as np
     import torch
 
     import dense_fp32_gemm_row_gb300 as g
+    import oracle
     from seeded_inputs import make_workload
 
     g.load()
@@ -534,11 +539,12 @@ def run_curve(args) -> int:
     stream = torch.cuda.current_stream(dev)
     peaks, _ = load_peaks()
     props = torch.cuda.get_device_properties(dev)
+    max_threads = int(getattr(props, "max_threads_per_multi_processor", 2048) or 2048)
     mhz = float(peaks.get("sm_max_mhz") or 2070.0)
     peak_ffma = props.multi_processor_count * FFMA_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
     peak_3x = float(peaks.get("bf16_tflops", 1900.0)) * NOMINAL_TF32_TFLOPS / NOMINAL_BF16_TFLOPS / 3
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    print("kernel,size,ms,tflops,bytes_gb,ai,bw_gbs,pct_roofline,xcheck_cublas", flush=True)
+    print("kernel,size,ms,tflops,bytes_gb,ai,bw_gbs,pct_roofline,occup,check,checked", flush=True)
     sizes = [int(x) for x in args.curve_sizes.split(",")]
     for n in sizes:
         A_np, B_np = make_workload(2, M=n, N=n, K=n)
@@ -546,13 +552,23 @@ def run_curve(args) -> int:
         b = torch.from_numpy(B_np).to(dev)
         c = torch.empty((n, n), dtype=torch.float32, device=dev)
         big = 8 * n * n >= 256 * 1024 * 1024
-        prev = torch.backends.cuda.matmul.allow_tf32
-        torch.backends.cuda.matmul.allow_tf32 = False
-        ref = torch.matmul(a, b)
-        torch.backends.cuda.matmul.allow_tf32 = prev
+        # the oracle's values: the whole product up to 2048, else edge rows
+        # and columns and random entries
+        if n <= 2048:
+            rows = cols = None
+            want = oracle.ref_gemm(A_np, B_np)
+        else:
+            rng = np.random.default_rng(n)
+            ar = np.arange(n)
+            rows = np.concatenate([np.zeros(n, np.int64), np.full(n, n - 1), ar, ar,
+                                   rng.integers(0, n, 4096)])
+            cols = np.concatenate([ar, ar, np.zeros(n, np.int64), np.full(n, n - 1),
+                                   rng.integers(0, n, 4096)])
+            want = oracle.ref_gemm_entries(A_np, B_np, rows, cols)
         flops = 2.0 * n ** 3
         bytes_ = 4.0 * 3 * n * n
         for name in ("ffma", "3xtf32", "cublas"):
+            occup = ""
             if name == "cublas":
                 prev = torch.backends.cuda.matmul.allow_tf32
                 torch.backends.cuda.matmul.allow_tf32 = False
@@ -561,6 +577,10 @@ def run_curve(args) -> int:
                     torch.matmul(a, b, out=c)
             else:
                 algo = g.ALGOS[name]
+                st, plan = g.gemm_f32_plan(n, n, n, algo, 0, a.data_ptr(), b.data_ptr(),
+                                           c.data_ptr())
+                g.check(st, "gemm_f32_plan")
+                occup = f"{plan['ctas_per_sm'] * plan['threads_per_cta'] / max_threads:.3f}"
 
                 def call():
                     g.check(g.gemm_f32_algo(a.data_ptr(), b.data_ptr(), c.data_ptr(), n, n, n,
@@ -582,11 +602,13 @@ def run_curve(args) -> int:
                 torch.backends.cuda.matmul.allow_tf32 = prev
             ms = statistics.median(times)
             tf = flops / (ms * 1e-3) / 1e12
-            ok = bool(((c - ref).abs() <= 1e-3 + 1e-3 * ref.abs()).all().item())
+            got = c.cpu().numpy()
+            got = got if rows is None else got[rows, cols]
+            ok = oracle.compare(got, want)["pass"]
             peak = {"ffma": peak_ffma, "3xtf32": peak_3x, "cublas": peak_ffma}[name]
             print(f"{name},{n},{ms:.4f},{tf:.2f},{bytes_ / 1e9:.4f},{flops / bytes_:.1f},"
-                  f"{bytes_ / (ms * 1e-3) / 1e9:.1f},{100 * tf / peak:.1f},"
-                  f"{'pass' if ok else 'FAIL'}", flush=True)
+                  f"{bytes_ / (ms * 1e-3) / 1e9:.1f},{100 * tf / peak:.1f},{occup},"
+                  f"{'pass' if ok else 'FAIL'},{got.size}", flush=True)
     return 0
 
 

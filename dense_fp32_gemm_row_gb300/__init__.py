@@ -32,6 +32,8 @@ __all__ = [
     "gemm_f32_configured", "gemm_f32_plan_config", "Config", "TILE_AUTO", "TILE_128x128",
     "TILE_128x256", "TILE_256x256_PAIR", "TILE_256x256_PAIR_SPLIT", "TILE_128x128_SPLIT",
     "gemm_f32_plan", "gemm_f32_device_status", "gemm_f32_selftest_watchdog",
+    "gemm_f32_noalloc_selftest_watchdog", "gemm_f32_inject_host_fault", "INJECT_NONE",
+    "INJECT_WORKSPACE", "INJECT_DESCRIPTOR",
     "gemm_f32_release", "gemm_f32_status_string", "gemm_f32_version", "matmul", "check",
 ]
 
@@ -82,6 +84,7 @@ class PlanInfo(ctypes.Structure):
         ("ctas", ctypes.c_int), ("stage_a", ctypes.c_int), ("stage_b", ctypes.c_int),
         ("kernels", ctypes.c_int), ("workspace_bytes", ctypes.c_longlong),
         ("split_in_kernel", ctypes.c_int), ("cluster_reduce", ctypes.c_int),
+        ("ctas_per_sm", ctypes.c_int), ("threads_per_cta", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:
@@ -118,6 +121,8 @@ def load():
         lib.gemm_f32_ex.argtypes = [i, i, i, i, i, f, vp, ll, vp, ll, f, vp, ll, i, i, vp]
         lib.gemm_f32_device_status.argtypes = [i]
         lib.gemm_f32_selftest_watchdog.argtypes = [ll, vp]
+        lib.gemm_f32_noalloc_selftest_watchdog.argtypes = [ll, vp]
+        lib.gemm_f32_inject_host_fault.argtypes = [i]
         lib.gemm_f32_release.argtypes = []
         lib.gemm_f32_status_string.argtypes = [i]
         lib.gemm_f32_status_string.restype = ctypes.c_char_p
@@ -125,7 +130,9 @@ def load():
         for name in ("gemm_f32", "gemm_f32_algo", "gemm_f32_algo_splitk",
                      "gemm_f32_algo_splitk_ev", "gemm_f32_plan", "gemm_f32_noalloc",
                      "gemm_f32_host", "gemm_f32_ex", "gemm_f32_configured", "gemm_f32_plan_config",
-                     "gemm_f32_device_status", "gemm_f32_selftest_watchdog", "gemm_f32_release",
+                     "gemm_f32_device_status", "gemm_f32_selftest_watchdog",
+                     "gemm_f32_noalloc_selftest_watchdog", "gemm_f32_inject_host_fault",
+                     "gemm_f32_release",
                      "gemm_f32_version"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -199,6 +206,21 @@ def gemm_f32_device_status(clear: int = 1) -> int:
 
 def gemm_f32_selftest_watchdog(timeout_ns: int, stream=0) -> int:
     return load().gemm_f32_selftest_watchdog(int(timeout_ns), _p(stream))
+
+
+def gemm_f32_noalloc_selftest_watchdog(timeout_ns: int, stream=0) -> int:
+    """Watchdog self-test on gemm_f32_noalloc's fault word (left set for the status call)."""
+    return load().gemm_f32_noalloc_selftest_watchdog(int(timeout_ns), _p(stream))
+
+
+INJECT_NONE = 0
+INJECT_WORKSPACE = 1
+INJECT_DESCRIPTOR = 2
+
+
+def gemm_f32_inject_host_fault(kind: int) -> int:
+    """Testing aid: the next workspace allocation (1) or descriptor encoding (2) fails; 0 disarms."""
+    return load().gemm_f32_inject_host_fault(int(kind))
 
 
 def gemm_f32_release() -> int:

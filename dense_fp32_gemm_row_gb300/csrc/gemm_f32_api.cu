@@ -9,6 +9,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <map>
@@ -51,6 +52,16 @@ std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 EncodeTiledFn g_encode = nullptr;
+
+// A host-side failure armed by gemm_f32_inject_host_fault (0: none), taken
+// by the first site of its kind that runs.
+std::atomic<int> g_inject{GEMM_F32_INJECT_NONE};
+
+bool injected(int kind) {
+    int want = kind;
+    return g_inject.load(std::memory_order_relaxed) == kind &&
+           g_inject.compare_exchange_strong(want, GEMM_F32_INJECT_NONE);
+}
 
 long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
 
@@ -124,6 +135,7 @@ int get_encoder() {
 // with a row stride of ld elements.
 int encode_2d(CUtensorMap* map, const float* base, long long dim0, long long dim1, long long ld,
               int box0, int box1, CUtensorMapSwizzle swizzle) {
+    if (injected(GEMM_F32_INJECT_DESCRIPTOR)) return GEMM_F32_ERR_DESCRIPTOR;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(dim0), static_cast<cuuint64_t>(dim1)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4u};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(box0), static_cast<cuuint32_t>(box1)};
@@ -154,7 +166,7 @@ int workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
             w.captured = false;
         }
         const size_t grow = static_cast<size_t>(round_up(static_cast<long long>(bytes), 1 << 20));
-        if (cudaMalloc(&w.ptr, grow) != cudaSuccess) {
+        if (injected(GEMM_F32_INJECT_WORKSPACE) || cudaMalloc(&w.ptr, grow) != cudaSuccess) {
             cudaGetLastError();
             w.ptr = nullptr;
             return GEMM_F32_ERR_WORKSPACE;
@@ -865,8 +877,9 @@ int host_pipe(int dev, cudaStream_t stream, size_t bytes, HostPipe** out) {
             hp.dev_bytes = 0;
             hp.captured = false;
         }
-        if (cudaMalloc(&hp.dev_buf, bytes) != cudaSuccess) {
+        if (injected(GEMM_F32_INJECT_WORKSPACE) || cudaMalloc(&hp.dev_buf, bytes) != cudaSuccess) {
             cudaGetLastError();
+            hp.dev_buf = nullptr;
             return GEMM_F32_ERR_WORKSPACE;
         }
         hp.dev_bytes = bytes;
@@ -1259,6 +1272,28 @@ int gemm_f32_plan_config(int M, int N, int K, const gemm_f32_config* cfg, const 
     out->workspace_bytes = static_cast<long long>(p.ws_bytes);
     out->split_in_kernel = p.split_in_kernel;
     out->cluster_reduce = p.cluster_splits ? 1 : 0;
+    // residency of the main kernel, from the occupancy calculator
+    int per_sm = 0;
+    cudaError_t e = cudaSuccess;
+    if (p.algo == GEMM_F32_ALGO_FFMA) {
+        e = ffma_ctas_per_sm(p.variant, &per_sm);
+        out->threads_per_cta = ffma_config(p.variant).threads;
+    } else if (p.pair) {
+        int clusters = 0;
+        e = tf32x3_pair_clusters(d->sm_count, &clusters);
+        per_sm = d->sm_count ? (2 * clusters + d->sm_count - 1) / d->sm_count : 0;
+        out->threads_per_cta = tf32x3_config(256, true).threads;
+    } else {
+        int ctas = 0;
+        e = tf32x3_single_cluster_capacity(p.bn, 1, &ctas);
+        per_sm = d->sm_count ? (ctas + d->sm_count - 1) / d->sm_count : 0;
+        out->threads_per_cta = tf32x3_config(p.bn, false).threads;
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        per_sm = 0;
+    }
+    out->ctas_per_sm = per_sm;
     return GEMM_F32_SUCCESS;
 }
 
@@ -1273,20 +1308,40 @@ int gemm_f32_plan(int M, int N, int K, int algo, int splits, const float* A, con
 
 int gemm_f32_device_status(int clear) {
     std::lock_guard<std::mutex> lock(g_mutex);
-    DeviceState* d = nullptr;
     int dev = 0;
-    int st = device_state(&d, &dev);
-    if (st != GEMM_F32_SUCCESS) return st;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_F32_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_F32_ERR_UNSUPPORTED_DEVICE;
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_F32_ERR_UNSUPPORTED_DEVICE;
+        }
+        if (major != 10 || minor != 3) return GEMM_F32_ERR_UNSUPPORTED_DEVICE;
+    }
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return static_cast<int>(e);
+    // the library's own word, if its set-up has run on this device (a status
+    // query never sets the device up, so it allocates nothing)
     unsigned word = 0;
-    e = cudaMemcpy(&word, d->fault, sizeof(word), cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return static_cast<int>(e);
-    if (clear && word) {
-        e = cudaMemset(d->fault, 0, sizeof(unsigned));
+    if (d.ready) {
+        e = cudaMemcpy(&word, d.fault, sizeof(word), cudaMemcpyDeviceToHost);
         if (e != cudaSuccess) return static_cast<int>(e);
+        if (clear && word) {
+            e = cudaMemset(d.fault, 0, sizeof(unsigned));
+            if (e != cudaSuccess) return static_cast<int>(e);
+        }
     }
-    return word ? GEMM_F32_ERR_DEVICE_TIMEOUT : GEMM_F32_SUCCESS;
+    // and gemm_f32_noalloc's word, which lives in that entry point's array
+    unsigned noalloc_word = 0;
+    int st = noalloc_fault_word(dev, clear, &noalloc_word);
+    if (st != GEMM_F32_SUCCESS) return st;
+    return (word | noalloc_word) ? GEMM_F32_ERR_DEVICE_TIMEOUT : GEMM_F32_SUCCESS;
 }
 
 int gemm_f32_selftest_watchdog(long long timeout_ns, cudaStream_t stream) {
@@ -1364,6 +1419,14 @@ const char* gemm_f32_status_string(int status) {
     }
     if (status > 0) return cudaGetErrorString(static_cast<cudaError_t>(status));
     return "unknown status";
+}
+
+int gemm_f32_inject_host_fault(int kind) {
+    if (kind != GEMM_F32_INJECT_NONE && kind != GEMM_F32_INJECT_WORKSPACE &&
+        kind != GEMM_F32_INJECT_DESCRIPTOR)
+        return GEMM_F32_ERR_INVALID_VALUE;
+    g_inject.store(kind);
+    return GEMM_F32_SUCCESS;
 }
 
 int gemm_f32_version(void) { return 100; }

@@ -21,8 +21,11 @@
 // begins.  All calls share the one array: calls whose executions overlap on
 // the GPU (different streams, or several host threads) race on it and must
 // be serialised by the caller.  Its first 256 bytes hold the kernels' fault
-// word, cleared at set-up; the rest is scratch that every call writes
-// before it reads, so nothing else needs clearing between calls.
+// word, cleared (and the clear waited for) at set-up; the rest is scratch
+// that every call writes before it reads, so nothing else needs clearing
+// between calls.  A kernel whose bounded wait gave up sets a bit in that
+// word; gemm_f32_device_status() reads it (and clears it on request) beside
+// the library's own word, and allocates nothing to do so.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -74,6 +77,8 @@ int noalloc_encode(CUtensorMap* map, const float* base, long long dim0, long lon
 }
 
 // One-time set-up for the current device; g_noalloc_mutex must be held.
+// The set-up waits for work on `stream`, so it is refused while that stream
+// is being captured into a graph.
 int noalloc_setup(NoallocDevice** out, cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -82,6 +87,12 @@ int noalloc_setup(NoallocDevice** out, cudaStream_t stream) {
     }
     NoallocDevice& d = g_noalloc_dev[dev];
     if (!d.ready) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_F32_ERR_CAPTURE;
+        }
+        if (cs != cudaStreamCaptureStatusNone) return GEMM_F32_ERR_CAPTURE;
         int major = 0, minor = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -105,8 +116,10 @@ int noalloc_setup(NoallocDevice** out, cudaStream_t stream) {
         void* p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return static_cast<int>(e);
-        // the fault word must start at zero
-        e = launch_fill_zero(static_cast<float*>(p), kHeaderBytes / 4, stream);
+        // the fault word must start at zero before any call (on any stream)
+        // can use it: clear it and wait for the clear here
+        e = cudaMemsetAsync(p, 0, kHeaderBytes, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
         if (e != cudaSuccess) return static_cast<int>(e);
         d.base = static_cast<unsigned char*>(p);
         d.ready = true;
@@ -116,6 +129,45 @@ int noalloc_setup(NoallocDevice** out, cudaStream_t stream) {
 }
 
 }  // namespace
+
+namespace gemm_f32_impl {
+
+// The no-allocation entry point's fault word on device `dev`: 0 when that
+// device has not been set up by it.  Reading synchronises with the device
+// (a blocking copy); `clear` zeroes a nonzero word afterwards.
+int noalloc_fault_word(int dev, int clear, unsigned* word) {
+    *word = 0;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (dev < 0 || dev >= kMaxDevices || !g_noalloc_dev[dev].ready) return GEMM_F32_SUCCESS;
+    unsigned* fault = reinterpret_cast<unsigned*>(g_noalloc_dev[dev].base);
+    cudaError_t e = cudaMemcpy(word, fault, sizeof(unsigned), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    if (clear && *word) {
+        e = cudaMemset(fault, 0, sizeof(unsigned));
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return static_cast<int>(e);
+    }
+    return GEMM_F32_SUCCESS;
+}
+
+}  // namespace gemm_f32_impl
+
+extern "C" int gemm_f32_noalloc_selftest_watchdog(long long timeout_ns, cudaStream_t stream) {
+    if (timeout_ns < 1000 || timeout_ns > 10000000000LL) return GEMM_F32_ERR_INVALID_VALUE;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    NoallocDevice* d = nullptr;
+    int st = noalloc_setup(&d, stream);
+    if (st != GEMM_F32_SUCCESS) return st;
+    unsigned* fault = reinterpret_cast<unsigned*>(d->base);
+    cudaError_t e = launch_watchdog_selftest(fault, timeout_ns, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    unsigned word = 0;
+    e = cudaMemcpy(&word, fault, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    // the bit stays set, as after a real timeout, until a status call clears it
+    return word ? GEMM_F32_ERR_DEVICE_TIMEOUT : GEMM_F32_SUCCESS;
+}
 
 extern "C" int gemm_f32_noalloc(const float* A, const float* B, float* C, int M, int N, int K,
                                 int splits, cudaStream_t stream) {

@@ -28,6 +28,8 @@ struct FfmaConfig {
     int variant;     // 0: 128 x 128 tiles, 8 x 8 per thread; 1: 128 x 256, 8 x 16
 };
 FfmaConfig ffma_config(int variant);
+// Resident CTAs per SM of a variant, from the occupancy calculator.
+cudaError_t ffma_ctas_per_sm(int variant, int* ctas_per_sm);
 
 struct FfmaArgs {
     CUtensorMap tmA;  // A as {K, M}, box {bk, bm}, swizzled
@@ -147,5 +149,9 @@ cudaError_t launch_scale_c(float* C, long long ldc, int M, int N, float beta, cu
 cudaError_t launch_fill_zero(float* C, long long count, cudaStream_t s);
 // watchdog self-test: waits on a never-completed barrier for timeout_ns
 cudaError_t launch_watchdog_selftest(unsigned* fault, long long timeout_ns, cudaStream_t s);
+
+// gemm_f32_noalloc's fault word on device `dev` (0 if that entry point has
+// not set the device up); blocking read, zeroed afterwards when `clear`.
+int noalloc_fault_word(int dev, int clear, unsigned* word);
 
 }  // namespace gemm_f32_impl

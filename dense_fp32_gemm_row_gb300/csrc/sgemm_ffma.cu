@@ -395,6 +395,23 @@ FfmaConfig ffma_config(int variant) {
     return {BM, Narrow::BN, BK, 3, THREADS, 2, Narrow::SMEM_BYTES, 0};
 }
 
+namespace {
+template <int G, int STAGES, int LAG, int MIN_BLOCKS>
+cudaError_t occupancy(int* ctas_per_sm) {
+    using V = FfmaVariant<G, STAGES, LAG, MIN_BLOCKS>;
+    auto kern = sgemm_ffma_kernel<G, STAGES, LAG, MIN_BLOCKS>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, V::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, kern, THREADS,
+                                                         V::SMEM_BYTES);
+}
+}  // namespace
+
+cudaError_t ffma_ctas_per_sm(int variant, int* ctas_per_sm) {
+    return variant == 1 ? occupancy<4, 4, 2, 1>(ctas_per_sm) : occupancy<2, 3, 1, 2>(ctas_per_sm);
+}
+
 cudaError_t launch_sgemm_ffma(const FfmaArgs& a, cudaStream_t s) {
     if (a.variant == 1) return launch_variant<4, 4, 2, 1>(a, s);
     return launch_variant<2, 3, 1, 2>(a, s);

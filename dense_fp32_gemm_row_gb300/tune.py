@@ -10,11 +10,15 @@ correctness before it is timed, then ranked).  Here the configuration space
 is the library's own: algorithm (CUDA-core FFMA or 3xTF32 tensor cores) x
 tile (128x128, 128x256, and for 3xTF32 the 256x256 two-CTA tile, fed by
 staging kernels or splitting its operands in shared memory, and a 128x128
-tile that splits in shared memory too) x split-K factor.  Every configuration runs once through ``gemm_f32_configured`` and
-must match cuBLAS SGEMM (TF32 off) within 1e-3 + 1e-3 |ref| on every output
-before it is timed (median of ``--repeats`` calls, CUDA events, L2 flushed
-between calls when the inputs fit in it; the configurations of a shape are
-timed round-robin, one call each per round).  The library's own choice
+tile that splits in shared memory too) x split-K factor.  Every configuration
+runs once through ``gemm_f32_configured`` and must pass a correctness check
+before it is timed.  From the command line that check is cuBLAS SGEMM (TF32
+off) within 1e-3 + 1e-3 |ref| on every output: this module belongs to the
+library and does not load the test suite's CPU oracle.  ``sweep(check=...)``
+takes any other check, and the test suite runs the sweep with the oracle as
+its check.  Timing is the median of ``--repeats`` calls (CUDA events, L2
+flushed between calls when the inputs fit in it; the configurations of a
+shape are timed round-robin, one call each per round).  The library's own choice
 (``gemm_f32``, AUTO) is timed alongside so the table shows how far AUTO is
 from the best configuration per shape.
 
@@ -49,7 +53,12 @@ def _configs(g, quick: bool = False):
                 yield algo, tile, splits
 
 
-def sweep(shapes, repeats: int, out=sys.stdout, quick: bool = False) -> list[dict]:
+def sweep(shapes, repeats: int, out=sys.stdout, quick: bool = False, check=None) -> list[dict]:
+    """Check, time and rank every configuration on each (M, N, K) shape.
+
+    ``check(a, b, c) -> bool`` decides whether the output ``c`` of ``a @ b``
+    (device tensors) is correct; the default compares it with cuBLAS SGEMM.
+    """
     import torch
 
     import dense_fp32_gemm_row_gb300 as g
@@ -71,10 +80,17 @@ def sweep(shapes, repeats: int, out=sys.stdout, quick: bool = False) -> list[dic
         a = torch.rand((M, K), device=dev, generator=gen) * 2 - 1
         b = torch.rand((K, N), device=dev, generator=gen) * 2 - 1
         c = torch.empty((M, N), device=dev)
-        prev = torch.backends.cuda.matmul.allow_tf32
-        torch.backends.cuda.matmul.allow_tf32 = False
-        ref = a @ b
-        torch.backends.cuda.matmul.allow_tf32 = prev
+        if check is None:
+            prev = torch.backends.cuda.matmul.allow_tf32
+            torch.backends.cuda.matmul.allow_tf32 = False
+            ref = a @ b
+            torch.backends.cuda.matmul.allow_tf32 = prev
+
+            def passes(c=c, ref=ref):
+                return bool(((c - ref).abs() <= 1e-3 + 1e-3 * ref.abs()).all().item())
+        else:
+            def passes(c=c, a=a, b=b):
+                return bool(check(a, b, c))
         fits_l2 = 4 * (M * K + K * N) < 256 * 1024 * 1024
         flops = 2.0 * M * N * K
 
@@ -115,7 +131,7 @@ def sweep(shapes, repeats: int, out=sys.stdout, quick: bool = False) -> list[dic
             c.fill_(float("nan"))
             call()
             stream.synchronize()
-            ok = bool(((c - ref).abs() <= 1e-3 + 1e-3 * ref.abs()).all().item())
+            ok = passes()
             results.append({"shape": f"{M}x{N}x{K}", "algo": names[algo],
                             "tile": tiles[tile] if algo != g.ALGO_AUTO else
                             f"{plan['tile_m']}x{plan['tile_n']}"

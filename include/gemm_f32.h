@@ -199,6 +199,9 @@ typedef struct gemm_f32_plan_info {
     int split_in_kernel; /* 1 if the 3XTF32 TF32 split happens inside the GEMM kernel */
     int cluster_reduce;  /* 1 if split-K partials are added inside thread-block clusters
                             (no workspace, no reduction kernel) */
+    int ctas_per_sm;     /* CTAs of the main kernel one SM holds at once (occupancy
+                            calculator; 0 if it could not be asked) */
+    int threads_per_cta; /* threads of one CTA of the main kernel */
 } gemm_f32_plan_info;
 
 int gemm_f32_plan(int M, int N, int K, int algo, int splits,
@@ -240,11 +243,14 @@ int gemm_f32_plan_config(int M, int N, int K, const gemm_f32_config* cfg, const 
                          const float* B, const float* C, gemm_f32_plan_info* out);
 
 /*
- * gemm_f32_device_status -- read (and with clear != 0, reset) the device
- * fault word that kernels set when a bounded wait on one of their pipeline
- * barriers runs out.  Synchronises the current device.  Returns 0, or
+ * gemm_f32_device_status -- read (and with clear != 0, reset) the fault
+ * words that kernels set on the current device when a bounded wait on one of
+ * their pipeline barriers runs out: the library's own word and, once
+ * gemm_f32_noalloc has run on the device, the word at the head of that entry
+ * point's fixed array.  Synchronises the current device.  Allocates nothing
+ * and sets nothing up (a device no call has used reports 0).  Returns 0, or
  * GEMM_F32_ERR_DEVICE_TIMEOUT if a kernel reported a timeout since the last
- * clear, or a positive cudaError_t.
+ * clear, GEMM_F32_ERR_UNSUPPORTED_DEVICE, or a positive cudaError_t.
  */
 int gemm_f32_device_status(int clear);
 
@@ -275,8 +281,13 @@ int gemm_f32_selftest_watchdog(long long timeout_ns, cudaStream_t stream);
  * (splits x M x roundup(N, 4) floats), do not fit returns
  * GEMM_F32_ERR_INVALID_VALUE and launches nothing.  The first call on each
  * device looks up the array's device address and clears its fault word (a
- * kernel-side watchdog flag at the start of the array); make that first call
- * before any stream capture begins.  Every call uses the same array, so
+ * kernel-side watchdog flag at the start of the array), waiting on `stream`
+ * for the clear; make that first call before any stream capture begins (made
+ * on a capturing stream it returns GEMM_F32_ERR_CAPTURE and enqueues
+ * nothing).  A kernel of this entry point whose bounded wait runs out sets
+ * that word and returns; the call itself has already returned 0, so, as with
+ * gemm_f32, the timeout is seen through gemm_f32_device_status, which reads
+ * and clears this word too.  Every call uses the same array, so
  * calls whose work overlaps on the GPU (other streams, other host threads)
  * race on it: serialise them.  No cudaMalloc, cudaFree or allocating
  * library routine is called.
@@ -285,11 +296,44 @@ int gemm_f32_selftest_watchdog(long long timeout_ns, cudaStream_t stream);
 int gemm_f32_noalloc(const float* A, const float* B, float* C, int M, int N, int K,
                      int splits, cudaStream_t stream);
 
+/*
+ * gemm_f32_noalloc_selftest_watchdog -- the watchdog self-test of
+ * gemm_f32_selftest_watchdog, aimed at gemm_f32_noalloc's fault word instead
+ * of the library's: one kernel on `stream` waits on a barrier nothing
+ * completes, with a limit of timeout_ns nanoseconds (1e3 .. 1e10), and the
+ * stream is synchronised.  Returns GEMM_F32_ERR_DEVICE_TIMEOUT when the wait
+ * gave up and set the word (the working outcome), 0 if it did not.  The bit
+ * is left set, as after a real timeout, for gemm_f32_device_status to report
+ * and clear.  Allocates nothing; the pages have no counterpart.
+ */
+int gemm_f32_noalloc_selftest_watchdog(long long timeout_ns, cudaStream_t stream);
+
 /* Release every workspace (synchronises each device that has one). */
 int gemm_f32_release(void);
 
 /* Static text for a status code. */
 const char* gemm_f32_status_string(int status);
+
+/*
+ * gemm_f32_inject_host_fault -- a testing aid that makes one host-side
+ * failure happen on purpose, so that a caller's handling of
+ * GEMM_F32_ERR_WORKSPACE and GEMM_F32_ERR_DESCRIPTOR can be exercised
+ * without any fault on the GPU.  kind = GEMM_F32_INJECT_WORKSPACE: the next
+ * workspace (or host-entry buffer) allocation the library attempts reports
+ * failure as if cudaMalloc had failed; GEMM_F32_INJECT_DESCRIPTOR: the next
+ * TMA descriptor encoding reports failure; GEMM_F32_INJECT_NONE disarms.
+ * One-shot and process-wide; off unless called.  The call that meets it
+ * returns the status and launches no GEMM kernel (a descriptor failure may
+ * follow staging copies already enqueued into the workspace; C is never
+ * written); the next call runs normally.  Returns 0, or
+ * GEMM_F32_ERR_INVALID_VALUE for an unknown kind.  The pages' counterpart is
+ * the error-check macro of "Lecture 5", which exits the process; here the
+ * status codes replace the exit.
+ */
+#define GEMM_F32_INJECT_NONE 0
+#define GEMM_F32_INJECT_WORKSPACE 1
+#define GEMM_F32_INJECT_DESCRIPTOR 2
+int gemm_f32_inject_host_fault(int kind);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int gemm_f32_version(void);

@@ -142,3 +142,12 @@ def test_tune_configuration_space():
                                                        g.TILE_256x256_PAIR,
                                                        g.TILE_256x256_PAIR_SPLIT,
                                                        g.TILE_128x128_SPLIT)]
+
+
+def test_host_fault_injection_arms_and_disarms(lib):
+    # the testing aid is host-only: arming and disarming need no device
+    assert g.gemm_f32_inject_host_fault(g.INJECT_WORKSPACE) == g.SUCCESS
+    assert g.gemm_f32_inject_host_fault(g.INJECT_DESCRIPTOR) == g.SUCCESS
+    assert g.gemm_f32_inject_host_fault(g.INJECT_NONE) == g.SUCCESS
+    assert g.gemm_f32_inject_host_fault(3) == g.ERR_INVALID_VALUE
+    assert g.gemm_f32_inject_host_fault(-1) == g.ERR_INVALID_VALUE

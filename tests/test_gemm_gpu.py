@@ -48,6 +48,7 @@ def _check(got, want, exact=False, label=""):
 # arithmetic (a lost promotion chunk, a dropped correction term) shows here
 # before it fails the tolerance.
 HEADROOM = 0.5
+HEADROOM_FULL = 0.9
 
 
 _REF_CACHE = {}
@@ -85,6 +86,24 @@ def test_square_8192_normal_sampled_parity(algo):
     want = oracle.ref_gemm_entries(A, B, rows, cols)
     res = _check(C[rows, cols], want, label=f"square_8192_normal/{algo}")
     assert res["worst_ratio"] < HEADROOM, res
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("algo", [g.ALGO_AUTO, g.ALGO_FFMA], ids=["auto", "ffma"])
+def test_square_8192_normal_full_parity(algo):
+    # every one of the 67M outputs of the 8192^3 workload, in the benchmark's
+    # launch configuration, against the oracle's full product (computed once
+    # for both algorithms: about three minutes on 16 host cores)
+    A, B, C_ref = _workload_with_ref(3)
+    C = _gpu.run(A, B, algo, check_guards=True)
+    res = _check(C, C_ref, label=f"square_8192_normal full/{algo}")
+    print(f"square_8192_normal full/{algo}: worst_ratio={res['worst_ratio']:.4f}")
+    # over all 67M outputs the tail of the error distribution is wider than
+    # on the sampled entries: the CUDA-core kernel, which adds its 8192
+    # products in fp32 one by one, reaches 0.66 of the tolerance somewhere
+    # (the tensor-core path, promoted every 128 of K, stays below 0.5), so
+    # the early-warning bar here is 0.9 for both
+    assert res["worst_ratio"] < HEADROOM_FULL, res
 
 
 EDGE_SHAPES = [
