@@ -184,6 +184,7 @@ struct Plan {
     int bn = 0;
     int pair = 0;     // 3xTF32: two-CTA kernel
     int split_in_kernel = 0;  // 3xTF32 pair kernel: TF32 split done in shared memory
+    int tmem_b = 0;           // 3xTF32: the 128 x 128 kernel with B's split in tensor memory
     int cluster_splits = 0;   // FFMA: split-K partials added inside a cluster (2..4)
     int fused_staging = 0;    // 3xTF32 staged: A and B split by one launch
     int box_n = 0;    // 3xTF32: B^T rows per TMA box
@@ -457,12 +458,16 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         }
         if (tile != GEMM_F32_TILE_AUTO) {
             p->pair = tile == GEMM_F32_TILE_256x256_PAIR || tile == GEMM_F32_TILE_256x256_PAIR_SPLIT;
-            p->split_in_kernel =
-                tile == GEMM_F32_TILE_256x256_PAIR_SPLIT || tile == GEMM_F32_TILE_128x128_SPLIT;
-            p->bn = (tile == GEMM_F32_TILE_128x128 || tile == GEMM_F32_TILE_128x128_SPLIT) ? 128
-                                                                                          : 256;
+            p->tmem_b = tile == GEMM_F32_TILE_128x128_TMEM;
+            p->split_in_kernel = tile == GEMM_F32_TILE_256x256_PAIR_SPLIT ||
+                                 tile == GEMM_F32_TILE_128x128_SPLIT || p->tmem_b;
+            p->bn = (tile == GEMM_F32_TILE_128x128 || tile == GEMM_F32_TILE_128x128_SPLIT ||
+                     p->tmem_b)
+                        ? 128
+                        : 256;
         }
-        const Tf32x3Config tc = tf32x3_config(p->bn, p->pair != 0);
+        const Tf32x3Config tc =
+            p->tmem_b ? tf32x3_tmem_config() : tf32x3_config(p->bn, p->pair != 0);
         bm = tc.bm;
         bn = tc.bn;
         bk = tc.bk;
@@ -499,7 +504,7 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     // 25.8 us, 16 through the workspace 28.3 us), and for K <= 1024 four
     // splits beat eight (400 x 400 x 1024: 21.1 against 25.2 us); its
     // clusters must all fit on the device at once (single_cta_splits)
-    if (p->algo == GEMM_F32_ALGO_3XTF32 && !p->pair)
+    if (p->algo == GEMM_F32_ALGO_3XTF32 && !p->pair && !p->tmem_b)
         s = single_cta_splits(d.sm_count, tiles, K, splits, p->bn);
     p->kb_per_split = (kb_total + s - 1) / s;
     p->splits = (kb_total + p->kb_per_split - 1) / p->kb_per_split;
@@ -543,8 +548,8 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         p->cluster_splits = p->splits;
     // The single-CTA tensor-core kernel likewise, when every CTA gets exactly
     // one unit (its stage memory then holds the partial after the main loop)
-    if (p->algo == GEMM_F32_ALGO_3XTF32 && !p->pair && p->splits >= 2 && p->splits <= 8 &&
-        units <= d.sm_count) {
+    if (p->algo == GEMM_F32_ALGO_3XTF32 && !p->pair && !p->tmem_b && p->splits >= 2 &&
+        p->splits <= 8 && units <= d.sm_count) {
         // ... whose clusters all fit on the device at once (else, with a
         // caller's split factor, the workspace reduction)
         int fit = 0;
@@ -665,6 +670,41 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
     if (p.algo == GEMM_F32_ALGO_3XTF32) {
         Tf32x3Args ta;
         std::memset(&ta, 0, sizeof(ta));
+        if (p.tmem_b) {
+            // the operands as stored: A {K, M} in 128 x 32 boxes, B {N, K}
+            // in 32 x 32 boxes (one 128-byte swizzle row wide)
+            if ((st = encode_2d(&ta.tmAhi, o.a, K, M, p.lda, p.tile_k, 128,
+                                CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
+                (st = encode_2d(&ta.tmBhi, o.b, N, K, p.ldb, 32, p.tile_k,
+                                CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS)
+                return st;
+            ta.out = out;
+            ta.ldo = ldo;
+            ta.split_stride = split_stride;
+            ta.M = M;
+            ta.N = N;
+            ta.K = K;
+            ta.bn = p.bn;
+            ta.kb_per_split = p.kb_per_split;
+            ta.splits = p.splits;
+            ta.fault = d.fault;
+            ta.timeout_ns = kDefaultTimeoutNs;
+            ta.alpha = alpha;
+            ta.beta = beta;
+            ta.scale_mode = kmode;
+            if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
+                return static_cast<int>(e);
+            if ((e = launch_sgemm_3xtf32_tmem(ta, stream, d.sm_count)) != cudaSuccess)
+                return static_cast<int>(e);
+            if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess)
+                return static_cast<int>(e);
+            if (p.splits > 1 && !p.cluster_splits) {
+                e = launch_splitk_reduce(out, split_stride, p.ldw, p.splits, C, ldc, M, N, alpha,
+                                         beta, mode, stream);
+                if (e != cudaSuccess) return static_cast<int>(e);
+            }
+            return GEMM_F32_SUCCESS;
+        }
         if (p.split_in_kernel) {
             // the operands as stored: A {K, M} in 128 x 32 boxes, B {N, K}
             // in 32 x 32 boxes (one 128-byte swizzle row wide)
@@ -1168,10 +1208,10 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
 // A forced configuration: tile id within range and valid for the algorithm.
 int check_config(const gemm_f32_config* cfg) {
     if (!cfg) return GEMM_F32_ERR_INVALID_VALUE;
-    if (cfg->tile < GEMM_F32_TILE_AUTO || cfg->tile > GEMM_F32_TILE_128x128_SPLIT)
+    if (cfg->tile < GEMM_F32_TILE_AUTO || cfg->tile > GEMM_F32_TILE_128x128_TMEM)
         return GEMM_F32_ERR_INVALID_VALUE;
     if ((cfg->tile == GEMM_F32_TILE_256x256_PAIR || cfg->tile == GEMM_F32_TILE_256x256_PAIR_SPLIT ||
-         cfg->tile == GEMM_F32_TILE_128x128_SPLIT) &&
+         cfg->tile == GEMM_F32_TILE_128x128_SPLIT || cfg->tile == GEMM_F32_TILE_128x128_TMEM) &&
         cfg->algo == GEMM_F32_ALGO_FFMA)
         return GEMM_F32_ERR_INVALID_VALUE;
     if (cfg->tile != GEMM_F32_TILE_AUTO && cfg->algo == GEMM_F32_ALGO_AUTO)
@@ -1278,6 +1318,9 @@ int gemm_f32_plan_config(int M, int N, int K, const gemm_f32_config* cfg, const 
     if (p.algo == GEMM_F32_ALGO_FFMA) {
         e = ffma_ctas_per_sm(p.variant, &per_sm);
         out->threads_per_cta = ffma_config(p.variant).threads;
+    } else if (p.tmem_b) {
+        e = tf32x3_tmem_ctas_per_sm(&per_sm);
+        out->threads_per_cta = tf32x3_tmem_config().threads;
     } else if (p.pair) {
         int clusters = 0;
         e = tf32x3_pair_clusters(d->sm_count, &clusters);

@@ -114,6 +114,12 @@ cudaError_t tf32x3_single_cluster_capacity(int bn, int splits, int* clusters);
 // persistent grid: min(units, sm_count) CTAs, or for the pair kernel
 // 2 x min(units, co-resident clusters)
 cudaError_t launch_sgemm_3xtf32(const Tf32x3Args& a, cudaStream_t s, int sm_count);
+// The 128 x 128 kernel with B's split in tensor memory (A and B as stored,
+// in tmAhi {K, M} boxes 32 x 128 and tmBhi {N, K} boxes 32 x 32, both with
+// 128-byte swizzle); out gets C, or split partials, like the kernels above.
+cudaError_t launch_sgemm_3xtf32_tmem(const Tf32x3Args& a, cudaStream_t s, int sm_count);
+Tf32x3Config tf32x3_tmem_config();
+cudaError_t tf32x3_tmem_ctas_per_sm(int* ctas_per_sm);
 
 // ---- TF32 hi/lo staging (tf32_split.cu) --------------------------------------
 // hi = x as stored (read by the tensor core as trunc(x)), lo = tf32(x - trunc(x)).

@@ -1,0 +1,444 @@
+// sgemm_3xtf32_tmem.cu -- the 3xTF32 GEMM with B's split held in tensor
+// memory, for operands read as stored (no staging pass).
+//
+// The tensor core reads a kind::tf32 operand from shared memory only K-major
+// (with the B-major bit of the instruction descriptor set, kind::tf32 MMAs
+// wrote zeros on this part; the same descriptors with bf16 operands were
+// exact).  A row-major K x N matrix B is N-contiguous, so the kernels that
+// split in shared memory transpose B there, and that transpose, with the
+// hi and lo planes it writes, is what bounds them.  An MMA can instead take
+// its A operand from tensor memory, one operand row per lane; and a thread
+// that writes tensor memory writes its own lane.  So here each CTA computes
+// the transposed tile:
+//
+//     D[n][m] (+)= sum_k B[k][n] * A[m][k]      (tensor memory: lane n, column m)
+//
+// with B^T as the MMA's A operand in tensor memory and A as its B operand in
+// shared memory (K-major as stored).  Thread n of the B splitter warpgroup
+// reads column n of the stage's B box (32 k values, one 128-byte row per k:
+// conflict-free), splits each value into hi = trunc(x) (x with its low 13
+// mantissa bits cleared: the TF32 value the tensor core reads from the word)
+// and lo = tf32(x - hi), rounded to nearest even, and stores both as 32
+// columns of its lane: the transpose costs nothing.  Per K step of 8 the MMA
+// lane issues  Bhi*Alo + Blo*Ahi + Bhi*Ahi  (the products of the other
+// 3xTF32 kernels, small terms first, Blo*Alo dropped), with the chunked
+// promotion of those kernels.  The epilogue thread of lane n holds column n
+// of the tile's C for 128 rows m, so each warp store writes 32 consecutive
+// columns of one row of C: 128 contiguous bytes.  A measured microbenchmark
+// put MMAs with A in tensor memory ahead of shared-memory operands (M128 N256:
+// 1130 against 912 TFLOP/s tf32; M128 N128: 841 against 729).
+//
+// One 128 x 128 tile per work unit; a persistent grid of one CTA per SM;
+// 384 threads:
+//   warp 0       one lane issues the TMA loads of a stage: a 128 x 32 box of
+//                A ({K, M}, 128-byte swizzle) and four 32 x 32 boxes of B
+//                ({N, K}, N-contiguous), into a 4-deep ring of 48 KB stages
+//                (A, A lo, B), with an L2 prefetch two K blocks ahead;
+//   warp 1       allocates all 512 tensor-memory columns (two 128-column
+//                accumulators, then four 64-column B operand stages: hi in
+//                the first 32, lo in the next 32) and one lane issues the
+//                MMAs (M = 128 lanes of n, N = 128 of m, K = 8) and commits;
+//   warps 2-3    split A in shared memory, taking stage fills in turn: x
+//                stays as its own high part, lo = tf32(x - trunc(x)) goes
+//                16 KB further on;
+//   warps 4-7    split B into tensor memory (warp 4 + q owns lanes 32q ..
+//                32q + 31, the lane quarter its index gives it);
+//   warps 8-11   the epilogue: per chunk, load the accumulator lanes of the
+//                warp's quarter (128 columns), hand the buffer back and add
+//                them into 128 registers in chunk order; at the end of a
+//                unit store them to C (or to the split-K partials).
+// Every wait is bounded; a timeout sets the device fault word and a shared
+// abort flag that ends the other roles' waits, and the CTA winds down (its
+// in-flight copies and MMAs waited for, bounded) before freeing its tensor
+// memory.  The kernel is launched as a programmatic dependent.
+#include <cstdint>
+
+#include "device_sync.cuh"
+#include "epilogue.cuh"
+#include "gemm_internal.h"
+#include "tcgen05.cuh"
+#include "tf32x3_common.cuh"
+
+namespace gemm_f32_impl {
+namespace {
+
+using namespace gemm_f32_dev;
+
+struct TmemCfg {
+    static constexpr int BN = 128;                 // tile columns n: tensor-memory lanes
+    static constexpr int STAGES = 4;
+    static constexpr int A_BYTES = BM * BK * 4;    // A as stored: its own high part
+    static constexpr int B_BYTES = BN * BK * 4;    // B as stored: four 32 x 32 boxes
+    static constexpr int B_BOX_BYTES = 32 * BK * 4;
+    static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;  // A, A lo, B
+    static constexpr int NSPLIT_A = 2;             // A splitter warps, taking fills in turn
+    // one full barrier per (fill mod STAGES * NSPLIT_A): each A splitter warp
+    // then waits on its own barriers phase after phase; the B splitters wait
+    // on every fill's
+    static constexpr int NFULL = STAGES * NSPLIT_A;
+    static constexpr int THREADS = 384;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int D_COLS = BM;              // accumulator columns: m
+    static constexpr int OP_COL0 = 2 * D_COLS;     // B operand stage s at OP_COL0 + 64 s
+    static constexpr int OP_COLS = 2 * BK;         // hi (32 columns), lo (32 columns)
+    // full (NFULL), empty, A converted, B converted (per stage),
+    // acc_full x2, acc_empty x2, drain
+    static constexpr int NBARS = NFULL + 3 * STAGES + 5;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NBARS * 8 + 16 + 1024;
+    // MMA M = the tile's 128 columns n (lanes), N = its 128 rows m
+    static constexpr uint32_t IDESC = idesc_tf32_f32(BN, BM);
+    static_assert(OP_COL0 + STAGES * OP_COLS <= TMEM_COLS, "tensor-memory columns");
+    static_assert(A_BYTES == 16384, "split_a_stage's map: a 16 KB A slot, lo 16 KB further on");
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
+
+__device__ __forceinline__ float lds32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__global__ void __launch_bounds__(TmemCfg::THREADS, 1)
+sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
+                         const __grid_constant__ CUtensorMap tmB, float* __restrict__ out,
+                         long long ldo, long long split_stride, int M, int N, int K,
+                         int kb_per_split, int splits, unsigned* fault, long long timeout_ns,
+                         float alpha, float beta, int scale_mode) {
+    using C = TmemCfg;
+    constexpr int STAGES = C::STAGES;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t full0 = sbase + STAGES * C::STAGE_BYTES;  // full[f]: + 8 f
+    const uint32_t empty0 = full0 + 8 * C::NFULL;            // empty[s]: + 8 s
+    const uint32_t aconv0 = empty0 + 8 * STAGES;             // A lo written[s]
+    const uint32_t bconv0 = aconv0 + 8 * STAGES;             // B in tensor memory[s]
+    const uint32_t accf0 = bconv0 + 8 * STAGES;              // acc_full[b]
+    const uint32_t acce0 = accf0 + 16;                       // acc_empty[b]
+    const uint32_t drain = acce0 + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + STAGES * C::STAGE_BYTES + C::NBARS * 8);
+    const uint32_t abort_flag = smem_addr(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int tiles_m = (M + BM - 1) / BM;
+    const int tiles_n = (N + C::BN - 1) / C::BN;
+    const int units = tiles_m * tiles_n * splits;
+    const int kb_total = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        for (int f = 0; f < C::NFULL; ++f) mbar_init(full0 + 8 * f, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(aconv0 + 8 * s, 1);
+            mbar_init(bconv0 + 8 * s, 4);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf0 + 8 * b, 1);
+            mbar_init(acce0 + 8 * b, 4);
+        }
+        mbar_init(drain, 1);
+        st_shared_volatile(abort_flag, 0u);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    // launched programmatically: the set-up above overlapped the kernel
+    // before this one; its outputs are read only after this
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------ TMA producer ------------------------------
+            int it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM);
+                for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    if (it >= STAGES &&
+                        !role_wait(empty0 + 8 * s, ((it / STAGES) & 1) ^ 1, timeout_ns, fault,
+                                   kFaultEmptyBarrier, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = sbase + s * C::STAGE_BYTES;
+                    const int k0 = (w.kb_begin + kb) * BK;
+                    const uint32_t fb = full0 + 8 * (it % C::NFULL);
+                    mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES);
+                    tma_load_2d(st, &tmA, fb, k0, w.m0);
+#pragma unroll
+                    for (int j = 0; j < C::BN / 32; ++j)
+                        tma_load_2d(st + 2 * C::A_BYTES + j * C::B_BOX_BYTES, &tmB, fb,
+                                    w.n0 + 32 * j, k0);
+                    if (kb + kPrefetchAhead < w.nkb) {
+                        const int kp = k0 + kPrefetchAhead * BK;
+                        tma_prefetch_2d(&tmA, kp, w.m0);
+#pragma unroll
+                        for (int j = 0; j < C::BN / 32; ++j)
+                            tma_prefetch_2d(&tmB, w.n0 + 32 * j, kp);
+                    }
+                }
+            }
+            // wind down: every issued copy has landed and every stage has been
+            // released by the MMA commits before the CTA may exit
+            const long long tail = ok ? timeout_ns : timeout_ns / 8 + 1000;
+            for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j) {
+                mbar_wait(full0 + 8 * (j % C::NFULL), (j / C::NFULL) & 1, tail, fault,
+                          kFaultDrain);
+                mbar_wait(empty0 + 8 * (j % STAGES), (j / STAGES) & 1, tail, fault, kFaultDrain);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------ MMA issuer --------------------------------
+            int it = 0;  // K blocks consumed (ring position)
+            int g = 0;   // chunks issued (accumulator buffer g & 1)
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM);
+                for (int c0 = 0; c0 < w.nkb && ok; c0 += CH, ++g) {
+                    const int buf = g & 1;
+                    if (g >= 2 && !role_wait(acce0 + 8 * buf, ((g >> 1) & 1) ^ 1, timeout_ns, fault,
+                                             kFaultAccumBarrier, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(buf * C::D_COLS);
+                    const int c1 = min(w.nkb, c0 + CH);
+                    for (int kb = c0; kb < c1; ++kb, ++it) {
+                        const int s = it % STAGES;
+                        const uint32_t par = (it / STAGES) & 1;
+                        if (!role_wait(aconv0 + 8 * s, par, timeout_ns, fault, kFaultFullBarrier,
+                                       abort_flag) ||
+                            !role_wait(bconv0 + 8 * s, par, timeout_ns, fault, kFaultFullBarrier,
+                                       abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t st = sbase + s * C::STAGE_BYTES;
+                        const uint64_t a_hi = smem_desc_sw128_kmajor(st);
+                        const uint64_t a_lo = smem_desc_sw128_kmajor(st + C::A_BYTES);
+                        const uint32_t b_hi =
+                            tmem_base + static_cast<uint32_t>(C::OP_COL0 + C::OP_COLS * s);
+                        const uint32_t b_lo = b_hi + BK;
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k) {
+                            // shared-memory start address + k * 32 bytes (encoded >> 4);
+                            // tensor-memory operand columns + k * 8
+                            const uint64_t off = static_cast<uint64_t>(k * UMMA_K * 4) >> 4;
+                            const uint32_t kc = static_cast<uint32_t>(k * UMMA_K);
+                            const uint32_t acc = (kb > c0 || k > 0) ? 1u : 0u;
+                            mma_tf32_tmem_a(d, b_hi + kc, a_lo + off, C::IDESC, acc);
+                            mma_tf32_tmem_a(d, b_lo + kc, a_hi + off, C::IDESC, 1u);
+                            mma_tf32_tmem_a(d, b_hi + kc, a_hi + off, C::IDESC, 1u);
+                        }
+                        mma_commit(empty0 + 8 * s);
+                    }
+                    if (!ok) break;
+                    mma_commit(accf0 + 8 * buf);
+                }
+            }
+            // all issued MMAs complete before tensor memory is released
+            mma_commit(drain);
+            mbar_wait(drain, 0, ok ? timeout_ns : timeout_ns / 8 + 1000, fault, kFaultDrain);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------ A splitters (warps 2-3) -------------------
+        // warp 2 the even-numbered stage fills, warp 3 the odd ones, each a
+        // whole stage, so that one warp's store drain overlaps the other's
+        // conversions
+        int it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM);
+            for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+                if (it % C::NSPLIT_A != warp - 2) continue;  // the other warp's turn
+                const int s = it % STAGES;
+                const bool got = role_wait(full0 + 8 * (it % C::NFULL), (it / C::NFULL) & 1,
+                                           timeout_ns, fault, kFaultFullBarrier, abort_flag);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t st = sbase + s * C::STAGE_BYTES;
+                split_a_stage(st, lane);
+                split_a_stage(st, lane + 32);
+                // the tensor core reads these words through the async proxy
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(aconv0 + 8 * s);
+            }
+        }
+        __syncwarp();
+    } else if (warp < 8) {
+        // ------------------------------ B splitters (warps 4-7) -------------------
+        // Lane quarter q = warp - 4: tile columns n = 32 q + lane, i.e. box q
+        // of the stage's B.  Column n of k-row r of a box sits in 16-byte
+        // chunk (n / 4) ^ (r % 8) of that 128-byte row (the TMA's swizzle),
+        // word n % 4: for each r the warp reads one whole row.
+        const int q = warp & 3;
+        const uint32_t chunk = static_cast<uint32_t>(lane >> 2);
+        const uint32_t word = static_cast<uint32_t>(lane & 3) * 4u;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+        int it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM);
+            for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+                const int s = it % STAGES;
+                const bool got = role_wait(full0 + 8 * (it % C::NFULL), (it / C::NFULL) & 1,
+                                           timeout_ns, fault, kFaultFullBarrier, abort_flag);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                // the MMAs that last read operand stage s completed before its
+                // smem stage was refilled (the producer waited on empty[s]),
+                // so its tensor-memory columns are free
+                const uint32_t box =
+                    sbase + s * C::STAGE_BYTES + 2 * C::A_BYTES + q * C::B_BOX_BYTES;
+                const uint32_t col = lane_base + static_cast<uint32_t>(C::OP_COL0 + C::OP_COLS * s);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t hi[16], lo[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const uint32_t r = static_cast<uint32_t>(16 * h + i);
+                        const float x = lds32(box + r * 128u + ((chunk ^ (r & 7u)) << 4) + word);
+                        hi[i] = __float_as_uint(x) & 0xFFFFE000u;
+                        lo[i] = __float_as_uint(to_tf32(x - __uint_as_float(hi[i])));
+                    }
+                    tmem_st_32x32b_x16(col + 16u * h, hi);
+                    tmem_st_32x32b_x16(col + BK + 16u * h, lo);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bconv0 + 8 * s);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------ epilogue (warps 8-11) ---------------------
+        const int q = warp & 3;              // tensor-memory lanes 32q .. 32q + 31
+        const int nl = 32 * q + lane;        // this thread's tile column
+        float acc[EPI_COLS];
+        static_assert(EPI_COLS == BM, "one thread holds its column of the whole tile");
+        int g = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM);
+            for (int c0 = 0; c0 < w.nkb; c0 += CH, ++g) {
+                const int buf = g & 1;
+                const bool got = role_wait(accf0 + 8 * buf, (g >> 1) & 1, timeout_ns, fault,
+                                           kFaultAccumBarrier, abort_flag);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                                       static_cast<uint32_t>(buf * C::D_COLS);
+#pragma unroll
+                for (int j = 0; j < EPI_COLS / 16; ++j) {
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(tbase + 16 * j, r);
+                    tmem_ld_wait(r);
+                    if (c0 == 0) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[16 * j + i] = __uint_as_float(r[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[16 * j + i] += __uint_as_float(r[i]);
+                    }
+                }
+                // the chunk is in registers: give the buffer back to the MMA lane
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce0 + 8 * buf);
+            }
+            if (!ok) break;
+            const int n = w.n0 + nl;
+            if (n < N) {
+                float* p = out + static_cast<long long>(w.split) * split_stride +
+                           static_cast<long long>(w.m0) * ldo + n;
+                const int rows = M - w.m0;
+#pragma unroll
+                for (int j = 0; j < EPI_COLS; ++j, p += ldo)
+                    if (j < rows) *p = scale1(acc[j], p, alpha, beta, scale_mode);
+            }
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_sgemm_3xtf32_tmem(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
+    using C = TmemCfg;
+    constexpr auto kern = sgemm_3xtf32_tmem_kernel;
+    static thread_local int attr_done_dev = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (attr_done_dev != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done_dev = dev;
+    }
+    if (a.bn != C::BN || a.pair || a.cluster_splits || a.tail_tiles) return cudaErrorInvalidValue;
+    const int units = ((a.M + BM - 1) / BM) * ((a.N + C::BN - 1) / C::BN) * a.splits;
+    const int grid = units < sm_count ? units : sm_count;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a.tmAhi, a.tmBhi, a.out, a.ldo, a.split_stride, a.M, a.N,
+                           a.K, a.kb_per_split, a.splits, a.fault, a.timeout_ns, a.alpha, a.beta,
+                           a.scale_mode);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+Tf32x3Config tf32x3_tmem_config() {
+    using C = TmemCfg;
+    return {BM, C::BN, BK, C::STAGES, C::THREADS, C::SMEM_BYTES, 0, 32};
+}
+
+cudaError_t tf32x3_tmem_ctas_per_sm(int* ctas_per_sm) {
+    using C = TmemCfg;
+    cudaError_t e = cudaFuncSetAttribute(sgemm_3xtf32_tmem_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, sgemm_3xtf32_tmem_kernel,
+                                                         C::THREADS, C::SMEM_BYTES);
+}
+
+}  // namespace gemm_f32_impl

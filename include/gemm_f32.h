@@ -231,6 +231,7 @@ int gemm_f32_plan(int M, int N, int K, int algo, int splits,
 #define GEMM_F32_TILE_256x256_PAIR  3
 #define GEMM_F32_TILE_256x256_PAIR_SPLIT 4
 #define GEMM_F32_TILE_128x128_SPLIT 5
+#define GEMM_F32_TILE_128x128_TMEM  6
 typedef struct gemm_f32_config {
     int algo;
     int tile;

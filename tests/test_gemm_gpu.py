@@ -378,9 +378,10 @@ def test_general_form_on_the_pair_kernel():
                                        (g.ALGO_3XTF32, g.TILE_128x256),
                                        (g.ALGO_3XTF32, g.TILE_256x256_PAIR),
                                        (g.ALGO_3XTF32, g.TILE_256x256_PAIR_SPLIT),
-                                       (g.ALGO_3XTF32, g.TILE_128x128_SPLIT)],
+                                       (g.ALGO_3XTF32, g.TILE_128x128_SPLIT),
+                                       (g.ALGO_3XTF32, g.TILE_128x128_TMEM)],
                          ids=["ffma-128", "ffma-256", "3x-128", "3x-256", "3x-pair", "3x-pair-split",
-                              "3x-128-split"])
+                              "3x-128-split", "3x-128-tmem"])
 @pytest.mark.parametrize("splits", [1, 5])
 def test_forced_configurations(algo, tile, splits):
     t = _gpu.torch()
@@ -390,7 +391,7 @@ def test_forced_configurations(algo, tile, splits):
     assert st == 0 and p["algo"] == algo and p["splits"] == splits
     want_tile = {g.TILE_128x128: (128, 128), g.TILE_128x256: (128, 256),
                  g.TILE_256x256_PAIR: (256, 256), g.TILE_256x256_PAIR_SPLIT: (256, 256),
-                 g.TILE_128x128_SPLIT: (128, 128)}[tile]
+                 g.TILE_128x128_SPLIT: (128, 128), g.TILE_128x128_TMEM: (128, 128)}[tile]
     assert (p["tile_m"], p["tile_n"]) == want_tile
     a = t.from_numpy(A).cuda()
     b = t.from_numpy(B).cuda()
@@ -413,8 +414,10 @@ def test_invalid_configurations_are_refused():
                                  0) == g.ERR_INVALID_VALUE
     assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_FFMA, g.TILE_128x128_SPLIT,
                                  0) == g.ERR_INVALID_VALUE
-    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_3XTF32, 6, 0) == g.ERR_INVALID_VALUE
+    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_FFMA, g.TILE_128x128_TMEM,
+                                 0) == g.ERR_INVALID_VALUE
     assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_3XTF32, 7, 0) == g.ERR_INVALID_VALUE
+    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_3XTF32, -1, 0) == g.ERR_INVALID_VALUE
 
 
 @pytest.mark.parametrize("algo", [g.ALGO_FFMA, g.ALGO_3XTF32], ids=["ffma", "3xtf32"])
