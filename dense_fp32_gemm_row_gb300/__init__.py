@@ -87,6 +87,7 @@ class PlanInfo(ctypes.Structure):
         ("kernels", ctypes.c_int), ("workspace_bytes", ctypes.c_longlong),
         ("split_in_kernel", ctypes.c_int), ("cluster_reduce", ctypes.c_int),
         ("ctas_per_sm", ctypes.c_int), ("threads_per_cta", ctypes.c_int),
+        ("b_in_tmem", ctypes.c_int), ("reduce_in_kernel", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:

@@ -9,6 +9,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -171,6 +172,13 @@ int workspace(int dev, cudaStream_t stream, size_t bytes, void** out) {
             w.ptr = nullptr;
             return GEMM_F32_ERR_WORKSPACE;
         }
+        // the in-kernel split-K counters start at zero
+        cudaError_t e = cudaMemsetAsync(w.ptr, 0, kWorkspaceCounterBytes, stream);
+        if (e != cudaSuccess) {
+            cudaFree(w.ptr);
+            w.ptr = nullptr;
+            return static_cast<int>(e);
+        }
         w.bytes = grow;
     }
     if (capturing) w.captured = true;
@@ -185,6 +193,7 @@ struct Plan {
     int pair = 0;     // 3xTF32: two-CTA kernel
     int split_in_kernel = 0;  // 3xTF32 pair kernel: TF32 split done in shared memory
     int tmem_b = 0;           // 3xTF32: the 128 x 128 kernel with B's split in tensor memory
+    int reduce_in_kernel = 0; // that kernel adds its split-K partials itself (one unit per CTA)
     int cluster_splits = 0;   // FFMA: split-K partials added inside a cluster (2..4)
     int fused_staging = 0;    // 3xTF32 staged: A and B split by one launch
     int box_n = 0;    // 3xTF32: B^T rows per TMA box
@@ -329,6 +338,35 @@ double single_cta_fill(int sm_count, int M, int N, int K, int bn, int splits) {
     return busy * N / (static_cast<double>(tiles_n) * bn);
 }
 
+// The split-K factor of the kernel with B's split in tensor memory: the one
+// that minimises its modelled time, rounds of the persistent grid x K blocks
+// per unit, plus for S > 1 the reduction launch (~4 us, about 6 K blocks of
+// a unit) and its traffic ((S + 1) M N floats at ~3 TB/s).  Measured: one K
+// block of a unit takes ~0.64 us (8192^3: 4392 us for 27 rounds of 256).
+// 1280^2 x 8192: 100 tiles, S = 3 (two rounds of 86 blocks) over S = 1 (one
+// round of 256, 52 SMs idle); 256 x 256 x 65536: 4 tiles, S = 38.
+int tmem_splits(int sm_count, int tiles, int kb_total, int M, int N) {
+    constexpr double kUsPerBlock = 0.64, kReduceLaunchUs = 4.0, kReduceBytesPerUs = 3.0e6;
+    int best = 1;
+    double best_us = 0.0;
+    const int s_max = std::min(GEMM_F32_MAX_SPLITS, std::max(1, kb_total / 4));
+    for (int s = 1; s <= s_max; ++s) {
+        const int per = (kb_total + s - 1) / s;
+        const int eff = (kb_total + per - 1) / per;  // splits that get work
+        if (eff != s) continue;
+        const long long units = static_cast<long long>(tiles) * s;
+        const long long rounds = (units + sm_count - 1) / sm_count;
+        double us = static_cast<double>(rounds) * per * kUsPerBlock;
+        if (s > 1)
+            us += kReduceLaunchUs + (s + 1.0) * M * static_cast<double>(N) * 4.0 / kReduceBytesPerUs;
+        if (s == 1 || us < best_us) {
+            best = s;
+            best_us = us;
+        }
+    }
+    return best;
+}
+
 size_t carve(size_t* off, long long bytes) {
     const size_t at = *off;
     *off += static_cast<size_t>(round_up(bytes, 256));
@@ -399,60 +437,27 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
             else if (u256 > 1.1 * u128) p->bn = 256;
             else if (u128 > 1.1 * u256) p->bn = 128;
         }
-        // Few flops per operand element: the staging pass over A and B (8-12
-        // bytes per element) then costs more than the tensor work saved by
-        // the staged kernel, so the pair kernel that splits A and B in shared
-        // memory (about 130-210 TFLOP/s, reading each operand once as
-        // stored) is faster.  The rule, fitted to measurements (at least 4M
-        // operand elements in both cases):
-        //  * 2 M N / (M + N) below 700 with the 256 x 256 pair tiles wasting
-        //    at most 15 % on padding: 256 x 256 x 65536 (65 against 116 us
-        //    staged), 512^2 x 4096 (32.8 against 35.5 us); 768^2 x 4096
-        //    stays staged (39.6 against 45.7 us: the pair kernel's split-K
-        //    goes through a workspace, the staged 128 x 128 tiles' through a
-        //    cluster);
-        //  * K >= 8192 (the split kernel's reduction is then a small part of
-        //    the call) with 2 M N / (M + N) below 1800 and at most 40 %
-        //    padding: 1024^2 x 8192 (101 against 109 us), 1280^2 x 8192 (132
-        //    against 145), 1536^2 x 8192 (182 against 191); 640^2 x 8192
-        //    (44 % padding) stays staged since the staged kernels write C
-        //    with TMA stores (60 against 62-68 us), as do 2048^2 x 8192 (309
-        //    against 326 us), 8192^3, 700^2 x 4096 and 512^3.
+        // A and B read as stored (K-contiguous A and N-contiguous B rows,
+        // 16-byte row strides and bases): the 128 x 128 kernel with B's split
+        // in tensor memory needs no staging pass and no transpose in shared
+        // memory, and beats the staged kernels up to 2 M N / (M + N) of about
+        // 2560 (the boundary sweep: 256 x 256 x 65536 51.9 against 66.2 us,
+        // 896^2 x 4096 39.6 against 58.0, 1024^2 x 8192 90.8 against 105.1,
+        // 2048^3 86.7 against 88.7, 2560^3 154.3 against 158.4); beyond
+        // that the two-CTA kernel's N = 256 MMAs win (3072^3 234.1 against
+        // 240.3 us, 4096^3 520.8 against 543.4).  It also beat the two
+        // kernels that split A and B in shared memory (the pair and the
+        // single-CTA 128 x 128 one, now forced configurations only) on every
+        // shape they were chosen for (89 x 1216 x 24336 47.7 against 74.4
+        // us, 512^2 x 8192 35.5 against 43.7).  Operands that need padded
+        // copies keep the staged kernels: the copies and their launches lost
+        // it most such shapes (339 x 1810 x 4223 88.7 against 57.3 us).
         const double per_element = 2.0 * M * N / (static_cast<double>(M) + N);
-        const double padded =
-            static_cast<double>(round_up(M, 256)) * static_cast<double>(round_up(N, 256));
-        const double waste = padded / (static_cast<double>(M) * N);
-        const double operand_elements = (static_cast<double>(M) + N) * K;
-        const bool few_flops = per_element < 700.0 && waste <= 1.15;
-        const bool deep_k = K >= 8192 && per_element < 1800.0 && waste <= 1.4;
-        // Both kernels that split in shared memory pay off only when they
-        // read A and B as stored: operands whose row stride or base is not a
-        // multiple of 16 bytes need padded copies for TMA anyway (177 x 4459
-        // x 16098: 502 us splitting in the pair kernel, 359 us staged on 128 x
-        // 256 tiles; 1500 x 2079 x 21955: 1202 against 1079 us)
         const bool in_place = !q.ta && !q.tb && q.lda % 4 == 0 && q.ldb % 4 == 0 &&
                               !misaligned16(q.A) && !misaligned16(q.B);
-        if (operand_elements >= 4e6 && (few_flops || deep_k) && in_place) {
-            p->pair = 1;
-            p->split_in_kernel = 1;
-            p->bn = 256;
-        }
-        // The single-CTA 128 x 128 kernel that splits in shared memory: its
-        // main loop is bound by the splitter warps (a 128 x 128 tile has half
-        // the pair tile's tensor work per stage split), so it only wins where
-        // the staging pass is large beside the GEMM and A and B can be read
-        // as stored: more than 75 MB of staging traffic (8 bytes per element
-        // of A, 12 per element of B) and fewer than 400 flops per operand
-        // element.  Against the staged 128 x 128 kernel: 89 x 1216 x 24336
-        // 74 against 120 us, 128 x 2048 x 32768 136 against 242, 384^2 x
-        // 32768 89 against 105, 160 x 640 x 24000 76 against 91, 384^2 x
-        // 20000 62 against 71, 200^2 x 20000 43.7 against 45.7; 300 x 296 x
-        // 12000 (71 MB) 47.7 against 44.7 stays staged, as do 512^3 (19.1
-        // against 18.1 us), 1025 x 1023 x 1000 (35.5 against 27.3 us) and
-        // 386 x 358 x 15342 (124 against 71 us), whose row strides need
-        // padded copies anyway.
-        const double staging_bytes = 8.0 * M * K + 12.0 * static_cast<double>(K) * N;
-        if (!p->pair && in_place && staging_bytes > 75e6 && per_element < 400.0) {
+        if (in_place && per_element <= 2560.0) {
+            p->tmem_b = 1;
+            p->pair = 0;
             p->split_in_kernel = 1;
             p->bn = 128;
         }
@@ -506,12 +511,13 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     // clusters must all fit on the device at once (single_cta_splits)
     if (p->algo == GEMM_F32_ALGO_3XTF32 && !p->pair && !p->tmem_b)
         s = single_cta_splits(d.sm_count, tiles, K, splits, p->bn);
+    if (p->tmem_b && splits == 0) s = tmem_splits(d.sm_count, tiles, kb_total, M, N);
     p->kb_per_split = (kb_total + s - 1) / s;
     p->splits = (kb_total + p->kb_per_split - 1) / p->kb_per_split;
     const int units = tiles * p->splits;
     p->ldw = round_up(N, 4);
 
-    size_t off = 0;
+    size_t off = kWorkspaceCounterBytes;  // the counters of in-kernel split-K reductions
     if (p->algo == GEMM_F32_ALGO_3XTF32 && !p->split_in_kernel) {
         // A -> Alo (M x K), and Ahi unless TMA can read A in place as its own
         // high part; B -> B^T hi, lo (N x K); rows padded to 16 bytes
@@ -580,12 +586,21 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         }
     }
     cudaGetLastError();
-    p->ws_bytes = off;
+    // The kernel with B's split in tensor memory adds its partials itself when
+    // every CTA has exactly one unit (all co-resident, a cooperative launch):
+    // the CTAs of a tile wait for each other's partials and each sums a band
+    // of the tile's rows in split order.  No reduction launch (256 x 256 x
+    // 65536, 38 splits: the separate reduction took ~8 us of a 56 us call).
+    if (p->tmem_b && p->splits > 1 && units <= d.sm_count &&
+        2 * tiles * static_cast<long long>(sizeof(int)) <= static_cast<long long>(kWorkspaceCounterBytes))
+        p->reduce_in_kernel = 1;
+    p->ws_bytes = off > kWorkspaceCounterBytes ? off : 0;
     // pre-split operands as stored (A row-major, B not transposed): one
     // staging launch for both
     p->fused_staging = p->algo == GEMM_F32_ALGO_3XTF32 && !p->split_in_kernel && !q.ta && !q.tb;
     p->kernels = 1 + p->stage_a + p->stage_b - p->fused_staging +
-                 (p->splits > 1 && !p->cluster_splits ? 1 : 0) + (p->tail_tiles ? 1 : 0);
+                 (p->splits > 1 && !p->cluster_splits && !p->reduce_in_kernel ? 1 : 0) +
+                 (p->tail_tiles ? 1 : 0);
 }
 
 // Device operands the GEMM kernel reads, after staging.
@@ -692,13 +707,19 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
             ta.alpha = alpha;
             ta.beta = beta;
             ta.scale_mode = kmode;
+            if (p.reduce_in_kernel) {
+                ta.counters = reinterpret_cast<int*>(ws);
+                ta.c_final = C;
+                ta.ldc = ldc;
+                ta.c_mode = mode;
+            }
             if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
                 return static_cast<int>(e);
             if ((e = launch_sgemm_3xtf32_tmem(ta, stream, d.sm_count)) != cudaSuccess)
                 return static_cast<int>(e);
             if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess)
                 return static_cast<int>(e);
-            if (p.splits > 1 && !p.cluster_splits) {
+            if (p.splits > 1 && !p.cluster_splits && !p.reduce_in_kernel) {
                 e = launch_splitk_reduce(out, split_stride, p.ldw, p.splits, C, ldc, M, N, alpha,
                                          beta, mode, stream);
                 if (e != cudaSuccess) return static_cast<int>(e);
@@ -1312,6 +1333,7 @@ int gemm_f32_plan_config(int M, int N, int K, const gemm_f32_config* cfg, const 
     out->workspace_bytes = static_cast<long long>(p.ws_bytes);
     out->split_in_kernel = p.split_in_kernel;
     out->cluster_reduce = p.cluster_splits ? 1 : 0;
+    out->reduce_in_kernel = p.reduce_in_kernel;
     // residency of the main kernel, from the occupancy calculator
     int per_sm = 0;
     cudaError_t e = cudaSuccess;
@@ -1337,6 +1359,7 @@ int gemm_f32_plan_config(int M, int N, int K, const gemm_f32_config* cfg, const 
         per_sm = 0;
     }
     out->ctas_per_sm = per_sm;
+    out->b_in_tmem = p.tmem_b;
     return GEMM_F32_SUCCESS;
 }
 

@@ -103,7 +103,20 @@ struct Tf32x3Args {
     // tile's splits run as one cluster and add their partials in split order
     // through distributed shared memory; out is C
     int cluster_splits;
+    // the kernel with B's split in tensor memory, splits > 1 with one unit
+    // per CTA: out holds the split partials, and the CTAs add them up in
+    // split order inside the kernel (counters: 2 x tiles ints, zero between
+    // calls) and write c_final (row stride ldc, alpha/beta by c_mode)
+    int* counters;
+    float* c_final;
+    long long ldc;
+    int c_mode;
 };
+
+// Bytes at the start of every workspace reserved for the in-kernel split-K
+// counters: zeroed when the workspace is allocated, and each kernel that
+// uses them leaves them zero again.
+constexpr size_t kWorkspaceCounterBytes = 4096;
 // co-resident two-CTA clusters of the pair kernel on the current device
 cudaError_t tf32x3_pair_clusters(int sm_count, int* clusters);
 // co-resident clusters of `splits` (1..8) CTAs of the single-CTA kernel with

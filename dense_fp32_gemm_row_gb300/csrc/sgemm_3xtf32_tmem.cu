@@ -98,12 +98,85 @@ __device__ __forceinline__ float lds32(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// The split-K partials of this CTA's tile added inside the kernel (every
+// CTA holds exactly one unit: split w.split of tile t; all CTAs are
+// co-resident, the launch being cooperative).  Each CTA announces its
+// partial on the tile's arrival counter, waits (bounded) until all S have
+// arrived, then sums a band of ceil(128 / S) tile rows over the S partials
+// in split order (the order of the separate reduction kernel) and writes C;
+// the last CTA of the tile to finish resets both counters for the next call.
+// All threads of the CTA call this.
+__device__ __forceinline__ void reduce_tile_in_kernel(
+    const float* __restrict__ parts, long long ldw, long long split_stride, int* counters,
+    int tiles, int t, const Unit& w, int S, float* __restrict__ C, long long ldc, int M, int N,
+    float alpha, float beta, int mode, unsigned* fault, long long timeout_ns, uint32_t abort_flag) {
+    __shared__ int go;
+    if (threadIdx.x == 0) {
+        // the epilogue threads fenced their partial stores before the barrier
+        // that precedes this call
+        atomicAdd(counters + t, 1);
+        int ok = 1;
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(counters + t) < S) {
+            if (globaltimer_ns() - t0 > static_cast<uint64_t>(timeout_ns)) {
+                if (fault) atomicOr(fault, kFaultAccumBarrier);
+                ok = 0;
+                break;
+            }
+        }
+        go = ok && ld_shared_volatile(abort_flag) == 0u;
+    }
+    __syncthreads();
+    if (go) {
+        const int rows = (BM + S - 1) / S;
+        const int r0 = w.split * rows;
+        const int r1 = min(BM, r0 + rows);
+        constexpr int TN = 128;  // tile columns
+        // partials in flight per thread: a thread sums about one output, so
+        // its chain of L2 round trips bounds the band (as in the separate
+        // reduction kernel, which loads 40 at once)
+        constexpr int CHUNK = 40;
+        for (int idx = threadIdx.x; idx < (r1 - r0) * TN; idx += blockDim.x) {
+            const int m = w.m0 + r0 + idx / TN;
+            const int n = w.n0 + idx % TN;
+            if (m >= M || n >= N) continue;
+            const float* src = parts + static_cast<long long>(m) * ldw + n;
+            float sum = __ldcg(src);
+            for (int s0 = 1; s0 < S; s0 += CHUNK) {
+                float v[CHUNK];
+#pragma unroll
+                for (int j = 0; j < CHUNK; ++j)
+                    v[j] = s0 + j < S ? __ldcg(src + static_cast<long long>(s0 + j) * split_stride)
+                                      : 0.0f;
+#pragma unroll
+                for (int j = 0; j < CHUNK; ++j)
+                    if (s0 + j < S) sum += v[j];
+            }
+            float* dst = C + static_cast<long long>(m) * ldc + n;
+            *dst = scale1(sum, dst, alpha, beta, mode);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && atomicAdd(counters + tiles + t, 1) == S - 1) {
+        // every CTA of the tile has passed its wait: reset for the next call
+        counters[t] = 0;
+        counters[tiles + t] = 0;
+    }
+}
+
 __global__ void __launch_bounds__(TmemCfg::THREADS, 1)
 sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB, float* __restrict__ out,
                          long long ldo, long long split_stride, int M, int N, int K,
                          int kb_per_split, int splits, unsigned* fault, long long timeout_ns,
-                         float alpha, float beta, int scale_mode) {
+                         float alpha, float beta, int scale_mode, int* counters,
+                         float* __restrict__ c_final, long long ldc, int c_mode) {
     using C = TmemCfg;
     constexpr int STAGES = C::STAGES;
     extern __shared__ unsigned char smem_raw[];
@@ -383,6 +456,9 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
                     if (j < rows) *p = scale1(acc[j], p, alpha, beta, scale_mode);
             }
         }
+        // the partial must be visible to the other CTAs of the tile before
+        // this CTA announces it
+        if (counters) __threadfence();
         __syncwarp();
     }
 
@@ -391,6 +467,14 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+    if (counters) {
+        const int tiles = tiles_m * tiles_n;
+        const int u = blockIdx.x;  // this CTA's only unit
+        const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM);
+        reduce_tile_in_kernel(out, ldo, split_stride, counters, tiles, u - w.split * tiles, w,
+                              splits, c_final, ldc, M, N, alpha, beta, c_mode, fault, timeout_ns,
+                              abort_flag);
     }
 }
 
@@ -411,17 +495,22 @@ cudaError_t launch_sgemm_3xtf32_tmem(const Tf32x3Args& a, cudaStream_t s, int sm
     if (a.bn != C::BN || a.pair || a.cluster_splits || a.tail_tiles) return cudaErrorInvalidValue;
     const int units = ((a.M + BM - 1) / BM) * ((a.N + C::BN - 1) / C::BN) * a.splits;
     const int grid = units < sm_count ? units : sm_count;
+    // the in-kernel reduction: one unit per CTA, every CTA resident at once
+    if (a.counters && (a.splits < 2 || units > sm_count)) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cudaLaunchAttribute attr[2];
+    attr[0] = pdl_attribute();
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = a.counters ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, kern, a.tmAhi, a.tmBhi, a.out, a.ldo, a.split_stride, a.M, a.N,
                            a.K, a.kb_per_split, a.splits, a.fault, a.timeout_ns, a.alpha, a.beta,
-                           a.scale_mode);
+                           a.scale_mode, a.counters, a.c_final, a.ldc, a.c_mode);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

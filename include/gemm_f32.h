@@ -202,6 +202,10 @@ typedef struct gemm_f32_plan_info {
     int ctas_per_sm;     /* CTAs of the main kernel one SM holds at once (occupancy
                             calculator; 0 if it could not be asked) */
     int threads_per_cta; /* threads of one CTA of the main kernel */
+    int b_in_tmem;       /* 1 if the 3XTF32 kernel holds B's split in tensor memory
+                            (GEMM_F32_TILE_128x128_TMEM) */
+    int reduce_in_kernel; /* 1 if that kernel adds its split-K partials itself, in
+                             split order (no reduction kernel) */
 } gemm_f32_plan_info;
 
 int gemm_f32_plan(int M, int N, int K, int algo, int splits,
@@ -223,7 +227,12 @@ int gemm_f32_plan(int M, int N, int K, int algo, int splits,
  * staging pass).  _128x128_SPLIT is the single-CTA 128 x 128 tile that
  * likewise reads A and B as stored and splits them in shared memory (no
  * staging launch: for small calls, where that launch is a large part of
- * the call).  Invalid combinations return GEMM_F32_ERR_INVALID_VALUE.
+ * the call).  _128x128_TMEM reads A and B as stored too; it splits A in
+ * shared memory and B into tensor memory, where the MMA takes B^T as its
+ * operand, and computes each 128 x 128 tile transposed (no staging pass and
+ * no transpose in shared memory; AUTO's choice for operands read in place
+ * up to 2 M N / (M + N) of 2560).  Invalid combinations return
+ * GEMM_F32_ERR_INVALID_VALUE.
  */
 #define GEMM_F32_TILE_AUTO          0
 #define GEMM_F32_TILE_128x128       1

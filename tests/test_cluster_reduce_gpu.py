@@ -49,9 +49,13 @@ def test_auto_reduces_in_cluster():
     assert st == 0 and p["splits"] == 4 and p["cluster_reduce"] == 1
     A, B = make_workload(2, M=M, N=N, K=K)
     _check(_gpu.run(A, B, g.ALGO_FFMA), oracle.ref_gemm(A, B), label="ffma 1000x1000x250")
-    # AUTO's choice there: the tensor-core kernel, 2 splits, in a cluster
-    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    # AUTO's choice there when A and B cannot be read in place (A's base 4
+    # bytes off a 16-byte boundary): the staged tensor-core kernel, 2 splits,
+    # in a cluster
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=(1 << 32) + 4, B=1 << 36, C=1 << 40)
     assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["splits"] == 2 and p["cluster_reduce"] == 1
+    _check(_gpu.run(A, B, g.ALGO_AUTO, offsets=(1, 0, 0)), oracle.ref_gemm(A, B),
+           label="auto 1000x1000x250, A misaligned")
     _check(_gpu.run(A, B, g.ALGO_AUTO), oracle.ref_gemm(A, B), label="auto 1000x1000x250")
 
 

@@ -137,10 +137,12 @@ def test_pair_kernel_rule(shape, want):
     # (2048^2: 64 tiles on 76 pairs), or, net of padding, at least as much of
     # the machine as 128 x 128 tiles with their split-K factor (1792^2 x 4096:
     # 49 pair tiles and 196 single tiles both fill 64 %; 1536^2 x 4096: 36
-    # pair tiles fill 47 %, 144 single tiles 95 %)
+    # pair tiles fill 47 %, 144 single tiles 95 %).  A's base 4 bytes off a
+    # 16-byte boundary keeps the operands from being read in place, which
+    # would send these shapes to the kernel with B's split in tensor memory.
     M, N, K = shape
-    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_3XTF32, 0, A=1 << 32, B=1 << 36, C=1 << 40)
-    assert st == 0 and (p["tile_m"] == 256) == bool(want), p
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_3XTF32, 0, A=(1 << 32) + 4, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["b_in_tmem"] == 0 and (p["tile_m"] == 256) == bool(want), p
 
 
 @pytest.mark.parametrize("shape,bn", [((5170, 151, 5906), 256), ((2378, 4792, 286), 128),
@@ -155,10 +157,11 @@ def test_single_cta_width_rule(shape, bn):
     # of the SMs busy, net of padding and of the 2-stage kernel's lower rate
     # (x 0.85), than 128 x 128 tiles (and vice versa); with K >= 8192 and
     # at least 2048 of it per 128 x 256 unit, 128 x 256 unless 128 x 128
-    # tiles keep 3 % more of the SMs busy (640^2 x 8192: 10 splits of 819)
+    # tiles keep 3 % more of the SMs busy (640^2 x 8192: 10 splits of 819);
+    # A off a 16-byte boundary, so that the staged kernels are the choice
     M, N, K = shape
-    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_3XTF32, 0, A=1 << 32, B=1 << 36, C=1 << 40)
-    assert st == 0 and p["tile_m"] == 128 and p["tile_n"] == bn, p
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_3XTF32, 0, A=(1 << 32) + 4, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["b_in_tmem"] == 0 and p["tile_m"] == 128 and p["tile_n"] == bn, p
 
 
 @pytest.mark.parametrize("shape", PAIR_SHAPES, ids=lambda s: "x".join(map(str, s)))

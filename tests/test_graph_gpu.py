@@ -86,7 +86,7 @@ def test_captured_calls_replay_on_new_inputs():
 def test_capture_refuses_to_grow_the_workspace():
     t = _gpu.torch()
     s = t.cuda.Stream()  # a new stream: its workspace is empty
-    M = N = K = 2304
+    M = N = K = 3072  # the two-CTA kernel on staged operands: needs the workspace
     a = t.rand((M, K), device="cuda")
     b = t.rand((K, N), device="cuda")
     c = t.zeros((M, N), device="cuda")

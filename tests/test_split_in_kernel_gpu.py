@@ -106,37 +106,36 @@ def test_quantised_exact():
 
 
 @pytest.mark.parametrize("shape,want", [((256, 256, 65536), 1), ((65536, 256, 1024), 1),
-                                        ((2048, 2048, 2048), 0), ((8192, 8192, 8192), 0),
-                                        ((1025, 1023, 1000), 0), ((512, 512, 512), 0),
-                                        ((384, 384, 20000), 0), ((300, 260, 30000), 0),
-                                        ((177, 4459, 16098), 0), ((9000, 200, 8190), 0),
-                                        ((9000, 200, 8192), 1),
-                                        ((1024, 256, 16384), 1), ((512, 512, 8192), 1),
-                                        ((2048, 512, 8192), 1), ((700, 700, 4096), 0),
-                                        ((768, 768, 4096), 0), ((512, 512, 4096), 1),
-                                        ((1024, 1024, 8192), 1), ((640, 640, 8192), 0),
-                                        ((1536, 1536, 8192), 1), ((2048, 2048, 8192), 0),
-                                        ((1536, 1536, 4096), 0), ((384, 384, 32768), 0),
-                                        ((1024, 1024, 4096), 0)],
+                                        ((2048, 2048, 2048), 1), ((8192, 8192, 8192), 0),
+                                        ((1025, 1023, 1000), 0), ((512, 512, 512), 1),
+                                        ((384, 384, 20000), 1), ((177, 4459, 16098), 0),
+                                        ((9000, 200, 8190), 0), ((9000, 200, 8192), 1),
+                                        ((2560, 2560, 2560), 1), ((3072, 3072, 3072), 0),
+                                        ((4096, 4096, 4096), 0), ((1024, 1024, 8192), 1),
+                                        ((2304, 2304, 512), 1), ((386, 358, 15342), 0),
+                                        ((89, 1216, 24336), 1), ((2900, 2900, 1024), 0)],
                          ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
-def test_auto_splits_in_kernel_when_staging_dominates(shape, want):
-    # AUTO takes the pair kernel's in-kernel split when the operands hold at least 4M
-    # elements and either 2 M N / (M + N) < 700 with the pair tiles wasting
-    # at most 15 % on padding, or K >= 8192 with 2 M N / (M + N) < 1800 and
-    # at most 40 % padding (the staging pass would cost more than it saves),
-    # and A and B can be read as stored (177 x 4459 x 16098 and 9000 x 200 x
-    # 8190 have row strides that are not multiples of 16 bytes)
+def test_auto_b_in_tensor_memory_rule(shape, want):
+    # AUTO takes the kernel with B's split in tensor memory when A and B can
+    # be read as stored and 2 M N / (M + N) <= 2560 (beyond, the two-CTA
+    # kernel on staged operands: 3072^3, 4096^3, 8192^3); a row stride that
+    # is not a multiple of 16 bytes (1025 x 1023, 177 x 4459, 9000 x 200 x
+    # 8190, 386 x 358 x 15342) keeps the staged kernels
     M, N, K = shape
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
-    pair_split = p["split_in_kernel"] == 1 and (p["tile_m"], p["tile_n"]) == (256, 256)
-    assert st == 0 and p["algo"] == g.ALGO_3XTF32 and pair_split == bool(want), p
+    assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["b_in_tmem"] == want, p
     if want:
-        assert p["stage_a"] == 0 and p["stage_b"] == 0
+        assert (p["tile_m"], p["tile_n"]) == (128, 128) and p["split_in_kernel"] == 1, p
+        assert p["stage_a"] == 0 and p["stage_b"] == 0, p
+        assert p["cluster_reduce"] == 0 and p["kernels"] == (1 if p["splits"] == 1 else 2), p
+    # A misaligned by 4 bytes: never read in place, so never this kernel
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=(1 << 32) + 4, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["b_in_tmem"] == 0, p
 
 
 def test_auto_skinny_parity():
-    # the in-kernel split chosen by AUTO on a tall, narrow, deep product
-    # (ragged M and N: 31 % of the pair tiles' area is padding)
+    # AUTO on a tall, narrow, deep product read in place (B's split in
+    # tensor memory; ragged M)
     M, N, K = 9000, 200, 8192
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and p["split_in_kernel"] == 1, p
@@ -149,7 +148,7 @@ def test_auto_skinny_parity():
 @pytest.mark.parametrize("ta,tb", [(0, 0), (1, 1)])
 def test_general_form_through_the_in_kernel_split(ta, tb):
     # alpha/beta, leading dimensions and (staged) transposes on a shape AUTO
-    # sends to the pair kernel that splits in shared memory
+    # sends, read in place, to the kernel with B's split in tensor memory
     from .test_gemm_gpu import _ex_case
     M, N, K = 1024, 256, 16384
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
@@ -226,26 +225,27 @@ def test_pair_output_boxes(tile, shape):
 
 def test_pair_output_boxes_alpha():
     # alpha without beta: the pair kernel scales the values it stages for the
-    # TMA stores; ragged N (2100 = 8 * 256 + 52) and a padded row stride
+    # TMA stores; ragged N (2900 = 11 * 256 + 84) and a padded row stride
     from .test_gemm_gpu import _ex_case
-    M, N, K = 2100, 2100, 1024
+    M, N, K = 2900, 2900, 1024
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and (p["tile_m"], p["tile_n"]) == (256, 256), p
     _ex_case(M, N, K, 0, 0, 4, 0.5, 0.0, g.ALGO_AUTO)
 
 
-@pytest.mark.parametrize("shape,algo", [((2100, 2100, 1024), g.ALGO_AUTO),
-                                        ((300, 200, 40), g.ALGO_3XTF32),
-                                        ((520, 100, 2000), g.ALGO_3XTF32)],
+@pytest.mark.parametrize("shape,algo,ta", [((2900, 2900, 1024), g.ALGO_AUTO, 0),
+                                           ((300, 200, 40), g.ALGO_3XTF32, 1),
+                                           ((520, 100, 2000), g.ALGO_3XTF32, 1)],
                          ids=["pair", "single-128", "single-ragged-m"])
-def test_output_boxes_with_beta(shape, algo):
+def test_output_boxes_with_beta(shape, algo, ta):
     # alpha and beta: the kernels load each 32 x 16 box of the old C into
     # their shared-memory slab (TMA, clipped boxes zero-filled outside C),
-    # replace it by alpha v + beta C and store it back
+    # replace it by alpha v + beta C and store it back (a transposed A keeps
+    # the small shapes on the staged single-CTA kernels)
     from .test_gemm_gpu import _ex_case
     M, N, K = shape
-    _ex_case(M, N, K, 0, 0, 4, 0.5, -0.75, algo)
-    _ex_case(M, N, K, 0, 0, 0, 1.0, 1.0, algo)
+    _ex_case(M, N, K, ta, 0, 4, 0.5, -0.75, algo)
+    _ex_case(M, N, K, ta, 0, 0, 1.0, 1.0, algo)
 
 
 def test_pair_output_ragged_row_in_padded_stride():
@@ -253,7 +253,7 @@ def test_pair_output_ragged_row_in_padded_stride():
     # columns past N (the padding) must come back untouched, so the kernel may
     # not store the last row piece as a whole 16-byte unit
     from .test_gemm_gpu import _ex_case
-    M, N, K = 2100, 2102, 1024
+    M, N, K = 2900, 2902, 1024
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and (p["tile_m"], p["tile_n"]) == (256, 256), p
     _ex_case(M, N, K, 0, 0, 2, 1.0, 0.0, g.ALGO_AUTO)
@@ -313,31 +313,10 @@ def test_single_cta_split_quantised_exact():
     _check(C, oracle.ref_gemm(A, B), exact=True, label="quantised 512^3, single-CTA split")
 
 
-@pytest.mark.parametrize("shape,want", [((89, 1216, 24336), 1), ((200, 200, 20000), 1),
-                                        ((128, 2048, 32768), 1), ((386, 360, 15344), 1),
-                                        ((386, 358, 15342), 0), ((640, 384, 16384), 0),
-                                        ((512, 512, 512), 0), ((1025, 1023, 1000), 0),
-                                        ((128, 4096, 1024), 0), ((256, 256, 65536), 0),
-                                        ((300, 296, 12000), 0), ((384, 384, 20000), 1)],
-                         ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
-def test_auto_single_cta_split_rule(shape, want):
-    # AUTO takes the single-CTA kernel that splits in shared memory when the
-    # pair kernel is not chosen, A and B can be read as stored, staging would
-    # move more than 75 MB and there are under 400 flops per operand element
-    # (386 x 358 x 15342: strides not a multiple of 16 bytes; 640 x 384 x
-    # 16384: 480 flops per element; 128 x 4096 x 1024: 51 MB and 300 x 296 x
-    # 12000: 71 MB of staging; 256 x 256 x 65536: the pair kernel that
-    # splits in shared memory)
-    M, N, K = shape
-    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
-    assert st == 0, st
-    single_split = p["split_in_kernel"] == 1 and (p["tile_m"], p["tile_n"]) == (128, 128)
-    assert single_split == bool(want), p
-
-
-def test_auto_single_cta_split_parity():
+def test_auto_skinny_deep_parity():
+    # few flops per operand element, read in place: B's split in tensor memory
     M, N, K = 89, 1216, 24336
     A, B = make_workload(1, M=M, N=N, K=K)
     C = _gpu.run(A, B, g.ALGO_AUTO)
     rows, cols = _sample(M, N, 9)
-    _check(C[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols), label="auto single-CTA split")
+    _check(C[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols), label="auto skinny deep")

@@ -1,0 +1,172 @@
+"""GPU parity of the 3xTF32 kernel that holds B's TF32 split in tensor memory
+(GEMM_F32_TILE_128x128_TMEM): each 128 x 128 tile is computed transposed,
+D[n][m] = sum_k B[k][n] A[m][k], with B^T as the MMA's tensor-memory operand.
+
+Against the oracle, elementwise within 1e-3 + 1e-3 |C_ref| ("Lecture 12:
+final project", section 4) with NaN guard bands around C; bit-exact on the
+quantised workload; bit for bit against the staged 128 x 128 kernel without
+split-K (the same high and low parts, the same three products per K step in
+the same order, the same 128-deep promotion chunks: only the roles of the
+operands in the MMA are swapped); and run to run with split-K.
+"""
+
+import numpy as np
+import pytest
+
+import dense_fp32_gemm_row_gb300 as g
+import oracle
+from seeded_inputs import make_workload
+
+from . import _gpu
+from .test_gemm_gpu import _check, _ex_case
+
+pytestmark = pytest.mark.gpu
+
+TMEM = g.TILE_128x128_TMEM
+
+# ragged in M, N (not a multiple of the 32-column B boxes) and K; several
+# rounds of the persistent grid; K shorter than one stage
+SHAPES = [(128, 128, 32), (300, 200, 40), (1, 1, 1), (129, 33, 7), (2304, 2304, 512),
+          (2305, 2049, 1000), (2560, 2330, 77), (1025, 1023, 1000), (513, 4100, 333)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    torch = pytest.importorskip("torch")
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    g.load()
+    yield
+    g.gemm_f32_release()
+
+
+def _sample(M, N, seed, n=3000):
+    rng = np.random.default_rng(seed)
+    rows = np.concatenate([np.arange(M), rng.integers(0, M, n), np.full(N, M - 1)])
+    cols = np.concatenate([rng.integers(0, N, M), rng.integers(0, N, n), np.arange(N)])
+    return rows, cols
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_parity_and_equal_to_staged(shape):
+    M, N, K = shape
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, TMEM, 1, A=1 << 32, B=1 << 36,
+                                   C=1 << 40)
+    assert st == 0 and p["b_in_tmem"] == 1 and (p["tile_m"], p["tile_n"]) == (128, 128), p
+    # read in place unless a row stride is not a multiple of 16 bytes
+    assert p["stage_a"] == (K % 4 != 0) and p["stage_b"] == (N % 4 != 0), p
+    A, B = make_workload(2, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, TMEM, 1)
+    if M * N <= 300 * 300:
+        _check(C, oracle.ref_gemm(A, B), label=f"tmem {shape}")
+    else:
+        rows, cols = _sample(M, N, M * 3 + N + K)
+        _check(C[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols), label=f"tmem {shape}")
+    S = _gpu.run_configured(A, B, g.ALGO_3XTF32, g.TILE_128x128, 1)
+    assert np.array_equal(C.view(np.uint32), S.view(np.uint32)), \
+        f"differs from the staged kernel at {np.argwhere(C.view(np.uint32) != S.view(np.uint32))[:5]}"
+
+
+@pytest.mark.parametrize("splits", [2, 5, 38])
+def test_split_k_parity_and_determinism(splits):
+    M, N, K = 256, 256, 16384
+    A, B = make_workload(4, M=M, N=N, K=K)
+    C1 = _gpu.run_configured(A, B, g.ALGO_3XTF32, TMEM, splits)
+    _check(C1, oracle.ref_gemm(A, B), label=f"tmem split-K {splits}")
+    C2 = _gpu.run_configured(A, B, g.ALGO_3XTF32, TMEM, splits)
+    assert np.array_equal(C1.view(np.uint32), C2.view(np.uint32)), "not run-to-run deterministic"
+
+
+def test_deep_k_workload_auto():
+    # 256 x 256 x 65536: AUTO's plan is this kernel with split-K, the
+    # partials added inside the kernel (one launch, no reduction kernel)
+    A, B = make_workload(4)
+    st, p = g.gemm_f32_plan(256, 256, 65536, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["b_in_tmem"] == 1 and p["splits"] > 1, p
+    assert p["reduce_in_kernel"] == 1 and p["kernels"] == 1, p
+    C = _gpu.run(A, B, g.ALGO_AUTO)
+    _check(C, oracle.ref_gemm(A, B), label="tmem deep K (AUTO)")
+    # deterministic from call to call (the counters reset themselves)
+    for _ in range(3):
+        C2 = _gpu.run(A, B, g.ALGO_AUTO)
+        assert np.array_equal(C.view(np.uint32), C2.view(np.uint32))
+
+
+@pytest.mark.parametrize("shape,splits", [((256, 256, 16384), 5), ((300, 200, 4000), 3),
+                                          ((129, 1000, 2049), 4)],
+                         ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
+def test_in_kernel_reduction_equals_split_order_sum(shape, splits):
+    # each split's partial is the same kernel run alone on that K range (same
+    # MMAs, same promotion chunks from the start of the range), so the
+    # in-kernel reduction must equal those partials added in split order
+    M, N, K = shape
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, TMEM, splits, A=1 << 32, B=1 << 36,
+                                   C=1 << 40)
+    assert st == 0 and p["splits"] == splits and p["reduce_in_kernel"] == 1, p
+    A, B = make_workload(2, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, TMEM, splits)
+    _check(C, oracle.ref_gemm(A, B), label=f"tmem in-kernel reduction {shape} s{splits}")
+    kb = (K + 31) // 32
+    per = (kb + splits - 1) // splits
+    total = None
+    for s in range(splits):
+        k0, k1 = s * per * 32, min(K, (s + 1) * per * 32)
+        part = _gpu.run_configured(np.ascontiguousarray(A[:, k0:k1]),
+                                   np.ascontiguousarray(B[k0:k1]), g.ALGO_3XTF32, TMEM, 1)
+        total = part if total is None else (total + part).astype(np.float32)
+    assert np.array_equal(C.view(np.uint32), total.view(np.uint32)), \
+        "in-kernel sum differs from the split-order sum of the partials"
+
+
+def test_more_units_than_sms_uses_the_reduction_kernel():
+    # 40 x 40 tiles x 2 splits: CTAs take several units, so the partials go
+    # through the workspace and the reduction kernel
+    st, p = g.gemm_f32_plan_config(5120, 5120, 4096, g.ALGO_3XTF32, TMEM, 2, A=1 << 32,
+                                   B=1 << 36, C=1 << 40)
+    assert st == 0 and p["reduce_in_kernel"] == 0 and p["kernels"] == 2, p
+    M, N, K = 1280, 1408, 1024  # 110 tiles x 2 splits = 220 units > 152 SMs
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, TMEM, 2, A=1 << 32, B=1 << 36,
+                                   C=1 << 40)
+    assert st == 0 and p["reduce_in_kernel"] == 0, p
+    A, B = make_workload(1, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, TMEM, 2)
+    rows, cols = _sample(M, N, 17)
+    _check(C[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols), label="tmem s2 workspace")
+
+
+@pytest.mark.parametrize("offsets", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (3, 2, 1)])
+def test_misaligned_operands(offsets):
+    # operands TMA cannot read in place get padded copies first
+    M, N, K = 700, 900, 300
+    A, B = make_workload(1, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, TMEM, 0, offsets=offsets)
+    _check(C, oracle.ref_gemm(A, B), label=f"tmem, offsets {offsets}")
+
+
+def test_quantised_exact():
+    A, B = make_workload(0)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, TMEM, 0)
+    _check(C, oracle.ref_gemm(A, B), exact=True, label="quantised 512^3, tmem")
+
+
+@pytest.mark.parametrize("pad", [0, 4])
+def test_general_form_alpha_beta(pad):
+    # alpha/beta and leading dimensions on shapes AUTO sends to this kernel
+    # (operands read in place), with and without split-K
+    _ex_case(520, 300, 2000, 0, 0, pad, 0.5, -0.75, g.ALGO_AUTO)
+    _ex_case(256, 256, 20000, 0, 0, pad, -1.5, 0.25, g.ALGO_AUTO)
+    _ex_case(300, 200, 96, 0, 0, pad, 2.0, 0.0, g.ALGO_AUTO, c_nan=True)  # beta 0: C not read
+
+
+def test_split_reconstructs_each_operand():
+    # a 0/1 selection operand makes C reproduce each element of the other
+    # operand through the whole split-and-multiply path: to 2^-20 relative,
+    # which a tensor-core read that rounded the word would miss by up to 2^-11
+    rng = np.random.default_rng(11)
+    M, N, K = 256, 256, 256
+    X = (rng.standard_normal((M, K)) * np.exp(rng.uniform(-6, 6, (M, K)))).astype(np.float32)
+    I = np.eye(K, N, dtype=np.float32)
+    C = _gpu.run_configured(X, I, g.ALGO_3XTF32, TMEM, 1)
+    assert np.allclose(C, X, rtol=2.0 ** -20, atol=0), np.max(np.abs(C - X) / np.abs(X))
+    Y = (rng.standard_normal((K, N)) * np.exp(rng.uniform(-6, 6, (K, N)))).astype(np.float32)
+    C = _gpu.run_configured(np.eye(M, K, dtype=np.float32), Y, g.ALGO_3XTF32, TMEM, 1)
+    assert np.allclose(C, Y, rtol=2.0 ** -20, atol=0), np.max(np.abs(C - Y) / np.abs(Y))
