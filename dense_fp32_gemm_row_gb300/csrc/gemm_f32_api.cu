@@ -338,15 +338,18 @@ double single_cta_fill(int sm_count, int M, int N, int K, int bn, int splits) {
     return busy * N / (static_cast<double>(tiles_n) * bn);
 }
 
-// The split-K factor of the kernel with B's split in tensor memory: the one
-// that minimises its modelled time, rounds of the persistent grid x K blocks
-// per unit, plus for S > 1 the reduction launch (~4 us, about 6 K blocks of
-// a unit) and its traffic ((S + 1) M N floats at ~3 TB/s).  Measured: one K
-// block of a unit takes ~0.64 us (8192^3: 4392 us for 27 rounds of 256).
+// The split-K factor of the kernels with B's split in tensor memory: the one
+// that minimises their modelled time, rounds of the persistent grid (slots:
+// CTAs, or clusters of the pair form) x K blocks per unit, plus for S > 1 the
+// reduction launch (~4 us) and its traffic ((S + 1) M N floats at ~3 TB/s).
+// Measured: one K block of a 128 x 128 unit takes ~0.64 us (8192^3: 4392
+// us for 27 rounds of 256); of a 256 x 256 pair unit, ~0.8 us.
 // 1280^2 x 8192: 100 tiles, S = 3 (two rounds of 86 blocks) over S = 1 (one
 // round of 256, 52 SMs idle); 256 x 256 x 65536: 4 tiles, S = 38.
-int tmem_splits(int sm_count, int tiles, int kb_total, int M, int N) {
-    constexpr double kUsPerBlock = 0.64, kReduceLaunchUs = 4.0, kReduceBytesPerUs = 3.0e6;
+int tmem_splits(int slots, int tiles, int kb_total, int M, int N, double us_per_block) {
+    constexpr double kReduceLaunchUs = 4.0, kReduceBytesPerUs = 3.0e6;
+    const double kUsPerBlock = us_per_block;
+    const int sm_count = slots;
     int best = 1;
     double best_us = 0.0;
     const int s_max = std::min(GEMM_F32_MAX_SPLITS, std::max(1, kb_total / 4));
@@ -462,17 +465,18 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
             p->bn = 128;
         }
         if (tile != GEMM_F32_TILE_AUTO) {
-            p->pair = tile == GEMM_F32_TILE_256x256_PAIR || tile == GEMM_F32_TILE_256x256_PAIR_SPLIT;
-            p->tmem_b = tile == GEMM_F32_TILE_128x128_TMEM;
+            p->pair = tile == GEMM_F32_TILE_256x256_PAIR ||
+                      tile == GEMM_F32_TILE_256x256_PAIR_SPLIT || tile == GEMM_F32_TILE_256x256_TMEM;
+            p->tmem_b = tile == GEMM_F32_TILE_128x128_TMEM || tile == GEMM_F32_TILE_256x256_TMEM;
             p->split_in_kernel = tile == GEMM_F32_TILE_256x256_PAIR_SPLIT ||
                                  tile == GEMM_F32_TILE_128x128_SPLIT || p->tmem_b;
             p->bn = (tile == GEMM_F32_TILE_128x128 || tile == GEMM_F32_TILE_128x128_SPLIT ||
-                     p->tmem_b)
+                     tile == GEMM_F32_TILE_128x128_TMEM)
                         ? 128
                         : 256;
         }
-        const Tf32x3Config tc =
-            p->tmem_b ? tf32x3_tmem_config() : tf32x3_config(p->bn, p->pair != 0);
+        const Tf32x3Config tc = p->tmem_b ? tf32x3_tmem_config(p->pair != 0)
+                                          : tf32x3_config(p->bn, p->pair != 0);
         bm = tc.bm;
         bn = tc.bn;
         bk = tc.bk;
@@ -511,7 +515,9 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     // clusters must all fit on the device at once (single_cta_splits)
     if (p->algo == GEMM_F32_ALGO_3XTF32 && !p->pair && !p->tmem_b)
         s = single_cta_splits(d.sm_count, tiles, K, splits, p->bn);
-    if (p->tmem_b && splits == 0) s = tmem_splits(d.sm_count, tiles, kb_total, M, N);
+    if (p->tmem_b && splits == 0)
+        s = p->pair ? tmem_splits(slots, tiles, kb_total, M, N, 0.8)
+                    : tmem_splits(slots, tiles, kb_total, M, N, 0.64);
     p->kb_per_split = (kb_total + s - 1) / s;
     p->splits = (kb_total + p->kb_per_split - 1) / p->kb_per_split;
     const int units = tiles * p->splits;
@@ -571,7 +577,7 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     // those tiles into T K shares (T * tail <= clusters) so that the last
     // round takes 1/T of the time; a fix-up kernel adds the shares.
     int clusters = 0;
-    if (p->pair && p->splits == 1 && splits == 0 &&
+    if (p->pair && !p->tmem_b && p->splits == 1 && splits == 0 &&
         tf32x3_pair_clusters(d.sm_count, &clusters) == cudaSuccess && tiles > clusters) {
         const int r = tiles % clusters;
         int t = r ? clusters / r : 0;
@@ -591,7 +597,7 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     // the CTAs of a tile wait for each other's partials and each sums a band
     // of the tile's rows in split order.  No reduction launch (256 x 256 x
     // 65536, 38 splits: the separate reduction took ~8 us of a 56 us call).
-    if (p->tmem_b && p->splits > 1 && units <= d.sm_count &&
+    if (p->tmem_b && !p->pair && p->splits > 1 && units <= d.sm_count &&
         2 * tiles * static_cast<long long>(sizeof(int)) <= static_cast<long long>(kWorkspaceCounterBytes))
         p->reduce_in_kernel = 1;
     p->ws_bytes = off > kWorkspaceCounterBytes ? off : 0;
@@ -715,7 +721,9 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
             }
             if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
                 return static_cast<int>(e);
-            if ((e = launch_sgemm_3xtf32_tmem(ta, stream, d.sm_count)) != cudaSuccess)
+            ta.pair = p.pair;
+            if ((e = p.pair ? launch_sgemm_3xtf32_tmem_pair(ta, stream, d.sm_count)
+                            : launch_sgemm_3xtf32_tmem(ta, stream, d.sm_count)) != cudaSuccess)
                 return static_cast<int>(e);
             if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess)
                 return static_cast<int>(e);
@@ -1229,10 +1237,11 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
 // A forced configuration: tile id within range and valid for the algorithm.
 int check_config(const gemm_f32_config* cfg) {
     if (!cfg) return GEMM_F32_ERR_INVALID_VALUE;
-    if (cfg->tile < GEMM_F32_TILE_AUTO || cfg->tile > GEMM_F32_TILE_128x128_TMEM)
+    if (cfg->tile < GEMM_F32_TILE_AUTO || cfg->tile > GEMM_F32_TILE_256x256_TMEM)
         return GEMM_F32_ERR_INVALID_VALUE;
     if ((cfg->tile == GEMM_F32_TILE_256x256_PAIR || cfg->tile == GEMM_F32_TILE_256x256_PAIR_SPLIT ||
-         cfg->tile == GEMM_F32_TILE_128x128_SPLIT || cfg->tile == GEMM_F32_TILE_128x128_TMEM) &&
+         cfg->tile == GEMM_F32_TILE_128x128_SPLIT || cfg->tile == GEMM_F32_TILE_128x128_TMEM ||
+         cfg->tile == GEMM_F32_TILE_256x256_TMEM) &&
         cfg->algo == GEMM_F32_ALGO_FFMA)
         return GEMM_F32_ERR_INVALID_VALUE;
     if (cfg->tile != GEMM_F32_TILE_AUTO && cfg->algo == GEMM_F32_ALGO_AUTO)
@@ -1340,9 +1349,14 @@ int gemm_f32_plan_config(int M, int N, int K, const gemm_f32_config* cfg, const 
     if (p.algo == GEMM_F32_ALGO_FFMA) {
         e = ffma_ctas_per_sm(p.variant, &per_sm);
         out->threads_per_cta = ffma_config(p.variant).threads;
+    } else if (p.tmem_b && p.pair) {
+        int clusters = 0;
+        e = tf32x3_tmem_pair_clusters(d->sm_count, &clusters);
+        per_sm = d->sm_count ? (2 * clusters + d->sm_count - 1) / d->sm_count : 0;
+        out->threads_per_cta = tf32x3_tmem_config(true).threads;
     } else if (p.tmem_b) {
         e = tf32x3_tmem_ctas_per_sm(&per_sm);
-        out->threads_per_cta = tf32x3_tmem_config().threads;
+        out->threads_per_cta = tf32x3_tmem_config(false).threads;
     } else if (p.pair) {
         int clusters = 0;
         e = tf32x3_pair_clusters(d->sm_count, &clusters);

@@ -131,8 +131,12 @@ cudaError_t launch_sgemm_3xtf32(const Tf32x3Args& a, cudaStream_t s, int sm_coun
 // in tmAhi {K, M} boxes 32 x 128 and tmBhi {N, K} boxes 32 x 32, both with
 // 128-byte swizzle); out gets C, or split partials, like the kernels above.
 cudaError_t launch_sgemm_3xtf32_tmem(const Tf32x3Args& a, cudaStream_t s, int sm_count);
-Tf32x3Config tf32x3_tmem_config();
+Tf32x3Config tf32x3_tmem_config(bool pair);
 cudaError_t tf32x3_tmem_ctas_per_sm(int* ctas_per_sm);
+// Its CTA-pair form: 256 x 256 tiles (pair = 1; A {K, M} boxes 32 x 128, B
+// {N, K} boxes 32 x 32); co-resident clusters of two on the current device.
+cudaError_t launch_sgemm_3xtf32_tmem_pair(const Tf32x3Args& a, cudaStream_t s, int sm_count);
+cudaError_t tf32x3_tmem_pair_clusters(int sm_count, int* clusters);
 
 // ---- TF32 hi/lo staging (tf32_split.cu) --------------------------------------
 // hi = x as stored (read by the tensor core as trunc(x)), lo = tf32(x - trunc(x)).

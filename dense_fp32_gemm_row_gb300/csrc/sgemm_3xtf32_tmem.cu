@@ -478,6 +478,402 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
     }
 }
 
+// ============================================================================
+// The CTA-pair form: a cluster of two CTAs computes a 256 x 256 tile with
+// tcgen05.mma.cta_group::2 (M = 256 tile columns n across the pair, N = 256
+// tile rows m, K = 8), B^T in tensor memory, A in shared memory.  CTA rank r
+// holds tile columns n0 + 128 r .. in its tensor-memory lanes and tile rows
+// m0 + 128 r .. of A in its shared memory; each MMA reads half of its
+// shared-memory operand from each SM.  N = 256 MMAs run at the tensor
+// core's full rate (a microbenchmark: 1215 TFLOP/s tf32 with A in tensor
+// memory, against 841 for the N = 128 MMAs of the single-CTA form), but the
+// 256-column accumulator then fits only once beside four 64-column operand
+// stages: it is single-buffered, and the MMA lane waits at the start of each
+// chunk until both epilogues have drained the previous one (measured: 5 %
+// of the MMA rate at 128-deep chunks).
+//
+// 512 threads per CTA, four warpgroups, registers rebalanced at start
+// (launched at 128 per thread): warpgroups 0-1 down to 56, the two epilogue
+// warpgroups up to 200 (2 x 128 x 56 + 2 x 128 x 200 = 65536), so that an
+// epilogue thread can hold 64 loaded values beside its 128 sums:
+//   warp 0      one lane: TMA loads of the stage (A {32 k, 128 m}, four B
+//               boxes {32 n, 32 k}) onto this CTA's own full barrier;
+//   warp 1      tensor-memory allocation for the pair; in the leader, one
+//               lane issues the MMAs and multicasts the commits;
+//   warps 2-3   split A in shared memory (stage fills in turn), arriving on
+//               this CTA's A-converted barrier;
+//   warps 4-7   split B into this CTA's tensor memory (warp 4 + q: lanes
+//               32 q ..), arriving on this CTA's B-converted barrier; in the
+//               peer, one lane of warp 1 relays both to the leader (one
+//               cluster-scope arrival per stage fill);
+//   warps 8-15  the epilogue: warp 8 + e drains lanes 32 (e % 4) .., columns
+//               128 (e / 4) .. of the accumulator and arrives on the
+//               leader's acc-empty barrier.
+// ============================================================================
+struct TmemPairCfg {
+    static constexpr int TN = 256;                 // tile columns n (lanes across the pair)
+    static constexpr int TM = 256;                 // tile rows m (MMA N)
+    static constexpr int HALF = 128;               // per CTA
+    static constexpr int STAGES = 4;
+    static constexpr int A_BYTES = HALF * BK * 4;
+    static constexpr int B_BYTES = HALF * BK * 4;
+    static constexpr int B_BOX_BYTES = 32 * BK * 4;
+    static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;  // A, A lo, B
+    static constexpr int NSPLIT_A = 2;
+    static constexpr int NFULL = STAGES * NSPLIT_A;
+    static constexpr int THREADS = 512;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int D_COLS = TM;              // one accumulator: m
+    static constexpr int OP_COL0 = D_COLS;         // operand stage s at OP_COL0 + 64 s
+    static constexpr int OP_COLS = 2 * BK;
+    static constexpr int EPI_WARPS = 8;
+    // full (NFULL), empty, A converted, B converted, peer ready (per
+    // stage), acc_full, acc_empty, drain
+    static constexpr int NBARS = NFULL + 4 * STAGES + 3;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NBARS * 8 + 16 + 1024;
+    static constexpr uint32_t IDESC = idesc_tf32_f32(TN, TM);
+    static constexpr int REGS_LOW = 56, REGS_HIGH = 200;
+    static constexpr int DRAIN_BATCH = 4;  // 16-column loads in flight per wait
+    static_assert(2 * 128 * REGS_LOW + 2 * 128 * REGS_HIGH == 65536, "register shares");
+    static_assert(OP_COL0 + STAGES * OP_COLS <= TMEM_COLS, "tensor-memory columns");
+    static_assert(A_BYTES == 16384, "split_a_stage's map");
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
+
+__global__ void __launch_bounds__(TmemPairCfg::THREADS, 1)
+sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                              const __grid_constant__ CUtensorMap tmB, float* __restrict__ out,
+                              long long ldo, long long split_stride, int M, int N, int K,
+                              int kb_per_split, int splits, unsigned* fault,
+                              long long timeout_ns, float alpha, float beta, int scale_mode) {
+    using C = TmemPairCfg;
+    constexpr int STAGES = C::STAGES;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t full0 = sbase + STAGES * C::STAGE_BYTES;  // own: + 8 f
+    const uint32_t empty0 = full0 + 8 * C::NFULL;            // own, multicast commit: + 8 s
+    const uint32_t aconv0 = empty0 + 8 * STAGES;             // own: the A splitter warp
+    const uint32_t bconv0 = aconv0 + 8 * STAGES;             // own: 4 B splitter warps
+    const uint32_t peer0 = bconv0 + 8 * STAGES;              // leader: the peer's relay
+    const uint32_t accf = peer0 + 8 * STAGES;                // own, multicast commit
+    const uint32_t acce = accf + 8;                          // leader: 8 warps x 2 CTAs
+    const uint32_t drain = acce + 8;
+    uint32_t* tmem_slot =
+        reinterpret_cast<uint32_t*>(smem + STAGES * C::STAGE_BYTES + C::NBARS * 8);
+    const uint32_t abort_flag = smem_addr(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int cluster = blockIdx.x >> 1;
+    const int nclusters = gridDim.x >> 1;
+    const int tiles_m = (M + C::TM - 1) / C::TM;
+    const int tiles_n = (N + C::TN - 1) / C::TN;
+    const int units = tiles_m * tiles_n * splits;
+    const int kb_total = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        for (int f = 0; f < C::NFULL; ++f) mbar_init(full0 + 8 * f, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(aconv0 + 8 * s, 1);
+            mbar_init(bconv0 + 8 * s, 4);
+            mbar_init(peer0 + 8 * s, 1);
+        }
+        mbar_init(accf, 1);
+        mbar_init(acce, 2 * C::EPI_WARPS);
+        mbar_init(drain, 1);
+        st_shared_volatile(abort_flag, 0u);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_addr(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp < 8) {
+        // warpgroups 0-1 give registers to the epilogue warpgroups
+        regs_dec<C::REGS_LOW>();
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------ TMA producer (both CTAs) ------------------
+            int it = 0;
+            bool ok = true;
+            for (int u = cluster; u < units && ok; u += nclusters) {
+                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
+                const int ma = w.m0 + static_cast<int>(rank) * C::HALF;
+                const int nb = w.n0 + static_cast<int>(rank) * C::HALF;
+                for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    if (it >= STAGES &&
+                        !role_wait(empty0 + 8 * s, ((it / STAGES) & 1) ^ 1, timeout_ns, fault,
+                                   kFaultEmptyBarrier, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = sbase + s * C::STAGE_BYTES;
+                    const int k0 = (w.kb_begin + kb) * BK;
+                    const uint32_t fb = full0 + 8 * (it % C::NFULL);
+                    mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES);
+                    tma_load_2d(st, &tmA, fb, k0, ma);
+#pragma unroll
+                    for (int j = 0; j < C::HALF / 32; ++j)
+                        tma_load_2d(st + 2 * C::A_BYTES + j * C::B_BOX_BYTES, &tmB, fb,
+                                    nb + 32 * j, k0);
+                    if (kb + kPrefetchAhead < w.nkb) {
+                        const int kp = k0 + kPrefetchAhead * BK;
+                        tma_prefetch_2d(&tmA, kp, ma);
+#pragma unroll
+                        for (int j = 0; j < C::HALF / 32; ++j)
+                            tma_prefetch_2d(&tmB, nb + 32 * j, kp);
+                    }
+                }
+            }
+            // wind down: this CTA's copies have landed and its stages have been
+            // released by the MMAs
+            const long long tail = ok ? timeout_ns : timeout_ns / 8 + 1000;
+            for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j) {
+                mbar_wait(full0 + 8 * (j % C::NFULL), (j / C::NFULL) & 1, tail, fault,
+                          kFaultDrain);
+                mbar_wait(empty0 + 8 * (j % STAGES), (j / STAGES) & 1, tail, fault, kFaultDrain);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // ------------------------------ MMA issuer (leader) -----------------------
+            int it = 0;
+            int g = 0;  // chunks issued
+            bool ok = true;
+            for (int u = cluster; u < units && ok; u += nclusters) {
+                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
+                for (int c0 = 0; c0 < w.nkb && ok; c0 += CH, ++g) {
+                    // the single accumulator: both epilogues have drained chunk g - 1
+                    if (g >= 1 && !role_wait(acce, (g - 1) & 1, timeout_ns, fault,
+                                             kFaultAccumBarrier, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int c1 = min(w.nkb, c0 + CH);
+                    for (int kb = c0; kb < c1; ++kb, ++it) {
+                        const int s = it % STAGES;
+                        const uint32_t par = (it / STAGES) & 1;
+                        // this CTA's splitters (CTA scope), then the peer's,
+                        // relayed by one lane there (cluster scope)
+                        if (!role_wait(aconv0 + 8 * s, par, timeout_ns, fault, kFaultFullBarrier,
+                                       abort_flag) ||
+                            !role_wait(bconv0 + 8 * s, par, timeout_ns, fault, kFaultFullBarrier,
+                                       abort_flag) ||
+                            !role_wait(peer0 + 8 * s, par, timeout_ns, fault, kFaultFullBarrier,
+                                       abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t st = sbase + s * C::STAGE_BYTES;
+                        const uint64_t a_hi = smem_desc_sw128_kmajor(st);
+                        const uint64_t a_lo = smem_desc_sw128_kmajor(st + C::A_BYTES);
+                        const uint32_t b_hi =
+                            tmem_base + static_cast<uint32_t>(C::OP_COL0 + C::OP_COLS * s);
+                        const uint32_t b_lo = b_hi + BK;
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k) {
+                            const uint64_t off = static_cast<uint64_t>(k * UMMA_K * 4) >> 4;
+                            const uint32_t kc = static_cast<uint32_t>(k * UMMA_K);
+                            const uint32_t acc = (kb > c0 || k > 0) ? 1u : 0u;
+                            mma_tf32_pair_tmem_a(tmem_base, b_hi + kc, a_lo + off, C::IDESC, acc);
+                            mma_tf32_pair_tmem_a(tmem_base, b_lo + kc, a_hi + off, C::IDESC, 1u);
+                            mma_tf32_pair_tmem_a(tmem_base, b_hi + kc, a_hi + off, C::IDESC, 1u);
+                        }
+                        mma_commit_pair_multicast(empty0 + 8 * s, 0x3);
+                    }
+                    if (!ok) break;
+                    mma_commit_pair_multicast(accf, 0x3);
+                }
+            }
+            mma_commit_pair(drain);
+            mbar_wait(drain, 0, ok ? timeout_ns : timeout_ns / 8 + 1000, fault, kFaultDrain);
+        } else if (lane == 0) {
+            // ------------------------------ relay (peer CTA) --------------------------
+            // One cluster-scope arrival per stage fill on the leader, once this
+            // CTA's splitters have arrived on its own barriers (a release at
+            // cluster scope by every splitter warp stalled them on memory
+            // barriers: 1.25 us a fill against 0.79 us of MMA work, 4096^3).
+            const uint32_t peer_leader = map_to_cta(peer0, 0);
+            int it = 0;
+            bool ok = true;
+            for (int u = cluster; u < units && ok; u += nclusters) {
+                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
+                for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t par = (it / STAGES) & 1;
+                    if (!role_wait(aconv0 + 8 * s, par, timeout_ns, fault, kFaultFullBarrier,
+                                   abort_flag) ||
+                        !role_wait(bconv0 + 8 * s, par, timeout_ns, fault, kFaultFullBarrier,
+                                   abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_cluster(peer_leader + 8 * s);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------ A splitters (warps 2-3, both CTAs) --------
+        int it = 0;
+        bool ok = true;
+        for (int u = cluster; u < units && ok; u += nclusters) {
+            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
+            for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+                if (it % C::NSPLIT_A != warp - 2) continue;
+                const int s = it % STAGES;
+                const bool got = role_wait(full0 + 8 * (it % C::NFULL), (it / C::NFULL) & 1,
+                                           timeout_ns, fault, kFaultFullBarrier, abort_flag);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t st = sbase + s * C::STAGE_BYTES;
+                split_a_stage(st, lane);
+                split_a_stage(st, lane + 32);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(aconv0 + 8 * s);
+            }
+        }
+        __syncwarp();
+    } else if (warp < 8) {
+        // ------------------------------ B splitters (warps 4-7, both CTAs) --------
+        const int q = warp & 3;
+        const uint32_t chunk = static_cast<uint32_t>(lane >> 2);
+        const uint32_t word = static_cast<uint32_t>(lane & 3) * 4u;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+        int it = 0;
+        bool ok = true;
+        for (int u = cluster; u < units && ok; u += nclusters) {
+            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
+            for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+                const int s = it % STAGES;
+                const bool got = role_wait(full0 + 8 * (it % C::NFULL), (it / C::NFULL) & 1,
+                                           timeout_ns, fault, kFaultFullBarrier, abort_flag);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t box =
+                    sbase + s * C::STAGE_BYTES + 2 * C::A_BYTES + q * C::B_BOX_BYTES;
+                const uint32_t col =
+                    lane_base + static_cast<uint32_t>(C::OP_COL0 + C::OP_COLS * s);
+                // eight k at a time: this warpgroup runs on 56 registers
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t r = static_cast<uint32_t>(8 * h + i);
+                        const float x = lds32(box + r * 128u + ((chunk ^ (r & 7u)) << 4) + word);
+                        hi[i] = __float_as_uint(x) & 0xFFFFE000u;
+                        lo[i] = __float_as_uint(to_tf32(x - __uint_as_float(hi[i])));
+                    }
+                    tmem_st_32x32b_x8(col + 8u * h, hi);
+                    tmem_st_32x32b_x8(col + BK + 8u * h, lo);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bconv0 + 8 * s);
+            }
+        }
+        __syncwarp();
+    }
+    } else {
+        // ------------------------------ epilogue (warps 8-15, both CTAs) ----------
+        regs_inc<C::REGS_HIGH>();
+        const int e = warp - 8;
+        const int q = warp & 3;                 // lanes 32 q .. 32 q + 31
+        const int col0 = (e >> 2) * EPI_COLS;   // accumulator columns (tile rows m)
+        const int nl = static_cast<int>(rank) * C::HALF + 32 * q + lane;  // tile column
+        const uint32_t acce_leader = map_to_cta(acce, 0);
+        float acc[EPI_COLS];
+        int g = 0;
+        bool ok = true;
+        for (int u = cluster; u < units && ok; u += nclusters) {
+            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
+            for (int c0 = 0; c0 < w.nkb; c0 += CH, ++g) {
+                const bool got = role_wait(accf, g & 1, timeout_ns, fault, kFaultAccumBarrier,
+                                           abort_flag);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                                       static_cast<uint32_t>(col0);
+                // the MMA lane waits for this drain (one accumulator): keep
+                // DRAIN_BATCH loads in flight per wait (one at a time, the
+                // eight round trips took ~1.07 us a chunk)
+#pragma unroll
+                for (int j0 = 0; j0 < EPI_COLS / 16; j0 += C::DRAIN_BATCH) {
+                    uint32_t r[C::DRAIN_BATCH][16];
+#pragma unroll
+                    for (int b = 0; b < C::DRAIN_BATCH; ++b)
+                        tmem_ld_32x32b_x16(tbase + 16 * (j0 + b), r[b]);
+#pragma unroll
+                    for (int b = 0; b < C::DRAIN_BATCH; ++b) tmem_ld_wait(r[b]);
+#pragma unroll
+                    for (int b = 0; b < C::DRAIN_BATCH; ++b) {
+                        const int j = j0 + b;
+                        if (c0 == 0) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) acc[16 * j + i] = __uint_as_float(r[b][i]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) acc[16 * j + i] += __uint_as_float(r[b][i]);
+                        }
+                    }
+                }
+                // the loads have completed: the arrival hands the accumulator
+                // back and orders no writes, so CTA-scope release suffices
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(acce_leader);
+            }
+            if (!ok) break;
+            const int n = w.n0 + nl;
+            if (n < N) {
+                float* p = out + static_cast<long long>(w.split) * split_stride +
+                           static_cast<long long>(w.m0 + col0) * ldo + n;
+                const int rows = M - (w.m0 + col0);
+#pragma unroll
+                for (int j = 0; j < EPI_COLS; ++j, p += ldo)
+                    if (j < rows) *p = scale1(acc[j], p, alpha, beta, scale_mode);
+            }
+        }
+        __syncwarp();
+    }
+
+    // neither CTA may leave while its partner can still reach its shared or
+    // tensor memory
+    tc_fence_before();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_sgemm_3xtf32_tmem(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
@@ -515,7 +911,11 @@ cudaError_t launch_sgemm_3xtf32_tmem(const Tf32x3Args& a, cudaStream_t s, int sm
     return cudaGetLastError();
 }
 
-Tf32x3Config tf32x3_tmem_config() {
+Tf32x3Config tf32x3_tmem_config(bool pair) {
+    if (pair) {
+        using P = TmemPairCfg;
+        return {P::TM, P::TN, BK, P::STAGES, P::THREADS, P::SMEM_BYTES, 1, 32};
+    }
     using C = TmemCfg;
     return {BM, C::BN, BK, C::STAGES, C::THREADS, C::SMEM_BYTES, 0, 32};
 }
@@ -528,6 +928,69 @@ cudaError_t tf32x3_tmem_ctas_per_sm(int* ctas_per_sm) {
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, sgemm_3xtf32_tmem_kernel,
                                                          C::THREADS, C::SMEM_BYTES);
+}
+
+
+// Co-resident clusters of the pair form on this device (cached per device).
+cudaError_t tf32x3_tmem_pair_clusters(int sm_count, int* out) {
+    using C = TmemPairCfg;
+    static thread_local int done_dev = -1;
+    static thread_local int clusters = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (done_dev != dev) {
+        e = cudaFuncSetAttribute(sgemm_3xtf32_tmem_pair_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * (sm_count / 2));
+        cfg.blockDim = dim3(C::THREADS);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, sgemm_3xtf32_tmem_pair_kernel, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        clusters = n;
+        done_dev = dev;
+    }
+    *out = clusters;
+    return cudaSuccess;
+}
+
+cudaError_t launch_sgemm_3xtf32_tmem_pair(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
+    using C = TmemPairCfg;
+    if (!a.pair || a.cluster_splits || a.tail_tiles || a.counters) return cudaErrorInvalidValue;
+    int max_clusters = 0;
+    cudaError_t e = tf32x3_tmem_pair_clusters(sm_count, &max_clusters);
+    if (e != cudaSuccess) return e;
+    const int units = ((a.M + C::TM - 1) / C::TM) * ((a.N + C::TN - 1) / C::TN) * a.splits;
+    const int clusters = units < max_clusters ? units : max_clusters;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, sgemm_3xtf32_tmem_pair_kernel, a.tmAhi, a.tmBhi, a.out, a.ldo,
+                           a.split_stride, a.M, a.N, a.K, a.kb_per_split, a.splits, a.fault,
+                           a.timeout_ns, a.alpha, a.beta, a.scale_mode);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 }  // namespace gemm_f32_impl

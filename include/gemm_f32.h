@@ -231,7 +231,8 @@ int gemm_f32_plan(int M, int N, int K, int algo, int splits,
  * shared memory and B into tensor memory, where the MMA takes B^T as its
  * operand, and computes each 128 x 128 tile transposed (no staging pass and
  * no transpose in shared memory; AUTO's choice for operands read in place
- * up to 2 M N / (M + N) of 2560).  Invalid combinations return
+ * up to 2 M N / (M + N) of 2560).  _256x256_TMEM is its CTA-pair form
+ * (256 x 256 tiles, N = 256 MMAs).  Invalid combinations return
  * GEMM_F32_ERR_INVALID_VALUE.
  */
 #define GEMM_F32_TILE_AUTO          0
@@ -241,6 +242,7 @@ int gemm_f32_plan(int M, int N, int K, int algo, int splits,
 #define GEMM_F32_TILE_256x256_PAIR_SPLIT 4
 #define GEMM_F32_TILE_128x128_SPLIT 5
 #define GEMM_F32_TILE_128x128_TMEM  6
+#define GEMM_F32_TILE_256x256_TMEM  7
 typedef struct gemm_f32_config {
     int algo;
     int tile;

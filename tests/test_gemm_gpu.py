@@ -382,9 +382,10 @@ def test_general_form_on_the_pair_kernel():
                                        (g.ALGO_3XTF32, g.TILE_256x256_PAIR),
                                        (g.ALGO_3XTF32, g.TILE_256x256_PAIR_SPLIT),
                                        (g.ALGO_3XTF32, g.TILE_128x128_SPLIT),
-                                       (g.ALGO_3XTF32, g.TILE_128x128_TMEM)],
+                                       (g.ALGO_3XTF32, g.TILE_128x128_TMEM),
+                                       (g.ALGO_3XTF32, g.TILE_256x256_TMEM)],
                          ids=["ffma-128", "ffma-256", "3x-128", "3x-256", "3x-pair", "3x-pair-split",
-                              "3x-128-split", "3x-128-tmem"])
+                              "3x-128-split", "3x-128-tmem", "3x-pair-tmem"])
 @pytest.mark.parametrize("splits", [1, 5])
 def test_forced_configurations(algo, tile, splits):
     t = _gpu.torch()
@@ -394,7 +395,8 @@ def test_forced_configurations(algo, tile, splits):
     assert st == 0 and p["algo"] == algo and p["splits"] == splits
     want_tile = {g.TILE_128x128: (128, 128), g.TILE_128x256: (128, 256),
                  g.TILE_256x256_PAIR: (256, 256), g.TILE_256x256_PAIR_SPLIT: (256, 256),
-                 g.TILE_128x128_SPLIT: (128, 128), g.TILE_128x128_TMEM: (128, 128)}[tile]
+                 g.TILE_128x128_SPLIT: (128, 128), g.TILE_128x128_TMEM: (128, 128),
+                 g.TILE_256x256_TMEM: (256, 256)}[tile]
     assert (p["tile_m"], p["tile_n"]) == want_tile
     a = t.from_numpy(A).cuda()
     b = t.from_numpy(B).cuda()
@@ -419,7 +421,9 @@ def test_invalid_configurations_are_refused():
                                  0) == g.ERR_INVALID_VALUE
     assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_FFMA, g.TILE_128x128_TMEM,
                                  0) == g.ERR_INVALID_VALUE
-    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_3XTF32, 7, 0) == g.ERR_INVALID_VALUE
+    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_FFMA, g.TILE_256x256_TMEM,
+                                 0) == g.ERR_INVALID_VALUE
+    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_3XTF32, 8, 0) == g.ERR_INVALID_VALUE
     assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_3XTF32, -1, 0) == g.ERR_INVALID_VALUE
 
 

@@ -170,3 +170,49 @@ def test_split_reconstructs_each_operand():
     Y = (rng.standard_normal((K, N)) * np.exp(rng.uniform(-6, 6, (K, N)))).astype(np.float32)
     C = _gpu.run_configured(np.eye(M, K, dtype=np.float32), Y, g.ALGO_3XTF32, TMEM, 1)
     assert np.allclose(C, Y, rtol=2.0 ** -20, atol=0), np.max(np.abs(C - Y) / np.abs(Y))
+
+
+# ---- the CTA-pair form: 256 x 256 tiles, N = 256 MMAs, one accumulator ----
+PAIR = g.TILE_256x256_TMEM
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_pair_parity_and_equal_to_single(shape):
+    # the same products per output in the same order and the same 128-deep
+    # promotion chunks as the single-CTA form, so the same bits
+    M, N, K = shape
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, PAIR, 1, A=1 << 32, B=1 << 36,
+                                   C=1 << 40)
+    assert st == 0 and p["b_in_tmem"] == 1 and (p["tile_m"], p["tile_n"]) == (256, 256), p
+    A, B = make_workload(2, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, PAIR, 1)
+    if M * N <= 300 * 300:
+        _check(C, oracle.ref_gemm(A, B), label=f"tmem pair {shape}")
+    else:
+        rows, cols = _sample(M, N, M * 5 + N + K)
+        _check(C[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols),
+               label=f"tmem pair {shape}")
+    S = _gpu.run_configured(A, B, g.ALGO_3XTF32, TMEM, 1)
+    assert np.array_equal(C.view(np.uint32), S.view(np.uint32)), \
+        f"differs from the single-CTA form at {np.argwhere(C.view(np.uint32) != S.view(np.uint32))[:5]}"
+
+
+@pytest.mark.parametrize("splits", [2, 7])
+def test_pair_split_k(splits):
+    M, N, K = 520, 700, 6000
+    A, B = make_workload(1, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, PAIR, splits)
+    _check(C, oracle.ref_gemm(A, B), label=f"tmem pair split-K {splits}")
+    C2 = _gpu.run_configured(A, B, g.ALGO_3XTF32, PAIR, splits)
+    assert np.array_equal(C.view(np.uint32), C2.view(np.uint32)), "not run-to-run deterministic"
+
+
+def test_pair_quantised_exact_and_misaligned():
+    A, B = make_workload(0)
+    _check(_gpu.run_configured(A, B, g.ALGO_3XTF32, PAIR, 0), oracle.ref_gemm(A, B), exact=True,
+           label="quantised 512^3, tmem pair")
+    M, N, K = 700, 900, 300
+    A, B = make_workload(1, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, PAIR, 0, offsets=(3, 2, 1))
+    _check(C, oracle.ref_gemm(A, B), label="tmem pair, misaligned operands")
+
