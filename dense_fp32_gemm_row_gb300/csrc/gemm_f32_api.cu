@@ -441,14 +441,13 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
             else if (u128 > 1.1 * u256) p->bn = 128;
         }
         // A and B read as stored (K-contiguous A and N-contiguous B rows,
-        // 16-byte row strides and bases): the 128 x 128 kernel with B's split
-        // in tensor memory needs no staging pass and no transpose in shared
-        // memory, and beats the staged kernels up to 2 M N / (M + N) of about
-        // 2560 (the boundary sweep: 256 x 256 x 65536 51.9 against 66.2 us,
-        // 896^2 x 4096 39.6 against 58.0, 1024^2 x 8192 90.8 against 105.1,
-        // 2048^3 86.7 against 88.7, 2560^3 154.3 against 158.4); beyond
-        // that the two-CTA kernel's N = 256 MMAs win (3072^3 234.1 against
-        // 240.3 us, 4096^3 520.8 against 543.4).  It also beat the two
+        // 16-byte row strides and bases): the kernels with B's split in
+        // tensor memory need no staging pass and no transpose in shared
+        // memory.  The single-CTA 128 x 128 form beat the staged kernels up
+        // to 2 M N / (M + N) of about 2560 (the boundary sweep: 256 x 256 x
+        // 65536 51.9 against 66.2 us, 896^2 x 4096 39.6 against 58.0, 1024^2
+        // x 8192 90.8 against 105.1, 2048^3 86.7 against 88.7, 2560^3 154.3
+        // against 158.4), and its pair form beats them beyond.  It also beat the two
         // kernels that split A and B in shared memory (the pair and the
         // single-CTA 128 x 128 one, now forced configurations only) on every
         // shape they were chosen for (89 x 1216 x 24336 47.7 against 74.4
@@ -458,11 +457,23 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         const double per_element = 2.0 * M * N / (static_cast<double>(M) + N);
         const bool in_place = !q.ta && !q.tb && q.lda % 4 == 0 && q.ldb % 4 == 0 &&
                               !misaligned16(q.A) && !misaligned16(q.B);
-        if (in_place && per_element <= 2560.0) {
+        if (in_place) {
+            // and its CTA-pair form (256 x 256 tiles, N = 256 MMAs, 256-deep
+            // promotion chunks) once its tiles fill half the SM pairs: 8192^3
+            // 3.18 against 3.53 ms staged, 3072^3 205 against 234 us, 2048^3
+            // 76 against 89 us; fewer, deeper tiles keep the single-CTA form,
+            // which adds its split-K partials inside the kernel (256 x 256 x
+            // 65536: 51.9 against 53.4 us)
+            int clusters = 0;
+            const int tiles_pair = ((M + 255) / 256) * ((N + 255) / 256);
+            const bool pair_fills =
+                tf32x3_tmem_pair_clusters(d.sm_count, &clusters) == cudaSuccess &&
+                2 * tiles_pair >= clusters;
+            cudaGetLastError();
             p->tmem_b = 1;
-            p->pair = 0;
+            p->pair = pair_fills ? 1 : 0;
             p->split_in_kernel = 1;
-            p->bn = 128;
+            p->bn = pair_fills ? 256 : 128;
         }
         if (tile != GEMM_F32_TILE_AUTO) {
             p->pair = tile == GEMM_F32_TILE_256x256_PAIR ||
@@ -577,8 +588,10 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     // those tiles into T K shares (T * tail <= clusters) so that the last
     // round takes 1/T of the time; a fix-up kernel adds the shares.
     int clusters = 0;
-    if (p->pair && !p->tmem_b && p->splits == 1 && splits == 0 &&
-        tf32x3_pair_clusters(d.sm_count, &clusters) == cudaSuccess && tiles > clusters) {
+    if (p->pair && p->splits == 1 && splits == 0 &&
+        (p->tmem_b ? tf32x3_tmem_pair_clusters(d.sm_count, &clusters)
+                   : tf32x3_pair_clusters(d.sm_count, &clusters)) == cudaSuccess &&
+        tiles > clusters) {
         const int r = tiles % clusters;
         int t = r ? clusters / r : 0;
         if (t > 4) t = 4;
@@ -593,11 +606,14 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     }
     cudaGetLastError();
     // The kernel with B's split in tensor memory adds its partials itself when
-    // every CTA has exactly one unit (all co-resident, a cooperative launch):
-    // the CTAs of a tile wait for each other's partials and each sums a band
-    // of the tile's rows in split order.  No reduction launch (256 x 256 x
-    // 65536, 38 splits: the separate reduction took ~8 us of a 56 us call).
-    if (p->tmem_b && !p->pair && p->splits > 1 && units <= d.sm_count &&
+    // every CTA has exactly one unit (all co-resident, a cooperative launch)
+    // and there are at least 16 of them: the CTAs of a tile wait for each
+    // other's partials and each sums a band of the tile's rows in split
+    // order.  No reduction launch (256 x 256 x 65536, 38 splits: one launch
+    // of ~52 us against ~51-56 us for the kernel and a separate reduction);
+    // with few splits the cooperative launch costs more than the reduction
+    // launch it saves (512^3, 4 splits: ~25 against ~17 us).
+    if (p->tmem_b && !p->pair && p->splits >= 16 && units <= d.sm_count &&
         2 * tiles * static_cast<long long>(sizeof(int)) <= static_cast<long long>(kWorkspaceCounterBytes))
         p->reduce_in_kernel = 1;
     p->ws_bytes = off > kWorkspaceCounterBytes ? off : 0;
@@ -722,6 +738,11 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
             if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess)
                 return static_cast<int>(e);
             ta.pair = p.pair;
+            // the tail split names tiles of the extent it was planned for
+            const bool tail = p.tail_tiles && M == p.tail_m && N == p.tail_n;
+            ta.tail_tiles = tail ? p.tail_tiles : 0;
+            ta.tail_splits = tail ? p.tail_splits : 0;
+            ta.tail_ws = tail ? reinterpret_cast<float*>(ws + p.off_t) : nullptr;
             if ((e = p.pair ? launch_sgemm_3xtf32_tmem_pair(ta, stream, d.sm_count)
                             : launch_sgemm_3xtf32_tmem(ta, stream, d.sm_count)) != cudaSuccess)
                 return static_cast<int>(e);
@@ -1104,12 +1125,25 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
     // are on the device (B's blocks are staged into the full B^T planes, so
     // the middle panels reuse them), and the last panel's blocks go back to
     // the host one by one, so only the last block's copy is not overlapped.
+    // With B's split in tensor memory there is nothing to stage: a block's
+    // GEMM reads its columns of B where they landed (row stride N).
     const int nc = static_cast<int>(round_up((N + 3) / 4, 256));
     const int nblk = (N + nc - 1) / nc;
     Plan pc;
+    const bool tmem_blocks = p.algo == GEMM_F32_ALGO_3XTF32 && p.tmem_b && p.splits == 1 &&
+                             panels >= 2 && N >= 1024 && nblk >= 2 && nblk <= kMaxColBlocks;
     bool col_blocks = p.algo == GEMM_F32_ALGO_3XTF32 && !p.split_in_kernel && p.splits == 1 &&
                       panels >= 2 && N >= 1024 && nblk >= 2 && nblk <= kMaxColBlocks;
-    if (col_blocks) {
+    if (tmem_blocks) {
+        Problem qc = qp;
+        qc.N = nc;
+        qc.ldb = N;
+        qc.ldc = N;
+        make_plan(*d, qc, GEMM_F32_ALGO_3XTF32, 0, &pc);
+        col_blocks = pc.tmem_b && pc.splits == 1;
+        pc.off_w += p.ws_bytes;
+        pc.off_t += p.ws_bytes;
+    } else if (col_blocks) {
         Problem qc = qp;
         qc.N = nc;
         // the two-CTA kernel for a block (2048 x 2048: 64 pair tiles in one
@@ -1178,10 +1212,11 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
             GEMM_F32_TRY(cudaEventRecord(hp->ev_a[i], hp->s_in));
         }
         Operands o;
-        float* bt_hi = reinterpret_cast<float*>(ws + p.off_b);
-        float* bt_lo = reinterpret_cast<float*>(ws + p.off_b2);
+        float* bt_hi = tmem_blocks ? nullptr : reinterpret_cast<float*>(ws + p.off_b);
+        float* bt_lo = tmem_blocks ? nullptr : reinterpret_cast<float*>(ws + p.off_b2);
         o.b_hi = bt_hi;
         o.b_lo = bt_lo;
+        o.b = dB;
         for (int i = 0; i < panels; ++i) {
             const int r0 = i * P;
             const int mp = (M - r0) < P ? (M - r0) : P;
@@ -1192,16 +1227,21 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
                 for (int c = 0; c < nblk; ++c) {
                     const int c0 = c * nc, w = (N - c0) < nc ? (N - c0) : nc;
                     if (i == 0) {
-                        // stage this block of B into rows c0.. of the B^T planes
                         GEMM_F32_TRY(cudaStreamWaitEvent(stream, hp->ev_bblk[c], 0));
-                        GEMM_F32_TRY(launch_split_transpose(dB + c0, N, K, w,
-                                                            bt_hi + static_cast<size_t>(c0) * p.ldb,
-                                                            bt_lo + static_cast<size_t>(c0) * p.ldb,
-                                                            p.ldb, stream));
+                        // staged operands: this block of B into rows c0.. of
+                        // the B^T planes
+                        if (!tmem_blocks)
+                            GEMM_F32_TRY(launch_split_transpose(
+                                dB + c0, N, K, w, bt_hi + static_cast<size_t>(c0) * p.ldb,
+                                bt_lo + static_cast<size_t>(c0) * p.ldb, p.ldb, stream));
                     }
                     Operands ob = o;
-                    ob.b_hi = bt_hi + static_cast<size_t>(c0) * p.ldb;
-                    ob.b_lo = bt_lo + static_cast<size_t>(c0) * p.ldb;
+                    if (tmem_blocks) {
+                        ob.b = dB + c0;
+                    } else {
+                        ob.b_hi = bt_hi + static_cast<size_t>(c0) * p.ldb;
+                        ob.b_lo = bt_lo + static_cast<size_t>(c0) * p.ldb;
+                    }
                     if ((st = launch_gemm(pc, *d, ob, dC + off_c + c0, N, mp, w, K, 1.0f, 0.0f, 0,
                                           ws, stream, nullptr, nullptr)) != GEMM_F32_SUCCESS)
                         return st;

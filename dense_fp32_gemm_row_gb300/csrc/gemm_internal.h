@@ -136,6 +136,9 @@ cudaError_t tf32x3_tmem_ctas_per_sm(int* ctas_per_sm);
 // Its CTA-pair form: 256 x 256 tiles (pair = 1; A {K, M} boxes 32 x 128, B
 // {N, K} boxes 32 x 32); co-resident clusters of two on the current device.
 cudaError_t launch_sgemm_3xtf32_tmem_pair(const Tf32x3Args& a, cudaStream_t s, int sm_count);
+// Adds the tail shares of a pair kernel's K-split last round (tail_ws) into
+// C (out, ldo) in share order, with alpha/beta.
+cudaError_t launch_pair_tail_fixup(const Tf32x3Args& a, cudaStream_t s);
 cudaError_t tf32x3_tmem_pair_clusters(int sm_count, int* clusters);
 
 // ---- TF32 hi/lo staging (tf32_split.cu) --------------------------------------

@@ -117,27 +117,6 @@ struct Cfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
-// Work units of the pair kernel.  Without a tail (tail_tiles == 0) they are
-// (tile, split) pairs as above.  With one, the last tail_tiles tiles of the
-// raster (what would otherwise be a partly idle last round of the persistent
-// grid) are each cut into tail_splits K ranges: unit full + t is share
-// t % tail_splits of tile full + t / tail_splits, and its raw sum goes to
-// slot t of the tail workspace, to be added up by the fix-up kernel.
-__device__ __forceinline__ Unit decode_pair(int u, int tiles_m, int tiles_n, int kb_per_split,
-                                            int kb_total, int bn, int tail_tiles,
-                                            int tail_splits) {
-    const int full = tiles_m * tiles_n - tail_tiles;
-    if (tail_tiles == 0 || u < full) return decode(u, tiles_m, tiles_n, kb_per_split, kb_total, bn, 2 * BM);
-    const int t = u - full;
-    Unit w = decode(full + t / tail_splits, tiles_m, tiles_n, kb_total, kb_total, bn, 2 * BM);
-    const int per = (kb_total + tail_splits - 1) / tail_splits;
-    w.kb_begin = (t % tail_splits) * per;
-    w.nkb = max(0, min(kb_total, w.kb_begin + per) - w.kb_begin);
-    w.slot = t;
-    return w;
-}
-
-
 // One warp's 32 rows x EPI_COLS columns of C (lane = row y + lane, columns x0
 // ..) through its two shared-memory slabs and TMA stores.  A 16-column piece
 // goes to a slab (the 16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3),
@@ -1164,24 +1143,32 @@ cudaError_t launch_pair(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
                            a.tail_splits, a.tail_ws, a.tmC, a.tma_store);
     if (e != cudaSuccess) return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (a.tail_tiles) {
-        cudaLaunchConfig_t fc = {};
-        cudaLaunchAttribute fattr[1] = {pdl_attribute()};
-        fc.gridDim = dim3(static_cast<unsigned>(a.tail_tiles), 2 * BM);
-        fc.blockDim = dim3(C::BN);
-        fc.stream = s;
-        fc.attrs = fattr;
-        fc.numAttrs = 1;
-        e = cudaLaunchKernelEx(&fc, pair_tail_fixup_kernel, static_cast<const float*>(a.tail_ws),
-                               tiles_m, tiles_n, a.tail_tiles, a.tail_splits, a.out, a.ldo, a.M,
-                               a.N, a.alpha, a.beta, a.scale_mode);
-        if (e != cudaSuccess) return e;
-        e = cudaGetLastError();
-    }
+    if (a.tail_tiles) e = launch_pair_tail_fixup(a, s);
     return e;
 }
 
 }  // namespace
+
+// The tail fix-up of a 256 x 256 pair kernel's K-split last round (either
+// pair kernel: both write the shares as tile-local 256 x 256 raw sums).
+cudaError_t launch_pair_tail_fixup(const Tf32x3Args& a, cudaStream_t s) {
+    constexpr int TM = 2 * BM, TN = PairCfg<3>::BN;
+    const int tiles_m = (a.M + TM - 1) / TM;
+    const int tiles_n = (a.N + TN - 1) / TN;
+    cudaLaunchConfig_t fc = {};
+    cudaLaunchAttribute fattr[1] = {pdl_attribute()};
+    fc.gridDim = dim3(static_cast<unsigned>(a.tail_tiles), TM);
+    fc.blockDim = dim3(TN);
+    fc.stream = s;
+    fc.attrs = fattr;
+    fc.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&fc, pair_tail_fixup_kernel,
+                                       static_cast<const float*>(a.tail_ws), tiles_m, tiles_n,
+                                       a.tail_tiles, a.tail_splits, a.out, a.ldo, a.M, a.N,
+                                       a.alpha, a.beta, a.scale_mode);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
 
 cudaError_t tf32x3_pair_clusters(int sm_count, int* clusters) {
     return pair_clusters(sm_count, clusters);

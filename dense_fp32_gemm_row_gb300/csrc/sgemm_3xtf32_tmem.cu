@@ -534,6 +534,9 @@ struct TmemPairCfg {
     static constexpr uint32_t IDESC = idesc_tf32_f32(TN, TM);
     static constexpr int REGS_LOW = 56, REGS_HIGH = 200;
     static constexpr int DRAIN_BATCH = 4;  // 16-column loads in flight per wait
+    // K blocks per promotion chunk: the single accumulator stalls the MMAs
+    // for each drain, so the chunks are twice as deep as the other kernels'
+    static constexpr int CHUNK = 2 * CH;
     static_assert(2 * 128 * REGS_LOW + 2 * 128 * REGS_HIGH == 65536, "register shares");
     static_assert(OP_COL0 + STAGES * OP_COLS <= TMEM_COLS, "tensor-memory columns");
     static_assert(A_BYTES == 16384, "split_a_stage's map");
@@ -545,7 +548,8 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                               const __grid_constant__ CUtensorMap tmB, float* __restrict__ out,
                               long long ldo, long long split_stride, int M, int N, int K,
                               int kb_per_split, int splits, unsigned* fault,
-                              long long timeout_ns, float alpha, float beta, int scale_mode) {
+                              long long timeout_ns, float alpha, float beta, int scale_mode,
+                              int tail_tiles, int tail_splits, float* __restrict__ tail_ws) {
     using C = TmemPairCfg;
     constexpr int STAGES = C::STAGES;
     extern __shared__ unsigned char smem_raw[];
@@ -571,7 +575,8 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     const int nclusters = gridDim.x >> 1;
     const int tiles_m = (M + C::TM - 1) / C::TM;
     const int tiles_n = (N + C::TN - 1) / C::TN;
-    const int units = tiles_m * tiles_n * splits;
+    const int units = tail_tiles ? tiles_m * tiles_n - tail_tiles + tail_tiles * tail_splits
+                                 : tiles_m * tiles_n * splits;
     const int kb_total = (K + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
@@ -610,7 +615,7 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             int it = 0;
             bool ok = true;
             for (int u = cluster; u < units && ok; u += nclusters) {
-                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
+                const Unit w = decode_pair(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, tail_tiles, tail_splits);
                 const int ma = w.m0 + static_cast<int>(rank) * C::HALF;
                 const int nb = w.n0 + static_cast<int>(rank) * C::HALF;
                 for (int kb = 0; kb < w.nkb; ++kb, ++it) {
@@ -656,8 +661,8 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             int g = 0;  // chunks issued
             bool ok = true;
             for (int u = cluster; u < units && ok; u += nclusters) {
-                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
-                for (int c0 = 0; c0 < w.nkb && ok; c0 += CH, ++g) {
+                const Unit w = decode_pair(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, tail_tiles, tail_splits);
+                for (int c0 = 0; c0 < w.nkb && ok; c0 += C::CHUNK, ++g) {
                     // the single accumulator: both epilogues have drained chunk g - 1
                     if (g >= 1 && !role_wait(acce, (g - 1) & 1, timeout_ns, fault,
                                              kFaultAccumBarrier, abort_flag)) {
@@ -665,7 +670,7 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         break;
                     }
                     tc_fence_after();
-                    const int c1 = min(w.nkb, c0 + CH);
+                    const int c1 = min(w.nkb, c0 + C::CHUNK);
                     for (int kb = c0; kb < c1; ++kb, ++it) {
                         const int s = it % STAGES;
                         const uint32_t par = (it / STAGES) & 1;
@@ -714,7 +719,7 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             int it = 0;
             bool ok = true;
             for (int u = cluster; u < units && ok; u += nclusters) {
-                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
+                const Unit w = decode_pair(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, tail_tiles, tail_splits);
                 for (int kb = 0; kb < w.nkb; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t par = (it / STAGES) & 1;
@@ -735,7 +740,7 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         int it = 0;
         bool ok = true;
         for (int u = cluster; u < units && ok; u += nclusters) {
-            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
+            const Unit w = decode_pair(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, tail_tiles, tail_splits);
             for (int kb = 0; kb < w.nkb; ++kb, ++it) {
                 if (it % C::NSPLIT_A != warp - 2) continue;
                 const int s = it % STAGES;
@@ -763,7 +768,7 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         int it = 0;
         bool ok = true;
         for (int u = cluster; u < units && ok; u += nclusters) {
-            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
+            const Unit w = decode_pair(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, tail_tiles, tail_splits);
             for (int kb = 0; kb < w.nkb; ++kb, ++it) {
                 const int s = it % STAGES;
                 const bool got = role_wait(full0 + 8 * (it % C::NFULL), (it / C::NFULL) & 1,
@@ -810,8 +815,8 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         int g = 0;
         bool ok = true;
         for (int u = cluster; u < units && ok; u += nclusters) {
-            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
-            for (int c0 = 0; c0 < w.nkb; c0 += CH, ++g) {
+            const Unit w = decode_pair(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, tail_tiles, tail_splits);
+            for (int c0 = 0; c0 < w.nkb; c0 += C::CHUNK, ++g) {
                 const bool got = role_wait(accf, g & 1, timeout_ns, fault, kFaultAccumBarrier,
                                            abort_flag);
                 if (!__all_sync(0xffffffffu, got)) {
@@ -851,6 +856,14 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                 if (lane == 0) mbar_arrive_remote(acce_leader);
             }
             if (!ok) break;
+            if (w.slot >= 0) {
+                // a K share of a tail tile: the raw 256 x 256 sum, tile-local
+                float* p = tail_ws + static_cast<long long>(w.slot) * (C::TM * C::TN) +
+                           static_cast<long long>(col0) * C::TN + nl;
+#pragma unroll
+                for (int j = 0; j < EPI_COLS; ++j) p[static_cast<long long>(j) * C::TN] = acc[j];
+                continue;
+            }
             const int n = w.n0 + nl;
             if (n < N) {
                 float* p = out + static_cast<long long>(w.split) * split_stride +
@@ -967,11 +980,13 @@ cudaError_t tf32x3_tmem_pair_clusters(int sm_count, int* out) {
 
 cudaError_t launch_sgemm_3xtf32_tmem_pair(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
     using C = TmemPairCfg;
-    if (!a.pair || a.cluster_splits || a.tail_tiles || a.counters) return cudaErrorInvalidValue;
+    if (!a.pair || a.cluster_splits || a.counters) return cudaErrorInvalidValue;
     int max_clusters = 0;
     cudaError_t e = tf32x3_tmem_pair_clusters(sm_count, &max_clusters);
     if (e != cudaSuccess) return e;
-    const int units = ((a.M + C::TM - 1) / C::TM) * ((a.N + C::TN - 1) / C::TN) * a.splits;
+    const int tiles = ((a.M + C::TM - 1) / C::TM) * ((a.N + C::TN - 1) / C::TN);
+    const int units = a.tail_tiles ? tiles - a.tail_tiles + a.tail_tiles * a.tail_splits
+                                   : tiles * a.splits;
     const int clusters = units < max_clusters ? units : max_clusters;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -988,9 +1003,12 @@ cudaError_t launch_sgemm_3xtf32_tmem_pair(const Tf32x3Args& a, cudaStream_t s, i
     cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, sgemm_3xtf32_tmem_pair_kernel, a.tmAhi, a.tmBhi, a.out, a.ldo,
                            a.split_stride, a.M, a.N, a.K, a.kb_per_split, a.splits, a.fault,
-                           a.timeout_ns, a.alpha, a.beta, a.scale_mode);
+                           a.timeout_ns, a.alpha, a.beta, a.scale_mode, a.tail_tiles,
+                           a.tail_splits, a.tail_ws);
     if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (a.tail_tiles) e = launch_pair_tail_fixup(a, s);
+    return e;
 }
 
 }  // namespace gemm_f32_impl

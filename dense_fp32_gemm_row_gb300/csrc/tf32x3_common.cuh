@@ -154,5 +154,25 @@ __device__ __forceinline__ void split_a_stage(uint32_t sa, int t) {
     }
 }
 
+// Work units of the pair kernel.  Without a tail (tail_tiles == 0) they are
+// (tile, split) pairs as above.  With one, the last tail_tiles tiles of the
+// raster (what would otherwise be a partly idle last round of the persistent
+// grid) are each cut into tail_splits K ranges: unit full + t is share
+// t % tail_splits of tile full + t / tail_splits, and its raw sum goes to
+// slot t of the tail workspace, to be added up by the fix-up kernel.
+__device__ __forceinline__ Unit decode_pair(int u, int tiles_m, int tiles_n, int kb_per_split,
+                                            int kb_total, int bn, int tail_tiles,
+                                            int tail_splits) {
+    const int full = tiles_m * tiles_n - tail_tiles;
+    if (tail_tiles == 0 || u < full) return decode(u, tiles_m, tiles_n, kb_per_split, kb_total, bn, 2 * BM);
+    const int t = u - full;
+    Unit w = decode(full + t / tail_splits, tiles_m, tiles_n, kb_total, kb_total, bn, 2 * BM);
+    const int per = (kb_total + tail_splits - 1) / tail_splits;
+    w.kb_begin = (t % tail_splits) * per;
+    w.nkb = max(0, min(kb_total, w.kb_begin + per) - w.kb_begin);
+    w.slot = t;
+    return w;
+}
+
 }  // namespace
 }  // namespace gemm_f32_impl

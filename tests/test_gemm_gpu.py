@@ -248,18 +248,25 @@ def test_plan_reports_split_k_and_staging():
     st, p = g.gemm_f32_plan(8192, 8192, 8192, g.ALGO_FFMA, 0, A=fa, B=fb, C=fc)
     assert st == 0 and p["splits"] == 1 and p["stage_a"] == 0 and p["stage_b"] == 0
     assert p["kernels"] == 1
-    # the tensor-core path always stages the TF32 split of both operands
+    # operands read in place: the pair kernel with B's split in tensor memory,
+    # no staging; the GEMM and the fix-up of the K-split last round
     st, p = g.gemm_f32_plan(8192, 8192, 8192, g.ALGO_AUTO, 0, A=fa, B=fb, C=fc)
     assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["splits"] == 1
-    # one launch splitting A and split-transposing B, the GEMM, and the fix-up
-    # of the K-split last round
-    assert p["stage_a"] == 1 and p["stage_b"] == 1 and p["kernels"] == 3
+    assert p["b_in_tmem"] == 1 and (p["tile_m"], p["tile_n"]) == (256, 256), p
+    assert p["stage_a"] == 0 and p["stage_b"] == 0 and p["kernels"] == 2, p
+    # the staged tensor-core path (forced): one launch splitting A and
+    # split-transposing B, the GEMM, and the fix-up of the K-split last round
+    st, p = g.gemm_f32_plan_config(8192, 8192, 8192, g.ALGO_3XTF32, g.TILE_256x256_PAIR, 0,
+                                   A=fa, B=fb, C=fc)
+    assert st == 0 and p["stage_a"] == 1 and p["stage_b"] == 1 and p["kernels"] == 3
     # A read in place as its own high part: its low plane and B's two planes
     plane = 8192 * 8192 * 4
     assert p["ctas"] <= 160 and 3 * plane <= p["workspace_bytes"] < 4 * plane
-    # A that TMA cannot read in place (4-byte offset) gets a hi plane too
+    # A that TMA cannot read in place (4-byte offset): AUTO stages, and A
+    # gets a hi plane too
     st, p = g.gemm_f32_plan(8192, 8192, 8192, g.ALGO_AUTO, 0, A=fa + 4, B=fb, C=fc)
-    assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["workspace_bytes"] >= 4 * plane
+    assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["b_in_tmem"] == 0, p
+    assert p["workspace_bytes"] >= 4 * plane
 
 
 def test_status_codes_on_device():

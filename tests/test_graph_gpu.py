@@ -86,8 +86,9 @@ def test_captured_calls_replay_on_new_inputs():
 def test_capture_refuses_to_grow_the_workspace():
     t = _gpu.torch()
     s = t.cuda.Stream()  # a new stream: its workspace is empty
-    M = N = K = 3072  # the two-CTA kernel on staged operands: needs the workspace
-    a = t.rand((M, K), device="cuda")
+    M = N = K = 3072
+    # A 4 bytes off a 16-byte boundary: staged operands, which need the workspace
+    a = t.rand((M * K + 1,), device="cuda")[1:].view(M, K)
     b = t.rand((K, N), device="cuda")
     c = t.zeros((M, N), device="cuda")
     t.cuda.synchronize()

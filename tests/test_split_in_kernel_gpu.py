@@ -105,29 +105,33 @@ def test_quantised_exact():
     _check(C, oracle.ref_gemm(A, B), exact=True, label="quantised 512^3, split in kernel")
 
 
-@pytest.mark.parametrize("shape,want", [((256, 256, 65536), 1), ((65536, 256, 1024), 1),
-                                        ((2048, 2048, 2048), 1), ((8192, 8192, 8192), 0),
+# want: 0 staged kernels, 1 the single-CTA form with B in tensor memory, 2 its pair form
+@pytest.mark.parametrize("shape,want", [((256, 256, 65536), 1), ((65536, 256, 1024), 2),
+                                        ((2048, 2048, 2048), 2), ((8192, 8192, 8192), 2),
                                         ((1025, 1023, 1000), 0), ((512, 512, 512), 1),
                                         ((384, 384, 20000), 1), ((177, 4459, 16098), 0),
                                         ((9000, 200, 8190), 0), ((9000, 200, 8192), 1),
-                                        ((2560, 2560, 2560), 1), ((3072, 3072, 3072), 0),
-                                        ((4096, 4096, 4096), 0), ((1024, 1024, 8192), 1),
-                                        ((2304, 2304, 512), 1), ((386, 358, 15342), 0),
-                                        ((89, 1216, 24336), 1), ((2900, 2900, 1024), 0)],
+                                        ((2560, 2560, 2560), 2), ((3072, 3072, 3072), 2),
+                                        ((4096, 4096, 4096), 2), ((1024, 1024, 8192), 1),
+                                        ((2304, 2304, 512), 2), ((386, 358, 15342), 0),
+                                        ((89, 1216, 24336), 1), ((2900, 2900, 1024), 2),
+                                        ((1536, 1536, 4096), 1), ((1792, 1792, 4096), 2)],
                          ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
 def test_auto_b_in_tensor_memory_rule(shape, want):
-    # AUTO takes the kernel with B's split in tensor memory when A and B can
-    # be read as stored and 2 M N / (M + N) <= 2560 (beyond, the two-CTA
-    # kernel on staged operands: 3072^3, 4096^3, 8192^3); a row stride that
-    # is not a multiple of 16 bytes (1025 x 1023, 177 x 4459, 9000 x 200 x
-    # 8190, 386 x 358 x 15342) keeps the staged kernels
+    # AUTO takes a kernel with B's split in tensor memory whenever A and B
+    # can be read as stored: the pair form when its 256 x 256 tiles fill at
+    # least half the SM pairs (1792^2: 49 tiles on 76 pairs), else the
+    # single-CTA form (1536^2: 36); a row stride that is not a multiple of
+    # 16 bytes (1025 x 1023, 177 x 4459, 9000 x 200 x 8190, 386 x 358 x
+    # 15342) keeps the staged kernels
     M, N, K = shape
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
-    assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["b_in_tmem"] == want, p
+    assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["b_in_tmem"] == (want > 0), p
     if want:
-        assert (p["tile_m"], p["tile_n"]) == (128, 128) and p["split_in_kernel"] == 1, p
+        tile = 256 if want == 2 else 128
+        assert (p["tile_m"], p["tile_n"]) == (tile, tile) and p["split_in_kernel"] == 1, p
         assert p["stage_a"] == 0 and p["stage_b"] == 0, p
-        assert p["cluster_reduce"] == 0 and p["kernels"] == (1 if p["splits"] == 1 else 2), p
+        assert p["cluster_reduce"] == 0, p
     # A misaligned by 4 bytes: never read in place, so never this kernel
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=(1 << 32) + 4, B=1 << 36, C=1 << 40)
     assert st == 0 and p["b_in_tmem"] == 0, p
@@ -224,16 +228,19 @@ def test_pair_output_boxes(tile, shape):
 
 
 def test_pair_output_boxes_alpha():
-    # alpha without beta: the pair kernel scales the values it stages for the
-    # TMA stores; ragged N (2900 = 11 * 256 + 84) and a padded row stride
+    # alpha without beta: the staged pair kernel scales the values it stages
+    # for the TMA stores; ragged N (2900 = 11 * 256 + 84) and a padded row
+    # stride; a transposed A keeps it on staged operands (and AUTO's plan for
+    # the operands read in place, the pair with B in tensor memory, runs too)
     from .test_gemm_gpu import _ex_case
     M, N, K = 2900, 2900, 1024
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and (p["tile_m"], p["tile_n"]) == (256, 256), p
+    _ex_case(M, N, K, 1, 0, 4, 0.5, 0.0, g.ALGO_AUTO)
     _ex_case(M, N, K, 0, 0, 4, 0.5, 0.0, g.ALGO_AUTO)
 
 
-@pytest.mark.parametrize("shape,algo,ta", [((2900, 2900, 1024), g.ALGO_AUTO, 0),
+@pytest.mark.parametrize("shape,algo,ta", [((2900, 2900, 1024), g.ALGO_AUTO, 1),
                                            ((300, 200, 40), g.ALGO_3XTF32, 1),
                                            ((520, 100, 2000), g.ALGO_3XTF32, 1)],
                          ids=["pair", "single-128", "single-ragged-m"])
@@ -241,7 +248,7 @@ def test_output_boxes_with_beta(shape, algo, ta):
     # alpha and beta: the kernels load each 32 x 16 box of the old C into
     # their shared-memory slab (TMA, clipped boxes zero-filled outside C),
     # replace it by alpha v + beta C and store it back (a transposed A keeps
-    # the small shapes on the staged single-CTA kernels)
+    # these shapes on the staged kernels)
     from .test_gemm_gpu import _ex_case
     M, N, K = shape
     _ex_case(M, N, K, ta, 0, 4, 0.5, -0.75, algo)
@@ -256,7 +263,8 @@ def test_pair_output_ragged_row_in_padded_stride():
     M, N, K = 2900, 2902, 1024
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and (p["tile_m"], p["tile_n"]) == (256, 256), p
-    _ex_case(M, N, K, 0, 0, 2, 1.0, 0.0, g.ALGO_AUTO)
+    _ex_case(M, N, K, 1, 0, 2, 1.0, 0.0, g.ALGO_AUTO)  # staged pair, TMA stores
+    _ex_case(M, N, K, 0, 0, 2, 1.0, 0.0, g.ALGO_AUTO)  # B in tensor memory
 
 
 SINGLE_SPLIT = g.TILE_128x128_SPLIT
