@@ -343,10 +343,13 @@ double single_cta_fill(int sm_count, int M, int N, int K, int bn, int splits) {
 // CTAs, or clusters of the pair form) x K blocks per unit, plus for S > 1 the
 // reduction launch (~4 us) and its traffic ((S + 1) M N floats at ~3 TB/s).
 // Measured: one K block of a 128 x 128 unit takes ~0.64 us (8192^3: 4392
-// us for 27 rounds of 256); of a 256 x 256 pair unit, ~0.8 us.
+// us for 27 rounds of 256); of a 256 x 256 pair unit, ~0.8 us.  The pair
+// form's tail split counts: 2048 x 8192 x 8192 (256 tiles on 76 clusters)
+// keeps S = 1, 3.5 rounds of 256 blocks, rather than S = 2 and a reduction.
 // 1280^2 x 8192: 100 tiles, S = 3 (two rounds of 86 blocks) over S = 1 (one
 // round of 256, 52 SMs idle); 256 x 256 x 65536: 4 tiles, S = 38.
-int tmem_splits(int slots, int tiles, int kb_total, int M, int N, double us_per_block) {
+int tmem_splits(int slots, int tiles, int kb_total, int M, int N, double us_per_block,
+                bool tail_split) {
     constexpr double kReduceLaunchUs = 4.0, kReduceBytesPerUs = 3.0e6;
     const double kUsPerBlock = us_per_block;
     const int sm_count = slots;
@@ -358,8 +361,14 @@ int tmem_splits(int slots, int tiles, int kb_total, int M, int N, double us_per_
         const int eff = (kb_total + per - 1) / per;  // splits that get work
         if (eff != s) continue;
         const long long units = static_cast<long long>(tiles) * s;
-        const long long rounds = (units + sm_count - 1) / sm_count;
-        double us = static_cast<double>(rounds) * per * kUsPerBlock;
+        double rounds = static_cast<double>((units + sm_count - 1) / sm_count);
+        // without split-K the pair form cuts a partly idle last round into
+        // T K shares (see make_plan): that round then takes 1 / T
+        const int r = tiles % sm_count;
+        const int t = r ? std::min(sm_count / r, 4) : 0;
+        if (s == 1 && tail_split && tiles > sm_count && t >= 2 && kb_total >= 2 * t)
+            rounds = static_cast<double>(tiles / sm_count) + 1.0 / t;
+        double us = rounds * per * kUsPerBlock;
         if (s > 1)
             us += kReduceLaunchUs + (s + 1.0) * M * static_cast<double>(N) * 4.0 / kReduceBytesPerUs;
         if (s == 1 || us < best_us) {
@@ -527,8 +536,8 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     if (p->algo == GEMM_F32_ALGO_3XTF32 && !p->pair && !p->tmem_b)
         s = single_cta_splits(d.sm_count, tiles, K, splits, p->bn);
     if (p->tmem_b && splits == 0)
-        s = p->pair ? tmem_splits(slots, tiles, kb_total, M, N, 0.8)
-                    : tmem_splits(slots, tiles, kb_total, M, N, 0.64);
+        s = p->pair ? tmem_splits(slots, tiles, kb_total, M, N, 0.8, true)
+                    : tmem_splits(slots, tiles, kb_total, M, N, 0.64, false);
     p->kb_per_split = (kb_total + s - 1) / s;
     p->splits = (kb_total + p->kb_per_split - 1) / p->kb_per_split;
     const int units = tiles * p->splits;
