@@ -137,7 +137,8 @@ def sweep(shapes, repeats: int, out=sys.stdout, quick: bool = False, check=None)
             results.append({"shape": f"{M}x{N}x{K}", "algo": names[algo],
                             "tile": tiles[tile] if algo != g.ALGO_AUTO else
                             f"{plan['tile_m']}x{plan['tile_n']}"
-                            + ("-split" if plan.get("split_in_kernel") else ""),
+                            + ("-tmem" if plan.get("b_in_tmem") else
+                               "-split" if plan.get("split_in_kernel") else ""),
                             "splits": plan["splits"], "ctas": plan["ctas"],
                             "kernels": plan["kernels"], "ms": float("nan"), "tflops": 0.0,
                             "check": "pass" if ok else "FAIL", "auto": algo == g.ALGO_AUTO})
