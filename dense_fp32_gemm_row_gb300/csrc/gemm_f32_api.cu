@@ -338,45 +338,58 @@ double single_cta_fill(int sm_count, int M, int N, int K, int bn, int splits) {
     return busy * N / (static_cast<double>(tiles_n) * bn);
 }
 
-// The split-K factor of the kernels with B's split in tensor memory: the one
-// that minimises their modelled time, rounds of the persistent grid (slots:
-// CTAs, or clusters of the pair form) x K blocks per unit, plus for S > 1 the
-// reduction launch (~4 us) and its traffic ((S + 1) M N floats at ~3 TB/s).
-// Measured: one K block of a 128 x 128 unit takes ~0.64 us (8192^3: 4392
-// us for 27 rounds of 256); of a 256 x 256 pair unit, ~0.8 us.  The pair
-// form's tail split counts: 2048 x 8192 x 8192 (256 tiles on 76 clusters)
-// keeps S = 1, 3.5 rounds of 256 blocks, rather than S = 2 and a reduction.
-// 1280^2 x 8192: 100 tiles, S = 3 (two rounds of 86 blocks) over S = 1 (one
-// round of 256, 52 SMs idle); 256 x 256 x 65536: 4 tiles, S = 38.
-int tmem_splits(int slots, int tiles, int kb_total, int M, int N, double us_per_block,
-                bool tail_split) {
+// Modelled time of the kernels with B's split in tensor memory: rounds of
+// the persistent grid (slots: CTAs, or clusters of the pair form) x K blocks
+// per unit x the time of one K block, plus a fixed cost (launch, pipeline
+// fill, last epilogue) and, for S > 1, the reduction (~4 us and its traffic,
+// (S + 1) M N floats at ~3 TB/s).  Fitted on the boundary sweep: one K block
+// of a 128 x 128 unit ~0.62 us, fixed ~6 us (4096 x 512 x 8192: one round
+// of 256 blocks, 164.5 us; 4096^3: 7 rounds of 128, 555.7 us); of a 256 x
+// 256 pair unit ~0.93 us, fixed ~12 us (2048^2 x 8192: 242 us; 8192^3:
+// 13.5 rounds of 256, 3.2 ms).  The pair form's tail split counts: 2048 x
+// 8192 x 8192 (256 tiles on 76 clusters) keeps S = 1, 3.5 rounds of 256
+// blocks, rather than S = 2 and a reduction.  Returns the modelled us and
+// the S that minimises it (1280^2 x 8192 on 128 x 128 tiles: 100 tiles, S
+// = 3, two rounds of 86 blocks, over S = 1, one round of 256 with 52 SMs
+// idle; 256 x 256 x 65536: 4 tiles, S = 38).
+struct TmemModel {
+    double us_per_block;
+    double fixed_us;
+    bool tail_split;
+};
+constexpr TmemModel kTmemSingle = {0.62, 6.0, false};
+constexpr TmemModel kTmemPair = {0.93, 12.0, true};
+
+double tmem_estimate(int slots, int tiles, int kb_total, int M, int N, const TmemModel& mdl,
+                     int forced_splits, int* splits_out) {
     constexpr double kReduceLaunchUs = 4.0, kReduceBytesPerUs = 3.0e6;
-    const double kUsPerBlock = us_per_block;
-    const int sm_count = slots;
     int best = 1;
     double best_us = 0.0;
     const int s_max = std::min(GEMM_F32_MAX_SPLITS, std::max(1, kb_total / 4));
-    for (int s = 1; s <= s_max; ++s) {
+    const int s_lo = forced_splits > 0 ? std::min(forced_splits, std::max(kb_total, 1)) : 1;
+    const int s_hi = forced_splits > 0 ? s_lo : s_max;
+    for (int s = s_lo; s <= s_hi; ++s) {
         const int per = (kb_total + s - 1) / s;
         const int eff = (kb_total + per - 1) / per;  // splits that get work
-        if (eff != s) continue;
+        if (eff != s && forced_splits <= 0) continue;
         const long long units = static_cast<long long>(tiles) * s;
-        double rounds = static_cast<double>((units + sm_count - 1) / sm_count);
+        double rounds = static_cast<double>((units + slots - 1) / slots);
         // without split-K the pair form cuts a partly idle last round into
         // T K shares (see make_plan): that round then takes 1 / T
-        const int r = tiles % sm_count;
-        const int t = r ? std::min(sm_count / r, 4) : 0;
-        if (s == 1 && tail_split && tiles > sm_count && t >= 2 && kb_total >= 2 * t)
-            rounds = static_cast<double>(tiles / sm_count) + 1.0 / t;
-        double us = rounds * per * kUsPerBlock;
+        const int r = tiles % slots;
+        const int t = r ? std::min(slots / r, 4) : 0;
+        if (s == 1 && mdl.tail_split && tiles > slots && t >= 2 && kb_total >= 2 * t)
+            rounds = static_cast<double>(tiles / slots) + 1.0 / t;
+        double us = rounds * per * mdl.us_per_block + mdl.fixed_us;
         if (s > 1)
             us += kReduceLaunchUs + (s + 1.0) * M * static_cast<double>(N) * 4.0 / kReduceBytesPerUs;
-        if (s == 1 || us < best_us) {
+        if (s == s_lo || us < best_us) {
             best = s;
             best_us = us;
         }
     }
-    return best;
+    if (splits_out) *splits_out = best;
+    return best_us;
 }
 
 size_t carve(size_t* off, long long bytes) {
@@ -451,38 +464,42 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         }
         // A and B read as stored (K-contiguous A and N-contiguous B rows,
         // 16-byte row strides and bases): the kernels with B's split in
-        // tensor memory need no staging pass and no transpose in shared
-        // memory.  The single-CTA 128 x 128 form beat the staged kernels up
-        // to 2 M N / (M + N) of about 2560 (the boundary sweep: 256 x 256 x
-        // 65536 51.9 against 66.2 us, 896^2 x 4096 39.6 against 58.0, 1024^2
-        // x 8192 90.8 against 105.1, 2048^3 86.7 against 88.7, 2560^3 154.3
-        // against 158.4), and its pair form beats them beyond.  It also beat the two
-        // kernels that split A and B in shared memory (the pair and the
-        // single-CTA 128 x 128 one, now forced configurations only) on every
-        // shape they were chosen for (89 x 1216 x 24336 47.7 against 74.4
-        // us, 512^2 x 8192 35.5 against 43.7).  Operands that need padded
-        // copies keep the staged kernels: the copies and their launches lost
-        // it most such shapes (339 x 1810 x 4223 88.7 against 57.3 us).
-        const double per_element = 2.0 * M * N / (static_cast<double>(M) + N);
+        // tensor memory, which need no staging pass and no transpose in
+        // shared memory.  They beat the staged kernels on every such shape
+        // of the boundary sweep (256 x 256 x 65536 51.9 against 66.2 us,
+        // 896^2 x 4096 39.6 against 58.0, 2048^3 76 against 89, 8192^3 3.18
+        // against 3.53 ms), and the kernels that split A and B in shared
+        // memory (now forced configurations only) on every shape those were
+        // chosen for (89 x 1216 x 24336 47.7 against 74.4 us).  Operands that
+        // need padded copies take them too once C has 3M elements, where the
+        // copies' cost is small beside the kernel's gain (random shapes:
+        // 1172 x 3326 x 163 27 against 44 us, 1570 x 4603 x 750 83 against
+        // 111, 1500 x 2079 x 21955 827 against 1086); below that the staged
+        // kernels mostly win (339 x 1810 x 4223 88.7 against 56.0 us).  The
+        // CTA-pair form (256 x 256 tiles, N = 256 MMAs) or the single-CTA
+        // one, whichever the model times shorter with its own split-K
+        // factor: 1536^2 x 8192 pair with 2 splits 136 against 164.5 us for
+        // one round of 128 x 128 tiles; 512^2 x 4096 single with 9 splits
+        // 25 against 27 us.
         const bool in_place = !q.ta && !q.tb && q.lda % 4 == 0 && q.ldb % 4 == 0 &&
                               !misaligned16(q.A) && !misaligned16(q.B);
-        if (in_place) {
-            // and its CTA-pair form (256 x 256 tiles, N = 256 MMAs, 256-deep
-            // promotion chunks) once its tiles fill half the SM pairs: 8192^3
-            // 3.18 against 3.53 ms staged, 3072^3 205 against 234 us, 2048^3
-            // 76 against 89 us; fewer, deeper tiles keep the single-CTA form,
-            // which adds its split-K partials inside the kernel (256 x 256 x
-            // 65536: 51.9 against 53.4 us)
+        if (in_place || static_cast<double>(M) * N >= 3.0e6) {
             int clusters = 0;
-            const int tiles_pair = ((M + 255) / 256) * ((N + 255) / 256);
-            const bool pair_fills =
-                tf32x3_tmem_pair_clusters(d.sm_count, &clusters) == cudaSuccess &&
-                2 * tiles_pair >= clusters;
+            const bool have_pair =
+                tf32x3_tmem_pair_clusters(d.sm_count, &clusters) == cudaSuccess && clusters > 0;
             cudaGetLastError();
+            const int kb = (K + tf32x3_tmem_config(false).bk - 1) / tf32x3_tmem_config(false).bk;
+            const int t128 = ((M + 127) / 128) * ((N + 127) / 128);
+            const int t256 = ((M + 255) / 256) * ((N + 255) / 256);
+            const double us1 = tmem_estimate(d.sm_count, t128, kb, M, N, kTmemSingle, splits,
+                                             nullptr);
+            const double us2 =
+                have_pair ? tmem_estimate(clusters, t256, kb, M, N, kTmemPair, splits, nullptr)
+                          : us1 + 1.0;
             p->tmem_b = 1;
-            p->pair = pair_fills ? 1 : 0;
+            p->pair = us2 < us1 ? 1 : 0;
             p->split_in_kernel = 1;
-            p->bn = pair_fills ? 256 : 128;
+            p->bn = p->pair ? 256 : 128;
         }
         if (tile != GEMM_F32_TILE_AUTO) {
             p->pair = tile == GEMM_F32_TILE_256x256_PAIR ||
@@ -535,9 +552,14 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     // clusters must all fit on the device at once (single_cta_splits)
     if (p->algo == GEMM_F32_ALGO_3XTF32 && !p->pair && !p->tmem_b)
         s = single_cta_splits(d.sm_count, tiles, K, splits, p->bn);
-    if (p->tmem_b && splits == 0)
-        s = p->pair ? tmem_splits(slots, tiles, kb_total, M, N, 0.8, true)
-                    : tmem_splits(slots, tiles, kb_total, M, N, 0.64, false);
+    if (p->tmem_b && splits == 0) {
+        int clusters = 0;
+        if (p->pair && tf32x3_tmem_pair_clusters(d.sm_count, &clusters) == cudaSuccess &&
+            clusters > 0)
+            slots = clusters;
+        cudaGetLastError();
+        tmem_estimate(slots, tiles, kb_total, M, N, p->pair ? kTmemPair : kTmemSingle, 0, &s);
+    }
     p->kb_per_split = (kb_total + s - 1) / s;
     p->splits = (kb_total + p->kb_per_split - 1) / p->kb_per_split;
     const int units = tiles * p->splits;
@@ -622,9 +644,20 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     // of ~52 us against ~51-56 us for the kernel and a separate reduction);
     // with few splits the cooperative launch costs more than the reduction
     // launch it saves (512^3, 4 splits: ~25 against ~17 us).
-    if (p->tmem_b && !p->pair && p->splits >= 16 && units <= d.sm_count &&
-        2 * tiles * static_cast<long long>(sizeof(int)) <= static_cast<long long>(kWorkspaceCounterBytes))
+    // The CTA pair likewise, with one unit per cluster (and no tail split):
+    // its two CTAs each sum a band of the tile's rows.  There the reduction
+    // launch it saves is no dearer than the wait for the tile's slowest
+    // split (1536^2 x 8192, 2 splits: 139.9 against 135.8 us with the
+    // reduction kernel; 256 x 256 x 65536, 76 splits: 53.9 either way), so
+    // it too starts at 16 splits, for the single launch.
+    const bool counters_fit = 2 * tiles * static_cast<long long>(sizeof(int)) <=
+                              static_cast<long long>(kWorkspaceCounterBytes);
+    if (p->tmem_b && !p->pair && p->splits >= 16 && units <= d.sm_count && counters_fit)
         p->reduce_in_kernel = 1;
+    if (p->tmem_b && p->pair && p->splits >= 16 && !p->tail_tiles && counters_fit &&
+        tf32x3_tmem_pair_clusters(d.sm_count, &clusters) == cudaSuccess && units <= clusters)
+        p->reduce_in_kernel = 1;
+    cudaGetLastError();
     p->ws_bytes = off > kWorkspaceCounterBytes ? off : 0;
     // pre-split operands as stored (A row-major, B not transposed): one
     // staging launch for both

@@ -104,26 +104,94 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
     return v;
 }
 
-// The split-K partials of this CTA's tile added inside the kernel (every
-// CTA holds exactly one unit: split w.split of tile t; all CTAs are
-// co-resident, the launch being cooperative).  Each CTA announces its
-// partial on the tile's arrival counter, waits (bounded) until all S have
-// arrived, then sums a band of ceil(128 / S) tile rows over the S partials
-// in split order (the order of the separate reduction kernel) and writes C;
-// the last CTA of the tile to finish resets both counters for the next call.
-// All threads of the CTA call this.
+// Hardware barrier `id` for the `count` threads (whole warps) that execute
+// it; id 0 with the whole CTA is __syncthreads.
+__device__ __forceinline__ void bar_sync_named(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Sum the S partials of float4 groups [tid, ngroups) step nthreads of a
+// band (group i: row row0 + i / (TN_ / 4), columns n0 + 4 (i % (TN_ / 4))
+// .. + 3) in split order, and write them to C.  G groups a pass, CHUNK
+// partials of each loaded before any is added.
+template <int G, int CHUNK, int TN_>
+__device__ __forceinline__ void reduce_band(const float* __restrict__ parts, long long ldw,
+                                            long long split_stride, int row0, int n0,
+                                            int ngroups, int S, int tid, int nthreads,
+                                            float* __restrict__ C, long long ldc, int M, int N,
+                                            float alpha, float beta, int mode) {
+    constexpr int TN4 = TN_ / 4;
+    const long long stride4 = split_stride / 4;
+    for (int base = tid; base < ngroups; base += G * nthreads) {
+        const float4* src[G];
+        float4 sum[G];
+        bool live[G];
+        int m[G], n[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const int idx = base + g * nthreads;
+            m[g] = row0 + idx / TN4;
+            n[g] = n0 + 4 * (idx % TN4);
+            live[g] = idx < ngroups && m[g] < M && n[g] < N;
+            src[g] = reinterpret_cast<const float4*>(
+                parts + (live[g] ? static_cast<long long>(m[g]) * ldw + n[g] : 0));
+            if (live[g]) sum[g] = __ldcg(src[g]);
+        }
+        for (int s0 = 1; s0 < S; s0 += CHUNK) {
+            float4 v[G][CHUNK];
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int j = 0; j < CHUNK; ++j)
+                    if (live[g] && s0 + j < S)
+                        v[g][j] = __ldcg(src[g] + static_cast<long long>(s0 + j) * stride4);
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int j = 0; j < CHUNK; ++j)
+                    if (live[g] && s0 + j < S) {
+                        sum[g].x += v[g][j].x;
+                        sum[g].y += v[g][j].y;
+                        sum[g].z += v[g][j].z;
+                        sum[g].w += v[g][j].w;
+                    }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            if (!live[g]) continue;
+            float* dst = C + static_cast<long long>(m[g]) * ldc + n[g];
+            const float r[4] = {sum[g].x, sum[g].y, sum[g].z, sum[g].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (n[g] + i < N) dst[i] = scale1(r[i], dst + i, alpha, beta, mode);
+        }
+    }
+}
+
+// The split-K partials of a tile added inside the kernel.  Every CTA holds
+// exactly one unit (one K split of one tile) and all CTAs are co-resident,
+// the launch being cooperative.  The tile's `parts` contributors (S CTAs,
+// or 2 S for the CTA pair, which writes its partial in two halves) each
+// announce their partial on the tile's arrival counter, wait (bounded) until
+// all have arrived, then each sums a band of ceil(TM_ / parts) tile rows
+// over the S partials in split order (the order of the separate reduction
+// kernel) and writes C; the last contributor to finish resets both counters
+// for the next call.  `nthreads` threads (tid 0 .. nthreads - 1) call this
+// together; `bar_id` is their named barrier (0 for the whole CTA).
+template <int TM_, int TN_>
 __device__ __forceinline__ void reduce_tile_in_kernel(
     const float* __restrict__ parts, long long ldw, long long split_stride, int* counters,
-    int tiles, int t, const Unit& w, int S, float* __restrict__ C, long long ldc, int M, int N,
-    float alpha, float beta, int mode, unsigned* fault, long long timeout_ns, uint32_t abort_flag) {
+    int tiles, int t, int m0, int n0, int S, int nparts, int part, int tid, int nthreads,
+    int bar_id, float* __restrict__ C, long long ldc, int M, int N, float alpha, float beta,
+    int mode, unsigned* fault, long long timeout_ns, uint32_t abort_flag) {
     __shared__ int go;
-    if (threadIdx.x == 0) {
-        // the epilogue threads fenced their partial stores before the barrier
-        // that precedes this call
+    if (tid == 0) {
+        // the threads that stored the partial fenced their stores before the
+        // barrier that precedes this call
         atomicAdd(counters + t, 1);
         int ok = 1;
         const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_gpu(counters + t) < S) {
+        while (ld_acquire_gpu(counters + t) < nparts) {
             if (globaltimer_ns() - t0 > static_cast<uint64_t>(timeout_ns)) {
                 if (fault) atomicOr(fault, kFaultAccumBarrier);
                 ok = 0;
@@ -132,39 +200,29 @@ __device__ __forceinline__ void reduce_tile_in_kernel(
         }
         go = ok && ld_shared_volatile(abort_flag) == 0u;
     }
-    __syncthreads();
+    bar_sync_named(bar_id, nthreads);
     if (go) {
-        const int rows = (BM + S - 1) / S;
-        const int r0 = w.split * rows;
-        const int r1 = min(BM, r0 + rows);
-        constexpr int TN = 128;  // tile columns
-        // partials in flight per thread: a thread sums about one output, so
-        // its chain of L2 round trips bounds the band (as in the separate
-        // reduction kernel, which loads 40 at once)
-        constexpr int CHUNK = 40;
-        for (int idx = threadIdx.x; idx < (r1 - r0) * TN; idx += blockDim.x) {
-            const int m = w.m0 + r0 + idx / TN;
-            const int n = w.n0 + idx % TN;
-            if (m >= M || n >= N) continue;
-            const float* src = parts + static_cast<long long>(m) * ldw + n;
-            float sum = __ldcg(src);
-            for (int s0 = 1; s0 < S; s0 += CHUNK) {
-                float v[CHUNK];
-#pragma unroll
-                for (int j = 0; j < CHUNK; ++j)
-                    v[j] = s0 + j < S ? __ldcg(src + static_cast<long long>(s0 + j) * split_stride)
-                                      : 0.0f;
-#pragma unroll
-                for (int j = 0; j < CHUNK; ++j)
-                    if (s0 + j < S) sum += v[j];
-            }
-            float* dst = C + static_cast<long long>(m) * ldc + n;
-            *dst = scale1(sum, dst, alpha, beta, mode);
-        }
+        const int rows = (TM_ + nparts - 1) / nparts;
+        const int r0 = part * rows;
+        const int r1 = min(TM_, r0 + rows);
+        // four adjacent outputs (a float4 group: the workspace rows are
+        // padded to a multiple of 4 floats, its bases 256-byte aligned) at a
+        // time; a thread's chain of L2 round trips bounds the band, so its
+        // loads go out in batches: with one group a thread, 20 partials of
+        // it at once; with several (few splits, wide bands), 5 partials of
+        // each of 4 groups
+        const int ngroups = (r1 - r0) * (TN_ / 4);
+        if (ngroups <= nthreads)
+            reduce_band<1, 20, TN_>(parts, ldw, split_stride, m0 + r0, n0, ngroups, S, tid,
+                                    nthreads, C, ldc, M, N, alpha, beta, mode);
+        else
+            reduce_band<4, 5, TN_>(parts, ldw, split_stride, m0 + r0, n0, ngroups, S, tid,
+                                   nthreads, C, ldc, M, N, alpha, beta, mode);
     }
-    __syncthreads();
-    if (threadIdx.x == 0 && atomicAdd(counters + tiles + t, 1) == S - 1) {
-        // every CTA of the tile has passed its wait: reset for the next call
+    bar_sync_named(bar_id, nthreads);
+    if (tid == 0 && atomicAdd(counters + tiles + t, 1) == nparts - 1) {
+        // every contributor of the tile has passed its wait: reset for the
+        // next call
         counters[t] = 0;
         counters[tiles + t] = 0;
     }
@@ -472,9 +530,10 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
         const int tiles = tiles_m * tiles_n;
         const int u = blockIdx.x;  // this CTA's only unit
         const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM);
-        reduce_tile_in_kernel(out, ldo, split_stride, counters, tiles, u - w.split * tiles, w,
-                              splits, c_final, ldc, M, N, alpha, beta, c_mode, fault, timeout_ns,
-                              abort_flag);
+        reduce_tile_in_kernel<BM, C::BN>(out, ldo, split_stride, counters, tiles,
+                                         u - w.split * tiles, w.m0, w.n0, splits, splits,
+                                         w.split, threadIdx.x, blockDim.x, 0, c_final, ldc, M, N,
+                                         alpha, beta, c_mode, fault, timeout_ns, abort_flag);
     }
 }
 
@@ -549,7 +608,9 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                               long long ldo, long long split_stride, int M, int N, int K,
                               int kb_per_split, int splits, unsigned* fault,
                               long long timeout_ns, float alpha, float beta, int scale_mode,
-                              int tail_tiles, int tail_splits, float* __restrict__ tail_ws) {
+                              int tail_tiles, int tail_splits, float* __restrict__ tail_ws,
+                              int* counters, float* __restrict__ c_final, long long ldc,
+                              int c_mode) {
     using C = TmemPairCfg;
     constexpr int STAGES = C::STAGES;
     extern __shared__ unsigned char smem_raw[];
@@ -874,6 +935,22 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                     if (j < rows) *p = scale1(acc[j], p, alpha, beta, scale_mode);
             }
         }
+        if (counters) {
+            // the in-kernel reduction, here on the epilogue's register share:
+            // the partial must be visible to the other CTAs of the tile
+            // before this CTA announces it; then each CTA of each split sums
+            // its band of the tile's rows
+            __threadfence();
+            bar_sync_named(1, 32 * C::EPI_WARPS);
+            const int tiles = tiles_m * tiles_n;
+            const Unit w =
+                decode_pair(cluster, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, 0, 0);
+            reduce_tile_in_kernel<C::TM, C::TN>(
+                out, ldo, split_stride, counters, tiles, cluster - w.split * tiles, w.m0, w.n0,
+                splits, 2 * splits, 2 * w.split + static_cast<int>(rank), 32 * e + lane,
+                32 * C::EPI_WARPS, 1, c_final, ldc, M, N, alpha, beta, c_mode, fault, timeout_ns,
+                abort_flag);
+        }
         __syncwarp();
     }
 
@@ -980,7 +1057,7 @@ cudaError_t tf32x3_tmem_pair_clusters(int sm_count, int* out) {
 
 cudaError_t launch_sgemm_3xtf32_tmem_pair(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
     using C = TmemPairCfg;
-    if (!a.pair || a.cluster_splits || a.counters) return cudaErrorInvalidValue;
+    if (!a.pair || a.cluster_splits) return cudaErrorInvalidValue;
     int max_clusters = 0;
     cudaError_t e = tf32x3_tmem_pair_clusters(sm_count, &max_clusters);
     if (e != cudaSuccess) return e;
@@ -988,23 +1065,29 @@ cudaError_t launch_sgemm_3xtf32_tmem_pair(const Tf32x3Args& a, cudaStream_t s, i
     const int units = a.tail_tiles ? tiles - a.tail_tiles + a.tail_tiles * a.tail_splits
                                    : tiles * a.splits;
     const int clusters = units < max_clusters ? units : max_clusters;
+    // the in-kernel reduction: one unit per cluster, every cluster resident
+    // at once, no tail split
+    if (a.counters && (a.splits < 2 || units > max_clusters || a.tail_tiles))
+        return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1] = pdl_attribute();
+    attr[2].id = cudaLaunchAttributeCooperative;
+    attr[2].val.cooperative = 1;
     cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = a.counters ? 3 : 2;
     e = cudaLaunchKernelEx(&cfg, sgemm_3xtf32_tmem_pair_kernel, a.tmAhi, a.tmBhi, a.out, a.ldo,
                            a.split_stride, a.M, a.N, a.K, a.kb_per_split, a.splits, a.fault,
                            a.timeout_ns, a.alpha, a.beta, a.scale_mode, a.tail_tiles,
-                           a.tail_splits, a.tail_ws);
+                           a.tail_splits, a.tail_ws, a.counters, a.c_final, a.ldc, a.c_mode);
     if (e != cudaSuccess) return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (a.tail_tiles) e = launch_pair_tail_fixup(a, s);

@@ -139,10 +139,16 @@ def test_pair_kernel_rule(shape, want):
     # 49 pair tiles and 196 single tiles both fill 64 %; 1536^2 x 4096: 36
     # pair tiles fill 47 %, 144 single tiles 95 %).  A's base 4 bytes off a
     # 16-byte boundary keeps the operands from being read in place, which
-    # would send these shapes to the kernel with B's split in tensor memory.
+    # would send these shapes to the kernels with B's split in tensor memory;
+    # with C of 3M elements or more AUTO takes those all the same, after a
+    # padded copy of A.
     M, N, K = shape
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_3XTF32, 0, A=(1 << 32) + 4, B=1 << 36, C=1 << 40)
-    assert st == 0 and p["b_in_tmem"] == 0 and (p["tile_m"] == 256) == bool(want), p
+    assert st == 0 and p["b_in_tmem"] == (M * N >= 3_000_000), p
+    if p["b_in_tmem"]:
+        assert p["stage_a"] == 1 and p["stage_b"] == 0, p
+        return
+    assert (p["tile_m"] == 256) == bool(want), p
 
 
 @pytest.mark.parametrize("shape,bn", [((5170, 151, 5906), 256), ((2378, 4792, 286), 128),
@@ -159,9 +165,13 @@ def test_single_cta_width_rule(shape, bn):
     # at least 2048 of it per 128 x 256 unit, 128 x 256 unless 128 x 128
     # tiles keep 3 % more of the SMs busy (640^2 x 8192: 10 splits of 819);
     # A off a 16-byte boundary, so that the staged kernels are the choice
+    # while C has fewer than 3M elements
     M, N, K = shape
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_3XTF32, 0, A=(1 << 32) + 4, B=1 << 36, C=1 << 40)
-    assert st == 0 and p["b_in_tmem"] == 0 and p["tile_m"] == 128 and p["tile_n"] == bn, p
+    assert st == 0 and p["b_in_tmem"] == (M * N >= 3_000_000), p
+    if p["b_in_tmem"]:
+        return
+    assert p["tile_m"] == 128 and p["tile_n"] == bn, p
 
 
 @pytest.mark.parametrize("shape", PAIR_SHAPES, ids=lambda s: "x".join(map(str, s)))
@@ -262,11 +272,16 @@ def test_plan_reports_split_k_and_staging():
     # A read in place as its own high part: its low plane and B's two planes
     plane = 8192 * 8192 * 4
     assert p["ctas"] <= 160 and 3 * plane <= p["workspace_bytes"] < 4 * plane
-    # A that TMA cannot read in place (4-byte offset): AUTO stages, and A
-    # gets a hi plane too
+    # A that TMA cannot read in place (4-byte offset): AUTO copies A into a
+    # padded buffer (one plane) and keeps the kernel with B in tensor memory
     st, p = g.gemm_f32_plan(8192, 8192, 8192, g.ALGO_AUTO, 0, A=fa + 4, B=fb, C=fc)
-    assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["b_in_tmem"] == 0, p
-    assert p["workspace_bytes"] >= 4 * plane
+    assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["b_in_tmem"] == 1, p
+    assert p["stage_a"] == 1 and p["stage_b"] == 0 and p["kernels"] >= 2, p
+    assert plane <= p["workspace_bytes"] < 2 * plane
+    # the staged path, forced, for the same A: A gets a hi plane too
+    st, p = g.gemm_f32_plan_config(8192, 8192, 8192, g.ALGO_3XTF32, g.TILE_256x256_PAIR, 0,
+                                   A=fa + 4, B=fb, C=fc)
+    assert st == 0 and p["b_in_tmem"] == 0 and p["workspace_bytes"] >= 4 * plane, p
 
 
 def test_status_codes_on_device():

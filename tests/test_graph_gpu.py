@@ -87,7 +87,7 @@ def test_capture_refuses_to_grow_the_workspace():
     t = _gpu.torch()
     s = t.cuda.Stream()  # a new stream: its workspace is empty
     M = N = K = 3072
-    # A 4 bytes off a 16-byte boundary: staged operands, which need the workspace
+    # A 4 bytes off a 16-byte boundary: a padded copy of A, in the workspace
     a = t.rand((M * K + 1,), device="cuda")[1:].view(M, K)
     b = t.rand((K, N), device="cuda")
     c = t.zeros((M, N), device="cuda")

@@ -110,20 +110,22 @@ def test_quantised_exact():
                                         ((2048, 2048, 2048), 2), ((8192, 8192, 8192), 2),
                                         ((1025, 1023, 1000), 0), ((512, 512, 512), 1),
                                         ((384, 384, 20000), 1), ((177, 4459, 16098), 0),
-                                        ((9000, 200, 8190), 0), ((9000, 200, 8192), 1),
+                                        ((9000, 200, 8190), 0), ((9000, 200, 8192), 2),
                                         ((2560, 2560, 2560), 2), ((3072, 3072, 3072), 2),
-                                        ((4096, 4096, 4096), 2), ((1024, 1024, 8192), 1),
+                                        ((4096, 4096, 4096), 2), ((1024, 1024, 8192), 2),
                                         ((2304, 2304, 512), 2), ((386, 358, 15342), 0),
                                         ((89, 1216, 24336), 1), ((2900, 2900, 1024), 2),
-                                        ((1536, 1536, 4096), 1), ((1792, 1792, 4096), 2)],
+                                        ((1536, 1536, 4096), 2), ((512, 512, 4096), 1),
+                                        ((1792, 1792, 4096), 2)],
                          ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
 def test_auto_b_in_tensor_memory_rule(shape, want):
     # AUTO takes a kernel with B's split in tensor memory whenever A and B
-    # can be read as stored: the pair form when its 256 x 256 tiles fill at
-    # least half the SM pairs (1792^2: 49 tiles on 76 pairs), else the
-    # single-CTA form (1536^2: 36); a row stride that is not a multiple of
-    # 16 bytes (1025 x 1023, 177 x 4459, 9000 x 200 x 8190, 386 x 358 x
-    # 15342) keeps the staged kernels
+    # can be read as stored, the CTA-pair form or the single-CTA one as its
+    # model times them (each with its own split-K factor: 1536^2 x 4096, two
+    # splits of 36 pair tiles against one round of 144 single tiles; 512^2 x
+    # 4096, 9 splits of 16 single tiles); a row stride that is not a multiple
+    # of 16 bytes (1025 x 1023, 177 x 4459, 9000 x 200 x 8190, 386 x 358 x
+    # 15342) keeps the staged kernels unless C has 3M elements or more
     M, N, K = shape
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["b_in_tmem"] == (want > 0), p
@@ -132,9 +134,12 @@ def test_auto_b_in_tensor_memory_rule(shape, want):
         assert (p["tile_m"], p["tile_n"]) == (tile, tile) and p["split_in_kernel"] == 1, p
         assert p["stage_a"] == 0 and p["stage_b"] == 0, p
         assert p["cluster_reduce"] == 0, p
-    # A misaligned by 4 bytes: never read in place, so never this kernel
+    # A misaligned by 4 bytes: a padded copy of A, which only a large C pays
+    # for
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=(1 << 32) + 4, B=1 << 36, C=1 << 40)
-    assert st == 0 and p["b_in_tmem"] == 0, p
+    assert st == 0 and p["b_in_tmem"] == (M * N >= 3_000_000), p
+    if p["b_in_tmem"]:
+        assert p["stage_a"] == 1 and p["stage_b"] == 0, p
 
 
 def test_auto_skinny_parity():

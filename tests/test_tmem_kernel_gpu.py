@@ -201,12 +201,61 @@ def test_pair_parity_and_equal_to_single(shape):
 
 @pytest.mark.parametrize("splits", [2, 7])
 def test_pair_split_k(splits):
+    # 9 tiles x 2 or 7 splits, one unit per cluster: below 16 splits the
+    # partials go to the reduction kernel
     M, N, K = 520, 700, 6000
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, PAIR, splits, A=1 << 32, B=1 << 36,
+                                   C=1 << 40)
+    assert st == 0 and p["splits"] == splits and p["reduce_in_kernel"] == 0, p
+    assert p["kernels"] == 2, p
     A, B = make_workload(1, M=M, N=N, K=K)
     C = _gpu.run_configured(A, B, g.ALGO_3XTF32, PAIR, splits)
     _check(C, oracle.ref_gemm(A, B), label=f"tmem pair split-K {splits}")
     C2 = _gpu.run_configured(A, B, g.ALGO_3XTF32, PAIR, splits)
     assert np.array_equal(C.view(np.uint32), C2.view(np.uint32)), "not run-to-run deterministic"
+
+
+@pytest.mark.parametrize("shape,splits", [((256, 256, 16384), 16), ((300, 200, 40000), 20),
+                                          ((129, 384, 20490), 17), ((256, 256, 65536), 76)],
+                         ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
+def test_pair_in_kernel_reduction_equals_split_order_sum(shape, splits):
+    # the CTA pair's in-kernel reduction (each CTA of each split sums a band
+    # of the tile's rows) equals the per-split partials, each the pair kernel
+    # run alone on its K range, added in split order
+    M, N, K = shape
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, PAIR, splits, A=1 << 32, B=1 << 36,
+                                   C=1 << 40)
+    assert st == 0 and p["splits"] == splits and p["reduce_in_kernel"] == 1, p
+    A, B = make_workload(2, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, PAIR, splits)
+    _check(C, oracle.ref_gemm(A, B), label=f"tmem pair in-kernel reduction {shape} s{splits}")
+    kb = (K + 31) // 32
+    per = (kb + splits - 1) // splits
+    total = None
+    for s in range(splits):
+        k0, k1 = s * per * 32, min(K, (s + 1) * per * 32)
+        part = _gpu.run_configured(np.ascontiguousarray(A[:, k0:k1]),
+                                   np.ascontiguousarray(B[k0:k1]), g.ALGO_3XTF32, PAIR, 1)
+        total = part if total is None else (total + part).astype(np.float32)
+    assert np.array_equal(C.view(np.uint32), total.view(np.uint32)), \
+        "in-kernel sum differs from the split-order sum of the partials"
+    # the counters reset themselves: the next calls give the same bits
+    for _ in range(2):
+        C2 = _gpu.run_configured(A, B, g.ALGO_3XTF32, PAIR, splits)
+        assert np.array_equal(C.view(np.uint32), C2.view(np.uint32))
+
+
+def test_pair_more_units_than_clusters_uses_the_reduction_kernel():
+    # 64 pair tiles x 2 splits = 128 units: clusters take several units, so
+    # the partials go through the workspace and the reduction kernel
+    M, N, K = 2048, 2048, 4096
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, PAIR, 2, A=1 << 32, B=1 << 36,
+                                   C=1 << 40)
+    assert st == 0 and p["splits"] == 2 and p["reduce_in_kernel"] == 0 and p["kernels"] == 2, p
+    A, B = make_workload(1, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, PAIR, 2)
+    rows, cols = _sample(M, N, 23)
+    _check(C[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols), label="tmem pair s2 workspace")
 
 
 def test_pair_quantised_exact_and_misaligned():
