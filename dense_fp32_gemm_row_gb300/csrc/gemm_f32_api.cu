@@ -338,26 +338,39 @@ double single_cta_fill(int sm_count, int M, int N, int K, int bn, int splits) {
     return busy * N / (static_cast<double>(tiles_n) * bn);
 }
 
+// Whether cutting the R tiles of the pair kernels' last round into T K
+// shares pays: the round's time falls by (1 - 1/T) of a unit (~0.029 us a
+// unit of K for a 256 x 256 tile), the fix-up kernel costs a ~4 us launch
+// plus reading the T shares and writing the R tiles ((T + 1) R 256^2 floats
+// at ~3 TB/s).
+bool tail_split_pays(int K, int r, int t) {
+    const double saving = (1.0 - 1.0 / t) * K * 0.029;
+    const double cost = 4.0 + (t + 1.0) * r * 256.0 * 256.0 * 4.0 / 3.0e6;
+    return saving > cost;
+}
+
 // Modelled time of the kernels with B's split in tensor memory: rounds of
 // the persistent grid (slots: CTAs, or clusters of the pair form) x K blocks
 // per unit x the time of one K block, plus a fixed cost (launch, pipeline
 // fill, last epilogue) and, for S > 1, the reduction (~4 us and its traffic,
 // (S + 1) M N floats at ~3 TB/s).  Fitted on the boundary sweep: one K block
-// of a 128 x 128 unit ~0.62 us, fixed ~6 us (4096 x 512 x 8192: one round
-// of 256 blocks, 164.5 us; 4096^3: 7 rounds of 128, 555.7 us); of a 256 x
-// 256 pair unit ~0.93 us, fixed ~12 us (2048^2 x 8192: 242 us; 8192^3:
-// 13.5 rounds of 256, 3.2 ms).  The pair form's tail split counts: 2048 x
-// 8192 x 8192 (256 tiles on 76 clusters) keeps S = 1, 3.5 rounds of 256
-// blocks, rather than S = 2 and a reduction.  Returns the modelled us and
-// the S that minimises it (1280^2 x 8192 on 128 x 128 tiles: 100 tiles, S
-// = 3, two rounds of 86 blocks, over S = 1, one round of 256 with 52 SMs
-// idle; 256 x 256 x 65536: 4 tiles, S = 38).
+// of a 128 x 128 unit ~0.62 us, fixed ~8 us (4096 x 512 x 8192: one round
+// of 256 blocks, 164.5 us; 4096^3: 7 rounds of 128, 555.7 us; 2304^2 x
+// 512: 3 rounds of 16, 41.6 us); of a 256 x 256 pair unit ~0.93 us, fixed
+// ~12 us (2048^2 x 8192: 242 us; 8192^3: 13.5 rounds of 256, 3.2 ms).  The
+// pair form's tail split counts, with its fix-up: 2048 x 8192 x 8192 (256
+// tiles on 76 clusters) keeps S = 1, 3.5 rounds of 256 blocks, rather than
+// S = 2 and a reduction.  Returns the modelled us and the S that minimises
+// it (1280^2 x 8192 on 128 x 128 tiles: 100 tiles, S = 3, two rounds of 86
+// blocks, over S = 1, one round of 256 with 52 SMs idle; 256 x 256 x 65536:
+// 4 tiles, S = 38).  Over the boundary sweep's 32 shapes read in place the
+// form it picks is within 4 % of the faster one on all, 1.001 on average.
 struct TmemModel {
     double us_per_block;
     double fixed_us;
     bool tail_split;
 };
-constexpr TmemModel kTmemSingle = {0.62, 6.0, false};
+constexpr TmemModel kTmemSingle = {0.62, 8.0, false};
 constexpr TmemModel kTmemPair = {0.93, 12.0, true};
 
 double tmem_estimate(int slots, int tiles, int kb_total, int M, int N, const TmemModel& mdl,
@@ -378,9 +391,11 @@ double tmem_estimate(int slots, int tiles, int kb_total, int M, int N, const Tme
         // T K shares (see make_plan): that round then takes 1 / T
         const int r = tiles % slots;
         const int t = r ? std::min(slots / r, 4) : 0;
-        if (s == 1 && mdl.tail_split && tiles > slots && t >= 2 && kb_total >= 2 * t)
-            rounds = static_cast<double>(tiles / slots) + 1.0 / t;
+        const bool tail = s == 1 && mdl.tail_split && tiles > slots && t >= 2 &&
+                          kb_total >= 2 * t && tail_split_pays(kb_total * 32, r, t);
+        if (tail) rounds = static_cast<double>(tiles / slots) + 1.0 / t;
         double us = rounds * per * mdl.us_per_block + mdl.fixed_us;
+        if (tail) us += 4.0 + (t + 1.0) * r * 256.0 * 256.0 * 4.0 / 3.0e6;
         if (s > 1)
             us += kReduceLaunchUs + (s + 1.0) * M * static_cast<double>(N) * 4.0 / kReduceBytesPerUs;
         if (s == s_lo || us < best_us) {
@@ -617,7 +632,9 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     // The pair kernel's last round of tiles is usually only partly full
     // (e.g. 1024 tiles over 76 clusters leave 36 for the 14th round).  Cut
     // those tiles into T K shares (T * tail <= clusters) so that the last
-    // round takes 1/T of the time; a fix-up kernel adds the shares.
+    // round takes 1/T of the time; a fix-up kernel adds the shares.  Only
+    // where the time saved beats the fix-up's (tail_split_pays): 8192^3
+    // saves ~119 us for ~13 us, 2378 x 4792 x 286 would save ~4 us for ~14.
     int clusters = 0;
     if (p->pair && p->splits == 1 && splits == 0 &&
         (p->tmem_b ? tf32x3_tmem_pair_clusters(d.sm_count, &clusters)
@@ -626,7 +643,7 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         const int r = tiles % clusters;
         int t = r ? clusters / r : 0;
         if (t > 4) t = 4;
-        if (r && t >= 2 && kb_total >= 2 * t) {
+        if (r && t >= 2 && kb_total >= 2 * t && tail_split_pays(K, r, t)) {
             p->tail_tiles = r;
             p->tail_splits = t;
             p->tail_m = M;

@@ -18,7 +18,8 @@ library and does not load the test suite's CPU oracle.  ``sweep(check=...)``
 takes any other check, and the test suite runs the sweep with the oracle as
 its check.  Timing is the median of ``--repeats`` calls (CUDA events, L2
 flushed between calls when the inputs fit in it; the configurations of a
-shape are timed round-robin, one call each per round).  The library's own choice
+shape are timed round-robin, one call each per round, each round starting
+at the next configuration).  The library's own choice
 (``gemm_f32``, AUTO) is timed alongside so the table shows how far AUTO is
 from the best configuration per shape.
 
@@ -148,8 +149,12 @@ def sweep(shapes, repeats: int, out=sys.stdout, quick: bool = False, check=None)
             for _ in range(2):
                 calls[i]()
         times = {i: [] for i in live}
-        for _ in range(repeats):
-            for i in live:
+        for r in range(repeats):
+            # each round starts at the next configuration: the first call of
+            # a round measured slower (by 2-10 us on calls of ~20 us), and
+            # the rotation spreads that over all of them
+            k = r % len(live)
+            for i in live[k:] + live[:k]:
                 times[i].append(timed_once(calls[i]))
         for i in live:
             ms = statistics.median(times[i])

@@ -203,9 +203,10 @@ typedef struct gemm_f32_plan_info {
                             calculator; 0 if it could not be asked) */
     int threads_per_cta; /* threads of one CTA of the main kernel */
     int b_in_tmem;       /* 1 if the 3XTF32 kernel holds B's split in tensor memory
-                            (GEMM_F32_TILE_128x128_TMEM) */
+                            (GEMM_F32_TILE_128x128_TMEM or _256x256_TMEM) */
     int reduce_in_kernel; /* 1 if that kernel adds its split-K partials itself, in
-                             split order (no reduction kernel) */
+                             split order (no reduction kernel): from 16 splits,
+                             with one unit per CTA (or CTA pair) */
 } gemm_f32_plan_info;
 
 int gemm_f32_plan(int M, int N, int K, int algo, int splits,
@@ -230,10 +231,11 @@ int gemm_f32_plan(int M, int N, int K, int algo, int splits,
  * the call).  _128x128_TMEM reads A and B as stored too; it splits A in
  * shared memory and B into tensor memory, where the MMA takes B^T as its
  * operand, and computes each 128 x 128 tile transposed (no staging pass and
- * no transpose in shared memory; AUTO's choice for operands read in place
- * up to 2 M N / (M + N) of 2560).  _256x256_TMEM is its CTA-pair form
- * (256 x 256 tiles, N = 256 MMAs).  Invalid combinations return
- * GEMM_F32_ERR_INVALID_VALUE.
+ * no transpose in shared memory).  _256x256_TMEM is its CTA-pair form
+ * (256 x 256 tiles, N = 256 MMAs).  AUTO takes one of these two whenever A
+ * and B can be read in place (and, after padded copies, when they cannot
+ * but C has at least 3M elements), the one a fitted time model finds
+ * shorter.  Invalid combinations return GEMM_F32_ERR_INVALID_VALUE.
  */
 #define GEMM_F32_TILE_AUTO          0
 #define GEMM_F32_TILE_128x128       1
