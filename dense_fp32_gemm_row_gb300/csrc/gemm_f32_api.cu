@@ -352,30 +352,31 @@ bool tail_split_pays(int K, int r, int t) {
 // Modelled time of the kernels with B's split in tensor memory: rounds of
 // the persistent grid (slots: CTAs, or clusters of the pair form) x K blocks
 // per unit x the time of one K block, plus a fixed cost (launch, pipeline
-// fill, last epilogue) and, for S > 1, the reduction (~4 us and its traffic,
-// (S + 1) M N floats at ~3 TB/s).  Fitted on the boundary sweep: one K block
-// of a 128 x 128 unit ~0.62 us, fixed ~8 us (4096 x 512 x 8192: one round
-// of 256 blocks, 164.5 us; 4096^3: 7 rounds of 128, 555.7 us; 2304^2 x
-// 512: 3 rounds of 16, 41.6 us); of a 256 x 256 pair unit ~0.93 us, fixed
-// ~12 us (2048^2 x 8192: 242 us; 8192^3: 13.5 rounds of 256, 3.2 ms).  The
+// fill, last epilogue) and, for S > 1, the partials' cost: ~3 us and their
+// traffic, S M N floats written and read back and M N written, at ~5 TB/s
+// (1536^2 x 4096 with 2 pair splits: 76 us; 1024^2 x 8192 with 4: 76 us,
+// with 9 in two rounds: 85).  Fitted on the boundary sweep: one K block of
+// a 128 x 128 unit ~0.57 us, fixed ~12 us (4096 x 512 x 8192: one round of
+// 256 blocks, 154.3 us; 1536^2 x 4096: one round of 128, 84.6 us); of a
+// 256 x 256 pair unit ~0.92 us, fixed ~12 us (2048^2 x 8192: 242 us;
+// 8192^3: 13.5 rounds of 256, 3.14 ms).  The
 // pair form's tail split counts, with its fix-up: 2048 x 8192 x 8192 (256
 // tiles on 76 clusters) keeps S = 1, 3.5 rounds of 256 blocks, rather than
 // S = 2 and a reduction.  Returns the modelled us and the S that minimises
 // it (1280^2 x 8192 on 128 x 128 tiles: 100 tiles, S = 3, two rounds of 86
 // blocks, over S = 1, one round of 256 with 52 SMs idle; 256 x 256 x 65536:
-// 4 tiles, S = 38).  Over the boundary sweep's 32 shapes read in place the
-// form it picks is within 4 % of the faster one on all, 1.001 on average.
+// 4 tiles, S = 38).
 struct TmemModel {
     double us_per_block;
     double fixed_us;
-    bool tail_split;
+    bool tail_split;  // the pair form's K-split last round
 };
-constexpr TmemModel kTmemSingle = {0.62, 8.0, false};
-constexpr TmemModel kTmemPair = {0.93, 12.0, true};
+constexpr TmemModel kTmemSingle = {0.57, 12.0, false};
+constexpr TmemModel kTmemPair = {0.92, 12.0, true};
 
 double tmem_estimate(int slots, int tiles, int kb_total, int M, int N, const TmemModel& mdl,
                      int forced_splits, int* splits_out) {
-    constexpr double kReduceLaunchUs = 4.0, kReduceBytesPerUs = 3.0e6;
+    constexpr double kReduceLaunchUs = 3.0, kReduceBytesPerUs = 5.0e6;
     int best = 1;
     double best_us = 0.0;
     const int s_max = std::min(GEMM_F32_MAX_SPLITS, std::max(1, kb_total / 4));
@@ -397,7 +398,8 @@ double tmem_estimate(int slots, int tiles, int kb_total, int M, int N, const Tme
         double us = rounds * per * mdl.us_per_block + mdl.fixed_us;
         if (tail) us += 4.0 + (t + 1.0) * r * 256.0 * 256.0 * 4.0 / 3.0e6;
         if (s > 1)
-            us += kReduceLaunchUs + (s + 1.0) * M * static_cast<double>(N) * 4.0 / kReduceBytesPerUs;
+            us += kReduceLaunchUs +
+                  (2.0 * s + 1.0) * M * static_cast<double>(N) * 4.0 / kReduceBytesPerUs;
         if (s == s_lo || us < best_us) {
             best = s;
             best_us = us;

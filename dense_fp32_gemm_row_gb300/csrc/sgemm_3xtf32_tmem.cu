@@ -38,11 +38,13 @@
 //                accumulators, then four 64-column B operand stages: hi in
 //                the first 32, lo in the next 32) and one lane issues the
 //                MMAs (M = 128 lanes of n, N = 128 of m, K = 8) and commits;
-//   warps 2-3    split A in shared memory, taking stage fills in turn: x
-//                stays as its own high part, lo = tf32(x - trunc(x)) goes
+//   warps 2-3    split A in shared memory, half of every stage fill each:
+//                x stays as its own high part, lo = tf32(x - trunc(x)) goes
 //                16 KB further on;
 //   warps 4-7    split B into tensor memory (warp 4 + q owns lanes 32q ..
-//                32q + 31, the lane quarter its index gives it);
+//                32q + 31, the lane quarter its index gives it); all six
+//                splitter warps arrive on one barrier per stage, the MMA
+//                lane's one wait per fill;
 //   warps 8-11   the epilogue: per chunk, load the accumulator lanes of the
 //                warp's quarter (128 columns), hand the buffer back and add
 //                them into 128 registers in chunk order; at the end of a
@@ -71,10 +73,8 @@ struct TmemCfg {
     static constexpr int B_BYTES = BN * BK * 4;    // B as stored: four 32 x 32 boxes
     static constexpr int B_BOX_BYTES = 32 * BK * 4;
     static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;  // A, A lo, B
-    static constexpr int NSPLIT_A = 2;             // A splitter warps, taking fills in turn
-    // one full barrier per (fill mod STAGES * NSPLIT_A): each A splitter warp
-    // then waits on its own barriers phase after phase; the B splitters wait
-    // on every fill's
+    static constexpr int NSPLIT_A = 2;             // A splitter warps, half of every fill each
+    // full barriers: one per (fill mod STAGES * NSPLIT_A)
     static constexpr int NFULL = STAGES * NSPLIT_A;
     static constexpr int THREADS = 384;
     static constexpr int TMEM_COLS = 512;
@@ -83,7 +83,7 @@ struct TmemCfg {
     static constexpr int OP_COLS = 2 * BK;         // hi (32 columns), lo (32 columns)
     // full (NFULL), empty, A converted, B converted (per stage),
     // acc_full x2, acc_empty x2, drain
-    static constexpr int NBARS = NFULL + 3 * STAGES + 5;
+    static constexpr int NBARS = NFULL + 2 * STAGES + 5;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NBARS * 8 + 16 + 1024;
     // MMA M = the tile's 128 columns n (lanes), N = its 128 rows m
     static constexpr uint32_t IDESC = idesc_tf32_f32(BN, BM);
@@ -243,9 +243,8 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
     const uint32_t sbase = smem_addr(smem);
     const uint32_t full0 = sbase + STAGES * C::STAGE_BYTES;  // full[f]: + 8 f
     const uint32_t empty0 = full0 + 8 * C::NFULL;            // empty[s]: + 8 s
-    const uint32_t aconv0 = empty0 + 8 * STAGES;             // A lo written[s]
-    const uint32_t bconv0 = aconv0 + 8 * STAGES;             // B in tensor memory[s]
-    const uint32_t accf0 = bconv0 + 8 * STAGES;              // acc_full[b]
+    const uint32_t aconv0 = empty0 + 8 * STAGES;             // A lo written, B in TMEM[s]
+    const uint32_t accf0 = aconv0 + 8 * STAGES;              // acc_full[b]
     const uint32_t acce0 = accf0 + 16;                       // acc_empty[b]
     const uint32_t drain = acce0 + 16;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + STAGES * C::STAGE_BYTES + C::NBARS * 8);
@@ -264,8 +263,9 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int f = 0; f < C::NFULL; ++f) mbar_init(full0 + 8 * f, 1);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(empty0 + 8 * s, 1);
-            mbar_init(aconv0 + 8 * s, 1);
-            mbar_init(bconv0 + 8 * s, 4);
+            // every arrival the MMA lane needs for a fill: A's two splitter
+            // warps and B's four
+            mbar_init(aconv0 + 8 * s, C::NSPLIT_A + 4);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf0 + 8 * b, 1);
@@ -352,9 +352,8 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
                     for (int kb = c0; kb < c1; ++kb, ++it) {
                         const int s = it % STAGES;
                         const uint32_t par = (it / STAGES) & 1;
+                        // A's and B's splitters, on one barrier
                         if (!role_wait(aconv0 + 8 * s, par, timeout_ns, fault, kFaultFullBarrier,
-                                       abort_flag) ||
-                            !role_wait(bconv0 + 8 * s, par, timeout_ns, fault, kFaultFullBarrier,
                                        abort_flag)) {
                             ok = false;
                             break;
@@ -390,15 +389,13 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
         __syncwarp();
     } else if (warp < 4) {
         // ------------------------------ A splitters (warps 2-3) -------------------
-        // warp 2 the even-numbered stage fills, warp 3 the odd ones, each a
-        // whole stage, so that one warp's store drain overlaps the other's
-        // conversions
+        // each warp half of every stage fill (whole fills taken in turn left
+        // a fill's split as long as one warp's ~0.8 us)
         int it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
             const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM);
             for (int kb = 0; kb < w.nkb; ++kb, ++it) {
-                if (it % C::NSPLIT_A != warp - 2) continue;  // the other warp's turn
                 const int s = it % STAGES;
                 const bool got = role_wait(full0 + 8 * (it % C::NFULL), (it / C::NFULL) & 1,
                                            timeout_ns, fault, kFaultFullBarrier, abort_flag);
@@ -407,8 +404,7 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
                     break;
                 }
                 const uint32_t st = sbase + s * C::STAGE_BYTES;
-                split_a_stage(st, lane);
-                split_a_stage(st, lane + 32);
+                split_a_stage(st, lane + 32 * (warp - 2));  // this warp's half
                 // the tensor core reads these words through the async proxy
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -460,7 +456,7 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bconv0 + 8 * s);
+                if (lane == 0) mbar_arrive(aconv0 + 8 * s);
             }
         }
         __syncwarp();
@@ -559,12 +555,14 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
 //               boxes {32 n, 32 k}) onto this CTA's own full barrier;
 //   warp 1      tensor-memory allocation for the pair; in the leader, one
 //               lane issues the MMAs and multicasts the commits;
-//   warps 2-3   split A in shared memory (stage fills in turn), arriving on
-//               this CTA's A-converted barrier;
+//   warps 2-3   split A in shared memory (half of every fill each);
 //   warps 4-7   split B into this CTA's tensor memory (warp 4 + q: lanes
-//               32 q ..), arriving on this CTA's B-converted barrier; in the
-//               peer, one lane of warp 1 relays both to the leader (one
-//               cluster-scope arrival per stage fill);
+//               32 q ..); in the leader all six arrive on its stage-ready
+//               barrier, which the MMA lane waits on; in the peer they
+//               arrive on its own A- and B-converted barriers and one lane
+//               of warp 1 relays both to the leader's stage-ready barrier
+//               (one cluster-scope arrival per stage fill; the MMA lane's
+//               three waits a fill on separate barriers cost ~1 %);
 //   warps 8-15  the epilogue: warp 8 + e drains lanes 32 (e % 4) .., columns
 //               128 (e / 4) .. of the accumulator and arrives on the
 //               leader's acc-empty barrier.
@@ -578,6 +576,10 @@ struct TmemPairCfg {
     static constexpr int B_BYTES = HALF * BK * 4;
     static constexpr int B_BOX_BYTES = 32 * BK * 4;
     static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;  // A, A lo, B
+    // A splitter warps, each splitting half of every fill: a fill's split
+    // then takes half as long (alternating whole fills between the two
+    // warps, ~0.84 us each, left the four-stage ring short of ready stages
+    // at the MMA rate)
     static constexpr int NSPLIT_A = 2;
     static constexpr int NFULL = STAGES * NSPLIT_A;
     static constexpr int THREADS = 512;
@@ -646,7 +648,9 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int f = 0; f < C::NFULL; ++f) mbar_init(full0 + 8 * f, 1);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(empty0 + 8 * s, 1);
-            mbar_init(aconv0 + 8 * s, 1);
+            // the leader's A-converted barrier takes every arrival the MMA
+            // lane needs: its A and B splitters and the peer's relay
+            mbar_init(aconv0 + 8 * s, rank == 0 ? C::NSPLIT_A + 4 + 1 : C::NSPLIT_A);
             mbar_init(bconv0 + 8 * s, 4);
             mbar_init(peer0 + 8 * s, 1);
         }
@@ -735,13 +739,10 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                     for (int kb = c0; kb < c1; ++kb, ++it) {
                         const int s = it % STAGES;
                         const uint32_t par = (it / STAGES) & 1;
-                        // this CTA's splitters (CTA scope), then the peer's,
-                        // relayed by one lane there (cluster scope)
+                        // this CTA's splitters (CTA scope) and the peer's,
+                        // relayed by one lane there (cluster scope), all on
+                        // one barrier
                         if (!role_wait(aconv0 + 8 * s, par, timeout_ns, fault, kFaultFullBarrier,
-                                       abort_flag) ||
-                            !role_wait(bconv0 + 8 * s, par, timeout_ns, fault, kFaultFullBarrier,
-                                       abort_flag) ||
-                            !role_wait(peer0 + 8 * s, par, timeout_ns, fault, kFaultFullBarrier,
                                        abort_flag)) {
                             ok = false;
                             break;
@@ -776,7 +777,7 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             // CTA's splitters have arrived on its own barriers (a release at
             // cluster scope by every splitter warp stalled them on memory
             // barriers: 1.25 us a fill against 0.79 us of MMA work, 4096^3).
-            const uint32_t peer_leader = map_to_cta(peer0, 0);
+            const uint32_t peer_leader = map_to_cta(aconv0, 0);
             int it = 0;
             bool ok = true;
             for (int u = cluster; u < units && ok; u += nclusters) {
@@ -803,7 +804,6 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int u = cluster; u < units && ok; u += nclusters) {
             const Unit w = decode_pair(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, tail_tiles, tail_splits);
             for (int kb = 0; kb < w.nkb; ++kb, ++it) {
-                if (it % C::NSPLIT_A != warp - 2) continue;
                 const int s = it % STAGES;
                 const bool got = role_wait(full0 + 8 * (it % C::NFULL), (it / C::NFULL) & 1,
                                            timeout_ns, fault, kFaultFullBarrier, abort_flag);
@@ -812,8 +812,7 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                     break;
                 }
                 const uint32_t st = sbase + s * C::STAGE_BYTES;
-                split_a_stage(st, lane);
-                split_a_stage(st, lane + 32);
+                split_a_stage(st, lane + 32 * (warp - 2));  // this warp's half
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(aconv0 + 8 * s);
@@ -859,7 +858,7 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bconv0 + 8 * s);
+                if (lane == 0) mbar_arrive((rank == 0 ? aconv0 : bconv0) + 8 * s);
             }
         }
         __syncwarp();
