@@ -369,10 +369,15 @@ bool tail_split_pays(int K, int r, int t) {
 struct TmemModel {
     double us_per_block;
     double fixed_us;
-    bool tail_split;  // the pair form's K-split last round
+    bool tail_split;        // the pair form's K-split last round
+    double reduce_wait_us;  // extra per split for a reduction inside the kernel
 };
-constexpr TmemModel kTmemSingle = {0.57, 12.0, false};
-constexpr TmemModel kTmemPair = {0.92, 12.0, true};
+// The pair's in-kernel reduction (16 splits or more, one unit per cluster)
+// measured ~70 ns a split above the model: 256 x 256 x 65536 with 76 splits
+// 52-54 us against 48 modelled (the single-CTA form with 38: 50 against
+// 50), 512^2 x 16384 with 19 splits 47.8 against 48
+constexpr TmemModel kTmemSingle = {0.57, 12.0, false, 0.0};
+constexpr TmemModel kTmemPair = {0.92, 12.0, true, 0.07};
 
 double tmem_estimate(int slots, int tiles, int kb_total, int M, int N, const TmemModel& mdl,
                      int forced_splits, int* splits_out) {
@@ -400,6 +405,7 @@ double tmem_estimate(int slots, int tiles, int kb_total, int M, int N, const Tme
         if (s > 1)
             us += kReduceLaunchUs +
                   (2.0 * s + 1.0) * M * static_cast<double>(N) * 4.0 / kReduceBytesPerUs;
+        if (s >= 16 && units <= slots) us += mdl.reduce_wait_us * s;
         if (s == s_lo || us < best_us) {
             best = s;
             best_us = us;
