@@ -135,8 +135,29 @@ class ClockSampler:
         self.gpu_id = gpu_id
         self.proc = None
         self.path = None
+        self.c0 = None
+
+    COUNTERS = ["clocks_event_reasons_counters.sw_power_cap",
+                "clocks_event_reasons_counters.sw_thermal_slowdown",
+                "clocks_event_reasons_counters.hw_thermal_slowdown"]
+
+    def counters(self) -> list | None:
+        """Microseconds each clock-reducing reason has been active (None if unknown).
+
+        nvidia-smi's sampled readings lag a timed region of a few hundred
+        milliseconds; these running totals, read before and after it, do not.
+        """
+        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.COUNTERS), "--format=csv,noheader,nounits"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            out = subprocess.run(cmd, capture_output=True, text=True, timeout=10).stdout
+            return [float(x) for x in out.strip().splitlines()[0].split(",")]
+        except (OSError, ValueError, IndexError, subprocess.SubprocessError):
+            return None
 
     def start(self):
+        self.c0 = self.counters()
         try:
             fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
             os.close(fd)
@@ -162,7 +183,15 @@ class ClockSampler:
         with open(self.path) as f:
             text = f.read()
         os.unlink(self.path)
-        return self.summarise(text)
+        summary = self.summarise(text)
+        c1 = self.counters()
+        if self.c0 is not None and c1 is not None:
+            names = ["sw_power_cap", "sw_thermal_slowdown", "hw_thermal_slowdown"]
+            active_us = {n: max(0.0, b - a) for n, a, b in zip(names, self.c0, c1)}
+            summary["reason_active_us"] = active_us
+            summary["reasons"] = sorted(set(summary["reasons"]) |
+                                        {n for n, v in active_us.items() if v > 0})
+        return summary
 
     @staticmethod
     def summarise(text: str) -> dict:
