@@ -223,6 +223,8 @@ KERNEL_SOURCES = {
                           "tcgen05.cuh"],
     "sgemm_3xtf32_tmem_pair": ["sgemm_3xtf32_tmem.cu", "tf32x3_common.cuh", "device_sync.cuh",
                                "tcgen05.cuh"],
+    "sgemm_3xtf32_tmem_wide": ["sgemm_3xtf32_tmem.cu", "tf32x3_common.cuh", "device_sync.cuh",
+                               "tcgen05.cuh"],
 }
 
 
@@ -463,8 +465,9 @@ def run_ours(args, world, rank, local):
         bf16 = float(peaks.get(key, FALLBACK_PEAKS[key]))
         peak = bf16 * (NOMINAL_TF32_TFLOPS / NOMINAL_BF16_TFLOPS) / 3.0
         bound = "tensor"
-        kname = ("sgemm_3xtf32_tmem" + ("_pair" if plan["tile_m"] == 256 else "")
-                 if plan.get("b_in_tmem") else "sgemm_3xtf32")
+        form = {(256, 256): "_pair", (256, 128): "_wide"}.get(
+            (plan["tile_m"], plan["tile_n"]), "")
+        kname = "sgemm_3xtf32_tmem" + form if plan.get("b_in_tmem") else "sgemm_3xtf32"
     else:
         mhz = float(peaks.get("sm_max_mhz") or clocks.get("sm_max_mhz") or 2070.0)
         peak = props.multi_processor_count * FFMA_LANES_PER_SM * 2 * mhz * 1e6 / 1e12

@@ -31,7 +31,7 @@ __all__ = [
     "gemm_f32_algo_splitk_ev", "gemm_f32_noalloc", "gemm_f32_host", "gemm_f32_ex",
     "gemm_f32_configured", "gemm_f32_plan_config", "Config", "TILE_AUTO", "TILE_128x128",
     "TILE_128x256", "TILE_256x256_PAIR", "TILE_256x256_PAIR_SPLIT", "TILE_128x128_SPLIT",
-    "TILE_128x128_TMEM", "TILE_256x256_TMEM",
+    "TILE_128x128_TMEM", "TILE_256x256_TMEM", "TILE_256x128_TMEM",
     "gemm_f32_plan", "gemm_f32_device_status", "gemm_f32_selftest_watchdog",
     "gemm_f32_noalloc_selftest_watchdog", "gemm_f32_inject_host_fault", "INJECT_NONE",
     "INJECT_WORKSPACE", "INJECT_DESCRIPTOR",
@@ -74,6 +74,7 @@ TILE_256x256_PAIR_SPLIT = 4
 TILE_128x128_SPLIT = 5
 TILE_128x128_TMEM = 6
 TILE_256x256_TMEM = 7
+TILE_256x128_TMEM = 8
 
 
 class Config(ctypes.Structure):

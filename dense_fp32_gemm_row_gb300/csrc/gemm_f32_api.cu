@@ -193,6 +193,7 @@ struct Plan {
     int pair = 0;     // 3xTF32: two-CTA kernel
     int split_in_kernel = 0;  // 3xTF32 pair kernel: TF32 split done in shared memory
     int tmem_b = 0;           // 3xTF32: the 128 x 128 kernel with B's split in tensor memory
+    int tmem_wide = 0;        // ... in its wide single-CTA form (256 x 128 tiles, N = 256 MMAs)
     int reduce_in_kernel = 0; // that kernel adds its split-K partials itself (one unit per CTA)
     int cluster_splits = 0;   // FFMA: split-K partials added inside a cluster (2..4)
     int fused_staging = 0;    // 3xTF32 staged: A and B split by one launch
@@ -378,6 +379,10 @@ struct TmemModel {
 // 50), 512^2 x 16384 with 19 splits 47.8 against 48
 constexpr TmemModel kTmemSingle = {0.57, 12.0, false, 0.0};
 constexpr TmemModel kTmemPair = {0.92, 12.0, true, 0.07};
+// the wide single-CTA form: a 16-deep K block of a 256 x 128 unit ~0.455 us
+// (2048^3: one round of 128 blocks, 70.3 us), as efficient per SM as the
+// pair, on tiles of half its size
+constexpr TmemModel kTmemWide = {0.455, 12.0, false, 0.0};
 
 double tmem_estimate(int slots, int tiles, int kb_total, int M, int N, const TmemModel& mdl,
                      int forced_splits, int* splits_out) {
@@ -512,30 +517,38 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
                 tf32x3_tmem_pair_clusters(d.sm_count, &clusters) == cudaSuccess && clusters > 0;
             cudaGetLastError();
             const int kb = (K + tf32x3_tmem_config(false).bk - 1) / tf32x3_tmem_config(false).bk;
+            const int kbw = (K + tf32x3_tmem_wide_config().bk - 1) / tf32x3_tmem_wide_config().bk;
             const int t128 = ((M + 127) / 128) * ((N + 127) / 128);
             const int t256 = ((M + 255) / 256) * ((N + 255) / 256);
+            const int twide = ((M + 255) / 256) * ((N + 127) / 128);
             const double us1 = tmem_estimate(d.sm_count, t128, kb, M, N, kTmemSingle, splits,
                                              nullptr);
             const double us2 =
                 have_pair ? tmem_estimate(clusters, t256, kb, M, N, kTmemPair, splits, nullptr)
                           : us1 + 1.0;
+            const double us3 = tmem_estimate(d.sm_count, twide, kbw, M, N, kTmemWide, splits,
+                                             nullptr);
             p->tmem_b = 1;
-            p->pair = us2 < us1 ? 1 : 0;
+            p->pair = us2 < us1 && us2 <= us3 ? 1 : 0;
+            p->tmem_wide = !p->pair && us3 < us1 ? 1 : 0;
             p->split_in_kernel = 1;
             p->bn = p->pair ? 256 : 128;
         }
         if (tile != GEMM_F32_TILE_AUTO) {
             p->pair = tile == GEMM_F32_TILE_256x256_PAIR ||
                       tile == GEMM_F32_TILE_256x256_PAIR_SPLIT || tile == GEMM_F32_TILE_256x256_TMEM;
-            p->tmem_b = tile == GEMM_F32_TILE_128x128_TMEM || tile == GEMM_F32_TILE_256x256_TMEM;
+            p->tmem_b = tile == GEMM_F32_TILE_128x128_TMEM || tile == GEMM_F32_TILE_256x256_TMEM ||
+                        tile == GEMM_F32_TILE_256x128_TMEM;
+            p->tmem_wide = tile == GEMM_F32_TILE_256x128_TMEM;
             p->split_in_kernel = tile == GEMM_F32_TILE_256x256_PAIR_SPLIT ||
                                  tile == GEMM_F32_TILE_128x128_SPLIT || p->tmem_b;
             p->bn = (tile == GEMM_F32_TILE_128x128 || tile == GEMM_F32_TILE_128x128_SPLIT ||
-                     tile == GEMM_F32_TILE_128x128_TMEM)
+                     tile == GEMM_F32_TILE_128x128_TMEM || tile == GEMM_F32_TILE_256x128_TMEM)
                         ? 128
                         : 256;
         }
-        const Tf32x3Config tc = p->tmem_b ? tf32x3_tmem_config(p->pair != 0)
+        const Tf32x3Config tc = p->tmem_wide ? tf32x3_tmem_wide_config()
+                                : p->tmem_b  ? tf32x3_tmem_config(p->pair != 0)
                                           : tf32x3_config(p->bn, p->pair != 0);
         bm = tc.bm;
         bn = tc.bn;
@@ -581,7 +594,8 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
             clusters > 0)
             slots = clusters;
         cudaGetLastError();
-        tmem_estimate(slots, tiles, kb_total, M, N, p->pair ? kTmemPair : kTmemSingle, 0, &s);
+        tmem_estimate(slots, tiles, kb_total, M, N,
+                      p->pair ? kTmemPair : p->tmem_wide ? kTmemWide : kTmemSingle, 0, &s);
     }
     p->kb_per_split = (kb_total + s - 1) / s;
     p->splits = (kb_total + p->kb_per_split - 1) / p->kb_per_split;
@@ -776,9 +790,11 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
         std::memset(&ta, 0, sizeof(ta));
         if (p.tmem_b) {
             // the operands as stored: A {K, M} in 128 x 32 boxes, B {N, K}
-            // in 32 x 32 boxes (one 128-byte swizzle row wide)
-            if ((st = encode_2d(&ta.tmAhi, o.a, K, M, p.lda, p.tile_k, 128,
-                                CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
+            // in 32 x 32 boxes (one 128-byte swizzle row wide); the wide form
+            // A in 256 x 16 boxes (64-byte swizzle), B in 32 x 16
+            if ((st = encode_2d(&ta.tmAhi, o.a, K, M, p.lda, p.tile_k, p.tmem_wide ? 256 : 128,
+                                p.tmem_wide ? CU_TENSOR_MAP_SWIZZLE_64B
+                                            : CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS ||
                 (st = encode_2d(&ta.tmBhi, o.b, N, K, p.ldb, 32, p.tile_k,
                                 CU_TENSOR_MAP_SWIZZLE_128B)) != GEMM_F32_SUCCESS)
                 return st;
@@ -810,8 +826,9 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
             ta.tail_tiles = tail ? p.tail_tiles : 0;
             ta.tail_splits = tail ? p.tail_splits : 0;
             ta.tail_ws = tail ? reinterpret_cast<float*>(ws + p.off_t) : nullptr;
-            if ((e = p.pair ? launch_sgemm_3xtf32_tmem_pair(ta, stream, d.sm_count)
-                            : launch_sgemm_3xtf32_tmem(ta, stream, d.sm_count)) != cudaSuccess)
+            if ((e = p.pair        ? launch_sgemm_3xtf32_tmem_pair(ta, stream, d.sm_count)
+                     : p.tmem_wide ? launch_sgemm_3xtf32_tmem_wide(ta, stream, d.sm_count)
+                                   : launch_sgemm_3xtf32_tmem(ta, stream, d.sm_count)) != cudaSuccess)
                 return static_cast<int>(e);
             if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess)
                 return static_cast<int>(e);
@@ -1344,11 +1361,11 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
 // A forced configuration: tile id within range and valid for the algorithm.
 int check_config(const gemm_f32_config* cfg) {
     if (!cfg) return GEMM_F32_ERR_INVALID_VALUE;
-    if (cfg->tile < GEMM_F32_TILE_AUTO || cfg->tile > GEMM_F32_TILE_256x256_TMEM)
+    if (cfg->tile < GEMM_F32_TILE_AUTO || cfg->tile > GEMM_F32_TILE_256x128_TMEM)
         return GEMM_F32_ERR_INVALID_VALUE;
     if ((cfg->tile == GEMM_F32_TILE_256x256_PAIR || cfg->tile == GEMM_F32_TILE_256x256_PAIR_SPLIT ||
          cfg->tile == GEMM_F32_TILE_128x128_SPLIT || cfg->tile == GEMM_F32_TILE_128x128_TMEM ||
-         cfg->tile == GEMM_F32_TILE_256x256_TMEM) &&
+         cfg->tile == GEMM_F32_TILE_256x256_TMEM || cfg->tile == GEMM_F32_TILE_256x128_TMEM) &&
         cfg->algo == GEMM_F32_ALGO_FFMA)
         return GEMM_F32_ERR_INVALID_VALUE;
     if (cfg->tile != GEMM_F32_TILE_AUTO && cfg->algo == GEMM_F32_ALGO_AUTO)
@@ -1461,6 +1478,9 @@ int gemm_f32_plan_config(int M, int N, int K, const gemm_f32_config* cfg, const 
         e = tf32x3_tmem_pair_clusters(d->sm_count, &clusters);
         per_sm = d->sm_count ? (2 * clusters + d->sm_count - 1) / d->sm_count : 0;
         out->threads_per_cta = tf32x3_tmem_config(true).threads;
+    } else if (p.tmem_wide) {
+        per_sm = 1;  // the whole tensor memory and 201 KB of shared memory
+        out->threads_per_cta = tf32x3_tmem_wide_config().threads;
     } else if (p.tmem_b) {
         e = tf32x3_tmem_ctas_per_sm(&per_sm);
         out->threads_per_cta = tf32x3_tmem_config(false).threads;

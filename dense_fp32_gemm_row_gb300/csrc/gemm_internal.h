@@ -133,6 +133,11 @@ cudaError_t launch_sgemm_3xtf32(const Tf32x3Args& a, cudaStream_t s, int sm_coun
 cudaError_t launch_sgemm_3xtf32_tmem(const Tf32x3Args& a, cudaStream_t s, int sm_count);
 Tf32x3Config tf32x3_tmem_config(bool pair);
 cudaError_t tf32x3_tmem_ctas_per_sm(int* ctas_per_sm);
+// Its wide single-CTA form: 256 x 128 tiles (256 rows m, 128 columns n) with
+// N = 256 MMAs and 16-deep stages (A {K, M} boxes 16 x 256 with 64-byte
+// swizzle, B {N, K} boxes 32 x 16 with 128-byte swizzle).
+cudaError_t launch_sgemm_3xtf32_tmem_wide(const Tf32x3Args& a, cudaStream_t s, int sm_count);
+Tf32x3Config tf32x3_tmem_wide_config();
 // Its CTA-pair form: 256 x 256 tiles (pair = 1; A {K, M} boxes 32 x 128, B
 // {N, K} boxes 32 x 32); co-resident clusters of two on the current device.
 cudaError_t launch_sgemm_3xtf32_tmem_pair(const Tf32x3Args& a, cudaStream_t s, int sm_count);

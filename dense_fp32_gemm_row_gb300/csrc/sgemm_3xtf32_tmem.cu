@@ -177,8 +177,11 @@ __device__ __forceinline__ void reduce_band(const float* __restrict__ parts, lon
 // over the S partials in split order (the order of the separate reduction
 // kernel) and writes C; the last contributor to finish resets both counters
 // for the next call.  `nthreads` threads (tid 0 .. nthreads - 1) call this
-// together; `bar_id` is their named barrier (0 for the whole CTA).
-template <int TM_, int TN_>
+// together; `bar_id` is their named barrier (0 for the whole CTA).  LOADS:
+// partials of one output group a thread keeps in flight (20 on the
+// 128 x 128 form's registers; 25 on the epilogue warpgroups' 200, the most
+// that stays unspilled: 76 partials in three round trips instead of four).
+template <int TM_, int TN_, int LOADS = 20>
 __device__ __forceinline__ void reduce_tile_in_kernel(
     const float* __restrict__ parts, long long ldw, long long split_stride, int* counters,
     int tiles, int t, int m0, int n0, int S, int nparts, int part, int tid, int nthreads,
@@ -208,12 +211,12 @@ __device__ __forceinline__ void reduce_tile_in_kernel(
         // four adjacent outputs (a float4 group: the workspace rows are
         // padded to a multiple of 4 floats, its bases 256-byte aligned) at a
         // time; a thread's chain of L2 round trips bounds the band, so its
-        // loads go out in batches: with one group a thread, 20 partials of
-        // it at once; with several (few splits, wide bands), 5 partials of
-        // each of 4 groups
+        // loads go out in batches: with one group a thread, LOADS partials
+        // of it at once; with several (few splits, wide bands), 5 partials
+        // of each of 4 groups
         const int ngroups = (r1 - r0) * (TN_ / 4);
         if (ngroups <= nthreads)
-            reduce_band<1, 20, TN_>(parts, ldw, split_stride, m0 + r0, n0, ngroups, S, tid,
+            reduce_band<1, LOADS, TN_>(parts, ldw, split_stride, m0 + r0, n0, ngroups, S, tid,
                                     nthreads, C, ldc, M, N, alpha, beta, mode);
         else
             reduce_band<4, 5, TN_>(parts, ldw, split_stride, m0 + r0, n0, ngroups, S, tid,
@@ -944,7 +947,7 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
             const int tiles = tiles_m * tiles_n;
             const Unit w =
                 decode_pair(cluster, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, 0, 0);
-            reduce_tile_in_kernel<C::TM, C::TN>(
+            reduce_tile_in_kernel<C::TM, C::TN, 25>(
                 out, ldo, split_stride, counters, tiles, cluster - w.split * tiles, w.m0, w.n0,
                 splits, 2 * splits, 2 * w.split + static_cast<int>(rank), 32 * e + lane,
                 32 * C::EPI_WARPS, 1, c_final, ldc, M, N, alpha, beta, c_mode, fault, timeout_ns,
@@ -960,6 +963,365 @@ sgemm_3xtf32_tmem_pair_kernel(const __grid_constant__ CUtensorMap tmA,
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    }
+}
+
+
+// ============================================================================
+// The wide single-CTA form: one CTA computes a 256 x 128 tile (256 rows m of
+// C by 128 columns n) with tcgen05.mma.cta_group::1 M128 N256 K8 (M = the
+// tile's columns n in tensor-memory lanes, N = its rows m), B^T in tensor
+// memory, A in shared memory.  N = 256 MMAs run at ~1130 TFLOP/s tf32 with A
+// in tensor memory (a microbenchmark) against 841 for the N = 128 MMAs of
+// the 128 x 128 form, without the CTA pair's cluster; the price is shared
+// memory: a 32-deep stage would hold 256 rows of A and of A lo (64 KB) beside
+// B, so the stages are 16 deep (A as {16 k, 256 m} boxes with 64-byte
+// swizzle, 40 KB a stage, five stages), and, as in the pair form, the
+// 256-column accumulator is single-buffered with 256-deep promotion chunks.
+//
+// 512 threads in four warpgroups, registers rebalanced as in the pair form
+// (56 for warpgroups 0-1, 200 for the epilogue warpgroups):
+//   warp 0      one lane: TMA loads of the stage (A {16 k, 256 m}, four B
+//               boxes {32 n, 16 k});
+//   warp 1      tensor-memory allocation; one lane issues the MMAs;
+//   warps 2-3   split A in shared memory, half of every fill each;
+//   warps 4-7   split B into tensor memory (warp 4 + q: lanes 32 q ..);
+//               all six splitter warps arrive on one barrier per stage;
+//   warps 8-15  the epilogue: warp 8 + e drains lanes 32 (e % 4) .., columns
+//               128 (e / 4) .. of the accumulator.
+// ============================================================================
+struct TmemWideCfg {
+    static constexpr int TN = 128;                   // tile columns n (lanes)
+    static constexpr int TM = 256;                   // tile rows m (MMA N)
+    static constexpr int KB = 16;                    // K per stage
+    static constexpr int STAGES = 5;
+    static constexpr int A_BYTES = TM * KB * 4;
+    static constexpr int B_BYTES = TN * KB * 4;
+    static constexpr int B_BOX_BYTES = 32 * KB * 4;
+    static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;  // A, A lo, B
+    static constexpr int NSPLIT_A = 2;
+    static constexpr int NFULL = STAGES * NSPLIT_A;
+    static constexpr int THREADS = 512;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int D_COLS = TM;                // one accumulator: m
+    static constexpr int OP_COL0 = D_COLS;           // operand stage s at OP_COL0 + 32 s
+    static constexpr int OP_COLS = 2 * KB;           // hi, then lo
+    static constexpr int EPI_WARPS = 8;
+    // full (NFULL), empty, stage ready (per stage), acc_full, acc_empty, drain
+    static constexpr int NBARS = NFULL + 2 * STAGES + 3;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NBARS * 8 + 16 + 1024;
+    static constexpr uint32_t IDESC = idesc_tf32_f32(TN, TM);
+    static constexpr int REGS_LOW = 56, REGS_HIGH = 200;
+    static constexpr int DRAIN_BATCH = 4;
+    static constexpr int CHUNK = 256 / KB;           // K blocks a promotion chunk (256 deep)
+    static_assert(2 * 128 * REGS_LOW + 2 * 128 * REGS_HIGH == 65536, "register shares");
+    static_assert(OP_COL0 + STAGES * OP_COLS <= TMEM_COLS, "tensor-memory columns");
+    static_assert(A_BYTES == 16384, "split_a_stage's map");
+    static_assert(STAGE_BYTES % 1024 == 0, "stage bases 1024-byte aligned");
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
+
+__global__ void __launch_bounds__(TmemWideCfg::THREADS, 1)
+sgemm_3xtf32_tmem_wide_kernel(const __grid_constant__ CUtensorMap tmA,
+                              const __grid_constant__ CUtensorMap tmB, float* __restrict__ out,
+                              long long ldo, long long split_stride, int M, int N, int K,
+                              int kb_per_split, int splits, unsigned* fault,
+                              long long timeout_ns, float alpha, float beta, int scale_mode,
+                              int* counters, float* __restrict__ c_final, long long ldc,
+                              int c_mode) {
+    using C = TmemWideCfg;
+    constexpr int STAGES = C::STAGES;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t full0 = sbase + STAGES * C::STAGE_BYTES;  // + 8 f
+    const uint32_t empty0 = full0 + 8 * C::NFULL;            // + 8 s
+    const uint32_t ready0 = empty0 + 8 * STAGES;             // + 8 s: A and B split
+    const uint32_t accf = ready0 + 8 * STAGES;
+    const uint32_t acce = accf + 8;
+    const uint32_t drain = acce + 8;
+    uint32_t* tmem_slot =
+        reinterpret_cast<uint32_t*>(smem + STAGES * C::STAGE_BYTES + C::NBARS * 8);
+    const uint32_t abort_flag = smem_addr(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int tiles_m = (M + C::TM - 1) / C::TM;
+    const int tiles_n = (N + C::TN - 1) / C::TN;
+    const int units = tiles_m * tiles_n * splits;
+    const int kb_total = (K + C::KB - 1) / C::KB;
+
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        for (int f = 0; f < C::NFULL; ++f) mbar_init(full0 + 8 * f, 1);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(ready0 + 8 * s, C::NSPLIT_A + 4);
+        }
+        mbar_init(accf, 1);
+        mbar_init(acce, C::EPI_WARPS);
+        mbar_init(drain, 1);
+        st_shared_volatile(abort_flag, 0u);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp < 8) {
+        // warpgroups 0-1 give registers to the epilogue warpgroups
+        regs_dec<C::REGS_LOW>();
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------ TMA producer ------------------------------
+            int it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
+                for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    if (it >= STAGES &&
+                        !role_wait(empty0 + 8 * s, ((it / STAGES) & 1) ^ 1, timeout_ns, fault,
+                                   kFaultEmptyBarrier, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = sbase + s * C::STAGE_BYTES;
+                    const int k0 = (w.kb_begin + kb) * C::KB;
+                    const uint32_t fb = full0 + 8 * (it % C::NFULL);
+                    mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES);
+                    tma_load_2d(st, &tmA, fb, k0, w.m0);
+#pragma unroll
+                    for (int j = 0; j < C::TN / 32; ++j)
+                        tma_load_2d(st + 2 * C::A_BYTES + j * C::B_BOX_BYTES, &tmB, fb,
+                                    w.n0 + 32 * j, k0);
+                    // the same distance ahead in K as the 32-deep kernels
+                    if (kb + 2 * kPrefetchAhead < w.nkb) {
+                        const int kp = k0 + 2 * kPrefetchAhead * C::KB;
+                        tma_prefetch_2d(&tmA, kp, w.m0);
+#pragma unroll
+                        for (int j = 0; j < C::TN / 32; ++j)
+                            tma_prefetch_2d(&tmB, w.n0 + 32 * j, kp);
+                    }
+                }
+            }
+            // wind down: every issued copy has landed and every stage has been
+            // released by the MMA commits before the CTA may exit
+            const long long tail = ok ? timeout_ns : timeout_ns / 8 + 1000;
+            for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j) {
+                mbar_wait(full0 + 8 * (j % C::NFULL), (j / C::NFULL) & 1, tail, fault,
+                          kFaultDrain);
+                mbar_wait(empty0 + 8 * (j % STAGES), (j / STAGES) & 1, tail, fault, kFaultDrain);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------ MMA issuer --------------------------------
+            int it = 0;
+            int g = 0;  // chunks issued
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
+                for (int c0 = 0; c0 < w.nkb && ok; c0 += C::CHUNK, ++g) {
+                    // the single accumulator: the epilogue has drained chunk g - 1
+                    if (g >= 1 && !role_wait(acce, (g - 1) & 1, timeout_ns, fault,
+                                             kFaultAccumBarrier, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int c1 = min(w.nkb, c0 + C::CHUNK);
+                    for (int kb = c0; kb < c1; ++kb, ++it) {
+                        const int s = it % STAGES;
+                        const uint32_t par = (it / STAGES) & 1;
+                        if (!role_wait(ready0 + 8 * s, par, timeout_ns, fault, kFaultFullBarrier,
+                                       abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t st = sbase + s * C::STAGE_BYTES;
+                        const uint64_t a_hi = smem_desc_sw64_kmajor(st);
+                        const uint64_t a_lo = smem_desc_sw64_kmajor(st + C::A_BYTES);
+                        const uint32_t b_hi =
+                            tmem_base + static_cast<uint32_t>(C::OP_COL0 + C::OP_COLS * s);
+                        const uint32_t b_lo = b_hi + C::KB;
+#pragma unroll
+                        for (int k = 0; k < C::KB / UMMA_K; ++k) {
+                            // start address + k * 32 bytes (encoded >> 4)
+                            const uint64_t off = static_cast<uint64_t>(k * UMMA_K * 4) >> 4;
+                            const uint32_t kc = static_cast<uint32_t>(k * UMMA_K);
+                            const uint32_t acc = (kb > c0 || k > 0) ? 1u : 0u;
+                            mma_tf32_tmem_a(tmem_base, b_hi + kc, a_lo + off, C::IDESC, acc);
+                            mma_tf32_tmem_a(tmem_base, b_lo + kc, a_hi + off, C::IDESC, 1u);
+                            mma_tf32_tmem_a(tmem_base, b_hi + kc, a_hi + off, C::IDESC, 1u);
+                        }
+                        mma_commit(empty0 + 8 * s);
+                    }
+                    if (!ok) break;
+                    mma_commit(accf);
+                }
+            }
+            // all issued MMAs complete before tensor memory is released
+            mma_commit(drain);
+            mbar_wait(drain, 0, ok ? timeout_ns : timeout_ns / 8 + 1000, fault, kFaultDrain);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------ A splitters (warps 2-3) -------------------
+        int it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
+            for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+                const int s = it % STAGES;
+                const bool got = role_wait(full0 + 8 * (it % C::NFULL), (it / C::NFULL) & 1,
+                                           timeout_ns, fault, kFaultFullBarrier, abort_flag);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                split_a_stage(sbase + s * C::STAGE_BYTES, lane + 32 * (warp - 2));
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ready0 + 8 * s);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------ B splitters (warps 4-7) -------------------
+        const int q = warp & 3;
+        const uint32_t chunk = static_cast<uint32_t>(lane >> 2);
+        const uint32_t word = static_cast<uint32_t>(lane & 3) * 4u;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+        int it = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
+            for (int kb = 0; kb < w.nkb; ++kb, ++it) {
+                const int s = it % STAGES;
+                const bool got = role_wait(full0 + 8 * (it % C::NFULL), (it / C::NFULL) & 1,
+                                           timeout_ns, fault, kFaultFullBarrier, abort_flag);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t box =
+                    sbase + s * C::STAGE_BYTES + 2 * C::A_BYTES + q * C::B_BOX_BYTES;
+                const uint32_t col =
+                    lane_base + static_cast<uint32_t>(C::OP_COL0 + C::OP_COLS * s);
+                // eight k at a time: this warpgroup runs on 56 registers
+#pragma unroll
+                for (int h = 0; h < C::KB / 8; ++h) {
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t r = static_cast<uint32_t>(8 * h + i);
+                        const float x = lds32(box + r * 128u + ((chunk ^ (r & 7u)) << 4) + word);
+                        hi[i] = __float_as_uint(x) & 0xFFFFE000u;
+                        lo[i] = __float_as_uint(to_tf32(x - __uint_as_float(hi[i])));
+                    }
+                    tmem_st_32x32b_x8(col + 8u * h, hi);
+                    tmem_st_32x32b_x8(col + C::KB + 8u * h, lo);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ready0 + 8 * s);
+            }
+        }
+        __syncwarp();
+    }
+    } else {
+        // ------------------------------ epilogue (warps 8-15) ---------------------
+        regs_inc<C::REGS_HIGH>();
+        const int e = warp - 8;
+        const int q = warp & 3;                 // lanes 32 q .. 32 q + 31
+        const int col0 = (e >> 2) * EPI_COLS;   // accumulator columns (tile rows m)
+        const int nl = 32 * q + lane;           // tile column
+        float acc[EPI_COLS];
+        int g = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::TN, C::TM);
+            for (int c0 = 0; c0 < w.nkb; c0 += C::CHUNK, ++g) {
+                const bool got = role_wait(accf, g & 1, timeout_ns, fault, kFaultAccumBarrier,
+                                           abort_flag);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                                       static_cast<uint32_t>(col0);
+#pragma unroll
+                for (int j0 = 0; j0 < EPI_COLS / 16; j0 += C::DRAIN_BATCH) {
+                    uint32_t r[C::DRAIN_BATCH][16];
+#pragma unroll
+                    for (int b = 0; b < C::DRAIN_BATCH; ++b)
+                        tmem_ld_32x32b_x16(tbase + 16 * (j0 + b), r[b]);
+#pragma unroll
+                    for (int b = 0; b < C::DRAIN_BATCH; ++b) tmem_ld_wait(r[b]);
+#pragma unroll
+                    for (int b = 0; b < C::DRAIN_BATCH; ++b) {
+                        const int j = j0 + b;
+                        if (c0 == 0) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) acc[16 * j + i] = __uint_as_float(r[b][i]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) acc[16 * j + i] += __uint_as_float(r[b][i]);
+                        }
+                    }
+                }
+                // the chunk is in registers: hand the accumulator back
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acce);
+            }
+            if (!ok) break;
+            const int n = w.n0 + nl;
+            if (n < N) {
+                float* p = out + static_cast<long long>(w.split) * split_stride +
+                           static_cast<long long>(w.m0 + col0) * ldo + n;
+                const int rows = M - (w.m0 + col0);
+#pragma unroll
+                for (int j = 0; j < EPI_COLS; ++j, p += ldo)
+                    if (j < rows) *p = scale1(acc[j], p, alpha, beta, scale_mode);
+            }
+        }
+        if (counters) {
+            // the in-kernel reduction, on the epilogue's register share: the
+            // partial is made visible before this CTA announces it, then each
+            // CTA of the tile sums its band of the tile's rows
+            __threadfence();
+            bar_sync_named(1, 32 * C::EPI_WARPS);
+            const int tiles = tiles_m * tiles_n;
+            const Unit w = decode(blockIdx.x, tiles_m, tiles_n, kb_per_split, kb_total, C::TN,
+                                  C::TM);
+            reduce_tile_in_kernel<C::TM, C::TN, 25>(
+                out, ldo, split_stride, counters, tiles, static_cast<int>(blockIdx.x) - w.split * tiles,
+                w.m0, w.n0, splits, splits, w.split, 32 * e + lane, 32 * C::EPI_WARPS, 1,
+                c_final, ldc, M, N, alpha, beta, c_mode, fault, timeout_ns, abort_flag);
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
 }
 
@@ -998,6 +1360,46 @@ cudaError_t launch_sgemm_3xtf32_tmem(const Tf32x3Args& a, cudaStream_t s, int sm
                            a.scale_mode, a.counters, a.c_final, a.ldc, a.c_mode);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+cudaError_t launch_sgemm_3xtf32_tmem_wide(const Tf32x3Args& a, cudaStream_t s, int sm_count) {
+    using C = TmemWideCfg;
+    constexpr auto kern = sgemm_3xtf32_tmem_wide_kernel;
+    static thread_local int attr_done_dev = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (attr_done_dev != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done_dev = dev;
+    }
+    if (a.pair || a.cluster_splits || a.tail_tiles) return cudaErrorInvalidValue;
+    const int units = ((a.M + C::TM - 1) / C::TM) * ((a.N + C::TN - 1) / C::TN) * a.splits;
+    const int grid = units < sm_count ? units : sm_count;
+    // the in-kernel reduction: one unit per CTA, every CTA resident at once
+    if (a.counters && (a.splits < 2 || units > sm_count)) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0] = pdl_attribute();
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.counters ? 2 : 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a.tmAhi, a.tmBhi, a.out, a.ldo, a.split_stride, a.M, a.N,
+                           a.K, a.kb_per_split, a.splits, a.fault, a.timeout_ns, a.alpha, a.beta,
+                           a.scale_mode, a.counters, a.c_final, a.ldc, a.c_mode);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+Tf32x3Config tf32x3_tmem_wide_config() {
+    using C = TmemWideCfg;
+    return {C::TM, C::TN, C::KB, C::STAGES, C::THREADS, C::SMEM_BYTES, 0, 32};
 }
 
 Tf32x3Config tf32x3_tmem_config(bool pair) {

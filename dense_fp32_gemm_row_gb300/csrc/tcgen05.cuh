@@ -207,6 +207,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128_kmajor(uint32_t smem_byte_ad
     return d;
 }
 
+// The same for a tile written with 64-byte swizzle: rows of 64 bytes (16
+// tf32 values of K), 8-row groups 512 bytes apart, layout 4; the tile base
+// 512-byte aligned.
+__device__ __forceinline__ uint64_t smem_desc_sw64_kmajor(uint32_t smem_byte_addr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_byte_addr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>(1u) << 16;
+    d |= static_cast<uint64_t>(512u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(4u) << 61;
+    return d;
+}
+
 // Instruction descriptor for kind::tf32 with fp32 accumulation, both
 // operands K-major, no negation, dense: [4,6) D format (1 = f32),
 // [7,10) A format (2 = tf32), [10,13) B format (2 = tf32), [15] A major,

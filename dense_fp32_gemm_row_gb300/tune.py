@@ -44,13 +44,14 @@ def _configs(g, quick: bool = False):
     if quick:
         for tile in (g.TILE_128x128, g.TILE_128x256, g.TILE_256x256_PAIR,
                      g.TILE_256x256_PAIR_SPLIT, g.TILE_128x128_SPLIT, g.TILE_128x128_TMEM,
-                     g.TILE_256x256_TMEM):
+                     g.TILE_256x256_TMEM, g.TILE_256x128_TMEM):
             yield g.ALGO_3XTF32, tile, 0
         return
     for algo, tiles in ((g.ALGO_FFMA, (g.TILE_128x128, g.TILE_128x256)),
                         (g.ALGO_3XTF32, (g.TILE_128x128, g.TILE_128x256, g.TILE_256x256_PAIR,
                                          g.TILE_256x256_PAIR_SPLIT, g.TILE_128x128_SPLIT,
-                                         g.TILE_128x128_TMEM, g.TILE_256x256_TMEM))):
+                                         g.TILE_128x128_TMEM, g.TILE_256x256_TMEM,
+                                         g.TILE_256x128_TMEM))):
         for tile in tiles:
             for splits in SPLITS:
                 yield algo, tile, splits
@@ -72,7 +73,7 @@ def sweep(shapes, repeats: int, out=sys.stdout, quick: bool = False, check=None)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     names = {g.ALGO_FFMA: "ffma", g.ALGO_3XTF32: "3xtf32", g.ALGO_AUTO: "auto"}
     tiles = {0: "auto", 1: "128x128", 2: "128x256", 3: "256x256pair", 4: "256x256pair-split",
-             5: "128x128-split", 6: "128x128-tmem", 7: "256x256pair-tmem"}
+             5: "128x128-split", 6: "128x128-tmem", 7: "256x256pair-tmem", 8: "256x128-tmem"}
     writer = csv.writer(out)
     writer.writerow(["shape", "algo", "tile", "splits", "ctas", "kernels", "ms", "tflops",
                      "check", "rank"])

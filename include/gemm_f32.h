@@ -203,7 +203,8 @@ typedef struct gemm_f32_plan_info {
                             calculator; 0 if it could not be asked) */
     int threads_per_cta; /* threads of one CTA of the main kernel */
     int b_in_tmem;       /* 1 if the 3XTF32 kernel holds B's split in tensor memory
-                            (GEMM_F32_TILE_128x128_TMEM or _256x256_TMEM) */
+                            (GEMM_F32_TILE_128x128_TMEM, _256x256_TMEM or
+                            _256x128_TMEM) */
     int reduce_in_kernel; /* 1 if that kernel adds its split-K partials itself, in
                              split order (no reduction kernel): from 16 splits,
                              with one unit per CTA (or CTA pair) */
@@ -232,10 +233,11 @@ int gemm_f32_plan(int M, int N, int K, int algo, int splits,
  * shared memory and B into tensor memory, where the MMA takes B^T as its
  * operand, and computes each 128 x 128 tile transposed (no staging pass and
  * no transpose in shared memory).  _256x256_TMEM is its CTA-pair form
- * (256 x 256 tiles, N = 256 MMAs).  AUTO takes one of these two whenever A
- * and B can be read in place (and, after padded copies, when they cannot
- * but C has at least 3M elements), the one a fitted time model finds
- * shorter.  Invalid combinations return GEMM_F32_ERR_INVALID_VALUE.
+ * (256 x 256 tiles, N = 256 MMAs), and _256x128_TMEM its wide single-CTA
+ * form (256 rows by 128 columns, N = 256 MMAs, 16-deep stages).  AUTO
+ * takes one of these whenever A and B can be read in place (and, after
+ * padded copies, when they cannot but C has at least 3M elements), the one a
+ * fitted time model finds shorter.  Invalid combinations return GEMM_F32_ERR_INVALID_VALUE.
  */
 #define GEMM_F32_TILE_AUTO          0
 #define GEMM_F32_TILE_128x128       1
@@ -245,6 +247,7 @@ int gemm_f32_plan(int M, int N, int K, int algo, int splits,
 #define GEMM_F32_TILE_128x128_SPLIT 5
 #define GEMM_F32_TILE_128x128_TMEM  6
 #define GEMM_F32_TILE_256x256_TMEM  7
+#define GEMM_F32_TILE_256x128_TMEM  8
 typedef struct gemm_f32_config {
     int algo;
     int tile;

@@ -135,7 +135,7 @@ def test_tune_configuration_space():
     # the tensor-core tiles with the library's own split choice
     from dense_fp32_gemm_row_gb300 import tune
     full = list(tune._configs(g))
-    assert len(full) == len(set(full)) == (2 + 7) * len(tune.SPLITS)
+    assert len(full) == len(set(full)) == (2 + 8) * len(tune.SPLITS)
     assert {a for a, _, _ in full} == {g.ALGO_FFMA, g.ALGO_3XTF32}
     quick = list(tune._configs(g, quick=True))
     assert quick == [(g.ALGO_3XTF32, t, 0) for t in (g.TILE_128x128, g.TILE_128x256,
@@ -143,7 +143,8 @@ def test_tune_configuration_space():
                                                        g.TILE_256x256_PAIR_SPLIT,
                                                        g.TILE_128x128_SPLIT,
                                                        g.TILE_128x128_TMEM,
-                                                       g.TILE_256x256_TMEM)]
+                                                       g.TILE_256x256_TMEM,
+                                                       g.TILE_256x128_TMEM)]
 
 
 def test_host_fault_injection_arms_and_disarms(lib):

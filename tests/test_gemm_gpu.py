@@ -432,21 +432,19 @@ def test_forced_configurations(algo, tile, splits):
 
 
 def test_invalid_configurations_are_refused():
-    fa, fb, fc = 1 << 32, 1 << 36, 1 << 40
-    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_FFMA, g.TILE_256x256_PAIR, 0) == \
-        g.ERR_INVALID_VALUE
-    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_AUTO, g.TILE_128x128, 0) == \
-        g.ERR_INVALID_VALUE
-    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_FFMA, g.TILE_256x256_PAIR_SPLIT,
-                                 0) == g.ERR_INVALID_VALUE
-    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_FFMA, g.TILE_128x128_SPLIT,
-                                 0) == g.ERR_INVALID_VALUE
-    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_FFMA, g.TILE_128x128_TMEM,
-                                 0) == g.ERR_INVALID_VALUE
-    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_FFMA, g.TILE_256x256_TMEM,
-                                 0) == g.ERR_INVALID_VALUE
-    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_3XTF32, 8, 0) == g.ERR_INVALID_VALUE
-    assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, g.ALGO_3XTF32, -1, 0) == g.ERR_INVALID_VALUE
+    # real buffers, so that a call wrongly accepted fails the assertion
+    # rather than reading an address nothing backs
+    t = _gpu.torch()
+    buf = t.zeros(3 * 64, device="cuda")
+    fa, fb, fc = buf[0:64].data_ptr(), buf[64:128].data_ptr(), buf[128:192].data_ptr()
+    for algo, tile in ((g.ALGO_FFMA, g.TILE_256x256_PAIR), (g.ALGO_AUTO, g.TILE_128x128),
+                       (g.ALGO_FFMA, g.TILE_256x256_PAIR_SPLIT),
+                       (g.ALGO_FFMA, g.TILE_128x128_SPLIT), (g.ALGO_FFMA, g.TILE_128x128_TMEM),
+                       (g.ALGO_FFMA, g.TILE_256x256_TMEM), (g.ALGO_FFMA, g.TILE_256x128_TMEM),
+                       (g.ALGO_3XTF32, g.TILE_256x128_TMEM + 1), (g.ALGO_3XTF32, -1)):
+        assert g.gemm_f32_configured(fa, fb, fc, 8, 8, 8, algo, tile, 0) == \
+            g.ERR_INVALID_VALUE, (algo, tile)
+    t.cuda.synchronize()
 
 
 @pytest.mark.parametrize("algo", [g.ALGO_FFMA, g.ALGO_3XTF32], ids=["ffma", "3xtf32"])

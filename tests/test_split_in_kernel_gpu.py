@@ -105,34 +105,37 @@ def test_quantised_exact():
     _check(C, oracle.ref_gemm(A, B), exact=True, label="quantised 512^3, split in kernel")
 
 
-# want: 0 staged kernels, 1 the single-CTA form with B in tensor memory, 2 its pair form
+# want: 0 staged kernels, 1 the single-CTA form with B in tensor memory, 2 its pair
+# form, 3 its wide single-CTA form, 23 either of the last two (the model's
+# near-ties: per SM the two run at the same rate, on tiles of different size)
 @pytest.mark.parametrize("shape,want", [((65536, 256, 1024), 2),
-                                        ((2048, 2048, 2048), 2), ((8192, 8192, 8192), 2),
+                                        ((2048, 2048, 2048), 23), ((8192, 8192, 8192), 2),
                                         ((1025, 1023, 1000), 0), ((512, 512, 512), 1),
                                         ((384, 384, 20000), 1), ((177, 4459, 16098), 0),
-                                        ((9000, 200, 8190), 0), ((9000, 200, 8192), 2),
-                                        ((2560, 2560, 2560), 2), ((3072, 3072, 3072), 2),
-                                        ((4096, 4096, 4096), 2), ((1024, 1024, 8192), 2),
+                                        ((9000, 200, 8190), 0), ((9000, 200, 8192), 23),
+                                        ((2560, 2560, 2560), 2), ((3072, 3072, 3072), 23),
+                                        ((4096, 4096, 4096), 2), ((1024, 1024, 8192), 23),
                                         ((2304, 2304, 512), 2), ((386, 358, 15342), 0),
-                                        ((89, 1216, 24336), 1), ((2900, 2900, 1024), 2),
-                                        ((1536, 1536, 4096), 2), ((512, 512, 4096), 1),
-                                        ((1792, 1792, 4096), 2)],
+                                        ((89, 1216, 24336), 1), ((2900, 2900, 1024), 23),
+                                        ((1536, 1536, 4096), 23), ((512, 512, 4096), 1),
+                                        ((1792, 1792, 4096), 23), ((512, 512, 16384), 3)],
                          ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
 def test_auto_b_in_tensor_memory_rule(shape, want):
     # AUTO takes a kernel with B's split in tensor memory whenever A and B
-    # can be read as stored, the CTA-pair form or the single-CTA one as its
-    # model times them (each with its own split-K factor: 1536^2 x 4096, two
-    # splits of 36 pair tiles against one round of 144 single tiles; 512^2 x
-    # 4096, 9 splits of 16 single tiles; 256 x 256 x 65536, near a tie, in the
-    # deep-K test); a row stride that is not a multiple
-    # of 16 bytes (1025 x 1023, 177 x 4459, 9000 x 200 x 8190, 386 x 358 x
-    # 15342) keeps the staged kernels unless C has 3M elements or more
+    # can be read as stored: the single-CTA 128 x 128 form, the CTA pair or
+    # the wide single-CTA form, as its model times them (each with its own
+    # split-K factor: 512^2 x 4096, 9 splits of 16 single tiles; 512^2 x
+    # 16384, 19 splits of 8 wide tiles; 256 x 256 x 65536 in the deep-K
+    # test); a row stride that is not a multiple of 16 bytes (1025 x 1023,
+    # 177 x 4459, 9000 x 200 x 8190, 386 x 358 x 15342) keeps the staged
+    # kernels unless C has 3M elements or more
     M, N, K = shape
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["b_in_tmem"] == (want > 0), p
     if want:
-        tile = 256 if want == 2 else 128
-        assert (p["tile_m"], p["tile_n"]) == (tile, tile) and p["split_in_kernel"] == 1, p
+        forms = {1: [(128, 128)], 2: [(256, 256)], 3: [(256, 128)],
+                 23: [(256, 256), (256, 128)]}[want]
+        assert (p["tile_m"], p["tile_n"]) in forms and p["split_in_kernel"] == 1, p
         assert p["stage_a"] == 0 and p["stage_b"] == 0, p
         assert p["cluster_reduce"] == 0, p
     # A misaligned by 4 bytes: a padded copy of A, which only a large C pays
@@ -237,11 +240,12 @@ def test_pair_output_boxes_alpha():
     # alpha without beta: the staged pair kernel scales the values it stages
     # for the TMA stores; ragged N (2900 = 11 * 256 + 84) and a padded row
     # stride; a transposed A keeps it on staged operands (and AUTO's plan for
-    # the operands read in place, the pair with B in tensor memory, runs too)
+    # the operands read in place, a form with B in tensor memory and N = 256
+    # MMAs, the CTA pair or the wide single-CTA one, runs too)
     from .test_gemm_gpu import _ex_case
     M, N, K = 2900, 2900, 1024
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
-    assert st == 0 and (p["tile_m"], p["tile_n"]) == (256, 256), p
+    assert st == 0 and (p["tile_m"], p["tile_n"]) in ((256, 256), (256, 128)), p
     _ex_case(M, N, K, 1, 0, 4, 0.5, 0.0, g.ALGO_AUTO)
     _ex_case(M, N, K, 0, 0, 4, 0.5, 0.0, g.ALGO_AUTO)
 
@@ -268,7 +272,7 @@ def test_pair_output_ragged_row_in_padded_stride():
     from .test_gemm_gpu import _ex_case
     M, N, K = 2900, 2902, 1024
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
-    assert st == 0 and (p["tile_m"], p["tile_n"]) == (256, 256), p
+    assert st == 0 and (p["tile_m"], p["tile_n"]) in ((256, 256), (256, 128)), p
     _ex_case(M, N, K, 1, 0, 2, 1.0, 0.0, g.ALGO_AUTO)  # staged pair, TMA stores
     _ex_case(M, N, K, 0, 0, 2, 1.0, 0.0, g.ALGO_AUTO)  # B in tensor memory
 

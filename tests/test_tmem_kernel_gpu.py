@@ -285,3 +285,80 @@ def test_pair_tail_split(shape):
     _check(C[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols), label=f"tmem pair tail {shape}")
     C2 = _gpu.run_configured(A, B, g.ALGO_3XTF32, PAIR, 0)
     assert np.array_equal(C.view(np.uint32), C2.view(np.uint32)), "not run-to-run deterministic"
+
+
+WIDE = g.TILE_256x128_TMEM
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_wide_parity_and_equal_to_pair(shape):
+    # the wide single-CTA form (256 x 128 tiles, 16-deep stages with A in
+    # 64-byte swizzle) issues, per output, the pair form's MMAs in the same
+    # order with the same 256-deep promotion chunks: bit-equal to it without
+    # split-K
+    M, N, K = shape
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, WIDE, 1, A=1 << 32, B=1 << 36,
+                                   C=1 << 40)
+    assert st == 0 and p["b_in_tmem"] == 1 and (p["tile_m"], p["tile_n"], p["tile_k"]) == \
+        (256, 128, 16), p
+    assert p["stage_a"] == (K % 4 != 0) and p["stage_b"] == (N % 4 != 0), p
+    A, B = make_workload(2, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, WIDE, 1)
+    if M * N <= 300 * 300:
+        _check(C, oracle.ref_gemm(A, B), label=f"tmem wide {shape}")
+    else:
+        rows, cols = _sample(M, N, M * 7 + N + K)
+        _check(C[rows, cols], oracle.ref_gemm_entries(A, B, rows, cols),
+               label=f"tmem wide {shape}")
+    P = _gpu.run_configured(A, B, g.ALGO_3XTF32, PAIR, 1)
+    assert np.array_equal(C.view(np.uint32), P.view(np.uint32)), \
+        f"differs from the pair form at {np.argwhere(C.view(np.uint32) != P.view(np.uint32))[:5]}"
+
+
+@pytest.mark.parametrize("splits", [2, 7])
+def test_wide_split_k(splits):
+    M, N, K = 520, 700, 6000
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, WIDE, splits, A=1 << 32, B=1 << 36,
+                                   C=1 << 40)
+    assert st == 0 and p["splits"] == splits and p["reduce_in_kernel"] == 0, p
+    A, B = make_workload(1, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, WIDE, splits)
+    _check(C, oracle.ref_gemm(A, B), label=f"tmem wide split-K {splits}")
+    C2 = _gpu.run_configured(A, B, g.ALGO_3XTF32, WIDE, splits)
+    assert np.array_equal(C.view(np.uint32), C2.view(np.uint32)), "not run-to-run deterministic"
+
+
+@pytest.mark.parametrize("shape,splits", [((256, 256, 16384), 16), ((300, 200, 40000), 20),
+                                          ((256, 256, 65536), 76)],
+                         ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
+def test_wide_in_kernel_reduction_equals_split_order_sum(shape, splits):
+    M, N, K = shape
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, WIDE, splits, A=1 << 32, B=1 << 36,
+                                   C=1 << 40)
+    assert st == 0 and p["splits"] == splits and p["reduce_in_kernel"] == 1, p
+    A, B = make_workload(2, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, WIDE, splits)
+    _check(C, oracle.ref_gemm(A, B), label=f"tmem wide in-kernel reduction {shape} s{splits}")
+    kb = (K + 15) // 16
+    per = (kb + splits - 1) // splits
+    total = None
+    for s in range(splits):
+        k0, k1 = s * per * 16, min(K, (s + 1) * per * 16)
+        part = _gpu.run_configured(np.ascontiguousarray(A[:, k0:k1]),
+                                   np.ascontiguousarray(B[k0:k1]), g.ALGO_3XTF32, WIDE, 1)
+        total = part if total is None else (total + part).astype(np.float32)
+    assert np.array_equal(C.view(np.uint32), total.view(np.uint32)), \
+        "in-kernel sum differs from the split-order sum of the partials"
+    for _ in range(2):
+        C2 = _gpu.run_configured(A, B, g.ALGO_3XTF32, WIDE, splits)
+        assert np.array_equal(C.view(np.uint32), C2.view(np.uint32))
+
+
+def test_wide_quantised_exact_and_misaligned():
+    A, B = make_workload(0)
+    _check(_gpu.run_configured(A, B, g.ALGO_3XTF32, WIDE, 0), oracle.ref_gemm(A, B), exact=True,
+           label="quantised 512^3, tmem wide")
+    M, N, K = 700, 900, 300
+    A, B = make_workload(1, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, WIDE, 0, offsets=(3, 2, 1))
+    _check(C, oracle.ref_gemm(A, B), label="tmem wide, misaligned operands")
