@@ -372,23 +372,30 @@ struct TmemModel {
     double fixed_us;
     bool tail_split;        // the pair form's K-split last round
     double reduce_wait_us;  // extra per split for a reduction inside the kernel
+    bool one_round;         // only plans whose units all run at once
 };
 // The pair's in-kernel reduction (16 splits or more, one unit per cluster)
 // measured ~70 ns a split above the model: 256 x 256 x 65536 with 76 splits
 // 52-54 us against 48 modelled (the single-CTA form with 38: 50 against
 // 50), 512^2 x 16384 with 19 splits 47.8 against 48
-constexpr TmemModel kTmemSingle = {0.57, 12.0, false, 0.0};
-constexpr TmemModel kTmemPair = {0.92, 12.0, true, 0.07};
-// the wide single-CTA form: a 16-deep K block of a 256 x 128 unit ~0.455 us
-// (2048^3: one round of 128 blocks, 70.3 us), as efficient per SM as the
-// pair, on tiles of half its size
-constexpr TmemModel kTmemWide = {0.455, 12.0, false, 0.0};
+constexpr TmemModel kTmemSingle = {0.57, 12.0, false, 0.0, false};
+constexpr TmemModel kTmemPair = {0.92, 12.0, true, 0.07, false};
+// The wide single-CTA form: a 16-deep K block of a 256 x 128 unit ~0.455 us
+// (2048^3: one round of 128 blocks, 70.3 us), as fast per SM as the pair in
+// one round of its grid (and ~4 % faster with 16 or more splits added in
+// the kernel: 256 x 256 x 65536, 512^2 x 16384).  Over several rounds, and
+// on padded copies of the operands, it ran 10-25 % behind the pair (4096^3
+// 490 against 431 us, 2560^3 136 against 124, 961 x 6697 x 8131 810
+// against 650): a unit loads 1.5 times the pair's operand bytes per output,
+// so AUTO takes it only for operands read in place and one round of units.
+constexpr TmemModel kTmemWide = {0.455, 12.0, false, 0.0, true};
 
 double tmem_estimate(int slots, int tiles, int kb_total, int M, int N, const TmemModel& mdl,
                      int forced_splits, int* splits_out) {
     constexpr double kReduceLaunchUs = 3.0, kReduceBytesPerUs = 5.0e6;
     int best = 1;
     double best_us = 0.0;
+    bool found = false;
     const int s_max = std::min(GEMM_F32_MAX_SPLITS, std::max(1, kb_total / 4));
     const int s_lo = forced_splits > 0 ? std::min(forced_splits, std::max(kb_total, 1)) : 1;
     const int s_hi = forced_splits > 0 ? s_lo : s_max;
@@ -397,6 +404,7 @@ double tmem_estimate(int slots, int tiles, int kb_total, int M, int N, const Tme
         const int eff = (kb_total + per - 1) / per;  // splits that get work
         if (eff != s && forced_splits <= 0) continue;
         const long long units = static_cast<long long>(tiles) * s;
+        if (mdl.one_round && units > slots) continue;
         double rounds = static_cast<double>((units + slots - 1) / slots);
         // without split-K the pair form cuts a partly idle last round into
         // T K shares (see make_plan): that round then takes 1 / T
@@ -411,13 +419,14 @@ double tmem_estimate(int slots, int tiles, int kb_total, int M, int N, const Tme
             us += kReduceLaunchUs +
                   (2.0 * s + 1.0) * M * static_cast<double>(N) * 4.0 / kReduceBytesPerUs;
         if (s >= 16 && units <= slots) us += mdl.reduce_wait_us * s;
-        if (s == s_lo || us < best_us) {
+        if (!found || us < best_us) {
             best = s;
             best_us = us;
+            found = true;
         }
     }
     if (splits_out) *splits_out = best;
-    return best_us;
+    return found ? best_us : 1e30;
 }
 
 size_t carve(size_t* off, long long bytes) {
@@ -526,8 +535,9 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
             const double us2 =
                 have_pair ? tmem_estimate(clusters, t256, kb, M, N, kTmemPair, splits, nullptr)
                           : us1 + 1.0;
-            const double us3 = tmem_estimate(d.sm_count, twide, kbw, M, N, kTmemWide, splits,
-                                             nullptr);
+            const double us3 =
+                in_place ? tmem_estimate(d.sm_count, twide, kbw, M, N, kTmemWide, splits, nullptr)
+                         : 1e30;
             p->tmem_b = 1;
             p->pair = us2 < us1 && us2 <= us3 ? 1 : 0;
             p->tmem_wide = !p->pair && us3 < us1 ? 1 : 0;
