@@ -2,7 +2,8 @@
 //
 //  * pad_copy:       copies a row-major operand into a buffer whose row
 //                    stride is a multiple of 16 bytes and whose base is
-//                    256-byte aligned, the form a TMA descriptor requires.
+//                    256-byte aligned, the form a TMA descriptor requires
+//                    (16-byte stores of four columns a thread).
 //  * splitk_reduce:  C = sum of the split-K partial products, added in split
 //                    order 0, 1, ..., S-1 so that the result is deterministic;
 //                    the partials are loaded several at a time (independent
@@ -40,6 +41,33 @@ pad_copy_kernel(const float* __restrict__ src, long long lds, long long rows, lo
         for (long long c = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; c < cols;
              c += static_cast<long long>(gridDim.x) * kThreads)
             d[c] = s[c];
+    }
+}
+
+// Vector form: the destination rows 16-byte aligned (ldd a multiple of 4,
+// 16-byte base).  A thread copies four adjacent columns: four scalar loads
+// of the source (coalesced across the warp whatever its alignment) and one
+// 16-byte store, so that each thread has four loads in flight; a bounded
+// grid of blocks steps over the rows (one 256-column block a row moved 1 KB
+// a block and left the copies of deep-K operands at a fraction of HBM
+// bandwidth).
+__global__ void __launch_bounds__(kThreads)
+pad_copy4_kernel(const float* __restrict__ src, long long lds, long long rows, long long cols,
+                 float* __restrict__ dst, long long ldd) {
+    pdl_trigger();
+    const long long quads = (cols + 3) / 4;
+    for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
+        const float* s = src + r * lds;
+        float* d = dst + r * ldd;
+        for (long long q = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; q < quads;
+             q += static_cast<long long>(gridDim.x) * kThreads) {
+            const long long c = 4 * q;
+            if (c + 3 < cols) {
+                *reinterpret_cast<float4*>(d + c) = make_float4(s[c], s[c + 1], s[c + 2], s[c + 3]);
+            } else {
+                for (long long i = c; i < cols; ++i) d[i] = s[i];
+            }
+        }
     }
 }
 
@@ -191,6 +219,14 @@ unsigned grid_1d(long long work, long long per_block, unsigned cap) {
 cudaError_t launch_pad_copy(const float* src, long long lds, long long rows, long long cols,
                             float* dst, long long ldd, cudaStream_t s) {
     if (rows <= 0 || cols <= 0) return cudaSuccess;
+    if (ldd % 4 == 0 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+        // about 2048 blocks in all: a few per SM, each over many rows
+        const unsigned gx = grid_1d((cols + 3) / 4, kThreads, 64);
+        const long long gy_cap = (2048 + gx - 1) / gx;
+        const unsigned gy = static_cast<unsigned>(rows < gy_cap ? rows : gy_cap);
+        pad_copy4_kernel<<<dim3(gx, gy), kThreads, 0, s>>>(src, lds, rows, cols, dst, ldd);
+        return cudaGetLastError();
+    }
     dim3 grid(grid_1d(cols, kThreads, 64), static_cast<unsigned>(rows < 65535 ? rows : 65535));
     pad_copy_kernel<<<grid, kThreads, 0, s>>>(src, lds, rows, cols, dst, ldd);
     return cudaGetLastError();

@@ -362,3 +362,16 @@ def test_wide_quantised_exact_and_misaligned():
     A, B = make_workload(1, M=M, N=N, K=K)
     C = _gpu.run_configured(A, B, g.ALGO_3XTF32, WIDE, 0, offsets=(3, 2, 1))
     _check(C, oracle.ref_gemm(A, B), label="tmem wide, misaligned operands")
+
+
+@pytest.mark.parametrize("alpha,beta", [(0.5, -0.75), (1.0, 1.0)])
+def test_wide_general_form_through_auto(alpha, beta):
+    # alpha/beta and padded leading dimensions on a shape AUTO sends to the
+    # wide form with its partials added inside the kernel (19 splits of 8
+    # tiles: one round), so that the in-kernel reduction applies alpha/beta
+    from .test_gemm_gpu import _ex_case
+    M, N, K = 512, 512, 16384
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and (p["tile_m"], p["tile_n"]) == (256, 128), p
+    assert p["reduce_in_kernel"] == 1 and p["kernels"] == 1, p
+    _ex_case(M, N, K, 0, 0, 4, alpha, beta, g.ALGO_AUTO)
