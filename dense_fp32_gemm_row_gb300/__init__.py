@@ -32,7 +32,7 @@ __all__ = [
     "gemm_f32_configured", "gemm_f32_plan_config", "Config", "TILE_AUTO", "TILE_128x128",
     "TILE_128x256", "TILE_256x256_PAIR", "TILE_256x256_PAIR_SPLIT", "TILE_128x128_SPLIT",
     "TILE_128x128_TMEM", "TILE_256x256_TMEM", "TILE_256x128_TMEM",
-    "gemm_f32_plan", "gemm_f32_device_status", "gemm_f32_selftest_watchdog",
+    "gemm_f32_plan", "gemm_f32_plan_ex", "gemm_f32_device_status", "gemm_f32_selftest_watchdog",
     "gemm_f32_noalloc_selftest_watchdog", "gemm_f32_inject_host_fault", "INJECT_NONE",
     "INJECT_WORKSPACE", "INJECT_DESCRIPTOR",
     "gemm_f32_release", "gemm_f32_status_string", "gemm_f32_version", "matmul", "check",
@@ -117,6 +117,8 @@ def load():
         lib.gemm_f32_algo_splitk.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
         lib.gemm_f32_algo_splitk_ev.argtypes = [vp, vp, vp, i, i, i, i, i, vp, vp, vp]
         lib.gemm_f32_plan.argtypes = [i, i, i, i, i, vp, vp, vp, ctypes.POINTER(PlanInfo)]
+        lib.gemm_f32_plan_ex.argtypes = [i, i, i, i, i, vp, ll, vp, ll, vp, ll, i, i,
+                                         ctypes.POINTER(PlanInfo)]
         lib.gemm_f32_noalloc.argtypes = [vp, vp, vp, i, i, i, i, vp]
         lib.gemm_f32_host.argtypes = [vp, vp, vp, i, i, i, i, vp]
         lib.gemm_f32_configured.argtypes = [vp, vp, vp, i, i, i, ctypes.POINTER(Config), vp]
@@ -133,7 +135,8 @@ def load():
         lib.gemm_f32_status_string.restype = ctypes.c_char_p
         lib.gemm_f32_version.argtypes = []
         for name in ("gemm_f32", "gemm_f32_algo", "gemm_f32_algo_splitk",
-                     "gemm_f32_algo_splitk_ev", "gemm_f32_plan", "gemm_f32_noalloc",
+                     "gemm_f32_algo_splitk_ev", "gemm_f32_plan", "gemm_f32_plan_ex",
+                     "gemm_f32_noalloc",
                      "gemm_f32_host", "gemm_f32_ex", "gemm_f32_configured", "gemm_f32_plan_config",
                      "gemm_f32_device_status", "gemm_f32_selftest_watchdog",
                      "gemm_f32_noalloc_selftest_watchdog", "gemm_f32_inject_host_fault",
@@ -202,6 +205,17 @@ def gemm_f32_noalloc(A, B, C, M, N, K, splits=0, stream=0) -> int:
 def gemm_f32_plan(M, N, K, algo=ALGO_AUTO, splits=0, A=0, B=0, C=0) -> tuple[int, dict]:
     info = PlanInfo()
     st = load().gemm_f32_plan(M, N, K, algo, splits, _p(A), _p(B), _p(C), ctypes.byref(info))
+    return st, info.as_dict()
+
+
+def gemm_f32_plan_ex(transa, transb, M, N, K, lda, ldb, ldc, algo=ALGO_AUTO, splits=0, A=0,
+                     B=0, C=0) -> tuple[int, dict]:
+    """The plan gemm_f32_ex would run for these transposes, sizes and leading
+    dimensions (pointers optional: they only decide the alignment copies)."""
+    info = PlanInfo()
+    st = load().gemm_f32_plan_ex(int(transa), int(transb), M, N, K, _p(A), int(lda), _p(B),
+                                 int(ldb), _p(C), int(ldc), int(algo), int(splits),
+                                 ctypes.byref(info))
     return st, info.as_dict()
 
 

@@ -507,12 +507,15 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         // 896^2 x 4096 39.6 against 58.0, 2048^3 76 against 89, 8192^3 3.18
         // against 3.53 ms), and the kernels that split A and B in shared
         // memory (now forced configurations only) on every shape those were
-        // chosen for (89 x 1216 x 24336 47.7 against 74.4 us).  Operands that
-        // need padded copies take them too once C has 3M elements, where the
-        // copies' cost is small beside the kernel's gain (random shapes:
-        // 1172 x 3326 x 163 27 against 44 us, 1570 x 4603 x 750 83 against
-        // 111, 1500 x 2079 x 21955 827 against 1086); below that the staged
-        // kernels mostly win (339 x 1810 x 4223 88.7 against 56.0 us).  The
+        // chosen for (89 x 1216 x 24336 47.7 against 74.4 us).  Row-major
+        // operands that need padded copies (a row stride or base off 16
+        // bytes) take them too: with the copies at HBM rate the pair or
+        // single-CTA form after them beat the staged kernels on 24 of the 29
+        // such random shapes and trailed by at most 10 % on the others, all
+        // calls of ~20 us (5170 x 151 x 5906 126 against 166 us, 1184 x 988
+        // x 30671 321 against 490, 301 x 1874 x 563 25 against 23).
+        // Transposed operands do once C has 3M elements (their transposed
+        // copy against the staged kernels' split-and-transpose pass).  The
         // CTA-pair form (256 x 256 tiles, N = 256 MMAs) or the single-CTA
         // one, whichever the model times shorter with its own split-K
         // factor: 1536^2 x 8192 pair with 2 splits 136 against 164.5 us for
@@ -520,7 +523,7 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
         // 25 against 27 us.
         const bool in_place = !q.ta && !q.tb && q.lda % 4 == 0 && q.ldb % 4 == 0 &&
                               !misaligned16(q.A) && !misaligned16(q.B);
-        if (in_place || static_cast<double>(M) * N >= 3.0e6) {
+        if (in_place || (!q.ta && !q.tb) || static_cast<double>(M) * N >= 3.0e6) {
             int clusters = 0;
             const bool have_pair =
                 tf32x3_tmem_pair_clusters(d.sm_count, &clusters) == cudaSuccess && clusters > 0;
@@ -1220,12 +1223,15 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
     // the middle panels reuse them), and the last panel's blocks go back to
     // the host one by one, so only the last block's copy is not overlapped.
     // With B's split in tensor memory there is nothing to stage: a block's
-    // GEMM reads its columns of B where they landed (row stride N).
+    // GEMM reads its columns of B where they landed (row stride N), which
+    // TMA can do only when that stride (and A's, K) is a multiple of 16
+    // bytes; otherwise the row panels run on the padded copies.
     const int nc = static_cast<int>(round_up((N + 3) / 4, 256));
     const int nblk = (N + nc - 1) / nc;
     Plan pc;
     const bool tmem_blocks = p.algo == GEMM_F32_ALGO_3XTF32 && p.tmem_b && p.splits == 1 &&
-                             panels >= 2 && N >= 1024 && nblk >= 2 && nblk <= kMaxColBlocks;
+                             !p.stage_a && !p.stage_b && panels >= 2 && N >= 1024 &&
+                             nblk >= 2 && nblk <= kMaxColBlocks;
     bool col_blocks = p.algo == GEMM_F32_ALGO_3XTF32 && !p.split_in_kernel && p.splits == 1 &&
                       panels >= 2 && N >= 1024 && nblk >= 2 && nblk <= kMaxColBlocks;
     if (tmem_blocks) {
@@ -1234,7 +1240,7 @@ int run_host(const float* A, const float* B, float* C, int M, int N, int K, int 
         qc.ldb = N;
         qc.ldc = N;
         make_plan(*d, qc, GEMM_F32_ALGO_3XTF32, 0, &pc);
-        col_blocks = pc.tmem_b && pc.splits == 1;
+        col_blocks = pc.tmem_b && pc.splits == 1 && !pc.stage_a && !pc.stage_b;
         pc.off_w += p.ws_bytes;
         pc.off_t += p.ws_bytes;
     } else if (col_blocks) {
@@ -1383,71 +1389,14 @@ int check_config(const gemm_f32_config* cfg) {
     return GEMM_F32_SUCCESS;
 }
 
-}  // namespace
-
-extern "C" {
-
-int gemm_f32(const float* A, const float* B, float* C, int M, int N, int K, cudaStream_t stream) {
-    return run(packed(A, B, C, M, N, K), GEMM_F32_ALGO_AUTO, 0, stream);
-}
-
-int gemm_f32_algo(const float* A, const float* B, float* C, int M, int N, int K, int algo,
-                  cudaStream_t stream) {
-    return run(packed(A, B, C, M, N, K), algo, 0, stream);
-}
-
-int gemm_f32_algo_splitk(const float* A, const float* B, float* C, int M, int N, int K, int algo,
-                         int splits, cudaStream_t stream) {
-    return run(packed(A, B, C, M, N, K), algo, splits, stream);
-}
-
-int gemm_f32_ex(int transa, int transb, int M, int N, int K, float alpha, const float* A,
-                long long lda, const float* B, long long ldb, float beta, float* C, long long ldc,
-                int algo, int splits, cudaStream_t stream) {
-    Problem q;
-    q.M = M;
-    q.N = N;
-    q.K = K;
-    q.A = A;
-    q.lda = lda;
-    q.ta = transa;
-    q.B = B;
-    q.ldb = ldb;
-    q.tb = transb;
-    q.C = C;
-    q.ldc = ldc;
-    q.alpha = alpha;
-    q.beta = beta;
-    return run(q, algo, splits, stream);
-}
-
-int gemm_f32_algo_splitk_ev(const float* A, const float* B, float* C, int M, int N, int K,
-                            int algo, int splits, cudaStream_t stream, cudaEvent_t main_begin,
-                            cudaEvent_t main_end) {
-    return run(packed(A, B, C, M, N, K), algo, splits, stream, main_begin, main_end);
-}
-
-int gemm_f32_configured(const float* A, const float* B, float* C, int M, int N, int K,
-                        const gemm_f32_config* cfg, cudaStream_t stream) {
-    const int st = check_config(cfg);
-    if (st != GEMM_F32_SUCCESS) return st;
-    return run(packed(A, B, C, M, N, K), cfg->algo, cfg->splits, stream, nullptr, nullptr,
-               cfg->tile);
-}
-
-int gemm_f32_host(const float* A, const float* B, float* C, int M, int N, int K, int algo,
-                  cudaStream_t stream) {
-    return run_host(A, B, C, M, N, K, algo, stream);
-}
-
-int gemm_f32_plan_config(int M, int N, int K, const gemm_f32_config* cfg, const float* A,
-                         const float* B, const float* C, gemm_f32_plan_info* out) {
+// The plan a call of problem q with configuration cfg would run, without
+// running it (plan_info out): the body of the gemm_f32_plan entry points.
+int plan_problem(const Problem& q, const gemm_f32_config* cfg, gemm_f32_plan_info* out) {
     if (!out) return GEMM_F32_ERR_INVALID_VALUE;
     std::memset(out, 0, sizeof(*out));
     int st = check_config(cfg);
     if (st != GEMM_F32_SUCCESS) return st;
-    // pointers are optional here: they only decide the alignment staging
-    const Problem q = packed(A, B, const_cast<float*>(C), M, N, K);
+    const int M = q.M, N = q.N, K = q.K;
     st = validate(q, cfg->algo, cfg->splits, false);
     if (st != GEMM_F32_SUCCESS) return st;
     out->splits = 1;
@@ -1513,6 +1462,92 @@ int gemm_f32_plan_config(int M, int N, int K, const gemm_f32_config* cfg, const 
     out->b_in_tmem = p.tmem_b;
     return GEMM_F32_SUCCESS;
 }
+
+}  // namespace
+
+extern "C" {
+
+int gemm_f32(const float* A, const float* B, float* C, int M, int N, int K, cudaStream_t stream) {
+    return run(packed(A, B, C, M, N, K), GEMM_F32_ALGO_AUTO, 0, stream);
+}
+
+int gemm_f32_algo(const float* A, const float* B, float* C, int M, int N, int K, int algo,
+                  cudaStream_t stream) {
+    return run(packed(A, B, C, M, N, K), algo, 0, stream);
+}
+
+int gemm_f32_algo_splitk(const float* A, const float* B, float* C, int M, int N, int K, int algo,
+                         int splits, cudaStream_t stream) {
+    return run(packed(A, B, C, M, N, K), algo, splits, stream);
+}
+
+int gemm_f32_ex(int transa, int transb, int M, int N, int K, float alpha, const float* A,
+                long long lda, const float* B, long long ldb, float beta, float* C, long long ldc,
+                int algo, int splits, cudaStream_t stream) {
+    Problem q;
+    q.M = M;
+    q.N = N;
+    q.K = K;
+    q.A = A;
+    q.lda = lda;
+    q.ta = transa;
+    q.B = B;
+    q.ldb = ldb;
+    q.tb = transb;
+    q.C = C;
+    q.ldc = ldc;
+    q.alpha = alpha;
+    q.beta = beta;
+    return run(q, algo, splits, stream);
+}
+
+int gemm_f32_algo_splitk_ev(const float* A, const float* B, float* C, int M, int N, int K,
+                            int algo, int splits, cudaStream_t stream, cudaEvent_t main_begin,
+                            cudaEvent_t main_end) {
+    return run(packed(A, B, C, M, N, K), algo, splits, stream, main_begin, main_end);
+}
+
+int gemm_f32_configured(const float* A, const float* B, float* C, int M, int N, int K,
+                        const gemm_f32_config* cfg, cudaStream_t stream) {
+    const int st = check_config(cfg);
+    if (st != GEMM_F32_SUCCESS) return st;
+    return run(packed(A, B, C, M, N, K), cfg->algo, cfg->splits, stream, nullptr, nullptr,
+               cfg->tile);
+}
+
+int gemm_f32_host(const float* A, const float* B, float* C, int M, int N, int K, int algo,
+                  cudaStream_t stream) {
+    return run_host(A, B, C, M, N, K, algo, stream);
+}
+
+int gemm_f32_plan_config(int M, int N, int K, const gemm_f32_config* cfg, const float* A,
+                         const float* B, const float* C, gemm_f32_plan_info* out) {
+    // pointers are optional here: they only decide the alignment staging
+    return plan_problem(packed(A, B, const_cast<float*>(C), M, N, K), cfg, out);
+}
+
+int gemm_f32_plan_ex(int transa, int transb, int M, int N, int K, const float* A, long long lda,
+                     const float* B, long long ldb, const float* C, long long ldc, int algo,
+                     int splits, gemm_f32_plan_info* out) {
+    Problem q;
+    q.M = M;
+    q.N = N;
+    q.K = K;
+    q.A = A;
+    q.lda = lda;
+    q.ta = transa;
+    q.B = B;
+    q.ldb = ldb;
+    q.tb = transb;
+    q.C = const_cast<float*>(C);
+    q.ldc = ldc;
+    gemm_f32_config cfg;
+    cfg.algo = algo;
+    cfg.tile = GEMM_F32_TILE_AUTO;
+    cfg.splits = splits;
+    return plan_problem(q, &cfg, out);
+}
+
 
 int gemm_f32_plan(int M, int N, int K, int algo, int splits, const float* A, const float* B,
                   const float* C, gemm_f32_plan_info* out) {

@@ -215,6 +215,17 @@ int gemm_f32_plan(int M, int N, int K, int algo, int splits,
                   gemm_f32_plan_info* out);
 
 /*
+ * gemm_f32_plan_ex -- the plan gemm_f32_ex would run for the same transa,
+ * transb, sizes, leading dimensions, algo and splits (alpha and beta do not
+ * change it), without running it.  A, B, C are optional (NULL): like the
+ * leading dimensions they only decide which operands need a padded or
+ * transposed copy.  Returns GEMM_F32_SUCCESS or GEMM_F32_ERR_INVALID_VALUE.
+ */
+int gemm_f32_plan_ex(int transa, int transb, int M, int N, int K, const float* A, long long lda,
+                     const float* B, long long ldb, const float* C, long long ldc, int algo,
+                     int splits, gemm_f32_plan_info* out);
+
+/*
  * gemm_f32_config / gemm_f32_configured / gemm_f32_plan_config -- run (or
  * plan) C = A * B with a forced kernel configuration instead of the
  * library's choice: the tool behind design-space sweeps ("Lecture 12: final
@@ -235,9 +246,10 @@ int gemm_f32_plan(int M, int N, int K, int algo, int splits,
  * no transpose in shared memory).  _256x256_TMEM is its CTA-pair form
  * (256 x 256 tiles, N = 256 MMAs), and _256x128_TMEM its wide single-CTA
  * form (256 rows by 128 columns, N = 256 MMAs, 16-deep stages).  AUTO
- * takes one of these whenever A and B can be read in place (and, after
- * padded copies, when they cannot but C has at least 3M elements), the one a
- * fitted time model finds shorter.  Invalid combinations return GEMM_F32_ERR_INVALID_VALUE.
+ * takes one of these for row-major A and B (after padded copies where a
+ * row stride or base is not 16-byte aligned; for transposed operands, after
+ * transposed copies, once C has at least 3M elements), the one a fitted time
+ * model finds shorter (the wide form only for operands read in place).  Invalid combinations return GEMM_F32_ERR_INVALID_VALUE.
  */
 #define GEMM_F32_TILE_AUTO          0
 #define GEMM_F32_TILE_128x128       1

@@ -49,11 +49,16 @@ def test_auto_reduces_in_cluster():
     assert st == 0 and p["splits"] == 4 and p["cluster_reduce"] == 1
     A, B = make_workload(2, M=M, N=N, K=K)
     _check(_gpu.run(A, B, g.ALGO_FFMA), oracle.ref_gemm(A, B), label="ffma 1000x1000x250")
-    # AUTO's choice there when A and B cannot be read in place (A's base 4
-    # bytes off a 16-byte boundary): the staged tensor-core kernel, 2 splits,
-    # in a cluster
-    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=(1 << 32) + 4, B=1 << 36, C=1 << 40)
+    # AUTO's choice there for a transposed A (staged operands: the split and
+    # transpose in one pass): the staged tensor-core kernel, 2 splits, in a
+    # cluster
+    st, p = g.gemm_f32_plan_ex(1, 0, M, N, K, M, N, N, g.ALGO_AUTO)
     assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["splits"] == 2 and p["cluster_reduce"] == 1
+    _ex_case(M, N, K, 1, 0, 0, 1.0, 0.0, g.ALGO_AUTO)
+    # A's base 4 bytes off a 16-byte boundary: a padded copy of A, then the
+    # kernel with B's split in tensor memory
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=(1 << 32) + 4, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["b_in_tmem"] == 1 and p["stage_a"] == 1, p
     _check(_gpu.run(A, B, g.ALGO_AUTO, offsets=(1, 0, 0)), oracle.ref_gemm(A, B),
            label="auto 1000x1000x250, A misaligned")
     _check(_gpu.run(A, B, g.ALGO_AUTO), oracle.ref_gemm(A, B), label="auto 1000x1000x250")
@@ -139,7 +144,9 @@ def test_3xtf32_cluster_equals_split_order_sum_of_partials(tile, splits):
 
 
 def test_3xtf32_auto_ragged_plan_reduces_in_cluster():
-    st, p = g.gemm_f32_plan(1025, 1023, 1000, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    # AUTO's staged plan for the ragged shape (a transposed A keeps the
+    # operands staged): 2 splits added in a cluster
+    st, p = g.gemm_f32_plan_ex(1, 0, 1025, 1023, 1000, 1025, 1023, 1023, g.ALGO_AUTO)
     assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["splits"] == 2 and p["cluster_reduce"] == 1
 
 
@@ -168,7 +175,10 @@ def test_3xtf32_clusters_that_do_not_all_fit_use_the_workspace():
     st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, g.TILE_128x256, 7,
                                    A=1 << 32, B=1 << 36, C=1 << 40)
     assert st == 0 and p["splits"] == 7 and p["cluster_reduce"] == 0, p
-    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
+    # (AUTO's staged plan: a transposed A keeps the operands staged; row-major
+    # ones, with N odd, take the kernels with B's split in tensor memory
+    # after a padded copy of B)
+    st, p = g.gemm_f32_plan_ex(1, 0, M, N, K, M, N, N, g.ALGO_AUTO)
     assert st == 0 and p["tile_m"] == 128 and 2 <= p["splits"] <= 8, p
     assert p["cluster_reduce"] == 1, p
     tiles = ((M + 127) // 128) * ((N + p["tile_n"] - 1) // p["tile_n"])

@@ -137,13 +137,12 @@ def test_pair_kernel_rule(shape, want):
     # (2048^2: 64 tiles on 76 pairs), or, net of padding, at least as much of
     # the machine as 128 x 128 tiles with their split-K factor (1792^2 x 4096:
     # 49 pair tiles and 196 single tiles both fill 64 %; 1536^2 x 4096: 36
-    # pair tiles fill 47 %, 144 single tiles 95 %).  A's base 4 bytes off a
-    # 16-byte boundary keeps the operands from being read in place, which
-    # would send these shapes to the kernels with B's split in tensor memory;
-    # with C of 3M elements or more AUTO takes those all the same, after a
-    # padded copy of A.
+    # pair tiles fill 47 %, 144 single tiles 95 %).  A transposed A keeps the
+    # operands staged (row-major ones go to the kernels with B's split in
+    # tensor memory, after padded copies if need be); with C of 3M elements
+    # or more AUTO takes those all the same, after a transposed copy of A.
     M, N, K = shape
-    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_3XTF32, 0, A=(1 << 32) + 4, B=1 << 36, C=1 << 40)
+    st, p = g.gemm_f32_plan_ex(1, 0, M, N, K, M, N, N, g.ALGO_3XTF32)
     assert st == 0 and p["b_in_tmem"] == (M * N >= 3_000_000), p
     if p["b_in_tmem"]:
         assert p["stage_a"] == 1 and p["stage_b"] == 0, p
@@ -164,10 +163,10 @@ def test_single_cta_width_rule(shape, bn):
     # (x 0.85), than 128 x 128 tiles (and vice versa); with K >= 8192 and
     # at least 2048 of it per 128 x 256 unit, 128 x 256 unless 128 x 128
     # tiles keep 3 % more of the SMs busy (640^2 x 8192: 10 splits of 819);
-    # A off a 16-byte boundary, so that the staged kernels are the choice
-    # while C has fewer than 3M elements
+    # A transposed, so that the staged kernels are the choice while C has
+    # fewer than 3M elements
     M, N, K = shape
-    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_3XTF32, 0, A=(1 << 32) + 4, B=1 << 36, C=1 << 40)
+    st, p = g.gemm_f32_plan_ex(1, 0, M, N, K, M, N, N, g.ALGO_3XTF32)
     assert st == 0 and p["b_in_tmem"] == (M * N >= 3_000_000), p
     if p["b_in_tmem"]:
         return

@@ -105,45 +105,48 @@ def test_quantised_exact():
     _check(C, oracle.ref_gemm(A, B), exact=True, label="quantised 512^3, split in kernel")
 
 
-# want: 0 staged kernels, 1 the single-CTA form with B in tensor memory, 2 its pair
-# form, 3 its wide single-CTA form, 23 either of the last two (the model's
-# near-ties: per SM the two run at the same rate, on tiles of different size)
+# want: 1 the single-CTA form with B in tensor memory, 2 its pair form, 3 its
+# wide single-CTA form, 23 either of the last two (the model's near-ties: per
+# SM the two run at the same rate, on tiles of different size), 12 the
+# single-CTA or pair form after padded copies (a row stride not a multiple
+# of 16 bytes)
 @pytest.mark.parametrize("shape,want", [((65536, 256, 1024), 2),
                                         ((2048, 2048, 2048), 23), ((8192, 8192, 8192), 2),
-                                        ((1025, 1023, 1000), 0), ((512, 512, 512), 1),
-                                        ((384, 384, 20000), 1), ((177, 4459, 16098), 0),
-                                        ((9000, 200, 8190), 0), ((9000, 200, 8192), 23),
+                                        ((1025, 1023, 1000), 12), ((512, 512, 512), 1),
+                                        ((384, 384, 20000), 1), ((177, 4459, 16098), 12),
+                                        ((9000, 200, 8190), 12), ((9000, 200, 8192), 23),
                                         ((2560, 2560, 2560), 2), ((3072, 3072, 3072), 23),
                                         ((4096, 4096, 4096), 2), ((1024, 1024, 8192), 23),
-                                        ((2304, 2304, 512), 2), ((386, 358, 15342), 0),
+                                        ((2304, 2304, 512), 2), ((386, 358, 15342), 12),
                                         ((89, 1216, 24336), 1), ((2900, 2900, 1024), 23),
                                         ((1536, 1536, 4096), 23), ((512, 512, 4096), 1),
                                         ((1792, 1792, 4096), 23), ((512, 512, 16384), 3)],
                          ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
 def test_auto_b_in_tensor_memory_rule(shape, want):
-    # AUTO takes a kernel with B's split in tensor memory whenever A and B
-    # can be read as stored: the single-CTA 128 x 128 form, the CTA pair or
-    # the wide single-CTA form, as its model times them (each with its own
-    # split-K factor: 512^2 x 4096, 9 splits of 16 single tiles; 512^2 x
-    # 16384, 19 splits of 8 wide tiles; 256 x 256 x 65536 in the deep-K
-    # test); a row stride that is not a multiple of 16 bytes (1025 x 1023,
-    # 177 x 4459, 9000 x 200 x 8190, 386 x 358 x 15342) keeps the staged
-    # kernels unless C has 3M elements or more
+    # AUTO takes a kernel with B's split in tensor memory for row-major A and
+    # B: the single-CTA 128 x 128 form, the CTA pair or the wide single-CTA
+    # form, as its model times them (each with its own split-K factor: 512^2
+    # x 4096, 9 splits of 16 single tiles; 512^2 x 16384, 19 splits of 8 wide
+    # tiles; 256 x 256 x 65536 in the deep-K test); a row stride that is not
+    # a multiple of 16 bytes (1025 x 1023, 177 x 4459, 9000 x 200 x 8190,
+    # 386 x 358 x 15342) first gets a padded copy, and the wide form is not
+    # offered on copies
     M, N, K = shape
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=1 << 32, B=1 << 36, C=1 << 40)
-    assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["b_in_tmem"] == (want > 0), p
-    if want:
-        forms = {1: [(128, 128)], 2: [(256, 256)], 3: [(256, 128)],
-                 23: [(256, 256), (256, 128)]}[want]
-        assert (p["tile_m"], p["tile_n"]) in forms and p["split_in_kernel"] == 1, p
-        assert p["stage_a"] == 0 and p["stage_b"] == 0, p
-        assert p["cluster_reduce"] == 0, p
-    # A misaligned by 4 bytes: a padded copy of A, which only a large C pays
-    # for
+    assert st == 0 and p["algo"] == g.ALGO_3XTF32 and p["b_in_tmem"] == 1, p
+    forms = {1: [(128, 128)], 2: [(256, 256)], 3: [(256, 128)], 23: [(256, 256), (256, 128)],
+             12: [(128, 128), (256, 256)]}[want]
+    assert (p["tile_m"], p["tile_n"]) in forms and p["split_in_kernel"] == 1, p
+    assert p["stage_a"] == (K % 4 != 0) and p["stage_b"] == (N % 4 != 0), p
+    assert p["cluster_reduce"] == 0, p
+    # A misaligned by 4 bytes: a padded copy of A, then the single-CTA or
+    # pair form
     st, p = g.gemm_f32_plan(M, N, K, g.ALGO_AUTO, 0, A=(1 << 32) + 4, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["b_in_tmem"] == 1 and p["stage_a"] == 1, p
+    assert (p["tile_m"], p["tile_n"]) in ((128, 128), (256, 256)), p
+    # transposed A: staged unless C has 3M elements or more
+    st, p = g.gemm_f32_plan_ex(1, 0, M, N, K, M, N, N, g.ALGO_AUTO)
     assert st == 0 and p["b_in_tmem"] == (M * N >= 3_000_000), p
-    if p["b_in_tmem"]:
-        assert p["stage_a"] == 1 and p["stage_b"] == 0, p
 
 
 def test_auto_skinny_parity():
