@@ -249,7 +249,8 @@ int gemm_f32_plan_ex(int transa, int transb, int M, int N, int K, const float* A
  * takes one of these for row-major A and B (after padded copies where a
  * row stride or base is not 16-byte aligned; for transposed operands, after
  * transposed copies, once C has at least 3M elements), the one a fitted time
- * model finds shorter (the wide form only for operands read in place).  Invalid combinations return GEMM_F32_ERR_INVALID_VALUE.
+ * model finds shorter (the wide form only for operands read in place).
+ * Invalid combinations return GEMM_F32_ERR_INVALID_VALUE.
  */
 #define GEMM_F32_TILE_AUTO          0
 #define GEMM_F32_TILE_128x128       1
