@@ -88,15 +88,20 @@ splitk_reduce_kernel(const float* __restrict__ ws, long long split_stride, long 
     }
 }
 
-// Vector form: ldw, ldc, N multiples of 4 and both bases 16-byte aligned.
-// The partials are loaded kVecBatch at a time (independent loads in flight)
-// and added in split order, as above.
+// Vector form: the partials are read as float4 (ldw and the split stride
+// multiples of 4, ldw at least N rounded up to 4, the workspace 16-byte
+// aligned: the padding columns are read and dropped), kVecBatch at a time
+// (independent loads in flight), and added in split order, as above.  C is
+// written as float4 where its rows allow (cvec: ldc a multiple of 4 and C
+// 16-byte aligned) and element by element otherwise, so that an odd N keeps
+// the vector loads.
 constexpr int kVecBatch = 4;
 __global__ void __launch_bounds__(kThreads)
 splitk_reduce4_kernel(const float4* __restrict__ ws, long long split_stride4, long long ldw4,
-                      int splits, float* __restrict__ C, long long ldc, int M, int N4, float alpha,
-                      float beta, int mode) {
+                      int splits, float* __restrict__ C, long long ldc, int M, int N, bool cvec,
+                      float alpha, float beta, int mode) {
     pdl_wait();  // the partials of the GEMM kernel before it
+    const long long N4 = (static_cast<long long>(N) + 3) / 4;
     for (long long r = blockIdx.y; r < M; r += gridDim.y) {
         const float4* w = ws + r * ldw4;
         float* c = C + r * ldc;
@@ -118,7 +123,7 @@ splitk_reduce4_kernel(const float4* __restrict__ ws, long long split_stride4, lo
                     }
                 }
             }
-            store4(c, static_cast<int>(4 * j), 4 * N4, sum, true, alpha, beta, mode);
+            store4(c, static_cast<int>(4 * j), N, sum, cvec, alpha, beta, mode);
         }
     }
 }
@@ -237,9 +242,9 @@ cudaError_t launch_splitk_reduce(const float* ws, long long split_stride, long l
                                  float beta, int scale_mode, cudaStream_t s) {
     if (M <= 0 || N <= 0) return cudaSuccess;
     const unsigned gy = static_cast<unsigned>(M < 65535 ? M : 65535);
-    const bool vec = (N % 4 == 0) && (ldw % 4 == 0) && (ldc % 4 == 0) && (split_stride % 4 == 0) &&
-                     (reinterpret_cast<uintptr_t>(ws) % 16 == 0) &&
-                     (reinterpret_cast<uintptr_t>(C) % 16 == 0);
+    const bool vec = (ldw % 4 == 0) && (ldw >= (static_cast<long long>(N) + 3) / 4 * 4) &&
+                     (split_stride % 4 == 0) && (reinterpret_cast<uintptr_t>(ws) % 16 == 0);
+    const bool cvec = (ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(C) % 16 == 0);
     // launched programmatically after the GEMM kernel (pdl_wait in the kernel)
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
@@ -256,9 +261,9 @@ cudaError_t launch_splitk_reduce(const float* ws, long long split_stride, long l
         e = cudaLaunchKernelEx(&cfg, splitk_reduce_deep_kernel, ws, split_stride, ldw, splits, C,
                                ldc, M, N, alpha, beta, scale_mode);
     } else if (vec) {
-        cfg.gridDim = dim3(grid_1d(N / 4, kThreads, 64), gy);
+        cfg.gridDim = dim3(grid_1d((N + 3) / 4, kThreads, 64), gy);
         e = cudaLaunchKernelEx(&cfg, splitk_reduce4_kernel, reinterpret_cast<const float4*>(ws),
-                               split_stride / 4, ldw / 4, splits, C, ldc, M, N / 4, alpha, beta,
+                               split_stride / 4, ldw / 4, splits, C, ldc, M, N, cvec, alpha, beta,
                                scale_mode);
     } else {
         cfg.gridDim = dim3(grid_1d(N, kThreads, 64), gy);
