@@ -195,7 +195,8 @@ struct Plan {
     int tmem_b = 0;           // 3xTF32: the 128 x 128 kernel with B's split in tensor memory
     int tmem_wide = 0;        // ... in its wide single-CTA form (256 x 128 tiles, N = 256 MMAs)
     int reduce_in_kernel = 0; // that kernel adds its split-K partials itself (one unit per CTA)
-    int cluster_splits = 0;   // FFMA: split-K partials added inside a cluster (2..4)
+    int cluster_splits = 0;   // split-K partials added inside a cluster (FFMA 2..4, the
+                              // single-CTA tensor-core kernels 2..8)
     int fused_staging = 0;    // 3xTF32 staged: A and B split by one launch
     int box_n = 0;    // 3xTF32: B^T rows per TMA box
     int tail_tiles = 0, tail_splits = 0;  // pair kernel: K-split last partial round
@@ -662,6 +663,18 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
             p->cluster_splits = p->splits;
         cudaGetLastError();
     }
+    // The single-CTA form with B's split in tensor memory likewise (its stage
+    // memory holds the 128 x 128 partial after the main loop): no workspace
+    // and no reduction launch (1025 x 1023 x 1000, 2 splits: the reduction
+    // kernel was ~4 us of a ~35 us call).  From 16 splits it adds them in
+    // the kernel through the workspace instead (below).
+    if (p->tmem_b && !p->pair && !p->tmem_wide && p->splits >= 2 && p->splits <= 8 &&
+        units <= d.sm_count) {
+        int fit = 0;
+        if (tf32x3_tmem_cluster_capacity(p->splits, &fit) == cudaSuccess && tiles <= fit)
+            p->cluster_splits = p->splits;
+        cudaGetLastError();
+    }
     if (p->splits > 1 && !p->cluster_splits)
         p->off_w = carve(&off, static_cast<long long>(p->splits) * M * p->ldw * 4);
     // The pair kernel's last round of tiles is usually only partly full
@@ -825,6 +838,8 @@ int launch_gemm(const Plan& p, const DeviceState& d, const Operands& o, float* C
             ta.alpha = alpha;
             ta.beta = beta;
             ta.scale_mode = kmode;
+            ta.cluster_splits = p.cluster_splits;
+            ta.vec_store = vec_store;
             if (p.reduce_in_kernel) {
                 ta.counters = reinterpret_cast<int*>(ws);
                 ta.c_final = C;

@@ -129,8 +129,11 @@ cudaError_t tf32x3_single_cluster_capacity(int bn, int splits, int* clusters);
 cudaError_t launch_sgemm_3xtf32(const Tf32x3Args& a, cudaStream_t s, int sm_count);
 // The 128 x 128 kernel with B's split in tensor memory (A and B as stored,
 // in tmAhi {K, M} boxes 32 x 128 and tmBhi {N, K} boxes 32 x 32, both with
-// 128-byte swizzle); out gets C, or split partials, like the kernels above.
+// 128-byte swizzle); out gets C, or split partials, like the kernels above
+// (with cluster_splits, C: the splits of a tile added inside a cluster).
 cudaError_t launch_sgemm_3xtf32_tmem(const Tf32x3Args& a, cudaStream_t s, int sm_count);
+// clusters of `splits` CTAs of the single-CTA form resident at once
+cudaError_t tf32x3_tmem_cluster_capacity(int splits, int* clusters);
 Tf32x3Config tf32x3_tmem_config(bool pair);
 cudaError_t tf32x3_tmem_ctas_per_sm(int* ctas_per_sm);
 // Its wide single-CTA form: 256 x 128 tiles (256 rows m, 128 columns n) with

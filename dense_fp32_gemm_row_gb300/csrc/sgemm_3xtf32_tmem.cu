@@ -49,6 +49,11 @@
 //                warp's quarter (128 columns), hand the buffer back and add
 //                them into 128 registers in chunk order; at the end of a
 //                unit store them to C (or to the split-K partials).
+// With 2..8 K splits and one unit per CTA the splits of a tile can run as
+// one thread-block cluster (cluster_splits): each CTA parks its partial in
+// its drained stage memory, and after a cluster barrier every CTA sums a
+// band of the tile's rows over the S partials through distributed shared
+// memory, in split order, and writes C; no workspace, no reduction launch.
 // Every wait is bounded; a timeout sets the device fault word and a shared
 // abort flag that ends the other roles' waits, and the CTA winds down (its
 // in-flight copies and MMAs waited for, bounded) before freeing its tensor
@@ -97,6 +102,23 @@ __device__ __forceinline__ float lds32(uint32_t addr) {
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
 }
+
+__device__ __forceinline__ void sts32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// 16 bytes of another CTA's shared memory (a shared::cluster address)
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t cluster_addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
+// split-K partials of the single-CTA form added inside a (portable) cluster
+constexpr int kMaxTmemClusterSplits = 8;
 
 __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
     int v;
@@ -237,7 +259,8 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
                          long long ldo, long long split_stride, int M, int N, int K,
                          int kb_per_split, int splits, unsigned* fault, long long timeout_ns,
                          float alpha, float beta, int scale_mode, int* counters,
-                         float* __restrict__ c_final, long long ldc, int c_mode) {
+                         float* __restrict__ c_final, long long ldc, int c_mode,
+                         int cluster_splits, int vec_store) {
     using C = TmemCfg;
     constexpr int STAGES = C::STAGES;
     extern __shared__ unsigned char smem_raw[];
@@ -297,7 +320,8 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
             int it = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM);
+                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM,
+                                      cluster_splits);
                 for (int kb = 0; kb < w.nkb; ++kb, ++it) {
                     const int s = it % STAGES;
                     if (it >= STAGES &&
@@ -341,7 +365,8 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
             int g = 0;   // chunks issued (accumulator buffer g & 1)
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM);
+                const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM,
+                                      cluster_splits);
                 for (int c0 = 0; c0 < w.nkb && ok; c0 += CH, ++g) {
                     const int buf = g & 1;
                     if (g >= 2 && !role_wait(acce0 + 8 * buf, ((g >> 1) & 1) ^ 1, timeout_ns, fault,
@@ -397,7 +422,8 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
         int it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM);
+            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM,
+                                  cluster_splits);
             for (int kb = 0; kb < w.nkb; ++kb, ++it) {
                 const int s = it % STAGES;
                 const bool got = role_wait(full0 + 8 * (it % C::NFULL), (it / C::NFULL) & 1,
@@ -428,7 +454,8 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
         int it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM);
+            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM,
+                                  cluster_splits);
             for (int kb = 0; kb < w.nkb; ++kb, ++it) {
                 const int s = it % STAGES;
                 const bool got = role_wait(full0 + 8 * (it % C::NFULL), (it / C::NFULL) & 1,
@@ -472,7 +499,8 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
         int g = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM);
+            const Unit w = decode(u, tiles_m, tiles_n, kb_per_split, kb_total, C::BN, BM,
+                                  cluster_splits);
             for (int c0 = 0; c0 < w.nkb; c0 += CH, ++g) {
                 const int buf = g & 1;
                 const bool got = role_wait(accf0 + 8 * buf, (g >> 1) & 1, timeout_ns, fault,
@@ -503,6 +531,17 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
                 if (lane == 0) mbar_arrive(acce0 + 8 * buf);
             }
             if (!ok) break;
+            if (cluster_splits) {
+                // this CTA's only unit: its raw partial goes into the stage
+                // memory, row-major 128 x 128 (every MMA of the unit, and so
+                // every read of a stage, has completed); a warp writes 32
+                // consecutive words of a row
+                const uint32_t pcol = sbase + 4u * static_cast<uint32_t>(nl);
+#pragma unroll
+                for (int j = 0; j < EPI_COLS; ++j)
+                    sts32(pcol + 4u * static_cast<uint32_t>(C::BN * j), acc[j]);
+                continue;
+            }
             const int n = w.n0 + nl;
             if (n < N) {
                 float* p = out + static_cast<long long>(w.split) * split_stride +
@@ -524,6 +563,67 @@ sgemm_3xtf32_tmem_kernel(const __grid_constant__ CUtensorMap tmA,
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+    if (cluster_splits) {
+        // ---- split-K inside the cluster: CTA rank q of the cluster holds
+        // split q of one tile.  Each CTA sums a 1/S band of the tile's rows
+        // over the S partials through distributed shared memory, in split
+        // order, and writes C (alpha and beta applied there).  Every thread
+        // takes both cluster barriers, whatever its role did. ----
+        cluster_sync();  // every partial parked and visible across the cluster
+        const int S = cluster_splits;
+        const Unit w = decode(static_cast<int>(blockIdx.x), tiles_m, tiles_n, kb_per_split,
+                              kb_total, C::BN, BM, S);
+        const int rows = (BM + S - 1) / S;
+        const int r0 = static_cast<int>(cluster_ctarank()) * rows;
+        const int r1 = min(BM, r0 + rows);
+        constexpr int Q = C::BN / 4;  // 16-byte words per tile row
+        // G float4 groups a thread, each partial's G loads issued together
+        constexpr int G = 6;
+        const int ngroups = (r1 - r0) * Q;
+        if (ld_shared_volatile(abort_flag) == 0u) {
+            for (int base = threadIdx.x; base < ngroups; base += G * C::THREADS) {
+                uint32_t off[G];
+                bool live[G];
+                float4 sum[G];
+                const uint32_t p0 = map_to_cta(sbase, 0u);
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    const int idx = base + j * C::THREADS;
+                    const int i = r0 + idx / Q;
+                    const int c4 = idx - (idx / Q) * Q;
+                    live[j] = idx < ngroups && w.m0 + i < M && w.n0 + 4 * c4 < N;
+                    off[j] = 16u * static_cast<uint32_t>(i * Q + c4);
+                    if (live[j]) sum[j] = ld_dsmem_v4(p0 + off[j]);
+                }
+                for (int q = 1; q < S; ++q) {
+                    const uint32_t pq = map_to_cta(sbase, static_cast<uint32_t>(q));
+                    float4 v[G];
+#pragma unroll
+                    for (int j = 0; j < G; ++j)
+                        if (live[j]) v[j] = ld_dsmem_v4(pq + off[j]);
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        if (live[j]) {
+                            sum[j].x += v[j].x;
+                            sum[j].y += v[j].y;
+                            sum[j].z += v[j].z;
+                            sum[j].w += v[j].w;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    if (!live[j]) continue;
+                    const int idx = base + j * C::THREADS;
+                    const int i = r0 + idx / Q;
+                    const int c4 = idx - (idx / Q) * Q;
+                    store4(out + static_cast<long long>(w.m0 + i) * ldo, w.n0 + 4 * c4, N, sum[j],
+                           vec_store != 0, alpha, beta, scale_mode);
+                }
+            }
+        }
+        cluster_sync();  // no CTA leaves while a partner may still read its partial
     }
     if (counters) {
         const int tiles = tiles_m * tiles_n;
@@ -1339,9 +1439,14 @@ cudaError_t launch_sgemm_3xtf32_tmem(const Tf32x3Args& a, cudaStream_t s, int sm
         if (e != cudaSuccess) return e;
         attr_done_dev = dev;
     }
-    if (a.bn != C::BN || a.pair || a.cluster_splits || a.tail_tiles) return cudaErrorInvalidValue;
+    if (a.bn != C::BN || a.pair || a.tail_tiles) return cudaErrorInvalidValue;
+    // split-K in a cluster: one unit per CTA, the S splits of a tile as one
+    // cluster of S CTAs, C written by the kernel (no workspace)
+    if (a.cluster_splits && (a.cluster_splits != a.splits || a.splits < 2 ||
+                             a.splits > kMaxTmemClusterSplits || a.counters))
+        return cudaErrorInvalidValue;
     const int units = ((a.M + BM - 1) / BM) * ((a.N + C::BN - 1) / C::BN) * a.splits;
-    const int grid = units < sm_count ? units : sm_count;
+    int grid = units < sm_count ? units : sm_count;
     // the in-kernel reduction: one unit per CTA, every CTA resident at once
     if (a.counters && (a.splits < 2 || units > sm_count)) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
@@ -1349,17 +1454,64 @@ cudaError_t launch_sgemm_3xtf32_tmem(const Tf32x3Args& a, cudaStream_t s, int sm
     attr[0] = pdl_attribute();
     attr[1].id = cudaLaunchAttributeCooperative;
     attr[1].val.cooperative = 1;
+    cfg.numAttrs = a.counters ? 2 : 1;
+    if (a.cluster_splits) {
+        grid = units;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(a.splits);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = a.counters ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, kern, a.tmAhi, a.tmBhi, a.out, a.ldo, a.split_stride, a.M, a.N,
                            a.K, a.kb_per_split, a.splits, a.fault, a.timeout_ns, a.alpha, a.beta,
-                           a.scale_mode, a.counters, a.c_final, a.ldc, a.c_mode);
+                           a.scale_mode, a.counters, a.c_final, a.ldc, a.c_mode,
+                           a.cluster_splits, a.vec_store);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+// How many clusters of `splits` CTAs of the single-CTA form can be resident
+// at once (one CTA per SM; clusters are placed within a GPC, so this is
+// below sm_count / splits for most sizes).
+cudaError_t tf32x3_tmem_cluster_capacity(int splits, int* clusters) {
+    using C = TmemCfg;
+    constexpr auto kern = sgemm_3xtf32_tmem_kernel;
+    if (splits < 1 || splits > kMaxTmemClusterSplits) return cudaErrorInvalidValue;
+    static thread_local int cached_dev = -1;
+    static thread_local int cap[kMaxTmemClusterSplits + 1] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (cached_dev != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        for (int sz = 1; sz <= kMaxTmemClusterSplits; ++sz) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = static_cast<unsigned>(sz);
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(static_cast<unsigned>(sz));
+            cfg.blockDim = dim3(C::THREADS);
+            cfg.dynamicSmemBytes = C::SMEM_BYTES;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+            if (e != cudaSuccess) return e;
+            cap[sz] = n;
+        }
+        cached_dev = dev;
+    }
+    *clusters = cap[splits];
+    return cudaSuccess;
 }
 
 cudaError_t launch_sgemm_3xtf32_tmem_wide(const Tf32x3Args& a, cudaStream_t s, int sm_count) {

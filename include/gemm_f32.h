@@ -250,6 +250,12 @@ int gemm_f32_plan_ex(int transa, int transb, int M, int N, int K, const float* A
  * row stride or base is not 16-byte aligned; for transposed operands, after
  * transposed copies, once C has at least 3M elements), the one a fitted time
  * model finds shorter (the wide form only for operands read in place).
+ * Split-K partials are added in split order: by the 128 x 128 forms (staged,
+ * _SPLIT and _TMEM) inside a thread-block cluster when 2..8 splits give
+ * every CTA one unit and the clusters all fit at once (cluster_reduce = 1:
+ * no workspace for them, no reduction launch); by the _TMEM forms inside the
+ * kernel from 16 splits (reduce_in_kernel = 1); otherwise by a reduction
+ * kernel over a workspace.
  * Invalid combinations return GEMM_F32_ERR_INVALID_VALUE.
  */
 #define GEMM_F32_TILE_AUTO          0

@@ -34,11 +34,13 @@ def _device():
     g.gemm_f32_release()
 
 
-# (M, N, K, algo, alpha, beta): the two-CTA kernel, a K split through the
-# workspace, the single-CTA kernel with a clipped output box and a beta
+# (M, N, K, algo, alpha, beta): the two-CTA kernel, K splits (added in a
+# cluster, or through the workspace and the reduction kernel: 512^2 x 4096,
+# 9 splits), the single-CTA kernel with a clipped output box and a beta
 # term, and the CUDA-core kernel
 CASES = [(2304, 2304, 512, g.ALGO_AUTO, 1.0, 0.0),
          (600, 700, 5000, g.ALGO_3XTF32, 1.0, 0.0),
+         (512, 512, 4096, g.ALGO_3XTF32, 1.0, 0.0),
          (300, 200, 40, g.ALGO_3XTF32, 0.5, -0.75),
          (200, 160, 96, g.ALGO_FFMA, 1.0, 0.0)]
 
@@ -125,10 +127,13 @@ def test_replay_after_the_workspace_grew():
     # the captured graph holds must stay allocated (retired, not freed)
     t = _gpu.torch()
     s = t.cuda.Stream()
-    M, N, K = 300, 260, 512
+    M, N, K = 300, 260, 514  # A's rows not 16-byte strides: its padded copy is in the workspace
     a = t.rand((M, K), device="cuda") - 0.5
     b = t.rand((K, N), device="cuda") - 0.5
     c = t.zeros((M, N), device="cuda")
+    st, p = g.gemm_f32_plan(M, N, K, g.ALGO_3XTF32, 0, A=a.data_ptr(), B=b.data_ptr(),
+                            C=c.data_ptr())
+    assert st == 0 and p["workspace_bytes"] > 0, p
 
     def call():
         return g.gemm_f32_algo(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K,

@@ -117,6 +117,55 @@ def test_in_kernel_reduction_equals_split_order_sum(shape, splits):
         "in-kernel sum differs from the split-order sum of the partials"
 
 
+@pytest.mark.parametrize("shape,splits", [((300, 260, 3000), 2), ((300, 260, 3000), 3),
+                                          ((300, 260, 3000), 8), ((1025, 1023, 1000), 2),
+                                          ((129, 384, 2049), 4)],
+                         ids=lambda v: "x".join(map(str, v)) if isinstance(v, tuple) else str(v))
+def test_cluster_split_equals_split_order_sum(shape, splits):
+    # 2..8 splits with one unit per CTA: the splits of a tile run as one
+    # cluster and add their partials through distributed shared memory, no
+    # workspace and no reduction launch; each split's partial is the same
+    # kernel run alone on its K range, so C must equal those partials added
+    # in split order, bit for bit
+    M, N, K = shape
+    st, p = g.gemm_f32_plan_config(M, N, K, g.ALGO_3XTF32, TMEM, splits, A=1 << 32, B=1 << 36,
+                                   C=1 << 40)
+    assert st == 0 and p["splits"] == splits and p["cluster_reduce"] == 1, p
+    assert p["reduce_in_kernel"] == 0, p
+    assert p["kernels"] == 1 + p["stage_a"] + p["stage_b"], p
+    if not p["stage_a"] and not p["stage_b"]:
+        assert p["workspace_bytes"] == 0, p
+    A, B = make_workload(2, M=M, N=N, K=K)
+    C = _gpu.run_configured(A, B, g.ALGO_3XTF32, TMEM, splits)
+    _check(C, oracle.ref_gemm(A, B), label=f"tmem cluster split {shape} s{splits}")
+    kb = (K + 31) // 32
+    per = (kb + splits - 1) // splits
+    total = None
+    for s in range(splits):
+        k0, k1 = s * per * 32, min(K, (s + 1) * per * 32)
+        part = _gpu.run_configured(np.ascontiguousarray(A[:, k0:k1]),
+                                   np.ascontiguousarray(B[k0:k1]), g.ALGO_3XTF32, TMEM, 1)
+        total = part if total is None else (total + part).astype(np.float32)
+    assert np.array_equal(C.view(np.uint32), total.view(np.uint32)), \
+        "cluster sum differs from the split-order sum of the partials"
+    C2 = _gpu.run_configured(A, B, g.ALGO_3XTF32, TMEM, splits)
+    assert np.array_equal(C.view(np.uint32), C2.view(np.uint32)), "not run-to-run deterministic"
+
+
+@pytest.mark.parametrize("pad", [0, 1, 4])
+def test_cluster_split_general_form(pad):
+    # the ragged workload's AUTO plan (N odd: B padded, then this kernel with
+    # 2 splits added in a cluster), with alpha/beta applied where the cluster
+    # writes C: element by element (pad 0, 4: a row stride that is not a
+    # multiple of 4) or by 16-byte words (pad 1: ldc 1024)
+    M, N, K = 1025, 1023, 1000
+    st, p = g.gemm_f32_plan_ex(0, 0, M, N, K, K + pad, N + pad, N + pad, g.ALGO_AUTO, 0,
+                               A=1 << 32, B=1 << 36, C=1 << 40)
+    assert st == 0 and p["b_in_tmem"] == 1 and (p["tile_m"], p["tile_n"]) == (128, 128), p
+    assert p["splits"] == 2 and p["cluster_reduce"] == 1, p
+    _ex_case(M, N, K, 0, 0, pad, -0.75, 1.5, g.ALGO_AUTO)
+
+
 def test_more_units_than_sms_uses_the_reduction_kernel():
     # 40 x 40 tiles x 2 splits: CTAs take several units, so the partials go
     # through the workspace and the reduction kernel
