@@ -665,13 +665,18 @@ void make_plan(const DeviceState& d, const Problem& q, int algo, int splits, Pla
     }
     // The single-CTA form with B's split in tensor memory likewise (its stage
     // memory holds the 128 x 128 partial after the main loop): no workspace
-    // and no reduction launch (1025 x 1023 x 1000, 2 splits: the reduction
-    // kernel was ~4 us of a ~35 us call).  From 16 splits it adds them in
-    // the kernel through the workspace instead (below).
+    // and no reduction launch (1025 x 1023 x 1000, 2 splits: 72 clusters of
+    // 2 of the 76 that fit, 37.2 -> 34.6 us a call).  Clusters of 3 or more
+    // keep a tenth of the capacity free: with the device filled to the last
+    // cluster they were not always placed at once (301 x 1874 x 563, 45
+    // clusters of 3 of 46: 35.5 us against 27.3 through the workspace).
+    // From 16 splits the kernel adds them itself through the workspace
+    // (below).
     if (p->tmem_b && !p->pair && !p->tmem_wide && p->splits >= 2 && p->splits <= 8 &&
         units <= d.sm_count) {
         int fit = 0;
-        if (tf32x3_tmem_cluster_capacity(p->splits, &fit) == cudaSuccess && tiles <= fit)
+        if (tf32x3_tmem_cluster_capacity(p->splits, &fit) == cudaSuccess && tiles <= fit &&
+            (p->splits == 2 || 10 * tiles <= 9 * fit))
             p->cluster_splits = p->splits;
         cudaGetLastError();
     }
