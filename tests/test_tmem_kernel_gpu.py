@@ -164,6 +164,7 @@ def test_cluster_split_general_form(pad):
     assert st == 0 and p["b_in_tmem"] == 1 and (p["tile_m"], p["tile_n"]) == (128, 128), p
     assert p["splits"] == 2 and p["cluster_reduce"] == 1, p
     _ex_case(M, N, K, 0, 0, pad, -0.75, 1.5, g.ALGO_AUTO)
+    _ex_case(M, N, K, 0, 0, pad, 2.0, 0.0, g.ALGO_AUTO, c_nan=True)  # beta 0: C never read
 
 
 def test_more_units_than_sms_uses_the_reduction_kernel():
